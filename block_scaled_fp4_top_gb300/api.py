@@ -1,0 +1,213 @@
+"""Python binding of the fp4moe C ABI: torch tensors in, C calls out.
+
+Each function has the name of its C entry point and only marshals arguments:
+it takes the device pointers of contiguous CUDA tensors and the current
+stream, calls the library and raises Fp4MoeError on a non-OK status. All the
+layer's arithmetic runs in the CUDA kernels of libfp4moe.so.
+
+``MoELayer`` is a convenience owner of the buffers (allocated through torch)
+for one configuration. It also runs the load-time prep: weight quantisation,
+calibration and alpha tables.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+from ._lib import Config
+
+
+class Fp4MoeError(RuntimeError):
+    pass
+
+
+def config(hidden: int, inter: int, num_experts: int, top_k: int, max_tokens: int, swiglu_limit: float,
+           inter_logical: int = 0, w_format: int = _lib.W_NVFP4) -> Config:
+    return Config(hidden, inter, inter_logical or inter, num_experts, top_k, max_tokens, swiglu_limit, w_format)
+
+
+def _p(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if not t.is_cuda or not t.is_contiguous():
+        raise Fp4MoeError("tensors must be contiguous CUDA tensors")
+    return t.data_ptr()
+
+
+def _s(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(rc: int, what: str):
+    if rc != _lib.OK:
+        name = _lib.load().fp4moe_status_string(rc).decode()
+        raise Fp4MoeError(f"{what}: {name}")
+
+
+def capacity_rows(cfg: Config, T: int) -> int:
+    return _lib.load().fp4moe_capacity_rows(ctypes.byref(cfg), T)
+
+
+def workspace_bytes(cfg: Config) -> int:
+    return _lib.load().fp4moe_workspace_bytes(ctypes.byref(cfg))
+
+
+def weight_bytes(cfg: Config):
+    v = [ctypes.c_size_t() for _ in range(4)]
+    _check(_lib.load().fp4moe_weight_bytes(ctypes.byref(cfg), *[ctypes.byref(x) for x in v]), "fp4moe_weight_bytes")
+    return tuple(x.value for x in v)
+
+
+def moe_route(cfg, T, x, router_w, router_bias, logits_out, topk_ids, topk_w, counts, offsets, padded_offsets,
+              slot_of_pair, pair_of_row, ws, stream=None):
+    _check(_lib.load().moe_route(ctypes.byref(cfg), T, _p(x), _p(router_w), _p(router_bias), _p(logits_out),
+                                 _p(topk_ids), _p(topk_w), _p(counts), _p(offsets), _p(padded_offsets),
+                                 _p(slot_of_pair), _p(pair_of_row), _p(ws), _s(stream)), "moe_route")
+
+
+def moe_quantize_scatter(cfg, T, x, gs1, padded_offsets, pair_of_row, a1_fp4, a1_sf, ws, stream=None):
+    _check(_lib.load().moe_quantize_scatter(ctypes.byref(cfg), T, _p(x), _p(gs1), _p(padded_offsets),
+                                            _p(pair_of_row), _p(a1_fp4), _p(a1_sf), _p(ws), _s(stream)),
+           "moe_quantize_scatter")
+
+
+def moe_grouped_gemm_w1_swiglu(cfg, T, a1_fp4, a1_sf, padded_offsets, pair_of_row, w1_fp4, w1_sf, alpha1, gs2,
+                               a2_fp4, a2_sf, ws, stream=None):
+    _check(_lib.load().moe_grouped_gemm_w1_swiglu(ctypes.byref(cfg), T, _p(a1_fp4), _p(a1_sf), _p(padded_offsets),
+                                                  _p(pair_of_row), _p(w1_fp4), _p(w1_sf), _p(alpha1), _p(gs2),
+                                                  _p(a2_fp4), _p(a2_sf), _p(ws), _s(stream)),
+           "moe_grouped_gemm_w1_swiglu")
+
+
+def moe_grouped_gemm_w2(cfg, T, a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, o_pairs, ws,
+                        stream=None):
+    _check(_lib.load().moe_grouped_gemm_w2(ctypes.byref(cfg), T, _p(a2_fp4), _p(a2_sf), _p(padded_offsets),
+                                           _p(pair_of_row), _p(w2_fp4), _p(w2_sf), _p(alpha2), _p(o_pairs), _p(ws),
+                                           _s(stream)), "moe_grouped_gemm_w2")
+
+
+def moe_combine(cfg, T, o_pairs, topk_w, y, stream=None):
+    _check(_lib.load().moe_combine(ctypes.byref(cfg), T, _p(o_pairs), _p(topk_w), _p(y), _s(stream)), "moe_combine")
+
+
+def moe_grouped_gemm_w2_combine(cfg, T, a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, topk_w,
+                                y, ws, stream=None):
+    _check(_lib.load().moe_grouped_gemm_w2_combine(ctypes.byref(cfg), T, _p(a2_fp4), _p(a2_sf), _p(padded_offsets),
+                                                   _p(pair_of_row), _p(w2_fp4), _p(w2_sf), _p(alpha2), _p(topk_w),
+                                                   _p(y), _p(ws), _s(stream)), "moe_grouped_gemm_w2_combine")
+
+
+def moe_forward(cfg, T, x, router_w, router_bias, gs1, gs2, w1_fp4, w1_sf, alpha1, w2_fp4, w2_sf, alpha2, y,
+                topk_ids_out, topk_w_out, ws, stream=None):
+    _check(_lib.load().moe_forward(ctypes.byref(cfg), T, _p(x), _p(router_w), _p(router_bias), _p(gs1), _p(gs2),
+                                   _p(w1_fp4), _p(w1_sf), _p(alpha1), _p(w2_fp4), _p(w2_sf), _p(alpha2), _p(y),
+                                   _p(topk_ids_out), _p(topk_w_out), _p(ws), _s(stream)), "moe_forward")
+
+
+def fp4moe_quantize_weights(cfg, which, n_experts, w, codes_out, sf_out, gs_out, stream=None):
+    _check(_lib.load().fp4moe_quantize_weights(ctypes.byref(cfg), which, n_experts, _p(w), _p(codes_out),
+                                               _p(sf_out), _p(gs_out), _s(stream)), "fp4moe_quantize_weights")
+
+
+def fp4moe_make_alpha(n, gs_act, gs_w, alpha, stream=None):
+    _check(_lib.load().fp4moe_make_alpha(n, _p(gs_act), _p(gs_w), _p(alpha), _s(stream)), "fp4moe_make_alpha")
+
+
+def fp4moe_calibrate(cfg, T, x_warm, router_w, router_bias, w1_fp4, w1_sf, gw1, gs1_out, gs2_out, ws, stream=None):
+    _check(_lib.load().fp4moe_calibrate(ctypes.byref(cfg), T, _p(x_warm), _p(router_w), _p(router_bias), _p(w1_fp4),
+                                        _p(w1_sf), _p(gw1), _p(gs1_out), _p(gs2_out), _p(ws), _s(stream)),
+           "fp4moe_calibrate")
+
+
+def fp4moe_quantize_rows_f32(rows, K, inp, g, codes, sf, stream=None):
+    _check(_lib.load().fp4moe_quantize_rows_f32(rows, K, _p(inp), _p(g), _p(codes), _p(sf), _s(stream)),
+           "fp4moe_quantize_rows_f32")
+
+
+def fp4moe_read_error(ws, clear=True, stream=None) -> int:
+    v = ctypes.c_uint32()
+    _check(_lib.load().fp4moe_read_error(_p(ws), ctypes.byref(v), 1 if clear else 0, _s(stream)), "fp4moe_read_error")
+    return v.value
+
+
+# --------------------------------------------------------------------------
+@dataclass
+class Weights:
+    w1_fp4: torch.Tensor
+    w1_sf: torch.Tensor
+    gw1: torch.Tensor
+    w2_fp4: torch.Tensor
+    w2_sf: torch.Tensor
+    gw2: torch.Tensor
+
+
+class MoELayer:
+    """Owns the device buffers of one layer configuration and calls the C ABI on them."""
+
+    def __init__(self, cfg: Config, device: str = "cuda"):
+        self.cfg = cfg
+        self.device = device
+        E, H, I = cfg.num_experts, cfg.hidden, cfg.inter
+        b1, s1, b2, s2 = weight_bytes(cfg)
+        u8 = dict(dtype=torch.uint8, device=device)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.weights = Weights(torch.empty(b1, **u8), torch.empty(s1, **u8), torch.empty(E, **f32),
+                               torch.empty(b2, **u8), torch.empty(s2, **u8), torch.empty(E, **f32))
+        self.ws = torch.zeros(workspace_bytes(cfg), **u8)
+        self.gs1 = torch.ones(1, **f32)
+        self.gs2 = torch.ones(1, **f32)
+        self.alpha1 = torch.empty(E, **f32)
+        self.alpha2 = torch.empty(E, **f32)
+        self.router_w = None
+        self.router_bias = None
+
+    # ---- load-time prep
+    def quantize_weights(self, which: int, e0: int, w: torch.Tensor):
+        """Quantise experts [e0, e0 + w.shape[0]) of W1 (which=1, [n, 2I, H]) or W2 (which=2, [n, H, I])."""
+        cfg, W = self.cfg, self.weights
+        n = w.shape[0]
+        if which == 1:
+            per_c, per_s = 2 * cfg.inter * cfg.hidden // 2, 2 * cfg.inter * cfg.hidden // 16
+            codes, sf, gs = W.w1_fp4, W.w1_sf, W.gw1
+        else:
+            per_c, per_s = cfg.hidden * cfg.inter // 2, cfg.hidden * cfg.inter // 16
+            codes, sf, gs = W.w2_fp4, W.w2_sf, W.gw2
+        fp4moe_quantize_weights(cfg, which, n, w.contiguous(), codes[e0 * per_c:(e0 + n) * per_c],
+                                sf[e0 * per_s:(e0 + n) * per_s], gs[e0:e0 + n])
+
+    def set_router(self, router_w: torch.Tensor, router_bias: torch.Tensor | None = None):
+        self.router_w = router_w.contiguous()
+        self.router_bias = None if router_bias is None else router_bias.contiguous()
+
+    def calibrate(self, x_warm: torch.Tensor):
+        T = x_warm.shape[0]
+        W = self.weights
+        fp4moe_calibrate(self.cfg, T, x_warm, self.router_w, self.router_bias, W.w1_fp4, W.w1_sf, W.gw1, self.gs1,
+                         self.gs2, self.ws)
+        self.update_alpha()
+
+    def set_global_scales(self, gs1: float, gs2: float):
+        self.gs1.fill_(gs1)
+        self.gs2.fill_(gs2)
+        self.update_alpha()
+
+    def update_alpha(self):
+        E = self.cfg.num_experts
+        fp4moe_make_alpha(E, self.gs1, self.weights.gw1, self.alpha1)
+        fp4moe_make_alpha(E, self.gs2, self.weights.gw2, self.alpha2)
+
+    # ---- hot path
+    def forward(self, x: torch.Tensor, y: torch.Tensor, topk_ids: torch.Tensor | None = None,
+                topk_w: torch.Tensor | None = None, stream=None):
+        W = self.weights
+        moe_forward(self.cfg, x.shape[0], x, self.router_w, self.router_bias, self.gs1, self.gs2, W.w1_fp4, W.w1_sf,
+                    self.alpha1, W.w2_fp4, W.w2_sf, self.alpha2, y, topk_ids, topk_w, self.ws, stream)
+
+    def read_error(self, clear=True) -> int:
+        return fp4moe_read_error(self.ws, clear)

@@ -1,0 +1,321 @@
+// C ABI of libfp4moe: argument checks, workspace layout and the composed
+// calls (moe_forward, moe_grouped_gemm_w2_combine, fp4moe_calibrate).
+//
+// Host code here validates host-known integers and pointer alignment, then
+// enqueues kernels. It never synchronises and never allocates, apart from
+// fp4moe_read_error and the documented prep helpers. It never reads device
+// values. "CUDA-Graph Safety / GPU-Native Requirements", SECTION B, lists the
+// hidden host syncs, allocations and device-value branches that a captured
+// step must not contain.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace fp4moe {
+
+namespace {
+
+inline bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+fp4moe_status check_cfg(const fp4moe_config* c) {
+  if (c == nullptr) return FP4MOE_INVALID_ARG;
+  if (c->hidden <= 0 || c->inter <= 0 || c->num_experts <= 0 || c->top_k <= 0 || c->max_tokens < 0 ||
+      !(c->swiglu_limit > 0.0f))
+    return FP4MOE_INVALID_ARG;
+  if (c->w_format != FP4MOE_W_NVFP4) return FP4MOE_UNSUPPORTED;
+  if (c->hidden % 256 != 0 || c->inter % 128 != 0) return FP4MOE_UNSUPPORTED;
+  if (c->top_k > kMaxTopK || c->num_experts > kMaxExperts || c->top_k > c->num_experts) return FP4MOE_UNSUPPORTED;
+  if (c->inter_logical != 0 && c->inter_logical != c->inter) return FP4MOE_UNSUPPORTED;
+  return FP4MOE_OK;
+}
+
+fp4moe_status check_T(const fp4moe_config* c, int32_t T) {
+  if (T < 0) return FP4MOE_INVALID_ARG;
+  if (T > c->max_tokens) return FP4MOE_CAPACITY;
+  return FP4MOE_OK;
+}
+
+// every pointer non-null and 16-byte aligned
+template <typename... P>
+fp4moe_status check_ptrs(P... ps) {
+  const void* arr[] = {static_cast<const void*>(ps)...};
+  for (const void* p : arr)
+    if (p == nullptr) return FP4MOE_INVALID_ARG;
+  for (const void* p : arr)
+    if (!a16(p)) return FP4MOE_MISALIGNED;
+  return FP4MOE_OK;
+}
+
+inline fp4moe_status check_opt(const void* p) { return (p == nullptr || a16(p)) ? FP4MOE_OK : FP4MOE_MISALIGNED; }
+
+#define FP4_TRY(expr)                          \
+  do {                                         \
+    const fp4moe_status s_ = (expr);           \
+    if (s_ != FP4MOE_OK) return s_;            \
+  } while (0)
+
+template <typename Tp>
+Tp* at(void* ws, size_t off) {
+  return reinterpret_cast<Tp*>(static_cast<uint8_t*>(ws) + off);
+}
+inline uint32_t* err_word(void* ws) { return at<uint32_t>(ws, kWsErr); }
+
+}  // namespace
+
+size_t capacity_rows(const fp4moe_config& cfg, int32_t T) {
+  const int64_t pairs = (int64_t)T * cfg.top_k;
+  const int64_t cap = (pairs + 127 * std::min<int64_t>(cfg.num_experts, pairs)) / 128 * 128;
+  return (size_t)std::max<int64_t>(cap, 128);
+}
+
+WsLayout ws_layout(const fp4moe_config& c) {
+  WsLayout L{};
+  size_t off = kWsHeader;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + std::max<size_t>(bytes, 1), 256);
+    return o;
+  };
+  const size_t Tm = (size_t)c.max_tokens, E = (size_t)c.num_experts, k = (size_t)c.top_k;
+  const size_t cap = capacity_rows(c, c.max_tokens);
+  const size_t nchunks = std::max<size_t>(1, (Tm + kRouteChunk - 1) / kRouteChunk);
+  L.hist = take(nchunks * E * 4);
+  L.logits = take(Tm * E * 4);
+  L.ids = take(Tm * k * 4);
+  L.w = take(Tm * k * 4);
+  L.counts = take(E * 4);
+  L.offsets = take(E * 4);
+  L.poff = take(E * 4);
+  L.slot = take(Tm * k * 4);
+  L.por = take(cap * 4);
+  L.a1 = take(cap * (size_t)c.hidden / 2);
+  L.a1sf = take(cap * (size_t)c.hidden / 16);
+  L.a2 = take(cap * (size_t)c.inter / 2);
+  L.a2sf = take(cap * (size_t)c.inter / 16);
+  L.opairs = take(Tm * k * (size_t)c.hidden * 4);
+  L.alpha_tmp = take(E * 4);
+  L.total = off;
+  return L;
+}
+
+}  // namespace fp4moe
+
+using namespace fp4moe;
+
+extern "C" {
+
+int32_t fp4moe_abi_version(void) { return 100; }
+
+const char* fp4moe_status_string(fp4moe_status s) {
+  switch (s) {
+    case FP4MOE_OK: return "FP4MOE_OK";
+    case FP4MOE_INVALID_ARG: return "FP4MOE_INVALID_ARG";
+    case FP4MOE_MISALIGNED: return "FP4MOE_MISALIGNED";
+    case FP4MOE_CAPACITY: return "FP4MOE_CAPACITY";
+    case FP4MOE_UNSUPPORTED: return "FP4MOE_UNSUPPORTED";
+    case FP4MOE_CUDA_ERROR: return "FP4MOE_CUDA_ERROR";
+  }
+  return "FP4MOE_UNKNOWN";
+}
+
+size_t fp4moe_capacity_rows(const fp4moe_config* cfg, int32_t T) {
+  if (check_cfg(cfg) != FP4MOE_OK || T < 0) return 0;
+  return capacity_rows(*cfg, T);
+}
+
+size_t fp4moe_workspace_bytes(const fp4moe_config* cfg) {
+  if (check_cfg(cfg) != FP4MOE_OK) return 0;
+  return ws_layout(*cfg).total;
+}
+
+fp4moe_status fp4moe_weight_bytes(const fp4moe_config* cfg, size_t* w1_codes, size_t* w1_sf, size_t* w2_codes,
+                                  size_t* w2_sf) {
+  FP4_TRY(check_cfg(cfg));
+  const size_t E = cfg->num_experts, H = cfg->hidden, I = cfg->inter;
+  if (w1_codes) *w1_codes = E * 2 * I * H / 2;
+  if (w1_sf) *w1_sf = E * 2 * I * H / 16;
+  if (w2_codes) *w2_codes = E * H * I / 2;
+  if (w2_sf) *w2_sf = E * H * I / 16;
+  return FP4MOE_OK;
+}
+
+fp4moe_status moe_route(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
+                        const float* router_bias, float* logits_out, int32_t* topk_ids, float* topk_w,
+                        int32_t* counts, int32_t* offsets, int32_t* padded_offsets, int32_t* slot_of_pair,
+                        int32_t* pair_of_row, void* ws, fp4moe_stream_t stream) {
+  FP4_TRY(check_cfg(cfg));
+  FP4_TRY(check_T(cfg, T));
+  FP4_TRY(check_ptrs(x, router_w, topk_ids, topk_w, counts, offsets, padded_offsets, slot_of_pair, pair_of_row, ws));
+  FP4_TRY(check_opt(router_bias));
+  FP4_TRY(check_opt(logits_out));
+  const WsLayout L = ws_layout(*cfg);
+  float* logits = logits_out ? logits_out : at<float>(ws, L.logits);
+  return route_launch(*cfg, T, x, router_w, router_bias, logits, topk_ids, topk_w, counts, offsets, padded_offsets,
+                      slot_of_pair, pair_of_row, at<int32_t>(ws, L.hist), err_word(ws), (cudaStream_t)stream);
+}
+
+fp4moe_status moe_quantize_scatter(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const float* gs1,
+                                   const int32_t* padded_offsets, const int32_t* pair_of_row, uint8_t* a1_fp4,
+                                   uint8_t* a1_sf, void* ws, fp4moe_stream_t stream) {
+  FP4_TRY(check_cfg(cfg));
+  FP4_TRY(check_T(cfg, T));
+  FP4_TRY(check_ptrs(x, gs1, padded_offsets, pair_of_row, a1_fp4, a1_sf, ws));
+  return quant_scatter_launch(*cfg, T, x, gs1, padded_offsets, pair_of_row, a1_fp4, a1_sf, (cudaStream_t)stream);
+}
+
+fp4moe_status moe_grouped_gemm_w1_swiglu(const fp4moe_config* cfg, int32_t T, const uint8_t* a1_fp4,
+                                         const uint8_t* a1_sf, const int32_t* padded_offsets,
+                                         const int32_t* pair_of_row, const uint8_t* w1_fp4, const uint8_t* w1_sf,
+                                         const float* alpha1, const float* gs2, uint8_t* a2_fp4, uint8_t* a2_sf,
+                                         void* ws, fp4moe_stream_t stream) {
+  FP4_TRY(check_cfg(cfg));
+  FP4_TRY(check_T(cfg, T));
+  FP4_TRY(check_ptrs(a1_fp4, a1_sf, padded_offsets, pair_of_row, w1_fp4, w1_sf, alpha1, gs2, a2_fp4, a2_sf, ws));
+  return gemm_launch(kW1SwiGLU, *cfg, T, a1_fp4, a1_sf, padded_offsets, pair_of_row, w1_fp4, w1_sf, alpha1, gs2,
+                     a2_fp4, a2_sf, nullptr, nullptr, err_word(ws), (cudaStream_t)stream);
+}
+
+fp4moe_status moe_grouped_gemm_w2(const fp4moe_config* cfg, int32_t T, const uint8_t* a2_fp4, const uint8_t* a2_sf,
+                                  const int32_t* padded_offsets, const int32_t* pair_of_row, const uint8_t* w2_fp4,
+                                  const uint8_t* w2_sf, const float* alpha2, float* o_pairs, void* ws,
+                                  fp4moe_stream_t stream) {
+  FP4_TRY(check_cfg(cfg));
+  FP4_TRY(check_T(cfg, T));
+  FP4_TRY(check_ptrs(a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, o_pairs, ws));
+  return gemm_launch(kW2Rows, *cfg, T, a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, nullptr,
+                     nullptr, nullptr, nullptr, o_pairs, err_word(ws), (cudaStream_t)stream);
+}
+
+fp4moe_status moe_combine(const fp4moe_config* cfg, int32_t T, const float* o_pairs, const float* topk_w,
+                          uint16_t* y, fp4moe_stream_t stream) {
+  FP4_TRY(check_cfg(cfg));
+  FP4_TRY(check_T(cfg, T));
+  FP4_TRY(check_ptrs(o_pairs, topk_w, y));
+  return combine_launch(*cfg, T, o_pairs, topk_w, y, (cudaStream_t)stream);
+}
+
+fp4moe_status moe_grouped_gemm_w2_combine(const fp4moe_config* cfg, int32_t T, const uint8_t* a2_fp4,
+                                          const uint8_t* a2_sf, const int32_t* padded_offsets,
+                                          const int32_t* pair_of_row, const uint8_t* w2_fp4, const uint8_t* w2_sf,
+                                          const float* alpha2, const float* topk_w, uint16_t* y, void* ws,
+                                          fp4moe_stream_t stream) {
+  FP4_TRY(check_cfg(cfg));
+  FP4_TRY(check_T(cfg, T));
+  FP4_TRY(check_ptrs(a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, topk_w, y, ws));
+  const WsLayout L = ws_layout(*cfg);
+  float* o = at<float>(ws, L.opairs);
+  FP4_TRY(gemm_launch(kW2Rows, *cfg, T, a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, nullptr,
+                      nullptr, nullptr, nullptr, o, err_word(ws), (cudaStream_t)stream));
+  return combine_launch(*cfg, T, o, topk_w, y, (cudaStream_t)stream);
+}
+
+fp4moe_status moe_forward(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
+                          const float* router_bias, const float* gs1, const float* gs2, const uint8_t* w1_fp4,
+                          const uint8_t* w1_sf, const float* alpha1, const uint8_t* w2_fp4, const uint8_t* w2_sf,
+                          const float* alpha2, uint16_t* y, int32_t* topk_ids_out, float* topk_w_out, void* ws,
+                          fp4moe_stream_t stream) {
+  FP4_TRY(check_cfg(cfg));
+  FP4_TRY(check_T(cfg, T));
+  FP4_TRY(check_ptrs(x, router_w, gs1, gs2, w1_fp4, w1_sf, alpha1, w2_fp4, w2_sf, alpha2, y, ws));
+  FP4_TRY(check_opt(router_bias));
+  FP4_TRY(check_opt(topk_ids_out));
+  FP4_TRY(check_opt(topk_w_out));
+  const cudaStream_t st = (cudaStream_t)stream;
+  const WsLayout L = ws_layout(*cfg);
+  uint32_t* err = err_word(ws);
+  int32_t* ids = at<int32_t>(ws, L.ids);
+  float* w = at<float>(ws, L.w);
+  int32_t* poff = at<int32_t>(ws, L.poff);
+  int32_t* por = at<int32_t>(ws, L.por);
+  FP4_TRY(route_launch(*cfg, T, x, router_w, router_bias, at<float>(ws, L.logits), ids, w, at<int32_t>(ws, L.counts),
+                       at<int32_t>(ws, L.offsets), poff, at<int32_t>(ws, L.slot), por, at<int32_t>(ws, L.hist), err,
+                       st));
+  FP4_TRY(quant_scatter_launch(*cfg, T, x, gs1, poff, por, at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf), st));
+  FP4_TRY(gemm_launch(kW1SwiGLU, *cfg, T, at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf), poff, por, w1_fp4, w1_sf,
+                      alpha1, gs2, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), nullptr, nullptr, err, st));
+  FP4_TRY(gemm_launch(kW2Rows, *cfg, T, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), poff, por, w2_fp4, w2_sf,
+                      alpha2, nullptr, nullptr, nullptr, nullptr, at<float>(ws, L.opairs), err, st));
+  FP4_TRY(combine_launch(*cfg, T, at<float>(ws, L.opairs), w, y, st));
+  const size_t pk = (size_t)T * cfg->top_k;
+  if (topk_ids_out && pk && cudaMemcpyAsync(topk_ids_out, ids, pk * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return FP4MOE_CUDA_ERROR;
+  if (topk_w_out && pk && cudaMemcpyAsync(topk_w_out, w, pk * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return FP4MOE_CUDA_ERROR;
+  return FP4MOE_OK;
+}
+
+fp4moe_status fp4moe_quantize_weights(const fp4moe_config* cfg, int32_t which, int32_t n_experts, const float* w,
+                                      uint8_t* codes_out, uint8_t* sf_out, float* gs_out, fp4moe_stream_t stream) {
+  FP4_TRY(check_cfg(cfg));
+  if (which != 1 && which != 2) return FP4MOE_INVALID_ARG;
+  if (n_experts < 0 || n_experts > cfg->num_experts) return FP4MOE_INVALID_ARG;
+  FP4_TRY(check_ptrs(w, codes_out, sf_out, gs_out));
+  const cudaStream_t st = (cudaStream_t)stream;
+  const int32_t rows = which == 1 ? 2 * cfg->inter : cfg->hidden;
+  const int32_t K = which == 1 ? cfg->hidden : cfg->inter;
+  FP4_TRY(amax_f32_launch(n_experts, (int64_t)rows * K, w, gs_out, st));
+  FP4_TRY(gs_from_amax_launch(n_experts, gs_out, st));
+  return quant_rows_launch((int64_t)n_experts * rows, K, rows, which == 1 ? cfg->inter : 0, w, gs_out, rows,
+                           codes_out, sf_out, st);
+}
+
+fp4moe_status fp4moe_make_alpha(int32_t n, const float* gs_act, const float* gs_w, float* alpha,
+                                fp4moe_stream_t stream) {
+  if (n < 0) return FP4MOE_INVALID_ARG;
+  FP4_TRY(check_ptrs(gs_act, gs_w, alpha));
+  return make_alpha_launch(n, gs_act, gs_w, alpha, (cudaStream_t)stream);
+}
+
+fp4moe_status fp4moe_calibrate(const fp4moe_config* cfg, int32_t T, const uint16_t* x_warm, const uint16_t* router_w,
+                               const float* router_bias, const uint8_t* w1_fp4, const uint8_t* w1_sf,
+                               const float* gw1, float* gs1_out, float* gs2_out, void* ws, fp4moe_stream_t stream) {
+  FP4_TRY(check_cfg(cfg));
+  FP4_TRY(check_T(cfg, T));
+  FP4_TRY(check_ptrs(x_warm, router_w, w1_fp4, w1_sf, gw1, gs1_out, gs2_out, ws));
+  FP4_TRY(check_opt(router_bias));
+  const cudaStream_t st = (cudaStream_t)stream;
+  const WsLayout L = ws_layout(*cfg);
+  uint32_t* err = err_word(ws);
+  float* amax_x = at<float>(ws, kWsAmaxX);
+  float* amax_h = at<float>(ws, kWsAmaxH);
+  int32_t* poff = at<int32_t>(ws, L.poff);
+  int32_t* por = at<int32_t>(ws, L.por);
+  FP4_TRY(amax_bf16_launch((int64_t)T * cfg->hidden, x_warm, amax_x, st));
+  if (cudaMemcpyAsync(gs1_out, amax_x, 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
+  FP4_TRY(gs_from_amax_launch(1, gs1_out, st));
+  FP4_TRY(route_launch(*cfg, T, x_warm, router_w, router_bias, at<float>(ws, L.logits), at<int32_t>(ws, L.ids),
+                       at<float>(ws, L.w), at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets), poff,
+                       at<int32_t>(ws, L.slot), por, at<int32_t>(ws, L.hist), err, st));
+  FP4_TRY(quant_scatter_launch(*cfg, T, x_warm, gs1_out, poff, por, at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf),
+                               st));
+  float* alpha = at<float>(ws, L.alpha_tmp);
+  FP4_TRY(make_alpha_launch(cfg->num_experts, gs1_out, gw1, alpha, st));
+  if (cudaMemsetAsync(amax_h, 0, 4, st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
+  FP4_TRY(gemm_launch(kW1Amax, *cfg, T, at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf), poff, por, w1_fp4, w1_sf,
+                      alpha, nullptr, nullptr, nullptr, amax_h, nullptr, err, st));
+  if (cudaMemcpyAsync(gs2_out, amax_h, 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
+  return gs_from_amax_launch(1, gs2_out, st);
+}
+
+fp4moe_status fp4moe_quantize_rows_f32(int32_t rows, int32_t K, const float* in, const float* g, uint8_t* codes,
+                                       uint8_t* sf, fp4moe_stream_t stream) {
+  if (rows < 0 || K <= 0 || K % 64 != 0 || rows % 128 != 0) return FP4MOE_INVALID_ARG;
+  FP4_TRY(check_ptrs(in, g, codes, sf));
+  return quant_rows_launch(rows, K, rows > 0 ? rows : 1, 0, in, g, 1, codes, sf, (cudaStream_t)stream);
+}
+
+fp4moe_status fp4moe_read_error(void* ws, uint32_t* err_host, int32_t clear, fp4moe_stream_t stream) {
+  if (ws == nullptr || err_host == nullptr) return FP4MOE_INVALID_ARG;
+  const cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(err_host, ws, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
+  if (clear) {
+    if (cudaMemsetAsync(ws, 0, 4, st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
+  }
+  return FP4MOE_OK;
+}
+
+}  // extern "C"

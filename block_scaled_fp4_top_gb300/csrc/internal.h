@@ -1,0 +1,50 @@
+// Internal declarations shared by the translation units of libfp4moe.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "fp4moe.h"
+
+namespace fp4moe {
+
+size_t capacity_rows(const fp4moe_config& cfg, int32_t T);
+
+// Byte offsets of the regions of a workspace sized for cfg.max_tokens.
+struct WsLayout {
+  size_t hist, logits, ids, w, counts, offsets, poff, slot, por, a1, a1sf, a2, a2sf, opairs, alpha_tmp, total;
+};
+WsLayout ws_layout(const fp4moe_config& cfg);
+
+fp4moe_status route_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
+                           const float* bias, float* logits, int32_t* ids, float* w, int32_t* counts,
+                           int32_t* offsets, int32_t* poff, int32_t* slot_of_pair, int32_t* pair_of_row,
+                           int32_t* hist, uint32_t* err, cudaStream_t st);
+
+fp4moe_status quant_scatter_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const float* gs1,
+                                   const int32_t* poff, const int32_t* pair_of_row, uint8_t* a1, uint8_t* a1_sf,
+                                   cudaStream_t st);
+
+// rows [n_rows_total][K] fp32 -> NVFP4; g indexed by row / g_div; optional W1 gate/up row permutation
+// (rows_per_group = rows of one expert, inter = I, or 0 for no permutation).
+fp4moe_status quant_rows_launch(int64_t n_rows_total, int32_t K, int32_t rows_per_group, int32_t inter,
+                                const float* in, const float* g, int32_t g_div, uint8_t* codes, uint8_t* sf,
+                                cudaStream_t st);
+
+fp4moe_status amax_f32_launch(int32_t n_groups, int64_t per_group, const float* in, float* amax, cudaStream_t st);
+fp4moe_status amax_bf16_launch(int64_t n, const uint16_t* in, float* amax, cudaStream_t st);
+fp4moe_status gs_from_amax_launch(int32_t n, float* inout, cudaStream_t st);
+fp4moe_status make_alpha_launch(int32_t n, const float* gs_act, const float* gs_w, float* alpha, cudaStream_t st);
+
+enum GemmMode { kW1SwiGLU = 0, kW1Amax = 1, kW2Rows = 2 };
+fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, const uint8_t* a_codes,
+                          const uint8_t* a_sf, const int32_t* poff, const int32_t* pair_of_row,
+                          const uint8_t* b_codes, const uint8_t* b_sf, const float* alpha, const float* gs2,
+                          uint8_t* out_codes, uint8_t* out_sf, float* amax, float* o_pairs, uint32_t* err,
+                          cudaStream_t st);
+
+fp4moe_status combine_launch(const fp4moe_config& cfg, int32_t T, const float* o_pairs, const float* w,
+                             uint16_t* y, cudaStream_t st);
+
+}  // namespace fp4moe

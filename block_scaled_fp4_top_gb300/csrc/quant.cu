@@ -1,0 +1,180 @@
+// NVFP4 quantisation kernels: activation quantise-and-scatter into slot order,
+// weight quantisation (with the W1 gate/up tile interleave), amax reductions,
+// global scales and alpha tables.
+//
+// Per 16-element block this is quantize_activation_nvfp4 on "Current Bug:
+// CuTeDSLMoERunner" ("Data Flow"). The scale assembly is the graph-safe
+// per-expert swizzle of "Bug 1", "Bug 11" and "Bug 14". Every expert's rows
+// start on a 128-row boundary, so writing each scale byte straight to its
+// 128x4 tile position gives exactly the concatenation of independently
+// swizzled per-expert blocks. The kernel needs no second scale pass and no
+// staging buffer.
+#include "common.cuh"
+#include "internal.h"
+
+namespace fp4moe {
+namespace {
+
+// One warp per slot row, 8 rows per CTA. Each lane quantises 16-element
+// blocks lane, lane+32, ... of the row.
+__global__ void __launch_bounds__(256) quant_scatter_kernel(int H, int E, int k, int cap,
+                                                            const uint16_t* __restrict__ x,
+                                                            const float* __restrict__ gs1,
+                                                            const int32_t* __restrict__ poff,
+                                                            const int32_t* __restrict__ pair_of_row,
+                                                            uint8_t* __restrict__ a1, uint8_t* __restrict__ a1_sf) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + warp;
+  const int R = min(__ldg(poff + E - 1), cap);
+  if (r >= R) return;
+  const int p = __ldg(pair_of_row + r);
+  const int C = H >> 4;
+  uint8_t* dst = a1 + (size_t)r * (H >> 1);
+  if (p < 0) {  // padding row: zero codes and zero scales
+    for (int b = lane; b < C; b += 32) {
+      *reinterpret_cast<uint2*>(dst + b * 8) = make_uint2(0u, 0u);
+      a1_sf[sf_offset(r, b, C)] = 0;
+    }
+    return;
+  }
+  const float g = __ldg(gs1);
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(p / k) * H);
+  for (int b = lane; b < C; b += 32) {
+    const uint4 u0 = __ldg(src + 2 * b), u1 = __ldg(src + 2 * b + 1);
+    const float v[16] = {bf16_lo(u0.x), bf16_hi(u0.x), bf16_lo(u0.y), bf16_hi(u0.y), bf16_lo(u0.z), bf16_hi(u0.z),
+                         bf16_lo(u0.w), bf16_hi(u0.w), bf16_lo(u1.x), bf16_hi(u1.x), bf16_lo(u1.y), bf16_hi(u1.y),
+                         bf16_lo(u1.z), bf16_hi(u1.z), bf16_lo(u1.w), bf16_hi(u1.w)};
+    uint32_t lo, hi;
+    const uint32_t sf = quant_block16(v, g, lo, hi);
+    *reinterpret_cast<uint2*>(dst + b * 8) = make_uint2(lo, hi);
+    a1_sf[sf_offset(r, b, C)] = (uint8_t)sf;
+  }
+}
+
+// Generic fp32 row quantiser. Row gr belongs to group gr / rows_per_group,
+// and its output row inside the group is either the same row or, when
+// inter > 0, the W1 kernel order: gate feature f -> 128*(f/64) + f%64,
+// up feature f -> 128*(f/64) + 64 + f%64.
+__global__ void __launch_bounds__(256) quant_rows_kernel(int64_t n_rows, int K, int rows_per_group, int inter,
+                                                         const float* __restrict__ in, const float* __restrict__ g,
+                                                         int g_div, uint8_t* __restrict__ codes,
+                                                         uint8_t* __restrict__ sf) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t gr = (int64_t)blockIdx.x * 8 + warp;
+  if (gr >= n_rows) return;
+  const int64_t grp = gr / rows_per_group;
+  int i = (int)(gr - grp * rows_per_group);
+  if (inter > 0) {
+    const int up = i >= inter;
+    const int f = up ? i - inter : i;
+    i = 128 * (f >> 6) + 64 * up + (f & 63);
+  }
+  const int C = K >> 4;
+  const float gg = __ldg(g + gr / g_div);
+  const float4* src = reinterpret_cast<const float4*>(in + gr * K);
+  uint8_t* dst = codes + (grp * rows_per_group + i) * (int64_t)(K >> 1);
+  uint8_t* sdst = sf + grp * (int64_t)rows_per_group * C;
+  for (int b = lane; b < C; b += 32) {
+    const float4 a = __ldg(src + 4 * b), c = __ldg(src + 4 * b + 1), d = __ldg(src + 4 * b + 2),
+                 e = __ldg(src + 4 * b + 3);
+    const float v[16] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w, e.x, e.y, e.z, e.w};
+    uint32_t lo, hi;
+    const uint32_t s = quant_block16(v, gg, lo, hi);
+    *reinterpret_cast<uint2*>(dst + b * 8) = make_uint2(lo, hi);
+    sdst[sf_offset(i, b, C)] = (uint8_t)s;
+  }
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+  return v;
+}
+
+// amax over each group of `per_group` fp32 values (grid.y = group). Result via an unsigned max on the
+// bit patterns of non-negative floats, which orders them correctly. The caller zeroes amax first.
+__global__ void __launch_bounds__(256) amax_f32_kernel(int64_t per_group, const float* __restrict__ in,
+                                                       float* __restrict__ amax) {
+  const float* base = in + (int64_t)blockIdx.y * per_group;
+  float m = 0.0f;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < per_group; i += (int64_t)gridDim.x * blockDim.x)
+    m = fmaxf(m, fabsf(base[i]));
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<unsigned int*>(amax + blockIdx.y), __float_as_uint(m));
+}
+
+__global__ void __launch_bounds__(256) amax_bf16_kernel(int64_t n, const uint16_t* __restrict__ in,
+                                                        float* __restrict__ amax) {
+  float m = 0.0f;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    m = fmaxf(m, fabsf(__uint_as_float((uint32_t)in[i] << 16)));
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<unsigned int*>(amax), __float_as_uint(m));
+}
+
+__global__ void gs_from_amax_kernel(int n, float* inout) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) inout[i] = global_scale_from_amax(inout[i]);
+}
+
+__global__ void make_alpha_kernel(int n, const float* __restrict__ gs_act, const float* __restrict__ gs_w,
+                                  float* __restrict__ alpha) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) alpha[i] = __fdiv_rn(1.0f, __fmul_rn(gs_act[0], gs_w[i]));
+}
+
+inline fp4moe_status last_status() { return cudaGetLastError() == cudaSuccess ? FP4MOE_OK : FP4MOE_CUDA_ERROR; }
+
+}  // namespace
+
+fp4moe_status quant_scatter_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const float* gs1,
+                                   const int32_t* poff, const int32_t* pair_of_row, uint8_t* a1, uint8_t* a1_sf,
+                                   cudaStream_t st) {
+  if (T == 0) return FP4MOE_OK;
+  const int cap = (int)capacity_rows(cfg, T);
+  quant_scatter_kernel<<<cap / 8, 256, 0, st>>>(cfg.hidden, cfg.num_experts, cfg.top_k, cap, x, gs1, poff,
+                                                pair_of_row, a1, a1_sf);
+  return last_status();
+}
+
+fp4moe_status quant_rows_launch(int64_t n_rows_total, int32_t K, int32_t rows_per_group, int32_t inter,
+                                const float* in, const float* g, int32_t g_div, uint8_t* codes, uint8_t* sf,
+                                cudaStream_t st) {
+  if (n_rows_total == 0) return FP4MOE_OK;
+  const int64_t blocks = (n_rows_total + 7) / 8;
+  quant_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>(n_rows_total, K, rows_per_group, inter, in, g, g_div, codes,
+                                                      sf);
+  return last_status();
+}
+
+fp4moe_status amax_f32_launch(int32_t n_groups, int64_t per_group, const float* in, float* amax, cudaStream_t st) {
+  if (n_groups == 0) return FP4MOE_OK;
+  if (cudaMemsetAsync(amax, 0, sizeof(float) * n_groups, st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
+  const int64_t want = (per_group + 256 * 16 - 1) / (256 * 16);
+  const unsigned bx = (unsigned)(want < 1 ? 1 : (want > 1024 ? 1024 : want));
+  amax_f32_kernel<<<dim3(bx, n_groups), 256, 0, st>>>(per_group, in, amax);
+  return last_status();
+}
+
+fp4moe_status amax_bf16_launch(int64_t n, const uint16_t* in, float* amax, cudaStream_t st) {
+  if (cudaMemsetAsync(amax, 0, sizeof(float), st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
+  if (n == 0) return FP4MOE_OK;
+  const int64_t want = (n + 256 * 16 - 1) / (256 * 16);
+  const unsigned bx = (unsigned)(want < 1 ? 1 : (want > 2048 ? 2048 : want));
+  amax_bf16_kernel<<<bx, 256, 0, st>>>(n, in, amax);
+  return last_status();
+}
+
+fp4moe_status gs_from_amax_launch(int32_t n, float* inout, cudaStream_t st) {
+  if (n == 0) return FP4MOE_OK;
+  gs_from_amax_kernel<<<(n + 255) / 256, 256, 0, st>>>(n, inout);
+  return last_status();
+}
+
+fp4moe_status make_alpha_launch(int32_t n, const float* gs_act, const float* gs_w, float* alpha, cudaStream_t st) {
+  if (n == 0) return FP4MOE_OK;
+  make_alpha_kernel<<<(n + 255) / 256, 256, 0, st>>>(n, gs_act, gs_w, alpha);
+  return last_status();
+}
+
+}  // namespace fp4moe

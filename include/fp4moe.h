@@ -1,0 +1,288 @@
+/*
+ * fp4moe.h - C ABI of a single-GPU routed mixture-of-experts FFN layer with
+ * block-scaled FP4 (NVFP4) experts, for GB300 (sm_103a).
+ *
+ * The layer is the one on "Current Bug: CuTeDSLMoERunner - Status & Debug
+ * History", section "Key Architecture: CuTeDSL NVFP4 MoE / Data Flow":
+ *   route -> per-expert counts and offsets -> scatter into 128-row-padded
+ *   expert slots -> NVFP4 quantise with per-expert swizzled block scales ->
+ *   grouped GEMM W13 (gate | up) -> clamped SwiGLU -> NVFP4 requantise ->
+ *   grouped GEMM W2 -> weighted top-k combine.
+ * At the DeepSeek-V4-Flash shape ("Lucifer-CUTLASS TP3 virtual-padding
+ * audit", section "TP3 shape plan") that is hidden 4096, intermediate 2048,
+ * 256 experts, top-k 6 and swiglu_limit 10.
+ *
+ * Conventions, shared by every call:
+ *  - Each call returns fp4moe_status. FP4MOE_OK means the work was ENQUEUED on
+ *    `stream`. It does not mean the work has finished.
+ *  - The caller owns all device memory. The library never allocates device
+ *    memory, never synchronises, and never reads device values on the host
+ *    (exceptions: the prep helpers marked so, and fp4moe_read_error).
+ *    "CUDA-Graph Safety / GPU-Native Requirements", SECTION B, asks this of
+ *    every graph-captured step. The hot-path calls can therefore be captured
+ *    into a CUDA graph once they have each been called once outside capture:
+ *    the first call configures kernel attributes.
+ *  - Pointers are DEVICE pointers unless named *_host. Every device pointer
+ *    must be 16-byte aligned, or FP4MOE_MISALIGNED is returned.
+ *  - bf16 tensors are passed as uint16_t bit patterns.
+ *  - T (tokens) is a host integer, 0 <= T <= cfg->max_tokens. It selects the
+ *    launch sizes, so one CUDA graph is captured per T.
+ *  - `ws` is a device workspace of fp4moe_workspace_bytes(cfg) bytes. Zero it
+ *    once before first use. Its first 4 bytes are a sticky device error word:
+ *    a bitwise OR of FP4MOE_ERR_* values. Kernels set bits there instead of
+ *    trapping. Read and clear it with fp4moe_read_error outside any graph.
+ *    Calls that share a workspace must be ordered on one stream.
+ *
+ * Padded layout (from "Current Bug", sections "Bug 2", "Bug 4", "Bug 9" and
+ * "Bug 14"):
+ *  - counts[e]: number of (token, k) pairs routed to expert e.
+ *  - offsets[e]: inclusive running sum of counts, with NO leading 0
+ *    (counts [4,4,0] -> offsets [4,8,8]).
+ *  - P_e = align_up(counts[e], 128). padded_offsets[e] is the inclusive
+ *    running sum of P_e, also with no leading 0. Expert e owns rows
+ *    [padded_offsets[e] - P_e, padded_offsets[e]). A row's expert is
+ *    searchsorted(padded_offsets, row, right=True).
+ *  - R = padded_offsets[E-1] <= fp4moe_capacity_rows(cfg, T) = CAP, where
+ *    CAP = align_down(T*k + 127*min(E, T*k), 128), at least 128.
+ *  - Inside an expert, real rows come first, in ascending pair index
+ *    p = t*k + j. Padding rows follow.
+ *  - pair_of_row[r] = p for a real row, -1 for a padding row (r < R). Rows
+ *    r >= R are not written. The row's token is p / k.
+ *  - Activations in slot order: a*_fp4 is [CAP][K/2] bytes, two E2M1 codes
+ *    per byte, element 2i in the low nibble. a*_sf holds the E4M3 block
+ *    scales (one per 16 elements) in the 128x4 "32_4_4" tile layout
+ *    ("Bug 1", "Bug 11"), with C = K/16 scale columns:
+ *      byte(r, c) = ((r/128)*(C/4) + c/4)*512 + (r%32)*16 + ((r%128)/32)*4 + c%4
+ *    Padding rows hold zero codes and zero scales.
+ *
+ * NVFP4 value of code q under block scale sf and global scale g:
+ *   decode_e2m1(q) * decode_e4m3(sf) / g.
+ * g is the quant-direction global scale RN(2688 / amax) ("Current Bug",
+ * sections "Bug 5" and "Bug 6": separate L1 and L2 activation scales, fixed
+ * in a warmup pass).
+ *
+ * Expert weights (written by fp4moe_quantize_weights, K-major):
+ *  - W1: [E][2I][H/2] codes and [E][2I/128][H/64][512] scales. Rows are in
+ *    KERNEL order: for each 64-feature group f = 0 .. I/64-1, rows
+ *    [128f, 128f+64) are gate features [64f, 64f+64) and rows
+ *    [128f+64, 128f+128) are up features [64f, 64f+64). Logical W13 has the
+ *    gate in rows [0, I) and up in rows [I, 2I).
+ *  - W2: [E][H][I/2] codes and [E][H/128][I/64][512] scales.
+ *  - One fp32 quant-direction global scale per expert per matrix.
+ *  - alpha1[e] = 1 / (gs1 * gw1[e]) and alpha2[e] = 1 / (gs2 * gw2[e]),
+ *    written by fp4moe_make_alpha.
+ *
+ * Supported shapes: H % 256 == 0, I % 128 == 0, 1 <= k <= 16, k <= E <= 1024,
+ * w_format == FP4MOE_W_NVFP4. Anything else returns FP4MOE_UNSUPPORTED.
+ */
+#ifndef FP4MOE_H_
+#define FP4MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* fp4moe_stream_t;
+
+typedef enum fp4moe_status {
+  FP4MOE_OK = 0,
+  FP4MOE_INVALID_ARG = 1,   /* null pointer, T out of range, bad config field */
+  FP4MOE_MISALIGNED = 2,    /* a device pointer is not 16-byte aligned */
+  FP4MOE_CAPACITY = 3,      /* T > max_tokens, or a buffer bound would be exceeded */
+  FP4MOE_UNSUPPORTED = 4,   /* shape or format outside the supported set */
+  FP4MOE_CUDA_ERROR = 5     /* a CUDA runtime call or launch failed */
+} fp4moe_status;
+
+/* Device error word bits (sticky; see fp4moe_read_error). */
+#define FP4MOE_ERR_TIMEOUT   0x1u  /* a bounded wait inside a kernel expired; its tile was skipped */
+#define FP4MOE_ERR_EXPERT_ID 0x2u  /* a routed expert id was outside [0, E) */
+#define FP4MOE_ERR_CAPACITY  0x4u  /* padded rows R exceeded CAP */
+
+#define FP4MOE_W_NVFP4 0
+#define FP4MOE_W_MXFP4 1
+
+typedef struct fp4moe_config {
+  int32_t hidden;        /* H */
+  int32_t inter;         /* I, kernel-local intermediate width */
+  int32_t inter_logical; /* logical intermediate (== inter for NVFP4) */
+  int32_t num_experts;   /* E */
+  int32_t top_k;         /* k */
+  int32_t max_tokens;    /* largest T any call will pass */
+  float swiglu_limit;    /* L of the clamped SwiGLU */
+  int32_t w_format;      /* FP4MOE_W_NVFP4 */
+} fp4moe_config;
+
+/* Version of this ABI (major*100 + minor). */
+int32_t fp4moe_abi_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* fp4moe_status_string(fp4moe_status s);
+
+/* CAP(T): rows of every slot-ordered activation buffer for a T-token call. */
+size_t fp4moe_capacity_rows(const fp4moe_config* cfg, int32_t T);
+
+/* Bytes of the workspace for any T <= cfg->max_tokens (0 on a bad config). */
+size_t fp4moe_workspace_bytes(const fp4moe_config* cfg);
+
+/* Byte sizes of the kernel-ready expert weight buffers (any output may be NULL). */
+fp4moe_status fp4moe_weight_bytes(const fp4moe_config* cfg, size_t* w1_codes, size_t* w1_sf,
+                                  size_t* w2_codes, size_t* w2_sf);
+
+/*
+ * moe_route: router logits, softmax top-k, per-expert counts, offsets and
+ * 128-row-padded slots.
+ *   l[t,e] = RN_f32(sum_h x[t,h]*router_w[e,h]) (+ router_bias[e] in fp32).
+ *     The sum is an fp32 compensated (two-sum) reduction in a fixed order, so
+ *     it equals the exact sum rounded once except within about an ulp.
+ *   topk_ids[t,:]: the k largest l[t,:], in descending order; ties go to the
+ *     lower expert id.
+ *   topk_w[t,j] = exp(l_j - l_max) / sum_selected exp(l - l_max) (fp32).
+ *   counts, offsets, padded_offsets, slot_of_pair, pair_of_row as above.
+ * Slot ranks are integer-deterministic: they do not depend on the order of
+ * atomics.
+ *   x [T][H] bf16, router_w [E][H] bf16, router_bias [E] fp32 or NULL,
+ *   logits_out [T][E] fp32 or NULL, topk_ids [T][k] int32, topk_w [T][k] fp32,
+ *   counts/offsets/padded_offsets [E] int32, slot_of_pair [T*k] int32,
+ *   pair_of_row [CAP] int32.
+ * Source: "Current Bug", "Data Flow" (remap -> sort by expert). "CUDA-Graph
+ * Safety", SECTION B (counts by scatter-add into a fixed buffer, no
+ * bincount) and SECTION C row 4.
+ */
+fp4moe_status moe_route(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
+                        const float* router_bias, float* logits_out, int32_t* topk_ids, float* topk_w,
+                        int32_t* counts, int32_t* offsets, int32_t* padded_offsets, int32_t* slot_of_pair,
+                        int32_t* pair_of_row, void* ws, fp4moe_stream_t stream);
+
+/*
+ * moe_quantize_scatter: L1 activation quantisation into slot order. Each
+ * row r < R gets NVFP4(x[pair_of_row[r]/k]) under the global scale *gs1.
+ * Codes go to a1_fp4 [CAP][H/2] and swizzled scales to a1_sf
+ * [CAP*H/16 bytes]. Padding rows get zeros.
+ * Per 16-element block, in IEEE fp32 with RNE:
+ *   a = max|v|; s = RN(RN(a/6)*g); sf = E4M3_satfinite(s);
+ *   inv = sf ? RN(g/sf) : 0; q = E2M1_satfinite(RN(v*inv)).
+ * Source: "Current Bug", "Data Flow" (quantize_activation_nvfp4 and
+ * _assemble_scales_cudagraph_safe), "Bug 1" and "Bug 14".
+ */
+fp4moe_status moe_quantize_scatter(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const float* gs1,
+                                   const int32_t* padded_offsets, const int32_t* pair_of_row, uint8_t* a1_fp4,
+                                   uint8_t* a1_sf, void* ws, fp4moe_stream_t stream);
+
+/*
+ * moe_grouped_gemm_w1_swiglu: for every padded row r of expert e,
+ *   [g; u] = alpha1[e] * (A1[r] . W1_e), a block-scaled FP4 MMA with fp32
+ *   accumulation,
+ *   h = silu(min(g, L)) * clamp(u, -L, L)  (fp32),
+ * then NVFP4-requantise h under *gs2 into a2_fp4 [CAP][I/2] and a2_sf
+ * (swizzled, C = I/16). Padding rows get zeros.
+ * Source: "Current Bug", "Data Flow" (run_nvfp4_grouped_gemm -> l1_out ->
+ * SiLU(gate)*up -> quantise), "Bug 6" and "Bug 7". "Lucifer-CUTLASS TP3
+ * virtual-padding audit", "TP3 shape plan" (swiglu_limit).
+ */
+fp4moe_status moe_grouped_gemm_w1_swiglu(const fp4moe_config* cfg, int32_t T, const uint8_t* a1_fp4,
+                                         const uint8_t* a1_sf, const int32_t* padded_offsets,
+                                         const int32_t* pair_of_row, const uint8_t* w1_fp4, const uint8_t* w1_sf,
+                                         const float* alpha1, const float* gs2, uint8_t* a2_fp4, uint8_t* a2_sf,
+                                         void* ws, fp4moe_stream_t stream);
+
+/*
+ * moe_grouped_gemm_w2: the second grouped GEMM on its own. For every real
+ * row r (pair p = pair_of_row[r]),
+ *   o_pairs[p][:] = alpha2[e] * (A2[r] . W2_e)  (fp32 [T*k][H]).
+ * Source: "Current Bug", "Data Flow" (L2 grouped GEMM -> l2_out).
+ */
+fp4moe_status moe_grouped_gemm_w2(const fp4moe_config* cfg, int32_t T, const uint8_t* a2_fp4, const uint8_t* a2_sf,
+                                  const int32_t* padded_offsets, const int32_t* pair_of_row, const uint8_t* w2_fp4,
+                                  const uint8_t* w2_sf, const float* alpha2, float* o_pairs, void* ws,
+                                  fp4moe_stream_t stream);
+
+/*
+ * moe_combine: y[t][:] = bf16( sum_{j=0..k-1} topk_w[t][j] * o_pairs[t*k+j][:] ),
+ * accumulated in fp32 in j order. Source: "Current Bug", "Data Flow"
+ * (scatter_add -> y) and "Bug 14" (padding rows are dropped).
+ */
+fp4moe_status moe_combine(const fp4moe_config* cfg, int32_t T, const float* o_pairs, const float* topk_w,
+                          uint16_t* y, fp4moe_stream_t stream);
+
+/* moe_grouped_gemm_w2 followed by moe_combine, with o_pairs inside `ws`. */
+fp4moe_status moe_grouped_gemm_w2_combine(const fp4moe_config* cfg, int32_t T, const uint8_t* a2_fp4,
+                                          const uint8_t* a2_sf, const int32_t* padded_offsets,
+                                          const int32_t* pair_of_row, const uint8_t* w2_fp4, const uint8_t* w2_sf,
+                                          const float* alpha2, const float* topk_w, uint16_t* y, void* ws,
+                                          fp4moe_stream_t stream);
+
+/*
+ * moe_forward: the whole layer (route, quantize_scatter, W1+SwiGLU+requant,
+ * W2, combine) on one stream, with every intermediate inside `ws`.
+ * y [T][H] bf16. topk_ids_out / topk_w_out may be NULL. When they are not,
+ * the routing decision is copied there.
+ */
+fp4moe_status moe_forward(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
+                          const float* router_bias, const float* gs1, const float* gs2, const uint8_t* w1_fp4,
+                          const uint8_t* w1_sf, const float* alpha1, const uint8_t* w2_fp4, const uint8_t* w2_sf,
+                          const float* alpha2, uint16_t* y, int32_t* topk_ids_out, float* topk_w_out, void* ws,
+                          fp4moe_stream_t stream);
+
+/* ------------------------------------------------------------------ prep --
+ * Load-time helpers. They run outside the timed hot path and may use
+ * cudaMemsetAsync. They still never synchronise.
+ */
+
+/*
+ * fp4moe_quantize_weights: NVFP4-quantise n_experts experts of one matrix.
+ *   which = 1: w [n][2I][H] fp32 logical W13 (gate rows first) -> W1 layout
+ *   which = 2: w [n][H][I] fp32 -> W2 layout
+ * gs_out[e] = RN(2688 / amax(w_e)) is the quant-direction global scale of
+ * expert e. Codes and swizzled scales go to the layouts described above.
+ * Experts are independent, so a caller may convert them in chunks by passing
+ * offset pointers.
+ * Source: "Current Bug", "vLLM Integration Status" (weight stacking
+ * make_b_k_major + assemble_scales_3d_side).
+ */
+fp4moe_status fp4moe_quantize_weights(const fp4moe_config* cfg, int32_t which, int32_t n_experts, const float* w,
+                                      uint8_t* codes_out, uint8_t* sf_out, float* gs_out, fp4moe_stream_t stream);
+
+/* alpha[e] = RN(1 / RN(gs_act[0] * gs_w[e])) for e < n. */
+fp4moe_status fp4moe_make_alpha(int32_t n, const float* gs_act, const float* gs_w, float* alpha,
+                                fp4moe_stream_t stream);
+
+/*
+ * fp4moe_calibrate: activation global scales from a warmup batch
+ * ("Current Bug", sections "Bug 5" and "Bug 6": compute_activation_global_scales
+ * runs before capture, separately for L1 and L2).
+ *   gs1 = RN(2688 / amax|x_warm|)
+ *   gs2 = RN(2688 / amax|h|), where h is the SwiGLU output over every real
+ *         slot row of the warmup batch, quantised under gs1.
+ * Needs the gw1 table (weight global scales of W1) to form alpha1 internally.
+ * Writes gs1_out[0] and gs2_out[0].
+ */
+fp4moe_status fp4moe_calibrate(const fp4moe_config* cfg, int32_t T, const uint16_t* x_warm, const uint16_t* router_w,
+                               const float* router_bias, const uint8_t* w1_fp4, const uint8_t* w1_sf,
+                               const float* gw1, float* gs1_out, float* gs2_out, void* ws, fp4moe_stream_t stream);
+
+/*
+ * fp4moe_quantize_rows_f32: the NVFP4 block quantiser on its own. It is the
+ * same device routine the kernels above use, for tests of the codec and of
+ * the requantisation step on identical fp32 input.
+ *   in [rows][K] fp32; g[rows] per-row global scales (device);
+ *   codes [rows][K/2]; sf swizzled with C = K/16 (rows % 128 == 0, K % 64 == 0).
+ */
+fp4moe_status fp4moe_quantize_rows_f32(int32_t rows, int32_t K, const float* in, const float* g, uint8_t* codes,
+                                       uint8_t* sf, fp4moe_stream_t stream);
+
+/*
+ * fp4moe_read_error: copy the workspace's device error word to *err_host.
+ * If clear != 0, zero it afterwards. This call SYNCHRONISES `stream`: use it
+ * outside graphs, between steps.
+ */
+fp4moe_status fp4moe_read_error(void* ws, uint32_t* err_host, int32_t clear, fp4moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP4MOE_H_ */

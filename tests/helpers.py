@@ -1,0 +1,83 @@
+"""Shared test utilities: bf16 conversions, GPU layer set-up from the seeded
+generator, a lazily filled oracle expert table, and the float parity check."""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+
+import synthgen as sg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def ensure_built():
+    from block_scaled_fp4_top_gb300 import build as libbuild
+    from synthgen import build as synthbuild
+    libbuild.build()
+    synthbuild.build()
+
+
+def bits_to_torch(bits: np.ndarray, device="cuda"):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def torch_to_bits(t) -> np.ndarray:
+    import torch
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def make_layer(wl: sg.Workload, max_tokens: int, chunk: int = 16):
+    """GPU layer whose weights come from the GPU twin of the generator, quantised by the library."""
+    import torch
+    from block_scaled_fp4_top_gb300 import api
+    from synthgen import gpu as sgpu
+    cfg = api.config(wl.H, wl.I, wl.E, wl.k, max_tokens, wl.swiglu_limit)
+    layer = api.MoELayer(cfg)
+    for e0 in range(0, wl.E, chunk):
+        n = min(chunk, wl.E - e0)
+        w1 = sgpu.expert_w1(wl, e0, n)
+        layer.quantize_weights(1, e0, w1)
+        del w1
+        w2 = sgpu.expert_w2(wl, e0, n)
+        layer.quantize_weights(2, e0, w2)
+        del w2
+    bias = sg.router_bias_f32(wl)
+    layer.set_router(sgpu.router(wl), None if bias is None else torch.from_numpy(bias).cuda())
+    torch.cuda.synchronize()
+    return layer
+
+
+class OracleExperts:
+    """Expert weights for the oracle: numpy generator + oracle quantiser, cached per expert."""
+
+    def __init__(self, wl: sg.Workload):
+        self.wl = wl
+        self.cache = {}
+
+    def __call__(self, e: int):
+        from oracle import moe
+        if e not in self.cache:
+            self.cache[e] = moe.quantize_expert(sg.expert_w1_f32(self.wl, e), sg.expert_w2_f32(self.wl, e))
+        return self.cache[e]
+
+
+def float_parity(got: np.ndarray, ref: np.ndarray, rel_l2: float = 1e-2, max_abs_rms: float = 2e-2):
+    """The layer's float bar: relative L2 <= 1e-2 and max |err| <= 2e-2 * RMS(ref)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.isfinite(got).all(), "non-finite output"
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300)
+    rms = np.sqrt(np.mean(ref ** 2))
+    mx = np.abs(got - ref).max() if got.size else 0.0
+    assert rel <= rel_l2 and mx <= max_abs_rms * rms, f"rel L2 {rel:.3e} (<= {rel_l2}), max abs {mx:.3e} (<= {max_abs_rms} * rms {rms:.3e})"
+    return rel, mx / rms if rms > 0 else 0.0
+
+
+def dump(name: str, **arrays):
+    """Save arrays for offline diagnosis when FP4MOE_DUMP_DIR is set."""
+    d = os.environ.get("FP4MOE_DUMP_DIR")
+    if d:
+        os.makedirs(d, exist_ok=True)
+        np.savez_compressed(os.path.join(d, name + ".npz"), **arrays)

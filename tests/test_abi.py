@@ -1,0 +1,91 @@
+"""The C ABI library on the CPU: it loads, exports every symbol declared in
+include/fp4moe.h, and its host-side argument checks and sizing are right.
+No call here reaches a CUDA API: every checked call fails validation first."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from helpers import ROOT, ensure_built
+from oracle import layout
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ensure_built()
+    from block_scaled_fp4_top_gb300 import _lib
+    return _lib.load()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "fp4moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s+\*?([a-z_0-9]+)\s*\(", src, flags=re.M))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from block_scaled_fp4_top_gb300 import _lib
+    names = header_functions()
+    assert "moe_forward" in names and "moe_route" in names and len(names) >= 17
+    for n in names:
+        assert hasattr(lib, n), n
+    assert names == set(_lib.SIGNATURES), names ^ set(_lib.SIGNATURES)
+
+
+def test_library_does_not_link_libcuda():
+    ensure_built()
+    from block_scaled_fp4_top_gb300 import _lib
+    import subprocess
+    out = subprocess.run(["ldd", _lib.LIB_PATH], capture_output=True, text=True).stdout
+    assert "libcuda.so" not in out
+
+
+def _cfg(**kw):
+    from block_scaled_fp4_top_gb300 import api
+    d = dict(hidden=4096, inter=2048, num_experts=256, top_k=6, max_tokens=64, swiglu_limit=10.0)
+    d.update(kw)
+    return api.config(**d)
+
+
+def test_capacity_matches_oracle(lib):
+    for T in [0, 1, 2, 21, 22, 64, 100, 4096, 8192]:
+        for k, E in [(6, 256), (2, 8)]:
+            cfg = _cfg(top_k=k, num_experts=E, max_tokens=8192)
+            assert lib.fp4moe_capacity_rows(ctypes.byref(cfg), T) == layout.capacity_rows(T, k, E)
+
+
+def test_sizes(lib):
+    cfg = _cfg()
+    from block_scaled_fp4_top_gb300 import api
+    b1, s1, b2, s2 = api.weight_bytes(cfg)
+    assert (b1, s1, b2, s2) == (256 * 4096 * 4096 // 2, 256 * 4096 * 4096 // 16, 256 * 4096 * 2048 // 2,
+                                256 * 4096 * 2048 // 16)
+    ws = api.workspace_bytes(cfg)
+    cap = layout.capacity_rows(64, 6, 256)
+    assert ws >= cap * (4096 // 2 + 4096 // 16 + 2048 // 2 + 2048 // 16) + 64 * 6 * 4096 * 4
+    assert api.workspace_bytes(_cfg(hidden=100)) == 0  # unsupported shape -> 0
+
+
+def test_argument_checks(lib):
+    from block_scaled_fp4_top_gb300 import _lib
+    cfg = _cfg()
+    p = ctypes.c_void_p(0x10000)     # aligned, never dereferenced: validation fails first
+    bad = ctypes.c_void_p(0x10004)
+    null = None
+    args = [p] * 13
+    # null pointer
+    assert lib.moe_route(ctypes.byref(cfg), 8, null, *args[1:]) == _lib.INVALID_ARG
+    # misaligned
+    assert lib.moe_route(ctypes.byref(cfg), 8, bad, *args[1:]) == _lib.MISALIGNED
+    # T beyond max_tokens
+    assert lib.moe_route(ctypes.byref(cfg), 65, *args) == _lib.CAPACITY
+    assert lib.moe_route(ctypes.byref(cfg), -1, *args) == _lib.INVALID_ARG
+    # unsupported shapes / format
+    assert lib.moe_route(ctypes.byref(_cfg(hidden=4000)), 8, *args) == _lib.UNSUPPORTED
+    assert lib.moe_route(ctypes.byref(_cfg(top_k=17)), 8, *args) == _lib.UNSUPPORTED
+    assert lib.moe_route(ctypes.byref(_cfg(w_format=_lib.W_MXFP4)), 8, *args) == _lib.UNSUPPORTED
+    assert lib.moe_forward(None, 8, *([p] * 16)) == _lib.INVALID_ARG
+    assert lib.fp4moe_quantize_rows_f32(100, 64, p, p, p, p, p) == _lib.INVALID_ARG  # rows % 128
+    assert lib.fp4moe_status_string(_lib.CAPACITY) == b"FP4MOE_CAPACITY"
+    assert lib.fp4moe_abi_version() == 100
