@@ -108,6 +108,7 @@ def setup_layer(wl, max_tokens):
     layer.set_router(sgpu.router(wl), None if bias is None else torch.from_numpy(bias).cuda())
     layer.calibrate(sgpu.activations(wl, sg.WARMUP_SEED))
     torch.cuda.synchronize()
+    torch.cuda.empty_cache()  # drop the fp32 weight staging buffers
     return cfg, layer
 
 
@@ -298,10 +299,15 @@ def main():
     ap.add_argument("--workload", default=sg.DSV4_DECODE.name, choices=sorted(sg.WORKLOADS))
     ap.add_argument("--oracle-tokens", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override E (smaller case for profiler captures; the default is the workload's E)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     wl = sg.WORKLOADS[args.workload]
+    if args.experts:
+        import dataclasses
+        wl = dataclasses.replace(wl, E=args.experts, name=f"{wl.name}_E{args.experts}")
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
 
