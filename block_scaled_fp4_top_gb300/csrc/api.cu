@@ -134,9 +134,9 @@ fp4moe_status fp4moe_weight_bytes(const fp4moe_config* cfg, size_t* w1_codes, si
                                   size_t* w2_sf) {
   FP4_TRY(check_cfg(cfg));
   const size_t E = cfg->num_experts, H = cfg->hidden, I = cfg->inter;
-  if (w1_codes) *w1_codes = E * 2 * I * H / 2;
+  if (w1_codes) *w1_codes = E * tiled_weight_bytes(2 * cfg->inter, cfg->hidden);
   if (w1_sf) *w1_sf = E * 2 * I * H / 16;
-  if (w2_codes) *w2_codes = E * H * I / 2;
+  if (w2_codes) *w2_codes = E * tiled_weight_bytes(cfg->hidden, cfg->inter);
   if (w2_sf) *w2_sf = E * H * I / 16;
   return FP4MOE_OK;
 }
@@ -257,7 +257,10 @@ fp4moe_status fp4moe_quantize_weights(const fp4moe_config* cfg, int32_t which, i
   const int32_t K = which == 1 ? cfg->hidden : cfg->inter;
   FP4_TRY(amax_f32_launch(n_experts, (int64_t)rows * K, w, gs_out, st));
   FP4_TRY(gs_from_amax_launch(n_experts, gs_out, st));
-  return quant_rows_launch((int64_t)n_experts * rows, K, rows, which == 1 ? cfg->inter : 0, w, gs_out, rows,
+  if (K % 256 != 0 &&  // the last k-stage of every block is padded with zero codes
+      cudaMemsetAsync(codes_out, 0, (size_t)n_experts * tiled_weight_bytes(rows, K), st) != cudaSuccess)
+    return FP4MOE_CUDA_ERROR;
+  return quant_rows_launch((int64_t)n_experts * rows, K, rows, which == 1 ? cfg->inter : 0, 1, w, gs_out, rows,
                            codes_out, sf_out, st);
 }
 
@@ -303,7 +306,7 @@ fp4moe_status fp4moe_quantize_rows_f32(int32_t rows, int32_t K, const float* in,
                                        uint8_t* sf, fp4moe_stream_t stream) {
   if (rows < 0 || K <= 0 || K % 64 != 0 || rows % 128 != 0) return FP4MOE_INVALID_ARG;
   FP4_TRY(check_ptrs(in, g, codes, sf));
-  return quant_rows_launch(rows, K, rows > 0 ? rows : 1, 0, in, g, 1, codes, sf, (cudaStream_t)stream);
+  return quant_rows_launch(rows, K, rows > 0 ? rows : 1, 0, 0, in, g, 1, codes, sf, (cudaStream_t)stream);
 }
 
 fp4moe_status fp4moe_read_error(void* ws, uint32_t* err_host, int32_t clear, fp4moe_stream_t stream) {

@@ -8,15 +8,25 @@
 // searchsorted(padded_offsets, row, right=True) on offsets with no leading 0
 // ("Bug 2", "Bug 4").
 //
-// One CTA computes one 128 (rows) x 128 (weight rows) output tile:
-//   warp 4      TMA producer. FP4 tiles come in by cp.async.bulk.tensor with
-//               the 128-byte swizzle, and the 512-byte scale tiles by plain
-//               cp.async.bulk, all into a STAGES-deep shared-memory ring.
-//   warp 5      MMA issuer. tcgen05.cp moves the scale tiles into TMEM, then
-//               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X issues
-//               (K = 64 per instruction, fp32 accumulator in TMEM), and
-//               tcgen05.commit frees the ring slot.
-//   warps 0-3   epilogue. tcgen05.ld brings one accumulator row per thread.
+// Persistent kernel: one CTA per SM walks output tiles
+// tau = blockIdx.x, blockIdx.x + gridDim.x, ... Each tile is 128 activation
+// rows x 128 weight rows. Tiles are ordered expert, then n-tile, then the
+// expert's m-tiles, so CTAs that run at the same time share an expert's
+// activation tile in L2.
+//   warp 4      producer. Each stage moves one 16 KB weight block with a
+//               single contiguous cp.async.bulk: the weights are stored
+//               pre-tiled and pre-swizzled (see fp4moe.h). The 128-row
+//               activation tile arrives by cp.async.bulk.tensor with the
+//               128-byte swizzle, and the A and B scale tiles (2 KB each) by
+//               cp.async.bulk. The STAGES-deep shared-memory ring runs on
+//               across tile boundaries, so the weight stream never stops.
+//   warp 5      MMA issuer. tcgen05.cp moves the scale tiles into per-stage
+//               TMEM columns. tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
+//               (K = 64 each) accumulates in fp32 into one of two TMEM
+//               accumulator buffers. tcgen05.commit frees the ring slot and
+//               then hands the buffer to the epilogue.
+//   warps 0-3   epilogue. tcgen05.ld gives one accumulator row per thread.
+//               The epilogue of tile i overlaps the MMAs of tile i+1.
 //     W1: alpha, then the clamped SwiGLU (gate columns 0-63, up columns
 //         64-127, from the W1 kernel row order), then NVFP4 requantisation
 //         into the L2 slot buffers ("Bug 6", "Bug 7").
@@ -24,8 +34,8 @@
 //     W2: alpha, then fp32 rows stored per (token, k) pair. Padding rows are
 //         dropped ("Bug 14").
 // Every spin-wait is bounded (mbar_wait). A timeout sets FP4MOE_ERR_TIMEOUT
-// in the error word. The CTA then drains its in-flight copies and MMAs,
-// frees its TMEM and returns.
+// in the error word. Each role then stops, waits for its in-flight copies and
+// MMAs, and the CTA frees its TMEM and returns.
 #include <mutex>
 
 #include "common.cuh"
@@ -37,27 +47,29 @@ namespace {
 constexpr int BM = 128;            // activation rows per tile (MMA M)
 constexpr int BN = 128;            // weight rows per tile (MMA N)
 constexpr int KBYTES = 128;        // K bytes per stage: 256 FP4 elements = 4 MMAs of K = 64
-constexpr int STAGES = 3;
+constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * KBYTES;
-constexpr int B_BYTES = BN * KBYTES;
-constexpr int SF_TILE = 512;       // one 128x4 scale tile
+constexpr int B_BYTES = BN * KBYTES;  // one pre-tiled weight block
+constexpr int SF_TILE = 512;          // one 128x4 scale tile
 constexpr int SFA_OFF = A_BYTES + B_BYTES;
 constexpr int SFB_OFF = SFA_OFF + 4 * SF_TILE;
 constexpr int STAGE_BYTES = SFB_OFF + 4 * SF_TILE;  // 36864, a multiple of 1024
 constexpr int BAR_OFF = STAGES * STAGE_BYTES;
 constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;    // barriers + 1024-byte alignment slack
 constexpr int THREADS = 192;
-constexpr uint32_t TMEM_COLS = 256;
-constexpr uint32_t ACC_COL = 0;    // accumulator: columns [0, 128)
-constexpr uint32_t SF_COL = 128;   // per stage: 32 columns, [0,16) A scales, [16,32) B scales
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_COLS = 128;  // accumulator buffer b: columns [128 b, 128 b + 128)
+constexpr uint32_t SF_COL = 2 * ACC_COLS;  // stage s: 32 columns, [0,16) A scales, [16,32) B scales
 static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
 static_assert(SF_COL + STAGES * 32 <= TMEM_COLS, "TMEM budget");
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 struct Params {
-  int E, K, b_rows, NT, k, cap, I, H;
+  int E, K, KB, b_rows, NT, k, cap, I, H;
   float limit;
   const int32_t* poff;
   const int32_t* pair_of_row;
+  const uint8_t* b_codes;
   const uint8_t* a_sf;
   const uint8_t* b_sf;
   const float* alpha;
@@ -69,12 +81,35 @@ struct Params {
   uint32_t* err;
 };
 
+struct Tile {
+  int e, nt, mt;
+};
+
+// tau -> (expert, n-tile, m-tile): experts in order; inside an expert, n-tiles, then its m-tiles.
+__device__ __forceinline__ Tile map_tile(int tau, const int32_t* __restrict__ poff, int E, int NT) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if ((__ldg(poff + mid) / BM) * NT > tau) hi = mid;
+    else lo = mid + 1;
+  }
+  const int mt_end = __ldg(poff + lo) / BM;
+  const int mt_start = lo > 0 ? __ldg(poff + lo - 1) / BM : 0;
+  const int m_e = mt_end - mt_start;
+  const int local = tau - mt_start * NT;
+  return Tile{lo, local / m_e, mt_start + local % m_e};
+}
+
 // Bounded wait that ignores other CTAs' aborts: used only while draining.
 __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer() - t0 > kWaitLimitNs) return;
   }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ float swiglu(float g, float u, float L) {
@@ -84,39 +119,94 @@ __device__ __forceinline__ float swiglu(float g, float u, float L) {
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(THREADS, 2)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const Params prm) {
+__device__ __forceinline__ void epilogue_tile(const Params& prm, const Tile& tl_, uint32_t tacc, int warp, int lane) {
+  const int r = tl_.mt * BM + warp * 32 + lane;
+  const int p = __ldg(prm.pair_of_row + r);
+  const float alpha = __ldg(prm.alpha + tl_.e);
+  const uint32_t tl = tacc + ((uint32_t)(warp * 32) << 16);
+  if constexpr (MODE == kW2Rows) {
+    float* dst = prm.o_pairs + (size_t)(p < 0 ? 0 : p) * prm.H + tl_.nt * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float v[32];
+      tmem_ld32(tl + c * 32, v);
+      tmem_ld_wait();
+      if (p >= 0) {
+        float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          d4[q] = make_float4(__fmul_rn(v[4 * q], alpha), __fmul_rn(v[4 * q + 1], alpha),
+                              __fmul_rn(v[4 * q + 2], alpha), __fmul_rn(v[4 * q + 3], alpha));
+      }
+    }
+  } else {
+    const float L = prm.limit;
+    const float g2 = (MODE == kW1SwiGLU) ? __ldg(prm.gs2) : 1.0f;
+    uint32_t codes[8];
+    uint32_t sfw = 0;
+    float hmax = 0.0f;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float g[32], u[32];
+      tmem_ld32(tl + half * 32, g);
+      tmem_ld32(tl + 64 + half * 32, u);
+      tmem_ld_wait();
+#pragma unroll
+      for (int blk = 0; blk < 2; ++blk) {
+        float h[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          h[j] = swiglu(__fmul_rn(g[blk * 16 + j], alpha), __fmul_rn(u[blk * 16 + j], alpha), L);
+        if constexpr (MODE == kW1Amax) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) hmax = fmaxf(hmax, fabsf(h[j]));
+        } else {
+          uint32_t lo2, hi2;
+          const uint32_t sf = quant_block16(h, g2, lo2, hi2);
+          codes[half * 4 + blk * 2] = lo2;
+          codes[half * 4 + blk * 2 + 1] = hi2;
+          sfw |= sf << (8 * (half * 2 + blk));
+        }
+      }
+    }
+    if constexpr (MODE == kW1Amax) {
+      if (p < 0) hmax = 0.0f;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) hmax = fmaxf(hmax, __shfl_xor_sync(0xFFFFFFFFu, hmax, off));
+      if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(prm.amax), __float_as_uint(hmax));
+    } else {
+      if (p < 0) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) codes[q] = 0u;
+        sfw = 0u;
+      }
+      uint4* dst = reinterpret_cast<uint4*>(prm.out_codes + (size_t)r * (prm.I >> 1) + tl_.nt * 32);
+      dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+      dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+      *reinterpret_cast<uint32_t*>(prm.out_sf + sf_offset(r, tl_.nt * 4, prm.I >> 4)) = sfw;
+    }
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const Params prm) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
 
   if (*(volatile uint32_t*)prm.err & kAbortMask) return;  // an earlier timeout poisons the call
-
-  // ---- tile -> (expert, n-tile, m-tile): experts in order, then n-tiles, then the expert's m-tiles
   const int E = prm.E, NT = prm.NT;
   const int R = min(__ldg(prm.poff + E - 1), prm.cap);
-  const int tau = blockIdx.x;
-  if (tau >= (R / BM) * NT) return;
-  int lo = 0, hi = E - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if ((__ldg(prm.poff + mid) / BM) * NT > tau) hi = mid;
-    else lo = mid + 1;
-  }
-  const int e = lo;
-  const int mt_end = __ldg(prm.poff + e) / BM;
-  const int mt_start = e > 0 ? __ldg(prm.poff + e - 1) / BM : 0;
-  const int m_e = mt_end - mt_start;
-  const int local = tau - mt_start * NT;
-  const int nt = local / m_e;
-  const int mt = mt_start + local % m_e;
+  const int total = (R / BM) * NT;
+  if ((int)blockIdx.x >= total) return;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t bar_full = smem + BAR_OFF;         // STAGES x 8 bytes
-  const uint32_t bar_empty = bar_full + 8 * STAGES;  // STAGES x 8 bytes
-  const uint32_t bar_acc = bar_empty + 8 * STAGES;
-  const uint32_t bar_drain = bar_acc + 8;
+  const uint32_t bar_full = smem + BAR_OFF;           // STAGES x 8 bytes
+  const uint32_t bar_empty = bar_full + 8 * STAGES;    // STAGES x 8 bytes
+  const uint32_t bar_tfull = bar_empty + 8 * STAGES;   // 2 x 8 bytes
+  const uint32_t bar_tempty = bar_tfull + 16;          // 2 x 8 bytes
+  const uint32_t bar_drain = bar_tempty + 16;
 
   if (warp == 0) {
     tmem_alloc(smem_u32(&s_tmem), TMEM_COLS);
@@ -127,7 +217,10 @@ __global__ void __launch_bounds__(THREADS, 2)
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    mbar_init(bar_acc, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull + 8 * b, 1);
+      mbar_init(bar_tempty + 8 * b, 4);  // one arrive per epilogue warp
+    }
     mbar_init(bar_drain, 1);
     fence_mbar_init();
   }
@@ -136,144 +229,91 @@ __global__ void __launch_bounds__(THREADS, 2)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  const int K = prm.K;
-  const int KB = (K + 255) / 256;   // stages of 256 elements
-  const int katoms_total = K / 64;  // 64-element scale atoms along K
+  const int KB = prm.KB;
+  const int katoms_total = prm.K / 64;
 
   if (warp == 4 && lane == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t pol_w = policy_evict_first();  // weights stream through once
     const uint64_t pol_a = policy_evict_last();   // activations are re-read by every n-tile
-    const int a_row = mt * BM;
-    const int b_row = e * prm.b_rows + nt * BN;
-    const uint8_t* sfa = prm.a_sf + (size_t)mt * katoms_total * SF_TILE;
-    const uint8_t* sfb = prm.b_sf + ((size_t)e * (prm.b_rows / 128) + nt) * katoms_total * SF_TILE;
-    int issued = 0;
+    int it = 0;
     bool ok = true;
-    for (int kb = 0; kb < KB; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-      if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, prm.err)) {
-        ok = false;
-        break;
+    for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x) {
+      const Tile t = map_tile(tau, prm.poff, E, NT);
+      const int a_row = t.mt * BM;
+      const uint8_t* bsrc = prm.b_codes + (size_t)(t.e * NT + t.nt) * KB * B_BYTES;
+      const uint8_t* sfa = prm.a_sf + (size_t)t.mt * katoms_total * SF_TILE;
+      const uint8_t* sfb = prm.b_sf + ((size_t)t.e * NT + t.nt) * katoms_total * SF_TILE;
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+        if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, prm.err)) {
+          ok = false;
+          break;
+        }
+        const int atoms = min(4, katoms_total - kb * 4);
+        const uint32_t st = smem + s * STAGE_BYTES;
+        mbar_arrive_expect_tx(bar_full + 8 * s, A_BYTES + B_BYTES + 2 * atoms * SF_TILE);
+        bulk_load(st + A_BYTES, bsrc + (size_t)kb * B_BYTES, B_BYTES, bar_full + 8 * s, pol_w);
+        tma_load_2d(st, &tmA, bar_full + 8 * s, kb * KBYTES, a_row, pol_a);
+        bulk_load(st + SFA_OFF, sfa + (size_t)kb * 4 * SF_TILE, atoms * SF_TILE, bar_full + 8 * s, pol_a);
+        bulk_load(st + SFB_OFF, sfb + (size_t)kb * 4 * SF_TILE, atoms * SF_TILE, bar_full + 8 * s, pol_w);
       }
-      const int atoms = min(4, katoms_total - kb * 4);
-      const uint32_t st = smem + s * STAGE_BYTES;
-      mbar_arrive_expect_tx(bar_full + 8 * s, A_BYTES + B_BYTES + 2 * atoms * SF_TILE);
-      tma_load_2d(st, &tmA, bar_full + 8 * s, kb * KBYTES, a_row, pol_a);
-      tma_load_2d(st + A_BYTES, &tmB, bar_full + 8 * s, kb * KBYTES, b_row, pol_w);
-      bulk_load(st + SFA_OFF, sfa + (size_t)kb * 4 * SF_TILE, atoms * SF_TILE, bar_full + 8 * s, pol_a);
-      bulk_load(st + SFB_OFF, sfb + (size_t)kb * 4 * SF_TILE, atoms * SF_TILE, bar_full + 8 * s, pol_w);
-      issued = kb + 1;
     }
-    (void)ok;  // on every path, let the copies already issued land before the CTA exits
-    for (int kb = max(0, issued - STAGES); kb < issued; ++kb)
-      drain_wait(bar_full + 8 * (kb % STAGES), (uint32_t)(kb / STAGES) & 1u);
+    // on every path, let the copies already issued land before the CTA exits
+    for (int j = max(0, it - STAGES); j < it; ++j) drain_wait(bar_full + 8 * (j % STAGES), (uint32_t)(j / STAGES) & 1u);
   } else if (warp == 5 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc = idesc_nvf4(BM, BN);
-    bool ok = true, any = false;
-    for (int kb = 0; kb < KB; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-      if (!mbar_wait(bar_full + 8 * s, ph, prm.err)) {
+    int it = 0, tl = 0;
+    bool ok = true;
+    for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x, ++tl) {
+      const int b = tl & 1;
+      if (!mbar_wait(bar_tempty + 8 * b, ((uint32_t)(tl >> 1) & 1u) ^ 1u, prm.err)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int atoms = min(4, katoms_total - kb * 4);
-      const uint32_t st = smem + s * STAGE_BYTES;
-      const uint32_t sfa_t = tmem + SF_COL + 32 * s;
-      const uint32_t sfb_t = sfa_t + 16;
-      for (int a = 0; a < atoms; ++a) {
-        tc_cp_scales(sfa_t + 4 * a, desc_scales(st + SFA_OFF + a * SF_TILE));
-        tc_cp_scales(sfb_t + 4 * a, desc_scales(st + SFB_OFF + a * SF_TILE));
+      const uint32_t acc = tmem + b * ACC_COLS;
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+        if (!mbar_wait(bar_full + 8 * s, ph, prm.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int atoms = min(4, katoms_total - kb * 4);
+        const uint32_t st = smem + s * STAGE_BYTES;
+        const uint32_t sfa_t = tmem + SF_COL + 32 * s;
+        const uint32_t sfb_t = sfa_t + 16;
+        for (int a = 0; a < atoms; ++a) {
+          tc_cp_scales(sfa_t + 4 * a, desc_scales(st + SFA_OFF + a * SF_TILE));
+          tc_cp_scales(sfb_t + 4 * a, desc_scales(st + SFB_OFF + a * SF_TILE));
+        }
+        for (int a = 0; a < atoms; ++a)
+          tc_mma_nvf4(acc, desc_sw128(st + a * 32), desc_sw128(st + A_BYTES + a * 32), idesc, sfa_t + 4 * a,
+                      sfb_t + 4 * a, (kb > 0 || a > 0) ? 1u : 0u);
+        tc_commit(bar_empty + 8 * s);
       }
-      for (int a = 0; a < atoms; ++a) {
-        tc_mma_nvf4(tmem + ACC_COL, desc_sw128(st + a * 32), desc_sw128(st + A_BYTES + a * 32), idesc, sfa_t + 4 * a,
-                    sfb_t + 4 * a, (kb > 0 || a > 0) ? 1u : 0u);
-      }
-      any = true;
-      tc_commit(bar_empty + 8 * s);
+      if (ok) tc_commit(bar_tfull + 8 * b);
     }
-    if (ok) {
-      tc_commit(bar_acc);
-      drain_wait(bar_acc, 0);  // no MMA may still write TMEM when it is freed
-    } else if (any) {
-      tc_commit(bar_drain);
-      drain_wait(bar_drain, 0);
-    }
+    // no MMA may still write TMEM when it is freed
+    tc_commit(bar_drain);
+    drain_wait(bar_drain, 0);
   } else if (warp < 4) {
     // ------------------------------------------------------------ epilogue
-    const int r = mt * BM + warp * 32 + lane;
-    const int p = __ldg(prm.pair_of_row + r);
-    const float alpha = __ldg(prm.alpha + e);
-    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16) + ACC_COL;
-    // the whole warp takes one decision: tcgen05.ld is warp-collective
-    if (__all_sync(0xFFFFFFFFu, mbar_wait(bar_acc, 0, prm.err) ? 1 : 0)) {
+    int tl = 0;
+    for (int tau = blockIdx.x; tau < total; tau += gridDim.x, ++tl) {
+      const int b = tl & 1;
+      const Tile t = map_tile(tau, prm.poff, E, NT);
+      // the whole warp takes one decision: tcgen05.ld is warp-collective
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_tfull + 8 * b, (uint32_t)(tl >> 1) & 1u, prm.err) ? 1 : 0)) break;
       tc_fence_after();
-      if constexpr (MODE == kW2Rows) {
-        float* dst = prm.o_pairs + (size_t)(p < 0 ? 0 : p) * prm.H + nt * BN;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_ld32(tl + c * 32, v);
-          tmem_ld_wait();
-          if (p >= 0) {
-            float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              d4[q] = make_float4(__fmul_rn(v[4 * q], alpha), __fmul_rn(v[4 * q + 1], alpha),
-                                  __fmul_rn(v[4 * q + 2], alpha), __fmul_rn(v[4 * q + 3], alpha));
-          }
-        }
-      } else {
-        const float L = prm.limit;
-        const float g2 = (MODE == kW1SwiGLU) ? __ldg(prm.gs2) : 1.0f;
-        uint32_t codes[8];
-        uint32_t sfw = 0;
-        float hmax = 0.0f;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float g[32], u[32];
-          tmem_ld32(tl + half * 32, g);
-          tmem_ld32(tl + 64 + half * 32, u);
-          tmem_ld_wait();
-#pragma unroll
-          for (int blk = 0; blk < 2; ++blk) {
-            float h[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              h[j] = swiglu(__fmul_rn(g[blk * 16 + j], alpha), __fmul_rn(u[blk * 16 + j], alpha), L);
-            if constexpr (MODE == kW1Amax) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) hmax = fmaxf(hmax, fabsf(h[j]));
-            } else {
-              uint32_t lo2, hi2;
-              const uint32_t sf = quant_block16(h, g2, lo2, hi2);
-              codes[half * 4 + blk * 2] = lo2;
-              codes[half * 4 + blk * 2 + 1] = hi2;
-              sfw |= sf << (8 * (half * 2 + blk));
-            }
-          }
-        }
-        if constexpr (MODE == kW1Amax) {
-          if (p < 0) hmax = 0.0f;
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) hmax = fmaxf(hmax, __shfl_xor_sync(0xFFFFFFFFu, hmax, off));
-          if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(prm.amax), __float_as_uint(hmax));
-        } else {
-          if (p < 0) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) codes[q] = 0u;
-            sfw = 0u;
-          }
-          uint4* dst = reinterpret_cast<uint4*>(prm.out_codes + (size_t)r * (prm.I >> 1) + nt * 32);
-          dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-          dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-          *reinterpret_cast<uint32_t*>(prm.out_sf + sf_offset(r, nt * 4, prm.I >> 4)) = sfw;
-        }
-      }
+      epilogue_tile<MODE>(prm, t, tmem + b * ACC_COLS, warp, lane);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_tempty + 8 * b);
     }
   }
 
@@ -330,7 +370,21 @@ bool configure_once() {
   return ok == 1;
 }
 
+int sm_count() {
+  static int counts[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (counts[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
 }  // namespace
+
+size_t tiled_weight_bytes(int32_t rows, int32_t K) { return (size_t)rows * (size_t)((K + 255) / 256) * KBYTES; }
 
 fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, const uint8_t* a_codes,
                           const uint8_t* a_sf, const int32_t* poff, const int32_t* pair_of_row,
@@ -342,6 +396,7 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
   Params prm;
   prm.E = cfg.num_experts;
   prm.K = w2 ? cfg.inter : cfg.hidden;
+  prm.KB = (prm.K + 255) / 256;
   prm.b_rows = w2 ? cfg.hidden : 2 * cfg.inter;
   prm.NT = prm.b_rows / BN;
   prm.k = cfg.top_k;
@@ -351,6 +406,7 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
   prm.limit = cfg.swiglu_limit;
   prm.poff = poff;
   prm.pair_of_row = pair_of_row;
+  prm.b_codes = b_codes;
   prm.a_sf = a_sf;
   prm.b_sf = b_sf;
   prm.alpha = alpha;
@@ -360,23 +416,24 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
   prm.amax = amax;
   prm.o_pairs = o_pairs;
   prm.err = err;
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA;
   if (!encode_u8_sw128(&tmA, a_codes, (uint64_t)prm.K / 2, (uint64_t)prm.cap, BM)) return FP4MOE_CUDA_ERROR;
-  if (!encode_u8_sw128(&tmB, b_codes, (uint64_t)prm.K / 2, (uint64_t)prm.E * prm.b_rows, BN))
-    return FP4MOE_CUDA_ERROR;
-  const unsigned grid = (unsigned)((prm.cap / BM) * prm.NT);
+  const int nsm = sm_count();
+  if (nsm <= 0) return FP4MOE_CUDA_ERROR;
+  const int max_tiles = (prm.cap / BM) * prm.NT;
+  const unsigned grid = (unsigned)(max_tiles < nsm ? max_tiles : nsm);
   switch (mode) {
     case kW1SwiGLU:
       if (!configure_once<kW1SwiGLU>()) return FP4MOE_CUDA_ERROR;
-      grouped_gemm_kernel<kW1SwiGLU><<<grid, THREADS, SMEM_BYTES, st>>>(tmA, tmB, prm);
+      grouped_gemm_kernel<kW1SwiGLU><<<grid, THREADS, SMEM_BYTES, st>>>(tmA, prm);
       break;
     case kW1Amax:
       if (!configure_once<kW1Amax>()) return FP4MOE_CUDA_ERROR;
-      grouped_gemm_kernel<kW1Amax><<<grid, THREADS, SMEM_BYTES, st>>>(tmA, tmB, prm);
+      grouped_gemm_kernel<kW1Amax><<<grid, THREADS, SMEM_BYTES, st>>>(tmA, prm);
       break;
     case kW2Rows:
       if (!configure_once<kW2Rows>()) return FP4MOE_CUDA_ERROR;
-      grouped_gemm_kernel<kW2Rows><<<grid, THREADS, SMEM_BYTES, st>>>(tmA, tmB, prm);
+      grouped_gemm_kernel<kW2Rows><<<grid, THREADS, SMEM_BYTES, st>>>(tmA, prm);
       break;
   }
   return cudaGetLastError() == cudaSuccess ? FP4MOE_OK : FP4MOE_CUDA_ERROR;

@@ -27,10 +27,14 @@ fp4moe_status quant_scatter_launch(const fp4moe_config& cfg, int32_t T, const ui
                                    cudaStream_t st);
 
 // rows [n_rows_total][K] fp32 -> NVFP4; g indexed by row / g_div; optional W1 gate/up row permutation
-// (rows_per_group = rows of one expert, inter = I, or 0 for no permutation).
+// (rows_per_group = rows of one expert, inter = I, or 0 for no permutation); tiled != 0 writes the codes in
+// the pre-tiled weight layout (16 KB blocks of 128 rows x 128 bytes, 128-byte swizzled).
 fp4moe_status quant_rows_launch(int64_t n_rows_total, int32_t K, int32_t rows_per_group, int32_t inter,
-                                const float* in, const float* g, int32_t g_div, uint8_t* codes, uint8_t* sf,
-                                cudaStream_t st);
+                                int32_t tiled, const float* in, const float* g, int32_t g_div, uint8_t* codes,
+                                uint8_t* sf, cudaStream_t st);
+
+// bytes of one matrix of `rows` x K in the pre-tiled weight layout (K padded up to a multiple of 256)
+size_t tiled_weight_bytes(int32_t rows, int32_t K);
 
 fp4moe_status amax_f32_launch(int32_t n_groups, int64_t per_group, const float* in, float* amax, cudaStream_t st);
 fp4moe_status amax_bf16_launch(int64_t n, const uint16_t* in, float* amax, cudaStream_t st);

@@ -51,14 +51,24 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(int H, int E, int k,
   }
 }
 
+// Byte offset of code byte `kbyte` of kernel row o in the pre-tiled weight
+// layout. Blocks of 128 rows x 128 bytes (16 KB) are ordered
+// [group][row tile][k stage]. Inside a block, row i's 16-byte chunk j sits at
+// i*128 + (j ^ (i % 8))*16: the 128-byte swizzle that the tensor cores read.
+__device__ __forceinline__ size_t tiled_offset(int64_t grp, int o, int kbyte, int n_row_tiles, int k_stages) {
+  return ((size_t)(grp * n_row_tiles + (o >> 7)) * k_stages + (kbyte >> 7)) * 16384u + (size_t)(o & 127) * 128u +
+         ((((kbyte & 127) >> 4) ^ (o & 7)) << 4) + (kbyte & 15);
+}
+
 // Generic fp32 row quantiser. Row gr belongs to group gr / rows_per_group,
 // and its output row inside the group is either the same row or, when
 // inter > 0, the W1 kernel order: gate feature f -> 128*(f/64) + f%64,
-// up feature f -> 128*(f/64) + 64 + f%64.
+// up feature f -> 128*(f/64) + 64 + f%64. With tiled != 0, the codes go to the
+// pre-tiled weight layout instead of row-major [row][K/2].
 __global__ void __launch_bounds__(256) quant_rows_kernel(int64_t n_rows, int K, int rows_per_group, int inter,
-                                                         const float* __restrict__ in, const float* __restrict__ g,
-                                                         int g_div, uint8_t* __restrict__ codes,
-                                                         uint8_t* __restrict__ sf) {
+                                                         int tiled, const float* __restrict__ in,
+                                                         const float* __restrict__ g, int g_div,
+                                                         uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t gr = (int64_t)blockIdx.x * 8 + warp;
   if (gr >= n_rows) return;
@@ -74,13 +84,15 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(int64_t n_rows, int K, 
   const float4* src = reinterpret_cast<const float4*>(in + gr * K);
   uint8_t* dst = codes + (grp * rows_per_group + i) * (int64_t)(K >> 1);
   uint8_t* sdst = sf + grp * (int64_t)rows_per_group * C;
+  const int n_row_tiles = rows_per_group >> 7, k_stages = (K + 255) >> 8;
   for (int b = lane; b < C; b += 32) {
     const float4 a = __ldg(src + 4 * b), c = __ldg(src + 4 * b + 1), d = __ldg(src + 4 * b + 2),
                  e = __ldg(src + 4 * b + 3);
     const float v[16] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w, e.x, e.y, e.z, e.w};
     uint32_t lo, hi;
     const uint32_t s = quant_block16(v, gg, lo, hi);
-    *reinterpret_cast<uint2*>(dst + b * 8) = make_uint2(lo, hi);
+    uint8_t* cd = tiled ? codes + tiled_offset(grp, i, b * 8, n_row_tiles, k_stages) : dst + b * 8;
+    *reinterpret_cast<uint2*>(cd) = make_uint2(lo, hi);
     sdst[sf_offset(i, b, C)] = (uint8_t)s;
   }
 }
@@ -138,12 +150,12 @@ fp4moe_status quant_scatter_launch(const fp4moe_config& cfg, int32_t T, const ui
 }
 
 fp4moe_status quant_rows_launch(int64_t n_rows_total, int32_t K, int32_t rows_per_group, int32_t inter,
-                                const float* in, const float* g, int32_t g_div, uint8_t* codes, uint8_t* sf,
-                                cudaStream_t st) {
+                                int32_t tiled, const float* in, const float* g, int32_t g_div, uint8_t* codes,
+                                uint8_t* sf, cudaStream_t st) {
   if (n_rows_total == 0) return FP4MOE_OK;
   const int64_t blocks = (n_rows_total + 7) / 8;
-  quant_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>(n_rows_total, K, rows_per_group, inter, in, g, g_div, codes,
-                                                      sf);
+  quant_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>(n_rows_total, K, rows_per_group, inter, tiled, in, g, g_div,
+                                                      codes, sf);
   return last_status();
 }
 

@@ -62,12 +62,22 @@
  * in a warmup pass).
  *
  * Expert weights (written by fp4moe_quantize_weights, K-major):
- *  - W1: [E][2I][H/2] codes and [E][2I/128][H/64][512] scales. Rows are in
- *    KERNEL order: for each 64-feature group f = 0 .. I/64-1, rows
- *    [128f, 128f+64) are gate features [64f, 64f+64) and rows
- *    [128f+64, 128f+128) are up features [64f, 64f+64). Logical W13 has the
- *    gate in rows [0, I) and up in rows [I, 2I).
- *  - W2: [E][H][I/2] codes and [E][H/128][I/64][512] scales.
+ *  - Codes are PRE-TILED so that the GEMM streams each stage as one
+ *    contiguous 16 KB read. A matrix of R rows (R % 128 == 0) by K elements
+ *    is stored as 16384-byte blocks ordered [expert][row tile r/128][k stage
+ *    (K index)/256]. Inside a block, row i (0..127) has 128 bytes (256 codes,
+ *    element 2c in the low nibble of byte c). Its 16-byte chunk j (bytes
+ *    16j .. 16j+15 of that K slice) is stored at offset i*128 + (j ^ (i%8))*16:
+ *    the 128-byte swizzle that the tensor cores read from shared memory.
+ *    K is zero-padded to a multiple of 256.
+ *  - Scales: E4M3, one per 16 elements, in the 128x4 tile layout per expert
+ *    (C = K/16 columns): [E][R/128][K/64][512] bytes.
+ *  - W1: R = 2I rows, K = H. Rows are in KERNEL order: for each 64-feature
+ *    group f = 0 .. I/64-1, rows [128f, 128f+64) are gate features
+ *    [64f, 64f+64) and rows [128f+64, 128f+128) are up features
+ *    [64f, 64f+64). Logical W13 has the gate in rows [0, I) and up in rows
+ *    [I, 2I).
+ *  - W2: R = H rows, K = I.
  *  - One fp32 quant-direction global scale per expert per matrix.
  *  - alpha1[e] = 1 / (gs1 * gw1[e]) and alpha2[e] = 1 / (gs2 * gw2[e]),
  *    written by fp4moe_make_alpha.

@@ -75,6 +75,37 @@ def float_parity(got: np.ndarray, ref: np.ndarray, rel_l2: float = 1e-2, max_abs
     return rel, mx / rms if rms > 0 else 0.0
 
 
+def tile_weights(packed: np.ndarray, rows_per_expert: int) -> np.ndarray:
+    """Row-major packed codes [E*R][K/2] -> the pre-tiled weight layout of include/fp4moe.h.
+
+    16 KB blocks [expert][row tile][k stage]; row i of a block holds 128 bytes
+    whose 16-byte chunk j sits at i*128 + (j ^ (i % 8))*16; K is zero-padded to 256.
+    """
+    n_rows, kbytes = packed.shape
+    E = n_rows // rows_per_expert
+    kst = (kbytes + 127) // 128
+    padded = np.zeros((n_rows, kst * 128), dtype=np.uint8)
+    padded[:, :kbytes] = packed
+    # [E, row_tiles, 128 rows, k_stages, 8 chunks, 16 bytes]
+    t = padded.reshape(E, rows_per_expert // 128, 128, kst, 8, 16)
+    i = np.arange(128)[:, None]
+    j = np.arange(8)[None, :]
+    out = np.zeros_like(t)
+    out[:, :, i, :, j ^ (i % 8), :] = t[:, :, i, :, j, :]
+    return out.transpose(0, 1, 3, 2, 4, 5).reshape(-1)
+
+
+def untile_weights(flat: np.ndarray, n_rows: int, kbytes: int, rows_per_expert: int) -> np.ndarray:
+    E = n_rows // rows_per_expert
+    kst = (kbytes + 127) // 128
+    t = flat.reshape(E, rows_per_expert // 128, kst, 128, 8, 16).transpose(0, 1, 3, 2, 4, 5)
+    i = np.arange(128)[:, None]
+    j = np.arange(8)[None, :]
+    out = np.zeros_like(t)
+    out[:, :, i, :, j, :] = t[:, :, i, :, j ^ (i % 8), :]
+    return out.reshape(n_rows, kst * 128)[:, :kbytes]
+
+
 def dump(name: str, **arrays):
     """Save arrays for offline diagnosis when FP4MOE_DUMP_DIR is set."""
     d = os.environ.get("FP4MOE_DUMP_DIR")

@@ -12,7 +12,7 @@ m-tiles, and K is partial (a stage of 2 atoms) or runs over several stages.
 import numpy as np
 import pytest
 
-from helpers import dump, ensure_built
+from helpers import dump, ensure_built, tile_weights
 from oracle import codecs, layout, moe, nvfp4
 
 pytestmark = pytest.mark.gpu
@@ -67,7 +67,7 @@ def _setup(H, I, counts, seed, which):
     t = dict(
         a=torch.from_numpy(nvfp4.pack_codes(qa).reshape(-1)).cuda(),
         asf=torch.from_numpy(nvfp4.swizzle(sa)).cuda(),
-        w=torch.from_numpy(nvfp4.pack_codes(qw).reshape(-1)).cuda(),
+        w=torch.from_numpy(tile_weights(nvfp4.pack_codes(qw), N)).cuda(),
         wsf=torch.from_numpy(np.concatenate([nvfp4.swizzle(sw[e * N:(e + 1) * N]) for e in range(E)])).cuda(),
         poff=torch.from_numpy(L["padded_offsets"].astype(np.int32)).cuda(),
         por=torch.from_numpy(por.astype(np.int32)).cuda(),
