@@ -8,31 +8,36 @@
 // searchsorted(padded_offsets, row, right=True) on offsets with no leading 0
 // ("Bug 2", "Bug 4").
 //
-// Persistent kernel: one CTA per SM walks output tiles
-// tau = blockIdx.x, blockIdx.x + gridDim.x, ... Each tile is 128 activation
-// rows x 128 weight rows. Tiles are ordered expert, then n-tile, then the
-// expert's m-tiles, so CTAs that run at the same time share an expert's
-// activation tile in L2.
+// Persistent kernel, one CTA per SM. Output tiles are 128 activation rows x
+// 128 weight rows, numbered in (m-tile, n-tile) order. CTA c takes the
+// contiguous share [c*T/G, (c+1)*T/G) of the T tiles, so it walks consecutive
+// n-tiles of the same m-tile (expert block):
 //   warp 4      producer. Each stage moves one 16 KB weight block with a
 //               single contiguous cp.async.bulk: the weights are stored
 //               pre-tiled and pre-swizzled (see fp4moe.h). The 128-row
 //               activation tile arrives by cp.async.bulk.tensor with the
-//               128-byte swizzle, and the A and B scale tiles (2 KB each) by
-//               cp.async.bulk. The STAGES-deep shared-memory ring runs on
-//               across tile boundaries, so the weight stream never stops.
-//   warp 5      MMA issuer. tcgen05.cp moves the scale tiles into per-stage
-//               TMEM columns. tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
-//               (K = 64 each) accumulates in fp32 into one of two TMEM
-//               accumulator buffers. tcgen05.commit frees the ring slot and
-//               then hands the buffer to the epilogue.
-//   warps 0-3   epilogue. tcgen05.ld gives one accumulator row per thread.
-//               The epilogue of tile i overlaps the MMAs of tile i+1.
+//               128-byte swizzle, and the 2 KB scale tiles by cp.async.bulk.
+//               The STAGES-deep shared-memory ring runs on across tile
+//               boundaries, so the weight stream never stops.
+//   warp 5      MMA issuer. tcgen05.cp costs about the same per instruction
+//               whatever its size, and it sits on this thread's critical path.
+//               So the activation (A) scales of an m-tile are copied into
+//               TMEM only once, for the whole of K, and stay resident while
+//               the CTA walks that m-tile's n-tiles. Each stage then copies
+//               only its 4 weight (B) scale tiles. Then
+//               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (K = 64
+//               each) accumulates in fp32 in TMEM, and tcgen05.commit frees the
+//               ring slot and then hands the accumulator to the epilogue.
+//   warps 0-3   epilogue. tcgen05.ld gives one accumulator row per thread. It
+//               moves all 128 columns to registers, frees the accumulator for
+//               the next tile's MMAs, then computes. Padding rows are skipped
+//               ("Bug 14"), and warps whose 32 rows are all padding do not read
+//               TMEM at all.
 //     W1: alpha, then the clamped SwiGLU (gate columns 0-63, up columns
 //         64-127, from the W1 kernel row order), then NVFP4 requantisation
 //         into the L2 slot buffers ("Bug 6", "Bug 7").
 //     W1 amax: the same SwiGLU, reduced to amax|h| for calibration.
-//     W2: alpha, then fp32 rows stored per (token, k) pair. Padding rows are
-//         dropped ("Bug 14").
+//     W2: alpha, then fp32 rows stored per (token, k) pair.
 // Every spin-wait is bounded (mbar_wait). A timeout sets FP4MOE_ERR_TIMEOUT
 // in the error word. Each role then stops, waits for its in-flight copies and
 // MMAs, and the CTA frees its TMEM and returns.
@@ -58,11 +63,12 @@ constexpr int BAR_OFF = STAGES * STAGE_BYTES;
 constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;    // barriers + 1024-byte alignment slack
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t ACC_COLS = 128;  // accumulator buffer b: columns [128 b, 128 b + 128)
-constexpr uint32_t SF_COL = 2 * ACC_COLS;  // stage s: 32 columns, [0,16) A scales, [16,32) B scales
+constexpr uint32_t ACC_COL = 0;    // the accumulator: columns [0, 128)
+constexpr uint32_t SFA_COL = 128;  // resident A scales: 4 columns per 64-element K atom, for all of K
+// B scales of ring stage s: 16 columns at SFA_COL + K/16 + 16 s
 static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
-static_assert(SF_COL + STAGES * 32 <= TMEM_COLS, "TMEM budget");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+constexpr int kMaxResidentK = (TMEM_COLS - SFA_COL - 16 * STAGES) * 16;  // 4608
 
 struct Params {
   int E, K, KB, b_rows, NT, k, cap, I, H;
@@ -85,19 +91,18 @@ struct Tile {
   int e, nt, mt;
 };
 
-// tau -> (expert, n-tile, m-tile): experts in order; inside an expert, n-tiles, then its m-tiles.
+// Tile tau in (m-tile, n-tile) order; the m-tile's expert is
+// searchsorted(padded_offsets, first row, right=True).
 __device__ __forceinline__ Tile map_tile(int tau, const int32_t* __restrict__ poff, int E, int NT) {
+  const int mt = tau / NT;
+  const int row = mt * BM;
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
-    if ((__ldg(poff + mid) / BM) * NT > tau) hi = mid;
+    if (__ldg(poff + mid) > row) hi = mid;
     else lo = mid + 1;
   }
-  const int mt_end = __ldg(poff + lo) / BM;
-  const int mt_start = lo > 0 ? __ldg(poff + lo - 1) / BM : 0;
-  const int m_e = mt_end - mt_start;
-  const int local = tau - mt_start * NT;
-  return Tile{lo, local / m_e, mt_start + local % m_e};
+  return Tile{lo, tau - mt * NT, mt};
 }
 
 // Bounded wait that ignores other CTAs' aborts: used only while draining.
@@ -112,80 +117,19 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// silu(min(g, L)) * clamp(u, -L, L). The exponential and the division use the
+// fast hardware approximations (a few ulp): h only feeds the requantiser
+// and the tolerance-checked output. The quantiser itself stays IEEE-exact.
 __device__ __forceinline__ float swiglu(float g, float u, float L) {
-  const float gc = fminf(g, L);
+  const float gc = fmaxf(fminf(g, L), -80.0f);  // silu(-80) is ~1e-33: the floor only keeps exp finite
   const float uc = fminf(fmaxf(u, -L), L);
-  return __fmul_rn(__fdiv_rn(gc, __fadd_rn(1.0f, expf(-gc))), uc);
+  return __fdividef(gc, 1.0f + __expf(-gc)) * uc;
 }
 
-template <int MODE>
-__device__ __forceinline__ void epilogue_tile(const Params& prm, const Tile& tl_, uint32_t tacc, int warp, int lane) {
-  const int r = tl_.mt * BM + warp * 32 + lane;
-  const int p = __ldg(prm.pair_of_row + r);
-  const float alpha = __ldg(prm.alpha + tl_.e);
-  const uint32_t tl = tacc + ((uint32_t)(warp * 32) << 16);
-  if constexpr (MODE == kW2Rows) {
-    float* dst = prm.o_pairs + (size_t)(p < 0 ? 0 : p) * prm.H + tl_.nt * BN;
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      float v[32];
-      tmem_ld32(tl + c * 32, v);
-      tmem_ld_wait();
-      if (p >= 0) {
-        float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          d4[q] = make_float4(__fmul_rn(v[4 * q], alpha), __fmul_rn(v[4 * q + 1], alpha),
-                              __fmul_rn(v[4 * q + 2], alpha), __fmul_rn(v[4 * q + 3], alpha));
-      }
-    }
-  } else {
-    const float L = prm.limit;
-    const float g2 = (MODE == kW1SwiGLU) ? __ldg(prm.gs2) : 1.0f;
-    uint32_t codes[8];
-    uint32_t sfw = 0;
-    float hmax = 0.0f;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float g[32], u[32];
-      tmem_ld32(tl + half * 32, g);
-      tmem_ld32(tl + 64 + half * 32, u);
-      tmem_ld_wait();
-#pragma unroll
-      for (int blk = 0; blk < 2; ++blk) {
-        float h[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          h[j] = swiglu(__fmul_rn(g[blk * 16 + j], alpha), __fmul_rn(u[blk * 16 + j], alpha), L);
-        if constexpr (MODE == kW1Amax) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) hmax = fmaxf(hmax, fabsf(h[j]));
-        } else {
-          uint32_t lo2, hi2;
-          const uint32_t sf = quant_block16(h, g2, lo2, hi2);
-          codes[half * 4 + blk * 2] = lo2;
-          codes[half * 4 + blk * 2 + 1] = hi2;
-          sfw |= sf << (8 * (half * 2 + blk));
-        }
-      }
-    }
-    if constexpr (MODE == kW1Amax) {
-      if (p < 0) hmax = 0.0f;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) hmax = fmaxf(hmax, __shfl_xor_sync(0xFFFFFFFFu, hmax, off));
-      if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(prm.amax), __float_as_uint(hmax));
-    } else {
-      if (p < 0) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) codes[q] = 0u;
-        sfw = 0u;
-      }
-      uint4* dst = reinterpret_cast<uint4*>(prm.out_codes + (size_t)r * (prm.I >> 1) + tl_.nt * 32);
-      dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-      dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-      *reinterpret_cast<uint32_t*>(prm.out_sf + sf_offset(r, tl_.nt * 4, prm.I >> 4)) = sfw;
-    }
-  }
+// Contiguous share [tau0, tau1) of `total` tiles for CTA c of G.
+__device__ __forceinline__ void cta_range(int total, int& tau0, int& tau1) {
+  tau0 = (int)(((long long)total * blockIdx.x) / gridDim.x);
+  tau1 = (int)(((long long)total * (blockIdx.x + 1)) / gridDim.x);
 }
 
 template <int MODE>
@@ -197,16 +141,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (*(volatile uint32_t*)prm.err & kAbortMask) return;  // an earlier timeout poisons the call
   const int E = prm.E, NT = prm.NT;
   const int R = min(__ldg(prm.poff + E - 1), prm.cap);
-  const int total = (R / BM) * NT;
-  if ((int)blockIdx.x >= total) return;
+  int tau0, tau1;
+  cta_range((R / BM) * NT, tau0, tau1);
+  if (tau0 >= tau1) return;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t bar_full = smem + BAR_OFF;           // STAGES x 8 bytes
-  const uint32_t bar_empty = bar_full + 8 * STAGES;    // STAGES x 8 bytes
-  const uint32_t bar_tfull = bar_empty + 8 * STAGES;   // 2 x 8 bytes
-  const uint32_t bar_tempty = bar_tfull + 16;          // 2 x 8 bytes
-  const uint32_t bar_drain = bar_tempty + 16;
+  const uint32_t bar_full = smem + BAR_OFF;          // STAGES x 8 bytes
+  const uint32_t bar_empty = bar_full + 8 * STAGES;   // STAGES x 8 bytes
+  const uint32_t bar_tfull = bar_empty + 8 * STAGES;
+  const uint32_t bar_tempty = bar_tfull + 8;
+  const uint32_t bar_drain = bar_tempty + 8;
 
   if (warp == 0) {
     tmem_alloc(smem_u32(&s_tmem), TMEM_COLS);
@@ -217,10 +162,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar_tfull + 8 * b, 1);
-      mbar_init(bar_tempty + 8 * b, 4);  // one arrive per epilogue warp
-    }
+    mbar_init(bar_tfull, 1);
+    mbar_init(bar_tempty, 4);  // one arrive per epilogue warp
     mbar_init(bar_drain, 1);
     fence_mbar_init();
   }
@@ -231,15 +174,18 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int KB = prm.KB;
   const int katoms_total = prm.K / 64;
+  const uint32_t sfb_col = SFA_COL + 4u * katoms_total;
 
   if (warp == 4 && lane == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t pol_w = policy_evict_first();  // weights stream through once
     const uint64_t pol_a = policy_evict_last();   // activations are re-read by every n-tile
-    int it = 0;
+    int it = 0, prev_mt = -1;
     bool ok = true;
-    for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x) {
+    for (int tau = tau0; tau < tau1 && ok; ++tau) {
       const Tile t = map_tile(tau, prm.poff, E, NT);
+      const bool new_a = (t.mt != prev_mt);  // A scales go to TMEM once per m-tile
+      prev_mt = t.mt;
       const int a_row = t.mt * BM;
       const uint8_t* bsrc = prm.b_codes + (size_t)(t.e * NT + t.nt) * KB * B_BYTES;
       const uint8_t* sfa = prm.a_sf + (size_t)t.mt * katoms_total * SF_TILE;
@@ -253,10 +199,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         const int atoms = min(4, katoms_total - kb * 4);
         const uint32_t st = smem + s * STAGE_BYTES;
-        mbar_arrive_expect_tx(bar_full + 8 * s, A_BYTES + B_BYTES + 2 * atoms * SF_TILE);
+        mbar_arrive_expect_tx(bar_full + 8 * s, A_BYTES + B_BYTES + (new_a ? 2 : 1) * atoms * SF_TILE);
         bulk_load(st + A_BYTES, bsrc + (size_t)kb * B_BYTES, B_BYTES, bar_full + 8 * s, pol_w);
         tma_load_2d(st, &tmA, bar_full + 8 * s, kb * KBYTES, a_row, pol_a);
-        bulk_load(st + SFA_OFF, sfa + (size_t)kb * 4 * SF_TILE, atoms * SF_TILE, bar_full + 8 * s, pol_a);
+        if (new_a) bulk_load(st + SFA_OFF, sfa + (size_t)kb * 4 * SF_TILE, atoms * SF_TILE, bar_full + 8 * s, pol_a);
         bulk_load(st + SFB_OFF, sfb + (size_t)kb * 4 * SF_TILE, atoms * SF_TILE, bar_full + 8 * s, pol_w);
       }
     }
@@ -265,16 +211,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 5 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc = idesc_nvf4(BM, BN);
-    int it = 0, tl = 0;
+    int it = 0, tl = 0, prev_mt = -1;
     bool ok = true;
-    for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x, ++tl) {
-      const int b = tl & 1;
-      if (!mbar_wait(bar_tempty + 8 * b, ((uint32_t)(tl >> 1) & 1u) ^ 1u, prm.err)) {
+    for (int tau = tau0; tau < tau1 && ok; ++tau, ++tl) {
+      const Tile t = map_tile(tau, prm.poff, E, NT);
+      const bool new_a = (t.mt != prev_mt);
+      prev_mt = t.mt;
+      // the epilogue has drained the accumulator, so every earlier MMA is complete:
+      // the resident A scales may now be overwritten
+      if (!mbar_wait(bar_tempty, ((uint32_t)tl & 1u) ^ 1u, prm.err)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t acc = tmem + b * ACC_COLS;
       for (int kb = 0; kb < KB; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
@@ -285,18 +234,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const int atoms = min(4, katoms_total - kb * 4);
         const uint32_t st = smem + s * STAGE_BYTES;
-        const uint32_t sfa_t = tmem + SF_COL + 32 * s;
-        const uint32_t sfb_t = sfa_t + 16;
-        for (int a = 0; a < atoms; ++a) {
-          tc_cp_scales(sfa_t + 4 * a, desc_scales(st + SFA_OFF + a * SF_TILE));
-          tc_cp_scales(sfb_t + 4 * a, desc_scales(st + SFB_OFF + a * SF_TILE));
-        }
+        const uint32_t sfa_t = tmem + SFA_COL + 16u * kb;
+        const uint32_t sfb_t = tmem + sfb_col + 16u * s;
+        if (new_a)
+          for (int a = 0; a < atoms; ++a) tc_cp_scales(sfa_t + 4 * a, desc_scales(st + SFA_OFF + a * SF_TILE));
+        for (int a = 0; a < atoms; ++a) tc_cp_scales(sfb_t + 4 * a, desc_scales(st + SFB_OFF + a * SF_TILE));
         for (int a = 0; a < atoms; ++a)
-          tc_mma_nvf4(acc, desc_sw128(st + a * 32), desc_sw128(st + A_BYTES + a * 32), idesc, sfa_t + 4 * a,
-                      sfb_t + 4 * a, (kb > 0 || a > 0) ? 1u : 0u);
+          tc_mma_nvf4(tmem + ACC_COL, desc_sw128(st + a * 32), desc_sw128(st + A_BYTES + a * 32), idesc,
+                      sfa_t + 4 * a, sfb_t + 4 * a, (kb > 0 || a > 0) ? 1u : 0u);
         tc_commit(bar_empty + 8 * s);
       }
-      if (ok) tc_commit(bar_tfull + 8 * b);
+      if (ok) tc_commit(bar_tfull);
     }
     // no MMA may still write TMEM when it is freed
     tc_commit(bar_drain);
@@ -304,16 +252,65 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp < 4) {
     // ------------------------------------------------------------ epilogue
     int tl = 0;
-    for (int tau = blockIdx.x; tau < total; tau += gridDim.x, ++tl) {
-      const int b = tl & 1;
+    for (int tau = tau0; tau < tau1; ++tau, ++tl) {
       const Tile t = map_tile(tau, prm.poff, E, NT);
+      const int r = t.mt * BM + warp * 32 + lane;
+      const int p = __ldg(prm.pair_of_row + r);
+      const bool any_real = __any_sync(0xFFFFFFFFu, p >= 0);
       // the whole warp takes one decision: tcgen05.ld is warp-collective
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_tfull + 8 * b, (uint32_t)(tl >> 1) & 1u, prm.err) ? 1 : 0)) break;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_tfull, (uint32_t)tl & 1u, prm.err) ? 1 : 0)) break;
       tc_fence_after();
-      epilogue_tile<MODE>(prm, t, tmem + b * ACC_COLS, warp, lane);
+      const uint32_t tacc = tmem + ACC_COL + ((uint32_t)(warp * 32) << 16);
+      float v[128];
+      if (any_real) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float q[32];
+          tmem_ld32(tacc + c * 32, q);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[c * 32 + j] = q[j];
+        }
+        tmem_ld_wait();
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_tempty + 8 * b);
+      if (lane == 0) mbar_arrive(bar_tempty);  // the accumulator is free for the next tile
+      if (p < 0) continue;                     // padding rows carry nothing ("Bug 14")
+      const float alpha = __ldg(prm.alpha + t.e);
+      if constexpr (MODE == kW2Rows) {
+        float4* d4 = reinterpret_cast<float4*>(prm.o_pairs + (size_t)p * prm.H + t.nt * BN);
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          d4[q] = make_float4(__fmul_rn(v[4 * q], alpha), __fmul_rn(v[4 * q + 1], alpha),
+                              __fmul_rn(v[4 * q + 2], alpha), __fmul_rn(v[4 * q + 3], alpha));
+      } else {
+        // columns [0, 64): gate of features 64 nt .. 64 nt + 63; columns [64, 128): up of the same features
+        const float L = prm.limit;
+        if constexpr (MODE == kW1Amax) {
+          float hmax = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            hmax = fmaxf(hmax, fabsf(swiglu(__fmul_rn(v[j], alpha), __fmul_rn(v[64 + j], alpha), L)));
+          atomicMax(reinterpret_cast<unsigned int*>(prm.amax), __float_as_uint(hmax));
+        } else {
+          const float g2 = __ldg(prm.gs2);
+          uint32_t codes[8];
+          uint32_t sfw = 0;
+#pragma unroll
+          for (int blk = 0; blk < 4; ++blk) {
+            float h[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              h[j] = swiglu(__fmul_rn(v[blk * 16 + j], alpha), __fmul_rn(v[64 + blk * 16 + j], alpha), L);
+            const uint32_t sf = quant_block16(h, g2, codes[2 * blk], codes[2 * blk + 1]);
+            sfw |= sf << (8 * blk);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(prm.out_codes + (size_t)r * (prm.I >> 1) + t.nt * 32);
+          dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+          dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+          *reinterpret_cast<uint32_t*>(prm.out_sf + sf_offset(r, t.nt * 4, prm.I >> 4)) = sfw;
+        }
+      }
     }
   }
 
@@ -393,6 +390,7 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
                           cudaStream_t st) {
   if (T == 0) return FP4MOE_OK;
   const bool w2 = (mode == kW2Rows);
+  if ((w2 ? cfg.inter : cfg.hidden) > kMaxResidentK) return FP4MOE_UNSUPPORTED;
   Params prm;
   prm.E = cfg.num_experts;
   prm.K = w2 ? cfg.inter : cfg.hidden;

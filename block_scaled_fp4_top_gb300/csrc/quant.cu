@@ -28,15 +28,9 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(int H, int E, int k,
   const int R = min(__ldg(poff + E - 1), cap);
   if (r >= R) return;
   const int p = __ldg(pair_of_row + r);
+  if (p < 0) return;  // padding rows carry nothing and are never read back ("Bug 14")
   const int C = H >> 4;
   uint8_t* dst = a1 + (size_t)r * (H >> 1);
-  if (p < 0) {  // padding row: zero codes and zero scales
-    for (int b = lane; b < C; b += 32) {
-      *reinterpret_cast<uint2*>(dst + b * 8) = make_uint2(0u, 0u);
-      a1_sf[sf_offset(r, b, C)] = 0;
-    }
-    return;
-  }
   const float g = __ldg(gs1);
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(p / k) * H);
   for (int b = lane; b < C; b += 32) {

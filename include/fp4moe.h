@@ -53,7 +53,9 @@
  *    scales (one per 16 elements) in the 128x4 "32_4_4" tile layout
  *    ("Bug 1", "Bug 11"), with C = K/16 scale columns:
  *      byte(r, c) = ((r/128)*(C/4) + c/4)*512 + (r%32)*16 + ((r%128)/32)*4 + c%4
- *    Padding rows hold zero codes and zero scales.
+ *    Padding rows are never written: their contents are unspecified. The
+ *    GEMMs compute them like any other row (the rows of an MMA are
+ *    independent) and then drop them, so no real row depends on them.
  *
  * NVFP4 value of code q under block scale sf and global scale g:
  *   decode_e2m1(q) * decode_e4m3(sf) / g.
@@ -82,7 +84,9 @@
  *  - alpha1[e] = 1 / (gs1 * gw1[e]) and alpha2[e] = 1 / (gs2 * gw2[e]),
  *    written by fp4moe_make_alpha.
  *
- * Supported shapes: H % 256 == 0, I % 128 == 0, 1 <= k <= 16, k <= E <= 1024,
+ * Supported shapes: H % 256 == 0, I % 128 == 0, H <= 4608, I <= 4608 (the
+ * activation scales of a 128-row tile stay resident in TMEM for all of K),
+ * 1 <= k <= 16, k <= E <= 1024,
  * w_format == FP4MOE_W_NVFP4. Anything else returns FP4MOE_UNSUPPORTED.
  */
 #ifndef FP4MOE_H_
@@ -171,7 +175,7 @@ fp4moe_status moe_route(const fp4moe_config* cfg, int32_t T, const uint16_t* x, 
  * moe_quantize_scatter: L1 activation quantisation into slot order. Each
  * row r < R gets NVFP4(x[pair_of_row[r]/k]) under the global scale *gs1.
  * Codes go to a1_fp4 [CAP][H/2] and swizzled scales to a1_sf
- * [CAP*H/16 bytes]. Padding rows get zeros.
+ * [CAP*H/16 bytes]. Padding rows are left untouched.
  * Per 16-element block, in IEEE fp32 with RNE:
  *   a = max|v|; s = RN(RN(a/6)*g); sf = E4M3_satfinite(s);
  *   inv = sf ? RN(g/sf) : 0; q = E2M1_satfinite(RN(v*inv)).
@@ -188,7 +192,7 @@ fp4moe_status moe_quantize_scatter(const fp4moe_config* cfg, int32_t T, const ui
  *   accumulation,
  *   h = silu(min(g, L)) * clamp(u, -L, L)  (fp32),
  * then NVFP4-requantise h under *gs2 into a2_fp4 [CAP][I/2] and a2_sf
- * (swizzled, C = I/16). Padding rows get zeros.
+ * (swizzled, C = I/16). Padding rows are left untouched.
  * Source: "Current Bug", "Data Flow" (run_nvfp4_grouped_gemm -> l1_out ->
  * SiLU(gate)*up -> quantise), "Bug 6" and "Bug 7". "Lucifer-CUTLASS TP3
  * virtual-padding audit", "TP3 shape plan" (swiglu_limit).

@@ -142,12 +142,12 @@ def test_w1_swiglu_requant(H, I, counts):
     q_ref, s_ref = nvfp4.quantize_rows(h[:R].astype(np.float32), gs2)
     got_deq = nvfp4.dequantize(nvfp4.unpack_codes(codes), sf, gs2)
     ref_deq = nvfp4.dequantize(q_ref, s_ref, gs2)
-    pad = L["pair_of_row"] < 0
-    agree = (nvfp4.unpack_codes(codes) == q_ref).mean()
-    if agree < 0.995 or not (codes[pad] == 0).all():
+    real = L["pair_of_row"] >= 0           # padding rows are left untouched: compare real rows
+    agree = (nvfp4.unpack_codes(codes)[real] == q_ref[real]).mean()
+    if agree < 0.995:
         dump(f"gemm_w1_{H}_{I}", codes=codes, sf=sf, q_ref=q_ref, s_ref=s_ref, h=h[:R], gs2=gs2)
-    assert (codes[pad] == 0).all() and (sf[pad] == 0).all(), "padding rows must be zero"
+    assert (codes[~real] == 0xEE).all(), "padding rows must not be written"
     assert agree >= 0.995, f"code agreement {agree:.4f}"
-    rel = np.linalg.norm(got_deq - ref_deq) / np.linalg.norm(ref_deq)
+    rel = np.linalg.norm(got_deq[real] - ref_deq[real]) / np.linalg.norm(ref_deq[real])
     assert rel < 2e-2, rel
-    assert (sf == s_ref).mean() >= 0.99
+    assert (sf[real] == s_ref[real]).mean() >= 0.99

@@ -111,9 +111,10 @@ def test_quantize_scatter_bit_exact(wl, T):
     q, s = nvfp4.quantize_rows(xf, gs1)
     qp = nvfp4.pack_codes(q)
     por_r = g["por"][:R]
-    want_c = np.where(por_r[:, None] >= 0, qp[np.maximum(por_r, 0) // wl.k], 0)
-    want_s = np.where(por_r[:, None] >= 0, s[np.maximum(por_r, 0) // wl.k], 0)
-    if not ((codes == want_c).all() and (sf == want_s).all()):
+    real = por_r >= 0                      # padding rows are unspecified and not compared
+    want_c = qp[por_r[real] // wl.k]
+    want_s = s[por_r[real] // wl.k]
+    if not ((codes[real] == want_c).all() and (sf[real] == want_s).all()):
         dump(f"qscatter_{wl.name}_{T}", codes=codes, sf=sf, want_c=want_c, want_s=want_s)
-    assert (sf == want_s).all()
-    assert (codes == want_c).all()
+    assert (sf[real] == want_s).all()
+    assert (codes[real] == want_c).all()
