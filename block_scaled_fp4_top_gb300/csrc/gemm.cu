@@ -62,16 +62,18 @@ constexpr int STAGE_BYTES = SFB_OFF + 4 * SF_TILE;  // 36864, a multiple of 1024
 constexpr int BAR_OFF = STAGES * STAGE_BYTES;
 constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;    // barriers + 1024-byte alignment slack
 constexpr int THREADS = 192;
+constexpr int PREFETCH = 10;        // weight stages pulled into L2 ahead of the ring
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t ACC_COL = 0;    // the accumulator: columns [0, 128)
-constexpr uint32_t SFA_COL = 128;  // resident A scales: 4 columns per 64-element K atom, for all of K
-// B scales of ring stage s: 16 columns at SFA_COL + K/16 + 16 s
+constexpr uint32_t ACC_COLS = 128;  // one accumulator: 128 fp32 columns
+// TMEM columns: nacc accumulators at [0, 128 nacc); resident A scales (4 columns
+// per 64-element K atom, all of K) at SFA_COL = 128 nacc; B scales of ring stage
+// s: 16 columns at SFA_COL + K/16 + 16 s. nacc is 2 when that fits, else 1.
 static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-constexpr int kMaxResidentK = (TMEM_COLS - SFA_COL - 16 * STAGES) * 16;  // 4608
+constexpr int kMaxResidentK = (TMEM_COLS - ACC_COLS - 16 * STAGES) * 16;  // 4608 with one accumulator
 
 struct Params {
-  int E, K, KB, b_rows, NT, k, cap, I, H;
+  int E, K, KB, b_rows, NT, k, cap, I, H, nacc;
   float limit;
   const int32_t* poff;
   const int32_t* pair_of_row;
@@ -149,9 +151,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t smem = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t bar_full = smem + BAR_OFF;          // STAGES x 8 bytes
   const uint32_t bar_empty = bar_full + 8 * STAGES;   // STAGES x 8 bytes
-  const uint32_t bar_tfull = bar_empty + 8 * STAGES;
-  const uint32_t bar_tempty = bar_tfull + 8;
-  const uint32_t bar_drain = bar_tempty + 8;
+  const uint32_t bar_tfull = bar_empty + 8 * STAGES;  // 2 x 8 bytes
+  const uint32_t bar_tempty = bar_tfull + 16;         // 2 x 8 bytes
+  const uint32_t bar_drain = bar_tempty + 16;
 
   if (warp == 0) {
     tmem_alloc(smem_u32(&s_tmem), TMEM_COLS);
@@ -162,8 +164,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    mbar_init(bar_tfull, 1);
-    mbar_init(bar_tempty, 4);  // one arrive per epilogue warp
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull + 8 * b, 1);
+      mbar_init(bar_tempty + 8 * b, 4);  // one arrive per epilogue warp
+    }
     mbar_init(bar_drain, 1);
     fence_mbar_init();
   }
@@ -174,12 +178,25 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int KB = prm.KB;
   const int katoms_total = prm.K / 64;
-  const uint32_t sfb_col = SFA_COL + 4u * katoms_total;
+  const int nacc = prm.nacc;
+  const uint32_t sfa_col = ACC_COLS * nacc;
+  const uint32_t sfb_col = sfa_col + 4u * katoms_total;
 
   if (warp == 4 && lane == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t pol_w = policy_evict_first();  // weights stream through once
     const uint64_t pol_a = policy_evict_last();   // activations are re-read by every n-tile
+    const int n_stages = (tau1 - tau0) * KB;
+    // L2 prefetch cursor: stage j of this CTA's range is k-stage j % KB of tile tau0 + j / KB
+    Tile pt{0, 0, 0};
+    auto prefetch = [&](int j) {
+      const int kb = j % KB;
+      if (kb == 0 || j == 0) pt = map_tile(tau0 + j / KB, prm.poff, E, NT);
+      const size_t blk = (size_t)(pt.e * NT + pt.nt);
+      bulk_prefetch_l2(prm.b_codes + (blk * KB + kb) * B_BYTES, B_BYTES);
+      bulk_prefetch_l2(prm.b_sf + (blk * katoms_total + 4 * kb) * SF_TILE, min(4, katoms_total - kb * 4) * SF_TILE);
+    };
+    for (int j = 0; j < min(PREFETCH, n_stages); ++j) prefetch(j);
     int it = 0, prev_mt = -1;
     bool ok = true;
     for (int tau = tau0; tau < tau1 && ok; ++tau) {
@@ -191,6 +208,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint8_t* sfa = prm.a_sf + (size_t)t.mt * katoms_total * SF_TILE;
       const uint8_t* sfb = prm.b_sf + ((size_t)t.e * NT + t.nt) * katoms_total * SF_TILE;
       for (int kb = 0; kb < KB; ++kb, ++it) {
+        if (it + PREFETCH < n_stages) prefetch(it + PREFETCH);
         const int s = it % STAGES;
         const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
         if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, prm.err)) {
@@ -217,13 +235,22 @@ __global__ void __launch_bounds__(THREADS, 1)
       const Tile t = map_tile(tau, prm.poff, E, NT);
       const bool new_a = (t.mt != prev_mt);
       prev_mt = t.mt;
-      // the epilogue has drained the accumulator, so every earlier MMA is complete:
-      // the resident A scales may now be overwritten
-      if (!mbar_wait(bar_tempty, ((uint32_t)tl & 1u) ^ 1u, prm.err)) {
+      const int b = tl % nacc;
+      const uint32_t use = (uint32_t)(tl / nacc);
+      // the epilogue has drained this accumulator buffer
+      if (!mbar_wait(bar_tempty + 8 * b, (use & 1u) ^ 1u, prm.err)) {
+        ok = false;
+        break;
+      }
+      // before new A scales overwrite the resident ones, every earlier MMA must be complete: with one buffer
+      // the wait above implies it; with two, also wait until the other buffer's last tile was drained
+      if (new_a && nacc == 2 && tl > 0 &&
+          !mbar_wait(bar_tempty + 8 * (b ^ 1), ((uint32_t)((tl - 1) / 2) & 1u), prm.err)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      const uint32_t acc = tmem + ACC_COLS * b;
       for (int kb = 0; kb < KB; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
@@ -234,17 +261,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const int atoms = min(4, katoms_total - kb * 4);
         const uint32_t st = smem + s * STAGE_BYTES;
-        const uint32_t sfa_t = tmem + SFA_COL + 16u * kb;
+        const uint32_t sfa_t = tmem + sfa_col + 16u * kb;
         const uint32_t sfb_t = tmem + sfb_col + 16u * s;
         if (new_a)
           for (int a = 0; a < atoms; ++a) tc_cp_scales(sfa_t + 4 * a, desc_scales(st + SFA_OFF + a * SF_TILE));
         for (int a = 0; a < atoms; ++a) tc_cp_scales(sfb_t + 4 * a, desc_scales(st + SFB_OFF + a * SF_TILE));
         for (int a = 0; a < atoms; ++a)
-          tc_mma_nvf4(tmem + ACC_COL, desc_sw128(st + a * 32), desc_sw128(st + A_BYTES + a * 32), idesc,
+          tc_mma_nvf4(acc, desc_sw128(st + a * 32), desc_sw128(st + A_BYTES + a * 32), idesc,
                       sfa_t + 4 * a, sfb_t + 4 * a, (kb > 0 || a > 0) ? 1u : 0u);
         tc_commit(bar_empty + 8 * s);
       }
-      if (ok) tc_commit(bar_tfull);
+      if (ok) tc_commit(bar_tfull + 8 * b);
     }
     // no MMA may still write TMEM when it is freed
     tc_commit(bar_drain);
@@ -257,10 +284,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int r = t.mt * BM + warp * 32 + lane;
       const int p = __ldg(prm.pair_of_row + r);
       const bool any_real = __any_sync(0xFFFFFFFFu, p >= 0);
+      const int b = tl % nacc;
+      const uint32_t use = (uint32_t)(tl / nacc);
       // the whole warp takes one decision: tcgen05.ld is warp-collective
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_tfull, (uint32_t)tl & 1u, prm.err) ? 1 : 0)) break;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_tfull + 8 * b, use & 1u, prm.err) ? 1 : 0)) break;
       tc_fence_after();
-      const uint32_t tacc = tmem + ACC_COL + ((uint32_t)(warp * 32) << 16);
+      const uint32_t tacc = tmem + ACC_COLS * b + ((uint32_t)(warp * 32) << 16);
       float v[128];
       if (any_real) {
 #pragma unroll
@@ -274,7 +303,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_tempty);  // the accumulator is free for the next tile
+      if (lane == 0) mbar_arrive(bar_tempty + 8 * b);  // the accumulator is free for the next tile
       if (p < 0) continue;                     // padding rows carry nothing ("Bug 14")
       const float alpha = __ldg(prm.alpha + t.e);
       if constexpr (MODE == kW2Rows) {
@@ -390,11 +419,13 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
                           cudaStream_t st) {
   if (T == 0) return FP4MOE_OK;
   const bool w2 = (mode == kW2Rows);
-  if ((w2 ? cfg.inter : cfg.hidden) > kMaxResidentK) return FP4MOE_UNSUPPORTED;
+  const int Kc = w2 ? cfg.inter : cfg.hidden;
+  if (Kc > kMaxResidentK) return FP4MOE_UNSUPPORTED;
   Params prm;
   prm.E = cfg.num_experts;
   prm.K = w2 ? cfg.inter : cfg.hidden;
   prm.KB = (prm.K + 255) / 256;
+  prm.nacc = (2 * (int)ACC_COLS + prm.K / 16 + 16 * STAGES <= (int)TMEM_COLS) ? 2 : 1;
   prm.b_rows = w2 ? cfg.hidden : 2 * cfg.inter;
   prm.NT = prm.b_rows / BN;
   prm.k = cfg.top_k;
