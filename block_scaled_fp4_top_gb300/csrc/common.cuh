@@ -117,11 +117,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait for the phase with `parity` to complete. It returns false if
-// kWaitLimitNs passes first (setting FP4MOE_ERR_TIMEOUT), or if another CTA
-// has already raised an abort bit in the error word.
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Slow path of mbar_wait: spin with a time limit.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint32_t* err) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -133,6 +130,14 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uin
       }
     }
   }
+}
+// Bounded wait for the phase with `parity` to complete. It returns false if
+// kWaitLimitNs passes first (setting FP4MOE_ERR_TIMEOUT), or if another CTA
+// has already raised an abort bit in the error word. The common case, a phase
+// that has already completed, stays inline.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, err);
 }
 
 // --------------------------------------------------------------- PTX: TMA --

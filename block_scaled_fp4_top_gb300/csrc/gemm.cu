@@ -228,8 +228,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int j = max(0, it - STAGES); j < it; ++j) drain_wait(bar_full + 8 * (j % STAGES), (uint32_t)(j / STAGES) & 1u);
   } else if (warp == 5 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
+    // This single thread is the throughput limit of the kernel: every instruction here runs at full
+    // latency. So the per-stage work is one wait, 4 (+4 on a new m-tile) scale copies, 4 MMAs and
+    // one commit, fully unrolled. Stage and phase are counters, and the shared-memory descriptors
+    // are advanced by constant adds (a descriptor's address field is the byte address / 16).
     constexpr uint32_t idesc = idesc_nvf4(BM, BN);
-    int it = 0, tl = 0, prev_mt = -1;
+    const uint64_t dA0 = desc_sw128(smem);
+    const uint64_t dS0 = desc_scales(smem);
+    constexpr uint64_t kStageD = STAGE_BYTES >> 4, kBD = A_BYTES >> 4, kSfaD = SFA_OFF >> 4, kSfbD = SFB_OFF >> 4;
+    int tl = 0, prev_mt = -1;
+    int s = 0;
+    uint32_t ph = 0;
     bool ok = true;
     for (int tau = tau0; tau < tau1 && ok; ++tau, ++tl) {
       const Tile t = map_tile(tau, prm.poff, E, NT);
@@ -251,25 +260,48 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc_fence_after();
       const uint32_t acc = tmem + ACC_COLS * b;
-      for (int kb = 0; kb < KB; ++kb, ++it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+      for (int kb = 0; kb < KB; ++kb) {
+        // the mbarrier completion orders the TMA writes before the tensor-core reads
+        // (both async proxy): no tcgen05 fence is needed here
         if (!mbar_wait(bar_full + 8 * s, ph, prm.err)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const int atoms = min(4, katoms_total - kb * 4);
-        const uint32_t st = smem + s * STAGE_BYTES;
+        const uint64_t dst = (uint64_t)s * kStageD;
+        const uint64_t dA = dA0 + dst, dB = dA0 + dst + kBD;
+        const uint64_t dSa = dS0 + dst + kSfaD, dSb = dS0 + dst + kSfbD;
         const uint32_t sfa_t = tmem + sfa_col + 16u * kb;
         const uint32_t sfb_t = tmem + sfb_col + 16u * s;
-        if (new_a)
-          for (int a = 0; a < atoms; ++a) tc_cp_scales(sfa_t + 4 * a, desc_scales(st + SFA_OFF + a * SF_TILE));
-        for (int a = 0; a < atoms; ++a) tc_cp_scales(sfb_t + 4 * a, desc_scales(st + SFB_OFF + a * SF_TILE));
-        for (int a = 0; a < atoms; ++a)
-          tc_mma_nvf4(acc, desc_sw128(st + a * 32), desc_sw128(st + A_BYTES + a * 32), idesc,
-                      sfa_t + 4 * a, sfb_t + 4 * a, (kb > 0 || a > 0) ? 1u : 0u);
+        const uint32_t acc0 = kb > 0 ? 1u : 0u;
+        if (kb * 4 + 4 <= katoms_total) {  // a full stage: 4 scale atoms, 4 MMAs
+          if (new_a) {
+            tc_cp_scales(sfa_t + 0, dSa + 0);
+            tc_cp_scales(sfa_t + 4, dSa + 32);
+            tc_cp_scales(sfa_t + 8, dSa + 64);
+            tc_cp_scales(sfa_t + 12, dSa + 96);
+          }
+          tc_cp_scales(sfb_t + 0, dSb + 0);
+          tc_cp_scales(sfb_t + 4, dSb + 32);
+          tc_cp_scales(sfb_t + 8, dSb + 64);
+          tc_cp_scales(sfb_t + 12, dSb + 96);
+          tc_mma_nvf4(acc, dA + 0, dB + 0, idesc, sfa_t + 0, sfb_t + 0, acc0);
+          tc_mma_nvf4(acc, dA + 2, dB + 2, idesc, sfa_t + 4, sfb_t + 4, 1u);
+          tc_mma_nvf4(acc, dA + 4, dB + 4, idesc, sfa_t + 8, sfb_t + 8, 1u);
+          tc_mma_nvf4(acc, dA + 6, dB + 6, idesc, sfa_t + 12, sfb_t + 12, 1u);
+        } else {  // the partial last stage of a K that is not a multiple of 256
+          const int atoms = katoms_total - kb * 4;
+          for (int a = 0; a < atoms; ++a) {
+            if (new_a) tc_cp_scales(sfa_t + 4 * a, dSa + 32 * a);
+            tc_cp_scales(sfb_t + 4 * a, dSb + 32 * a);
+          }
+          for (int a = 0; a < atoms; ++a)
+            tc_mma_nvf4(acc, dA + 2 * a, dB + 2 * a, idesc, sfa_t + 4 * a, sfb_t + 4 * a, (kb > 0 || a > 0) ? 1u : 0u);
+        }
         tc_commit(bar_empty + 8 * s);
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       if (ok) tc_commit(bar_tfull + 8 * b);
     }
