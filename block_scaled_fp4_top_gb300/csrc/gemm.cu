@@ -261,12 +261,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const uint32_t acc = tmem + ACC_COLS * b;
       for (int kb = 0; kb < KB; ++kb) {
-        // the mbarrier completion orders the TMA writes before the tensor-core reads
-        // (both async proxy): no tcgen05 fence is needed here
         if (!mbar_wait(bar_full + 8 * s, ph, prm.err)) {
           ok = false;
           break;
         }
+        // order the tensor-core reads of this stage after the mbarrier wait that made the TMA
+        // writes visible (without it MMAs can read stale shared memory)
+        tc_fence_after();
         const uint64_t dst = (uint64_t)s * kStageD;
         const uint64_t dA = dA0 + dst, dB = dA0 + dst + kBD;
         const uint64_t dSa = dS0 + dst + kSfaD, dSb = dS0 + dst + kSfbD;
