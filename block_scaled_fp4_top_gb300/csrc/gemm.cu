@@ -230,12 +230,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     // This single thread is the throughput limit of the kernel: every instruction here runs at full
     // latency. So the per-stage work is one wait, 4 (+4 on a new m-tile) scale copies, 4 MMAs and
-    // one commit, fully unrolled. Stage and phase are counters, and the shared-memory descriptors
-    // are advanced by constant adds (a descriptor's address field is the byte address / 16).
+    // one commit, fully unrolled, and stage and phase are counters. Every shared-memory descriptor is
+    // built from its full byte address: the 14-bit address field wraps with the shared window, so
+    // adding offsets to an already-masked descriptor could carry into the reserved bits.
     constexpr uint32_t idesc = idesc_nvf4(BM, BN);
-    const uint64_t dA0 = desc_sw128(smem);
-    const uint64_t dS0 = desc_scales(smem);
-    constexpr uint64_t kStageD = STAGE_BYTES >> 4, kBD = A_BYTES >> 4, kSfaD = SFA_OFF >> 4, kSfbD = SFB_OFF >> 4;
     int tl = 0, prev_mt = -1;
     int s = 0;
     uint32_t ph = 0;
@@ -268,35 +266,29 @@ __global__ void __launch_bounds__(THREADS, 1)
         // order the tensor-core reads of this stage after the mbarrier wait that made the TMA
         // writes visible (without it MMAs can read stale shared memory)
         tc_fence_after();
-        const uint64_t dst = (uint64_t)s * kStageD;
-        const uint64_t dA = dA0 + dst, dB = dA0 + dst + kBD;
-        const uint64_t dSa = dS0 + dst + kSfaD, dSb = dS0 + dst + kSfbD;
+        const uint32_t st = smem + (uint32_t)s * STAGE_BYTES;
         const uint32_t sfa_t = tmem + sfa_col + 16u * kb;
         const uint32_t sfb_t = tmem + sfb_col + 16u * s;
         const uint32_t acc0 = kb > 0 ? 1u : 0u;
         if (kb * 4 + 4 <= katoms_total) {  // a full stage: 4 scale atoms, 4 MMAs
-          if (new_a) {
-            tc_cp_scales(sfa_t + 0, dSa + 0);
-            tc_cp_scales(sfa_t + 4, dSa + 32);
-            tc_cp_scales(sfa_t + 8, dSa + 64);
-            tc_cp_scales(sfa_t + 12, dSa + 96);
-          }
-          tc_cp_scales(sfb_t + 0, dSb + 0);
-          tc_cp_scales(sfb_t + 4, dSb + 32);
-          tc_cp_scales(sfb_t + 8, dSb + 64);
-          tc_cp_scales(sfb_t + 12, dSb + 96);
-          tc_mma_nvf4(acc, dA + 0, dB + 0, idesc, sfa_t + 0, sfb_t + 0, acc0);
-          tc_mma_nvf4(acc, dA + 2, dB + 2, idesc, sfa_t + 4, sfb_t + 4, 1u);
-          tc_mma_nvf4(acc, dA + 4, dB + 4, idesc, sfa_t + 8, sfb_t + 8, 1u);
-          tc_mma_nvf4(acc, dA + 6, dB + 6, idesc, sfa_t + 12, sfb_t + 12, 1u);
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+            if (new_a) tc_cp_scales(sfa_t + 4 * a, desc_scales(st + SFA_OFF + a * SF_TILE));
+#pragma unroll
+          for (int a = 0; a < 4; ++a) tc_cp_scales(sfb_t + 4 * a, desc_scales(st + SFB_OFF + a * SF_TILE));
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+            tc_mma_nvf4(acc, desc_sw128(st + a * 32), desc_sw128(st + A_BYTES + a * 32), idesc, sfa_t + 4 * a,
+                        sfb_t + 4 * a, a > 0 ? 1u : acc0);
         } else {  // the partial last stage of a K that is not a multiple of 256
           const int atoms = katoms_total - kb * 4;
           for (int a = 0; a < atoms; ++a) {
-            if (new_a) tc_cp_scales(sfa_t + 4 * a, dSa + 32 * a);
-            tc_cp_scales(sfb_t + 4 * a, dSb + 32 * a);
+            if (new_a) tc_cp_scales(sfa_t + 4 * a, desc_scales(st + SFA_OFF + a * SF_TILE));
+            tc_cp_scales(sfb_t + 4 * a, desc_scales(st + SFB_OFF + a * SF_TILE));
           }
           for (int a = 0; a < atoms; ++a)
-            tc_mma_nvf4(acc, dA + 2 * a, dB + 2 * a, idesc, sfa_t + 4 * a, sfb_t + 4 * a, (kb > 0 || a > 0) ? 1u : 0u);
+            tc_mma_nvf4(acc, desc_sw128(st + a * 32), desc_sw128(st + A_BYTES + a * 32), idesc, sfa_t + 4 * a,
+                        sfb_t + 4 * a, (kb > 0 || a > 0) ? 1u : 0u);
         }
         tc_commit(bar_empty + 8 * s);
         if (++s == STAGES) {
