@@ -12,19 +12,21 @@
 // 128 weight rows, numbered in (m-tile, n-tile) order. CTA c takes the
 // contiguous share [c*T/G, (c+1)*T/G) of the T tiles, so it walks consecutive
 // n-tiles of the same m-tile (expert block):
-//   warp 4      producer. Each stage moves one 16 KB weight block with a
-//               single contiguous cp.async.bulk: the weights are stored
-//               pre-tiled and pre-swizzled (see fp4moe.h). The 128-row
-//               activation tile arrives by cp.async.bulk.tensor with the
-//               128-byte swizzle, and the 2 KB scale tiles by cp.async.bulk.
-//               The STAGES-deep shared-memory ring runs on across tile
-//               boundaries, so the weight stream never stops.
+//   warp 4      producer. A ring stage covers 512 elements of K. Its two
+//               consecutive 16 KB weight blocks arrive with one contiguous
+//               cp.async.bulk: the weights are stored pre-tiled and
+//               pre-swizzled (see fp4moe.h). The two 128-row activation
+//               blocks arrive by cp.async.bulk.tensor with the 128-byte
+//               swizzle, and the scale tiles by cp.async.bulk. Weight stages
+//               are also pulled into L2 a few stages ahead
+//               (cp.async.bulk.prefetch.L2). The shared-memory ring runs on
+//               across tile boundaries, so the weight stream never stops.
 //   warp 5      MMA issuer. tcgen05.cp costs about the same per instruction
 //               whatever its size, and it sits on this thread's critical path.
 //               So the activation (A) scales of an m-tile are copied into
 //               TMEM only once, for the whole of K, and stay resident while
 //               the CTA walks that m-tile's n-tiles. Each stage then copies
-//               only its 4 weight (B) scale tiles. Then
+//               only its 8 weight (B) scale tiles. Then
 //               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (K = 64
 //               each) accumulates in fp32 in TMEM, and tcgen05.commit frees the
 //               ring slot and then hands the accumulator to the epilogue.
@@ -51,26 +53,30 @@ namespace {
 
 constexpr int BM = 128;            // activation rows per tile (MMA M)
 constexpr int BN = 128;            // weight rows per tile (MMA N)
-constexpr int KBYTES = 128;        // K bytes per stage: 256 FP4 elements = 4 MMAs of K = 64
-constexpr int STAGES = 6;
-constexpr int A_BYTES = BM * KBYTES;
-constexpr int B_BYTES = BN * KBYTES;  // one pre-tiled weight block
-constexpr int SF_TILE = 512;          // one 128x4 scale tile
+constexpr int KBYTES = 128;        // bytes of K in one 128-byte swizzle atom: 256 FP4 = 4 MMAs of K = 64
+constexpr int HALVES = 2;          // K atoms per ring stage: 512 FP4 = 8 MMAs per stage
+constexpr int ATOMS = 4 * HALVES;  // 64-element scale atoms per stage
+constexpr int STAGES = 3;
+constexpr int HALF_BYTES = BM * KBYTES;        // one 128-row x 128-byte swizzled block (16 KB)
+constexpr int A_BYTES = HALVES * HALF_BYTES;
+constexpr int B_BYTES = HALVES * HALF_BYTES;   // pre-tiled weight blocks of consecutive k-stages
+constexpr int SF_TILE = 512;                   // one 128x4 scale tile
 constexpr int SFA_OFF = A_BYTES + B_BYTES;
-constexpr int SFB_OFF = SFA_OFF + 4 * SF_TILE;
-constexpr int STAGE_BYTES = SFB_OFF + 4 * SF_TILE;  // 36864, a multiple of 1024
+constexpr int SFB_OFF = SFA_OFF + ATOMS * SF_TILE;
+constexpr int STAGE_BYTES = SFB_OFF + ATOMS * SF_TILE;  // 73728, a multiple of 1024
 constexpr int BAR_OFF = STAGES * STAGE_BYTES;
 constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;    // barriers + 1024-byte alignment slack
 constexpr int THREADS = 192;
-constexpr int PREFETCH = 10;        // weight stages pulled into L2 ahead of the ring
+constexpr int PREFETCH = 6;         // ring stages pulled into L2 ahead of the ring
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 128;  // one accumulator: 128 fp32 columns
+constexpr uint32_t SFB_STAGE_COLS = 4 * ATOMS;  // B scales of one ring stage
 // TMEM columns: nacc accumulators at [0, 128 nacc); resident A scales (4 columns
 // per 64-element K atom, all of K) at SFA_COL = 128 nacc; B scales of ring stage
-// s: 16 columns at SFA_COL + K/16 + 16 s. nacc is 2 when that fits, else 1.
+// s: 32 columns at SFA_COL + K/16 + 32 s. nacc is 2 when that fits, else 1.
 static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-constexpr int kMaxResidentK = (TMEM_COLS - ACC_COLS - 16 * STAGES) * 16;  // 4608 with one accumulator
+constexpr int kMaxResidentK = (TMEM_COLS - ACC_COLS - SFB_STAGE_COLS * STAGES) * 16;  // 4608 with one accumulator
 
 struct Params {
   int E, K, KB, b_rows, NT, k, cap, I, H, nacc;
@@ -181,20 +187,24 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int nacc = prm.nacc;
   const uint32_t sfa_col = ACC_COLS * nacc;
   const uint32_t sfb_col = sfa_col + 4u * katoms_total;
+  (void)ATOMS;
 
   if (warp == 4 && lane == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t pol_w = policy_evict_first();  // weights stream through once
     const uint64_t pol_a = policy_evict_last();   // activations are re-read by every n-tile
     const int n_stages = (tau1 - tau0) * KB;
+    const int wblocks = (prm.K + 255) / 256;      // 16 KB weight blocks per tile
     // L2 prefetch cursor: stage j of this CTA's range is k-stage j % KB of tile tau0 + j / KB
     Tile pt{0, 0, 0};
     auto prefetch = [&](int j) {
       const int kb = j % KB;
       if (kb == 0 || j == 0) pt = map_tile(tau0 + j / KB, prm.poff, E, NT);
       const size_t blk = (size_t)(pt.e * NT + pt.nt);
-      bulk_prefetch_l2(prm.b_codes + (blk * KB + kb) * B_BYTES, B_BYTES);
-      bulk_prefetch_l2(prm.b_sf + (blk * katoms_total + 4 * kb) * SF_TILE, min(4, katoms_total - kb * 4) * SF_TILE);
+      const int nblk = min(HALVES, wblocks - kb * HALVES);
+      bulk_prefetch_l2(prm.b_codes + (blk * wblocks + (size_t)kb * HALVES) * HALF_BYTES, nblk * HALF_BYTES);
+      bulk_prefetch_l2(prm.b_sf + (blk * katoms_total + (size_t)kb * ATOMS) * SF_TILE,
+                       min(ATOMS, katoms_total - kb * ATOMS) * SF_TILE);
     };
     for (int j = 0; j < min(PREFETCH, n_stages); ++j) prefetch(j);
     int it = 0, prev_mt = -1;
@@ -204,7 +214,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool new_a = (t.mt != prev_mt);  // A scales go to TMEM once per m-tile
       prev_mt = t.mt;
       const int a_row = t.mt * BM;
-      const uint8_t* bsrc = prm.b_codes + (size_t)(t.e * NT + t.nt) * KB * B_BYTES;
+      const uint8_t* bsrc = prm.b_codes + (size_t)(t.e * NT + t.nt) * wblocks * HALF_BYTES;
       const uint8_t* sfa = prm.a_sf + (size_t)t.mt * katoms_total * SF_TILE;
       const uint8_t* sfb = prm.b_sf + ((size_t)t.e * NT + t.nt) * katoms_total * SF_TILE;
       for (int kb = 0; kb < KB; ++kb, ++it) {
@@ -215,13 +225,15 @@ __global__ void __launch_bounds__(THREADS, 1)
           ok = false;
           break;
         }
-        const int atoms = min(4, katoms_total - kb * 4);
+        const int atoms = min(ATOMS, katoms_total - kb * ATOMS);
+        const int halves = (atoms + 3) / 4;
         const uint32_t st = smem + s * STAGE_BYTES;
-        mbar_arrive_expect_tx(bar_full + 8 * s, A_BYTES + B_BYTES + (new_a ? 2 : 1) * atoms * SF_TILE);
-        bulk_load(st + A_BYTES, bsrc + (size_t)kb * B_BYTES, B_BYTES, bar_full + 8 * s, pol_w);
-        tma_load_2d(st, &tmA, bar_full + 8 * s, kb * KBYTES, a_row, pol_a);
-        if (new_a) bulk_load(st + SFA_OFF, sfa + (size_t)kb * 4 * SF_TILE, atoms * SF_TILE, bar_full + 8 * s, pol_a);
-        bulk_load(st + SFB_OFF, sfb + (size_t)kb * 4 * SF_TILE, atoms * SF_TILE, bar_full + 8 * s, pol_w);
+        mbar_arrive_expect_tx(bar_full + 8 * s, 2 * halves * HALF_BYTES + (new_a ? 2 : 1) * atoms * SF_TILE);
+        bulk_load(st + A_BYTES, bsrc + (size_t)kb * B_BYTES, halves * HALF_BYTES, bar_full + 8 * s, pol_w);
+        for (int h = 0; h < halves; ++h)
+          tma_load_2d(st + h * HALF_BYTES, &tmA, bar_full + 8 * s, (kb * HALVES + h) * KBYTES, a_row, pol_a);
+        if (new_a) bulk_load(st + SFA_OFF, sfa + (size_t)kb * ATOMS * SF_TILE, atoms * SF_TILE, bar_full + 8 * s, pol_a);
+        bulk_load(st + SFB_OFF, sfb + (size_t)kb * ATOMS * SF_TILE, atoms * SF_TILE, bar_full + 8 * s, pol_w);
       }
     }
     // on every path, let the copies already issued land before the CTA exits
@@ -267,28 +279,33 @@ __global__ void __launch_bounds__(THREADS, 1)
         // writes visible (without it MMAs can read stale shared memory)
         tc_fence_after();
         const uint32_t st = smem + (uint32_t)s * STAGE_BYTES;
-        const uint32_t sfa_t = tmem + sfa_col + 16u * kb;
-        const uint32_t sfb_t = tmem + sfb_col + 16u * s;
+        const uint32_t sfa_t = tmem + sfa_col + 4u * ATOMS * kb;
+        const uint32_t sfb_t = tmem + sfb_col + SFB_STAGE_COLS * s;
         const uint32_t acc0 = kb > 0 ? 1u : 0u;
-        if (kb * 4 + 4 <= katoms_total) {  // a full stage: 4 scale atoms, 4 MMAs
+        if (kb * ATOMS + ATOMS <= katoms_total) {  // a full stage: 8 scale atoms, 8 MMAs
+          if (new_a) {
 #pragma unroll
-          for (int a = 0; a < 4; ++a)
-            if (new_a) tc_cp_scales(sfa_t + 4 * a, desc_scales(st + SFA_OFF + a * SF_TILE));
+            for (int a = 0; a < ATOMS; ++a) tc_cp_scales(sfa_t + 4 * a, desc_scales(st + SFA_OFF + a * SF_TILE));
+          }
 #pragma unroll
-          for (int a = 0; a < 4; ++a) tc_cp_scales(sfb_t + 4 * a, desc_scales(st + SFB_OFF + a * SF_TILE));
+          for (int a = 0; a < ATOMS; ++a) tc_cp_scales(sfb_t + 4 * a, desc_scales(st + SFB_OFF + a * SF_TILE));
 #pragma unroll
-          for (int a = 0; a < 4; ++a)
-            tc_mma_nvf4(acc, desc_sw128(st + a * 32), desc_sw128(st + A_BYTES + a * 32), idesc, sfa_t + 4 * a,
+          for (int a = 0; a < ATOMS; ++a) {
+            const uint32_t ko = (a >> 2) * HALF_BYTES + (a & 3) * 32;  // K offset inside the stage
+            tc_mma_nvf4(acc, desc_sw128(st + ko), desc_sw128(st + A_BYTES + ko), idesc, sfa_t + 4 * a,
                         sfb_t + 4 * a, a > 0 ? 1u : acc0);
-        } else {  // the partial last stage of a K that is not a multiple of 256
-          const int atoms = katoms_total - kb * 4;
+          }
+        } else {  // the partial last stage of a K that is not a multiple of 512
+          const int atoms = katoms_total - kb * ATOMS;
           for (int a = 0; a < atoms; ++a) {
             if (new_a) tc_cp_scales(sfa_t + 4 * a, desc_scales(st + SFA_OFF + a * SF_TILE));
             tc_cp_scales(sfb_t + 4 * a, desc_scales(st + SFB_OFF + a * SF_TILE));
           }
-          for (int a = 0; a < atoms; ++a)
-            tc_mma_nvf4(acc, desc_sw128(st + a * 32), desc_sw128(st + A_BYTES + a * 32), idesc, sfa_t + 4 * a,
+          for (int a = 0; a < atoms; ++a) {
+            const uint32_t ko = (a >> 2) * HALF_BYTES + (a & 3) * 32;
+            tc_mma_nvf4(acc, desc_sw128(st + ko), desc_sw128(st + A_BYTES + ko), idesc, sfa_t + 4 * a,
                         sfb_t + 4 * a, (kb > 0 || a > 0) ? 1u : 0u);
+          }
         }
         tc_commit(bar_empty + 8 * s);
         if (++s == STAGES) {
@@ -449,8 +466,8 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
   Params prm;
   prm.E = cfg.num_experts;
   prm.K = w2 ? cfg.inter : cfg.hidden;
-  prm.KB = (prm.K + 255) / 256;
-  prm.nacc = (2 * (int)ACC_COLS + prm.K / 16 + 16 * STAGES <= (int)TMEM_COLS) ? 2 : 1;
+  prm.KB = (prm.K + 64 * ATOMS - 1) / (64 * ATOMS);
+  prm.nacc = (2 * (int)ACC_COLS + prm.K / 16 + (int)SFB_STAGE_COLS * STAGES <= (int)TMEM_COLS) ? 2 : 1;
   prm.b_rows = w2 ? cfg.hidden : 2 * cfg.inter;
   prm.NT = prm.b_rows / BN;
   prm.k = cfg.top_k;
