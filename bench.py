@@ -144,7 +144,7 @@ def run_ours(args, wl, rank, world):
                       b["offsets"], b["poff"], b["slot"], b["por"], layer.ws)
         if e is not None:
             e[1].record(stream)
-        api.moe_quantize_scatter(cfg, T, x, layer.gs1, b["poff"], b["por"], b["a1"], b["a1sf"], layer.ws)
+        api.moe_quantize_scatter(cfg, T, x, layer.gs1, b["slot"], b["a1"], b["a1sf"], layer.ws)
         if e is not None:
             e[2].record(stream)
         api.moe_grouped_gemm_w1_swiglu(cfg, T, b["a1"], b["a1sf"], b["poff"], b["por"], W.w1_fp4, W.w1_sf,

@@ -71,10 +71,9 @@ def moe_route(cfg, T, x, router_w, router_bias, logits_out, topk_ids, topk_w, co
                                  _p(slot_of_pair), _p(pair_of_row), _p(ws), _s(stream)), "moe_route")
 
 
-def moe_quantize_scatter(cfg, T, x, gs1, padded_offsets, pair_of_row, a1_fp4, a1_sf, ws, stream=None):
-    _check(_lib.load().moe_quantize_scatter(ctypes.byref(cfg), T, _p(x), _p(gs1), _p(padded_offsets),
-                                            _p(pair_of_row), _p(a1_fp4), _p(a1_sf), _p(ws), _s(stream)),
-           "moe_quantize_scatter")
+def moe_quantize_scatter(cfg, T, x, gs1, slot_of_pair, a1_fp4, a1_sf, ws, stream=None):
+    _check(_lib.load().moe_quantize_scatter(ctypes.byref(cfg), T, _p(x), _p(gs1), _p(slot_of_pair), _p(a1_fp4),
+                                            _p(a1_sf), _p(ws), _s(stream)), "moe_quantize_scatter")
 
 
 def moe_grouped_gemm_w1_swiglu(cfg, T, a1_fp4, a1_sf, padded_offsets, pair_of_row, w1_fp4, w1_sf, alpha1, gs2,

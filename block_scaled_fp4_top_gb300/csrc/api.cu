@@ -82,6 +82,7 @@ WsLayout ws_layout(const fp4moe_config& c) {
   const size_t cap = capacity_rows(c, c.max_tokens);
   const size_t nchunks = std::max<size_t>(1, (Tm + kRouteChunk - 1) / kRouteChunk);
   L.hist = take(nchunks * E * 4);
+  L.cnt = take(Tm * 4);  // zero at allocation; the routing leaves it zero
   L.logits = take(Tm * E * 4);
   L.ids = take(Tm * k * 4);
   L.w = take(Tm * k * 4);
@@ -153,16 +154,17 @@ fp4moe_status moe_route(const fp4moe_config* cfg, int32_t T, const uint16_t* x, 
   const WsLayout L = ws_layout(*cfg);
   float* logits = logits_out ? logits_out : at<float>(ws, L.logits);
   return route_launch(*cfg, T, x, router_w, router_bias, logits, topk_ids, topk_w, counts, offsets, padded_offsets,
-                      slot_of_pair, pair_of_row, at<int32_t>(ws, L.hist), err_word(ws), (cudaStream_t)stream);
+                      slot_of_pair, pair_of_row, at<int32_t>(ws, L.hist), at<int32_t>(ws, L.cnt), err_word(ws),
+                      (cudaStream_t)stream);
 }
 
 fp4moe_status moe_quantize_scatter(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const float* gs1,
-                                   const int32_t* padded_offsets, const int32_t* pair_of_row, uint8_t* a1_fp4,
-                                   uint8_t* a1_sf, void* ws, fp4moe_stream_t stream) {
+                                   const int32_t* slot_of_pair, uint8_t* a1_fp4, uint8_t* a1_sf, void* ws,
+                                   fp4moe_stream_t stream) {
   FP4_TRY(check_cfg(cfg));
   FP4_TRY(check_T(cfg, T));
-  FP4_TRY(check_ptrs(x, gs1, padded_offsets, pair_of_row, a1_fp4, a1_sf, ws));
-  return quant_scatter_launch(*cfg, T, x, gs1, padded_offsets, pair_of_row, a1_fp4, a1_sf, (cudaStream_t)stream);
+  FP4_TRY(check_ptrs(x, gs1, slot_of_pair, a1_fp4, a1_sf, ws));
+  return quant_scatter_launch(*cfg, T, x, gs1, slot_of_pair, a1_fp4, a1_sf, (cudaStream_t)stream);
 }
 
 fp4moe_status moe_grouped_gemm_w1_swiglu(const fp4moe_config* cfg, int32_t T, const uint8_t* a1_fp4,
@@ -230,9 +232,10 @@ fp4moe_status moe_forward(const fp4moe_config* cfg, int32_t T, const uint16_t* x
   int32_t* poff = at<int32_t>(ws, L.poff);
   int32_t* por = at<int32_t>(ws, L.por);
   FP4_TRY(route_launch(*cfg, T, x, router_w, router_bias, at<float>(ws, L.logits), ids, w, at<int32_t>(ws, L.counts),
-                       at<int32_t>(ws, L.offsets), poff, at<int32_t>(ws, L.slot), por, at<int32_t>(ws, L.hist), err,
-                       st));
-  FP4_TRY(quant_scatter_launch(*cfg, T, x, gs1, poff, por, at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf), st));
+                       at<int32_t>(ws, L.offsets), poff, at<int32_t>(ws, L.slot), por, at<int32_t>(ws, L.hist),
+                       at<int32_t>(ws, L.cnt), err, st));
+  FP4_TRY(quant_scatter_launch(*cfg, T, x, gs1, at<int32_t>(ws, L.slot), at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf),
+                               st));
   FP4_TRY(gemm_launch(kW1SwiGLU, *cfg, T, at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf), poff, por, w1_fp4, w1_sf,
                       alpha1, gs2, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), nullptr, nullptr, err, st));
   FP4_TRY(gemm_launch(kW2Rows, *cfg, T, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), poff, por, w2_fp4, w2_sf,
@@ -290,9 +293,9 @@ fp4moe_status fp4moe_calibrate(const fp4moe_config* cfg, int32_t T, const uint16
   FP4_TRY(gs_from_amax_launch(1, gs1_out, st));
   FP4_TRY(route_launch(*cfg, T, x_warm, router_w, router_bias, at<float>(ws, L.logits), at<int32_t>(ws, L.ids),
                        at<float>(ws, L.w), at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets), poff,
-                       at<int32_t>(ws, L.slot), por, at<int32_t>(ws, L.hist), err, st));
-  FP4_TRY(quant_scatter_launch(*cfg, T, x_warm, gs1_out, poff, por, at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf),
-                               st));
+                       at<int32_t>(ws, L.slot), por, at<int32_t>(ws, L.hist), at<int32_t>(ws, L.cnt), err, st));
+  FP4_TRY(quant_scatter_launch(*cfg, T, x_warm, gs1_out, at<int32_t>(ws, L.slot), at<uint8_t>(ws, L.a1),
+                               at<uint8_t>(ws, L.a1sf), st));
   float* alpha = at<float>(ws, L.alpha_tmp);
   FP4_TRY(make_alpha_launch(cfg->num_experts, gs1_out, gw1, alpha, st));
   if (cudaMemsetAsync(amax_h, 0, 4, st) != cudaSuccess) return FP4MOE_CUDA_ERROR;

@@ -5,7 +5,9 @@
 // pair and drops padding rows ("Bug 14"). Every token then sums its k rows in
 // a fixed j order, so the result has no atomics and is run-to-run
 // deterministic. One thread owns 8 consecutive columns, loaded and stored as
-// 128-bit vectors.
+// 128-bit vectors. Inputs written by the kernels just before are read through
+// L2 (ld.global.cg): with programmatic dependent launch this kernel may start
+// before they finish.
 #include "common.cuh"
 #include "internal.h"
 
@@ -20,14 +22,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float* __restrict__ o,
                                                       const float* __restrict__ w, uint16_t* __restrict__ y) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.y;
   const int col = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
   if (col >= H) return;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int j = 0; j < k; ++j) {
-    const float wj = __ldg(w + (size_t)t * k + j);
+    const float wj = __ldcg(w + (size_t)t * k + j);
     const float4* src = reinterpret_cast<const float4*>(o + ((size_t)t * k + j) * H + col);
-    const float4 a = __ldg(src), b = __ldg(src + 1);
+    const float4 a = __ldcg(src), b = __ldcg(src + 1);
     acc[0] = fmaf(wj, a.x, acc[0]);
     acc[1] = fmaf(wj, a.y, acc[1]);
     acc[2] = fmaf(wj, a.z, acc[2]);
@@ -48,8 +52,10 @@ fp4moe_status combine_launch(const fp4moe_config& cfg, int32_t T, const float* o
                              uint16_t* y, cudaStream_t st) {
   if (T == 0) return FP4MOE_OK;
   const int H = cfg.hidden;
-  combine_kernel<<<dim3((H / 8 + 255) / 256, T), 256, 0, st>>>(H, cfg.top_k, o_pairs, w, y);
-  return cudaGetLastError() == cudaSuccess ? FP4MOE_OK : FP4MOE_CUDA_ERROR;
+  return launch_pdl(combine_kernel, dim3((H / 8 + 255) / 256, T), dim3(256), 0, st, H, cfg.top_k, o_pairs, w, y) ==
+                 cudaSuccess
+             ? FP4MOE_OK
+             : FP4MOE_CUDA_ERROR;
 }
 
 }  // namespace fp4moe

@@ -91,6 +91,14 @@ __device__ __forceinline__ float global_scale_from_amax(float amax) {
   return amax > 0.0f ? __fdiv_rn(2688.0f, amax) : 1.0f;
 }
 
+// ------------------------------------------------ programmatic dependent launch --
+// Kernels on the hot path are launched with programmatic stream serialisation
+// (launch_pdl in the host code). Each one lets its successor start early,
+// which hides the launch gap, and waits for its predecessor's results before
+// reading them. Without a programmatic predecessor both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------- PTX: misc --
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 __device__ __forceinline__ uint64_t globaltimer() {

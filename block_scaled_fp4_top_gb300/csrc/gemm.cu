@@ -107,7 +107,7 @@ __device__ __forceinline__ Tile map_tile(int tau, const int32_t* __restrict__ po
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
-    if (__ldg(poff + mid) > row) hi = mid;
+    if (__ldcg(poff + mid) > row) hi = mid;
     else lo = mid + 1;
   }
   return Tile{lo, tau - mt * NT, mt};
@@ -146,9 +146,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
 
+  pdl_wait();  // the routing / quantisation results of the previous launch are needed from here on
+  pdl_trigger();
   if (*(volatile uint32_t*)prm.err & kAbortMask) return;  // an earlier timeout poisons the call
   const int E = prm.E, NT = prm.NT;
-  const int R = min(__ldg(prm.poff + E - 1), prm.cap);
+  const int R = min(__ldcg(prm.poff + E - 1), prm.cap);
   int tau0, tau1;
   cta_range((R / BM) * NT, tau0, tau1);
   if (tau0 >= tau1) return;
@@ -324,7 +326,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int tau = tau0; tau < tau1; ++tau, ++tl) {
       const Tile t = map_tile(tau, prm.poff, E, NT);
       const int r = t.mt * BM + warp * 32 + lane;
-      const int p = __ldg(prm.pair_of_row + r);
+      const int p = __ldcg(prm.pair_of_row + r);
       const bool any_real = __any_sync(0xFFFFFFFFu, p >= 0);
       const int b = tl % nacc;
       const uint32_t use = (uint32_t)(tl / nacc);
@@ -493,21 +495,22 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
   if (nsm <= 0) return FP4MOE_CUDA_ERROR;
   const int max_tiles = (prm.cap / BM) * prm.NT;
   const unsigned grid = (unsigned)(max_tiles < nsm ? max_tiles : nsm);
+  cudaError_t r = cudaErrorInvalidValue;
   switch (mode) {
     case kW1SwiGLU:
       if (!configure_once<kW1SwiGLU>()) return FP4MOE_CUDA_ERROR;
-      grouped_gemm_kernel<kW1SwiGLU><<<grid, THREADS, SMEM_BYTES, st>>>(tmA, prm);
+      r = launch_pdl(grouped_gemm_kernel<kW1SwiGLU>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, tmA, prm);
       break;
     case kW1Amax:
       if (!configure_once<kW1Amax>()) return FP4MOE_CUDA_ERROR;
-      grouped_gemm_kernel<kW1Amax><<<grid, THREADS, SMEM_BYTES, st>>>(tmA, prm);
+      r = launch_pdl(grouped_gemm_kernel<kW1Amax>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, tmA, prm);
       break;
     case kW2Rows:
       if (!configure_once<kW2Rows>()) return FP4MOE_CUDA_ERROR;
-      grouped_gemm_kernel<kW2Rows><<<grid, THREADS, SMEM_BYTES, st>>>(tmA, prm);
+      r = launch_pdl(grouped_gemm_kernel<kW2Rows>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, tmA, prm);
       break;
   }
-  return cudaGetLastError() == cudaSuccess ? FP4MOE_OK : FP4MOE_CUDA_ERROR;
+  return r == cudaSuccess ? FP4MOE_OK : FP4MOE_CUDA_ERROR;
 }
 
 }  // namespace fp4moe

@@ -9,22 +9,39 @@
 
 namespace fp4moe {
 
+// Launch `kernel` on `st` with programmatic stream serialisation allowed (see pdl_wait / pdl_trigger).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 size_t capacity_rows(const fp4moe_config& cfg, int32_t T);
 
 // Byte offsets of the regions of a workspace sized for cfg.max_tokens.
 struct WsLayout {
-  size_t hist, logits, ids, w, counts, offsets, poff, slot, por, a1, a1sf, a2, a2sf, opairs, alpha_tmp, total;
+  size_t hist, cnt, logits, ids, w, counts, offsets, poff, slot, por, a1, a1sf, a2, a2sf, opairs, alpha_tmp, total;
 };
 WsLayout ws_layout(const fp4moe_config& cfg);
 
+// hist: per-chunk histograms for large T; cnt: per-token arrival counters of the fused logits/top-k kernel
+// (zero when idle; every call leaves them zero)
 fp4moe_status route_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
                            const float* bias, float* logits, int32_t* ids, float* w, int32_t* counts,
                            int32_t* offsets, int32_t* poff, int32_t* slot_of_pair, int32_t* pair_of_row,
-                           int32_t* hist, uint32_t* err, cudaStream_t st);
+                           int32_t* hist, int32_t* cnt, uint32_t* err, cudaStream_t st);
 
 fp4moe_status quant_scatter_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const float* gs1,
-                                   const int32_t* poff, const int32_t* pair_of_row, uint8_t* a1, uint8_t* a1_sf,
-                                   cudaStream_t st);
+                                   const int32_t* slot_of_pair, uint8_t* a1, uint8_t* a1_sf, cudaStream_t st);
 
 // rows [n_rows_total][K] fp32 -> NVFP4; g indexed by row / g_div; optional W1 gate/up row permutation
 // (rows_per_group = rows of one expert, inter = I, or 0 for no permutation); tiled != 0 writes the codes in

@@ -15,24 +15,23 @@
 namespace fp4moe {
 namespace {
 
-// One warp per slot row, 8 rows per CTA. Each lane quantises 16-element
-// blocks lane, lane+32, ... of the row.
-__global__ void __launch_bounds__(256) quant_scatter_kernel(int H, int E, int k, int cap,
-                                                            const uint16_t* __restrict__ x,
+// One warp per token, 8 tokens per CTA. The token's row is quantised once
+// (each lane takes 16-element blocks lane, lane+32, ...) and written to its k
+// slot rows. Padding rows are never touched.
+__global__ void __launch_bounds__(256) quant_scatter_kernel(int T, int H, int k, const uint16_t* __restrict__ x,
                                                             const float* __restrict__ gs1,
-                                                            const int32_t* __restrict__ poff,
-                                                            const int32_t* __restrict__ pair_of_row,
+                                                            const int32_t* __restrict__ slot_of_pair,
                                                             uint8_t* __restrict__ a1, uint8_t* __restrict__ a1_sf) {
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.x * 8 + warp;
-  const int R = min(__ldg(poff + E - 1), cap);
-  if (r >= R) return;
-  const int p = __ldg(pair_of_row + r);
-  if (p < 0) return;  // padding rows carry nothing and are never read back ("Bug 14")
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  int rows[kMaxTopK];
+  for (int j = 0; j < k; ++j) rows[j] = __ldcg(slot_of_pair + (size_t)t * k + j);
   const int C = H >> 4;
-  uint8_t* dst = a1 + (size_t)r * (H >> 1);
   const float g = __ldg(gs1);
-  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(p / k) * H);
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
   for (int b = lane; b < C; b += 32) {
     const uint4 u0 = __ldg(src + 2 * b), u1 = __ldg(src + 2 * b + 1);
     const float v[16] = {bf16_lo(u0.x), bf16_hi(u0.x), bf16_lo(u0.y), bf16_hi(u0.y), bf16_lo(u0.z), bf16_hi(u0.z),
@@ -40,8 +39,10 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(int H, int E, int k,
                          bf16_lo(u1.z), bf16_hi(u1.z), bf16_lo(u1.w), bf16_hi(u1.w)};
     uint32_t lo, hi;
     const uint32_t sf = quant_block16(v, g, lo, hi);
-    *reinterpret_cast<uint2*>(dst + b * 8) = make_uint2(lo, hi);
-    a1_sf[sf_offset(r, b, C)] = (uint8_t)sf;
+    for (int j = 0; j < k; ++j) {
+      *reinterpret_cast<uint2*>(a1 + (size_t)rows[j] * (H >> 1) + b * 8) = make_uint2(lo, hi);
+      a1_sf[sf_offset(rows[j], b, C)] = (uint8_t)sf;
+    }
   }
 }
 
@@ -134,13 +135,12 @@ inline fp4moe_status last_status() { return cudaGetLastError() == cudaSuccess ? 
 }  // namespace
 
 fp4moe_status quant_scatter_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const float* gs1,
-                                   const int32_t* poff, const int32_t* pair_of_row, uint8_t* a1, uint8_t* a1_sf,
-                                   cudaStream_t st) {
+                                   const int32_t* slot_of_pair, uint8_t* a1, uint8_t* a1_sf, cudaStream_t st) {
   if (T == 0) return FP4MOE_OK;
-  const int cap = (int)capacity_rows(cfg, T);
-  quant_scatter_kernel<<<cap / 8, 256, 0, st>>>(cfg.hidden, cfg.num_experts, cfg.top_k, cap, x, gs1, poff,
-                                                pair_of_row, a1, a1_sf);
-  return last_status();
+  return launch_pdl(quant_scatter_kernel, dim3((T + 7) / 8), dim3(256), 0, st, T, cfg.hidden, cfg.top_k, x, gs1,
+                    slot_of_pair, a1, a1_sf) == cudaSuccess
+             ? FP4MOE_OK
+             : FP4MOE_CUDA_ERROR;
 }
 
 fp4moe_status quant_rows_launch(int64_t n_rows_total, int32_t K, int32_t rows_per_group, int32_t inter,

@@ -8,14 +8,22 @@
 // ("Bug 4"), searchsorted(right=True) ownership ("Bug 2") and 128-row-aligned
 // expert slots ("Bug 14").
 //
-// Four launches, each with a fixed grid chosen from the host-known T:
-//   1. router_logits  grid (ceil(E/32), T): a compensated fp32 dot product per (t, e)
-//   2. topk_hist      grid (chunks of 64 tokens): warp top-k, softmax, chunk histogram
-//   3. scan           1 CTA: chunk prefix per expert, counts, offsets, padded offsets
-//   4. slots          grid (chunks): ranks in ascending pair order, one warp per chunk
-// Nothing here depends on the order of floating-point atomics. The
-// histogram uses integer atomics only, so every output is run-to-run
-// deterministic.
+// Launches, each with a fixed grid chosen from the host-known T:
+//   1. logits_topk   grid (T, ceil(E/64)). Each CTA computes 64 logits of one
+//                    token, with a compensated fp32 dot product per expert. The
+//                    last CTA of the token to finish (an arrival counter)
+//                    takes the softmax top-k of all E logits.
+//   then, for T*k <= kSmallPairs (decode):
+//   2. layout_small  1 CTA: counts, offsets, padded offsets, slot ranks and
+//                    pair_of_row
+//   otherwise (prefill):
+//   2. hist          grid (chunks of 64 tokens): per-chunk expert histograms
+//   3. scan          1 CTA: chunk prefix per expert, counts, offsets, padded offsets
+//   4. slots         grid (chunks): slot ranks in ascending pair order
+// Every output is run-to-run deterministic: integer atomics only count, and
+// ranks never depend on the order of atomics. Results of the previous launch
+// are read through L2 (ld.global.cg), because with programmatic dependent
+// launch a kernel can start before its predecessor ends.
 #include <climits>
 
 #include "common.cuh"
@@ -25,6 +33,8 @@ namespace fp4moe {
 namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
+constexpr int kExpertsPerCta = 64;   // logits_topk: 8 warps x 8 experts
+constexpr int kSmallPairs = 4096;    // single-CTA layout up to this many (token, k) pairs
 
 // Error-free transformation a + b = s + e (Knuth's two-sum).
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
@@ -33,39 +43,113 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
-__device__ __forceinline__ void acc_pair(float& s, float& c, uint32_t xw, uint32_t ww) {
-  // bf16 x bf16 products are exact in fp32 (8-bit significands)
-  float e0, e1, s0;
-  const float p0 = __fmul_rn(bf16_lo(xw), bf16_lo(ww));
-  const float p1 = __fmul_rn(bf16_hi(xw), bf16_hi(ww));
-  two_sum(s, p0, s0, e0);
-  two_sum(s0, p1, s, e1);
-  c = __fadd_rn(c, __fadd_rn(e0, e1));
+// Add the exact bf16 x bf16 product to the compensated pair (s, c).
+__device__ __forceinline__ void acc_prod(float& s, float& c, float xv, float wv) {
+  float e;
+  two_sum(s, __fmul_rn(xv, wv), s, e);  // the product is exact in fp32 (8-bit significands)
+  c = __fadd_rn(c, e);
 }
 
-// One warp per (token, expert), 4 experts per warp, 8 warps per CTA.
-__global__ void __launch_bounds__(256) router_logits_kernel(int H, int E, const uint16_t* __restrict__ x,
-                                                            const uint16_t* __restrict__ wr,
-                                                            const float* __restrict__ bias,
-                                                            float* __restrict__ logits) {
-  const int t = blockIdx.y;
+// Top-k of one token's E logits by one warp: descending logit, ties to the
+// lower expert id. Then the renormalised softmax weights (lane 0 writes).
+template <int MAXV>
+__device__ void warp_topk(const float* __restrict__ l, int E, int k, int32_t* ids_out, float* w_out, uint32_t* err) {
+  const int lane = threadIdx.x & 31;
+  float v[MAXV];
+  uint32_t taken = 0;
+#pragma unroll
+  for (int q = 0; q < MAXV; ++q) {
+    const int e = q * 32 + lane;
+    v[q] = (e < E) ? __ldcg(l + e) : 0.0f;
+    if (e >= E) taken |= 1u << q;
+  }
+  float sel_v[kMaxTopK];
+  int sel_e[kMaxTopK];
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int be = INT_MAX;
+#pragma unroll
+    for (int q = 0; q < MAXV; ++q) {
+      const int e = q * 32 + lane;
+      if (!((taken >> q) & 1u) && (v[q] > bv || (v[q] == bv && e < be))) {
+        bv = v[q];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(kFull, bv, off);
+      const int oe = __shfl_xor_sync(kFull, be, off);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if (be >= E) {  // only possible with NaN logits
+      if (lane == 0) raise_error(err, FP4MOE_ERR_EXPERT_ID);
+      be = 0;
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    sel_v[j] = bv;
+    sel_e[j] = be;
+  }
+  if (lane == 0) {
+    const float lmax = sel_v[0];
+    float ex[kMaxTopK];
+    float sum = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      ex[j] = expf(__fsub_rn(sel_v[j], lmax));
+      sum = __fadd_rn(sum, ex[j]);
+    }
+    for (int j = 0; j < k; ++j) {
+      ids_out[j] = sel_e[j];
+      w_out[j] = __fdiv_rn(ex[j], sum);
+    }
+  }
+}
+
+// grid (T, ceil(E/64)), 256 threads. Warp w of CTA (t, g) computes the logits
+// of experts 64g + 8w .. 64g + 8w + 7 for token t. Each lane covers H/32
+// elements in a fixed order, with two independent compensated accumulators.
+// A fixed butterfly then combines the lanes.
+template <int MAXV>
+__global__ void __launch_bounds__(256) logits_topk_kernel(int T, int H, int E, int k, const uint16_t* __restrict__ x,
+                                                          const uint16_t* __restrict__ wr,
+                                                          const float* __restrict__ bias, float* __restrict__ logits,
+                                                          int32_t* __restrict__ cnt, int32_t* __restrict__ ids_out,
+                                                          float* __restrict__ w_out, uint32_t* err) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int s_last;
+  const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
   const int nit = H >> 8;  // 256 elements per warp iteration
 #pragma unroll 1
-  for (int q = 0; q < 4; ++q) {
-    const int e = blockIdx.x * 32 + warp * 4 + q;
+  for (int q = 0; q < 8; ++q) {
+    const int e = blockIdx.y * kExpertsPerCta + warp * 8 + q;
     if (e >= E) break;
     const uint4* wrow = reinterpret_cast<const uint4*>(wr + (size_t)e * H);
-    float s = 0.0f, c = 0.0f;
-#pragma unroll 4
+    float s0 = 0.0f, c0 = 0.0f, s1 = 0.0f, c1 = 0.0f;
+#pragma unroll 2
     for (int it = 0; it < nit; ++it) {
       const uint4 xv = __ldg(xr + it * 32 + lane);
       const uint4 wv = __ldg(wrow + it * 32 + lane);
-      acc_pair(s, c, xv.x, wv.x);
-      acc_pair(s, c, xv.y, wv.y);
-      acc_pair(s, c, xv.z, wv.z);
-      acc_pair(s, c, xv.w, wv.w);
+      acc_prod(s0, c0, bf16_lo(xv.x), bf16_lo(wv.x));
+      acc_prod(s1, c1, bf16_hi(xv.x), bf16_hi(wv.x));
+      acc_prod(s0, c0, bf16_lo(xv.y), bf16_lo(wv.y));
+      acc_prod(s1, c1, bf16_hi(xv.y), bf16_hi(wv.y));
+      acc_prod(s0, c0, bf16_lo(xv.z), bf16_lo(wv.z));
+      acc_prod(s1, c1, bf16_hi(xv.z), bf16_hi(wv.z));
+      acc_prod(s0, c0, bf16_lo(xv.w), bf16_lo(wv.w));
+      acc_prod(s1, c1, bf16_hi(xv.w), bf16_hi(wv.w));
+    }
+    float s, c;
+    {
+      float e0;
+      two_sum(s0, s1, s, e0);
+      c = __fadd_rn(__fadd_rn(c0, c1), e0);
     }
     // fixed butterfly; every lane ends with the same (s, c)
 #pragma unroll
@@ -83,78 +167,17 @@ __global__ void __launch_bounds__(256) router_logits_kernel(int H, int E, const 
       logits[(size_t)t * E + e] = l;
     }
   }
-}
-
-// Top-k per token (one warp per token), renormalised softmax weights, and the
-// per-chunk expert histogram.
-template <int MAXV>
-__global__ void __launch_bounds__(256) topk_hist_kernel(int T, int E, int k, const float* __restrict__ logits,
-                                                        int32_t* __restrict__ ids_out, float* __restrict__ w_out,
-                                                        int32_t* __restrict__ hist, uint32_t* err) {
-  __shared__ int sh[kMaxExperts];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
+  // the last CTA of this token to arrive takes the top-k (threadfence-reduction pattern)
+  __threadfence();
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#pragma unroll 1
-  for (int i = 0; i < kRouteChunk / 8; ++i) {
-    const int t = blockIdx.x * kRouteChunk + i * 8 + warp;
-    if (t >= T) break;
-    float v[MAXV];
-    uint32_t taken = 0;
-#pragma unroll
-    for (int q = 0; q < MAXV; ++q) {
-      const int e = q * 32 + lane;
-      v[q] = (e < E) ? logits[(size_t)t * E + e] : 0.0f;
-      if (e >= E) taken |= 1u << q;
-    }
-    float sel_v[kMaxTopK];
-    int sel_e[kMaxTopK];
-#pragma unroll 1
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int be = INT_MAX;
-#pragma unroll
-      for (int q = 0; q < MAXV; ++q) {
-        const int e = q * 32 + lane;
-        if (!((taken >> q) & 1u) && (v[q] > bv || (v[q] == bv && e < be))) {
-          bv = v[q];
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(kFull, bv, off);
-        const int oe = __shfl_xor_sync(kFull, be, off);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if (be >= E) {  // only possible with NaN logits
-        if (lane == 0) raise_error(err, FP4MOE_ERR_EXPERT_ID);
-        be = 0;
-      }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      sel_v[j] = bv;
-      sel_e[j] = be;
-    }
-    if (lane == 0) {
-      const float lmax = sel_v[0];
-      float ex[kMaxTopK];
-      float sum = 0.0f;
-      for (int j = 0; j < k; ++j) {
-        ex[j] = expf(__fsub_rn(sel_v[j], lmax));
-        sum = __fadd_rn(sum, ex[j]);
-      }
-      for (int j = 0; j < k; ++j) {
-        ids_out[(size_t)t * k + j] = sel_e[j];
-        w_out[(size_t)t * k + j] = __fdiv_rn(ex[j], sum);
-        atomicAdd(&sh[sel_e[j]], 1);
-      }
-    }
+  if (threadIdx.x == 0) s_last = (atomicAdd(cnt + t, 1) == (int)gridDim.y - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (warp == 0) {
+    warp_topk<MAXV>(logits + (size_t)t * E, E, k, ids_out + (size_t)t * k, w_out + (size_t)t * k, err);
+    if (lane == 0) cnt[t] = 0;  // ready for the next call
   }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(size_t)blockIdx.x * E + e] = sh[e];
 }
 
 __device__ __forceinline__ int block_inclusive_scan(int v, int* s_warp) {
@@ -181,45 +204,126 @@ __device__ __forceinline__ int block_inclusive_scan(int v, int* s_warp) {
   return r;
 }
 
-// One CTA of 1024 threads, thread e = expert e.
-__global__ void __launch_bounds__(1024) scan_kernel(int E, int nchunks, int cap, int32_t* __restrict__ hist,
-                                                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                                                    int32_t* __restrict__ poff, int32_t* __restrict__ pair_of_row,
-                                                    uint32_t* err) {
-  __shared__ int s_warp[32];
+// Counts, inclusive offsets and padded offsets for expert e = threadIdx.x
+// (1024 threads), given its count c; pads its padding rows with -1.
+// Returns the first row of the expert's block in `start`.
+__device__ __forceinline__ void offsets_and_pads(int E, int cap, int c, int* s_warp, int32_t* counts, int32_t* offsets,
+                                                 int32_t* poff, int32_t* pair_of_row, uint32_t* err, int& start) {
   const int e = threadIdx.x;
-  int c = 0;
-  if (e < E) {
-    for (int b = 0; b < nchunks; ++b) {  // exclusive prefix over chunks, in place
-      const int h = hist[(size_t)b * E + e];
-      hist[(size_t)b * E + e] = c;
-      c += h;
-    }
-  }
   const int P = (c + 127) & ~127;
   const int oc = block_inclusive_scan(c, s_warp);
   const int op = block_inclusive_scan(P, s_warp);
+  start = op - P;
   if (e < E) {
     counts[e] = c;
     offsets[e] = oc;
     poff[e] = op;
-    const int start = op - P;
     for (int r = start + c; r < op && r < cap; ++r) pair_of_row[r] = -1;
     if (e == E - 1 && op > cap) raise_error(err, FP4MOE_ERR_CAPACITY);
   }
 }
 
-// Slot of every pair in ascending pair order: warp 0 walks its chunk 32 pairs
-// at a time, and lanes that share an expert rank themselves by lane order.
+// Decode-sized layout in one CTA of 1024 threads: histogram, offsets, pads,
+// and slots in ascending pair order (warp 0 walks the pairs 32 at a time;
+// lanes sharing an expert rank themselves by lane order).
+__global__ void __launch_bounds__(1024) layout_small_kernel(int npairs, int E, int cap,
+                                                            const int32_t* __restrict__ ids,
+                                                            int32_t* __restrict__ counts,
+                                                            int32_t* __restrict__ offsets,
+                                                            int32_t* __restrict__ poff,
+                                                            int32_t* __restrict__ slot_of_pair,
+                                                            int32_t* __restrict__ pair_of_row, uint32_t* err) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int s_cnt[kMaxExperts];
+  __shared__ int s_base[kMaxExperts];
+  __shared__ int s_warp[32];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
+    const int e = __ldcg(ids + p);
+    if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+    else raise_error(err, FP4MOE_ERR_EXPERT_ID);
+  }
+  __syncthreads();
+  const int c = (threadIdx.x < E) ? s_cnt[threadIdx.x] : 0;
+  int start;
+  offsets_and_pads(E, cap, c, s_warp, counts, offsets, poff, pair_of_row, err, start);
+  if (threadIdx.x < E) s_base[threadIdx.x] = start;
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  for (int pb = 0; pb < npairs; pb += 32) {
+    const int p = pb + lane;
+    int e = (p < npairs) ? __ldcg(ids + p) : -1;
+    if (e >= E) e = -1;
+    const unsigned peers = __match_any_sync(kFull, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (e >= 0) {
+      const int slot = s_base[e] + rank;
+      slot_of_pair[p] = slot;
+      if (slot < cap) pair_of_row[slot] = p;
+      else raise_error(err, FP4MOE_ERR_CAPACITY);
+    }
+    __syncwarp();
+    if (e >= 0 && rank == 0) s_base[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// Per-chunk expert histograms (64 tokens per chunk), for large T.
+__global__ void __launch_bounds__(256) hist_kernel(int T, int E, int k, const int32_t* __restrict__ ids,
+                                                   int32_t* __restrict__ hist, uint32_t* err) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int sh[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
+  __syncthreads();
+  const int p0 = blockIdx.x * kRouteChunk * k;
+  const int p1 = min(T, (blockIdx.x + 1) * kRouteChunk) * k;
+  for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
+    const int e = __ldcg(ids + p);
+    if (e >= 0 && e < E) atomicAdd(&sh[e], 1);
+    else raise_error(err, FP4MOE_ERR_EXPERT_ID);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(size_t)blockIdx.x * E + e] = sh[e];
+}
+
+// One CTA of 1024 threads, thread e = expert e: exclusive prefix of the chunk
+// histograms (in place), then counts, offsets, padded offsets and pads.
+__global__ void __launch_bounds__(1024) scan_kernel(int E, int nchunks, int cap, int32_t* __restrict__ hist,
+                                                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                    int32_t* __restrict__ poff, int32_t* __restrict__ pair_of_row,
+                                                    uint32_t* err) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int s_warp[32];
+  const int e = threadIdx.x;
+  int c = 0;
+  if (e < E) {
+    for (int b = 0; b < nchunks; ++b) {
+      const int h = __ldcg(hist + (size_t)b * E + e);
+      hist[(size_t)b * E + e] = c;
+      c += h;
+    }
+  }
+  int start;
+  offsets_and_pads(E, cap, c, s_warp, counts, offsets, poff, pair_of_row, err, start);
+}
+
+// Slot of every pair of one 64-token chunk, in ascending pair order.
 __global__ void __launch_bounds__(256) slots_kernel(int T, int E, int k, int cap, const int32_t* __restrict__ ids,
                                                     const int32_t* __restrict__ counts,
                                                     const int32_t* __restrict__ poff,
                                                     const int32_t* __restrict__ chunk_base,
                                                     int32_t* __restrict__ slot_of_pair,
                                                     int32_t* __restrict__ pair_of_row, uint32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int base[kMaxExperts];
   for (int e = threadIdx.x; e < E; e += blockDim.x)
-    base[e] = chunk_base[(size_t)blockIdx.x * E + e] + (poff[e] - ((counts[e] + 127) & ~127));
+    base[e] = __ldcg(chunk_base + (size_t)blockIdx.x * E + e) + (__ldcg(poff + e) - ((__ldcg(counts + e) + 127) & ~127));
   __syncthreads();
   if (threadIdx.x >= 32) return;
   const int lane = threadIdx.x;
@@ -227,11 +331,8 @@ __global__ void __launch_bounds__(256) slots_kernel(int T, int E, int k, int cap
   const int p1 = min(T, (blockIdx.x + 1) * kRouteChunk) * k;
   for (int pb = p0; pb < p1; pb += 32) {
     const int p = pb + lane;
-    int e = (p < p1) ? ids[p] : -1;
-    if (p < p1 && (e < 0 || e >= E)) {
-      raise_error(err, FP4MOE_ERR_EXPERT_ID);
-      e = -1;
-    }
+    int e = (p < p1) ? __ldcg(ids + p) : -1;
+    if (e >= E) e = -1;
     const unsigned peers = __match_any_sync(kFull, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
     if (e >= 0) {
@@ -247,9 +348,10 @@ __global__ void __launch_bounds__(256) slots_kernel(int T, int E, int k, int cap
 }
 
 template <int MAXV>
-void launch_topk(int nchunks, cudaStream_t st, int T, int E, int k, const float* logits, int32_t* ids, float* w,
-                 int32_t* hist, uint32_t* err) {
-  topk_hist_kernel<MAXV><<<nchunks, 256, 0, st>>>(T, E, k, logits, ids, w, hist, err);
+cudaError_t launch_logits_topk(int T, int H, int E, int k, const uint16_t* x, const uint16_t* wr, const float* bias,
+                               float* logits, int32_t* cnt, int32_t* ids, float* w, uint32_t* err, cudaStream_t st) {
+  return launch_pdl(logits_topk_kernel<MAXV>, dim3(T, (E + kExpertsPerCta - 1) / kExpertsPerCta), dim3(256), 0, st,
+                    T, H, E, k, x, wr, bias, logits, cnt, ids, w, err);
 }
 
 }  // namespace
@@ -257,24 +359,36 @@ void launch_topk(int nchunks, cudaStream_t st, int T, int E, int k, const float*
 fp4moe_status route_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
                            const float* bias, float* logits, int32_t* ids, float* w, int32_t* counts,
                            int32_t* offsets, int32_t* poff, int32_t* slot_of_pair, int32_t* pair_of_row,
-                           int32_t* hist, uint32_t* err, cudaStream_t st) {
+                           int32_t* hist, int32_t* cnt, uint32_t* err, cudaStream_t st) {
   const int E = cfg.num_experts, H = cfg.hidden, k = cfg.top_k;
   const int cap = (int)capacity_rows(cfg, T);
-  const int nchunks = (T + kRouteChunk - 1) / kRouteChunk;
+  const int npairs = T * k;
+  cudaError_t r = cudaSuccess;
   if (T > 0) {
-    router_logits_kernel<<<dim3((E + 31) / 32, T), 256, 0, st>>>(H, E, x, router_w, bias, logits);
     const int maxv = (E + 31) / 32;
-    if (maxv <= 1) launch_topk<1>(nchunks, st, T, E, k, logits, ids, w, hist, err);
-    else if (maxv <= 2) launch_topk<2>(nchunks, st, T, E, k, logits, ids, w, hist, err);
-    else if (maxv <= 4) launch_topk<4>(nchunks, st, T, E, k, logits, ids, w, hist, err);
-    else if (maxv <= 8) launch_topk<8>(nchunks, st, T, E, k, logits, ids, w, hist, err);
-    else if (maxv <= 16) launch_topk<16>(nchunks, st, T, E, k, logits, ids, w, hist, err);
-    else launch_topk<32>(nchunks, st, T, E, k, logits, ids, w, hist, err);
+    if (maxv <= 1) r = launch_logits_topk<1>(T, H, E, k, x, router_w, bias, logits, cnt, ids, w, err, st);
+    else if (maxv <= 2) r = launch_logits_topk<2>(T, H, E, k, x, router_w, bias, logits, cnt, ids, w, err, st);
+    else if (maxv <= 4) r = launch_logits_topk<4>(T, H, E, k, x, router_w, bias, logits, cnt, ids, w, err, st);
+    else if (maxv <= 8) r = launch_logits_topk<8>(T, H, E, k, x, router_w, bias, logits, cnt, ids, w, err, st);
+    else if (maxv <= 16) r = launch_logits_topk<16>(T, H, E, k, x, router_w, bias, logits, cnt, ids, w, err, st);
+    else r = launch_logits_topk<32>(T, H, E, k, x, router_w, bias, logits, cnt, ids, w, err, st);
+    if (r != cudaSuccess) return FP4MOE_CUDA_ERROR;
   }
-  scan_kernel<<<1, 1024, 0, st>>>(E, nchunks, cap, hist, counts, offsets, poff, pair_of_row, err);
-  if (T > 0)
-    slots_kernel<<<nchunks, 256, 0, st>>>(T, E, k, cap, ids, counts, poff, hist, slot_of_pair, pair_of_row, err);
-  return cudaGetLastError() == cudaSuccess ? FP4MOE_OK : FP4MOE_CUDA_ERROR;
+  if (npairs <= kSmallPairs) {
+    r = launch_pdl(layout_small_kernel, dim3(1), dim3(1024), 0, st, npairs, E, cap, (const int32_t*)ids, counts,
+                   offsets, poff, slot_of_pair, pair_of_row, err);
+  } else {
+    const int nchunks = (T + kRouteChunk - 1) / kRouteChunk;
+    r = launch_pdl(hist_kernel, dim3(nchunks), dim3(256), 0, st, T, E, k, (const int32_t*)ids, hist, err);
+    if (r == cudaSuccess)
+      r = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, st, E, nchunks, cap, hist, counts, offsets, poff,
+                     pair_of_row, err);
+    if (r == cudaSuccess)
+      r = launch_pdl(slots_kernel, dim3(nchunks), dim3(256), 0, st, T, E, k, cap, (const int32_t*)ids,
+                     (const int32_t*)counts, (const int32_t*)poff, (const int32_t*)hist, slot_of_pair, pair_of_row,
+                     err);
+  }
+  return r == cudaSuccess ? FP4MOE_OK : FP4MOE_CUDA_ERROR;
 }
 
 }  // namespace fp4moe

@@ -148,7 +148,8 @@ fp4moe_status fp4moe_weight_bytes(const fp4moe_config* cfg, size_t* w1_codes, si
 
 /*
  * moe_route: router logits, softmax top-k, per-expert counts, offsets and
- * 128-row-padded slots.
+ * 128-row-padded slots. Hot-path calls launch their kernels with programmatic
+ * dependent launch, so consecutive kernels overlap their launch latency.
  *   l[t,e] = RN_f32(sum_h x[t,h]*router_w[e,h]) (+ router_bias[e] in fp32).
  *     The sum is an fp32 compensated (two-sum) reduction in a fixed order, so
  *     it equals the exact sum rounded once except within about an ulp.
@@ -172,10 +173,10 @@ fp4moe_status moe_route(const fp4moe_config* cfg, int32_t T, const uint16_t* x, 
                         int32_t* pair_of_row, void* ws, fp4moe_stream_t stream);
 
 /*
- * moe_quantize_scatter: L1 activation quantisation into slot order. Each
- * row r < R gets NVFP4(x[pair_of_row[r]/k]) under the global scale *gs1.
- * Codes go to a1_fp4 [CAP][H/2] and swizzled scales to a1_sf
- * [CAP*H/16 bytes]. Padding rows are left untouched.
+ * moe_quantize_scatter: L1 activation quantisation into slot order. Row
+ * slot_of_pair[t*k + j] gets NVFP4(x[t]) under the global scale *gs1, for
+ * every token t and every j < k. Codes go to a1_fp4 [CAP][H/2] and swizzled
+ * scales to a1_sf [CAP*H/16 bytes]. Padding rows are left untouched.
  * Per 16-element block, in IEEE fp32 with RNE:
  *   a = max|v|; s = RN(RN(a/6)*g); sf = E4M3_satfinite(s);
  *   inv = sf ? RN(g/sf) : 0; q = E2M1_satfinite(RN(v*inv)).
@@ -183,8 +184,8 @@ fp4moe_status moe_route(const fp4moe_config* cfg, int32_t T, const uint16_t* x, 
  * _assemble_scales_cudagraph_safe), "Bug 1" and "Bug 14".
  */
 fp4moe_status moe_quantize_scatter(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const float* gs1,
-                                   const int32_t* padded_offsets, const int32_t* pair_of_row, uint8_t* a1_fp4,
-                                   uint8_t* a1_sf, void* ws, fp4moe_stream_t stream);
+                                   const int32_t* slot_of_pair, uint8_t* a1_fp4, uint8_t* a1_sf, void* ws,
+                                   fp4moe_stream_t stream);
 
 /*
  * moe_grouped_gemm_w1_swiglu: for every padded row r of expert e,

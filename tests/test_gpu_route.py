@@ -99,10 +99,8 @@ def test_quantize_scatter_bit_exact(wl, T):
     gs1 = nvfp4.global_scale(np.abs(sg.bf16_bits_to_f32(sg.activations_bf16(wl, sg.WARMUP_SEED))).max())
     a1 = torch.full((cap * wl.H // 2,), 0xAB, dtype=torch.uint8, device="cuda")
     a1sf = torch.full((cap * wl.H // 16,), 0xCD, dtype=torch.uint8, device="cuda")
-    poff = torch.from_numpy(g["poff"]).cuda()
-    por = torch.from_numpy(g["por"]).cuda()
-    api.moe_quantize_scatter(cfg, T, x, torch.tensor([gs1], dtype=torch.float32, device="cuda"), poff, por, a1, a1sf,
-                             ws)
+    slot = torch.from_numpy(g["slot"]).cuda()
+    api.moe_quantize_scatter(cfg, T, x, torch.tensor([gs1], dtype=torch.float32, device="cuda"), slot, a1, a1sf, ws)
     torch.cuda.synchronize()
     R = int(g["poff"][-1])
     codes = a1.cpu().numpy().reshape(cap, wl.H // 2)[:R]
