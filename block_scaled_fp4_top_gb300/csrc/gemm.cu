@@ -75,7 +75,7 @@ constexpr uint32_t SFB_STAGE_COLS = 4 * ATOMS;  // B scales of one ring stage
 // per 64-element K atom, all of K) at SFA_COL = 128 nacc; B scales of ring stage
 // s: 32 columns at SFA_COL + K/16 + 32 s. nacc is 2 when that fits, else 1.
 static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(SMEM_BYTES + 4 * kMaxExperts + 64 <= 232448, "shared memory budget (dynamic + static)");
 constexpr int kMaxResidentK = (TMEM_COLS - ACC_COLS - SFB_STAGE_COLS * STAGES) * 16;  // 4608 with one accumulator
 
 struct Params {
@@ -100,14 +100,15 @@ struct Tile {
 };
 
 // Tile tau in (m-tile, n-tile) order; the m-tile's expert is
-// searchsorted(padded_offsets, first row, right=True).
-__device__ __forceinline__ Tile map_tile(int tau, const int32_t* __restrict__ poff, int E, int NT) {
+// searchsorted(padded_offsets, first row, right=True). `poff` is the CTA's
+// shared-memory copy of the padded offsets.
+__device__ __forceinline__ Tile map_tile(int tau, const int* poff, int E, int NT) {
   const int mt = tau / NT;
   const int row = mt * BM;
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
-    if (__ldcg(poff + mid) > row) hi = mid;
+    if (poff[mid] > row) hi = mid;
     else lo = mid + 1;
   }
   return Tile{lo, tau - mt * NT, mt};
@@ -145,6 +146,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const Params prm) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
+  __shared__ int s_poff[kMaxExperts];
 
   pdl_wait();  // the routing / quantisation results of the previous launch are needed from here on
   pdl_trigger();
@@ -163,6 +165,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t bar_tempty = bar_tfull + 16;         // 2 x 8 bytes
   const uint32_t bar_drain = bar_tempty + 16;
 
+  for (int e = threadIdx.x; e < E; e += THREADS) s_poff[e] = __ldcg(prm.poff + e);
   if (warp == 0) {
     tmem_alloc(smem_u32(&s_tmem), TMEM_COLS);
     tmem_relinquish();
@@ -201,7 +204,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     Tile pt{0, 0, 0};
     auto prefetch = [&](int j) {
       const int kb = j % KB;
-      if (kb == 0 || j == 0) pt = map_tile(tau0 + j / KB, prm.poff, E, NT);
+      if (kb == 0 || j == 0) pt = map_tile(tau0 + j / KB, s_poff, E, NT);
       const size_t blk = (size_t)(pt.e * NT + pt.nt);
       const int nblk = min(HALVES, wblocks - kb * HALVES);
       bulk_prefetch_l2(prm.b_codes + (blk * wblocks + (size_t)kb * HALVES) * HALF_BYTES, nblk * HALF_BYTES);
@@ -212,7 +215,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int it = 0, prev_mt = -1;
     bool ok = true;
     for (int tau = tau0; tau < tau1 && ok; ++tau) {
-      const Tile t = map_tile(tau, prm.poff, E, NT);
+      const Tile t = map_tile(tau, s_poff, E, NT);
       const bool new_a = (t.mt != prev_mt);  // A scales go to TMEM once per m-tile
       prev_mt = t.mt;
       const int a_row = t.mt * BM;
@@ -253,7 +256,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t ph = 0;
     bool ok = true;
     for (int tau = tau0; tau < tau1 && ok; ++tau, ++tl) {
-      const Tile t = map_tile(tau, prm.poff, E, NT);
+      const Tile t = map_tile(tau, s_poff, E, NT);
       const bool new_a = (t.mt != prev_mt);
       prev_mt = t.mt;
       const int b = tl % nacc;
@@ -324,7 +327,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ epilogue
     int tl = 0;
     for (int tau = tau0; tau < tau1; ++tau, ++tl) {
-      const Tile t = map_tile(tau, prm.poff, E, NT);
+      const Tile t = map_tile(tau, s_poff, E, NT);
       const int r = t.mt * BM + warp * 32 + lane;
       const int p = __ldcg(prm.pair_of_row + r);
       const bool any_real = __any_sync(0xFFFFFFFFu, p >= 0);
