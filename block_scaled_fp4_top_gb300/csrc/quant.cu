@@ -15,34 +15,32 @@
 namespace fp4moe {
 namespace {
 
-// One warp per token, 8 tokens per CTA. The token's row is quantised once
-// (each lane takes 16-element blocks lane, lane+32, ...) and written to its k
-// slot rows. Padding rows are never touched.
+// One thread per 16-element block: thread i quantises block i % (H/16) of
+// token i / (H/16) once and writes it to the token's k slot rows. Consecutive
+// threads cover consecutive blocks of a row, so loads and code stores are
+// contiguous. Padding rows are never touched.
 __global__ void __launch_bounds__(256) quant_scatter_kernel(int T, int H, int k, const uint16_t* __restrict__ x,
                                                             const float* __restrict__ gs1,
                                                             const int32_t* __restrict__ slot_of_pair,
                                                             uint8_t* __restrict__ a1, uint8_t* __restrict__ a1_sf) {
   pdl_wait();
   pdl_trigger();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
-  int rows[kMaxTopK];
-  for (int j = 0; j < k; ++j) rows[j] = __ldcg(slot_of_pair + (size_t)t * k + j);
   const int C = H >> 4;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)T * C) return;
+  const int t = (int)(i / C), b = (int)(i - (int64_t)t * C);
   const float g = __ldg(gs1);
-  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-  for (int b = lane; b < C; b += 32) {
-    const uint4 u0 = __ldg(src + 2 * b), u1 = __ldg(src + 2 * b + 1);
-    const float v[16] = {bf16_lo(u0.x), bf16_hi(u0.x), bf16_lo(u0.y), bf16_hi(u0.y), bf16_lo(u0.z), bf16_hi(u0.z),
-                         bf16_lo(u0.w), bf16_hi(u0.w), bf16_lo(u1.x), bf16_hi(u1.x), bf16_lo(u1.y), bf16_hi(u1.y),
-                         bf16_lo(u1.z), bf16_hi(u1.z), bf16_lo(u1.w), bf16_hi(u1.w)};
-    uint32_t lo, hi;
-    const uint32_t sf = quant_block16(v, g, lo, hi);
-    for (int j = 0; j < k; ++j) {
-      *reinterpret_cast<uint2*>(a1 + (size_t)rows[j] * (H >> 1) + b * 8) = make_uint2(lo, hi);
-      a1_sf[sf_offset(rows[j], b, C)] = (uint8_t)sf;
-    }
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H) + 2 * b;
+  const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
+  const float v[16] = {bf16_lo(u0.x), bf16_hi(u0.x), bf16_lo(u0.y), bf16_hi(u0.y), bf16_lo(u0.z), bf16_hi(u0.z),
+                       bf16_lo(u0.w), bf16_hi(u0.w), bf16_lo(u1.x), bf16_hi(u1.x), bf16_lo(u1.y), bf16_hi(u1.y),
+                       bf16_lo(u1.z), bf16_hi(u1.z), bf16_lo(u1.w), bf16_hi(u1.w)};
+  uint32_t lo, hi;
+  const uint32_t sf = quant_block16(v, g, lo, hi);
+  for (int j = 0; j < k; ++j) {
+    const int row = __ldcg(slot_of_pair + (size_t)t * k + j);
+    *reinterpret_cast<uint2*>(a1 + (size_t)row * (H >> 1) + b * 8) = make_uint2(lo, hi);
+    a1_sf[sf_offset(row, b, C)] = (uint8_t)sf;
   }
 }
 
@@ -137,8 +135,9 @@ inline fp4moe_status last_status() { return cudaGetLastError() == cudaSuccess ? 
 fp4moe_status quant_scatter_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const float* gs1,
                                    const int32_t* slot_of_pair, uint8_t* a1, uint8_t* a1_sf, cudaStream_t st) {
   if (T == 0) return FP4MOE_OK;
-  return launch_pdl(quant_scatter_kernel, dim3((T + 7) / 8), dim3(256), 0, st, T, cfg.hidden, cfg.top_k, x, gs1,
-                    slot_of_pair, a1, a1_sf) == cudaSuccess
+  const int64_t threads = (int64_t)T * (cfg.hidden / 16);
+  return launch_pdl(quant_scatter_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, st, T, cfg.hidden,
+                    cfg.top_k, x, gs1, slot_of_pair, a1, a1_sf) == cudaSuccess
              ? FP4MOE_OK
              : FP4MOE_CUDA_ERROR;
 }

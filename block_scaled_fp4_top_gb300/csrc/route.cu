@@ -9,8 +9,9 @@
 // expert slots ("Bug 14").
 //
 // Launches, each with a fixed grid chosen from the host-known T:
-//   1. logits_topk   grid (T, ceil(E/64)). Each CTA computes 64 logits of one
-//                    token, with a compensated fp32 dot product per expert. The
+//   1. logits_topk   grid (T, ceil(E/64)), 1024 threads. Each CTA computes 64
+//                    logits of one token, with a compensated fp32 dot product
+//                    per expert (4 H-quarters x 8 expert groups of warps). The
 //                    last CTA of the token to finish (an arrival counter)
 //                    takes the softmax top-k of all E logits.
 //   then, for T*k <= kSmallPairs (decode):
@@ -109,44 +110,50 @@ __device__ void warp_topk(const float* __restrict__ l, int E, int k, int32_t* id
   }
 }
 
-// grid (T, ceil(E/64)), 256 threads. Warp w of CTA (t, g) computes the logits
-// of experts 64g + 8w .. 64g + 8w + 7 for token t. Each lane covers H/32
-// elements in a fixed order, with two independent compensated accumulators.
-// A fixed butterfly then combines the lanes.
+// grid (T, ceil(E/64)), 1024 threads. Warp w of CTA (t, g) computes, for the
+// 8 experts 64g + 8(w % 8) .. +7, the compensated partial sum over H-quarter
+// w / 8. Inside the quarter each lane covers a fixed strided set of elements
+// with two independent compensated accumulators, and a fixed butterfly
+// combines the lanes. The 4 quarters are then summed in quarter order with
+// two-sums. The last CTA of the token to arrive takes the top-k.
 template <int MAXV>
-__global__ void __launch_bounds__(256) logits_topk_kernel(int T, int H, int E, int k, const uint16_t* __restrict__ x,
-                                                          const uint16_t* __restrict__ wr,
-                                                          const float* __restrict__ bias, float* __restrict__ logits,
-                                                          int32_t* __restrict__ cnt, int32_t* __restrict__ ids_out,
-                                                          float* __restrict__ w_out, uint32_t* err) {
+__global__ void __launch_bounds__(1024) logits_topk_kernel(int T, int H, int E, int k, const uint16_t* __restrict__ x,
+                                                           const uint16_t* __restrict__ wr,
+                                                           const float* __restrict__ bias, float* __restrict__ logits,
+                                                           int32_t* __restrict__ cnt, int32_t* __restrict__ ids_out,
+                                                           float* __restrict__ w_out, uint32_t* err) {
   pdl_wait();
   pdl_trigger();
+  __shared__ float s_part[4][kExpertsPerCta][2];
   __shared__ int s_last;
   const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = warp & 7, quarter = warp >> 3;
+  // 256 elements per warp iteration; quarter q takes iterations [q n / 4, (q + 1) n / 4) of n = H / 256
+  const int n_it = H >> 8;
+  const int it0 = quarter * n_it / 4, it1 = (quarter + 1) * n_it / 4;
   const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-  const int nit = H >> 8;  // 256 elements per warp iteration
 #pragma unroll 1
   for (int q = 0; q < 8; ++q) {
-    const int e = blockIdx.y * kExpertsPerCta + warp * 8 + q;
-    if (e >= E) break;
-    const uint4* wrow = reinterpret_cast<const uint4*>(wr + (size_t)e * H);
-    float s0 = 0.0f, c0 = 0.0f, s1 = 0.0f, c1 = 0.0f;
+    const int el = grp * 8 + q;  // expert index inside this CTA's 64
+    const int e = blockIdx.y * kExpertsPerCta + el;
+    float s = 0.0f, c = 0.0f;
+    if (e < E) {
+      const uint4* wrow = reinterpret_cast<const uint4*>(wr + (size_t)e * H);
+      float s0 = 0.0f, c0 = 0.0f, s1 = 0.0f, c1 = 0.0f;
 #pragma unroll 2
-    for (int it = 0; it < nit; ++it) {
-      const uint4 xv = __ldg(xr + it * 32 + lane);
-      const uint4 wv = __ldg(wrow + it * 32 + lane);
-      acc_prod(s0, c0, bf16_lo(xv.x), bf16_lo(wv.x));
-      acc_prod(s1, c1, bf16_hi(xv.x), bf16_hi(wv.x));
-      acc_prod(s0, c0, bf16_lo(xv.y), bf16_lo(wv.y));
-      acc_prod(s1, c1, bf16_hi(xv.y), bf16_hi(wv.y));
-      acc_prod(s0, c0, bf16_lo(xv.z), bf16_lo(wv.z));
-      acc_prod(s1, c1, bf16_hi(xv.z), bf16_hi(wv.z));
-      acc_prod(s0, c0, bf16_lo(xv.w), bf16_lo(wv.w));
-      acc_prod(s1, c1, bf16_hi(xv.w), bf16_hi(wv.w));
-    }
-    float s, c;
-    {
+      for (int it = it0; it < it1; ++it) {
+        const uint4 xv = __ldg(xr + it * 32 + lane);
+        const uint4 wv = __ldg(wrow + it * 32 + lane);
+        acc_prod(s0, c0, bf16_lo(xv.x), bf16_lo(wv.x));
+        acc_prod(s1, c1, bf16_hi(xv.x), bf16_hi(wv.x));
+        acc_prod(s0, c0, bf16_lo(xv.y), bf16_lo(wv.y));
+        acc_prod(s1, c1, bf16_hi(xv.y), bf16_hi(wv.y));
+        acc_prod(s0, c0, bf16_lo(xv.z), bf16_lo(wv.z));
+        acc_prod(s1, c1, bf16_hi(xv.z), bf16_hi(wv.z));
+        acc_prod(s0, c0, bf16_lo(xv.w), bf16_lo(wv.w));
+        acc_prod(s1, c1, bf16_hi(xv.w), bf16_hi(wv.w));
+      }
       float e0;
       two_sum(s0, s1, s, e0);
       c = __fadd_rn(__fadd_rn(c0, c1), e0);
@@ -162,6 +169,23 @@ __global__ void __launch_bounds__(256) logits_topk_kernel(int T, int H, int E, i
       c = __fadd_rn(__fadd_rn(c, co), ne);
     }
     if (lane == 0) {
+      s_part[quarter][el][0] = s;
+      s_part[quarter][el][1] = c;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < kExpertsPerCta) {
+    const int el = threadIdx.x;
+    const int e = blockIdx.y * kExpertsPerCta + el;
+    if (e < E) {
+      float s = s_part[0][el][0], c = s_part[0][el][1];
+#pragma unroll
+      for (int qq = 1; qq < 4; ++qq) {
+        float ns, ne;
+        two_sum(s, s_part[qq][el][0], ns, ne);
+        s = ns;
+        c = __fadd_rn(__fadd_rn(c, s_part[qq][el][1]), ne);
+      }
       float l = __fadd_rn(s, c);
       if (bias != nullptr) l = __fadd_rn(l, bias[e]);
       logits[(size_t)t * E + e] = l;
@@ -238,12 +262,17 @@ __global__ void __launch_bounds__(1024) layout_small_kernel(int npairs, int E, i
   __shared__ int s_cnt[kMaxExperts];
   __shared__ int s_base[kMaxExperts];
   __shared__ int s_warp[32];
+  __shared__ int s_ids[kSmallPairs];
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
   __syncthreads();
   for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
-    const int e = __ldcg(ids + p);
+    int e = __ldcg(ids + p);
     if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
-    else raise_error(err, FP4MOE_ERR_EXPERT_ID);
+    else {
+      raise_error(err, FP4MOE_ERR_EXPERT_ID);
+      e = -1;
+    }
+    s_ids[p] = e;
   }
   __syncthreads();
   const int c = (threadIdx.x < E) ? s_cnt[threadIdx.x] : 0;
@@ -255,8 +284,7 @@ __global__ void __launch_bounds__(1024) layout_small_kernel(int npairs, int E, i
   const int lane = threadIdx.x;
   for (int pb = 0; pb < npairs; pb += 32) {
     const int p = pb + lane;
-    int e = (p < npairs) ? __ldcg(ids + p) : -1;
-    if (e >= E) e = -1;
+    const int e = (p < npairs) ? s_ids[p] : -1;
     const unsigned peers = __match_any_sync(kFull, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
     if (e >= 0) {
@@ -350,7 +378,7 @@ __global__ void __launch_bounds__(256) slots_kernel(int T, int E, int k, int cap
 template <int MAXV>
 cudaError_t launch_logits_topk(int T, int H, int E, int k, const uint16_t* x, const uint16_t* wr, const float* bias,
                                float* logits, int32_t* cnt, int32_t* ids, float* w, uint32_t* err, cudaStream_t st) {
-  return launch_pdl(logits_topk_kernel<MAXV>, dim3(T, (E + kExpertsPerCta - 1) / kExpertsPerCta), dim3(256), 0, st,
+  return launch_pdl(logits_topk_kernel<MAXV>, dim3(T, (E + kExpertsPerCta - 1) / kExpertsPerCta), dim3(1024), 0, st,
                     T, H, E, k, x, wr, bias, logits, cnt, ids, w, err);
 }
 
