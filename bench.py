@@ -241,7 +241,8 @@ def run_ours(args, wl, rank, world):
         "roofline": {"kernel": "grouped_gemm_kernel<W1 SwiGLU requant>", "bound": "hbm", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": w1_bytes + act1, "traffic": None},
-        "gpu_launches": 8 * args.steps,
+        # route: logits_topk + layout_small (T*k <= 4096) or + hist, scan, slots; then quantise-scatter, W1, W2, combine
+        "gpu_launches": ((2 if T * k <= 4096 else 4) + 4) * args.steps,
         "e2e": {"value": tokens / (e2e_ms / args.steps * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2},
         "clocks": clk.summary(),

@@ -231,8 +231,11 @@ __device__ __forceinline__ int block_inclusive_scan(int v, int* s_warp) {
 // Counts, inclusive offsets and padded offsets for expert e = threadIdx.x
 // (1024 threads), given its count c; pads its padding rows with -1.
 // Returns the first row of the expert's block in `start`.
+// All padded rows [0, min(R, cap)) get -1 with coalesced stores; real rows
+// are overwritten by the slot pass that follows.
 __device__ __forceinline__ void offsets_and_pads(int E, int cap, int c, int* s_warp, int32_t* counts, int32_t* offsets,
                                                  int32_t* poff, int32_t* pair_of_row, uint32_t* err, int& start) {
+  __shared__ int s_R;
   const int e = threadIdx.x;
   const int P = (c + 127) & ~127;
   const int oc = block_inclusive_scan(c, s_warp);
@@ -242,9 +245,15 @@ __device__ __forceinline__ void offsets_and_pads(int E, int cap, int c, int* s_w
     counts[e] = c;
     offsets[e] = oc;
     poff[e] = op;
-    for (int r = start + c; r < op && r < cap; ++r) pair_of_row[r] = -1;
-    if (e == E - 1 && op > cap) raise_error(err, FP4MOE_ERR_CAPACITY);
   }
+  if (e == E - 1) {
+    s_R = op;
+    if (op > cap) raise_error(err, FP4MOE_ERR_CAPACITY);
+  }
+  __syncthreads();
+  const int R = min(s_R, cap);
+  for (int r = threadIdx.x; r < R; r += blockDim.x) pair_of_row[r] = -1;
+  __syncthreads();
 }
 
 // Decode-sized layout in one CTA of 1024 threads: histogram, offsets, pads,
