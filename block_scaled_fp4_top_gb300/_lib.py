@@ -33,6 +33,7 @@ SIGNATURES = {
     "fp4moe_weight_bytes": (c_i32, [CP, ctypes.POINTER(c_sz), ctypes.POINTER(c_sz), ctypes.POINTER(c_sz),
                                     ctypes.POINTER(c_sz)]),
     "moe_route": (c_i32, [CP, c_i32] + [c_vp] * 13),
+    "moe_route_noalloc": (c_i32, [CP, c_i32] + [c_vp] * 13),
     "moe_quantize_scatter": (c_i32, [CP, c_i32] + [c_vp] * 7),
     "moe_grouped_gemm_w1_swiglu": (c_i32, [CP, c_i32] + [c_vp] * 12),
     "moe_grouped_gemm_w2": (c_i32, [CP, c_i32] + [c_vp] * 10),

@@ -71,6 +71,17 @@ def moe_route(cfg, T, x, router_w, router_bias, logits_out, topk_ids, topk_w, co
                                  _p(slot_of_pair), _p(pair_of_row), _p(ws), _s(stream)), "moe_route")
 
 
+def moe_route_noalloc(cfg, T, x, router_w, router_bias, logits_out, topk_ids, topk_w, counts, offsets,
+                      padded_offsets, slot_of_pair, pair_of_row, err=None, stream=None):
+    """moe_route without a workspace: for callers that must not allocate device
+    memory. The library's own fixed scratch stands in for the workspace, so
+    calls on one device must not overlap (see include/fp4moe.h)."""
+    _check(_lib.load().moe_route_noalloc(ctypes.byref(cfg), T, _p(x), _p(router_w), _p(router_bias),
+                                         _p(logits_out), _p(topk_ids), _p(topk_w), _p(counts), _p(offsets),
+                                         _p(padded_offsets), _p(slot_of_pair), _p(pair_of_row), _p(err),
+                                         _s(stream)), "moe_route_noalloc")
+
+
 def moe_quantize_scatter(cfg, T, x, gs1, slot_of_pair, a1_fp4, a1_sf, ws, stream=None):
     _check(_lib.load().moe_quantize_scatter(ctypes.byref(cfg), T, _p(x), _p(gs1), _p(slot_of_pair), _p(a1_fp4),
                                             _p(a1_sf), _p(ws), _s(stream)), "moe_quantize_scatter")

@@ -8,6 +8,7 @@
 // hidden host syncs, allocations and device-value branches that a captured
 // step must not contain.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -101,6 +102,40 @@ WsLayout ws_layout(const fp4moe_config& c) {
   return L;
 }
 
+// Scratch of moe_route_noalloc, owned by the library image. Layout:
+// [0, 256) error word, then the per-token arrival counters of the logits
+// step, then the per-chunk expert histograms of the large-T layout.
+namespace {
+constexpr size_t kScratchErr = 0;
+constexpr size_t kScratchCnt = 256;
+constexpr size_t kScratchHist = kScratchCnt + 4 * (size_t)FP4MOE_NOALLOC_MAX_TOKENS;
+static_assert(kScratchHist + 4 * (size_t)FP4MOE_NOALLOC_MAX_EXPERTS *
+                                     ((FP4MOE_NOALLOC_MAX_TOKENS + kRouteChunk - 1) / kRouteChunk) ==
+                  FP4MOE_NOALLOC_SCRATCH_BYTES,
+              "scratch layout and its advertised size disagree");
+
+__device__ __align__(256) uint8_t g_route_scratch[FP4MOE_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+uint8_t* g_scratch_ptr[kMaxDevices];
+
+// Device address of the scratch on the current device. The first request on
+// a device looks it up with cudaGetSymbolAddress; later ones reuse it.
+fp4moe_status route_scratch(uint8_t** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP4MOE_CUDA_ERROR;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) return FP4MOE_CUDA_ERROR;
+    g_scratch_ptr[dev] = static_cast<uint8_t*>(p);
+  }
+  *out = g_scratch_ptr[dev];
+  return FP4MOE_OK;
+}
+}  // namespace
+
 }  // namespace fp4moe
 
 using namespace fp4moe;
@@ -156,6 +191,28 @@ fp4moe_status moe_route(const fp4moe_config* cfg, int32_t T, const uint16_t* x, 
   return route_launch(*cfg, T, x, router_w, router_bias, logits, topk_ids, topk_w, counts, offsets, padded_offsets,
                       slot_of_pair, pair_of_row, at<int32_t>(ws, L.hist), at<int32_t>(ws, L.cnt), err_word(ws),
                       (cudaStream_t)stream);
+}
+
+fp4moe_status moe_route_noalloc(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
+                                const float* router_bias, float* logits_out, int32_t* topk_ids, float* topk_w,
+                                int32_t* counts, int32_t* offsets, int32_t* padded_offsets, int32_t* slot_of_pair,
+                                int32_t* pair_of_row, uint32_t* err, fp4moe_stream_t stream) {
+  FP4_TRY(check_cfg(cfg));
+  FP4_TRY(check_T(cfg, T));
+  if (T > FP4MOE_NOALLOC_MAX_TOKENS || cfg->num_experts > FP4MOE_NOALLOC_MAX_EXPERTS) return FP4MOE_CAPACITY;
+  FP4_TRY(check_ptrs(x, router_w, logits_out, topk_ids, topk_w, counts, offsets, padded_offsets, slot_of_pair,
+                     pair_of_row));
+  FP4_TRY(check_opt(router_bias));
+  if ((reinterpret_cast<uintptr_t>(err) & 3u) != 0) return FP4MOE_MISALIGNED;
+  uint8_t* s = nullptr;
+  FP4_TRY(route_scratch(&s));
+  const cudaStream_t st = (cudaStream_t)stream;
+  // the arrival counters of this call's tokens and the scratch error word start at zero
+  if (cudaMemsetAsync(s, 0, kScratchCnt + 4 * (size_t)T, st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
+  return route_launch(*cfg, T, x, router_w, router_bias, logits_out, topk_ids, topk_w, counts, offsets,
+                      padded_offsets, slot_of_pair, pair_of_row, reinterpret_cast<int32_t*>(s + kScratchHist),
+                      reinterpret_cast<int32_t*>(s + kScratchCnt),
+                      err != nullptr ? err : reinterpret_cast<uint32_t*>(s + kScratchErr), st);
 }
 
 fp4moe_status moe_quantize_scatter(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const float* gs1,

@@ -173,6 +173,51 @@ fp4moe_status moe_route(const fp4moe_config* cfg, int32_t T, const uint16_t* x, 
                         int32_t* pair_of_row, void* ws, fp4moe_stream_t stream);
 
 /*
+ * moe_route_noalloc: moe_route for callers that cannot hand the library a
+ * workspace. None of the source pages describe such a call. It is here for
+ * embedders whose device memory is reserved in full up front and that forbid
+ * any later device allocation, and for C callers with no allocator of their
+ * own to size and own a workspace. cudaMalloc can also synchronise the whole
+ * device, which such callers must avoid. The call itself allocates nothing:
+ * no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * Its outputs and their meaning are those of moe_route, computed by the same
+ * kernels. What moe_route keeps in `ws` (the per-chunk expert histograms and
+ * the per-token arrival counters of the logits step) lives here in one
+ * library-owned scratch array in device memory, a file-scope __device__
+ * array of FP4MOE_NOALLOC_SCRATCH_BYTES bytes in the library image. The array
+ * bounds the sizes:
+ *   T <= FP4MOE_NOALLOC_MAX_TOKENS and num_experts <= FP4MOE_NOALLOC_MAX_EXPERTS,
+ * otherwise the call returns FP4MOE_CAPACITY before it enqueues anything.
+ * T must also respect cfg->max_tokens, as for moe_route.
+ *
+ * Differences from moe_route:
+ *   - logits_out is required (non-NULL): the scratch has no room for logits.
+ *   - err: optional device uint32. If non-NULL, FP4MOE_ERR_* bits are OR-ed
+ *     into it; the call never clears it. If NULL, errors go to a word in the
+ *     scratch that each call clears, so they are lost.
+ *
+ * Set-up and sharing:
+ *   - The first call made on each device (that device current) looks up the
+ *     array's device address with cudaGetSymbolAddress. It returns
+ *     FP4MOE_CUDA_ERROR if the lookup fails. Make that first call before any
+ *     stream capture begins.
+ *   - Every call on a device shares the one array. Each call clears, on
+ *     `stream`, the part that must start at zero (the arrival counters and
+ *     the scratch error word). Two calls whose work overlaps on the device
+ *     therefore race and corrupt each other's results. This happens with
+ *     different streams without an ordering between them, or with different
+ *     host threads. Order them on one stream or with events.
+ */
+#define FP4MOE_NOALLOC_MAX_TOKENS 8192
+#define FP4MOE_NOALLOC_MAX_EXPERTS 256
+#define FP4MOE_NOALLOC_SCRATCH_BYTES (256 + 4 * 8192 + 4 * 256 * (8192 / 64))
+fp4moe_status moe_route_noalloc(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
+                                const float* router_bias, float* logits_out, int32_t* topk_ids, float* topk_w,
+                                int32_t* counts, int32_t* offsets, int32_t* padded_offsets, int32_t* slot_of_pair,
+                                int32_t* pair_of_row, uint32_t* err, fp4moe_stream_t stream);
+
+/*
  * moe_quantize_scatter: L1 activation quantisation into slot order. Row
  * slot_of_pair[t*k + j] gets NVFP4(x[t]) under the global scale *gs1, for
  * every token t and every j < k. Codes go to a1_fp4 [CAP][H/2] and swizzled
