@@ -20,6 +20,7 @@ implementation of this layer.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -36,6 +37,29 @@ import synthgen as sg  # noqa: E402
 
 METRIC = "MoE layer tokens/s (DSV4 shape) + achieved HBM GB/s / FP4 tensor-pipe % on 1 GB300"
 FALLBACK_HBM_GBS = 6800.0
+
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one W1 GEMM launch per workload, from a
+# one-pass ncu capture summarised under profiles/. A figure holds only for the GEMM sources it was taken
+# with, so it is reported while their hash matches and as null otherwise.
+W1_TRAFFIC = {
+    # workload name: (bytes per launch, sha256 of the GEMM sources)
+    "dsv4_flash_decode_T64": (1953644800 + 3792384, "5ff759819ed38c92933ef9867a026851c67d95a3f113ea25088c8fb153463db1"),
+}
+GEMM_SOURCES = ("block_scaled_fp4_top_gb300/csrc/gemm.cu", "block_scaled_fp4_top_gb300/csrc/common.cuh")
+
+
+def gemm_sources_sha() -> str:
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def w1_traffic(workload: str):
+    t = W1_TRAFFIC.get(workload)
+    return float(t[0]) if t is not None and t[1] == gemm_sources_sha() else None
 
 
 def peaks():
@@ -240,7 +264,7 @@ def run_ours(args, wl, rank, world):
         "stages_us": {n: v * 1e3 for n, v in stage_ms.items()},
         "roofline": {"kernel": "grouped_gemm_kernel<W1 SwiGLU requant>", "bound": "hbm", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
-                     "algorithmic_bytes_per_launch": w1_bytes + act1, "traffic": None},
+                     "algorithmic_bytes_per_launch": w1_bytes + act1, "traffic": w1_traffic(wl.name)},
         # route: logits_topk + layout_small (T*k <= 4096) or + hist, scan, slots; then quantise-scatter, W1, W2, combine
         "gpu_launches": ((2 if T * k <= 4096 else 4) + 4) * args.steps,
         "e2e": {"value": tokens / (e2e_ms / args.steps * 1e-3), "unit": "tokens/s",

@@ -15,9 +15,15 @@
 //   warp 4      producer. A ring stage covers 512 elements of K. Its two
 //               consecutive 16 KB weight blocks arrive with one contiguous
 //               cp.async.bulk: the weights are stored pre-tiled and
-//               pre-swizzled (see fp4moe.h). The two 128-row activation
-//               blocks arrive by cp.async.bulk.tensor with the 128-byte
-//               swizzle, and the scale tiles by cp.async.bulk. Weight stages
+//               pre-swizzled (see fp4moe.h). The two activation blocks
+//               arrive by cp.async.bulk.tensor with the 128-byte swizzle,
+//               and the scale tiles by cp.async.bulk. Real rows lead every
+//               expert block, so an m-tile loads only its first 16, 32, 64
+//               or 128 rows: enough to cover the real ones. The rest of the
+//               128-row shared tile keeps stale bytes; MMA rows are
+//               independent and the epilogue drops those rows. At decode
+//               sizes (a few tokens per expert) this cuts the activation
+//               bytes re-read for every n-tile eightfold. Weight stages
 //               are also pulled into L2 a few stages ahead
 //               (cp.async.bulk.prefetch.L2). The shared-memory ring runs on
 //               across tile boundaries, so the weight stream never stops.
@@ -99,6 +105,12 @@ struct Tile {
   int e, nt, mt;
 };
 
+// Tensor maps of the activation codes whose boxes are 16, 32, 64 and 128 rows
+// high (128 bytes wide, 128-byte swizzle).
+struct AMaps {
+  CUtensorMap box[4];
+};
+
 // Tile tau in (m-tile, n-tile) order; the m-tile's expert is
 // searchsorted(padded_offsets, first row, right=True). `poff` is the CTA's
 // shared-memory copy of the padded offsets.
@@ -143,7 +155,7 @@ __device__ __forceinline__ void cta_range(int total, int& tau0, int& tau1) {
 
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const Params prm) {
+    grouped_gemm_kernel(const __grid_constant__ AMaps tmA, const Params prm) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_poff[kMaxExperts];
@@ -212,13 +224,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                        min(ATOMS, katoms_total - kb * ATOMS) * SF_TILE);
     };
     for (int j = 0; j < min(PREFETCH, n_stages); ++j) prefetch(j);
-    int it = 0, prev_mt = -1;
+    int it = 0, prev_mt = -1, a_box = 3;
     bool ok = true;
     for (int tau = tau0; tau < tau1 && ok; ++tau) {
       const Tile t = map_tile(tau, s_poff, E, NT);
       const bool new_a = (t.mt != prev_mt);  // A scales go to TMEM once per m-tile
       prev_mt = t.mt;
       const int a_row = t.mt * BM;
+      if (new_a) {
+        // the first padding row of the block bounds the rows this m-tile needs (rows < R are all written)
+        const int32_t* por = prm.pair_of_row + a_row;
+        const int p16 = __ldcg(por + 16), p32 = __ldcg(por + 32), p64 = __ldcg(por + 64);
+        a_box = p16 < 0 ? 0 : (p32 < 0 ? 1 : (p64 < 0 ? 2 : 3));
+      }
+      const uint32_t a_half = (uint32_t)(16 << a_box) * KBYTES;  // bytes of one activation block
       const uint8_t* bsrc = prm.b_codes + (size_t)(t.e * NT + t.nt) * wblocks * HALF_BYTES;
       const uint8_t* sfa = prm.a_sf + (size_t)t.mt * katoms_total * SF_TILE;
       const uint8_t* sfb = prm.b_sf + ((size_t)t.e * NT + t.nt) * katoms_total * SF_TILE;
@@ -233,10 +252,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int atoms = min(ATOMS, katoms_total - kb * ATOMS);
         const int halves = (atoms + 3) / 4;
         const uint32_t st = smem + s * STAGE_BYTES;
-        mbar_arrive_expect_tx(bar_full + 8 * s, 2 * halves * HALF_BYTES + (new_a ? 2 : 1) * atoms * SF_TILE);
+        mbar_arrive_expect_tx(bar_full + 8 * s,
+                              halves * (HALF_BYTES + a_half) + (new_a ? 2 : 1) * atoms * SF_TILE);
         bulk_load(st + A_BYTES, bsrc + (size_t)kb * B_BYTES, halves * HALF_BYTES, bar_full + 8 * s, pol_w);
         for (int h = 0; h < halves; ++h)
-          tma_load_2d(st + h * HALF_BYTES, &tmA, bar_full + 8 * s, (kb * HALVES + h) * KBYTES, a_row, pol_a);
+          tma_load_2d(st + h * HALF_BYTES, &tmA.box[a_box], bar_full + 8 * s, (kb * HALVES + h) * KBYTES, a_row,
+                      pol_a);
         if (new_a) bulk_load(st + SFA_OFF, sfa + (size_t)kb * ATOMS * SF_TILE, atoms * SF_TILE, bar_full + 8 * s, pol_a);
         bulk_load(st + SFB_OFF, sfb + (size_t)kb * ATOMS * SF_TILE, atoms * SF_TILE, bar_full + 8 * s, pol_w);
       }
@@ -492,8 +513,10 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
   prm.amax = amax;
   prm.o_pairs = o_pairs;
   prm.err = err;
-  CUtensorMap tmA;
-  if (!encode_u8_sw128(&tmA, a_codes, (uint64_t)prm.K / 2, (uint64_t)prm.cap, BM)) return FP4MOE_CUDA_ERROR;
+  AMaps tmA;
+  for (int b = 0; b < 4; ++b)
+    if (!encode_u8_sw128(&tmA.box[b], a_codes, (uint64_t)prm.K / 2, (uint64_t)prm.cap, 16u << b))
+      return FP4MOE_CUDA_ERROR;
   const int nsm = sm_count();
   if (nsm <= 0) return FP4MOE_CUDA_ERROR;
   const int max_tiles = (prm.cap / BM) * prm.NT;
