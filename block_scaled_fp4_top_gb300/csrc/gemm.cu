@@ -419,7 +419,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+}  // namespace
+
 // ------------------------------------------------------------ host side --
+namespace {
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -438,6 +441,8 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+}  // namespace
+
 // 2-D uint8 tensor [rows][inner_bytes], 128-byte-swizzled boxes of box_rows x 128 bytes.
 bool encode_u8_sw128(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
@@ -451,6 +456,7 @@ bool encode_u8_sw128(CUtensorMap* m, const void* base, uint64_t inner_bytes, uin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
 template <int MODE>
 bool configure_once() {
   static int ok = -1;
@@ -464,6 +470,8 @@ bool configure_once() {
   return ok == 1;
 }
 
+}  // namespace
+
 int sm_count() {
   static int counts[64] = {0};
   int dev = 0;
@@ -475,8 +483,6 @@ int sm_count() {
   }
   return counts[dev];
 }
-
-}  // namespace
 
 size_t tiled_weight_bytes(int32_t rows, int32_t K) { return (size_t)rows * (size_t)((K + 255) / 256) * KBYTES; }
 

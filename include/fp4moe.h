@@ -150,12 +150,18 @@ fp4moe_status fp4moe_weight_bytes(const fp4moe_config* cfg, size_t* w1_codes, si
  * moe_route: router logits, softmax top-k, per-expert counts, offsets and
  * 128-row-padded slots. Hot-path calls launch their kernels with programmatic
  * dependent launch, so consecutive kernels overlap their launch latency.
- *   l[t,e] = RN_f32(sum_h x[t,h]*router_w[e,h]) (+ router_bias[e] in fp32).
- *     The sum is an fp32 compensated (two-sum) reduction in a fixed order, so
- *     it equals the exact sum rounded once except within about an ulp.
+ *   l[t,e] = RN_f32(sum_h x[t,h]*router_w[e,h]) (+ router_bias[e] in fp32):
+ *     the exact sum rounded once, to within an ulp (an fp32 compensated
+ *     two-sum reduction in a fixed order).
  *   topk_ids[t,:]: the k largest l[t,:], in descending order; ties go to the
  *     lower expert id.
  *   topk_w[t,j] = exp(l_j - l_max) / sum_selected exp(l - l_max) (fp32).
+ *   The logits are found in two passes. A tensor-core pass gives every
+ *   l~[t,e] with a bound d[t,e] = 2^-12 |x_t| |w_e| + 2^-21 |l~|. Then every
+ *   expert whose interval [l~ - d, l~ + d] reaches the k-th largest lower
+ *   end gets the exact l above. So ids and weights are those of the exact
+ *   logits. logits_out[t,e] holds l for those candidate experts (always
+ *   including the k selected ones) and l~ for the others, and |l~ - l| <= d.
  *   counts, offsets, padded_offsets, slot_of_pair, pair_of_row as above.
  * Slot ranks are integer-deterministic: they do not depend on the order of
  * atomics.
@@ -183,7 +189,7 @@ fp4moe_status moe_route(const fp4moe_config* cfg, int32_t T, const uint16_t* x, 
  *
  * Its outputs and their meaning are those of moe_route, computed by the same
  * kernels. What moe_route keeps in `ws` (the per-chunk expert histograms and
- * the per-token arrival counters of the logits step) lives here in one
+ * the squared norms of the token and router rows) lives here in one
  * library-owned scratch array in device memory, a file-scope __device__
  * array of FP4MOE_NOALLOC_SCRATCH_BYTES bytes in the library image. The array
  * bounds the sizes:
@@ -203,15 +209,16 @@ fp4moe_status moe_route(const fp4moe_config* cfg, int32_t T, const uint16_t* x, 
  *     FP4MOE_CUDA_ERROR if the lookup fails. Make that first call before any
  *     stream capture begins.
  *   - Every call on a device shares the one array. Each call clears, on
- *     `stream`, the part that must start at zero (the arrival counters and
- *     the scratch error word). Two calls whose work overlaps on the device
+ *     `stream`, the part that must start at zero (the scratch error word);
+ *     every other byte it reads it has written first. Two calls whose work
+ *     overlaps on the device
  *     therefore race and corrupt each other's results. This happens with
  *     different streams without an ordering between them, or with different
  *     host threads. Order them on one stream or with events.
  */
 #define FP4MOE_NOALLOC_MAX_TOKENS 8192
 #define FP4MOE_NOALLOC_MAX_EXPERTS 256
-#define FP4MOE_NOALLOC_SCRATCH_BYTES (256 + 4 * 8192 + 4 * 256 * (8192 / 64))
+#define FP4MOE_NOALLOC_SCRATCH_BYTES (256 + 4 * 8192 + 4 * 256 + 4 * 256 * (8192 / 64))
 fp4moe_status moe_route_noalloc(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
                                 const float* router_bias, float* logits_out, int32_t* topk_ids, float* topk_w,
                                 int32_t* counts, int32_t* offsets, int32_t* padded_offsets, int32_t* slot_of_pair,
