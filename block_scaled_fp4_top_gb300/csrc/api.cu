@@ -83,7 +83,6 @@ WsLayout ws_layout(const fp4moe_config& c) {
   const size_t cap = capacity_rows(c, c.max_tokens);
   const size_t nchunks = std::max<size_t>(1, (Tm + kRouteChunk - 1) / kRouteChunk);
   L.hist = take(nchunks * E * 4);
-  L.nx2 = take(Tm * 4);
   L.nw2 = take(E * 4);
   L.logits = take(Tm * E * 4);
   L.ids = take(Tm * k * 4);
@@ -108,8 +107,7 @@ WsLayout ws_layout(const fp4moe_config& c) {
 // step, then the per-chunk expert histograms of the large-T layout.
 namespace {
 constexpr size_t kScratchErr = 0;
-constexpr size_t kScratchNx2 = 256;
-constexpr size_t kScratchNw2 = kScratchNx2 + 4 * (size_t)FP4MOE_NOALLOC_MAX_TOKENS;
+constexpr size_t kScratchNw2 = 256;
 constexpr size_t kScratchHist = kScratchNw2 + 4 * (size_t)FP4MOE_NOALLOC_MAX_EXPERTS;
 static_assert(kScratchHist + 4 * (size_t)FP4MOE_NOALLOC_MAX_EXPERTS *
                                      ((FP4MOE_NOALLOC_MAX_TOKENS + kRouteChunk - 1) / kRouteChunk) ==
@@ -191,8 +189,7 @@ fp4moe_status moe_route(const fp4moe_config* cfg, int32_t T, const uint16_t* x, 
   const WsLayout L = ws_layout(*cfg);
   float* logits = logits_out ? logits_out : at<float>(ws, L.logits);
   return route_launch(*cfg, T, x, router_w, router_bias, logits, topk_ids, topk_w, counts, offsets, padded_offsets,
-                      slot_of_pair, pair_of_row, at<int32_t>(ws, L.hist), at<float>(ws, L.nx2), at<float>(ws, L.nw2),
-                      err_word(ws),
+                      slot_of_pair, pair_of_row, at<int32_t>(ws, L.hist), at<float>(ws, L.nw2), err_word(ws),
                       (cudaStream_t)stream);
 }
 
@@ -214,7 +211,7 @@ fp4moe_status moe_route_noalloc(const fp4moe_config* cfg, int32_t T, const uint1
   if (cudaMemsetAsync(s + kScratchErr, 0, 4, st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
   return route_launch(*cfg, T, x, router_w, router_bias, logits_out, topk_ids, topk_w, counts, offsets,
                       padded_offsets, slot_of_pair, pair_of_row, reinterpret_cast<int32_t*>(s + kScratchHist),
-                      reinterpret_cast<float*>(s + kScratchNx2), reinterpret_cast<float*>(s + kScratchNw2),
+                      reinterpret_cast<float*>(s + kScratchNw2),
                       err != nullptr ? err : reinterpret_cast<uint32_t*>(s + kScratchErr), st);
 }
 
@@ -293,7 +290,7 @@ fp4moe_status moe_forward(const fp4moe_config* cfg, int32_t T, const uint16_t* x
   int32_t* por = at<int32_t>(ws, L.por);
   FP4_TRY(route_launch(*cfg, T, x, router_w, router_bias, at<float>(ws, L.logits), ids, w, at<int32_t>(ws, L.counts),
                        at<int32_t>(ws, L.offsets), poff, at<int32_t>(ws, L.slot), por, at<int32_t>(ws, L.hist),
-                       at<float>(ws, L.nx2), at<float>(ws, L.nw2), err, st));
+                       at<float>(ws, L.nw2), err, st));
   FP4_TRY(quant_scatter_launch(*cfg, T, x, gs1, at<int32_t>(ws, L.slot), at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf),
                                st));
   FP4_TRY(gemm_launch(kW1SwiGLU, *cfg, T, at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf), poff, por, w1_fp4, w1_sf,
@@ -353,8 +350,8 @@ fp4moe_status fp4moe_calibrate(const fp4moe_config* cfg, int32_t T, const uint16
   FP4_TRY(gs_from_amax_launch(1, gs1_out, st));
   FP4_TRY(route_launch(*cfg, T, x_warm, router_w, router_bias, at<float>(ws, L.logits), at<int32_t>(ws, L.ids),
                        at<float>(ws, L.w), at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets), poff,
-                       at<int32_t>(ws, L.slot), por, at<int32_t>(ws, L.hist), at<float>(ws, L.nx2),
-                       at<float>(ws, L.nw2), err, st));
+                       at<int32_t>(ws, L.slot), por, at<int32_t>(ws, L.hist), at<float>(ws, L.nw2),
+                       err, st));
   FP4_TRY(quant_scatter_launch(*cfg, T, x_warm, gs1_out, at<int32_t>(ws, L.slot), at<uint8_t>(ws, L.a1),
                                at<uint8_t>(ws, L.a1sf), st));
   float* alpha = at<float>(ws, L.alpha_tmp);

@@ -167,10 +167,16 @@ __global__ void __launch_bounds__(1024) scan_kernel(int E, int nchunks, int cap,
   const int e = threadIdx.x;
   int c = 0;
   if (e < E) {
-    for (int b = 0; b < nchunks; ++b) {
-      const int h = __ldcg(hist + (size_t)b * E + e);
-      hist[(size_t)b * E + e] = c;
-      c += h;
+    // 16 chunk counts are loaded before any is overwritten, so the loads overlap
+    for (int b0 = 0; b0 < nchunks; b0 += 16) {
+      int h[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) h[q] = (b0 + q < nchunks) ? __ldcg(hist + (size_t)(b0 + q) * E + e) : 0;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        if (b0 + q < nchunks) hist[(size_t)(b0 + q) * E + e] = c;
+        c += h[q];
+      }
     }
   }
   int start;
@@ -217,11 +223,11 @@ __global__ void __launch_bounds__(256) slots_kernel(int T, int E, int k, int cap
 fp4moe_status route_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
                            const float* bias, float* logits, int32_t* ids, float* w, int32_t* counts,
                            int32_t* offsets, int32_t* poff, int32_t* slot_of_pair, int32_t* pair_of_row,
-                           int32_t* hist, float* nx2, float* nw2, uint32_t* err, cudaStream_t st) {
+                           int32_t* hist, float* nw2, uint32_t* err, cudaStream_t st) {
   const int E = cfg.num_experts, k = cfg.top_k;
   const int cap = (int)capacity_rows(cfg, T);
   const int npairs = T * k;
-  const fp4moe_status rs = router_topk_launch(cfg, T, x, router_w, bias, logits, nx2, nw2, ids, w, err, st);
+  const fp4moe_status rs = router_topk_launch(cfg, T, x, router_w, bias, logits, nw2, ids, w, err, st);
   if (rs != FP4MOE_OK) return rs;
   cudaError_t r = cudaSuccess;
   if (npairs <= kSmallPairs) {

@@ -42,26 +42,26 @@ bool encode_u8_sw128(CUtensorMap* m, const void* base, uint64_t inner_bytes, uin
 namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr int RT_BM = 128;                 // tokens per tile (MMA M)
-constexpr int RT_BN = 128;                 // experts per tile (MMA N)
+constexpr int RT_BM = 128;                 // experts per tile (MMA M)
+constexpr int RT_MAX_BN = 256;             // tokens per tile (MMA N): min(256, T rounded up to 32)
 constexpr int RT_KBYTES = 128;             // one 64-element bf16 K atom per row (128-byte swizzle)
-constexpr int RT_HALF = RT_BM * RT_KBYTES; // 16 KB
-constexpr int RT_STAGE = 2 * RT_HALF;      // x tile + w tile of one K atom
+constexpr int RT_A = RT_BM * RT_KBYTES;    // w tile of one K atom: 16 KB
+constexpr int RT_STAGE = RT_A + RT_MAX_BN * RT_KBYTES;  // + x tile: 48 KB at most
 constexpr int RT_STAGES = 4;
 constexpr int RT_BAR_OFF = RT_STAGES * RT_STAGE;
 constexpr int RT_SMEM = RT_BAR_OFF + 128 + 1024;
 constexpr int RT_THREADS = 192;
-constexpr int RT_RS = RT_BN + 4;           // row stride (floats) of the cluster-reduction tile
+constexpr int RT_RS = RT_MAX_BN + 4;       // row stride (floats) of the cluster-reduction tile
 constexpr int RT_MAX_SPLIT = 8;            // portable cluster size
-static_assert(RT_BM * RT_RS * 4 + 2 * RT_BM * 4 <= RT_BAR_OFF, "reduction tile must fit in the ring");
-// d = kBoundRel |x||w| + kBoundAbsRel |l~|: 2^-12 and 2^-21
+constexpr int kWarpRefineMinT = 512;       // from this many tokens on, one warp (not one CTA) per token
+static_assert(RT_BM * RT_RS * 4 + RT_BM * 4 <= RT_BAR_OFF, "reduction tile must fit in the ring");
+// d = kBoundRel |x||w| + kBoundUlp |l~|: 2^-12 and 2^-21
 constexpr float kBoundRel = 2.44140625e-4f;
 constexpr float kBoundUlp = 4.76837158203125e-7f;
 
 struct RouterParams {
-  int T, H, E, S;
+  int T, H, E, S, BN;
   float* lt;     // [T][E] approximate logits (no bias)
-  float* nx2;    // [T] |x_t|^2
   float* nw2;    // [E] |w_e|^2
   uint32_t* err;
 };
@@ -90,7 +90,18 @@ __device__ __forceinline__ float sumsq8(uint4 v, float a) {
   return a;
 }
 
-// grid (ceil(T/128), ceil(E/128), S), cluster (1, 1, S), 192 threads.
+// Sum of squares of one 128-byte row of a 128-byte-swizzled tile. The swizzle
+// only permutes the row's eight 16-byte chunks, so any order covers them; thread
+// i starts at chunk i % 8, which keeps the eight threads of each shared-memory
+// phase on distinct banks.
+__device__ __forceinline__ float row_sumsq(const uint8_t* row, int i, float a) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) a = sumsq8(*reinterpret_cast<const uint4*>(row + (((c + i) & 7) << 4)), a);
+  return a;
+}
+
+// grid (ceil(E/128), ceil(T/BN), S), cluster (1, 1, S), 192 threads. The tile
+// is 128 experts (MMA M, TMEM lanes) x BN tokens (MMA N, TMEM columns).
 // warp 4: TMA producer; warp 5: MMA issuer; warps 0-3: norms, then epilogue.
 // Every CTA reaches both cluster barriers on every path: a bounded wait that
 // expires only skips work.
@@ -101,7 +112,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   __shared__ uint32_t s_tmem;
   pdl_wait();
   pdl_trigger();
-  const int mt = blockIdx.x, nt = blockIdx.y, split = blockIdx.z, S = p.S;
+  const int et = blockIdx.x, tt = blockIdx.y, split = blockIdx.z, S = p.S, BN = p.BN;
   const int atoms = p.H / 64;
   const int a0 = split * atoms / S, a1 = (split + 1) * atoms / S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -112,7 +123,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   const uint32_t bar_done = bar_empty + 8 * RT_STAGES;
 
   if (warp == 0) {
-    tmem_alloc(smem_u32(&s_tmem), 128);
+    tmem_alloc(smem_u32(&s_tmem), RT_MAX_BN);
     tmem_relinquish();
   }
   if (threadIdx.x == 128) {
@@ -128,8 +139,10 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  float acc[RT_BN];
-  float sx = 0.0f, sw = 0.0f;
+  const int i = threadIdx.x;
+  // squared norm of expert row i, accumulated by the CTAs of the first token tile
+  float sw = 0.0f;
+  const bool do_w = (tt == 0);
   bool ok = true;
   if (warp == 4 && lane == 0) {
     // ------------------------------------------------------------ producer
@@ -142,9 +155,9 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         break;
       }
       const uint32_t st = smem + s * RT_STAGE;
-      mbar_arrive_expect_tx(bar_full + 8 * s, RT_STAGE);
-      tma_load_2d(st, &tmX, bar_full + 8 * s, j * RT_KBYTES, mt * RT_BM, pol);
-      tma_load_2d(st + RT_HALF, &tmW, bar_full + 8 * s, j * RT_KBYTES, nt * RT_BN, pol);
+      mbar_arrive_expect_tx(bar_full + 8 * s, RT_A + BN * RT_KBYTES);
+      tma_load_2d(st, &tmW, bar_full + 8 * s, j * RT_KBYTES, et * RT_BM, pol);
+      tma_load_2d(st + RT_A, &tmX, bar_full + 8 * s, j * RT_KBYTES, tt * BN, pol);
     }
     // on every path, let the copies already issued land before the ring is reused or the CTA exits
     for (int j = max(a0, issued - RT_STAGES); j < issued; ++j) {
@@ -153,7 +166,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     }
   } else if (warp == 5 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = idesc_bf16(RT_BM, RT_BN);
+    const uint32_t idesc = idesc_bf16(RT_BM, BN);
     for (int j = a0; j < a1 && ok; ++j) {
       const int it = j - a0, s = it % RT_STAGES;
       if (!mbar_wait(bar_full + 8 * s, (uint32_t)(it / RT_STAGES) & 1u, p.err)) {
@@ -164,87 +177,72 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       const uint32_t st = smem + s * RT_STAGE;
 #pragma unroll
       for (int q = 0; q < 4; ++q)  // K = 16 bf16 = 32 bytes per MMA
-        tc_mma_bf16(tmem, desc_sw128(st + 32 * q), desc_sw128(st + RT_HALF + 32 * q), idesc,
+        tc_mma_bf16(tmem, desc_sw128(st + 32 * q), desc_sw128(st + RT_A + 32 * q), idesc,
                     (it > 0 || q > 0) ? 1u : 0u);
       tc_commit(bar_empty + 8 * s);
     }
     tc_commit(bar_done);
+    drain_wait(bar_done, 0);  // no MMA may still write TMEM when it is read or freed
   } else if (warp < 4) {
-    // ------------------------------------------------ norms, then epilogue
-    // thread i owns token row i of the x tile and expert row i of the w tile; the 128-byte swizzle only
-    // permutes 16-byte chunks inside a row's 128 bytes, so a row's sum of squares reads them in place
-    const int i = threadIdx.x;
+    // ------------------------------------------------------------------ norms
     for (int j = a0; j < a1 && ok; ++j) {
       const int it = j - a0, s = it % RT_STAGES;
       if (!mbar_wait(bar_full + 8 * s, (uint32_t)(it / RT_STAGES) & 1u, p.err)) {
         ok = false;
         break;
       }
-      const uint4* xa = reinterpret_cast<const uint4*>(smem_gen + s * RT_STAGE + i * RT_KBYTES);
-      const uint4* wa = reinterpret_cast<const uint4*>(smem_gen + s * RT_STAGE + RT_HALF + i * RT_KBYTES);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        sx = sumsq8(xa[c], sx);
-        sw = sumsq8(wa[c], sw);
-      }
+      if (do_w) sw = row_sumsq(smem_gen + s * RT_STAGE + i * RT_KBYTES, i, sw);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * s);
     }
-    if (ok && a1 > a0) ok = mbar_wait(bar_done, 0, p.err);
+    if (ok) ok = mbar_wait(bar_done, 0, p.err);
     tc_fence_after();
-    if (ok && a1 > a0) {
-      const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
-#pragma unroll
-      for (int c = 0; c < RT_BN / 32; ++c) {
-        float v[32];
-        tmem_ld32(taddr + 32 * c, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int q = 0; q < 32; ++q) acc[32 * c + q] = v[q];
-      }
-    } else {
-#pragma unroll
-      for (int c = 0; c < RT_BN; ++c) acc[c] = 0.0f;
-    }
   }
-  tc_fence_before();
   __syncthreads();  // the ring is idle from here on: every copy landed and every MMA completed
 
-  const int i = threadIdx.x;
-  const int t_row = mt * RT_BM + i;  // token of row i
-  const int e_row = nt * RT_BN + i;  // expert of row i
+  const int e_row = et * RT_BM + i;  // expert of TMEM lane / thread i (i < 128)
+  const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
   if (S == 1) {
-    if (i < RT_BM) {
-      if (t_row < p.T) {
-        float* dst = p.lt + (size_t)t_row * p.E + nt * RT_BN;
-        const int ne = min(RT_BN, p.E - nt * RT_BN);
+    if (warp < 4) {
+      for (int c = 0; c < BN; c += 32) {
+        float v[32];
+        tmem_ld32(taddr + c, v);
+        tmem_ld_wait();
+        if (ok && e_row < p.E) {
 #pragma unroll
-        for (int c = 0; c < RT_BN; ++c)
-          if (c < ne) dst[c] = acc[c];
-        if (nt == 0) p.nx2[t_row] = sx;
+          for (int q = 0; q < 32; ++q) {
+            const int t = tt * BN + c + q;
+            if (t < p.T) p.lt[(size_t)t * p.E + e_row] = v[q];  // a warp stores 32 consecutive experts
+          }
+        }
       }
-      if (mt == 0 && e_row < p.E) p.nw2[e_row] = sw;
+      if (do_w && e_row < p.E) p.nw2[e_row] = sw;
     }
   } else {
     // every CTA of the cluster parks its partial tile in its own (idle) ring memory
     float* red = reinterpret_cast<float*>(smem_gen);
-    float* red_nx = red + RT_BM * RT_RS;
-    float* red_nw = red_nx + RT_BM;
-    if (i < RT_BM) {
+    float* red_nw = red + RT_BM * RT_RS;
+    if (warp < 4) {
+      for (int c = 0; c < BN; c += 32) {
+        float v[32];
+        tmem_ld32(taddr + c, v);
+        tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < RT_BN; c += 4)
-        *reinterpret_cast<float4*>(red + i * RT_RS + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
-      red_nx[i] = sx;
+        for (int q = 0; q < 32; q += 4)
+          *reinterpret_cast<float4*>(red + i * RT_RS + c + q) =
+              ok ? make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
       red_nw[i] = sw;
     }
     cluster_sync();
-    // CTA r sums rows [r R, (r + 1) R) of the S partial tiles, in rank order
+    // CTA r sums expert rows [r R, (r + 1) R) of the S partial tiles, in rank order. Consecutive threads take
+    // consecutive experts of the same 4 tokens, so each store of a warp covers consecutive addresses.
     const uint32_t rank = cluster_ctarank();
     const int R = RT_BM / S;
     const uint32_t red_s = smem;
-    for (int idx = threadIdx.x; idx < R * (RT_BN / 4); idx += RT_THREADS) {
-      const int row = (int)rank * R + idx / (RT_BN / 4);
-      const int c = (idx % (RT_BN / 4)) * 4;
+    for (int idx = threadIdx.x; idx < R * (BN / 4); idx += RT_THREADS) {
+      const int row = (int)rank * R + idx % R;
+      const int c = (idx / R) * 4;
       const uint32_t off = (uint32_t)(row * RT_RS + c) * 4u;
       float4 a = ld_cluster_f4(map_cluster(red_s + off, 0));
       for (int q = 1; q < S; ++q) {
@@ -254,31 +252,28 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         a.z += b.z;
         a.w += b.w;
       }
-      const int t = mt * RT_BM + row, e = nt * RT_BN + c;
-      if (t < p.T) {
+      const int e = et * RT_BM + row, t = tt * BN + c;
+      if (e < p.E) {
         float* dst = p.lt + (size_t)t * p.E + e;
-        if (e + 0 < p.E) dst[0] = a.x;
-        if (e + 1 < p.E) dst[1] = a.y;
-        if (e + 2 < p.E) dst[2] = a.z;
-        if (e + 3 < p.E) dst[3] = a.w;
+        if (t + 0 < p.T) dst[0] = a.x;
+        if (t + 1 < p.T) dst[(size_t)p.E] = a.y;
+        if (t + 2 < p.T) dst[(size_t)2 * p.E] = a.z;
+        if (t + 3 < p.T) dst[(size_t)3 * p.E] = a.w;
       }
     }
-    if (rank == 0 && i < RT_BM) {
-      const uint32_t onx = (uint32_t)(RT_BM * RT_RS + i) * 4u, onw = onx + RT_BM * 4u;
-      float nx = ld_cluster_f32(map_cluster(red_s + onx, 0));
+    if (rank == 0 && warp < 4 && do_w) {
+      const uint32_t onw = (uint32_t)(RT_BM * RT_RS + i) * 4u;
       float nw = ld_cluster_f32(map_cluster(red_s + onw, 0));
-      for (int q = 1; q < S; ++q) {
-        nx += ld_cluster_f32(map_cluster(red_s + onx, (uint32_t)q));
-        nw += ld_cluster_f32(map_cluster(red_s + onw, (uint32_t)q));
-      }
-      if (nt == 0 && t_row < p.T) p.nx2[t_row] = nx;
-      if (mt == 0 && e_row < p.E) p.nw2[e_row] = nw;
+      for (int q = 1; q < S; ++q) nw += ld_cluster_f32(map_cluster(red_s + onw, (uint32_t)q));
+      if (e_row < p.E) p.nw2[e_row] = nw;
     }
     cluster_sync();  // no CTA leaves while another still reads its shared memory
   }
+  tc_fence_before();
+  __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, RT_MAX_BN);
   }
 }
 
@@ -296,23 +291,31 @@ __device__ __forceinline__ void acc_prod(float& s, float& c, float xv, float wv)
   c = __fadd_rn(c, e);
 }
 
-// Exact-sum-rounded-once logit (within an ulp) of token row x and expert row w, by one warp. Lane l takes
-// the 16-byte chunks l, l + 32, ... with two compensated accumulators; a fixed butterfly merges the lanes.
-__device__ float warp_exact_dot(const uint4* __restrict__ xr, const uint4* __restrict__ wrow, int nchunks) {
+constexpr int kMaxChunksPerLane = 18;  // H <= 4608: 576 16-byte chunks over 32 lanes
+
+// Exact-sum-rounded-once logit (within an ulp) of the token row xs (in shared memory) and expert row w, by
+// one warp. Lane l takes the 16-byte chunks l, l + 32, ..., all of whose loads are issued before the
+// arithmetic, with two compensated accumulators; a fixed butterfly merges the lanes.
+__device__ float warp_exact_dot(const uint4* xs, const uint4* __restrict__ wrow, int nchunks) {
   const int lane = threadIdx.x & 31;
+  uint4 wv[kMaxChunksPerLane];
+#pragma unroll
+  for (int j = 0; j < kMaxChunksPerLane; ++j)
+    if (lane + 32 * j < nchunks) wv[j] = __ldg(wrow + lane + 32 * j);
   float s0 = 0.0f, c0 = 0.0f, s1 = 0.0f, c1 = 0.0f;
-#pragma unroll 2
-  for (int ch = lane; ch < nchunks; ch += 32) {
-    const uint4 xv = __ldg(xr + ch);
-    const uint4 wv = __ldg(wrow + ch);
-    acc_prod(s0, c0, bf16_lo(xv.x), bf16_lo(wv.x));
-    acc_prod(s1, c1, bf16_hi(xv.x), bf16_hi(wv.x));
-    acc_prod(s0, c0, bf16_lo(xv.y), bf16_lo(wv.y));
-    acc_prod(s1, c1, bf16_hi(xv.y), bf16_hi(wv.y));
-    acc_prod(s0, c0, bf16_lo(xv.z), bf16_lo(wv.z));
-    acc_prod(s1, c1, bf16_hi(xv.z), bf16_hi(wv.z));
-    acc_prod(s0, c0, bf16_lo(xv.w), bf16_lo(wv.w));
-    acc_prod(s1, c1, bf16_hi(xv.w), bf16_hi(wv.w));
+#pragma unroll
+  for (int j = 0; j < kMaxChunksPerLane; ++j) {
+    if (lane + 32 * j < nchunks) {
+      const uint4 xv = xs[lane + 32 * j];
+      acc_prod(s0, c0, bf16_lo(xv.x), bf16_lo(wv[j].x));
+      acc_prod(s1, c1, bf16_hi(xv.x), bf16_hi(wv[j].x));
+      acc_prod(s0, c0, bf16_lo(xv.y), bf16_lo(wv[j].y));
+      acc_prod(s1, c1, bf16_hi(xv.y), bf16_hi(wv[j].y));
+      acc_prod(s0, c0, bf16_lo(xv.z), bf16_lo(wv[j].z));
+      acc_prod(s1, c1, bf16_hi(xv.z), bf16_hi(wv[j].z));
+      acc_prod(s0, c0, bf16_lo(xv.w), bf16_lo(wv[j].w));
+      acc_prod(s1, c1, bf16_hi(xv.w), bf16_hi(wv[j].w));
+    }
   }
   float s, e0;
   two_sum(s0, s1, s, e0);
@@ -372,22 +375,40 @@ __device__ float warp_select(const float* key, const int* list, int n, int k, in
 __global__ void __launch_bounds__(256) router_refine_kernel(int H, int E, int k, const uint16_t* __restrict__ x,
                                                             const uint16_t* __restrict__ wr,
                                                             const float* __restrict__ bias,
-                                                            const float* __restrict__ nx2,
                                                             const float* __restrict__ nw2, float* logits,
                                                             int32_t* __restrict__ ids_out,
                                                             float* __restrict__ w_out, uint32_t* err) {
   pdl_wait();
   pdl_trigger();
+  __shared__ uint4 s_x[kMaxChunksPerLane * 32];
   __shared__ float s_l[kMaxExperts];
   __shared__ float s_lo[kMaxExperts];
   __shared__ float s_hi[kMaxExperts];
   __shared__ int s_cand[kMaxExperts];
+  __shared__ float s_part[8];
   __shared__ int s_m;
   __shared__ float s_tau;
   const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nchunks = H / 8;
   float* lrow = logits + (size_t)t * E;
-  const float nx = sqrtf(__ldcg(nx2 + t));
+  // the token row goes to shared memory once; its squared norm is a fixed-order block sum
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  float sq = 0.0f;
+  for (int c = threadIdx.x; c < nchunks; c += blockDim.x) {
+    const uint4 v = __ldg(xr + c);
+    s_x[c] = v;
+    sq = sumsq8(v, sq);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(kFull, sq, off);
+  if (lane == 0) s_part[warp] = sq;
+  if (threadIdx.x == 0) s_m = 0;
+  __syncthreads();
+  float nx2 = 0.0f;
+#pragma unroll
+  for (int w8 = 0; w8 < 8; ++w8) nx2 += s_part[w8];
+  const float nx = sqrtf(nx2);
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     float l = __ldcg(lrow + e);
     if (bias != nullptr) l = __fadd_rn(l, bias[e]);
@@ -397,7 +418,6 @@ __global__ void __launch_bounds__(256) router_refine_kernel(int H, int E, int k,
     s_lo[e] = __fsub_rd(l, d);
     s_hi[e] = __fadd_ru(l, d);
   }
-  if (threadIdx.x == 0) s_m = 0;
   __syncthreads();
   if (warp == 0) {
     int se[kMaxTopK];
@@ -413,10 +433,9 @@ __global__ void __launch_bounds__(256) router_refine_kernel(int H, int E, int k,
   }
   __syncthreads();
   const int m = s_m;
-  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
   for (int c = warp; c < m; c += blockDim.x / 32) {
     const int e = s_cand[c];
-    float l = warp_exact_dot(xr, reinterpret_cast<const uint4*>(wr + (size_t)e * H), H / 8);
+    float l = warp_exact_dot(s_x, reinterpret_cast<const uint4*>(wr + (size_t)e * H), nchunks);
     if (bias != nullptr) l = __fadd_rn(l, bias[e]);
     if (lane == 0) s_l[e] = l;
   }
@@ -450,6 +469,214 @@ __global__ void __launch_bounds__(256) router_refine_kernel(int H, int E, int k,
   for (int e = threadIdx.x; e < E; e += blockDim.x) lrow[e] = s_l[e];
 }
 
+// Argmax over this warp's register arrays (item lane + 32 q is expert lane + 32 q): the largest v among the
+// items whose bit is set in `eligible`, ties to the lower expert id. Returns INT_MAX in be when no eligible
+// item compares (only NaNs left).
+template <int MAXV>
+__device__ __forceinline__ void warp_argmax(const float (&v)[MAXV], uint32_t eligible, int& be_out, float& bv_out) {
+  const int lane = threadIdx.x & 31;
+  float bv = -INFINITY;
+  int be = INT_MAX;
+#pragma unroll
+  for (int q = 0; q < MAXV; ++q) {
+    const int e = lane + 32 * q;
+    if (((eligible >> q) & 1u) && (v[q] > bv || (v[q] == bv && e < be))) {
+      bv = v[q];
+      be = e;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float ov = __shfl_xor_sync(kFull, bv, off);
+    const int oe = __shfl_xor_sync(kFull, be, off);
+    if (ov > bv || (ov == bv && oe < be)) {
+      bv = ov;
+      be = oe;
+    }
+  }
+  be_out = be;
+  bv_out = bv;
+}
+
+// The compensated dot product of warp_exact_dot, with the token row read from global memory (it stays in
+// L1 across the candidates of a token) in batches of 4 chunks per lane.
+__device__ __noinline__ float warp_exact_dot_global(const uint4* __restrict__ xr, const uint4* __restrict__ wrow,
+                                                   int nchunks) {
+  const int lane = threadIdx.x & 31;
+  float s0 = 0.0f, c0 = 0.0f, s1 = 0.0f, c1 = 0.0f;
+  for (int base = 0; base < nchunks; base += 32 * 4) {
+    uint4 xv[4], wv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int ch = base + lane + 32 * j;
+      if (ch < nchunks) {
+        xv[j] = __ldg(xr + ch);
+        wv[j] = __ldg(wrow + ch);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (base + lane + 32 * j < nchunks) {
+        acc_prod(s0, c0, bf16_lo(xv[j].x), bf16_lo(wv[j].x));
+        acc_prod(s1, c1, bf16_hi(xv[j].x), bf16_hi(wv[j].x));
+        acc_prod(s0, c0, bf16_lo(xv[j].y), bf16_lo(wv[j].y));
+        acc_prod(s1, c1, bf16_hi(xv[j].y), bf16_hi(wv[j].y));
+        acc_prod(s0, c0, bf16_lo(xv[j].z), bf16_lo(wv[j].z));
+        acc_prod(s1, c1, bf16_hi(xv[j].z), bf16_hi(wv[j].z));
+        acc_prod(s0, c0, bf16_lo(xv[j].w), bf16_lo(wv[j].w));
+        acc_prod(s1, c1, bf16_hi(xv[j].w), bf16_hi(wv[j].w));
+      }
+    }
+  }
+  float s, e0;
+  two_sum(s0, s1, s, e0);
+  float c = __fadd_rn(__fadd_rn(c0, c1), e0);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float so = __shfl_xor_sync(kFull, s, off);
+    const float co = __shfl_xor_sync(kFull, c, off);
+    float ns, ne;
+    two_sum(s, so, ns, ne);
+    s = ns;
+    c = __fadd_rn(__fadd_rn(c, co), ne);
+  }
+  return __fadd_rn(s, c);
+}
+
+// One warp per token, 8 tokens per CTA, no block barriers: for large T, where throughput matters more than
+// the latency of a single token. The same four steps as router_refine_kernel, on register arrays (expert
+// lane + 32 q in slot q of each lane), with the exact dot products of a token's candidates done one after
+// another by its warp.
+template <int MAXV>
+__global__ void __launch_bounds__(256, 3) router_refine_warp_kernel(int T, int H, int E, int k,
+                                                                 const uint16_t* __restrict__ x,
+                                                                 const uint16_t* __restrict__ wr,
+                                                                 const float* __restrict__ bias,
+                                                                 const float* __restrict__ nw2, float* logits,
+                                                                 int32_t* __restrict__ ids_out,
+                                                                 float* __restrict__ w_out, uint32_t* err) {
+  pdl_wait();
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;  // the whole warp leaves; nothing below synchronises beyond the warp
+  const int nchunks = H / 8;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  float sq = 0.0f;
+  for (int c = lane; c < nchunks; c += 32) sq = sumsq8(__ldg(xr + c), sq);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(kFull, sq, off);
+  const float nx = sqrtf(sq);
+  float* lrow = logits + (size_t)t * E;
+  float l[MAXV], d[MAXV];
+  uint32_t valid = 0;
+#pragma unroll
+  for (int q = 0; q < MAXV; ++q) {
+    const int e = lane + 32 * q;
+    l[q] = -INFINITY;
+    d[q] = 0.0f;
+    if (e < E) {
+      float v = __ldcg(lrow + e);
+      if (bias != nullptr) v = __fadd_rn(v, bias[e]);
+      // the fp32 norms are low by at most ~3e-4 relative: the (1 + 2^-10) factor keeps the bound above it
+      d[q] = fmaf(kBoundRel * 1.0009765625f, nx * sqrtf(__ldcg(nw2 + e)), kBoundUlp * fabsf(v));
+      l[q] = v;
+      valid |= 1u << q;
+    }
+  }
+  // tau = the k-th largest lower end
+  float lo[MAXV];
+#pragma unroll
+  for (int q = 0; q < MAXV; ++q) lo[q] = __fsub_rd(l[q], d[q]);
+  float tau = __int_as_float(0x7FC00000);
+  {
+    uint32_t left = valid;
+    for (int j = 0; j < k; ++j) {
+      int be;
+      float bv;
+      warp_argmax<MAXV>(lo, left, be, bv);
+      if (be == INT_MAX) {
+        tau = __int_as_float(0x7FC00000);
+        break;
+      }
+      if ((be & 31) == lane) left &= ~(1u << (be >> 5));
+      tau = bv;
+    }
+  }
+  // candidates (all valid experts when tau is NaN), each given its exact logit
+  uint32_t cand = 0;
+#pragma unroll
+  for (int q = 0; q < MAXV; ++q)
+    if (((valid >> q) & 1u) && !(__fadd_ru(l[q], d[q]) < tau)) cand |= 1u << q;
+  // one call site of the (out-of-line) dot product keeps the kernel small enough for the instruction cache
+  for (int q = 0; q < MAXV; ++q) {
+    uint32_t ball = __ballot_sync(kFull, (cand >> q) & 1u);
+    while (ball != 0u) {
+      const int src = __ffs(ball) - 1;
+      ball &= ball - 1u;
+      const int e = src + 32 * q;
+      float lv = warp_exact_dot_global(xr, reinterpret_cast<const uint4*>(wr + (size_t)e * H), nchunks);
+      if (bias != nullptr) lv = __fadd_rn(lv, bias[e]);
+      if (lane == src) {
+#pragma unroll
+        for (int qq = 0; qq < MAXV; ++qq)
+          if (qq == q) l[qq] = lv;
+      }
+    }
+  }
+  // the top k of the candidates by exact logit
+  int se[kMaxTopK];
+  float sv[kMaxTopK];
+  bool bad = false;
+  {
+    uint32_t left = cand;
+    for (int j = 0; j < k; ++j) {
+      int be;
+      float bv;
+      warp_argmax<MAXV>(l, left, be, bv);
+      if (be == INT_MAX) {
+        bad = true;
+        break;
+      }
+      if ((be & 31) == lane) left &= ~(1u << (be >> 5));
+      se[j] = be;
+      sv[j] = bv;
+    }
+  }
+  if (lane == 0) {
+    if (bad) {  // fewer than k comparable logits: NaN input
+      raise_error(err, FP4MOE_ERR_EXPERT_ID);
+      for (int j = 0; j < k; ++j) {
+        ids_out[(size_t)t * k + j] = 0;
+        w_out[(size_t)t * k + j] = 0.0f;
+      }
+    } else {
+      const float lmax = sv[0];
+      float ex[kMaxTopK];
+      float sum = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        ex[j] = expf(__fsub_rn(sv[j], lmax));
+        sum = __fadd_rn(sum, ex[j]);
+      }
+      for (int j = 0; j < k; ++j) {
+        ids_out[(size_t)t * k + j] = se[j];
+        w_out[(size_t)t * k + j] = __fdiv_rn(ex[j], sum);
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < MAXV; ++q)
+    if ((valid >> q) & 1u) lrow[lane + 32 * q] = l[q];
+}
+
+template <int MAXV>
+cudaError_t launch_refine_warp(int T, int H, int E, int k, const uint16_t* x, const uint16_t* wr, const float* bias,
+                               const float* nw2, float* logits, int32_t* ids, float* w, uint32_t* err,
+                               cudaStream_t st) {
+  return launch_pdl(router_refine_warp_kernel<MAXV>, dim3((T + 7) / 8), dim3(256), 0, st, T, H, E, k, x, wr, bias,
+                    nw2, logits, ids, w, err);
+}
+
 bool configure_router() {
   static int ok = -1;
   if (ok < 0)
@@ -463,32 +690,33 @@ bool configure_router() {
 }  // namespace
 
 fp4moe_status router_topk_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const uint16_t* wr,
-                                 const float* bias, float* logits, float* nx2, float* nw2, int32_t* ids, float* w,
-                                 uint32_t* err, cudaStream_t st) {
+                                 const float* bias, float* logits, float* nw2, int32_t* ids, float* w, uint32_t* err,
+                                 cudaStream_t st) {
   if (T == 0) return FP4MOE_OK;
   const int H = cfg.hidden, E = cfg.num_experts, k = cfg.top_k;
   if (!configure_router()) return FP4MOE_CUDA_ERROR;
+  const int BN = T >= RT_MAX_BN ? RT_MAX_BN : (T + 31) / 32 * 32;  // tokens per tile: a multiple of 32
   CUtensorMap tmX, tmW;
-  if (!encode_u8_sw128(&tmX, x, (uint64_t)H * 2, (uint64_t)T, RT_BM)) return FP4MOE_CUDA_ERROR;
-  if (!encode_u8_sw128(&tmW, wr, (uint64_t)H * 2, (uint64_t)E, RT_BN)) return FP4MOE_CUDA_ERROR;
-  const int n_mt = (T + RT_BM - 1) / RT_BM, n_nt = (E + RT_BN - 1) / RT_BN;
+  if (!encode_u8_sw128(&tmX, x, (uint64_t)H * 2, (uint64_t)T, (uint32_t)BN)) return FP4MOE_CUDA_ERROR;
+  if (!encode_u8_sw128(&tmW, wr, (uint64_t)H * 2, (uint64_t)E, RT_BM)) return FP4MOE_CUDA_ERROR;
+  const int n_et = (E + RT_BM - 1) / RT_BM, n_tt = (T + BN - 1) / BN;
   const int nsm = sm_count();
   if (nsm <= 0) return FP4MOE_CUDA_ERROR;
-  // split K over a cluster while the tiles alone leave SMs idle; at least 2 K atoms per split
+  // split K over a cluster while the tiles alone leave SMs idle, keeping at least 2 K atoms per split
   int S = 1;
-  while (S * 2 <= RT_MAX_SPLIT && n_mt * n_nt * S * 2 <= nsm && (H / 64) >= 4 * S) S *= 2;
+  while (S * 2 <= RT_MAX_SPLIT && n_et * n_tt * S * 2 <= nsm && (H / 64) >= 4 * S) S *= 2;
   RouterParams prm;
   prm.T = T;
   prm.H = H;
   prm.E = E;
   prm.S = S;
+  prm.BN = BN;
   prm.lt = logits;
-  prm.nx2 = nx2;
   prm.nw2 = nw2;
   prm.err = err;
 
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(n_mt, n_nt, S);
+  lc.gridDim = dim3(n_et, n_tt, S);
   lc.blockDim = dim3(RT_THREADS);
   lc.dynamicSmemBytes = RT_SMEM;
   lc.stream = st;
@@ -502,11 +730,20 @@ fp4moe_status router_topk_launch(const fp4moe_config& cfg, int32_t T, const uint
   lc.attrs = attr;
   lc.numAttrs = 2;
   if (cudaLaunchKernelEx(&lc, router_mma_kernel, tmX, tmW, prm) != cudaSuccess) return FP4MOE_CUDA_ERROR;
-  return launch_pdl(router_refine_kernel, dim3(T), dim3(256), 0, st, H, E, k, x, wr, bias,
-                    (const float*)nx2, (const float*)nw2, logits, ids, w, err) ==
-                 cudaSuccess
-             ? FP4MOE_OK
-             : FP4MOE_CUDA_ERROR;
+  cudaError_t r;
+  if (T < kWarpRefineMinT) {  // latency-bound: one CTA per token spreads its exact dot products over 8 warps
+    r = launch_pdl(router_refine_kernel, dim3(T), dim3(256), 0, st, H, E, k, x, wr, bias, (const float*)nw2, logits,
+                   ids, w, err);
+  } else {
+    const int maxv = (E + 31) / 32;
+    const float* cnw2 = nw2;
+    if (maxv <= 2) r = launch_refine_warp<2>(T, H, E, k, x, wr, bias, cnw2, logits, ids, w, err, st);
+    else if (maxv <= 4) r = launch_refine_warp<4>(T, H, E, k, x, wr, bias, cnw2, logits, ids, w, err, st);
+    else if (maxv <= 8) r = launch_refine_warp<8>(T, H, E, k, x, wr, bias, cnw2, logits, ids, w, err, st);
+    else if (maxv <= 16) r = launch_refine_warp<16>(T, H, E, k, x, wr, bias, cnw2, logits, ids, w, err, st);
+    else r = launch_refine_warp<32>(T, H, E, k, x, wr, bias, cnw2, logits, ids, w, err, st);
+  }
+  return r == cudaSuccess ? FP4MOE_OK : FP4MOE_CUDA_ERROR;
 }
 
 }  // namespace fp4moe

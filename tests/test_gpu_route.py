@@ -95,7 +95,8 @@ def check_route(wl, T, seed):
 
 
 @pytest.mark.parametrize("wl,T", [(sg.TINY, 16), (sg.TINY, 5), (sg.TINY, 0), (sg.DSV4_DECODE, 64),
-                                  (sg.DSV4_DECODE, 1), (sg.DSV4_DECODE, 333), (sg.DSV4_DECODE, 129)])
+                                  (sg.DSV4_DECODE, 1), (sg.DSV4_DECODE, 333), (sg.DSV4_DECODE, 129),
+                                  (sg.DSV4_DECODE, 600), (sg.TINY, 700)])
 def test_route_matches_oracle(wl, T):
     check_route(wl, T, sg.EVAL_SEED)
 
