@@ -9,9 +9,14 @@
 // ("Bug 2", "Bug 4").
 //
 // Persistent kernel, one CTA per SM. Output tiles are 128 activation rows x
-// 128 weight rows, numbered in (m-tile, n-tile) order. CTA c takes the
-// contiguous share [c*T/G, (c+1)*T/G) of the T tiles, so it walks consecutive
-// n-tiles of the same m-tile (expert block):
+// 128 weight rows. They are numbered expert by expert; inside expert e, with
+// M_e m-tiles, the n-tiles run slowest and the m-tiles fastest. CTA c takes
+// the contiguous share [c*T/G, (c+1)*T/G) of the T tiles. So an expert with
+// one m-tile (every expert at decode sizes) is walked across its n-tiles
+// with the activation tile fixed, and a weight tile of a larger expert is
+// used for all of the expert's m-tiles in a row, while it is still in L2.
+// The fixed operand keeps its block scales resident in TMEM ("resident"),
+// the other one streams them with every stage ("streamed"):
 //   warp 4      producer. A ring stage covers 512 elements of K. Its two
 //               consecutive 16 KB weight blocks arrive with one contiguous
 //               cp.async.bulk: the weights are stored pre-tiled and
@@ -29,10 +34,9 @@
 //               across tile boundaries, so the weight stream never stops.
 //   warp 5      MMA issuer. tcgen05.cp costs about the same per instruction
 //               whatever its size, and it sits on this thread's critical path.
-//               So the activation (A) scales of an m-tile are copied into
-//               TMEM only once, for the whole of K, and stay resident while
-//               the CTA walks that m-tile's n-tiles. Each stage then copies
-//               only its 8 weight (B) scale tiles. Then
+//               So the resident scales are copied into TMEM only once, for
+//               the whole of K, and stay there while the operand is fixed.
+//               Each stage then copies only its 8 streamed scale tiles. Then
 //               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (K = 64
 //               each) accumulates in fp32 in TMEM, and tcgen05.commit frees the
 //               ring slot and then hands the accumulator to the epilogue.
@@ -49,6 +53,7 @@
 // Every spin-wait is bounded (mbar_wait). A timeout sets FP4MOE_ERR_TIMEOUT
 // in the error word. Each role then stops, waits for its in-flight copies and
 // MMAs, and the CTA frees its TMEM and returns.
+#include <climits>
 #include <mutex>
 
 #include "common.cuh"
@@ -67,9 +72,9 @@ constexpr int HALF_BYTES = BM * KBYTES;        // one 128-row x 128-byte swizzle
 constexpr int A_BYTES = HALVES * HALF_BYTES;
 constexpr int B_BYTES = HALVES * HALF_BYTES;   // pre-tiled weight blocks of consecutive k-stages
 constexpr int SF_TILE = 512;                   // one 128x4 scale tile
-constexpr int SFA_OFF = A_BYTES + B_BYTES;
-constexpr int SFB_OFF = SFA_OFF + ATOMS * SF_TILE;
-constexpr int STAGE_BYTES = SFB_OFF + ATOMS * SF_TILE;  // 73728, a multiple of 1024
+constexpr int RES_OFF = A_BYTES + B_BYTES;            // scale tiles of the resident operand (new operand only)
+constexpr int STR_OFF = RES_OFF + ATOMS * SF_TILE;      // scale tiles of the streamed operand
+constexpr int STAGE_BYTES = STR_OFF + ATOMS * SF_TILE;  // 73728, a multiple of 1024
 constexpr int BAR_OFF = STAGES * STAGE_BYTES;
 constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;    // barriers + 1024-byte alignment slack
 constexpr int THREADS = 192;
@@ -77,9 +82,10 @@ constexpr int PREFETCH = 6;         // ring stages pulled into L2 ahead of the r
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 128;  // one accumulator: 128 fp32 columns
 constexpr uint32_t SFB_STAGE_COLS = 4 * ATOMS;  // B scales of one ring stage
-// TMEM columns: nacc accumulators at [0, 128 nacc); resident A scales (4 columns
-// per 64-element K atom, all of K) at SFA_COL = 128 nacc; B scales of ring stage
-// s: 32 columns at SFA_COL + K/16 + 32 s. nacc is 2 when that fits, else 1.
+// TMEM columns: nacc accumulators at [0, 128 nacc); resident scales (4 columns
+// per 64-element K atom, all of K) at RES_COL = 128 nacc; streamed scales of
+// ring stage s: 32 columns at RES_COL + K/16 + 32 s. nacc is 2 when that fits,
+// else 1.
 static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
 static_assert(SMEM_BYTES + 4 * kMaxExperts + 64 <= 232448, "shared memory budget (dynamic + static)");
 constexpr int kMaxResidentK = (TMEM_COLS - ACC_COLS - SFB_STAGE_COLS * STAGES) * 16;  // 4608 with one accumulator
@@ -102,7 +108,8 @@ struct Params {
 };
 
 struct Tile {
-  int e, nt, mt;
+  int e, nt, mt, me;  // expert, n-tile, m-tile, m-tiles of the expert
+  bool last;          // the expert's last m-tile: the only one that can hold padding rows
 };
 
 // Tensor maps of the activation codes whose boxes are 16, 32, 64 and 128 rows
@@ -111,20 +118,43 @@ struct AMaps {
   CUtensorMap box[4];
 };
 
-// Tile tau in (m-tile, n-tile) order; the m-tile's expert is
-// searchsorted(padded_offsets, first row, right=True). `poff` is the CTA's
-// shared-memory copy of the padded offsets.
-__device__ __forceinline__ Tile map_tile(int tau, const int* poff, int E, int NT) {
-  const int mt = tau / NT;
-  const int row = mt * BM;
-  int lo = 0, hi = E - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (poff[mid] > row) hi = mid;
-    else lo = mid + 1;
+// Position in the tile order. Expert e owns tiles [NT pm(e-1), NT pm(e)) with pm(e) = min(padded_offsets[e],
+// R) / 128, so the expert of tile tau is the first e with NT pm(e) > tau: the searchsorted(right=True) rule on
+// padded offsets. Inside the expert, local index L gives n-tile L / M_e and m-tile pm(e-1) + L % M_e. A
+// cursor finds its first tile with one binary search and then steps in O(1), because the MMA issuer, which
+// bounds the kernel's throughput, walks it once per tile. `poff` is the CTA's shared-memory copy of the
+// padded offsets; r128 = R / 128 keeps every tile inside the R rows that exist.
+struct TileCursor {
+  int e, nt, ml, me, pm0;  // expert, n-tile, m-tile inside the expert, m-tiles of the expert, its first m-tile
+
+  __device__ __forceinline__ void seek(int tau, const int* poff, int E, int NT, int r128) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (NT * min(poff[mid] >> 7, r128) > tau) hi = mid;
+      else lo = mid + 1;
+    }
+    e = lo;
+    pm0 = lo > 0 ? min(poff[lo - 1] >> 7, r128) : 0;
+    me = min(poff[lo] >> 7, r128) - pm0;
+    const int L = tau - NT * pm0;
+    nt = L / me;
+    ml = L - nt * me;
   }
-  return Tile{lo, tau - mt * NT, mt};
-}
+  // the next tile; only called while one exists
+  __device__ __forceinline__ void step(const int* poff, int E, int NT, int r128) {
+    if (++ml < me) return;
+    ml = 0;
+    if (++nt < NT) return;
+    nt = 0;
+    pm0 += me;
+    do {
+      ++e;
+      me = min(poff[e] >> 7, r128) - pm0;
+    } while (me == 0 && e < E - 1);
+  }
+  __device__ __forceinline__ Tile tile() const { return Tile{e, nt, pm0 + ml, me, ml == me - 1}; }
+};
 
 // Bounded wait that ignores other CTAs' aborts: used only while draining.
 __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -165,8 +195,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (*(volatile uint32_t*)prm.err & kAbortMask) return;  // an earlier timeout poisons the call
   const int E = prm.E, NT = prm.NT;
   const int R = min(__ldcg(prm.poff + E - 1), prm.cap);
+  const int r128 = R / BM;
   int tau0, tau1;
-  cta_range((R / BM) * NT, tau0, tau1);
+  cta_range(r128 * NT, tau0, tau1);
   if (tau0 >= tau1) return;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -202,45 +233,63 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int KB = prm.KB;
   const int katoms_total = prm.K / 64;
   const int nacc = prm.nacc;
-  const uint32_t sfa_col = ACC_COLS * nacc;
-  const uint32_t sfb_col = sfa_col + 4u * katoms_total;
-  (void)ATOMS;
+  const uint32_t res_col = ACC_COLS * nacc;
+  const uint32_t str_col = res_col + 4u * katoms_total;
 
   if (warp == 4 && lane == 0) {
     // ------------------------------------------------------------ producer
-    const uint64_t pol_w = policy_evict_first();  // weights stream through once
-    const uint64_t pol_a = policy_evict_last();   // activations are re-read by every n-tile
+    const uint64_t pol_once = policy_evict_first();  // weights of a one-m-tile expert are read once
+    const uint64_t pol_keep = policy_evict_last();   // activations are re-read by every n-tile
+    const uint64_t pol_reuse = policy_evict_normal();  // weights re-read by the next m-tiles of the expert
     const int n_stages = (tau1 - tau0) * KB;
     const int wblocks = (prm.K + 255) / 256;      // 16 KB weight blocks per tile
     // L2 prefetch cursor: stage j of this CTA's range is k-stage j % KB of tile tau0 + j / KB
-    Tile pt{0, 0, 0};
+    TileCursor pc;
+    pc.seek(tau0, s_poff, E, NT, r128);
     auto prefetch = [&](int j) {
       const int kb = j % KB;
-      if (kb == 0 || j == 0) pt = map_tile(tau0 + j / KB, s_poff, E, NT);
-      const size_t blk = (size_t)(pt.e * NT + pt.nt);
+      if (kb == 0 && j > 0) pc.step(s_poff, E, NT, r128);
+      const size_t blk = (size_t)(pc.e * NT + pc.nt);
       const int nblk = min(HALVES, wblocks - kb * HALVES);
       bulk_prefetch_l2(prm.b_codes + (blk * wblocks + (size_t)kb * HALVES) * HALF_BYTES, nblk * HALF_BYTES);
       bulk_prefetch_l2(prm.b_sf + (blk * katoms_total + (size_t)kb * ATOMS) * SF_TILE,
                        min(ATOMS, katoms_total - kb * ATOMS) * SF_TILE);
     };
     for (int j = 0; j < min(PREFETCH, n_stages); ++j) prefetch(j);
-    int it = 0, prev_mt = -1, a_box = 3;
+    int it = 0, prev_key = INT_MIN, prev_mt = -1, a_box = 3;
     bool ok = true;
+    TileCursor cur;
+    cur.seek(tau0, s_poff, E, NT, r128);
     for (int tau = tau0; tau < tau1 && ok; ++tau) {
-      const Tile t = map_tile(tau, s_poff, E, NT);
-      const bool new_a = (t.mt != prev_mt);  // A scales go to TMEM once per m-tile
-      prev_mt = t.mt;
+      if (tau > tau0) cur.step(s_poff, E, NT, r128);
+      const Tile t = cur.tile();
+      const bool res_a = (t.me == 1);  // one m-tile: the activations are the fixed operand, else the weights
+      const int key = res_a ? t.mt : -1 - (t.e * NT + t.nt);
+      const bool new_res = (key != prev_key);  // resident scales go to TMEM once per fixed operand
+      prev_key = key;
       const int a_row = t.mt * BM;
-      if (new_a) {
-        // the first padding row of the block bounds the rows this m-tile needs (rows < R are all written)
-        const int32_t* por = prm.pair_of_row + a_row;
-        const int p16 = __ldcg(por + 16), p32 = __ldcg(por + 32), p64 = __ldcg(por + 64);
-        a_box = p16 < 0 ? 0 : (p32 < 0 ? 1 : (p64 < 0 ? 2 : 3));
+      if (t.mt != prev_mt) {
+        prev_mt = t.mt;
+        a_box = 3;
+        if (t.last) {
+          // the first padding row of the block bounds the rows this m-tile needs (rows < R are all written)
+          const int32_t* por = prm.pair_of_row + a_row;
+          const int p16 = __ldcg(por + 16), p32 = __ldcg(por + 32), p64 = __ldcg(por + 64);
+          a_box = p16 < 0 ? 0 : (p32 < 0 ? 1 : (p64 < 0 ? 2 : 3));
+        }
       }
       const uint32_t a_half = (uint32_t)(16 << a_box) * KBYTES;  // bytes of one activation block
+      // one m-tile: weights stream through once and the activation tile is re-read by every n-tile;
+      // several: the weight tile is re-read by the next m-tiles, and no tile deserves to outlive the others
+      const uint64_t pol_w = res_a ? pol_once : pol_reuse;
+      const uint64_t pol_a = res_a ? pol_keep : pol_reuse;
       const uint8_t* bsrc = prm.b_codes + (size_t)(t.e * NT + t.nt) * wblocks * HALF_BYTES;
       const uint8_t* sfa = prm.a_sf + (size_t)t.mt * katoms_total * SF_TILE;
       const uint8_t* sfb = prm.b_sf + ((size_t)t.e * NT + t.nt) * katoms_total * SF_TILE;
+      const uint8_t* sf_res = res_a ? sfa : sfb;
+      const uint8_t* sf_str = res_a ? sfb : sfa;
+      const uint64_t pol_res = res_a ? pol_a : pol_w;
+      const uint64_t pol_str = res_a ? pol_w : pol_a;
       for (int kb = 0; kb < KB; ++kb, ++it) {
         if (it + PREFETCH < n_stages) prefetch(it + PREFETCH);
         const int s = it % STAGES;
@@ -253,13 +302,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int halves = (atoms + 3) / 4;
         const uint32_t st = smem + s * STAGE_BYTES;
         mbar_arrive_expect_tx(bar_full + 8 * s,
-                              halves * (HALF_BYTES + a_half) + (new_a ? 2 : 1) * atoms * SF_TILE);
+                              halves * (HALF_BYTES + a_half) + (new_res ? 2 : 1) * atoms * SF_TILE);
         bulk_load(st + A_BYTES, bsrc + (size_t)kb * B_BYTES, halves * HALF_BYTES, bar_full + 8 * s, pol_w);
         for (int h = 0; h < halves; ++h)
           tma_load_2d(st + h * HALF_BYTES, &tmA.box[a_box], bar_full + 8 * s, (kb * HALVES + h) * KBYTES, a_row,
                       pol_a);
-        if (new_a) bulk_load(st + SFA_OFF, sfa + (size_t)kb * ATOMS * SF_TILE, atoms * SF_TILE, bar_full + 8 * s, pol_a);
-        bulk_load(st + SFB_OFF, sfb + (size_t)kb * ATOMS * SF_TILE, atoms * SF_TILE, bar_full + 8 * s, pol_w);
+        if (new_res)
+          bulk_load(st + RES_OFF, sf_res + (size_t)kb * ATOMS * SF_TILE, atoms * SF_TILE, bar_full + 8 * s, pol_res);
+        bulk_load(st + STR_OFF, sf_str + (size_t)kb * ATOMS * SF_TILE, atoms * SF_TILE, bar_full + 8 * s, pol_str);
       }
     }
     // on every path, let the copies already issued land before the CTA exits
@@ -267,19 +317,24 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 5 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     // This single thread is the throughput limit of the kernel: every instruction here runs at full
-    // latency. So the per-stage work is one wait, 4 (+4 on a new m-tile) scale copies, 4 MMAs and
-    // one commit, fully unrolled, and stage and phase are counters. Every shared-memory descriptor is
+    // latency. So the per-stage work is one wait, 8 (+8 for a new fixed operand) scale copies, 8 MMAs
+    // and one commit, fully unrolled, and stage and phase are counters. Every shared-memory descriptor is
     // built from its full byte address: the 14-bit address field wraps with the shared window, so
     // adding offsets to an already-masked descriptor could carry into the reserved bits.
     constexpr uint32_t idesc = idesc_nvf4(BM, BN);
-    int tl = 0, prev_mt = -1;
+    int tl = 0, prev_key = INT_MIN;
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
+    TileCursor cur;
+    cur.seek(tau0, s_poff, E, NT, r128);
     for (int tau = tau0; tau < tau1 && ok; ++tau, ++tl) {
-      const Tile t = map_tile(tau, s_poff, E, NT);
-      const bool new_a = (t.mt != prev_mt);
-      prev_mt = t.mt;
+      if (tau > tau0) cur.step(s_poff, E, NT, r128);
+      const Tile t = cur.tile();
+      const bool res_a = (t.me == 1);
+      const int key = res_a ? t.mt : -1 - (t.e * NT + t.nt);
+      const bool new_res = (key != prev_key);
+      prev_key = key;
       const int b = tl % nacc;
       const uint32_t use = (uint32_t)(tl / nacc);
       // the epilogue has drained this accumulator buffer
@@ -287,9 +342,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         ok = false;
         break;
       }
-      // before new A scales overwrite the resident ones, every earlier MMA must be complete: with one buffer
+      // before new scales overwrite the resident ones, every earlier MMA must be complete: with one buffer
       // the wait above implies it; with two, also wait until the other buffer's last tile was drained
-      if (new_a && nacc == 2 && tl > 0 &&
+      if (new_res && nacc == 2 && tl > 0 &&
           !mbar_wait(bar_tempty + 8 * (b ^ 1), ((uint32_t)((tl - 1) / 2) & 1u), prm.err)) {
         ok = false;
         break;
@@ -305,16 +360,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         // writes visible (without it MMAs can read stale shared memory)
         tc_fence_after();
         const uint32_t st = smem + (uint32_t)s * STAGE_BYTES;
-        const uint32_t sfa_t = tmem + sfa_col + 4u * ATOMS * kb;
-        const uint32_t sfb_t = tmem + sfb_col + SFB_STAGE_COLS * s;
+        const uint32_t res_t = tmem + res_col + 4u * ATOMS * kb;
+        const uint32_t str_t = tmem + str_col + SFB_STAGE_COLS * s;
+        const uint32_t sfa_t = res_a ? res_t : str_t;  // TMEM scales of A and of B for this stage
+        const uint32_t sfb_t = res_a ? str_t : res_t;
         const uint32_t acc0 = kb > 0 ? 1u : 0u;
         if (kb * ATOMS + ATOMS <= katoms_total) {  // a full stage: 8 scale atoms, 8 MMAs
-          if (new_a) {
+          if (new_res) {
 #pragma unroll
-            for (int a = 0; a < ATOMS; ++a) tc_cp_scales(sfa_t + 4 * a, desc_scales(st + SFA_OFF + a * SF_TILE));
+            for (int a = 0; a < ATOMS; ++a) tc_cp_scales(res_t + 4 * a, desc_scales(st + RES_OFF + a * SF_TILE));
           }
 #pragma unroll
-          for (int a = 0; a < ATOMS; ++a) tc_cp_scales(sfb_t + 4 * a, desc_scales(st + SFB_OFF + a * SF_TILE));
+          for (int a = 0; a < ATOMS; ++a) tc_cp_scales(str_t + 4 * a, desc_scales(st + STR_OFF + a * SF_TILE));
 #pragma unroll
           for (int a = 0; a < ATOMS; ++a) {
             const uint32_t ko = (a >> 2) * HALF_BYTES + (a & 3) * 32;  // K offset inside the stage
@@ -324,8 +381,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         } else {  // the partial last stage of a K that is not a multiple of 512
           const int atoms = katoms_total - kb * ATOMS;
           for (int a = 0; a < atoms; ++a) {
-            if (new_a) tc_cp_scales(sfa_t + 4 * a, desc_scales(st + SFA_OFF + a * SF_TILE));
-            tc_cp_scales(sfb_t + 4 * a, desc_scales(st + SFB_OFF + a * SF_TILE));
+            if (new_res) tc_cp_scales(res_t + 4 * a, desc_scales(st + RES_OFF + a * SF_TILE));
+            tc_cp_scales(str_t + 4 * a, desc_scales(st + STR_OFF + a * SF_TILE));
           }
           for (int a = 0; a < atoms; ++a) {
             const uint32_t ko = (a >> 2) * HALF_BYTES + (a & 3) * 32;
@@ -347,8 +404,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp < 4) {
     // ------------------------------------------------------------ epilogue
     int tl = 0;
+    TileCursor cur;
+    cur.seek(tau0, s_poff, E, NT, r128);
     for (int tau = tau0; tau < tau1; ++tau, ++tl) {
-      const Tile t = map_tile(tau, s_poff, E, NT);
+      if (tau > tau0) cur.step(s_poff, E, NT, r128);
+      const Tile t = cur.tile();
       const int r = t.mt * BM + warp * 32 + lane;
       const int p = __ldcg(prm.pair_of_row + r);
       const bool any_real = __any_sync(0xFFFFFFFFu, p >= 0);
