@@ -140,6 +140,12 @@ def fp4moe_quantize_rows_f32(rows, K, inp, g, codes, sf, stream=None):
            "fp4moe_quantize_rows_f32")
 
 
+def fp4moe_selftest_wait_timeout(err, limit_ns, result, stream=None):
+    """One bounded wait that runs out on purpose (a test of the failure path; see include/fp4moe.h)."""
+    _check(_lib.load().fp4moe_selftest_wait_timeout(_p(err), int(limit_ns), _p(result), _s(stream)),
+           "fp4moe_selftest_wait_timeout")
+
+
 def fp4moe_read_error(ws, clear=True, stream=None) -> int:
     v = ctypes.c_uint32()
     _check(_lib.load().fp4moe_read_error(_p(ws), ctypes.byref(v), 1 if clear else 0, _s(stream)), "fp4moe_read_error")

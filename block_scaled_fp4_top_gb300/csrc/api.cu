@@ -370,6 +370,13 @@ fp4moe_status fp4moe_quantize_rows_f32(int32_t rows, int32_t K, const float* in,
   return quant_rows_launch(rows, K, rows > 0 ? rows : 1, 0, 0, in, g, 1, codes, sf, (cudaStream_t)stream);
 }
 
+fp4moe_status fp4moe_selftest_wait_timeout(uint32_t* err, int64_t limit_ns, uint32_t* result, fp4moe_stream_t stream) {
+  if (err == nullptr || result == nullptr) return FP4MOE_INVALID_ARG;
+  if (((reinterpret_cast<uintptr_t>(err) | reinterpret_cast<uintptr_t>(result)) & 3u) != 0) return FP4MOE_MISALIGNED;
+  if (limit_ns < 1000000 || limit_ns > 50000000) return FP4MOE_INVALID_ARG;
+  return selftest_wait_launch(err, limit_ns, result, (cudaStream_t)stream);
+}
+
 fp4moe_status fp4moe_read_error(void* ws, uint32_t* err_host, int32_t clear, fp4moe_stream_t stream) {
   if (ws == nullptr || err_host == nullptr) return FP4MOE_INVALID_ARG;
   const cudaStream_t st = (cudaStream_t)stream;

@@ -71,6 +71,9 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
                           uint8_t* out_codes, uint8_t* out_sf, float* amax, float* o_pairs, uint32_t* err,
                           cudaStream_t st);
 
+// selftest.cu: one bounded wait that runs out (see fp4moe_selftest_wait_timeout)
+fp4moe_status selftest_wait_launch(uint32_t* err, int64_t limit_ns, uint32_t* result, cudaStream_t st);
+
 fp4moe_status combine_launch(const fp4moe_config& cfg, int32_t T, const float* o_pairs, const float* w,
                              uint16_t* y, cudaStream_t st);
 

@@ -342,6 +342,22 @@ fp4moe_status fp4moe_quantize_rows_f32(int32_t rows, int32_t K, const float* in,
                                        uint8_t* sf, fp4moe_stream_t stream);
 
 /*
+ * fp4moe_selftest_wait_timeout: a test of the failure path, with no
+ * counterpart in the source pages. Every spin-wait in the library's kernels
+ * is bounded: when it runs out it sets FP4MOE_ERR_TIMEOUT in the error word,
+ * its kernel returns, and later kernels that see the bit skip their work, so
+ * a lost arrival never hangs the GPU. This call launches one kernel that
+ * waits, through that same routine, on an mbarrier nothing arrives at, for
+ * limit_ns nanoseconds (1 ms .. 50 ms, else FP4MOE_INVALID_ARG).
+ *   err    device uint32 error word (a workspace's first 4 bytes, or any
+ *          4-byte-aligned word); receives FP4MOE_ERR_TIMEOUT.
+ *   result device uint32; receives 0 (the wait gave up) or 1 (it completed,
+ *          which would be a fault in the bounded-wait routine).
+ * Nothing traps or faults: the context stays usable.
+ */
+fp4moe_status fp4moe_selftest_wait_timeout(uint32_t* err, int64_t limit_ns, uint32_t* result, fp4moe_stream_t stream);
+
+/*
  * fp4moe_read_error: copy the workspace's device error word to *err_host.
  * If clear != 0, zero it afterwards. This call SYNCHRONISES `stream`: use it
  * outside graphs, between steps.

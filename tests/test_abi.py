@@ -87,5 +87,8 @@ def test_argument_checks(lib):
     assert lib.moe_route(ctypes.byref(_cfg(w_format=_lib.W_MXFP4)), 8, *args) == _lib.UNSUPPORTED
     assert lib.moe_forward(None, 8, *([p] * 16)) == _lib.INVALID_ARG
     assert lib.fp4moe_quantize_rows_f32(100, 64, p, p, p, p, p) == _lib.INVALID_ARG  # rows % 128
+    assert lib.fp4moe_selftest_wait_timeout(p, 0, p, None) == _lib.INVALID_ARG          # limit below 1 ms
+    assert lib.fp4moe_selftest_wait_timeout(p, 60_000_000, p, None) == _lib.INVALID_ARG  # above 50 ms
+    assert lib.fp4moe_selftest_wait_timeout(ctypes.c_void_p(0x10002), 5_000_000, p, None) == _lib.MISALIGNED
     assert lib.fp4moe_status_string(_lib.CAPACITY) == b"FP4MOE_CAPACITY"
     assert lib.fp4moe_abi_version() == 100
