@@ -44,7 +44,7 @@ FALLBACK_HBM_GBS = 6800.0
 # with, so it is reported while their hash matches and as null otherwise.
 W1_TRAFFIC = {
     # workload name: (bytes per launch, sha256 of the GEMM sources)
-    "dsv4_flash_decode_T64": (1953644800 + 3792384, "5ff759819ed38c92933ef9867a026851c67d95a3f113ea25088c8fb153463db1"),
+    "dsv4_flash_decode_T64": (1954620928 + 3764992, "661d3a3ab411df46d0d7c424ed02b61b6517fd8446cfd87a09554419405869dd"),
 }
 GEMM_SOURCES = ("block_scaled_fp4_top_gb300/csrc/gemm.cu", "block_scaled_fp4_top_gb300/csrc/common.cuh")
 
@@ -271,8 +271,9 @@ def run_ours(args, wl, rank, world):
         "roofline": {"kernel": "grouped_gemm_kernel<W1 SwiGLU requant>", "bound": "hbm", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": w1_bytes + act1, "traffic": w1_traffic(wl.name)},
-        # route: logits_topk + layout_small (T*k <= 4096) or + hist, scan, slots; then quantise-scatter, W1, W2, combine
-        "gpu_launches": ((2 if T * k <= 4096 else 4) + 4) * args.steps,
+        # route: router_mma + router_refine + layout_small (T*k <= 4096) or + hist, scan, slots;
+        # then quantise-scatter, W1, W2, combine
+        "gpu_launches": ((3 if T * k <= 4096 else 5) + 4) * args.steps,
         "e2e": {"value": job_tokens_per_s(T, world, args.steps, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2},
         "clocks": clk.summary(),
