@@ -13,6 +13,11 @@ Source: "Lucifer-CUTLASS TP3 virtual-padding audit".
   logical slice is zero.
 * Section "2. CPU loader tests". The per-rank logical slices concatenate back
   to the source byte for byte.
+* Section "Remaining kernel assumptions". The layer on a shard takes BF16
+  activations with MXFP4 weights. Reading: h is rounded to bf16 before W2,
+  because bf16 is the activation type of this variant. Each rank returns
+  partial rows of the W2 output, and across ranks they sum to the
+  full-width layer.
 
 MXFP4 follows OCP Microscaling v1.0. Each block of 32 elements along K shares
 one E8M0 scale 2^X, with X = floor(log2(amax)) - 2, where 2 is the exponent of
@@ -87,6 +92,91 @@ def mx_quantize_rows(v: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
 
 
 def mx_dequantize(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """codes [R, K] and E8M0 scales [R, K/32] -> fp64 [R, K]."""
     R, K = q.shape
     el = codecs.e2m1_decode(q).reshape(R, K // MX_BLOCK, MX_BLOCK)
     return (el * codecs.e8m0_decode(s)[:, :, None]).reshape(R, K)
+
+
+# ------------------------------------------------------- the MXFP4 layer ----
+
+class MxExpert(NamedTuple):
+    """One expert's kernel-local MXFP4 shard: codes unpacked, scales as E8M0 bytes.
+
+    W13 rows [0, Ik) are the gate, [Ik, 2Ik) are up, each with its zero tail
+    past the logical width. W2 is [H, Ik], whose columns past the logical
+    width are zero codes with zero scale bytes.
+    """
+    w1_q: np.ndarray    # [2 Ik, H]
+    w1_s: np.ndarray    # [2 Ik, H / 32]
+    w2_q: np.ndarray    # [H, Ik]
+    w2_s: np.ndarray    # [H, Ik / 32]
+
+
+def mx_expert_shard(w1_full: np.ndarray, w2_full: np.ndarray, plan: TPPlan, rank: int) -> MxExpert:
+    """Quantise one expert's full logical matrices to MXFP4, then cut rank `rank`'s shard.
+
+    The shard follows "Required loader changes": source offsets counted in
+    logical elements and converted to each tensor's storage unit. W13 takes
+    1 unpacked row per element. Packed W2 takes 2 elements per byte. W2
+    scales take 32 elements per E8M0 group. The destination is zero-filled
+    first.
+    w1_full [2 I, H] (gate rows first), w2_full [H, I] fp32; I is the full width.
+    """
+    I = w2_full.shape[1]
+    q1, s1 = mx_quantize_rows(w1_full)
+    gate_q = shard_axis(q1[:I], 0, I, plan, rank, 1)
+    up_q = shard_axis(q1[I:], 0, I, plan, rank, 1)
+    gate_s = shard_axis(s1[:I], 0, I, plan, rank, 1)
+    up_s = shard_axis(s1[I:], 0, I, plan, rank, 1)
+    q2, s2 = mx_quantize_rows(w2_full)
+    packed = (q2[:, 0::2] | (q2[:, 1::2] << 4)).astype(np.uint8)           # element 2i in the low nibble
+    packed_shard = shard_axis(packed, 1, I, plan, rank, 2)
+    w2_q = np.empty((packed_shard.shape[0], packed_shard.shape[1] * 2), dtype=np.uint8)
+    w2_q[:, 0::2] = packed_shard & 0xF
+    w2_q[:, 1::2] = packed_shard >> 4
+    w2_s = shard_axis(s2, 1, I, plan, rank, 32)
+    return MxExpert(np.concatenate([gate_q, up_q]), np.concatenate([gate_s, up_s]), w2_q, w2_s)
+
+
+def _bf16_round(v: np.ndarray) -> np.ndarray:
+    """fp64 -> fp32 (round to nearest) -> bf16 (round to nearest even), returned as fp64."""
+    b = np.ascontiguousarray(v.astype(np.float32)).view(np.uint32).astype(np.uint64)
+    b = (b + np.uint64(0x7FFF) + ((b >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def mx_expert_out(qe: MxExpert, x: np.ndarray, limit: float) -> np.ndarray:
+    """One expert's partial output rows for bf16-valued token rows x [n, H] (fp64), before the combine.
+
+    [g; u] = W13~ x in fp64; h = silu(min(g, L)) * clamp(u, -L, L), rounded to
+    bf16 (the W2 input of the bf16-activation variant); o = W2~ h.
+    """
+    from .moe import swiglu
+    Ik = qe.w2_q.shape[1]
+    W1 = mx_dequantize(qe.w1_q, qe.w1_s)                                   # [2 Ik, H]
+    gu = x @ W1.T
+    h = _bf16_round(swiglu(gu[:, :Ik], gu[:, Ik:], limit))
+    return h @ mx_dequantize(qe.w2_q, qe.w2_s).T                            # [n, H]
+
+
+def mx_moe_partials(x_bits: np.ndarray, ids: np.ndarray, expert, limit: float) -> np.ndarray:
+    """Per-(token, j) partial rows o [n, k, H] (fp64) of the MXFP4 layer on one rank."""
+    from .moe import bf16_to_f64
+    x = bf16_to_f64(x_bits)
+    n, k = ids.shape
+    outs = np.zeros((n, k, x.shape[1]), dtype=np.float64)
+    for e in np.unique(ids):
+        tt, jj = np.nonzero(ids == e)
+        outs[tt, jj] = mx_expert_out(expert(int(e)), x[tt], limit)
+    return outs
+
+
+def mx_moe_tokens(x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray, expert, limit: float) -> np.ndarray:
+    """The MXFP4 layer on one rank: y = bf16(sum_j w_j o_j) in j order. Returns bf16 bits [n, H]."""
+    from .moe import f32_to_bf16_bits
+    outs = mx_moe_partials(x_bits, ids, expert, limit)
+    acc = np.zeros(outs.shape[::2], dtype=np.float64)
+    for j in range(ids.shape[1]):
+        acc = acc + w[:, j:j + 1] * outs[:, j]
+    return f32_to_bf16_bits(acc.astype(np.float32))

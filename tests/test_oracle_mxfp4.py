@@ -3,8 +3,9 @@ import json
 import os
 
 import numpy as np
+import pytest
 
-from oracle import codecs, mxfp4
+from oracle import codecs, moe, mxfp4
 
 GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "tp3_shard_plan.json")))
 
@@ -64,3 +65,88 @@ def test_mx_scale_is_floor_log2_amax_minus_2():
     d = mxfp4.mx_dequantize(q, s)
     assert d[0, 0] == 6.0 and d[1, 0] == 6.0 and d[2, 0] == 6.0 / 256
     assert (d[3] == 0).all()
+
+
+def _rand_w(rng, rows, cols, scale):
+    return (rng.standard_normal((rows, cols)) * scale).astype(np.float32)
+
+
+def test_tp3_partials_sum_to_the_full_width_layer():
+    """The pin of "4. MoE hardware tests": TP3 shards summed equal the full-width layer (fp64 rounding only).
+    A unit-blind W2 cut (byte offsets 0/384/768 for packed bytes) breaks it."""
+    rng = np.random.default_rng(5)
+    H, I, E, k, n = 64, 192, 3, 2, 5
+    full = [(_rand_w(rng, 2 * I, H, 0.05), _rand_w(rng, H, I, 0.05)) for _ in range(E)]
+    x_bits = moe.f32_to_bf16_bits(rng.standard_normal((n, H)).astype(np.float32))
+    ids = np.array([[0, 1], [2, 0], [1, 2], [0, 2], [1, 0]])
+    p3 = mxfp4.tp_plan(I, 3, 32, 128)
+    p1 = mxfp4.tp_plan(I, 1, 32, 128)
+    assert (p3.logical_per_rank, p3.kernel_local, p1.kernel_local) == (64, 128, 256)
+    ex1 = {e: mxfp4.mx_expert_shard(*full[e], p1, 0) for e in range(E)}
+    ref = mxfp4.mx_moe_partials(x_bits, ids, lambda e: ex1[e], 10.0)
+    tot = np.zeros_like(ref)
+    for r in range(3):
+        ex = {e: mxfp4.mx_expert_shard(*full[e], p3, r) for e in range(E)}
+        tot += mxfp4.mx_moe_partials(x_bits, ids, lambda e: ex[e], 10.0)
+    assert np.allclose(tot, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    # the unit-blind W2 cut of "Packed W2 weight is wrong" (source offsets counted in kernel-width storage
+    # units, rank * 128 columns here, instead of logical ones) does not sum to the layer
+    def unit_blind(e, r):
+        good = mxfp4.mx_expert_shard(*full[e], p3, r)
+        q2, s2 = mxfp4.mx_quantize_rows(full[e][1])
+        Ik = p3.kernel_local
+        q = np.zeros((H, Ik), np.uint8)
+        sc = np.zeros((H, Ik // 32), np.uint8)
+        c = q2[:, r * Ik:(r + 1) * Ik]
+        q[:, :c.shape[1]] = c
+        sc[:, :c.shape[1] // 32] = s2[:, r * Ik // 32:r * Ik // 32 + c.shape[1] // 32]
+        return good._replace(w2_q=q, w2_s=sc)
+    bad = np.zeros_like(ref)
+    for r in range(3):
+        ex = {e: unit_blind(e, r) for e in range(E)}
+        bad += mxfp4.mx_moe_partials(x_bits, ids, lambda e: ex[e], 10.0)
+    assert not np.allclose(bad, ref, rtol=1e-3, atol=1e-6)
+
+
+def test_layer_on_exactly_representable_weights_is_the_textbook_moe():
+    """Weights built as E2M1 x 2^X per 32-block survive MX quantisation exactly, so the oracle's layer must
+    equal a plain dense SwiGLU MoE on the original fp32 weights. That dense layer rounds h to bf16 through
+    torch's own conversion."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(11)
+    H, I, E, k, n, L = 64, 64, 2, 2, 4, 10.0
+    vals = codecs.e2m1_decode(np.arange(16, dtype=np.uint8))
+
+    def exact(rows, cols):
+        q = rng.integers(0, 16, (rows, cols)).astype(np.uint8)
+        q[:, ::32] = rng.choice([6, 7, 14, 15], size=(rows, cols // 32))  # |4| or |6|: amax sets X
+        X = rng.integers(-9, -4, (rows, cols // 32))
+        return (vals[q].reshape(rows, cols // 32, 32) * np.ldexp(1.0, X)[:, :, None]).reshape(rows, cols).astype(np.float32)
+
+    full = [(exact(2 * I, H), exact(H, I)) for _ in range(E)]
+    plan = mxfp4.tp_plan(I, 1, 32, 64)
+    ex = {e: mxfp4.mx_expert_shard(*full[e], plan, 0) for e in range(E)}
+    for e in range(E):
+        assert np.array_equal(mxfp4.mx_dequantize(ex[e].w1_q, ex[e].w1_s), full[e][0].astype(np.float64))
+    x_bits = moe.f32_to_bf16_bits(rng.standard_normal((n, H)).astype(np.float32))
+    ids = np.array([[0, 1], [1, 0], [0, 1], [1, 0]])
+    w = np.array([[0.7, 0.3], [0.6, 0.4], [0.5, 0.5], [0.9, 0.1]])
+    got = mxfp4.mx_moe_tokens(x_bits, ids, w, lambda e: ex[e], L)
+    xt = torch.from_numpy(sg_bf16_to_f32(x_bits)).double()
+    y = torch.zeros(n, H, dtype=torch.float64)
+    for t in range(n):
+        for j in range(k):
+            W1 = torch.from_numpy(full[ids[t, j]][0]).double()
+            W2 = torch.from_numpy(full[ids[t, j]][1]).double()
+            gu = W1 @ xt[t]
+            g, u = gu[:I], gu[I:]
+            h = torch.minimum(g, torch.tensor(L)) * torch.sigmoid(torch.minimum(g, torch.tensor(L))) * u.clamp(-L, L)
+            h = h.float().bfloat16().double()
+            y[t] += float(w[t, j]) * (W2 @ h)
+    ref = y.float().bfloat16().view(torch.int16).numpy().view(np.uint16)
+    ok = (got == ref) | (np.abs(sg_bf16_to_f32(got) - sg_bf16_to_f32(ref)) <= 2 ** -7 * np.abs(sg_bf16_to_f32(ref)))
+    assert ok.all()
+
+
+def sg_bf16_to_f32(u):
+    return (np.ascontiguousarray(u, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
