@@ -185,14 +185,21 @@ class MoELayer:
 
     # ---- load-time prep
     def quantize_weights(self, which: int, e0: int, w: torch.Tensor):
-        """Quantise experts [e0, e0 + w.shape[0]) of W1 (which=1, [n, 2I, H]) or W2 (which=2, [n, H, I])."""
+        """Quantise experts [e0, e0 + w.shape[0]) of W1 (which=1, [n, 2I, H]) or W2 (which=2, [n, H, I]).
+
+        NVFP4 layers quantise to E2M1 with E4M3 scales per 16 and a global scale per expert. MXFP4 layers
+        (w_format MXFP4) quantise to E2M1 with E8M0 scales per 32; their rows are the rank's kernel-local
+        shard, zero past the logical width.
+        """
         cfg, W = self.cfg, self.weights
         n = w.shape[0]
+        E = cfg.num_experts
+        b1, s1, b2, s2 = weight_bytes(cfg)
         if which == 1:
-            per_c, per_s = 2 * cfg.inter * cfg.hidden // 2, 2 * cfg.inter * cfg.hidden // 16
+            per_c, per_s = b1 // E, s1 // E
             codes, sf, gs = W.w1_fp4, W.w1_sf, W.gw1
         else:
-            per_c, per_s = cfg.hidden * cfg.inter // 2, cfg.hidden * cfg.inter // 16
+            per_c, per_s = b2 // E, s2 // E
             codes, sf, gs = W.w2_fp4, W.w2_sf, W.gw2
         fp4moe_quantize_weights(cfg, which, n, w.contiguous(), codes[e0 * per_c:(e0 + n) * per_c],
                                 sf[e0 * per_s:(e0 + n) * per_s], gs[e0:e0 + n])

@@ -25,12 +25,18 @@ fp4moe_status check_cfg(const fp4moe_config* c) {
   if (c->hidden <= 0 || c->inter <= 0 || c->num_experts <= 0 || c->top_k <= 0 || c->max_tokens < 0 ||
       !(c->swiglu_limit > 0.0f))
     return FP4MOE_INVALID_ARG;
-  if (c->w_format != FP4MOE_W_NVFP4) return FP4MOE_UNSUPPORTED;
+  if (c->w_format != FP4MOE_W_NVFP4 && c->w_format != FP4MOE_W_MXFP4) return FP4MOE_UNSUPPORTED;
   if (c->hidden % 256 != 0 || c->inter % 128 != 0) return FP4MOE_UNSUPPORTED;
   if (c->top_k > kMaxTopK || c->num_experts > kMaxExperts || c->top_k > c->num_experts) return FP4MOE_UNSUPPORTED;
-  if (c->inter_logical != 0 && c->inter_logical != c->inter) return FP4MOE_UNSUPPORTED;
+  if (c->w_format == FP4MOE_W_NVFP4) {
+    if (c->inter_logical != 0 && c->inter_logical != c->inter) return FP4MOE_UNSUPPORTED;
+  } else {  // MXFP4: the logical width is whole 32-element scale groups inside the kernel width
+    if (c->inter_logical < 0 || c->inter_logical > c->inter || c->inter_logical % 32 != 0) return FP4MOE_UNSUPPORTED;
+  }
   return FP4MOE_OK;
 }
+
+inline bool is_mx(const fp4moe_config* c) { return c->w_format == FP4MOE_W_MXFP4; }
 
 fp4moe_status check_T(const fp4moe_config* c, int32_t T) {
   if (T < 0) return FP4MOE_INVALID_ARG;
@@ -92,10 +98,11 @@ WsLayout ws_layout(const fp4moe_config& c) {
   L.poff = take(E * 4);
   L.slot = take(Tm * k * 4);
   L.por = take(cap * 4);
-  L.a1 = take(cap * (size_t)c.hidden / 2);
-  L.a1sf = take(cap * (size_t)c.hidden / 16);
-  L.a2 = take(cap * (size_t)c.inter / 2);
-  L.a2sf = take(cap * (size_t)c.inter / 16);
+  const bool mx = c.w_format == FP4MOE_W_MXFP4;  // MXFP4 layers keep their slot activations in bf16
+  L.a1 = take(mx ? cap * (size_t)c.hidden * 2 : cap * (size_t)c.hidden / 2);
+  L.a1sf = take(mx ? 0 : cap * (size_t)c.hidden / 16);
+  L.a2 = take(mx ? cap * (size_t)c.inter * 2 : cap * (size_t)c.inter / 2);
+  L.a2sf = take(mx ? 0 : cap * (size_t)c.inter / 16);
   L.opairs = take(Tm * k * (size_t)c.hidden * 4);
   L.alpha_tmp = take(E * 4);
   L.total = off;
@@ -170,6 +177,13 @@ fp4moe_status fp4moe_weight_bytes(const fp4moe_config* cfg, size_t* w1_codes, si
                                   size_t* w2_sf) {
   FP4_TRY(check_cfg(cfg));
   const size_t E = cfg->num_experts, H = cfg->hidden, I = cfg->inter;
+  if (is_mx(cfg)) {  // atom-tiled: two codes per byte, one E8M0 byte per 32 elements
+    if (w1_codes) *w1_codes = E * 2 * I * H / 2;
+    if (w1_sf) *w1_sf = E * 2 * I * H / 32;
+    if (w2_codes) *w2_codes = E * H * I / 2;
+    if (w2_sf) *w2_sf = E * H * I / 32;
+    return FP4MOE_OK;
+  }
   if (w1_codes) *w1_codes = E * tiled_weight_bytes(2 * cfg->inter, cfg->hidden);
   if (w1_sf) *w1_sf = E * 2 * I * H / 16;
   if (w2_codes) *w2_codes = E * tiled_weight_bytes(cfg->hidden, cfg->inter);
@@ -220,6 +234,11 @@ fp4moe_status moe_quantize_scatter(const fp4moe_config* cfg, int32_t T, const ui
                                    fp4moe_stream_t stream) {
   FP4_TRY(check_cfg(cfg));
   FP4_TRY(check_T(cfg, T));
+  if (is_mx(cfg)) {  // bf16 rows into slot order; gs1 and a1_sf are unused
+    FP4_TRY(check_ptrs(x, slot_of_pair, a1_fp4, ws));
+    return scatter_rows_bf16_launch(*cfg, T, x, slot_of_pair, reinterpret_cast<uint16_t*>(a1_fp4),
+                                    (cudaStream_t)stream);
+  }
   FP4_TRY(check_ptrs(x, gs1, slot_of_pair, a1_fp4, a1_sf, ws));
   return quant_scatter_launch(*cfg, T, x, gs1, slot_of_pair, a1_fp4, a1_sf, (cudaStream_t)stream);
 }
@@ -231,6 +250,12 @@ fp4moe_status moe_grouped_gemm_w1_swiglu(const fp4moe_config* cfg, int32_t T, co
                                          void* ws, fp4moe_stream_t stream) {
   FP4_TRY(check_cfg(cfg));
   FP4_TRY(check_T(cfg, T));
+  if (is_mx(cfg)) {  // bf16 slot rows in and out; a1_sf, alpha1, gs2 and a2_sf are unused
+    FP4_TRY(check_ptrs(a1_fp4, padded_offsets, pair_of_row, w1_fp4, w1_sf, a2_fp4, ws));
+    return mx_gemm_launch(false, *cfg, T, reinterpret_cast<const uint16_t*>(a1_fp4), padded_offsets, pair_of_row,
+                          w1_fp4, w1_sf, reinterpret_cast<uint16_t*>(a2_fp4), nullptr, err_word(ws),
+                          (cudaStream_t)stream);
+  }
   FP4_TRY(check_ptrs(a1_fp4, a1_sf, padded_offsets, pair_of_row, w1_fp4, w1_sf, alpha1, gs2, a2_fp4, a2_sf, ws));
   return gemm_launch(kW1SwiGLU, *cfg, T, a1_fp4, a1_sf, padded_offsets, pair_of_row, w1_fp4, w1_sf, alpha1, gs2,
                      a2_fp4, a2_sf, nullptr, nullptr, err_word(ws), (cudaStream_t)stream);
@@ -242,6 +267,11 @@ fp4moe_status moe_grouped_gemm_w2(const fp4moe_config* cfg, int32_t T, const uin
                                   fp4moe_stream_t stream) {
   FP4_TRY(check_cfg(cfg));
   FP4_TRY(check_T(cfg, T));
+  if (is_mx(cfg)) {
+    FP4_TRY(check_ptrs(a2_fp4, padded_offsets, pair_of_row, w2_fp4, w2_sf, o_pairs, ws));
+    return mx_gemm_launch(true, *cfg, T, reinterpret_cast<const uint16_t*>(a2_fp4), padded_offsets, pair_of_row,
+                          w2_fp4, w2_sf, nullptr, o_pairs, err_word(ws), (cudaStream_t)stream);
+  }
   FP4_TRY(check_ptrs(a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, o_pairs, ws));
   return gemm_launch(kW2Rows, *cfg, T, a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, nullptr,
                      nullptr, nullptr, nullptr, o_pairs, err_word(ws), (cudaStream_t)stream);
@@ -262,9 +292,15 @@ fp4moe_status moe_grouped_gemm_w2_combine(const fp4moe_config* cfg, int32_t T, c
                                           fp4moe_stream_t stream) {
   FP4_TRY(check_cfg(cfg));
   FP4_TRY(check_T(cfg, T));
-  FP4_TRY(check_ptrs(a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, topk_w, y, ws));
   const WsLayout L = ws_layout(*cfg);
   float* o = at<float>(ws, L.opairs);
+  if (is_mx(cfg)) {
+    FP4_TRY(check_ptrs(a2_fp4, padded_offsets, pair_of_row, w2_fp4, w2_sf, topk_w, y, ws));
+    FP4_TRY(mx_gemm_launch(true, *cfg, T, reinterpret_cast<const uint16_t*>(a2_fp4), padded_offsets, pair_of_row,
+                           w2_fp4, w2_sf, nullptr, o, err_word(ws), (cudaStream_t)stream));
+    return combine_launch(*cfg, T, o, topk_w, y, (cudaStream_t)stream);
+  }
+  FP4_TRY(check_ptrs(a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, topk_w, y, ws));
   FP4_TRY(gemm_launch(kW2Rows, *cfg, T, a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, nullptr,
                       nullptr, nullptr, nullptr, o, err_word(ws), (cudaStream_t)stream));
   return combine_launch(*cfg, T, o, topk_w, y, (cudaStream_t)stream);
@@ -277,7 +313,9 @@ fp4moe_status moe_forward(const fp4moe_config* cfg, int32_t T, const uint16_t* x
                           fp4moe_stream_t stream) {
   FP4_TRY(check_cfg(cfg));
   FP4_TRY(check_T(cfg, T));
-  FP4_TRY(check_ptrs(x, router_w, gs1, gs2, w1_fp4, w1_sf, alpha1, w2_fp4, w2_sf, alpha2, y, ws));
+  const bool mx = is_mx(cfg);  // MXFP4: gs1, gs2, alpha1 and alpha2 are unused and may be NULL
+  if (mx) FP4_TRY(check_ptrs(x, router_w, w1_fp4, w1_sf, w2_fp4, w2_sf, y, ws));
+  else FP4_TRY(check_ptrs(x, router_w, gs1, gs2, w1_fp4, w1_sf, alpha1, w2_fp4, w2_sf, alpha2, y, ws));
   FP4_TRY(check_opt(router_bias));
   FP4_TRY(check_opt(topk_ids_out));
   FP4_TRY(check_opt(topk_w_out));
@@ -291,12 +329,20 @@ fp4moe_status moe_forward(const fp4moe_config* cfg, int32_t T, const uint16_t* x
   FP4_TRY(route_launch(*cfg, T, x, router_w, router_bias, at<float>(ws, L.logits), ids, w, at<int32_t>(ws, L.counts),
                        at<int32_t>(ws, L.offsets), poff, at<int32_t>(ws, L.slot), por, at<int32_t>(ws, L.hist),
                        at<float>(ws, L.nw2), err, st));
-  FP4_TRY(quant_scatter_launch(*cfg, T, x, gs1, at<int32_t>(ws, L.slot), at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf),
-                               st));
-  FP4_TRY(gemm_launch(kW1SwiGLU, *cfg, T, at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf), poff, por, w1_fp4, w1_sf,
-                      alpha1, gs2, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), nullptr, nullptr, err, st));
-  FP4_TRY(gemm_launch(kW2Rows, *cfg, T, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), poff, por, w2_fp4, w2_sf,
-                      alpha2, nullptr, nullptr, nullptr, nullptr, at<float>(ws, L.opairs), err, st));
+  if (mx) {
+    uint16_t* a1 = at<uint16_t>(ws, L.a1);
+    uint16_t* a2 = at<uint16_t>(ws, L.a2);
+    FP4_TRY(scatter_rows_bf16_launch(*cfg, T, x, at<int32_t>(ws, L.slot), a1, st));
+    FP4_TRY(mx_gemm_launch(false, *cfg, T, a1, poff, por, w1_fp4, w1_sf, a2, nullptr, err, st));
+    FP4_TRY(mx_gemm_launch(true, *cfg, T, a2, poff, por, w2_fp4, w2_sf, nullptr, at<float>(ws, L.opairs), err, st));
+  } else {
+    FP4_TRY(quant_scatter_launch(*cfg, T, x, gs1, at<int32_t>(ws, L.slot), at<uint8_t>(ws, L.a1),
+                                 at<uint8_t>(ws, L.a1sf), st));
+    FP4_TRY(gemm_launch(kW1SwiGLU, *cfg, T, at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf), poff, por, w1_fp4, w1_sf,
+                        alpha1, gs2, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), nullptr, nullptr, err, st));
+    FP4_TRY(gemm_launch(kW2Rows, *cfg, T, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), poff, por, w2_fp4, w2_sf,
+                        alpha2, nullptr, nullptr, nullptr, nullptr, at<float>(ws, L.opairs), err, st));
+  }
   FP4_TRY(combine_launch(*cfg, T, at<float>(ws, L.opairs), w, y, st));
   const size_t pk = (size_t)T * cfg->top_k;
   if (topk_ids_out && pk && cudaMemcpyAsync(topk_ids_out, ids, pk * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
@@ -311,10 +357,15 @@ fp4moe_status fp4moe_quantize_weights(const fp4moe_config* cfg, int32_t which, i
   FP4_TRY(check_cfg(cfg));
   if (which != 1 && which != 2) return FP4MOE_INVALID_ARG;
   if (n_experts < 0 || n_experts > cfg->num_experts) return FP4MOE_INVALID_ARG;
-  FP4_TRY(check_ptrs(w, codes_out, sf_out, gs_out));
   const cudaStream_t st = (cudaStream_t)stream;
   const int32_t rows = which == 1 ? 2 * cfg->inter : cfg->hidden;
   const int32_t K = which == 1 ? cfg->hidden : cfg->inter;
+  if (is_mx(cfg)) {  // OCP MX scales per 32 elements; no global scale (gs_out is unused)
+    FP4_TRY(check_ptrs(w, codes_out, sf_out));
+    return mx_quant_rows_launch((int64_t)n_experts * rows, K, rows, which == 1 ? cfg->inter : 0, w, codes_out,
+                                sf_out, st);
+  }
+  FP4_TRY(check_ptrs(w, codes_out, sf_out, gs_out));
   FP4_TRY(amax_f32_launch(n_experts, (int64_t)rows * K, w, gs_out, st));
   FP4_TRY(gs_from_amax_launch(n_experts, gs_out, st));
   if (K % 256 != 0 &&  // the last k-stage of every block is padded with zero codes
@@ -336,6 +387,7 @@ fp4moe_status fp4moe_calibrate(const fp4moe_config* cfg, int32_t T, const uint16
                                const float* gw1, float* gs1_out, float* gs2_out, void* ws, fp4moe_stream_t stream) {
   FP4_TRY(check_cfg(cfg));
   FP4_TRY(check_T(cfg, T));
+  if (is_mx(cfg)) return FP4MOE_UNSUPPORTED;  // MXFP4 layers keep bf16 activations: no global scales
   FP4_TRY(check_ptrs(x_warm, router_w, w1_fp4, w1_sf, gw1, gs1_out, gs2_out, ws));
   FP4_TRY(check_opt(router_bias));
   const cudaStream_t st = (cudaStream_t)stream;

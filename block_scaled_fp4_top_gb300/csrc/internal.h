@@ -74,6 +74,17 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
 // selftest.cu: one bounded wait that runs out (see fp4moe_selftest_wait_timeout)
 fp4moe_status selftest_wait_launch(uint32_t* err, int64_t limit_ns, uint32_t* result, cudaStream_t st);
 
+// mxgemm.cu: MXFP4 weights x bf16 activations. w2 = false: W1 with SwiGLU into bf16 rows out_bf16 [cap][I];
+// w2 = true: W2 into fp32 rows o_pairs [T*k][H]. Weights in the atom-tiled MXFP4 layout (see fp4moe.h).
+fp4moe_status mx_gemm_launch(bool w2, const fp4moe_config& cfg, int32_t T, const uint16_t* a_bf16,
+                             const int32_t* poff, const int32_t* pair_of_row, const uint8_t* b_codes,
+                             const uint8_t* b_sf, uint16_t* out_bf16, float* o_pairs, uint32_t* err,
+                             cudaStream_t st);
+fp4moe_status mx_quant_rows_launch(int64_t n_rows, int32_t K, int32_t rows_per_group, int32_t inter, const float* in,
+                                   uint8_t* codes, uint8_t* sf, cudaStream_t st);
+fp4moe_status scatter_rows_bf16_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x,
+                                       const int32_t* slot_of_pair, uint16_t* a1, cudaStream_t st);
+
 fp4moe_status combine_launch(const fp4moe_config& cfg, int32_t T, const float* o_pairs, const float* w,
                              uint16_t* y, cudaStream_t st);
 

@@ -66,17 +66,6 @@ struct RouterParams {
   uint32_t* err;
 };
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kWaitLimitNs) return;
-  }
-}
-
 // sum of squares of 8 bf16 values packed in a uint4
 __device__ __forceinline__ float sumsq8(uint4 v, float a) {
   a = fmaf(bf16_lo(v.x), bf16_lo(v.x), a);

@@ -84,7 +84,14 @@ def test_argument_checks(lib):
     # unsupported shapes / format
     assert lib.moe_route(ctypes.byref(_cfg(hidden=4000)), 8, *args) == _lib.UNSUPPORTED
     assert lib.moe_route(ctypes.byref(_cfg(top_k=17)), 8, *args) == _lib.UNSUPPORTED
-    assert lib.moe_route(ctypes.byref(_cfg(w_format=_lib.W_MXFP4)), 8, *args) == _lib.UNSUPPORTED
+    assert lib.moe_route(ctypes.byref(_cfg(w_format=2)), 8, *args) == _lib.UNSUPPORTED          # unknown format
+    # MXFP4: the logical width must be whole 32-element groups inside the kernel width
+    assert lib.moe_route(ctypes.byref(_cfg(w_format=_lib.W_MXFP4, inter=768, inter_logical=800)), 8,
+                         *args) == _lib.UNSUPPORTED
+    assert lib.moe_route(ctypes.byref(_cfg(w_format=_lib.W_MXFP4, inter=768, inter_logical=700)), 8,
+                         *args) == _lib.UNSUPPORTED
+    assert lib.fp4moe_calibrate(ctypes.byref(_cfg(w_format=_lib.W_MXFP4, inter=768, inter_logical=704)), 8,
+                                *([p] * 10)) == _lib.UNSUPPORTED
     assert lib.moe_forward(None, 8, *([p] * 16)) == _lib.INVALID_ARG
     assert lib.fp4moe_quantize_rows_f32(100, 64, p, p, p, p, p) == _lib.INVALID_ARG  # rows % 128
     assert lib.fp4moe_selftest_wait_timeout(p, 0, p, None) == _lib.INVALID_ARG          # limit below 1 ms

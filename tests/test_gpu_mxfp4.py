@@ -1,0 +1,166 @@
+"""GPU: the MXFP4 TP3 shard variant against the oracle.
+
+This is the case of "Lucifer-CUTLASS TP3 virtual-padding audit": BF16
+activations with MXFP4 expert weights (E2M1 codes and one E8M0 scale per 32
+elements). Each rank holds a shard of logical width align_up(ceil(I / 3), 32)
+inside a kernel width rounded up to 128, and everything past the logical
+width is zero.
+
+The library quantises the kernel-local fp32 shard. Its codes and scale bytes
+must equal, bit for bit, those of the oracle's quantise-then-shard path. That
+path cuts the full-width tensors in logical units converted to each storage
+unit.
+
+The layer's outputs must meet the float bar against the oracle's layer, and
+the top-k ids must match exactly:
+* at a tiny TP3 shape, on all three ranks and all tokens;
+* at the DeepSeek-V4-Flash shard (hidden 4096, 704 of 768, 256 experts,
+  top-k 6, T = 512), on rank 0 and sampled tokens.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import synthgen as sg
+from helpers import bits_to_torch, ensure_built, float_parity, torch_to_bits
+from oracle import moe, mxfp4
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def untile_mx(codes: np.ndarray, sf: np.ndarray, E: int, R: int, K: int):
+    """Atom-tiled MXFP4 weights -> codes [E, R, K] and E8M0 bytes [E, R, K/32], rows in kernel order."""
+    ka = K // 64
+    c = codes.reshape(E, R // 128, ka, 128, 32)          # [e][row tile][atom][row][byte]
+    c = c.transpose(0, 1, 3, 2, 4).reshape(E, R, ka * 32)
+    q = np.empty((E, R, K), np.uint8)
+    q[:, :, 0::2] = c & 0xF
+    q[:, :, 1::2] = c >> 4
+    s = sf.reshape(E, R // 128, ka, 128, 2).transpose(0, 1, 3, 2, 4).reshape(E, R, K // 32)
+    return q, s
+
+
+def kernel_to_logical_w1(q: np.ndarray, Ik: int) -> np.ndarray:
+    """W1 rows from kernel order (gate/up interleaved per 64 features) back to gate rows then up rows."""
+    kr = np.arange(2 * Ik)
+    f = (kr // 128) * 64 + (kr % 128) % 64
+    logical = np.where((kr % 128) < 64, f, Ik + f)
+    out = np.empty_like(q)
+    out[:, logical] = q
+    return out
+
+
+def shard_fp32(w1_full, w2_full, plan, rank):
+    """The kernel-local fp32 shard the library quantises: logical rows / columns, zero past them."""
+    I = w2_full.shape[-1]
+    Ik, Il = plan.kernel_local, plan.logical_per_rank
+    a, n = rank * Il, max(0, min(Il, I - rank * Il))
+    w1 = np.zeros(w1_full.shape[:-2] + (2 * Ik, w1_full.shape[-1]), np.float32)
+    w1[..., :n, :] = w1_full[..., a:a + n, :]
+    w1[..., Ik:Ik + n, :] = w1_full[..., I + a:I + a + n, :]
+    w2 = np.zeros(w2_full.shape[:-1] + (Ik,), np.float32)
+    w2[..., :n] = w2_full[..., a:a + n]
+    return w1, w2
+
+
+def _mx_layer(H, Ik, Il, E, k, T):
+    from block_scaled_fp4_top_gb300 import _lib, api
+    cfg = api.config(H, Ik, E, k, T, 10.0, inter_logical=Il, w_format=_lib.W_MXFP4)
+    return api.MoELayer(cfg)
+
+
+def _forward(layer, x_bits, k):
+    import torch
+    T = x_bits.shape[0]
+    y = torch.empty(T, layer.cfg.hidden, dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    layer.forward(bits_to_torch(x_bits), y, ids)
+    torch.cuda.synchronize()
+    assert layer.read_error() == 0
+    return torch_to_bits(y), ids.cpu().numpy().reshape(T, k)
+
+
+def test_tiny_tp3_all_ranks():
+    import torch
+    rng = np.random.default_rng(21)
+    H, I, E, k, T = 256, 192, 8, 2, 16
+    plan = mxfp4.tp_plan(I, 3, 32, 128)
+    Ik, Il = plan.kernel_local, plan.logical_per_rank
+    assert (Il, Ik) == (64, 128)
+    w1f = (rng.standard_normal((E, 2 * I, H)) * 0.05).astype(np.float32)
+    w2f = (rng.standard_normal((E, H, I)) * 0.05).astype(np.float32)
+    router = moe.f32_to_bf16_bits((rng.standard_normal((E, H)) / 16).astype(np.float32))
+    x_bits = moe.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    ids_ref, w_ref = moe.topk_softmax(moe.router_logits(x_bits, router), k)
+    y_sum = np.zeros((T, H))
+    for rank in range(3):
+        layer = _mx_layer(H, Ik, Il, E, k, T)
+        w1l, w2l = shard_fp32(w1f, w2f, plan, rank)
+        layer.quantize_weights(1, 0, torch.from_numpy(w1l).cuda())
+        layer.quantize_weights(2, 0, torch.from_numpy(w2l).cuda())
+        layer.set_router(bits_to_torch(router))
+        torch.cuda.synchronize()
+        ex = {e: mxfp4.mx_expert_shard(w1f[e], w2f[e], plan, rank) for e in range(E)}
+        # codes and scale bytes, bit for bit
+        q1, s1 = untile_mx(layer.weights.w1_fp4.cpu().numpy(), layer.weights.w1_sf.cpu().numpy(), E, 2 * Ik, H)
+        q2, s2 = untile_mx(layer.weights.w2_fp4.cpu().numpy(), layer.weights.w2_sf.cpu().numpy(), E, H, Ik)
+        for e in range(E):
+            assert np.array_equal(kernel_to_logical_w1(q1[e:e + 1], Ik)[0], ex[e].w1_q), (rank, e)
+            assert np.array_equal(kernel_to_logical_w1(s1[e:e + 1], Ik)[0], ex[e].w1_s), (rank, e)
+            assert np.array_equal(q2[e], ex[e].w2_q) and np.array_equal(s2[e], ex[e].w2_s), (rank, e)
+        y, ids = _forward(layer, x_bits, k)
+        assert (ids == ids_ref).all()
+        y_ref = mxfp4.mx_moe_tokens(x_bits, ids_ref, w_ref, lambda e: ex[e], 10.0)
+        float_parity(sg.bf16_bits_to_f32(y), sg.bf16_bits_to_f32(y_ref))
+        y_sum += sg.bf16_bits_to_f32(y)
+    # the three ranks' outputs sum to the full-width layer
+    plan1 = mxfp4.tp_plan(I, 1, 32, 64)
+    ex1 = {e: mxfp4.mx_expert_shard(w1f[e], w2f[e], plan1, 0) for e in range(E)}
+    y_full = mxfp4.mx_moe_tokens(x_bits, ids_ref, w_ref, lambda e: ex1[e], 10.0)
+    float_parity(y_sum, sg.bf16_bits_to_f32(y_full))
+
+
+def test_dsv4_tp3_rank0_sampled_tokens():
+    import torch
+    from synthgen import gpu as sgpu
+    wl = sg.TP3_MXFP4
+    wl_full = dataclasses.replace(wl, I=2048, I_logical=2048)  # the generator's view of the unsharded experts
+    plan = mxfp4.tp_plan(2048, 3, 32, 128)
+    Ik, Il = plan.kernel_local, plan.logical_per_rank
+    assert (Il, Ik, wl.I, wl.I_logical) == (704, 768, 768, 704)
+    rank, chunk = 0, 8
+    layer = _mx_layer(wl.H, Ik, Il, wl.E, wl.k, wl.T)
+    for e0 in range(0, wl.E, chunk):
+        w1f = sgpu.expert_w1(wl_full, e0, chunk)
+        w1l = torch.zeros(chunk, 2 * Ik, wl.H, dtype=torch.float32, device="cuda")
+        w1l[:, :Il] = w1f[:, rank * Il:rank * Il + Il]
+        w1l[:, Ik:Ik + Il] = w1f[:, 2048 + rank * Il:2048 + rank * Il + Il]
+        del w1f
+        layer.quantize_weights(1, e0, w1l)
+        w2f = sgpu.expert_w2(wl_full, e0, chunk)
+        w2l = torch.zeros(chunk, wl.H, Ik, dtype=torch.float32, device="cuda")
+        w2l[:, :, :Il] = w2f[:, :, rank * Il:rank * Il + Il]
+        del w2f
+        layer.quantize_weights(2, e0, w2l)
+        torch.cuda.synchronize()
+    layer.set_router(sgpu.router(wl))
+    x_bits = sg.activations_bf16(wl, sg.EVAL_SEED)
+    y, ids = _forward(layer, x_bits, wl.k)
+    ids_ref, w_ref = moe.topk_softmax(moe.router_logits(x_bits, sg.router_bf16(wl)), wl.k)
+    assert (ids == ids_ref).all()
+    rows = np.array([0, 511])
+    cache = {}
+
+    def expert(e):
+        if e not in cache:
+            cache[e] = mxfp4.mx_expert_shard(sg.expert_w1_f32(wl_full, e), sg.expert_w2_f32(wl_full, e), plan, rank)
+        return cache[e]
+
+    y_ref = mxfp4.mx_moe_tokens(x_bits[rows], ids_ref[rows], w_ref[rows], expert, wl.swiglu_limit)
+    float_parity(sg.bf16_bits_to_f32(y[rows]), sg.bf16_bits_to_f32(y_ref))
