@@ -84,10 +84,34 @@
  *  - alpha1[e] = 1 / (gs1 * gw1[e]) and alpha2[e] = 1 / (gs2 * gw2[e]),
  *    written by fp4moe_make_alpha.
  *
+ * MXFP4 layers (w_format == FP4MOE_W_MXFP4) are the TP3 shard variant of
+ * "Lucifer-CUTLASS TP3 virtual-padding audit", section "Remaining kernel
+ * assumptions": BF16 activations with MXFP4 weights.
+ *  - cfg->inter is the kernel-local width (a multiple of 128).
+ *    cfg->inter_logical is the rank's logical width (a multiple of 32, at
+ *    most inter). W1 rows and W2 columns past it must be zero ("Required
+ *    loader changes", item 5).
+ *  - Weights: E2M1 codes with one E8M0 scale per 32 elements along K (OCP
+ *    Microscaling v1.0), written by fp4moe_quantize_weights from the fp32
+ *    kernel-local shard, in an atom-tiled layout. Blocks of one expert, one
+ *    128-row tile and one 64-element K atom are ordered [expert][row
+ *    tile][atom]:
+ *      codes: 4096 bytes per block, row i at bytes 32i .. 32i+31, element 2c
+ *        in the low nibble of byte c;
+ *      scales: 256 bytes per block, row i at bytes 2i (elements 0..31 of the
+ *        atom) and 2i+1 (elements 32..63).
+ *    W1 rows are in the kernel order above. There are no global scales: gw1,
+ *    gw2, gs1, gs2 and alpha are unused, and may be NULL in these calls.
+ *  - Activations in slot order stay bf16: a1_fp4 is [CAP][H] bf16 and
+ *    a2_fp4 is [CAP][I] bf16. a1_sf and a2_sf are unused.
+ *  - W1: h = silu(min(g, L)) * clamp(u, -L, L) is rounded to bf16. W2 and
+ *    the combine are those of the NVFP4 layer. fp4moe_calibrate returns
+ *    FP4MOE_UNSUPPORTED.
+ *
  * Supported shapes: H % 256 == 0, I % 128 == 0, H <= 4608, I <= 4608 (the
  * activation scales of a 128-row tile stay resident in TMEM for all of K),
- * 1 <= k <= 16, k <= E <= 1024,
- * w_format == FP4MOE_W_NVFP4. Anything else returns FP4MOE_UNSUPPORTED.
+ * 1 <= k <= 16, k <= E <= 1024, w_format FP4MOE_W_NVFP4 or FP4MOE_W_MXFP4.
+ * Anything else returns FP4MOE_UNSUPPORTED.
  */
 #ifndef FP4MOE_H_
 #define FP4MOE_H_
@@ -307,6 +331,14 @@ fp4moe_status moe_forward(const fp4moe_config* cfg, int32_t T, const uint16_t* x
  * expert e. Codes and swizzled scales go to the layouts described above.
  * Experts are independent, so a caller may convert them in chunks by passing
  * offset pointers.
+ * MXFP4 layers: w is the rank's kernel-local fp32 shard (I = cfg->inter,
+ * zero past inter_logical). Every 32 elements along K share the scale
+ * 2^X, X = floor(log2(amax)) - 2 clamped to [-127, 127] (-127 for an
+ * all-zero block). The codes are E2M1(v / 2^X) with round-to-nearest-even and
+ * saturation. They go to the atom-tiled MXFP4 layout, and gs_out is unused.
+ * Because 32-element groups never straddle a shard boundary, quantising the
+ * shard gives the same bytes as quantising the full tensor and cutting it
+ * ("Packed W2 weight is wrong", "W2 E8M0 scales are wrong").
  * Source: "Current Bug", "vLLM Integration Status" (weight stacking
  * make_b_k_major + assemble_scales_3d_side).
  */
