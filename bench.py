@@ -135,8 +135,10 @@ class ClockSampler:
 
 def setup_layer(wl, max_tokens):
     import torch
-    from block_scaled_fp4_top_gb300 import api
+    from block_scaled_fp4_top_gb300 import _lib, api
     from synthgen import gpu as sgpu
+    if wl.w_format == _lib.W_MXFP4:
+        return setup_mx_layer(wl, max_tokens)
     cfg = api.config(wl.H, wl.I, wl.E, wl.k, max_tokens, wl.swiglu_limit)
     layer = api.MoELayer(cfg)
     for e0 in range(0, wl.E, 16):
@@ -151,6 +153,39 @@ def setup_layer(wl, max_tokens):
     return cfg, layer
 
 
+def setup_mx_layer(wl, max_tokens, rank=0, tp=3):
+    """Rank `rank` of a TP `tp` MXFP4 shard: the full-width synthetic experts (intermediate 2048) cut in logical
+    units, zero past the logical width, quantised by the library."""
+    import dataclasses
+    import torch
+    from block_scaled_fp4_top_gb300 import _lib, api
+    from synthgen import gpu as sgpu
+    I_full = 2048
+    Il, Ik = wl.I_logical, wl.I
+    full = dataclasses.replace(wl, I=I_full, I_logical=I_full)
+    cfg = api.config(wl.H, Ik, wl.E, wl.k, max_tokens, wl.swiglu_limit, inter_logical=Il, w_format=_lib.W_MXFP4)
+    layer = api.MoELayer(cfg)
+    a = rank * Il
+    n = max(0, min(Il, I_full - a))
+    for e0 in range(0, wl.E, 8):
+        c = min(8, wl.E - e0)
+        w1f = sgpu.expert_w1(full, e0, c)
+        w1 = torch.zeros(c, 2 * Ik, wl.H, dtype=torch.float32, device="cuda")
+        w1[:, :n] = w1f[:, a:a + n]
+        w1[:, Ik:Ik + n] = w1f[:, I_full + a:I_full + a + n]
+        del w1f
+        layer.quantize_weights(1, e0, w1)
+        w2f = sgpu.expert_w2(full, e0, c)
+        w2 = torch.zeros(c, wl.H, Ik, dtype=torch.float32, device="cuda")
+        w2[:, :, :n] = w2f[:, :, a:a + n]
+        del w2f
+        layer.quantize_weights(2, e0, w2)
+    layer.set_router(sgpu.router(wl), None)
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return cfg, layer
+
+
 def run_ours(args, wl, rank, world):
     import torch
     from block_scaled_fp4_top_gb300 import api
@@ -159,6 +194,7 @@ def run_ours(args, wl, rank, world):
     torch.cuda.set_device(dev)
     cfg, layer = setup_layer(wl, wl.T)
     T, H, k, E = wl.T, wl.H, wl.k, wl.E
+    mx = wl.w_format == 1
     x = sgpu.activations(wl, sg.EVAL_SEED + rank)
     y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     W = layer.weights
@@ -167,10 +203,12 @@ def run_ours(args, wl, rank, world):
     bufs = dict(logits=torch.empty(T, E, dtype=torch.float32, device=dev), ids=torch.empty(T * k, **i32),
                 w=torch.empty(T * k, dtype=torch.float32, device=dev), counts=torch.empty(E, **i32),
                 offsets=torch.empty(E, **i32), poff=torch.empty(E, **i32), slot=torch.empty(T * k, **i32),
-                por=torch.empty(cap, **i32), a1=torch.empty(cap * H // 2, dtype=torch.uint8, device=dev),
-                a1sf=torch.empty(cap * H // 16, dtype=torch.uint8, device=dev),
-                a2=torch.empty(cap * wl.I // 2, dtype=torch.uint8, device=dev),
-                a2sf=torch.empty(cap * wl.I // 16, dtype=torch.uint8, device=dev))
+                por=torch.empty(cap, **i32),
+                # slot activations: NVFP4 codes + scales, or bf16 rows for MXFP4 layers
+                a1=torch.empty(cap * H * 2 if mx else cap * H // 2, dtype=torch.uint8, device=dev),
+                a1sf=torch.empty(16 if mx else cap * H // 16, dtype=torch.uint8, device=dev),
+                a2=torch.empty(cap * wl.I * 2 if mx else cap * wl.I // 2, dtype=torch.uint8, device=dev),
+                a2sf=torch.empty(16 if mx else cap * wl.I // 16, dtype=torch.uint8, device=dev))
     b = bufs
     stream = torch.cuda.current_stream()
     n_stage = 5
@@ -223,9 +261,13 @@ def run_ours(args, wl, rank, world):
     n_active = int((counts > 0).sum())
     R = int(b["poff"][-1].item())
     I = wl.I
-    w1_bytes = n_active * (2 * I * H // 2 + 2 * I * H // 16)
-    w2_bytes = n_active * (H * I // 2 + H * I // 16)
-    act1 = T * k * (H // 2 + H // 16) + T * k * (I // 2 + I // 16)   # A1 real rows read, A2 real rows written
+    sfdiv = 32 if mx else 16  # elements per block scale
+    w1_bytes = n_active * (2 * I * H // 2 + 2 * I * H // sfdiv)
+    w2_bytes = n_active * (H * I // 2 + H * I // sfdiv)
+    if mx:   # A1 real rows read, A2 real rows written: bf16 rows
+        act1 = T * k * H * 2 + T * k * I * 2
+    else:
+        act1 = T * k * (H // 2 + H // 16) + T * k * (I // 2 + I // 16)
     layer_bytes = w1_bytes + w2_bytes + E * H * 2 + 2 * T * H * 2
     peak, peak_kind = peaks()
     w1_ms = stage_ms["w1_swiglu_requant"]
@@ -259,7 +301,8 @@ def run_ours(args, wl, rank, world):
     out = {
         "metric": METRIC, "value": job_tokens_per_s(T, world, args.steps, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, e4m3 block scales, fp32 accumulate)",
+        "scaling": "weak", "vs_baseline": None, "dtype": ("mxfp4 weights x bf16 activations (exact bf16 expansion, fp32 accumulate)" if mx
+                                                         else "nvfp4 (e2m1 x e2m1, e4m3 block scales, fp32 accumulate)"),
         "data": "synthetic (seeded SplitMix64 / Irwin-Hall normal; NVFP4 weights quantised from N(0,0.02))",
         "config": {"workload": wl.name, "T": T, "H": H, "I": I, "E": E, "top_k": k, "swiglu_limit": wl.swiglu_limit,
                    "parallelism": f"replicas x{world}", "l2": "inputs larger than L2: ~2.8 GB of expert weights "
@@ -268,7 +311,8 @@ def run_ours(args, wl, rank, world):
         "layer_hbm_gbs": layer_bytes / (step_ms * 1e-3) / 1e9,
         "layer_algorithmic_bytes": layer_bytes, "n_active_experts": n_active, "padded_rows": R,
         "stages_us": {n: v * 1e3 for n, v in stage_ms.items()},
-        "roofline": {"kernel": "grouped_gemm_kernel<W1 SwiGLU requant>", "bound": "hbm", "achieved": achieved,
+        "roofline": {"kernel": "mx_gemm_kernel<W1 SwiGLU bf16>" if mx else "grouped_gemm_kernel<W1 SwiGLU requant>",
+                     "bound": "hbm", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": w1_bytes + act1, "traffic": w1_traffic(wl.name)},
         # route: router_mma + router_refine + layout_small (T*k <= 4096) or + hist, scan, slots;
@@ -283,16 +327,23 @@ def run_ours(args, wl, rank, world):
 
 def oracle_sample_time(wl, n_tokens: int, repeats: int = 1):
     """The oracle, as it stands, on the first n_tokens of the evaluation batch. Returns (tokens/s, seconds)."""
-    from oracle import moe
+    import dataclasses
+    from oracle import moe, mxfp4
     x = sg.activations_bf16(wl, sg.EVAL_SEED, T=n_tokens)
     wr = sg.router_bf16(wl)
     bias = sg.router_bias_f32(wl)
     ids, w = moe.topk_softmax(moe.router_logits(x, wr, bias), wl.k)
     cache = {}
+    mx = wl.w_format == 1
+    full = dataclasses.replace(wl, I=2048, I_logical=2048)
+    plan = mxfp4.tp_plan(2048, 3, 32, 128)
 
     def expert(e):
         if e not in cache:
-            cache[e] = moe.quantize_expert(sg.expert_w1_f32(wl, e), sg.expert_w2_f32(wl, e))
+            if mx:   # rank 0 of the TP3 shard, as the GPU arm runs it
+                cache[e] = mxfp4.mx_expert_shard(sg.expert_w1_f32(full, e), sg.expert_w2_f32(full, e), plan, 0)
+            else:
+                cache[e] = moe.quantize_expert(sg.expert_w1_f32(wl, e), sg.expert_w2_f32(wl, e))
         return cache[e]
 
     for e in np.unique(ids):   # weight prep is load time, outside the timed region
@@ -304,7 +355,10 @@ def oracle_sample_time(wl, n_tokens: int, repeats: int = 1):
     for _ in range(repeats):
         l = moe.router_logits(x, wr, bias)
         ids, w = moe.topk_softmax(l, wl.k)
-        moe.moe_tokens(x, ids, w, expert, gs1, gs2, wl.swiglu_limit)
+        if mx:
+            mxfp4.mx_moe_tokens(x, ids, w, expert, wl.swiglu_limit)
+        else:
+            moe.moe_tokens(x, ids, w, expert, gs1, gs2, wl.swiglu_limit)
     dt = time.perf_counter() - t0
     return n_tokens * repeats / dt, dt
 

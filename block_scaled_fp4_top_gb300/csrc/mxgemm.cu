@@ -17,11 +17,12 @@
 //   producer (warp 4)      TMA: the atom's activation rows (bf16, 128-byte
 //                          swizzle); bulk copies: the weight atom's 4 KB of
 //                          codes and 256 B of scales.
-//   converters (warps 6-9) thread j expands weight row j into 128 bytes of
-//                          bf16 in the tensor cores' 128-byte-swizzled layout.
-//                          A 256-entry table maps a code byte to its two bf16
-//                          values, and a bf16x2 multiply applies the scale
-//                          exactly.
+//   converters (warps 6-13) two threads expand weight row j into 128 bytes of
+//                          bf16 in the tensor cores' 128-byte-swizzled layout:
+//                          byte permutes map eight codes at a time to their
+//                          exact bf16 patterns (integer ALU work, no
+//                          conversion unit), and a bf16x2 multiply by the
+//                          power of two applies the scale exactly.
 //   MMA issuer (warp 5)    4 MMAs of K = 16 per atom into a TMEM accumulator
 //                          (two buffers).
 //   epilogue (warps 0-3)   W1: the clamped SwiGLU on gate columns 0-63 and up
@@ -54,7 +55,7 @@ constexpr int MX_STAGE = 40960;
 constexpr int MX_STAGES = 5;
 constexpr int MX_BAR_OFF = MX_STAGES * MX_STAGE;
 constexpr int MX_SMEM = MX_BAR_OFF + 256 + 1024;
-constexpr int MX_THREADS = 320;
+constexpr int MX_THREADS = 448;            // 4 epilogue, producer, MMA, 8 converter warps
 constexpr uint32_t MX_TMEM_COLS = 256;      // two 128-column accumulators
 static_assert(MX_STAGE % 1024 == 0 && MX_BB_OFF % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(MX_SMEM + 4 * kMaxExperts + 1024 + 64 <= 232448, "shared memory budget (dynamic + static)");
@@ -80,24 +81,36 @@ __device__ __forceinline__ void cta_range(int total, int& tau0, int& tau1) {
   tau1 = (int)(((long long)total * (blockIdx.x + 1)) / gridDim.x);
 }
 
-// bf16 bit pattern of E2M1 code c (sign in bit 3)
-__device__ __forceinline__ uint32_t e2m1_bf16_bits(uint32_t c) {
-  const uint32_t mag[8] = {0x0000u, 0x3F00u, 0x3F80u, 0x3FC0u, 0x4000u, 0x4040u, 0x4080u, 0x40C0u};
-  return mag[c & 7u] | ((c & 8u) << 12);
+// Eight E2M1 codes (w, element i in bits 4i .. 4i+3) as eight bf16 values: out[i] holds elements 2i (low
+// half) and 2i + 1. The magnitude index (bits 0-2) picks the low and the high byte of each bf16 pattern
+// from two 8-byte tables with byte permutes; a multiply by a sum of two powers of two moves each code's
+// sign bit (bit 3) to bit 15 or bit 31 of its word. The tables hold 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+__device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, uint32_t (&out)[4]) {
+  constexpr uint32_t kLo03 = 0xC0800000u, kLo47 = 0xC0804000u;  // low bytes of the bf16 patterns
+  constexpr uint32_t kHi03 = 0x3F3F3F00u, kHi47 = 0x40404040u;  // high bytes
+  const uint32_t m = w & 0x77777777u;                           // selector nibbles stay below 8
+  const uint32_t lo0 = __byte_perm(kLo03, kLo47, m), hi0 = __byte_perm(kHi03, kHi47, m);
+  const uint32_t lo1 = __byte_perm(kLo03, kLo47, m >> 16), hi1 = __byte_perm(kHi03, kHi47, m >> 16);
+  const uint32_t wh = w >> 16;
+  out[0] = __byte_perm(lo0, hi0, 0x5140) | (((w & 0x88u) * 0x01001000u) & 0x80008000u);
+  out[1] = __byte_perm(lo0, hi0, 0x7362) | (((w & 0x8800u) * 0x00010010u) & 0x80008000u);
+  out[2] = __byte_perm(lo1, hi1, 0x5140) | (((wh & 0x88u) * 0x01001000u) & 0x80008000u);
+  out[3] = __byte_perm(lo1, hi1, 0x7362) | (((wh & 0x8800u) * 0x00010010u) & 0x80008000u);
 }
 
-// bf16 bit pattern of the E8M0 scale 2^(s - 127) (255 is NaN)
-__device__ __forceinline__ uint32_t e8m0_bf16_bits(uint32_t s) {
-  if (s == 255u) return 0x7FC0u;
-  if (s == 0u) return 0x0040u;  // 2^-127: a bf16 subnormal
-  return s << 7;
-}
-
+// bf16x2 product; exact here, since one factor is a power of two
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
   __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);
   __nv_bfloat162 z = __hmul2(x, y);
   return *reinterpret_cast<uint32_t*>(&z);
+}
+
+// bf16 bit pattern of the E8M0 scale 2^(s - 127) (255 is NaN; 0 is the subnormal 2^-127)
+__device__ __forceinline__ uint32_t e8m0_bf16_bits(uint32_t s) {
+  if (s == 255u) return 0x7FC0u;
+  if (s == 0u) return 0x0040u;
+  return s << 7;
 }
 
 // silu(min(g, L)) * clamp(u, -L, L), as in gemm.cu
@@ -119,7 +132,6 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_poff[kMaxExperts];
-  __shared__ uint32_t s_lut[256];
 
   pdl_wait();
   pdl_trigger();
@@ -142,9 +154,6 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
   const uint32_t bar_drain = bar_tempty + 16;
 
   for (int e = threadIdx.x; e < E; e += MX_THREADS) s_poff[e] = __ldcg(prm.poff + e);
-  // code byte b -> its two bf16 values, element 2i (low nibble) in the low half
-  for (int b = threadIdx.x; b < 256; b += MX_THREADS)
-    s_lut[b] = e2m1_bf16_bits((uint32_t)b & 15u) | (e2m1_bf16_bits((uint32_t)b >> 4) << 16);
   if (warp == 0) {
     tmem_alloc(smem_u32(&s_tmem), MX_TMEM_COLS);
     tmem_relinquish();
@@ -152,7 +161,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
   if (threadIdx.x == 128) {
     for (int s = 0; s < MX_STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_conv + 8 * s, 4);   // one arrive per converter warp
+      mbar_init(bar_conv + 8 * s, 8);   // one arrive per converter warp
       mbar_init(bar_empty + 8 * s, 1);  // the MMA commit
     }
     for (int b = 0; b < 2; ++b) {
@@ -213,28 +222,25 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
       drain_wait(bar_full + 8 * (j % MX_STAGES), (uint32_t)(j / MX_STAGES) & 1u);
   } else if (warp >= 6) {
     // ------------------------------------------------------------ converters
-    const int j = threadIdx.x - 192;  // weight row of the atom
+    // thread t: weight row j = t % 128, elements 32 g .. 32 g + 31 (one E8M0 group) with g = t / 128
+    const int t = threadIdx.x - 192;
+    const int j = t & 127, g = t >> 7;
     for (int it = 0; it < n_stages; ++it) {
       const int s = it % MX_STAGES;
       if (!mbar_wait(bar_full + 8 * s, (uint32_t)(it / MX_STAGES) & 1u, prm.err)) break;
       const uint8_t* stg = smem_gen + s * MX_STAGE;
-      const uint4 c0 = *reinterpret_cast<const uint4*>(stg + MX_BC_OFF + 32 * j);
-      const uint4 c1 = *reinterpret_cast<const uint4*>(stg + MX_BC_OFF + 32 * j + 16);
-      const uint32_t sc = *reinterpret_cast<const uint16_t*>(stg + MX_BS_OFF + 2 * j);
-      const uint32_t s0 = e8m0_bf16_bits(sc & 0xFFu), s1 = e8m0_bf16_bits(sc >> 8);
-      const uint32_t sc0 = s0 | (s0 << 16), sc1 = s1 | (s1 << 16);
-      const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      const uint4 cw = *reinterpret_cast<const uint4*>(stg + MX_BC_OFF + 32 * j + 16 * g);
+      const uint32_t b = e8m0_bf16_bits(stg[MX_BS_OFF + 2 * j + g]);
+      const uint32_t scl = b | (b << 16);
+      const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
       uint8_t* dst_row = smem_gen + s * MX_STAGE + MX_BB_OFF + 128 * j;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {  // 16-byte chunk c holds elements 8c .. 8c + 7
-        const uint32_t w = words[c];
-        const uint32_t scl = c < 4 ? sc0 : sc1;
-        uint4 o;
-        o.x = bf16x2_mul(s_lut[w & 0xFFu], scl);
-        o.y = bf16x2_mul(s_lut[(w >> 8) & 0xFFu], scl);
-        o.z = bf16x2_mul(s_lut[(w >> 16) & 0xFFu], scl);
-        o.w = bf16x2_mul(s_lut[w >> 24], scl);
-        *reinterpret_cast<uint4*>(dst_row + ((c ^ (j & 7)) << 4)) = o;
+      for (int q = 0; q < 4; ++q) {  // 16-byte chunk c = 4 g + q holds elements 8c .. 8c + 7
+        const int c = 4 * g + q;
+        uint32_t o[4];
+        e2m1x8_to_bf16(words[q], o);
+        *reinterpret_cast<uint4*>(dst_row + ((c ^ (j & 7)) << 4)) =
+            make_uint4(bf16x2_mul(o[0], scl), bf16x2_mul(o[1], scl), bf16x2_mul(o[2], scl), bf16x2_mul(o[3], scl));
       }
       fence_proxy_async_smem();  // the tensor cores read these bytes through the async proxy
       __syncwarp();
@@ -293,35 +299,44 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_tfull + 8 * b, use & 1u, prm.err) ? 1 : 0)) break;
       tc_fence_after();
       const uint32_t tacc = tmem + 128u * b + ((uint32_t)(warp * 32) << 16);
-      float v[128];
+      // 32-column pieces keep the register footprint small enough for 448 threads; the accumulator is
+      // released after the last piece (the other buffer takes the next tile meanwhile)
       if (any_real) {
+        if constexpr (MODE == 0) {
+          const float L = prm.limit;
+#pragma unroll 1
+          for (int q = 0; q < 2; ++q) {  // features 32 q .. 32 q + 31 of this n-tile's 64
+            float gv[32], uv[32];
+            tmem_ld32(tacc + 32 * q, gv);
+            tmem_ld32(tacc + 64 + 32 * q, uv);
+            tmem_ld_wait();
+            if (p >= 0) {
+              uint32_t hw[16];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float q[32];
-          tmem_ld32(tacc + c * 32, q);
+              for (int i = 0; i < 16; ++i)
+                hw[i] = pack_bf16x2(swiglu(gv[2 * i], uv[2 * i], L), swiglu(gv[2 * i + 1], uv[2 * i + 1], L));
+              uint4* dst = reinterpret_cast<uint4*>(prm.out_bf16 + (size_t)r * prm.I + t.nt * 64 + 32 * q);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[c * 32 + i] = q[i];
+              for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hw[4 * i], hw[4 * i + 1], hw[4 * i + 2], hw[4 * i + 3]);
+            }
+          }
+        } else {
+#pragma unroll 1
+          for (int q = 0; q < 4; ++q) {
+            float v[32];
+            tmem_ld32(tacc + 32 * q, v);
+            tmem_ld_wait();
+            if (p >= 0) {
+              float4* d4 = reinterpret_cast<float4*>(prm.o_pairs + (size_t)p * prm.H + t.nt * MX_BN + 32 * q);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            }
+          }
         }
-        tmem_ld_wait();
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_tempty + 8 * b);
-      if (p < 0) continue;  // padding rows carry nothing
-      if constexpr (MODE == 0) {
-        const float L = prm.limit;
-        uint32_t hw[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          hw[i] = pack_bf16x2(swiglu(v[2 * i], v[64 + 2 * i], L), swiglu(v[2 * i + 1], v[64 + 2 * i + 1], L));
-        uint4* dst = reinterpret_cast<uint4*>(prm.out_bf16 + (size_t)r * prm.I + t.nt * 64);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(hw[4 * i], hw[4 * i + 1], hw[4 * i + 2], hw[4 * i + 3]);
-      } else {
-        float4* d4 = reinterpret_cast<float4*>(prm.o_pairs + (size_t)p * prm.H + t.nt * MX_BN);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-      }
     }
   }
 
