@@ -258,7 +258,7 @@ fp4moe_status moe_grouped_gemm_w1_swiglu(const fp4moe_config* cfg, int32_t T, co
   }
   FP4_TRY(check_ptrs(a1_fp4, a1_sf, padded_offsets, pair_of_row, w1_fp4, w1_sf, alpha1, gs2, a2_fp4, a2_sf, ws));
   return gemm_launch(kW1SwiGLU, *cfg, T, a1_fp4, a1_sf, padded_offsets, pair_of_row, w1_fp4, w1_sf, alpha1, gs2,
-                     a2_fp4, a2_sf, nullptr, nullptr, err_word(ws), (cudaStream_t)stream);
+                     a2_fp4, a2_sf, nullptr, nullptr, err_word(ws), at<int>(ws, kWsSchedW1), (cudaStream_t)stream);
 }
 
 fp4moe_status moe_grouped_gemm_w2(const fp4moe_config* cfg, int32_t T, const uint8_t* a2_fp4, const uint8_t* a2_sf,
@@ -274,7 +274,7 @@ fp4moe_status moe_grouped_gemm_w2(const fp4moe_config* cfg, int32_t T, const uin
   }
   FP4_TRY(check_ptrs(a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, o_pairs, ws));
   return gemm_launch(kW2Rows, *cfg, T, a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, nullptr,
-                     nullptr, nullptr, nullptr, o_pairs, err_word(ws), (cudaStream_t)stream);
+                     nullptr, nullptr, nullptr, o_pairs, err_word(ws), at<int>(ws, kWsSchedW2), (cudaStream_t)stream);
 }
 
 fp4moe_status moe_combine(const fp4moe_config* cfg, int32_t T, const float* o_pairs, const float* topk_w,
@@ -302,7 +302,7 @@ fp4moe_status moe_grouped_gemm_w2_combine(const fp4moe_config* cfg, int32_t T, c
   }
   FP4_TRY(check_ptrs(a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, topk_w, y, ws));
   FP4_TRY(gemm_launch(kW2Rows, *cfg, T, a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, nullptr,
-                      nullptr, nullptr, nullptr, o, err_word(ws), (cudaStream_t)stream));
+                      nullptr, nullptr, nullptr, o, err_word(ws), at<int>(ws, kWsSchedW2), (cudaStream_t)stream));
   return combine_launch(*cfg, T, o, topk_w, y, (cudaStream_t)stream);
 }
 
@@ -339,9 +339,9 @@ fp4moe_status moe_forward(const fp4moe_config* cfg, int32_t T, const uint16_t* x
     FP4_TRY(quant_scatter_launch(*cfg, T, x, gs1, at<int32_t>(ws, L.slot), at<uint8_t>(ws, L.a1),
                                  at<uint8_t>(ws, L.a1sf), st));
     FP4_TRY(gemm_launch(kW1SwiGLU, *cfg, T, at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf), poff, por, w1_fp4, w1_sf,
-                        alpha1, gs2, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), nullptr, nullptr, err, st));
+                        alpha1, gs2, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), nullptr, nullptr, err, at<int>(ws, kWsSchedW1), st));
     FP4_TRY(gemm_launch(kW2Rows, *cfg, T, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), poff, por, w2_fp4, w2_sf,
-                        alpha2, nullptr, nullptr, nullptr, nullptr, at<float>(ws, L.opairs), err, st));
+                        alpha2, nullptr, nullptr, nullptr, nullptr, at<float>(ws, L.opairs), err, at<int>(ws, kWsSchedW2), st));
   }
   FP4_TRY(combine_launch(*cfg, T, at<float>(ws, L.opairs), w, y, st));
   const size_t pk = (size_t)T * cfg->top_k;
@@ -410,7 +410,7 @@ fp4moe_status fp4moe_calibrate(const fp4moe_config* cfg, int32_t T, const uint16
   FP4_TRY(make_alpha_launch(cfg->num_experts, gs1_out, gw1, alpha, st));
   if (cudaMemsetAsync(amax_h, 0, 4, st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
   FP4_TRY(gemm_launch(kW1Amax, *cfg, T, at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf), poff, por, w1_fp4, w1_sf,
-                      alpha, nullptr, nullptr, nullptr, amax_h, nullptr, err, st));
+                      alpha, nullptr, nullptr, nullptr, amax_h, nullptr, err, at<int>(ws, kWsSchedW1), st));
   if (cudaMemcpyAsync(gs2_out, amax_h, 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
   return gs_from_amax_launch(1, gs2_out, st);
 }

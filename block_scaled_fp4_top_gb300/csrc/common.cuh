@@ -29,6 +29,8 @@ constexpr uint32_t kAbortMask = FP4MOE_ERR_TIMEOUT;
 constexpr size_t kWsErr = 0;        // uint32 error word
 constexpr size_t kWsAmaxH = 16;     // float, calibration scratch (amax of h)
 constexpr size_t kWsAmaxX = 20;     // float, calibration scratch (amax of x)
+constexpr size_t kWsSchedW1 = 32;   // int, dynamic-schedule chunk counter of the W1 GEMM
+constexpr size_t kWsSchedW2 = 36;   // int, dynamic-schedule chunk counter of the W2 GEMM
 constexpr size_t kWsHeader = 256;
 
 __device__ __forceinline__ void raise_error(uint32_t* err, uint32_t bits) { atomicOr(err, bits); }

@@ -88,7 +88,7 @@ constexpr uint32_t SFB_STAGE_COLS = 4 * ATOMS;  // B scales of one ring stage
 // ring stage s: 32 columns at RES_COL + K/16 + 32 s. nacc is 2 when that fits,
 // else 1.
 static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
-static_assert(SMEM_BYTES + 4 * kMaxExperts + 64 <= 232448, "shared memory budget (dynamic + static)");
+static_assert(SMEM_BYTES + 8 * kMaxExperts + 128 <= 232448, "shared memory budget (dynamic + static)");
 constexpr int kMaxResidentK = (TMEM_COLS - ACC_COLS - SFB_STAGE_COLS * STAGES) * 16;  // 4608 with one accumulator
 
 struct Params {
@@ -106,6 +106,145 @@ struct Params {
   float* amax;
   float* o_pairs;
   uint32_t* err;
+  int dyn;     // 1: dynamic chunk schedule (large T); 0: contiguous static ranges (decode sizes)
+  int* sched;  // dynamic schedule: next-chunk counter, zero at launch
+};
+
+// Dynamic schedule. A chunk is at most kChunk tiles of one expert: for a one-m-tile expert, up to kChunk
+// n-tiles (the activation tile fixed); otherwise one n-tile over up to kChunk m-tiles (the weight tile
+// fixed). Chunks are numbered expert by expert (for several m-tiles: m-block, then n-tile), and CTAs take
+// them in that order from a global counter. So the CTAs running at any moment share one expert's
+// activation and weight tiles in L2, and the load balances itself.
+constexpr int kChunk = 4;
+constexpr int kSchedSlots = 4;  // chunk ids handed from the producer to the MMA issuer and the epilogue
+
+__device__ __forceinline__ int expert_chunks(int me, int NT) {
+  return me == 0 ? 0 : (me == 1 ? (NT + kChunk - 1) / kChunk : ((me + kChunk - 1) / kChunk) * NT);
+}
+
+struct Chunk {
+  int e, pm0, me;  // expert, its first m-tile, its m-tiles
+  int n0, m0;      // first n-tile and m-tile of the chunk
+  int count;       // tiles in the chunk
+  bool along_n;    // one m-tile: walk n-tiles n0.. with m fixed; else m-tiles m0.. with n fixed
+
+  __device__ __forceinline__ Tile tile(int i) const {
+    const int mt = along_n ? m0 : m0 + i;
+    return Tile{e, along_n ? n0 + i : n0, mt, me, mt == pm0 + me - 1};
+  }
+};
+
+// Chunk c; s_cstart[e] is the first chunk of expert e (empty experts share the next one's start).
+__device__ __forceinline__ Chunk decode_chunk(int c, const int* s_cstart, const int* poff, int E, int NT, int r128) {
+  int lo = 0, hi = E - 1;  // the last expert whose first chunk is <= c
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_cstart[mid] <= c) lo = mid;
+    else hi = mid - 1;
+  }
+  Chunk k;
+  k.e = lo;
+  k.pm0 = lo > 0 ? min(poff[lo - 1] >> 7, r128) : 0;
+  k.me = min(poff[lo] >> 7, r128) - k.pm0;
+  const int l = c - s_cstart[lo];
+  k.along_n = (k.me == 1);
+  if (k.along_n) {
+    k.n0 = l * kChunk;
+    k.m0 = k.pm0;
+    k.count = min(kChunk, NT - k.n0);
+  } else {
+    k.n0 = l % NT;
+    const int mb = l / NT;
+    k.m0 = k.pm0 + mb * kChunk;
+    k.count = min(kChunk, k.me - mb * kChunk);
+  }
+  return k;
+}
+
+// The tiles of one CTA, in order, as each role sees them: its contiguous share [tau0, tau1) of the tile
+// order (static schedule), or the chunks it takes from the global counter (dynamic schedule). In the dynamic
+// schedule the producer takes a chunk and hands its id to the MMA issuer and the epilogue warps through a
+// small shared-memory ring; every role then walks the same tiles in the same order.
+enum SourceRole { kRoleProducer = 0, kRoleMma = 1, kRoleEpilogue = 2 };
+
+template <int ROLE>
+struct TileSource {
+  // static schedule
+  TileCursor cur;
+  int tau, tau1;
+  // dynamic schedule
+  Chunk ck;
+  int ci, q;
+  uint32_t qph;
+  bool dyn, done;
+
+  __device__ __forceinline__ void init(const Params& prm, int tau0_, int tau1_, const int* poff, int E, int NT,
+                                       int r128) {
+    dyn = prm.dyn != 0;
+    tau = tau0_;
+    tau1 = tau1_;
+    if (!dyn && tau < tau1) cur.seek(tau, poff, E, NT, r128);
+    ck.count = 0;
+    ci = 0;
+    q = 0;
+    qph = 0;
+    done = false;
+  }
+
+  // The next tile, or false at the end (or when a bounded wait gave up).
+  __device__ __forceinline__ bool next(Tile& t, const Params& prm, int tau0, const int* poff, const int* cstart,
+                                       int* s_sched, uint32_t bar_sfull, uint32_t bar_sempty, int n_chunks, int E,
+                                       int NT, int r128) {
+    if (!dyn) {
+      if (tau >= tau1) return false;
+      if (tau > tau0) cur.step(poff, E, NT, r128);
+      ++tau;
+      t = cur.tile();
+      return true;
+    }
+    while (ci >= ck.count) {
+      if (done) return false;
+      int c;
+      if constexpr (ROLE == kRoleProducer) {
+        if (!mbar_wait(bar_sempty + 8 * q, qph ^ 1u, prm.err)) {  // the slot's previous id was read by all
+          done = true;
+          return false;
+        }
+        c = atomicAdd(prm.sched, 1);
+        if (c >= n_chunks) c = -1;
+        s_sched[q] = c;
+        mbar_arrive(bar_sfull + 8 * q);
+      } else if constexpr (ROLE == kRoleMma) {
+        if (!mbar_wait(bar_sfull + 8 * q, qph, prm.err)) {
+          done = true;
+          return false;
+        }
+        c = s_sched[q];
+        mbar_arrive(bar_sempty + 8 * q);
+      } else {
+        // the whole warp takes one decision
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_sfull + 8 * q, qph, prm.err) ? 1 : 0)) {
+          done = true;
+          return false;
+        }
+        c = s_sched[q];
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(bar_sempty + 8 * q);
+      }
+      if (++q == kSchedSlots) {
+        q = 0;
+        qph ^= 1u;
+      }
+      if (c < 0) {
+        done = true;
+        return false;
+      }
+      ck = decode_chunk(c, cstart, poff, E, NT, r128);
+      ci = 0;
+    }
+    t = ck.tile(ci++);
+    return true;
+  }
 };
 
 // Tensor maps of the activation codes whose boxes are 16, 32, 64 and 128 rows
@@ -135,6 +274,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_poff[kMaxExperts];
+  __shared__ int s_cstart[kMaxExperts + 1];  // dynamic schedule: first chunk of every expert
+  __shared__ int s_sched[kSchedSlots];
 
   pdl_wait();  // the routing / quantisation results of the previous launch are needed from here on
   pdl_trigger();
@@ -153,8 +294,31 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t bar_tfull = bar_empty + 8 * STAGES;  // 2 x 8 bytes
   const uint32_t bar_tempty = bar_tfull + 16;         // 2 x 8 bytes
   const uint32_t bar_drain = bar_tempty + 16;
+  const uint32_t bar_sfull = bar_drain + 8;            // kSchedSlots x 8 bytes: a chunk id was written
+  const uint32_t bar_sempty = bar_sfull + 8 * kSchedSlots;  // kSchedSlots x 8 bytes: it was read
 
   for (int e = threadIdx.x; e < E; e += THREADS) s_poff[e] = __ldcg(prm.poff + e);
+  if (prm.dyn) {
+    __syncthreads();
+    if (warp == 0) {  // first chunk of every expert: per-lane sums over a block of experts, then a warp scan
+      const int per = (E + 31) / 32, e0 = lane * per, e1 = min(E, e0 + per);
+      int sum = 0;
+      for (int e = e0; e < e1; ++e)
+        sum += expert_chunks(min(s_poff[e] >> 7, r128) - (e > 0 ? min(s_poff[e - 1] >> 7, r128) : 0), NT);
+      int incl = sum;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      int run = incl - sum;
+      for (int e = e0; e < e1; ++e) {
+        s_cstart[e] = run;
+        run += expert_chunks(min(s_poff[e] >> 7, r128) - (e > 0 ? min(s_poff[e - 1] >> 7, r128) : 0), NT);
+      }
+      if (lane == 31) s_cstart[E] = incl;
+    }
+  }
   if (warp == 0) {
     tmem_alloc(smem_u32(&s_tmem), TMEM_COLS);
     tmem_relinquish();
@@ -169,12 +333,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(bar_tempty + 8 * b, 4);  // one arrive per epilogue warp
     }
     mbar_init(bar_drain, 1);
+    for (int q = 0; q < kSchedSlots; ++q) {
+      mbar_init(bar_sfull + 8 * q, 1);
+      mbar_init(bar_sempty + 8 * q, 1 + 4);  // the MMA issuer and the four epilogue warps
+    }
     fence_mbar_init();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+  const int n_chunks = prm.dyn ? s_cstart[E] : 0;
 
   const int KB = prm.KB;
   const int katoms_total = prm.K / 64;
@@ -201,14 +370,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       bulk_prefetch_l2(prm.b_sf + (blk * katoms_total + (size_t)kb * ATOMS) * SF_TILE,
                        min(ATOMS, katoms_total - kb * ATOMS) * SF_TILE);
     };
-    for (int j = 0; j < min(PREFETCH, n_stages); ++j) prefetch(j);
+    if (!prm.dyn)  // the dynamic schedule learns its tiles as it goes: no look-ahead prefetch
+      for (int j = 0; j < min(PREFETCH, n_stages); ++j) prefetch(j);
     int it = 0, prev_key = INT_MIN, prev_mt = -1, a_box = 3;
     bool ok = true;
-    TileCursor cur;
-    cur.seek(tau0, s_poff, E, NT, r128);
-    for (int tau = tau0; tau < tau1 && ok; ++tau) {
-      if (tau > tau0) cur.step(s_poff, E, NT, r128);
-      const Tile t = cur.tile();
+    TileSource<kRoleProducer> src;
+    src.init(prm, tau0, tau1, s_poff, E, NT, r128);
+    Tile t;
+    while (ok && src.next(t, prm, tau0, s_poff, s_cstart, s_sched, bar_sfull, bar_sempty, n_chunks, E, NT, r128)) {
       const bool res_a = (t.me == 1);  // one m-tile: the activations are the fixed operand, else the weights
       const int key = res_a ? t.mt : -1 - (t.e * NT + t.nt);
       const bool new_res = (key != prev_key);  // resident scales go to TMEM once per fixed operand
@@ -237,7 +406,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint64_t pol_res = res_a ? pol_a : pol_w;
       const uint64_t pol_str = res_a ? pol_w : pol_a;
       for (int kb = 0; kb < KB; ++kb, ++it) {
-        if (it + PREFETCH < n_stages) prefetch(it + PREFETCH);
+        if (!prm.dyn && it + PREFETCH < n_stages) prefetch(it + PREFETCH);
         const int s = it % STAGES;
         const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
         if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, prm.err)) {
@@ -272,11 +441,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
-    TileCursor cur;
-    cur.seek(tau0, s_poff, E, NT, r128);
-    for (int tau = tau0; tau < tau1 && ok; ++tau, ++tl) {
-      if (tau > tau0) cur.step(s_poff, E, NT, r128);
-      const Tile t = cur.tile();
+    TileSource<kRoleMma> src;
+    src.init(prm, tau0, tau1, s_poff, E, NT, r128);
+    Tile t;
+    for (; ok && src.next(t, prm, tau0, s_poff, s_cstart, s_sched, bar_sfull, bar_sempty, n_chunks, E, NT, r128);
+         ++tl) {
       const bool res_a = (t.me == 1);
       const int key = res_a ? t.mt : -1 - (t.e * NT + t.nt);
       const bool new_res = (key != prev_key);
@@ -350,11 +519,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp < 4) {
     // ------------------------------------------------------------ epilogue
     int tl = 0;
-    TileCursor cur;
-    cur.seek(tau0, s_poff, E, NT, r128);
-    for (int tau = tau0; tau < tau1; ++tau, ++tl) {
-      if (tau > tau0) cur.step(s_poff, E, NT, r128);
-      const Tile t = cur.tile();
+    TileSource<kRoleEpilogue> src;
+    src.init(prm, tau0, tau1, s_poff, E, NT, r128);
+    Tile t;
+    for (; src.next(t, prm, tau0, s_poff, s_cstart, s_sched, bar_sfull, bar_sempty, n_chunks, E, NT, r128); ++tl) {
       const int r = t.mt * BM + warp * 32 + lane;
       const int p = __ldcg(prm.pair_of_row + r);
       const bool any_real = __any_sync(0xFFFFFFFFu, p >= 0);
@@ -496,7 +664,7 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
                           const uint8_t* a_sf, const int32_t* poff, const int32_t* pair_of_row,
                           const uint8_t* b_codes, const uint8_t* b_sf, const float* alpha, const float* gs2,
                           uint8_t* out_codes, uint8_t* out_sf, float* amax, float* o_pairs, uint32_t* err,
-                          cudaStream_t st) {
+                          int* sched, cudaStream_t st) {
   if (T == 0) return FP4MOE_OK;
   const bool w2 = (mode == kW2Rows);
   const int Kc = w2 ? cfg.inter : cfg.hidden;
@@ -525,6 +693,11 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
   prm.amax = amax;
   prm.o_pairs = o_pairs;
   prm.err = err;
+  // the dynamic chunk schedule pays off once experts average a whole m-tile (prefill sizes)
+  prm.dyn = ((int64_t)T * cfg.top_k >= (int64_t)cfg.num_experts * BM) ? 1 : 0;
+  prm.sched = sched;
+  if (prm.dyn && (sched == nullptr || cudaMemsetAsync(sched, 0, sizeof(int), st) != cudaSuccess))
+    return FP4MOE_CUDA_ERROR;
   AMaps tmA;
   for (int b = 0; b < 4; ++b)
     if (!encode_u8_sw128(&tmA.box[b], a_codes, (uint64_t)prm.K / 2, (uint64_t)prm.cap, 16u << b))

@@ -69,7 +69,7 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
                           const uint8_t* a_sf, const int32_t* poff, const int32_t* pair_of_row,
                           const uint8_t* b_codes, const uint8_t* b_sf, const float* alpha, const float* gs2,
                           uint8_t* out_codes, uint8_t* out_sf, float* amax, float* o_pairs, uint32_t* err,
-                          cudaStream_t st);
+                          int* sched, cudaStream_t st);
 
 // selftest.cu: one bounded wait that runs out (see fp4moe_selftest_wait_timeout)
 fp4moe_status selftest_wait_launch(uint32_t* err, int64_t limit_ns, uint32_t* result, cudaStream_t st);

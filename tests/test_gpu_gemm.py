@@ -5,6 +5,8 @@ counts are ragged, with empty experts, partial 128-row tiles and several
 m-tiles, and K is partial (a stage of 2 atoms) or runs over several stages.
 * W2: every real pair's fp32 row is compared with an fp64 matmul of the
   decoded operands. Padding rows must not be written.
+* Cases with T >= E * 128 run the dynamic chunk schedule (prefill sizes),
+  the others the static contiguous one (decode sizes).
 * W1: the clamped SwiGLU + requantisation epilogue is compared with the
   oracle's quantiser applied to the fp64 reference h. Codes must agree
   except at rounding ties that the fp32 accumulation moves.
@@ -81,6 +83,7 @@ def _setup(H, I, counts, seed, which):
     (256, 128, [1, 0, 130, 5]),          # K = 128: one partial stage (2 scale atoms)
     (256, 768, [300, 1, 0]),             # K = 768: 3 full stages
     (512, 2048, [129, 128, 0, 2]),       # K = 2048: 8 stages around a 3-deep ring
+    (256, 768, [600, 5, 130]),           # T >= E * 128: the dynamic chunk schedule (5-, 1- and 2-m-tile experts)
 ])
 def test_w2_rows_against_fp64(H, I, counts):
     import torch
@@ -109,7 +112,8 @@ def test_w2_rows_against_fp64(H, I, counts):
     assert ok.all(), f"max err/bound {(err / np.maximum(bound, 1e-30)).max():.3e}"
 
 
-@pytest.mark.parametrize("H,I,counts", [(256, 128, [3, 0, 140]), (512, 256, [1, 257, 2])])
+@pytest.mark.parametrize("H,I,counts", [(256, 128, [3, 0, 140]), (512, 256, [1, 257, 2]),
+                                        (256, 128, [600, 5, 130])])   # the last one takes the dynamic schedule
 def test_w1_swiglu_requant(H, I, counts):
     import torch
     from block_scaled_fp4_top_gb300 import api
