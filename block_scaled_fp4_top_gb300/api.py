@@ -135,6 +135,11 @@ def fp4moe_calibrate(cfg, T, x_warm, router_w, router_bias, w1_fp4, w1_sf, gw1, 
            "fp4moe_calibrate")
 
 
+def fp4moe_batch_gs1(cfg, T, x, gw1, gs1_out, alpha1_out, ws, stream=None):
+    _check(_lib.load().fp4moe_batch_gs1(ctypes.byref(cfg), T, _p(x), _p(gw1), _p(gs1_out), _p(alpha1_out), _p(ws),
+                                        _s(stream)), "fp4moe_batch_gs1")
+
+
 def fp4moe_quantize_rows_f32(rows, K, inp, g, codes, sf, stream=None):
     _check(_lib.load().fp4moe_quantize_rows_f32(rows, K, _p(inp), _p(g), _p(codes), _p(sf), _s(stream)),
            "fp4moe_quantize_rows_f32")
@@ -219,6 +224,10 @@ class MoELayer:
         self.gs1.fill_(gs1)
         self.gs2.fill_(gs2)
         self.update_alpha()
+
+    def batch_gs1(self, x: torch.Tensor, stream=None):
+        """Take gs1 (and alpha1) from this batch's own amax, on the device (see fp4moe_batch_gs1)."""
+        fp4moe_batch_gs1(self.cfg, x.shape[0], x, self.weights.gw1, self.gs1, self.alpha1, self.ws, stream)
 
     def update_alpha(self):
         E = self.cfg.num_experts

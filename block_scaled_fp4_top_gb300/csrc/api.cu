@@ -415,6 +415,17 @@ fp4moe_status fp4moe_calibrate(const fp4moe_config* cfg, int32_t T, const uint16
   return gs_from_amax_launch(1, gs2_out, st);
 }
 
+fp4moe_status fp4moe_batch_gs1(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const float* gw1,
+                               float* gs1_out, float* alpha1_out, void* ws, fp4moe_stream_t stream) {
+  FP4_TRY(check_cfg(cfg));
+  FP4_TRY(check_T(cfg, T));
+  if (is_mx(cfg)) return FP4MOE_UNSUPPORTED;  // MXFP4 layers keep bf16 activations: no global scales
+  FP4_TRY(check_ptrs(x, gw1, gs1_out, alpha1_out, ws));
+  return batch_gs1_launch(T, cfg->hidden, x, cfg->num_experts, gw1, gs1_out, alpha1_out,
+                          at<unsigned int>(ws, kWsBatchAmax), at<unsigned int>(ws, kWsBatchDone),
+                          (cudaStream_t)stream);
+}
+
 fp4moe_status fp4moe_quantize_rows_f32(int32_t rows, int32_t K, const float* in, const float* g, uint8_t* codes,
                                        uint8_t* sf, fp4moe_stream_t stream) {
   if (rows < 0 || K <= 0 || K % 64 != 0 || rows % 128 != 0) return FP4MOE_INVALID_ARG;

@@ -31,6 +31,8 @@ constexpr size_t kWsAmaxH = 16;     // float, calibration scratch (amax of h)
 constexpr size_t kWsAmaxX = 20;     // float, calibration scratch (amax of x)
 constexpr size_t kWsSchedW1 = 32;   // int, dynamic-schedule chunk counter of the W1 GEMM
 constexpr size_t kWsSchedW2 = 36;   // int, dynamic-schedule chunk counter of the W2 GEMM
+constexpr size_t kWsBatchAmax = 40; // uint, batch amax accumulator of fp4moe_batch_gs1 (zero between calls)
+constexpr size_t kWsBatchDone = 44; // uint, its CTA arrival counter (zero between calls)
 constexpr size_t kWsHeader = 256;
 
 __device__ __forceinline__ void raise_error(uint32_t* err, uint32_t bits) { atomicOr(err, bits); }

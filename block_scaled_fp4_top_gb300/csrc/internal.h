@@ -63,6 +63,9 @@ fp4moe_status amax_f32_launch(int32_t n_groups, int64_t per_group, const float* 
 fp4moe_status amax_bf16_launch(int64_t n, const uint16_t* in, float* amax, cudaStream_t st);
 fp4moe_status gs_from_amax_launch(int32_t n, float* inout, cudaStream_t st);
 fp4moe_status make_alpha_launch(int32_t n, const float* gs_act, const float* gs_w, float* alpha, cudaStream_t st);
+// gs1 and alpha1 from the batch's own amax, one launch; acc and done are zero words that it leaves zero
+fp4moe_status batch_gs1_launch(int32_t T, int32_t H, const uint16_t* x, int32_t E, const float* gw1, float* gs1,
+                               float* alpha1, unsigned int* acc, unsigned int* done, cudaStream_t st);
 
 enum GemmMode { kW1SwiGLU = 0, kW1Amax = 1, kW2Rows = 2 };
 fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, const uint8_t* a_codes,

@@ -130,7 +130,51 @@ __global__ void make_alpha_kernel(int n, const float* __restrict__ gs_act, const
 
 inline fp4moe_status last_status() { return cudaGetLastError() == cudaSuccess ? FP4MOE_OK : FP4MOE_CUDA_ERROR; }
 
+// The L1 activation global scale of the batch in hand: gs1 = RN(2688 / amax|x|) and
+// alpha1[e] = RN(1 / RN(gs1 * gw1[e])), in one launch. Every CTA folds its part of the amax into `acc`
+// (float bits compare as unsigned for non-negative values); the last CTA to arrive reads and clears it,
+// writes gs1 and the alpha table, and clears the arrival counter, so both words are zero again afterwards.
+__global__ void __launch_bounds__(256) batch_gs1_kernel(int64_t n, const uint16_t* __restrict__ x, int E,
+                                                        const float* __restrict__ gw1, float* __restrict__ gs1,
+                                                        float* __restrict__ alpha1, unsigned int* acc,
+                                                        unsigned int* done) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ bool s_last;
+  float m = 0.0f;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    m = fmaxf(m, fabsf(__uint_as_float((uint32_t)x[i] << 16)));
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) atomicMax(acc, __float_as_uint(m));
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  __shared__ float s_g;
+  if (threadIdx.x == 0) {
+    s_g = global_scale_from_amax(__uint_as_float(atomicExch(acc, 0u)));
+    gs1[0] = s_g;
+    *done = 0u;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) alpha1[e] = __fdiv_rn(1.0f, __fmul_rn(s_g, gw1[e]));
+}
+
 }  // namespace
+
+fp4moe_status batch_gs1_launch(int32_t T, int32_t H, const uint16_t* x, int32_t E, const float* gw1, float* gs1,
+                               float* alpha1, unsigned int* acc, unsigned int* done, cudaStream_t st) {
+  const int64_t n = (int64_t)T * H;
+  const int64_t want = (n + 256 * 16 - 1) / (256 * 16);
+  const unsigned bx = (unsigned)(want < 1 ? 1 : (want > 1024 ? 1024 : want));
+  return launch_pdl(batch_gs1_kernel, dim3(bx), dim3(256), 0, st, n, x, (int)E, gw1, gs1, alpha1, acc, done) ==
+                 cudaSuccess
+             ? FP4MOE_OK
+             : FP4MOE_CUDA_ERROR;
+}
+
 
 fp4moe_status quant_scatter_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const float* gs1,
                                    const int32_t* slot_of_pair, uint8_t* a1, uint8_t* a1_sf, cudaStream_t st) {

@@ -345,6 +345,23 @@ fp4moe_status moe_forward(const fp4moe_config* cfg, int32_t T, const uint16_t* x
 fp4moe_status fp4moe_quantize_weights(const fp4moe_config* cfg, int32_t which, int32_t n_experts, const float* w,
                                       uint8_t* codes_out, uint8_t* sf_out, float* gs_out, fp4moe_stream_t stream);
 
+/*
+ * fp4moe_batch_gs1: the L1 activation global scale taken from the batch in
+ * hand rather than from a warm-up pass, with no host synchronisation:
+ *   gs1_out[0] = RN(2688 / amax|x[0..T)|) (1 for an all-zero batch),
+ *   alpha1_out[e] = RN(1 / RN(gs1_out[0] * gw1[e])) for e < E.
+ * Pass gs1_out and alpha1_out to moe_forward (or to moe_quantize_scatter and
+ * moe_grouped_gemm_w1_swiglu) on the same stream. Activations beyond a
+ * warm-up batch's range would otherwise saturate in E4M3: "Current Bug",
+ * "Bug 5", where the wrong input_scale makes block scales saturate at 448.
+ * gs2 stays the warm-up value, because the amax of h is known only after the
+ * whole W1 GEMM.
+ * One launch. It uses two words of the workspace header, which it leaves at
+ * zero. Calls that share a workspace must be ordered on one stream.
+ */
+fp4moe_status fp4moe_batch_gs1(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const float* gw1,
+                               float* gs1_out, float* alpha1_out, void* ws, fp4moe_stream_t stream);
+
 /* alpha[e] = RN(1 / RN(gs_act[0] * gs_w[e])) for e < n. */
 fp4moe_status fp4moe_make_alpha(int32_t n, const float* gs_act, const float* gs_w, float* alpha,
                                 fp4moe_stream_t stream);
