@@ -19,7 +19,8 @@ W_NVFP4, W_MXFP4 = 0, 1
 
 class Config(ctypes.Structure):
     _fields_ = [("hidden", c_i32), ("inter", c_i32), ("inter_logical", c_i32), ("num_experts", c_i32),
-                ("top_k", c_i32), ("max_tokens", c_i32), ("swiglu_limit", c_f32), ("w_format", c_i32)]
+                ("top_k", c_i32), ("max_tokens", c_i32), ("swiglu_limit", c_f32), ("w_format", c_i32),
+                ("ep_first", c_i32), ("ep_count", c_i32)]
 
 
 CP = ctypes.POINTER(Config)

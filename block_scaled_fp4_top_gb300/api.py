@@ -25,8 +25,10 @@ class Fp4MoeError(RuntimeError):
 
 
 def config(hidden: int, inter: int, num_experts: int, top_k: int, max_tokens: int, swiglu_limit: float,
-           inter_logical: int = 0, w_format: int = _lib.W_NVFP4) -> Config:
-    return Config(hidden, inter, inter_logical or inter, num_experts, top_k, max_tokens, swiglu_limit, w_format)
+           inter_logical: int = 0, w_format: int = _lib.W_NVFP4, ep_first: int = 0, ep_count: int = 0) -> Config:
+    """Layer configuration. ep_count > 0 makes the layer hold experts [ep_first, ep_first + ep_count) only."""
+    return Config(hidden, inter, inter_logical or inter, num_experts, top_k, max_tokens, swiglu_limit, w_format,
+                  ep_first, ep_count)
 
 
 def _p(t):
@@ -174,7 +176,7 @@ class MoELayer:
     def __init__(self, cfg: Config, device: str = "cuda"):
         self.cfg = cfg
         self.device = device
-        E, H, I = cfg.num_experts, cfg.hidden, cfg.inter
+        E, H, I = (cfg.ep_count or cfg.num_experts), cfg.hidden, cfg.inter
         b1, s1, b2, s2 = weight_bytes(cfg)
         u8 = dict(dtype=torch.uint8, device=device)
         f32 = dict(dtype=torch.float32, device=device)
@@ -198,7 +200,7 @@ class MoELayer:
         """
         cfg, W = self.cfg, self.weights
         n = w.shape[0]
-        E = cfg.num_experts
+        E = cfg.ep_count or cfg.num_experts
         b1, s1, b2, s2 = weight_bytes(cfg)
         if which == 1:
             per_c, per_s = b1 // E, s1 // E
@@ -230,7 +232,7 @@ class MoELayer:
         fp4moe_batch_gs1(self.cfg, x.shape[0], x, self.weights.gw1, self.gs1, self.alpha1, self.ws, stream)
 
     def update_alpha(self):
-        E = self.cfg.num_experts
+        E = self.cfg.ep_count or self.cfg.num_experts
         fp4moe_make_alpha(E, self.gs1, self.weights.gw1, self.alpha1)
         fp4moe_make_alpha(E, self.gs2, self.weights.gw2, self.alpha2)
 

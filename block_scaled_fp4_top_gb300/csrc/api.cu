@@ -28,6 +28,10 @@ fp4moe_status check_cfg(const fp4moe_config* c) {
   if (c->w_format != FP4MOE_W_NVFP4 && c->w_format != FP4MOE_W_MXFP4) return FP4MOE_UNSUPPORTED;
   if (c->hidden % 256 != 0 || c->inter % 128 != 0) return FP4MOE_UNSUPPORTED;
   if (c->top_k > kMaxTopK || c->num_experts > kMaxExperts || c->top_k > c->num_experts) return FP4MOE_UNSUPPORTED;
+  // expert parallelism: the layer holds experts [ep_first, ep_first + ep_count) of the router's num_experts
+  if (c->ep_count < 0 || (c->ep_count == 0 && c->ep_first != 0) ||
+      (c->ep_count > 0 && (c->ep_first < 0 || c->ep_first + c->ep_count > c->num_experts)))
+    return FP4MOE_INVALID_ARG;
   if (c->w_format == FP4MOE_W_NVFP4) {
     if (c->inter_logical != 0 && c->inter_logical != c->inter) return FP4MOE_UNSUPPORTED;
   } else {  // MXFP4: the logical width is whole 32-element scale groups inside the kernel width
@@ -73,7 +77,7 @@ inline uint32_t* err_word(void* ws) { return at<uint32_t>(ws, kWsErr); }
 
 size_t capacity_rows(const fp4moe_config& cfg, int32_t T) {
   const int64_t pairs = (int64_t)T * cfg.top_k;
-  const int64_t cap = (pairs + 127 * std::min<int64_t>(cfg.num_experts, pairs)) / 128 * 128;
+  const int64_t cap = (pairs + 127 * std::min<int64_t>(local_experts(cfg), pairs)) / 128 * 128;
   return (size_t)std::max<int64_t>(cap, 128);
 }
 
@@ -110,8 +114,9 @@ WsLayout ws_layout(const fp4moe_config& c) {
 }
 
 // Scratch of moe_route_noalloc, owned by the library image. Layout:
-// [0, 256) error word, then the per-token arrival counters of the logits
-// step, then the per-chunk expert histograms of the large-T layout.
+// [0, 256) error word, then the squared norms of the router rows (the
+// router's error bound), then the per-chunk expert histograms of the large-T
+// layout.
 namespace {
 constexpr size_t kScratchErr = 0;
 constexpr size_t kScratchNw2 = 256;
@@ -149,7 +154,7 @@ using namespace fp4moe;
 
 extern "C" {
 
-int32_t fp4moe_abi_version(void) { return 100; }
+int32_t fp4moe_abi_version(void) { return 101; }
 
 const char* fp4moe_status_string(fp4moe_status s) {
   switch (s) {
@@ -176,7 +181,7 @@ size_t fp4moe_workspace_bytes(const fp4moe_config* cfg) {
 fp4moe_status fp4moe_weight_bytes(const fp4moe_config* cfg, size_t* w1_codes, size_t* w1_sf, size_t* w2_codes,
                                   size_t* w2_sf) {
   FP4_TRY(check_cfg(cfg));
-  const size_t E = cfg->num_experts, H = cfg->hidden, I = cfg->inter;
+  const size_t E = local_experts(*cfg), H = cfg->hidden, I = cfg->inter;
   if (is_mx(cfg)) {  // atom-tiled: two codes per byte, one E8M0 byte per 32 elements
     if (w1_codes) *w1_codes = E * 2 * I * H / 2;
     if (w1_sf) *w1_sf = E * 2 * I * H / 32;
@@ -282,7 +287,8 @@ fp4moe_status moe_combine(const fp4moe_config* cfg, int32_t T, const float* o_pa
   FP4_TRY(check_cfg(cfg));
   FP4_TRY(check_T(cfg, T));
   FP4_TRY(check_ptrs(o_pairs, topk_w, y));
-  return combine_launch(*cfg, T, o_pairs, topk_w, y, (cudaStream_t)stream);
+  if (cfg->ep_count > 0) return FP4MOE_UNSUPPORTED;  // the pairs held elsewhere are known only to moe_forward
+  return combine_launch(*cfg, T, o_pairs, topk_w, nullptr, y, (cudaStream_t)stream);
 }
 
 fp4moe_status moe_grouped_gemm_w2_combine(const fp4moe_config* cfg, int32_t T, const uint8_t* a2_fp4,
@@ -292,18 +298,19 @@ fp4moe_status moe_grouped_gemm_w2_combine(const fp4moe_config* cfg, int32_t T, c
                                           fp4moe_stream_t stream) {
   FP4_TRY(check_cfg(cfg));
   FP4_TRY(check_T(cfg, T));
+  if (cfg->ep_count > 0) return FP4MOE_UNSUPPORTED;  // the pairs held elsewhere are known only to moe_forward
   const WsLayout L = ws_layout(*cfg);
   float* o = at<float>(ws, L.opairs);
   if (is_mx(cfg)) {
     FP4_TRY(check_ptrs(a2_fp4, padded_offsets, pair_of_row, w2_fp4, w2_sf, topk_w, y, ws));
     FP4_TRY(mx_gemm_launch(true, *cfg, T, reinterpret_cast<const uint16_t*>(a2_fp4), padded_offsets, pair_of_row,
                            w2_fp4, w2_sf, nullptr, o, err_word(ws), (cudaStream_t)stream));
-    return combine_launch(*cfg, T, o, topk_w, y, (cudaStream_t)stream);
+    return combine_launch(*cfg, T, o, topk_w, nullptr, y, (cudaStream_t)stream);
   }
   FP4_TRY(check_ptrs(a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, topk_w, y, ws));
   FP4_TRY(gemm_launch(kW2Rows, *cfg, T, a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, nullptr,
                       nullptr, nullptr, nullptr, o, err_word(ws), at<int>(ws, kWsSchedW2), (cudaStream_t)stream));
-  return combine_launch(*cfg, T, o, topk_w, y, (cudaStream_t)stream);
+  return combine_launch(*cfg, T, o, topk_w, nullptr, y, (cudaStream_t)stream);
 }
 
 fp4moe_status moe_forward(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
@@ -343,7 +350,8 @@ fp4moe_status moe_forward(const fp4moe_config* cfg, int32_t T, const uint16_t* x
     FP4_TRY(gemm_launch(kW2Rows, *cfg, T, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), poff, por, w2_fp4, w2_sf,
                         alpha2, nullptr, nullptr, nullptr, nullptr, at<float>(ws, L.opairs), err, at<int>(ws, kWsSchedW2), st));
   }
-  FP4_TRY(combine_launch(*cfg, T, at<float>(ws, L.opairs), w, y, st));
+  FP4_TRY(combine_launch(*cfg, T, at<float>(ws, L.opairs), w, cfg->ep_count > 0 ? at<int32_t>(ws, L.slot) : nullptr, y,
+                         st));
   const size_t pk = (size_t)T * cfg->top_k;
   if (topk_ids_out && pk && cudaMemcpyAsync(topk_ids_out, ids, pk * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
     return FP4MOE_CUDA_ERROR;
@@ -356,7 +364,7 @@ fp4moe_status fp4moe_quantize_weights(const fp4moe_config* cfg, int32_t which, i
                                       uint8_t* codes_out, uint8_t* sf_out, float* gs_out, fp4moe_stream_t stream) {
   FP4_TRY(check_cfg(cfg));
   if (which != 1 && which != 2) return FP4MOE_INVALID_ARG;
-  if (n_experts < 0 || n_experts > cfg->num_experts) return FP4MOE_INVALID_ARG;
+  if (n_experts < 0 || n_experts > local_experts(*cfg)) return FP4MOE_INVALID_ARG;
   const cudaStream_t st = (cudaStream_t)stream;
   const int32_t rows = which == 1 ? 2 * cfg->inter : cfg->hidden;
   const int32_t K = which == 1 ? cfg->hidden : cfg->inter;
@@ -407,7 +415,7 @@ fp4moe_status fp4moe_calibrate(const fp4moe_config* cfg, int32_t T, const uint16
   FP4_TRY(quant_scatter_launch(*cfg, T, x_warm, gs1_out, at<int32_t>(ws, L.slot), at<uint8_t>(ws, L.a1),
                                at<uint8_t>(ws, L.a1sf), st));
   float* alpha = at<float>(ws, L.alpha_tmp);
-  FP4_TRY(make_alpha_launch(cfg->num_experts, gs1_out, gw1, alpha, st));
+  FP4_TRY(make_alpha_launch(local_experts(*cfg), gs1_out, gw1, alpha, st));
   if (cudaMemsetAsync(amax_h, 0, 4, st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
   FP4_TRY(gemm_launch(kW1Amax, *cfg, T, at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf), poff, por, w1_fp4, w1_sf,
                       alpha, nullptr, nullptr, nullptr, amax_h, nullptr, err, at<int>(ws, kWsSchedW1), st));
@@ -421,7 +429,7 @@ fp4moe_status fp4moe_batch_gs1(const fp4moe_config* cfg, int32_t T, const uint16
   FP4_TRY(check_T(cfg, T));
   if (is_mx(cfg)) return FP4MOE_UNSUPPORTED;  // MXFP4 layers keep bf16 activations: no global scales
   FP4_TRY(check_ptrs(x, gw1, gs1_out, alpha1_out, ws));
-  return batch_gs1_launch(T, cfg->hidden, x, cfg->num_experts, gw1, gs1_out, alpha1_out,
+  return batch_gs1_launch(T, cfg->hidden, x, local_experts(*cfg), gw1, gs1_out, alpha1_out,
                           at<unsigned int>(ws, kWsBatchAmax), at<unsigned int>(ws, kWsBatchDone),
                           (cudaStream_t)stream);
 }

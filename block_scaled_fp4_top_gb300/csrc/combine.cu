@@ -21,7 +21,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float* __restrict__ o,
-                                                      const float* __restrict__ w, uint16_t* __restrict__ y) {
+                                                      const float* __restrict__ w,
+                                                      const int32_t* __restrict__ slot_of_pair,
+                                                      uint16_t* __restrict__ y) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.y;
@@ -29,6 +31,7 @@ __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float*
   if (col >= H) return;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int j = 0; j < k; ++j) {
+    if (slot_of_pair != nullptr && __ldcg(slot_of_pair + (size_t)t * k + j) < 0) continue;  // not held here
     const float wj = __ldcg(w + (size_t)t * k + j);
     const float4* src = reinterpret_cast<const float4*>(o + ((size_t)t * k + j) * H + col);
     const float4 a = __ldcg(src), b = __ldcg(src + 1);
@@ -49,10 +52,11 @@ __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float*
 }  // namespace
 
 fp4moe_status combine_launch(const fp4moe_config& cfg, int32_t T, const float* o_pairs, const float* w,
-                             uint16_t* y, cudaStream_t st) {
+                             const int32_t* slot_of_pair, uint16_t* y, cudaStream_t st) {
   if (T == 0) return FP4MOE_OK;
   const int H = cfg.hidden;
-  return launch_pdl(combine_kernel, dim3((H / 8 + 255) / 256, T), dim3(256), 0, st, H, cfg.top_k, o_pairs, w, y) ==
+  return launch_pdl(combine_kernel, dim3((H / 8 + 255) / 256, T), dim3(256), 0, st, H, cfg.top_k, o_pairs, w,
+                    slot_of_pair, y) ==
                  cudaSuccess
              ? FP4MOE_OK
              : FP4MOE_CUDA_ERROR;

@@ -670,7 +670,7 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
   const int Kc = w2 ? cfg.inter : cfg.hidden;
   if (Kc > kMaxResidentK) return FP4MOE_UNSUPPORTED;
   Params prm;
-  prm.E = cfg.num_experts;
+  prm.E = local_experts(cfg);
   prm.K = w2 ? cfg.inter : cfg.hidden;
   prm.KB = (prm.K + 64 * ATOMS - 1) / (64 * ATOMS);
   prm.nacc = (2 * (int)ACC_COLS + prm.K / 16 + (int)SFB_STAGE_COLS * STAGES <= (int)TMEM_COLS) ? 2 : 1;
@@ -694,7 +694,7 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
   prm.o_pairs = o_pairs;
   prm.err = err;
   // the dynamic chunk schedule pays off once experts average a whole m-tile (prefill sizes)
-  prm.dyn = ((int64_t)T * cfg.top_k >= (int64_t)cfg.num_experts * BM) ? 1 : 0;
+  prm.dyn = ((int64_t)T * cfg.top_k >= (int64_t)local_experts(cfg) * BM) ? 1 : 0;
   prm.sched = sched;
   if (prm.dyn && (sched == nullptr || cudaMemsetAsync(sched, 0, sizeof(int), st) != cudaSuccess))
     return FP4MOE_CUDA_ERROR;

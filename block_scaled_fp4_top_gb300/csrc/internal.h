@@ -27,6 +27,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 size_t capacity_rows(const fp4moe_config& cfg, int32_t T);
 
+// Experts this layer holds: [ep_first, ep_first + ep_count) of the router's num_experts, or all of them.
+inline int local_experts(const fp4moe_config& c) { return c.ep_count > 0 ? c.ep_count : c.num_experts; }
+
 // Byte offsets of the regions of a workspace sized for cfg.max_tokens.
 struct WsLayout {
   size_t hist, nw2, logits, ids, w, counts, offsets, poff, slot, por, a1, a1sf, a2, a2sf, opairs, alpha_tmp, total;
@@ -88,7 +91,9 @@ fp4moe_status mx_quant_rows_launch(int64_t n_rows, int32_t K, int32_t rows_per_g
 fp4moe_status scatter_rows_bf16_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x,
                                        const int32_t* slot_of_pair, uint16_t* a1, cudaStream_t st);
 
+// y[t] = bf16(sum_j w[t,j] o[t*k+j]); with slot_of_pair, pairs without a slot (held by no local expert) are
+// left out of the sum
 fp4moe_status combine_launch(const fp4moe_config& cfg, int32_t T, const float* o_pairs, const float* w,
-                             uint16_t* y, cudaStream_t st);
+                             const int32_t* slot_of_pair, uint16_t* y, cudaStream_t st);
 
 }  // namespace fp4moe

@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(256) scatter_rows_bf16_kernel(int H, int k, co
   const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + c);
   for (int j = 0; j < k; ++j) {
     const int s = __ldcg(slot_of_pair + (size_t)t * k + j);
-    reinterpret_cast<uint4*>(a1 + (size_t)s * H)[c] = v;
+    if (s >= 0) reinterpret_cast<uint4*>(a1 + (size_t)s * H)[c] = v;  // -1: held by no local expert
   }
 }
 
@@ -434,7 +434,7 @@ fp4moe_status mx_gemm_launch(bool w2, const fp4moe_config& cfg, int32_t T, const
                              cudaStream_t st) {
   if (T == 0) return FP4MOE_OK;
   MxParams prm;
-  prm.E = cfg.num_experts;
+  prm.E = local_experts(cfg);
   prm.K = w2 ? cfg.inter : cfg.hidden;
   prm.KA = prm.K / 64;
   prm.NT = (w2 ? cfg.hidden : 2 * cfg.inter) / MX_BN;

@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(int T, int H, int k,
   const uint32_t sf = quant_block16(v, g, lo, hi);
   for (int j = 0; j < k; ++j) {
     const int row = __ldcg(slot_of_pair + (size_t)t * k + j);
+    if (row < 0) continue;  // held by no local expert
     *reinterpret_cast<uint2*>(a1 + (size_t)row * (H >> 1) + b * 8) = make_uint2(lo, hi);
     a1_sf[sf_offset(row, b, C)] = (uint8_t)sf;
   }

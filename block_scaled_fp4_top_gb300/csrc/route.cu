@@ -87,7 +87,15 @@ __device__ __forceinline__ void offsets_and_pads(int E, int cap, int c, int* s_w
 // Decode-sized layout in one CTA of 1024 threads: histogram, offsets, pads,
 // and slots in ascending pair order (warp 0 walks the pairs 32 at a time;
 // lanes sharing an expert rank themselves by lane order).
-__global__ void __launch_bounds__(1024) layout_small_kernel(int npairs, int E, int cap,
+// Local expert of global id g: g - first for the experts [first, first + E) this layer holds, -1 for an
+// expert held elsewhere (its pair is masked out, "Bug 8"), -2 for an id outside [0, Eg) (an error).
+__device__ __forceinline__ int local_expert(int g, int Eg, int first, int E) {
+  if (g < 0 || g >= Eg) return -2;
+  const int l = g - first;
+  return (l >= 0 && l < E) ? l : -1;
+}
+
+__global__ void __launch_bounds__(1024) layout_small_kernel(int npairs, int Eg, int first, int E, int cap,
                                                             const int32_t* __restrict__ ids,
                                                             int32_t* __restrict__ counts,
                                                             int32_t* __restrict__ offsets,
@@ -103,13 +111,10 @@ __global__ void __launch_bounds__(1024) layout_small_kernel(int npairs, int E, i
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
   __syncthreads();
   for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
-    int e = __ldcg(ids + p);
-    if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
-    else {
-      raise_error(err, FP4MOE_ERR_EXPERT_ID);
-      e = -1;
-    }
-    s_ids[p] = e;
+    int e = local_expert(__ldcg(ids + p), Eg, first, E);
+    if (e >= 0) atomicAdd(&s_cnt[e], 1);
+    else if (e == -2) raise_error(err, FP4MOE_ERR_EXPERT_ID);
+    s_ids[p] = e < 0 ? -1 : e;
   }
   __syncthreads();
   const int c = (threadIdx.x < E) ? s_cnt[threadIdx.x] : 0;
@@ -129,6 +134,8 @@ __global__ void __launch_bounds__(1024) layout_small_kernel(int npairs, int E, i
       slot_of_pair[p] = slot;
       if (slot < cap) pair_of_row[slot] = p;
       else raise_error(err, FP4MOE_ERR_CAPACITY);
+    } else if (p < npairs) {
+      slot_of_pair[p] = -1;  // held by no local expert: no slot
     }
     __syncwarp();
     if (e >= 0 && rank == 0) s_base[e] += __popc(peers);
@@ -137,8 +144,9 @@ __global__ void __launch_bounds__(1024) layout_small_kernel(int npairs, int E, i
 }
 
 // Per-chunk expert histograms (64 tokens per chunk), for large T.
-__global__ void __launch_bounds__(256) hist_kernel(int T, int E, int k, const int32_t* __restrict__ ids,
-                                                   int32_t* __restrict__ hist, uint32_t* err) {
+__global__ void __launch_bounds__(256) hist_kernel(int T, int Eg, int first, int E, int k,
+                                                   const int32_t* __restrict__ ids, int32_t* __restrict__ hist,
+                                                   uint32_t* err) {
   pdl_wait();
   pdl_trigger();
   __shared__ int sh[kMaxExperts];
@@ -147,9 +155,9 @@ __global__ void __launch_bounds__(256) hist_kernel(int T, int E, int k, const in
   const int p0 = blockIdx.x * kRouteChunk * k;
   const int p1 = min(T, (blockIdx.x + 1) * kRouteChunk) * k;
   for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
-    const int e = __ldcg(ids + p);
-    if (e >= 0 && e < E) atomicAdd(&sh[e], 1);
-    else raise_error(err, FP4MOE_ERR_EXPERT_ID);
+    const int e = local_expert(__ldcg(ids + p), Eg, first, E);
+    if (e >= 0) atomicAdd(&sh[e], 1);
+    else if (e == -2) raise_error(err, FP4MOE_ERR_EXPERT_ID);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(size_t)blockIdx.x * E + e] = sh[e];
@@ -184,7 +192,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(int E, int nchunks, int cap,
 }
 
 // Slot of every pair of one 64-token chunk, in ascending pair order.
-__global__ void __launch_bounds__(256) slots_kernel(int T, int E, int k, int cap, const int32_t* __restrict__ ids,
+__global__ void __launch_bounds__(256) slots_kernel(int T, int Eg, int first, int E, int k, int cap,
+                                                    const int32_t* __restrict__ ids,
                                                     const int32_t* __restrict__ counts,
                                                     const int32_t* __restrict__ poff,
                                                     const int32_t* __restrict__ chunk_base,
@@ -202,8 +211,8 @@ __global__ void __launch_bounds__(256) slots_kernel(int T, int E, int k, int cap
   const int p1 = min(T, (blockIdx.x + 1) * kRouteChunk) * k;
   for (int pb = p0; pb < p1; pb += 32) {
     const int p = pb + lane;
-    int e = (p < p1) ? __ldcg(ids + p) : -1;
-    if (e >= E) e = -1;
+    int e = (p < p1) ? local_expert(__ldcg(ids + p), Eg, first, E) : -1;
+    if (e < 0) e = -1;
     const unsigned peers = __match_any_sync(kFull, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
     if (e >= 0) {
@@ -211,6 +220,8 @@ __global__ void __launch_bounds__(256) slots_kernel(int T, int E, int k, int cap
       slot_of_pair[p] = slot;
       if (slot < cap) pair_of_row[slot] = p;
       else raise_error(err, FP4MOE_ERR_CAPACITY);
+    } else if (p < p1) {
+      slot_of_pair[p] = -1;  // held by no local expert: no slot
     }
     __syncwarp();
     if (e >= 0 && rank == 0) base[e] += __popc(peers);
@@ -224,23 +235,24 @@ fp4moe_status route_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* 
                            const float* bias, float* logits, int32_t* ids, float* w, int32_t* counts,
                            int32_t* offsets, int32_t* poff, int32_t* slot_of_pair, int32_t* pair_of_row,
                            int32_t* hist, float* nw2, uint32_t* err, cudaStream_t st) {
-  const int E = cfg.num_experts, k = cfg.top_k;
+  const int Eg = cfg.num_experts, first = cfg.ep_count > 0 ? cfg.ep_first : 0, E = local_experts(cfg);
+  const int k = cfg.top_k;
   const int cap = (int)capacity_rows(cfg, T);
   const int npairs = T * k;
   const fp4moe_status rs = router_topk_launch(cfg, T, x, router_w, bias, logits, nw2, ids, w, err, st);
   if (rs != FP4MOE_OK) return rs;
   cudaError_t r = cudaSuccess;
   if (npairs <= kSmallPairs) {
-    r = launch_pdl(layout_small_kernel, dim3(1), dim3(1024), 0, st, npairs, E, cap, (const int32_t*)ids, counts,
-                   offsets, poff, slot_of_pair, pair_of_row, err);
+    r = launch_pdl(layout_small_kernel, dim3(1), dim3(1024), 0, st, npairs, Eg, first, E, cap, (const int32_t*)ids,
+                   counts, offsets, poff, slot_of_pair, pair_of_row, err);
   } else {
     const int nchunks = (T + kRouteChunk - 1) / kRouteChunk;
-    r = launch_pdl(hist_kernel, dim3(nchunks), dim3(256), 0, st, T, E, k, (const int32_t*)ids, hist, err);
+    r = launch_pdl(hist_kernel, dim3(nchunks), dim3(256), 0, st, T, Eg, first, E, k, (const int32_t*)ids, hist, err);
     if (r == cudaSuccess)
       r = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, st, E, nchunks, cap, hist, counts, offsets, poff,
                      pair_of_row, err);
     if (r == cudaSuccess)
-      r = launch_pdl(slots_kernel, dim3(nchunks), dim3(256), 0, st, T, E, k, cap, (const int32_t*)ids,
+      r = launch_pdl(slots_kernel, dim3(nchunks), dim3(256), 0, st, T, Eg, first, E, k, cap, (const int32_t*)ids,
                      (const int32_t*)counts, (const int32_t*)poff, (const int32_t*)hist, slot_of_pair, pair_of_row,
                      err);
   }

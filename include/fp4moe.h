@@ -108,6 +108,22 @@
  *    the combine are those of the NVFP4 layer. fp4moe_calibrate returns
  *    FP4MOE_UNSUPPORTED.
  *
+ * Expert parallelism ("Current Bug", "Bug 8", "Bug 13" and "EP Configuration"):
+ * with ep_count > 0 the layer holds experts [ep_first, ep_first + ep_count)
+ * of the router's num_experts.
+ *  - The router still scores all num_experts, and topk_ids / topk_w stay
+ *    global.
+ *  - counts, offsets, padded_offsets, the weights and alpha are per local
+ *    expert (ep_count entries); local id = global id - ep_first.
+ *  - A pair whose expert is held elsewhere gets slot_of_pair = -1, takes no
+ *    row, and is left out of this layer's sum, so y is this rank's part of
+ *    the output. Summing the parts of all ranks gives the whole layer.
+ *  - CAP uses ep_count in place of E.
+ *  - Warm-up calibration sees local ids only (the fix of "Bug 13").
+ *  - moe_combine and moe_grouped_gemm_w2_combine cannot tell which pairs are
+ *    held elsewhere, so they return FP4MOE_UNSUPPORTED for such layers. Use
+ *    moe_forward.
+ *
  * Supported shapes: H % 256 == 0, I % 128 == 0, H <= 4608, I <= 4608 (the
  * activation scales of a 128-row tile stay resident in TMEM for all of K),
  * 1 <= k <= 16, k <= E <= 1024, w_format FP4MOE_W_NVFP4 or FP4MOE_W_MXFP4.
@@ -151,7 +167,9 @@ typedef struct fp4moe_config {
   int32_t top_k;         /* k */
   int32_t max_tokens;    /* largest T any call will pass */
   float swiglu_limit;    /* L of the clamped SwiGLU */
-  int32_t w_format;      /* FP4MOE_W_NVFP4 */
+  int32_t w_format;      /* FP4MOE_W_NVFP4 or FP4MOE_W_MXFP4 */
+  int32_t ep_first;      /* expert parallelism: first expert this layer holds (global id) */
+  int32_t ep_count;      /* experts it holds; 0 = all num_experts (no expert parallelism) */
 } fp4moe_config;
 
 /* Version of this ABI (major*100 + minor). */

@@ -38,10 +38,20 @@ def capacity_rows(T: int, k: int, E: int) -> int:
     return max(cap, ROW_ALIGN)
 
 
+def local_ids(topk_ids: np.ndarray, first: int, count: int) -> np.ndarray:
+    """Expert parallelism ("Current Bug", "Bug 8"): the router's global expert ids become local ids
+    id - first for the experts [first, first + count) this layer holds, and -1 (masked out) otherwise."""
+    ids = np.asarray(topk_ids, dtype=np.int64)
+    local = ids - first
+    return np.where((local >= 0) & (local < count), local, -1)
+
+
 def counts(topk_ids: np.ndarray, E: int) -> np.ndarray:
+    """Pairs per expert; masked pairs (id -1) count for none."""
     c = np.zeros(E, dtype=np.int64)
     for e in np.asarray(topk_ids).reshape(-1):
-        c[int(e)] += 1
+        if e >= 0:
+            c[int(e)] += 1
     return c
 
 
@@ -81,7 +91,7 @@ def slots(topk_ids: np.ndarray, E: int):
 
     Returns a dict with:
       counts, offsets, padded_offsets : [E] int64
-      slot_of_pair                    : [T*k] int64
+      slot_of_pair                    : [T*k] int64, -1 for a masked pair (id -1)
       pair_of_row                     : [R] int64, -1 on padding rows (R = padded_offsets[-1])
     """
     ids = np.asarray(topk_ids).reshape(-1)
@@ -94,8 +104,12 @@ def slots(topk_ids: np.ndarray, E: int):
     slot = np.zeros(len(ids), dtype=np.int64)
     for p, e in enumerate(ids):
         e = int(e)
+        if e < 0:
+            slot[p] = -1
+            continue
         slot[p] = (poff[e] - P[e]) + seen[e]
         seen[e] += 1
     pair_of_row = np.full(R, -1, dtype=np.int64)
-    pair_of_row[slot] = np.arange(len(ids))
+    held = slot >= 0
+    pair_of_row[slot[held]] = np.arange(len(ids))[held]
     return dict(counts=c, offsets=off, padded_offsets=poff, slot_of_pair=slot, pair_of_row=pair_of_row, R=R)

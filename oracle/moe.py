@@ -144,6 +144,8 @@ def moe_tokens(x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray,
         xt = x
     outs = np.zeros((n, k, H), dtype=np.float64)
     for e in np.unique(ids):
+        if e < 0:   # a pair held by no local expert ("Bug 8"): left out of this layer's sum
+            continue
         tt, jj = np.nonzero(ids == e)
         qe = expert(int(e))
         h = expert_hidden(qe, xt[tt], limit)
@@ -154,7 +156,8 @@ def moe_tokens(x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray,
         outs[tt, jj] = o
     acc = np.zeros((n, H), dtype=np.float64)
     for j in range(k):
-        acc = acc + w[:, j:j + 1] * outs[:, j]
+        held = (ids[:, j] >= 0)[:, None]
+        acc = np.where(held, acc + w[:, j:j + 1] * outs[:, j], acc)
     return f32_to_bf16_bits(acc.astype(F32))
 
 
@@ -163,6 +166,8 @@ def calibrate(x_bits: np.ndarray, ids: np.ndarray, expert: Callable[[int], Quant
 
     gs1 = g(amax |x|). gs2 = g(amax |h|), taken over every routed (token, expert)
     pair of the warmup batch, with h computed from the gs1-quantised activations.
+    With expert parallelism the ids are local and masked pairs (-1) are skipped:
+    the fix of "Bug 13", where global ids matched no local expert and gs2 came out 0.
     """
     x = bf16_to_f64(x_bits)
     gs1 = nvfp4.global_scale(F32(np.abs(x).max()))
@@ -170,6 +175,8 @@ def calibrate(x_bits: np.ndarray, ids: np.ndarray, expert: Callable[[int], Quant
     xt = nvfp4.dequantize(q, sf, gs1)
     amax_h = 0.0
     for e in np.unique(ids):
+        if e < 0:
+            continue
         tt, _ = np.nonzero(ids == e)
         h = expert_hidden(expert(int(e)), xt[tt], limit)
         amax_h = max(amax_h, float(np.abs(h.astype(F32)).max()))

@@ -91,3 +91,28 @@ def test_slots_against_stable_sort():
             e = layout.searchsorted_right(L["padded_offsets"], r)
             if por[r] >= 0:
                 assert flat[por[r]] == e
+
+
+def test_expert_parallel_remap_and_mask():
+    """"Bug 8": global ids -> local ids for the held experts, the rest masked; the masked layout is the layout
+    of the held pairs alone, and every pair is held by exactly one rank of an EP split."""
+    rng = np.random.default_rng(8)
+    E, k, T = 256, 6, 40
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    first, count = 96, 48
+    loc = layout.local_ids(ids, first, count)
+    held = (ids >= first) & (ids < first + count)
+    assert (loc[held] == ids[held] - first).all() and (loc[~held] == -1).all()
+    L = layout.slots(loc, count)
+    flat = loc.reshape(-1)
+    assert (L["slot_of_pair"][flat < 0] == -1).all()
+    assert L["counts"].sum() == held.sum()
+    # the held pairs alone, in pair order, give the same rows
+    keep = np.nonzero(flat >= 0)[0]
+    L2 = layout.slots(flat[keep], count)
+    assert (L["counts"] == L2["counts"]).all() and (L["padded_offsets"] == L2["padded_offsets"]).all()
+    assert (L["slot_of_pair"][keep] == L2["slot_of_pair"]).all()
+    assert (L["pair_of_row"][L["pair_of_row"] >= 0] == keep[L2["pair_of_row"][L2["pair_of_row"] >= 0]]).all()
+    # an 8-way split holds every pair once
+    owners = sum((layout.local_ids(ids, 32 * r, 32) >= 0).astype(int) for r in range(8))
+    assert (owners == 1).all()

@@ -7,7 +7,7 @@ import torch
 import torch.nn.functional as F
 
 import synthgen as sg
-from oracle import moe, nvfp4
+from oracle import layout, moe, nvfp4
 
 
 def test_router_logits_are_the_exact_sum_rounded_once():
@@ -143,3 +143,40 @@ def test_calibration_scales_come_from_the_warmup_batch():
     hs = [moe.expert_hidden(experts[e], xt[np.nonzero(ids == e)[0]], wl.swiglu_limit) for e in np.unique(ids)]
     h = np.concatenate(hs).astype(np.float32)
     assert float(np.abs(h).max()) * float(gs2) == pytest.approx(2688.0, rel=1e-6)
+
+
+def test_expert_parallel_parts_sum_to_the_layer():
+    """The rank parts of an EP split (masked pairs left out) sum to the whole layer, before the bf16 rounding."""
+    wl = sg.TINY
+    x = sg.activations_bf16(wl, sg.EVAL_SEED, T=6)
+    ids, w = moe.topk_softmax(moe.router_logits(x, sg.router_bf16(wl), None), wl.k)
+    cache = {}
+
+    def expert(e):
+        if e not in cache:
+            cache[e] = moe.quantize_expert(sg.expert_w1_f32(wl, e), sg.expert_w2_f32(wl, e))
+        return cache[e]
+    gs1, gs2 = np.float32(200.0), np.float32(300.0)
+    xf = sg.bf16_bits_to_f32(x).astype(np.float64)
+
+    def layer_sum(ids_local, first):
+        """sum_j w_j o_j over held pairs, in fp64 (the layer before its final bf16 rounding)."""
+        q, s = nvfp4.quantize_rows(xf.astype(np.float32), gs1)
+        xt = nvfp4.dequantize(q, s, gs1)
+        acc = np.zeros((x.shape[0], wl.H))
+        for t in range(x.shape[0]):
+            for j in range(wl.k):
+                if ids_local[t, j] < 0:
+                    continue
+                qe = expert(first + int(ids_local[t, j]))
+                h = moe.expert_hidden(qe, xt[t:t + 1], wl.swiglu_limit)
+                acc[t] += w[t, j] * moe.expert_out(qe, h, gs2)[0]
+        return acc
+
+    full = layer_sum(ids, 0)
+    parts = sum(layer_sum(layout.local_ids(ids, f, 4), f) for f in (0, 4))
+    assert np.allclose(parts, full, rtol=1e-12, atol=1e-15)
+    # and moe_tokens with a masked routing rounds that part
+    part0 = moe.moe_tokens(x, layout.local_ids(ids, 0, 4), w, lambda l: expert(l), gs1, gs2, wl.swiglu_limit)
+    ref0 = moe.f32_to_bf16_bits(layer_sum(layout.local_ids(ids, 0, 4), 0).astype(np.float32))
+    assert (part0 == ref0).all()
