@@ -127,12 +127,14 @@ def expert_out(qe: QuantExpert, h: np.ndarray, gs2) -> np.ndarray:
 
 def moe_tokens(x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray,
                expert: Callable[[int], QuantExpert], gs1, gs2, limit: float,
-               quantize_activations: bool = True) -> np.ndarray:
+               quantize_activations: bool = True, shared: np.ndarray | None = None) -> np.ndarray:
     """The layer for a set of token rows with their routing. Returns y as bf16 bits [n, H].
 
     x_bits [n, H] bf16 bits, ids [n, k], w [n, k]. ``expert(e)`` gives the quantised
     weights of expert e. quantize_activations=False replaces both activation
     codecs by the identity (used to pin the layer against a textbook dense MoE).
+    ``shared`` [n, H] is a shared expert's output, added with weight 1 after the
+    routed terms (``fp8block.shared_out``).
     """
     x = bf16_to_f64(x_bits)
     n, H = x.shape
@@ -158,6 +160,8 @@ def moe_tokens(x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray,
     for j in range(k):
         held = (ids[:, j] >= 0)[:, None]
         acc = np.where(held, acc + w[:, j:j + 1] * outs[:, j], acc)
+    if shared is not None:
+        acc = acc + shared
     return f32_to_bf16_bits(acc.astype(F32))
 
 
