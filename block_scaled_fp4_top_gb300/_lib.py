@@ -20,10 +20,16 @@ W_NVFP4, W_MXFP4 = 0, 1
 class Config(ctypes.Structure):
     _fields_ = [("hidden", c_i32), ("inter", c_i32), ("inter_logical", c_i32), ("num_experts", c_i32),
                 ("top_k", c_i32), ("max_tokens", c_i32), ("swiglu_limit", c_f32), ("w_format", c_i32),
-                ("ep_first", c_i32), ("ep_count", c_i32)]
+                ("ep_first", c_i32), ("ep_count", c_i32), ("shared_inter", c_i32)]
+
+
+class SharedWeights(ctypes.Structure):
+    """fp4moe_shared_weights: device pointers of the shared expert's block-FP8 weights."""
+    _fields_ = [("w1", c_vp), ("w1_scales", c_vp), ("w2", c_vp), ("w2_scales", c_vp)]
 
 
 CP = ctypes.POINTER(Config)
+SWP = ctypes.POINTER(SharedWeights)
 
 # name -> (restype, argtypes); pointers to device memory are passed as c_void_p
 SIGNATURES = {
@@ -48,6 +54,12 @@ SIGNATURES = {
     "fp4moe_selftest_wait_timeout": (c_i32, [c_vp, ctypes.c_int64, c_vp, c_vp]),
     "fp4moe_batch_gs1": (c_i32, [CP, c_i32] + [c_vp] * 6),
     "fp4moe_read_error": (c_i32, [c_vp, ctypes.POINTER(c_u32), c_i32, c_vp]),
+    "fp4moe_shared_weight_bytes": (c_i32, [CP, ctypes.POINTER(c_sz), ctypes.POINTER(c_sz), ctypes.POINTER(c_sz),
+                                           ctypes.POINTER(c_sz)]),
+    "fp4moe_shared_quantize_weights": (c_i32, [CP, c_i32] + [c_vp] * 4),
+    "moe_shared_expert": (c_i32, [CP, c_i32, c_vp, SWP, c_vp, c_vp, c_vp]),
+    "moe_combine_shared": (c_i32, [CP, c_i32] + [c_vp] * 6),
+    "moe_forward_shared": (c_i32, [CP, c_i32] + [c_vp] * 11 + [SWP] + [c_vp] * 5),
 }
 
 _lib = None

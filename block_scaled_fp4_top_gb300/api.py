@@ -25,10 +25,12 @@ class Fp4MoeError(RuntimeError):
 
 
 def config(hidden: int, inter: int, num_experts: int, top_k: int, max_tokens: int, swiglu_limit: float,
-           inter_logical: int = 0, w_format: int = _lib.W_NVFP4, ep_first: int = 0, ep_count: int = 0) -> Config:
-    """Layer configuration. ep_count > 0 makes the layer hold experts [ep_first, ep_first + ep_count) only."""
+           inter_logical: int = 0, w_format: int = _lib.W_NVFP4, ep_first: int = 0, ep_count: int = 0,
+           shared_inter: int = 0) -> Config:
+    """Layer configuration. ep_count > 0 makes the layer hold experts [ep_first, ep_first + ep_count) only;
+    shared_inter > 0 gives it a block-FP8 shared expert of that (kernel-local) intermediate width."""
     return Config(hidden, inter, inter_logical or inter, num_experts, top_k, max_tokens, swiglu_limit, w_format,
-                  ep_first, ep_count)
+                  ep_first, ep_count, shared_inter)
 
 
 def _p(t):
@@ -153,6 +155,41 @@ def fp4moe_selftest_wait_timeout(err, limit_ns, result, stream=None):
            "fp4moe_selftest_wait_timeout")
 
 
+def _sw(se):
+    """fp4moe_shared_weights from a SharedWeights holder (device pointers of its four tensors)."""
+    return ctypes.byref(_lib.SharedWeights(_p(se.w1), _p(se.w1_scales), _p(se.w2), _p(se.w2_scales)))
+
+
+def shared_weight_bytes(cfg: Config):
+    v = [ctypes.c_size_t() for _ in range(4)]
+    _check(_lib.load().fp4moe_shared_weight_bytes(ctypes.byref(cfg), *[ctypes.byref(x) for x in v]),
+           "fp4moe_shared_weight_bytes")
+    return tuple(x.value for x in v)
+
+
+def fp4moe_shared_quantize_weights(cfg, which, w, codes_out, scales_out, stream=None):
+    _check(_lib.load().fp4moe_shared_quantize_weights(ctypes.byref(cfg), which, _p(w), _p(codes_out),
+                                                      _p(scales_out), _s(stream)), "fp4moe_shared_quantize_weights")
+
+
+def moe_shared_expert(cfg, T, x, se, o_shared, ws, stream=None):
+    _check(_lib.load().moe_shared_expert(ctypes.byref(cfg), T, _p(x), _sw(se), _p(o_shared), _p(ws), _s(stream)),
+           "moe_shared_expert")
+
+
+def moe_combine_shared(cfg, T, o_pairs, topk_w, slot_of_pair, o_shared, y, stream=None):
+    _check(_lib.load().moe_combine_shared(ctypes.byref(cfg), T, _p(o_pairs), _p(topk_w), _p(slot_of_pair),
+                                          _p(o_shared), _p(y), _s(stream)), "moe_combine_shared")
+
+
+def moe_forward_shared(cfg, T, x, router_w, router_bias, gs1, gs2, w1_fp4, w1_sf, alpha1, w2_fp4, w2_sf, alpha2, se,
+                       y, topk_ids_out, topk_w_out, ws, stream=None):
+    _check(_lib.load().moe_forward_shared(ctypes.byref(cfg), T, _p(x), _p(router_w), _p(router_bias), _p(gs1),
+                                          _p(gs2), _p(w1_fp4), _p(w1_sf), _p(alpha1), _p(w2_fp4), _p(w2_sf),
+                                          _p(alpha2), _sw(se), _p(y), _p(topk_ids_out), _p(topk_w_out), _p(ws),
+                                          _s(stream)), "moe_forward_shared")
+
+
 def fp4moe_read_error(ws, clear=True, stream=None) -> int:
     v = ctypes.c_uint32()
     _check(_lib.load().fp4moe_read_error(_p(ws), ctypes.byref(v), 1 if clear else 0, _s(stream)), "fp4moe_read_error")
@@ -168,6 +205,15 @@ class Weights:
     w2_fp4: torch.Tensor
     w2_sf: torch.Tensor
     gw2: torch.Tensor
+
+
+@dataclass
+class SharedWeights:
+    """The shared expert's block-FP8 weights in the layout of include/fp4moe.h."""
+    w1: torch.Tensor         # [2 Is][H] E4M3 bytes, kernel row order
+    w1_scales: torch.Tensor  # [2 Is / 128][H / 128] fp32
+    w2: torch.Tensor         # [H][Is]
+    w2_scales: torch.Tensor  # [H / 128][Is / 128]
 
 
 class MoELayer:
@@ -189,6 +235,11 @@ class MoELayer:
         self.alpha2 = torch.empty(E, **f32)
         self.router_w = None
         self.router_bias = None
+        self.shared = None
+        if cfg.shared_inter > 0:
+            sb = shared_weight_bytes(cfg)
+            self.shared = SharedWeights(torch.empty(sb[0], **u8), torch.empty(sb[1] // 4, **f32),
+                                        torch.empty(sb[2], **u8), torch.empty(sb[3] // 4, **f32))
 
     # ---- load-time prep
     def quantize_weights(self, which: int, e0: int, w: torch.Tensor):
@@ -210,6 +261,12 @@ class MoELayer:
             codes, sf, gs = W.w2_fp4, W.w2_sf, W.gw2
         fp4moe_quantize_weights(cfg, which, n, w.contiguous(), codes[e0 * per_c:(e0 + n) * per_c],
                                 sf[e0 * per_s:(e0 + n) * per_s], gs[e0:e0 + n])
+
+    def quantize_shared_weights(self, which: int, w: torch.Tensor):
+        """Block-FP8 of the shared expert's W1 (which=1, [2 Is, H], gate rows then up) or W2 (which=2, [H, Is])."""
+        se = self.shared
+        codes, scales = (se.w1, se.w1_scales) if which == 1 else (se.w2, se.w2_scales)
+        fp4moe_shared_quantize_weights(self.cfg, which, w.contiguous(), codes, scales)
 
     def set_router(self, router_w: torch.Tensor, router_bias: torch.Tensor | None = None):
         self.router_w = router_w.contiguous()
@@ -240,6 +297,11 @@ class MoELayer:
     def forward(self, x: torch.Tensor, y: torch.Tensor, topk_ids: torch.Tensor | None = None,
                 topk_w: torch.Tensor | None = None, stream=None):
         W = self.weights
+        if self.shared is not None:  # routed experts plus the shared expert, one combine
+            moe_forward_shared(self.cfg, x.shape[0], x, self.router_w, self.router_bias, self.gs1, self.gs2,
+                               W.w1_fp4, W.w1_sf, self.alpha1, W.w2_fp4, W.w2_sf, self.alpha2, self.shared, y,
+                               topk_ids, topk_w, self.ws, stream)
+            return
         moe_forward(self.cfg, x.shape[0], x, self.router_w, self.router_bias, self.gs1, self.gs2, W.w1_fp4, W.w1_sf,
                     self.alpha1, W.w2_fp4, W.w2_sf, self.alpha2, y, topk_ids, topk_w, self.ws, stream)
 

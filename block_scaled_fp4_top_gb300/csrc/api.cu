@@ -32,6 +32,8 @@ fp4moe_status check_cfg(const fp4moe_config* c) {
   if (c->ep_count < 0 || (c->ep_count == 0 && c->ep_first != 0) ||
       (c->ep_count > 0 && (c->ep_first < 0 || c->ep_first + c->ep_count > c->num_experts)))
     return FP4MOE_INVALID_ARG;
+  if (c->shared_inter < 0) return FP4MOE_INVALID_ARG;
+  if (c->shared_inter % 128 != 0) return FP4MOE_UNSUPPORTED;  // whole 128 x 128 FP8 blocks
   if (c->w_format == FP4MOE_W_NVFP4) {
     if (c->inter_logical != 0 && c->inter_logical != c->inter) return FP4MOE_UNSUPPORTED;
   } else {  // MXFP4: the logical width is whole 32-element scale groups inside the kernel width
@@ -109,6 +111,14 @@ WsLayout ws_layout(const fp4moe_config& c) {
   L.a2sf = take(mx ? 0 : cap * (size_t)c.inter / 16);
   L.opairs = take(Tm * k * (size_t)c.hidden * 4);
   L.alpha_tmp = take(E * 4);
+  if (c.shared_inter > 0) {  // the shared expert: FP8 activations, their scales, and its fp32 output
+    const size_t tcap = se_tcap(c), Is = (size_t)c.shared_inter, H = (size_t)c.hidden;
+    L.se_qx = take(tcap * H);
+    L.se_sx = take(H / 128 * tcap * 4);
+    L.se_qh = take(tcap * Is);
+    L.se_sh = take(Is / 128 * tcap * 4);
+    L.se_o = take(Tm * H * 4);
+  }
   L.total = off;
   return L;
 }
@@ -148,13 +158,81 @@ fp4moe_status route_scratch(uint8_t** out) {
 }
 }  // namespace
 
+namespace {
+fp4moe_status check_shared(const fp4moe_config* cfg, const fp4moe_shared_weights* se) {
+  if (cfg->shared_inter <= 0 || se == nullptr) return FP4MOE_INVALID_ARG;
+  return check_ptrs(se->w1, se->w1_scales, se->w2, se->w2_scales);
+}
+
+fp4moe_status shared_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const fp4moe_shared_weights& se,
+                            float* o_shared, void* ws, cudaStream_t st) {
+  const WsLayout L = ws_layout(cfg);
+  return se_forward_launch(cfg, T, x, se.w1, se.w1_scales, se.w2, se.w2_scales, at<uint8_t>(ws, L.se_qx),
+                           at<float>(ws, L.se_sx), at<uint8_t>(ws, L.se_qh), at<float>(ws, L.se_sh), o_shared,
+                           err_word(ws), st);
+}
+
+// The routed layer, with the shared expert's output added in the combine when se is not NULL.
+fp4moe_status forward_impl(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
+                           const float* router_bias, const float* gs1, const float* gs2, const uint8_t* w1_fp4,
+                           const uint8_t* w1_sf, const float* alpha1, const uint8_t* w2_fp4, const uint8_t* w2_sf,
+                           const float* alpha2, const fp4moe_shared_weights* se, uint16_t* y, int32_t* topk_ids_out,
+                           float* topk_w_out, void* ws, fp4moe_stream_t stream) {
+  FP4_TRY(check_cfg(cfg));
+  FP4_TRY(check_T(cfg, T));
+  const bool mx = is_mx(cfg);  // MXFP4: gs1, gs2, alpha1 and alpha2 are unused and may be NULL
+  if (mx) FP4_TRY(check_ptrs(x, router_w, w1_fp4, w1_sf, w2_fp4, w2_sf, y, ws));
+  else FP4_TRY(check_ptrs(x, router_w, gs1, gs2, w1_fp4, w1_sf, alpha1, w2_fp4, w2_sf, alpha2, y, ws));
+  FP4_TRY(check_opt(router_bias));
+  FP4_TRY(check_opt(topk_ids_out));
+  FP4_TRY(check_opt(topk_w_out));
+  const cudaStream_t st = (cudaStream_t)stream;
+  const WsLayout L = ws_layout(*cfg);
+  uint32_t* err = err_word(ws);
+  int32_t* ids = at<int32_t>(ws, L.ids);
+  float* w = at<float>(ws, L.w);
+  int32_t* poff = at<int32_t>(ws, L.poff);
+  int32_t* por = at<int32_t>(ws, L.por);
+  FP4_TRY(route_launch(*cfg, T, x, router_w, router_bias, at<float>(ws, L.logits), ids, w, at<int32_t>(ws, L.counts),
+                       at<int32_t>(ws, L.offsets), poff, at<int32_t>(ws, L.slot), por, at<int32_t>(ws, L.hist),
+                       at<float>(ws, L.nw2), err, st));
+  if (mx) {
+    uint16_t* a1 = at<uint16_t>(ws, L.a1);
+    uint16_t* a2 = at<uint16_t>(ws, L.a2);
+    FP4_TRY(scatter_rows_bf16_launch(*cfg, T, x, at<int32_t>(ws, L.slot), a1, st));
+    FP4_TRY(mx_gemm_launch(false, *cfg, T, a1, poff, por, w1_fp4, w1_sf, a2, nullptr, err, st));
+    FP4_TRY(mx_gemm_launch(true, *cfg, T, a2, poff, por, w2_fp4, w2_sf, nullptr, at<float>(ws, L.opairs), err, st));
+  } else {
+    FP4_TRY(quant_scatter_launch(*cfg, T, x, gs1, at<int32_t>(ws, L.slot), at<uint8_t>(ws, L.a1),
+                                 at<uint8_t>(ws, L.a1sf), st));
+    FP4_TRY(gemm_launch(kW1SwiGLU, *cfg, T, at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf), poff, por, w1_fp4, w1_sf,
+                        alpha1, gs2, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), nullptr, nullptr, err, at<int>(ws, kWsSchedW1), st));
+    FP4_TRY(gemm_launch(kW2Rows, *cfg, T, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), poff, por, w2_fp4, w2_sf,
+                        alpha2, nullptr, nullptr, nullptr, nullptr, at<float>(ws, L.opairs), err, at<int>(ws, kWsSchedW2), st));
+  }
+  float* o_shared = nullptr;
+  if (se != nullptr) {
+    o_shared = at<float>(ws, L.se_o);
+    FP4_TRY(shared_launch(*cfg, T, x, *se, o_shared, ws, st));
+  }
+  FP4_TRY(combine_launch(*cfg, T, at<float>(ws, L.opairs), w, cfg->ep_count > 0 ? at<int32_t>(ws, L.slot) : nullptr,
+                         o_shared, y, st));
+  const size_t pk = (size_t)T * cfg->top_k;
+  if (topk_ids_out && pk && cudaMemcpyAsync(topk_ids_out, ids, pk * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return FP4MOE_CUDA_ERROR;
+  if (topk_w_out && pk && cudaMemcpyAsync(topk_w_out, w, pk * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return FP4MOE_CUDA_ERROR;
+  return FP4MOE_OK;
+}
+}  // namespace
+
 }  // namespace fp4moe
 
 using namespace fp4moe;
 
 extern "C" {
 
-int32_t fp4moe_abi_version(void) { return 101; }
+int32_t fp4moe_abi_version(void) { return 102; }
 
 const char* fp4moe_status_string(fp4moe_status s) {
   switch (s) {
@@ -288,7 +366,7 @@ fp4moe_status moe_combine(const fp4moe_config* cfg, int32_t T, const float* o_pa
   FP4_TRY(check_T(cfg, T));
   FP4_TRY(check_ptrs(o_pairs, topk_w, y));
   if (cfg->ep_count > 0) return FP4MOE_UNSUPPORTED;  // the pairs held elsewhere are known only to moe_forward
-  return combine_launch(*cfg, T, o_pairs, topk_w, nullptr, y, (cudaStream_t)stream);
+  return combine_launch(*cfg, T, o_pairs, topk_w, nullptr, nullptr, y, (cudaStream_t)stream);
 }
 
 fp4moe_status moe_grouped_gemm_w2_combine(const fp4moe_config* cfg, int32_t T, const uint8_t* a2_fp4,
@@ -305,60 +383,77 @@ fp4moe_status moe_grouped_gemm_w2_combine(const fp4moe_config* cfg, int32_t T, c
     FP4_TRY(check_ptrs(a2_fp4, padded_offsets, pair_of_row, w2_fp4, w2_sf, topk_w, y, ws));
     FP4_TRY(mx_gemm_launch(true, *cfg, T, reinterpret_cast<const uint16_t*>(a2_fp4), padded_offsets, pair_of_row,
                            w2_fp4, w2_sf, nullptr, o, err_word(ws), (cudaStream_t)stream));
-    return combine_launch(*cfg, T, o, topk_w, nullptr, y, (cudaStream_t)stream);
+    return combine_launch(*cfg, T, o, topk_w, nullptr, nullptr, y, (cudaStream_t)stream);
   }
   FP4_TRY(check_ptrs(a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, topk_w, y, ws));
   FP4_TRY(gemm_launch(kW2Rows, *cfg, T, a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, nullptr,
                       nullptr, nullptr, nullptr, o, err_word(ws), at<int>(ws, kWsSchedW2), (cudaStream_t)stream));
-  return combine_launch(*cfg, T, o, topk_w, nullptr, y, (cudaStream_t)stream);
+  return combine_launch(*cfg, T, o, topk_w, nullptr, nullptr, y, (cudaStream_t)stream);
 }
+
 
 fp4moe_status moe_forward(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
                           const float* router_bias, const float* gs1, const float* gs2, const uint8_t* w1_fp4,
                           const uint8_t* w1_sf, const float* alpha1, const uint8_t* w2_fp4, const uint8_t* w2_sf,
                           const float* alpha2, uint16_t* y, int32_t* topk_ids_out, float* topk_w_out, void* ws,
                           fp4moe_stream_t stream) {
+  return forward_impl(cfg, T, x, router_w, router_bias, gs1, gs2, w1_fp4, w1_sf, alpha1, w2_fp4, w2_sf, alpha2,
+                      nullptr, y, topk_ids_out, topk_w_out, ws, stream);
+}
+
+fp4moe_status moe_forward_shared(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
+                                 const float* router_bias, const float* gs1, const float* gs2, const uint8_t* w1_fp4,
+                                 const uint8_t* w1_sf, const float* alpha1, const uint8_t* w2_fp4,
+                                 const uint8_t* w2_sf, const float* alpha2, const fp4moe_shared_weights* se,
+                                 uint16_t* y, int32_t* topk_ids_out, float* topk_w_out, void* ws,
+                                 fp4moe_stream_t stream) {
+  FP4_TRY(check_cfg(cfg));
+  FP4_TRY(check_shared(cfg, se));
+  return forward_impl(cfg, T, x, router_w, router_bias, gs1, gs2, w1_fp4, w1_sf, alpha1, w2_fp4, w2_sf, alpha2, se,
+                      y, topk_ids_out, topk_w_out, ws, stream);
+}
+
+fp4moe_status moe_shared_expert(const fp4moe_config* cfg, int32_t T, const uint16_t* x,
+                                const fp4moe_shared_weights* se, float* o_shared, void* ws, fp4moe_stream_t stream) {
   FP4_TRY(check_cfg(cfg));
   FP4_TRY(check_T(cfg, T));
-  const bool mx = is_mx(cfg);  // MXFP4: gs1, gs2, alpha1 and alpha2 are unused and may be NULL
-  if (mx) FP4_TRY(check_ptrs(x, router_w, w1_fp4, w1_sf, w2_fp4, w2_sf, y, ws));
-  else FP4_TRY(check_ptrs(x, router_w, gs1, gs2, w1_fp4, w1_sf, alpha1, w2_fp4, w2_sf, alpha2, y, ws));
-  FP4_TRY(check_opt(router_bias));
-  FP4_TRY(check_opt(topk_ids_out));
-  FP4_TRY(check_opt(topk_w_out));
-  const cudaStream_t st = (cudaStream_t)stream;
-  const WsLayout L = ws_layout(*cfg);
-  uint32_t* err = err_word(ws);
-  int32_t* ids = at<int32_t>(ws, L.ids);
-  float* w = at<float>(ws, L.w);
-  int32_t* poff = at<int32_t>(ws, L.poff);
-  int32_t* por = at<int32_t>(ws, L.por);
-  FP4_TRY(route_launch(*cfg, T, x, router_w, router_bias, at<float>(ws, L.logits), ids, w, at<int32_t>(ws, L.counts),
-                       at<int32_t>(ws, L.offsets), poff, at<int32_t>(ws, L.slot), por, at<int32_t>(ws, L.hist),
-                       at<float>(ws, L.nw2), err, st));
-  if (mx) {
-    uint16_t* a1 = at<uint16_t>(ws, L.a1);
-    uint16_t* a2 = at<uint16_t>(ws, L.a2);
-    FP4_TRY(scatter_rows_bf16_launch(*cfg, T, x, at<int32_t>(ws, L.slot), a1, st));
-    FP4_TRY(mx_gemm_launch(false, *cfg, T, a1, poff, por, w1_fp4, w1_sf, a2, nullptr, err, st));
-    FP4_TRY(mx_gemm_launch(true, *cfg, T, a2, poff, por, w2_fp4, w2_sf, nullptr, at<float>(ws, L.opairs), err, st));
-  } else {
-    FP4_TRY(quant_scatter_launch(*cfg, T, x, gs1, at<int32_t>(ws, L.slot), at<uint8_t>(ws, L.a1),
-                                 at<uint8_t>(ws, L.a1sf), st));
-    FP4_TRY(gemm_launch(kW1SwiGLU, *cfg, T, at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf), poff, por, w1_fp4, w1_sf,
-                        alpha1, gs2, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), nullptr, nullptr, err, at<int>(ws, kWsSchedW1), st));
-    FP4_TRY(gemm_launch(kW2Rows, *cfg, T, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), poff, por, w2_fp4, w2_sf,
-                        alpha2, nullptr, nullptr, nullptr, nullptr, at<float>(ws, L.opairs), err, at<int>(ws, kWsSchedW2), st));
-  }
-  FP4_TRY(combine_launch(*cfg, T, at<float>(ws, L.opairs), w, cfg->ep_count > 0 ? at<int32_t>(ws, L.slot) : nullptr, y,
-                         st));
-  const size_t pk = (size_t)T * cfg->top_k;
-  if (topk_ids_out && pk && cudaMemcpyAsync(topk_ids_out, ids, pk * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-    return FP4MOE_CUDA_ERROR;
-  if (topk_w_out && pk && cudaMemcpyAsync(topk_w_out, w, pk * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-    return FP4MOE_CUDA_ERROR;
+  FP4_TRY(check_shared(cfg, se));
+  FP4_TRY(check_ptrs(x, o_shared, ws));
+  return shared_launch(*cfg, T, x, *se, o_shared, ws, (cudaStream_t)stream);
+}
+
+fp4moe_status moe_combine_shared(const fp4moe_config* cfg, int32_t T, const float* o_pairs, const float* topk_w,
+                                 const int32_t* slot_of_pair, const float* o_shared, uint16_t* y,
+                                 fp4moe_stream_t stream) {
+  FP4_TRY(check_cfg(cfg));
+  FP4_TRY(check_T(cfg, T));
+  FP4_TRY(check_ptrs(o_pairs, topk_w, y));
+  FP4_TRY(check_opt(slot_of_pair));
+  FP4_TRY(check_opt(o_shared));
+  if (cfg->ep_count > 0 && slot_of_pair == nullptr) return FP4MOE_INVALID_ARG;  // which pairs are held here
+  return combine_launch(*cfg, T, o_pairs, topk_w, slot_of_pair, o_shared, y, (cudaStream_t)stream);
+}
+
+fp4moe_status fp4moe_shared_weight_bytes(const fp4moe_config* cfg, size_t* w1, size_t* w1_scales, size_t* w2,
+                                         size_t* w2_scales) {
+  FP4_TRY(check_cfg(cfg));
+  if (cfg->shared_inter <= 0) return FP4MOE_INVALID_ARG;
+  const size_t H = cfg->hidden, Is = cfg->shared_inter;
+  if (w1) *w1 = 2 * Is * H;
+  if (w1_scales) *w1_scales = (2 * Is / 128) * (H / 128) * 4;
+  if (w2) *w2 = H * Is;
+  if (w2_scales) *w2_scales = (H / 128) * (Is / 128) * 4;
   return FP4MOE_OK;
 }
+
+fp4moe_status fp4moe_shared_quantize_weights(const fp4moe_config* cfg, int32_t which, const float* w,
+                                             uint8_t* codes_out, float* scales_out, fp4moe_stream_t stream) {
+  FP4_TRY(check_cfg(cfg));
+  if (cfg->shared_inter <= 0 || (which != 1 && which != 2)) return FP4MOE_INVALID_ARG;
+  FP4_TRY(check_ptrs(w, codes_out, scales_out));
+  return se_quant_weights_launch(*cfg, which, w, codes_out, scales_out, (cudaStream_t)stream);
+}
+
 
 fp4moe_status fp4moe_quantize_weights(const fp4moe_config* cfg, int32_t which, int32_t n_experts, const float* w,
                                       uint8_t* codes_out, uint8_t* sf_out, float* gs_out, fp4moe_stream_t stream) {

@@ -1,4 +1,5 @@
-// Weighted top-k combine: y[t] = bf16( sum_{j=0..k-1} w[t,j] * o[t*k+j] ).
+// Weighted top-k combine: y[t] = bf16( sum_{j=0..k-1} w[t,j] * o[t*k+j] ), plus the shared
+// expert's row o_shared[t] (weight 1, added last) when the layer has one.
 //
 // This is the scatter_add of "Current Bug: CuTeDSLMoERunner" ("Data Flow"),
 // restated as a gather. The second GEMM stores one fp32 row per (token, k)
@@ -23,6 +24,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float* __restrict__ o,
                                                       const float* __restrict__ w,
                                                       const int32_t* __restrict__ slot_of_pair,
+                                                      const float* __restrict__ o_shared,
                                                       uint16_t* __restrict__ y) {
   pdl_wait();
   pdl_trigger();
@@ -44,6 +46,18 @@ __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float*
     acc[6] = fmaf(wj, b.z, acc[6]);
     acc[7] = fmaf(wj, b.w, acc[7]);
   }
+  if (o_shared != nullptr) {  // the shared expert, weight 1, after the routed terms
+    const float4* src = reinterpret_cast<const float4*>(o_shared + (size_t)t * H + col);
+    const float4 a = __ldcg(src), b = __ldcg(src + 1);
+    acc[0] += a.x;
+    acc[1] += a.y;
+    acc[2] += a.z;
+    acc[3] += a.w;
+    acc[4] += b.x;
+    acc[5] += b.y;
+    acc[6] += b.z;
+    acc[7] += b.w;
+  }
   *reinterpret_cast<uint4*>(y + (size_t)t * H + col) =
       make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
                  pack_bf16x2(acc[6], acc[7]));
@@ -52,11 +66,11 @@ __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float*
 }  // namespace
 
 fp4moe_status combine_launch(const fp4moe_config& cfg, int32_t T, const float* o_pairs, const float* w,
-                             const int32_t* slot_of_pair, uint16_t* y, cudaStream_t st) {
+                             const int32_t* slot_of_pair, const float* o_shared, uint16_t* y, cudaStream_t st) {
   if (T == 0) return FP4MOE_OK;
   const int H = cfg.hidden;
   return launch_pdl(combine_kernel, dim3((H / 8 + 255) / 256, T), dim3(256), 0, st, H, cfg.top_k, o_pairs, w,
-                    slot_of_pair, y) ==
+                    slot_of_pair, o_shared, y) ==
                  cudaSuccess
              ? FP4MOE_OK
              : FP4MOE_CUDA_ERROR;

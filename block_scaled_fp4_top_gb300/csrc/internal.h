@@ -32,7 +32,9 @@ inline int local_experts(const fp4moe_config& c) { return c.ep_count > 0 ? c.ep_
 
 // Byte offsets of the regions of a workspace sized for cfg.max_tokens.
 struct WsLayout {
-  size_t hist, nw2, logits, ids, w, counts, offsets, poff, slot, por, a1, a1sf, a2, a2sf, opairs, alpha_tmp, total;
+  size_t hist, nw2, logits, ids, w, counts, offsets, poff, slot, por, a1, a1sf, a2, a2sf, opairs, alpha_tmp;
+  size_t se_qx, se_sx, se_qh, se_sh, se_o;  // shared expert (cfg.shared_inter > 0)
+  size_t total;
 };
 WsLayout ws_layout(const fp4moe_config& cfg);
 
@@ -91,9 +93,18 @@ fp4moe_status mx_quant_rows_launch(int64_t n_rows, int32_t K, int32_t rows_per_g
 fp4moe_status scatter_rows_bf16_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x,
                                        const int32_t* slot_of_pair, uint16_t* a1, cudaStream_t st);
 
-// y[t] = bf16(sum_j w[t,j] o[t*k+j]); with slot_of_pair, pairs without a slot (held by no local expert) are
-// left out of the sum
+// y[t] = bf16(sum_j w[t,j] o[t*k+j] + o_shared[t]); with slot_of_pair, pairs without a slot (held by no local
+// expert) are left out of the sum; o_shared may be null
 fp4moe_status combine_launch(const fp4moe_config& cfg, int32_t T, const float* o_pairs, const float* w,
-                             const int32_t* slot_of_pair, uint16_t* y, cudaStream_t st);
+                             const int32_t* slot_of_pair, const float* o_shared, uint16_t* y, cudaStream_t st);
+
+// segemm.cu: the block-FP8 shared expert. se_tcap: rows of its activation buffers (max_tokens rounded up to
+// 128). se_forward_launch: x -> qx/sx, W1 + SwiGLU -> qh/sh, W2 -> out [T][H] fp32.
+size_t se_tcap(const fp4moe_config& cfg);
+fp4moe_status se_quant_weights_launch(const fp4moe_config& cfg, int32_t which, const float* w, uint8_t* codes,
+                                      float* scales, cudaStream_t st);
+fp4moe_status se_forward_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const uint8_t* w1,
+                                const float* s1, const uint8_t* w2, const float* s2, uint8_t* qx, float* sx,
+                                uint8_t* qh, float* sh, float* out, uint32_t* err, cudaStream_t st);
 
 }  // namespace fp4moe

@@ -170,6 +170,8 @@ typedef struct fp4moe_config {
   int32_t w_format;      /* FP4MOE_W_NVFP4 or FP4MOE_W_MXFP4 */
   int32_t ep_first;      /* expert parallelism: first expert this layer holds (global id) */
   int32_t ep_count;      /* experts it holds; 0 = all num_experts (no expert parallelism) */
+  int32_t shared_inter;  /* Is, the shared expert's kernel-local intermediate width (multiple of 128);
+                            0 = the layer has no shared expert */
 } fp4moe_config;
 
 /* Version of this ABI (major*100 + minor). */
@@ -335,6 +337,91 @@ fp4moe_status moe_forward(const fp4moe_config* cfg, int32_t T, const uint16_t* x
                           const uint8_t* w1_sf, const float* alpha1, const uint8_t* w2_fp4, const uint8_t* w2_sf,
                           const float* alpha2, uint16_t* y, int32_t* topk_ids_out, float* topk_w_out, void* ws,
                           fp4moe_stream_t stream);
+
+/* --------------------------------------------------------- shared expert --
+ * DeepSeek-V4-Flash has one shared expert of intermediate size 2048 beside
+ * the routed ones ("Lucifer-CUTLASS TP3 virtual-padding audit", "TP3 shape
+ * plan"; align_up(ceil(2048 / 3), 128) = 768 per TP3 rank, rank 2 holding 512
+ * real features and 256 zeros). Its weights and scales are block-FP8 ("Paths
+ * that already appear compatible"). It runs in the same captured step as the
+ * router and the routed MoE ("DSV4 -> vLLM: CUDA-Graph Safety", Graph B).
+ *
+ * Block-FP8, as read here (the pages name the format only; this is the FP8
+ * recipe of the DeepSeek-V3 technical report): E4M3 values with one fp32
+ * scale per 128 x 128 weight block and per 1 x 128 activation group along K.
+ * For each block or group, in IEEE fp32 with RNE:
+ *   s = amax / 448,  code_i = E4M3_satfinite(v_i / s),  and every code is 0
+ *   when s == 0.  The value of code q is q * s.
+ * The expert (every token, weight 1):
+ *   [g | u] = x~ W1~^T,  h = silu(min(g, L)) * clamp(u, -L, L),
+ *   o_shared = h~ W2~^T  (fp32 [T][H]),
+ * where x~ and h~ are x and h quantised per 1 x 128 group and dequantised,
+ * and L is cfg->swiglu_limit. The combine adds o_shared to the routed sum:
+ *   y[t] = bf16( sum_j w[t,j] * o[t*k+j] + o_shared[t] ).
+ *
+ * Weights (written by fp4moe_shared_quantize_weights, K-major, plain
+ * row-major bytes; 16-byte aligned):
+ *   w1        [2 Is][H] E4M3 in kernel row order: row block 2 j (rows
+ *             256 j .. 256 j + 127) holds gate features 128 j .. 128 j + 127 and
+ *             row block 2 j + 1 the up rows of the same features.
+ *   w1_scales [2 Is / 128][H / 128] fp32, in the same row-block order.
+ *   w2        [H][Is] E4M3.
+ *   w2_scales [H / 128][Is / 128] fp32.
+ * Under TP each rank holds its own 128-aligned slice of the features, zero
+ * past the end of the expert, and the ranks' o_shared sum to the whole.
+ * Requires cfg->shared_inter > 0 (else FP4MOE_INVALID_ARG).
+ */
+typedef struct fp4moe_shared_weights {
+  const uint8_t* w1;
+  const float* w1_scales;
+  const uint8_t* w2;
+  const float* w2_scales;
+} fp4moe_shared_weights;
+
+/* Byte sizes of the shared expert's weight buffers (any output may be NULL). */
+fp4moe_status fp4moe_shared_weight_bytes(const fp4moe_config* cfg, size_t* w1, size_t* w1_scales, size_t* w2,
+                                         size_t* w2_scales);
+
+/*
+ * fp4moe_shared_quantize_weights (load-time prep): block-FP8 of one matrix.
+ *   which = 1: w [2 Is][H] fp32, logical order (gate rows then up rows);
+ *   which = 2: w [H][Is] fp32.
+ * codes_out and scales_out get the layouts above.
+ */
+fp4moe_status fp4moe_shared_quantize_weights(const fp4moe_config* cfg, int32_t which, const float* w,
+                                             uint8_t* codes_out, float* scales_out, fp4moe_stream_t stream);
+
+/*
+ * moe_shared_expert: o_shared [T][H] fp32 for x [T][H] bf16. Three kernels:
+ * the 1 x 128 quantisation of x, W1 with the SwiGLU and the requantisation
+ * of h, and W2. Intermediates live in `ws`.
+ */
+fp4moe_status moe_shared_expert(const fp4moe_config* cfg, int32_t T, const uint16_t* x,
+                                const fp4moe_shared_weights* se, float* o_shared, void* ws, fp4moe_stream_t stream);
+
+/*
+ * moe_combine_shared: moe_combine with the shared expert's output added,
+ *   y[t] = bf16( sum_j w[t,j] * o[t*k+j] + o_shared[t] ),
+ * the shared term last. slot_of_pair may be NULL; when given, pairs with
+ * slot -1 (held by another rank) are left out, which makes it valid for
+ * expert-parallel layers. o_shared may be NULL (no shared term).
+ */
+fp4moe_status moe_combine_shared(const fp4moe_config* cfg, int32_t T, const float* o_pairs, const float* topk_w,
+                                 const int32_t* slot_of_pair, const float* o_shared, uint16_t* y,
+                                 fp4moe_stream_t stream);
+
+/*
+ * moe_forward_shared: moe_forward plus the shared expert, one stream, every
+ * intermediate inside `ws`: route, the routed experts, the shared expert,
+ * then one combine of both. Arguments are those of moe_forward plus `se`.
+ * moe_forward itself ignores cfg->shared_inter.
+ */
+fp4moe_status moe_forward_shared(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
+                                 const float* router_bias, const float* gs1, const float* gs2, const uint8_t* w1_fp4,
+                                 const uint8_t* w1_sf, const float* alpha1, const uint8_t* w2_fp4,
+                                 const uint8_t* w2_sf, const float* alpha2, const fp4moe_shared_weights* se,
+                                 uint16_t* y, int32_t* topk_ids_out, float* topk_w_out, void* ws,
+                                 fp4moe_stream_t stream);
 
 /* ------------------------------------------------------------------ prep --
  * Load-time helpers. They run outside the timed hot path and may use

@@ -46,6 +46,8 @@ TID_ROUTER = 3
 TID_W1 = 4
 TID_W2 = 5
 TID_ZIPF_PERM = 6
+TID_SE_W1 = 7
+TID_SE_W2 = 8
 
 
 def _mix64(z: np.ndarray) -> np.ndarray:
@@ -115,6 +117,7 @@ class Workload:
     zipf_dead: int = 0   # experts at the tail of the Zipf ranking that get bias -1e4
     I_logical: int = 0   # logical intermediate (MXFP4 TP shard); 0 = same as I
     w_format: int = 0    # 0 = NVFP4, 1 = MXFP4
+    shared_I: int = 0    # intermediate of the shared expert (block-FP8); 0 = none
 
     @property
     def I_log(self) -> int:
@@ -133,9 +136,12 @@ DSV4_PREFILL_ZIPF = dataclasses.replace(DSV4_DECODE, name="dsv4_flash_prefill_zi
                                         zipf_s=1.1, zipf_beta=1.0, zipf_dead=16)
 TP3_MXFP4 = dataclasses.replace(DSV4_DECODE, name="dsv4_flash_tp3_rank0_mxfp4_T512", T=512, I=768,
                                 I_logical=704, w_format=1, outlier_p=0.0, outlier_mult=1.0)
+# the layer with DeepSeek-V4-Flash's shared expert (intermediate 2048, "TP3 shape plan")
+TINY_SHARED = dataclasses.replace(TINY, name="tiny_shared", T=200, shared_I=256)
+DSV4_DECODE_SHARED = dataclasses.replace(DSV4_DECODE, name="dsv4_flash_decode_shared_T64", shared_I=2048)
 GRAPH_SWEEP_T = tuple(2**i for i in range(13))  # 1 .. 4096
 
-WORKLOADS = {w.name: w for w in (TINY, DSV4_DECODE, DSV4_PREFILL_ZIPF, TP3_MXFP4)}
+WORKLOADS = {w.name: w for w in (TINY, DSV4_DECODE, DSV4_PREFILL_ZIPF, TP3_MXFP4, TINY_SHARED, DSV4_DECODE_SHARED)}
 
 
 def activations_bf16(wl: Workload, seed: int, T: int | None = None, row0: int = 0) -> np.ndarray:
@@ -189,6 +195,18 @@ def expert_w2_f32(wl: Workload, e: int, I_full: int | None = None) -> np.ndarray
     I_full = wl.I_log if I_full is None else I_full
     n = wl.H * I_full
     return normal_f32(wl.model_seed, TID_W2, e * n, n, wl.w_sigma).reshape(wl.H, I_full)
+
+
+def shared_w1_f32(wl: Workload) -> np.ndarray:
+    """W1 of the shared expert, [2*shared_I, H] fp32: rows [0, shared_I) gate, then up."""
+    n = 2 * wl.shared_I * wl.H
+    return normal_f32(wl.model_seed, TID_SE_W1, 0, n, wl.w_sigma).reshape(2 * wl.shared_I, wl.H)
+
+
+def shared_w2_f32(wl: Workload) -> np.ndarray:
+    """W2 of the shared expert, [H, shared_I] fp32."""
+    n = wl.H * wl.shared_I
+    return normal_f32(wl.model_seed, TID_SE_W2, 0, n, wl.w_sigma).reshape(wl.H, wl.shared_I)
 
 
 def describe(wl: Workload) -> dict:

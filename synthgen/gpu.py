@@ -12,7 +12,7 @@ import os
 import numpy as np
 import torch
 
-from . import (TID_W1, TID_W2, TID_ROUTER, TID_X, TID_X_OUTLIER, Workload)
+from . import (TID_SE_W1, TID_SE_W2, TID_W1, TID_W2, TID_ROUTER, TID_X, TID_X_OUTLIER, Workload)
 from .build import LIB_PATH
 
 _lib = None
@@ -81,3 +81,14 @@ def expert_w2(wl: Workload, e0: int, n: int, out: torch.Tensor | None = None) ->
     if out is None:
         out = torch.empty(n, wl.H, wl.I_log, dtype=torch.float32, device="cuda")
     return normal_f32_(out, wl.model_seed, TID_W2, e0 * per, wl.w_sigma)
+
+
+def shared_w1(wl: Workload) -> torch.Tensor:
+    """W1 of the shared expert as fp32 [2 shared_I, H], same values as synthgen.shared_w1_f32."""
+    out = torch.empty(2 * wl.shared_I, wl.H, dtype=torch.float32, device="cuda")
+    return normal_f32_(out, wl.model_seed, TID_SE_W1, 0, wl.w_sigma)
+
+
+def shared_w2(wl: Workload) -> torch.Tensor:
+    out = torch.empty(wl.H, wl.shared_I, dtype=torch.float32, device="cuda")
+    return normal_f32_(out, wl.model_seed, TID_SE_W2, 0, wl.w_sigma)

@@ -98,4 +98,32 @@ def test_argument_checks(lib):
     assert lib.fp4moe_selftest_wait_timeout(p, 60_000_000, p, None) == _lib.INVALID_ARG  # above 50 ms
     assert lib.fp4moe_selftest_wait_timeout(ctypes.c_void_p(0x10002), 5_000_000, p, None) == _lib.MISALIGNED
     assert lib.fp4moe_status_string(_lib.CAPACITY) == b"FP4MOE_CAPACITY"
-    assert lib.fp4moe_abi_version() == 101
+    assert lib.fp4moe_abi_version() == 102
+
+
+def test_shared_expert_checks_and_sizes(lib):
+    from block_scaled_fp4_top_gb300 import _lib, api
+    p = ctypes.c_void_p(0x10000)
+    cfg = _cfg(shared_inter=2048)
+    assert api.shared_weight_bytes(cfg) == (2 * 2048 * 4096, 32 * 32 * 4, 4096 * 2048, 32 * 16 * 4)
+    tcap = 128                                            # max_tokens 64 rounded up to whole 128-row tiles
+    grow = tcap * 4096 + 32 * tcap * 4 + tcap * 2048 + 16 * tcap * 4 + 64 * 4096 * 4
+    assert api.workspace_bytes(cfg) >= api.workspace_bytes(_cfg()) + grow
+    # widths that are not whole 128 x 128 blocks, and negative widths
+    assert lib.moe_route(ctypes.byref(_cfg(shared_inter=100)), 8, *([p] * 13)) == _lib.UNSUPPORTED
+    assert lib.moe_route(ctypes.byref(_cfg(shared_inter=-128)), 8, *([p] * 13)) == _lib.INVALID_ARG
+    se = _lib.SharedWeights(0x10000, 0x10000, 0x10000, 0x10000)
+    se_bad = _lib.SharedWeights(0x10000, 0x10008, 0x10000, 0x10000)
+    se_null = _lib.SharedWeights(0x10000, None, 0x10000, 0x10000)
+    # a layer without a shared expert, a missing struct, null or misaligned members
+    assert lib.moe_shared_expert(ctypes.byref(_cfg()), 8, p, ctypes.byref(se), p, p, None) == _lib.INVALID_ARG
+    assert lib.moe_shared_expert(ctypes.byref(cfg), 8, p, None, p, p, None) == _lib.INVALID_ARG
+    assert lib.moe_shared_expert(ctypes.byref(cfg), 8, p, ctypes.byref(se_null), p, p, None) == _lib.INVALID_ARG
+    assert lib.moe_shared_expert(ctypes.byref(cfg), 8, p, ctypes.byref(se_bad), p, p, None) == _lib.MISALIGNED
+    assert lib.moe_shared_expert(ctypes.byref(cfg), 65, p, ctypes.byref(se), p, p, None) == _lib.CAPACITY
+    assert lib.moe_forward_shared(ctypes.byref(cfg), 8, *([p] * 11), None, *([p] * 5)) == _lib.INVALID_ARG
+    assert lib.fp4moe_shared_quantize_weights(ctypes.byref(cfg), 3, p, p, p, None) == _lib.INVALID_ARG
+    assert lib.fp4moe_shared_quantize_weights(ctypes.byref(_cfg()), 1, p, p, p, None) == _lib.INVALID_ARG
+    # an expert-parallel combine must be told which pairs are held here
+    ep = _cfg(ep_first=0, ep_count=64)
+    assert lib.moe_combine_shared(ctypes.byref(ep), 8, p, p, None, p, p, None) == _lib.INVALID_ARG

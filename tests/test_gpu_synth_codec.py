@@ -27,6 +27,9 @@ def test_generator_twin_matches_numpy():
     assert (torch_to_bits(sgpu.router(sg.TINY)) == sg.router_bf16(sg.TINY)).all()
     w2 = sgpu.expert_w2(wl, 255, 1)
     assert (w2.cpu().numpy()[0] == sg.expert_w2_f32(wl, 255)).all()
+    se = sg.TINY_SHARED
+    assert (sgpu.shared_w1(se).cpu().numpy().view(np.uint32) == sg.shared_w1_f32(se).view(np.uint32)).all()
+    assert (sgpu.shared_w2(se).cpu().numpy().view(np.uint32) == sg.shared_w2_f32(se).view(np.uint32)).all()
     torch.cuda.synchronize()
 
 
