@@ -5,7 +5,10 @@ Default workload: DeepSeek-V4-Flash decode, T=64 tokens, H=4096, I=2048,
 E=256, top-k 6, swiglu_limit 10. Weights are NVFP4, quantised from seeded
 synthetic N(0, 0.02) values. Activations are seeded, with 1% outliers x20.
 A step is one pass of the whole layer: route, quantise+scatter,
-W1+SwiGLU+requant, W2, combine.
+W1+SwiGLU+requant, W2, combine. Workloads with a shared expert
+(dsv4_flash_decode_shared_T64) also run its three block-FP8 kernels on a side
+stream beside the routed path (as moe_forward_shared does), and the combine
+adds its output.
 
 Prints ONE JSON line (rank 0). value = tokens/s over all ranks, with inputs
 resident in HBM; e2e = the same metric through moe_forward with pinned host
@@ -139,12 +142,15 @@ def setup_layer(wl, max_tokens):
     from synthgen import gpu as sgpu
     if wl.w_format == _lib.W_MXFP4:
         return setup_mx_layer(wl, max_tokens)
-    cfg = api.config(wl.H, wl.I, wl.E, wl.k, max_tokens, wl.swiglu_limit)
+    cfg = api.config(wl.H, wl.I, wl.E, wl.k, max_tokens, wl.swiglu_limit, shared_inter=wl.shared_I)
     layer = api.MoELayer(cfg)
     for e0 in range(0, wl.E, 16):
         n = min(16, wl.E - e0)
         layer.quantize_weights(1, e0, sgpu.expert_w1(wl, e0, n))
         layer.quantize_weights(2, e0, sgpu.expert_w2(wl, e0, n))
+    if wl.shared_I:
+        layer.quantize_shared_weights(1, sgpu.shared_w1(wl))
+        layer.quantize_shared_weights(2, sgpu.shared_w2(wl))
     bias = sg.router_bias_f32(wl)
     layer.set_router(sgpu.router(wl), None if bias is None else torch.from_numpy(bias).cuda())
     layer.calibrate(sgpu.activations(wl, sg.WARMUP_SEED))
@@ -209,12 +215,29 @@ def run_ours(args, wl, rank, world):
                 a1sf=torch.empty(16 if mx else cap * H // 16, dtype=torch.uint8, device=dev),
                 a2=torch.empty(cap * wl.I * 2 if mx else cap * wl.I // 2, dtype=torch.uint8, device=dev),
                 a2sf=torch.empty(16 if mx else cap * wl.I // 16, dtype=torch.uint8, device=dev))
+    se = wl.shared_I > 0
+    if se:   # the shared expert's fp32 output rows and the routed W2 rows, combined in one pass
+        bufs["o_shared"] = torch.empty(T, H, dtype=torch.float32, device=dev)
+        bufs["o_pairs"] = torch.empty(T * k, H, dtype=torch.float32, device=dev)
     b = bufs
     stream = torch.cuda.current_stream()
     n_stage = 5
+    if se:   # the shared expert runs beside the routed path, as moe_forward_shared runs it
+        side = torch.cuda.Stream()
+        fork_ev, join_ev = torch.cuda.Event(), torch.cuda.Event()
+        se_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_stage + 1)] for _ in range(args.steps)]
 
-    def step(e=None):
+    def step(e=None, es=None):
+        if se:
+            fork_ev.record(stream)
+            side.wait_event(fork_ev)
+            if es is not None:
+                es[0].record(side)
+            api.moe_shared_expert(cfg, T, x, layer.shared, b["o_shared"], layer.ws, stream=side)
+            if es is not None:
+                es[1].record(side)
+            join_ev.record(side)
         if e is not None:
             e[0].record(stream)
         api.moe_route(cfg, T, x, layer.router_w, layer.router_bias, b["logits"], b["ids"], b["w"], b["counts"],
@@ -228,6 +251,14 @@ def run_ours(args, wl, rank, world):
                                        layer.alpha1, layer.gs2, b["a2"], b["a2sf"], layer.ws)
         if e is not None:
             e[3].record(stream)
+        if se:
+            api.moe_grouped_gemm_w2(cfg, T, b["a2"], b["a2sf"], b["poff"], b["por"], W.w2_fp4, W.w2_sf,
+                                    layer.alpha2, b["o_pairs"], layer.ws)
+            stream.wait_event(join_ev)
+            api.moe_combine_shared(cfg, T, b["o_pairs"], b["w"], None, b["o_shared"], y)
+            if e is not None:
+                e[4].record(stream)
+            return
         api.moe_grouped_gemm_w2_combine(cfg, T, b["a2"], b["a2sf"], b["poff"], b["por"], W.w2_fp4, W.w2_sf,
                                         layer.alpha2, b["w"], y, layer.ws)
         if e is not None:
@@ -245,7 +276,7 @@ def run_ours(args, wl, rank, world):
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         for i in range(args.steps):
-            step(ev[i])
+            step(ev[i], se_ev[i] if se else None)
         t1.record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -256,6 +287,8 @@ def run_ours(args, wl, rank, world):
         raise RuntimeError(f"device error word {err:#x}")
     stage_names = ["route", "quantize_scatter", "w1_swiglu_requant", "w2_combine"]
     stage_ms = {n: float(np.mean([e[j].elapsed_time(e[j + 1]) for e in ev])) for j, n in enumerate(stage_names)}
+    if se:   # on the side stream, beside the routed stages
+        stage_ms["shared_expert"] = float(np.mean([e[0].elapsed_time(e[1]) for e in se_ev]))
 
     counts = b["counts"].cpu().numpy()
     n_active = int((counts > 0).sum())
@@ -269,6 +302,12 @@ def run_ours(args, wl, rank, world):
     else:
         act1 = T * k * (H // 2 + H // 16) + T * k * (I // 2 + I // 16)
     layer_bytes = w1_bytes + w2_bytes + E * H * 2 + 2 * T * H * 2
+    if se:
+        Is = wl.shared_I
+        # codes and block scales of both matrices; x read, its FP8 codes written and read, h codes written and
+        # read, fp32 output rows written and read back by the combine
+        se_bytes = 3 * Is * H + 3 * (Is // 128) * (H // 128) * 4 + T * H * 2 + 2 * T * H + 2 * T * Is + 2 * T * H * 4
+        layer_bytes += se_bytes
     peak, peak_kind = peaks()
     w1_ms = stage_ms["w1_swiglu_requant"]
     achieved = (w1_bytes + act1) / (w1_ms * 1e-3) / 1e9
@@ -317,11 +356,19 @@ def run_ours(args, wl, rank, world):
                      "algorithmic_bytes_per_launch": w1_bytes + act1, "traffic": w1_traffic(wl.name)},
         # route: router_mma + router_refine + layout_small (T*k <= 4096) or + hist, scan, slots;
         # then quantise-scatter, W1, W2, combine
-        "gpu_launches": ((3 if T * k <= 4096 else 5) + 4) * args.steps,
+        "gpu_launches": ((3 if T * k <= 4096 else 5) + 4 + (3 if se else 0)) * args.steps,
         "e2e": {"value": job_tokens_per_s(T, world, args.steps, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2},
         "clocks": clk.summary(),
     }
+    if se:
+        se_ms = stage_ms["shared_expert"]
+        se_gbs = se_bytes / (se_ms * 1e-3) / 1e9
+        out["shared_expert"] = {"kernels": "se_quant_x, se_gemm<W1 SwiGLU requant>, se_gemm<W2>",
+                                "stream": "a side stream beside route + routed experts, joined before the combine",
+                                "shared_inter": Is, "us": se_ms * 1e3, "algorithmic_bytes": se_bytes,
+                                "achieved_gbs": se_gbs, "frac_hbm": se_gbs / peak,
+                                "tflops": 2 * T * 3 * Is * H / (se_ms * 1e-3) / 1e12}
     return out
 
 
@@ -348,6 +395,10 @@ def oracle_sample_time(wl, n_tokens: int, repeats: int = 1):
 
     for e in np.unique(ids):   # weight prep is load time, outside the timed region
         expert(int(e))
+    shared = None
+    if wl.shared_I:
+        from oracle import fp8block
+        shared = fp8block.quantize_shared(sg.shared_w1_f32(wl), sg.shared_w2_f32(wl))
     # the timing needs plausible global scales, not calibrated ones: take gs1 from this sample's amax
     gs1 = np.float32(2688.0) / np.float32(np.abs(sg.bf16_bits_to_f32(x)).max())
     gs2 = np.float32(2688.0 / 100.0)
@@ -358,7 +409,8 @@ def oracle_sample_time(wl, n_tokens: int, repeats: int = 1):
         if mx:
             mxfp4.mx_moe_tokens(x, ids, w, expert, wl.swiglu_limit)
         else:
-            moe.moe_tokens(x, ids, w, expert, gs1, gs2, wl.swiglu_limit)
+            o_se = None if shared is None else fp8block.shared_out(x, shared, wl.swiglu_limit)
+            moe.moe_tokens(x, ids, w, expert, gs1, gs2, wl.swiglu_limit, shared=o_se)
     dt = time.perf_counter() - t0
     return n_tokens * repeats / dt, dt
 

@@ -34,6 +34,8 @@ fp4moe_status check_cfg(const fp4moe_config* c) {
     return FP4MOE_INVALID_ARG;
   if (c->shared_inter < 0) return FP4MOE_INVALID_ARG;
   if (c->shared_inter % 128 != 0) return FP4MOE_UNSUPPORTED;  // whole 128 x 128 FP8 blocks
+  if (c->shared_inter > 0 && (c->hidden > 4096 || c->shared_inter > 4096))
+    return FP4MOE_UNSUPPORTED;  // the shared GEMM keeps up to 32 K blocks of scales in shared memory
   if (c->w_format == FP4MOE_W_NVFP4) {
     if (c->inter_logical != 0 && c->inter_logical != c->inter) return FP4MOE_UNSUPPORTED;
   } else {  // MXFP4: the logical width is whole 32-element scale groups inside the kernel width
@@ -159,6 +161,34 @@ fp4moe_status route_scratch(uint8_t** out) {
 }  // namespace
 
 namespace {
+// The shared expert runs beside the routing and the routed experts: moe_forward_shared forks it onto a
+// library-owned stream and joins it back before the combine, with events. Each host thread gets its own side
+// stream and event pair per device (two threads never share an event), created on first use.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  ~SideStream() {
+    if (join) cudaEventDestroy(join);
+    if (fork) cudaEventDestroy(fork);
+    if (s) cudaStreamDestroy(s);
+  }
+};
+
+fp4moe_status side_stream(SideStream** out) {
+  thread_local SideStream per_dev[kMaxDevices];
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP4MOE_CUDA_ERROR;
+  SideStream& ss = per_dev[dev];
+  if (ss.s == nullptr) {
+    if (cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess)
+      return FP4MOE_CUDA_ERROR;
+  }
+  *out = &ss;
+  return FP4MOE_OK;
+}
+
 fp4moe_status check_shared(const fp4moe_config* cfg, const fp4moe_shared_weights* se) {
   if (cfg->shared_inter <= 0 || se == nullptr) return FP4MOE_INVALID_ARG;
   return check_ptrs(se->w1, se->w1_scales, se->w2, se->w2_scales);
@@ -193,28 +223,44 @@ fp4moe_status forward_impl(const fp4moe_config* cfg, int32_t T, const uint16_t* 
   float* w = at<float>(ws, L.w);
   int32_t* poff = at<int32_t>(ws, L.poff);
   int32_t* por = at<int32_t>(ws, L.por);
-  FP4_TRY(route_launch(*cfg, T, x, router_w, router_bias, at<float>(ws, L.logits), ids, w, at<int32_t>(ws, L.counts),
-                       at<int32_t>(ws, L.offsets), poff, at<int32_t>(ws, L.slot), por, at<int32_t>(ws, L.hist),
-                       at<float>(ws, L.nw2), err, st));
-  if (mx) {
-    uint16_t* a1 = at<uint16_t>(ws, L.a1);
-    uint16_t* a2 = at<uint16_t>(ws, L.a2);
-    FP4_TRY(scatter_rows_bf16_launch(*cfg, T, x, at<int32_t>(ws, L.slot), a1, st));
-    FP4_TRY(mx_gemm_launch(false, *cfg, T, a1, poff, por, w1_fp4, w1_sf, a2, nullptr, err, st));
-    FP4_TRY(mx_gemm_launch(true, *cfg, T, a2, poff, por, w2_fp4, w2_sf, nullptr, at<float>(ws, L.opairs), err, st));
-  } else {
+  // the shared expert needs only x: fork it off before the routing, join it back before the combine
+  float* o_shared = nullptr;
+  SideStream* side = nullptr;
+  fp4moe_status rs = FP4MOE_OK;
+  if (se != nullptr) {
+    FP4_TRY(side_stream(&side));
+    o_shared = at<float>(ws, L.se_o);
+    if (cudaEventRecord(side->fork, st) != cudaSuccess || cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess)
+      return FP4MOE_CUDA_ERROR;
+    rs = shared_launch(*cfg, T, x, *se, o_shared, ws, side->s);
+    if (cudaEventRecord(side->join, side->s) != cudaSuccess && rs == FP4MOE_OK) rs = FP4MOE_CUDA_ERROR;
+  }
+  auto routed = [&]() -> fp4moe_status {
+    FP4_TRY(route_launch(*cfg, T, x, router_w, router_bias, at<float>(ws, L.logits), ids, w,
+                         at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets), poff, at<int32_t>(ws, L.slot), por,
+                         at<int32_t>(ws, L.hist), at<float>(ws, L.nw2), err, st));
+    if (mx) {
+      uint16_t* a1 = at<uint16_t>(ws, L.a1);
+      uint16_t* a2 = at<uint16_t>(ws, L.a2);
+      FP4_TRY(scatter_rows_bf16_launch(*cfg, T, x, at<int32_t>(ws, L.slot), a1, st));
+      FP4_TRY(mx_gemm_launch(false, *cfg, T, a1, poff, por, w1_fp4, w1_sf, a2, nullptr, err, st));
+      return mx_gemm_launch(true, *cfg, T, a2, poff, por, w2_fp4, w2_sf, nullptr, at<float>(ws, L.opairs), err, st);
+    }
     FP4_TRY(quant_scatter_launch(*cfg, T, x, gs1, at<int32_t>(ws, L.slot), at<uint8_t>(ws, L.a1),
                                  at<uint8_t>(ws, L.a1sf), st));
     FP4_TRY(gemm_launch(kW1SwiGLU, *cfg, T, at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf), poff, por, w1_fp4, w1_sf,
-                        alpha1, gs2, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), nullptr, nullptr, err, at<int>(ws, kWsSchedW1), st));
-    FP4_TRY(gemm_launch(kW2Rows, *cfg, T, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), poff, por, w2_fp4, w2_sf,
-                        alpha2, nullptr, nullptr, nullptr, nullptr, at<float>(ws, L.opairs), err, at<int>(ws, kWsSchedW2), st));
-  }
-  float* o_shared = nullptr;
-  if (se != nullptr) {
-    o_shared = at<float>(ws, L.se_o);
-    FP4_TRY(shared_launch(*cfg, T, x, *se, o_shared, ws, st));
-  }
+                        alpha1, gs2, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), nullptr, nullptr, err,
+                        at<int>(ws, kWsSchedW1), st));
+    return gemm_launch(kW2Rows, *cfg, T, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), poff, por, w2_fp4, w2_sf,
+                       alpha2, nullptr, nullptr, nullptr, nullptr, at<float>(ws, L.opairs), err,
+                       at<int>(ws, kWsSchedW2), st);
+  };
+  const fp4moe_status rr = routed();
+  // the join is waited on every path, so a stream capture never ends with the side branch open
+  if (side != nullptr && cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess && rs == FP4MOE_OK)
+    rs = FP4MOE_CUDA_ERROR;
+  FP4_TRY(rr);
+  FP4_TRY(rs);
   FP4_TRY(combine_launch(*cfg, T, at<float>(ws, L.opairs), w, cfg->ep_count > 0 ? at<int32_t>(ws, L.slot) : nullptr,
                          o_shared, y, st));
   const size_t pk = (size_t)T * cfg->top_k;

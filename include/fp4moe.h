@@ -361,15 +361,17 @@ fp4moe_status moe_forward(const fp4moe_config* cfg, int32_t T, const uint16_t* x
  *
  * Weights (written by fp4moe_shared_quantize_weights, K-major, plain
  * row-major bytes; 16-byte aligned):
- *   w1        [2 Is][H] E4M3 in kernel row order: row block 2 j (rows
- *             256 j .. 256 j + 127) holds gate features 128 j .. 128 j + 127 and
- *             row block 2 j + 1 the up rows of the same features.
- *   w1_scales [2 Is / 128][H / 128] fp32, in the same row-block order.
+ *   w1        [2 Is][H] E4M3 in kernel row order: rows 128 j .. 128 j + 63
+ *             hold gate features 64 j .. 64 j + 63, and rows 128 j + 64 ..
+ *             128 j + 127 the up rows of the same features.
+ *   w1_scales [2 Is / 128][H / 128] fp32 in logical block order: rows
+ *             [0, Is / 128) are the gate blocks, the rest the up blocks.
  *   w2        [H][Is] E4M3.
  *   w2_scales [H / 128][Is / 128] fp32.
  * Under TP each rank holds its own 128-aligned slice of the features, zero
  * past the end of the expert, and the ranks' o_shared sum to the whole.
- * Requires cfg->shared_inter > 0 (else FP4MOE_INVALID_ARG).
+ * Requires cfg->shared_inter > 0 (else FP4MOE_INVALID_ARG), and H and Is
+ * at most 4096 (else FP4MOE_UNSUPPORTED).
  */
 typedef struct fp4moe_shared_weights {
   const uint8_t* w1;
@@ -411,10 +413,18 @@ fp4moe_status moe_combine_shared(const fp4moe_config* cfg, int32_t T, const floa
                                  fp4moe_stream_t stream);
 
 /*
- * moe_forward_shared: moe_forward plus the shared expert, one stream, every
- * intermediate inside `ws`: route, the routed experts, the shared expert,
- * then one combine of both. Arguments are those of moe_forward plus `se`.
- * moe_forward itself ignores cfg->shared_inter.
+ * moe_forward_shared: moe_forward plus the shared expert, every intermediate
+ * inside `ws`, then one combine of both. Arguments are those of moe_forward
+ * plus `se`. moe_forward itself ignores cfg->shared_inter.
+ * The shared expert needs only x, so it runs beside the routing and the
+ * routed experts: the call records an event on `stream`, runs the shared
+ * expert on a library-owned stream that waits for it, and makes `stream`
+ * wait for that branch before the combine. Everything stays ordered after
+ * the work already on `stream`, and the combine (and all later work on
+ * `stream`) after both branches. Under stream capture the branch joins the
+ * graph through the two events. Each host thread has its own side stream and
+ * events per device, created on its first call there: make that first call
+ * outside stream capture.
  */
 fp4moe_status moe_forward_shared(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
                                  const float* router_bias, const float* gs1, const float* gs2, const uint8_t* w1_fp4,

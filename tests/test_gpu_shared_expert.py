@@ -34,15 +34,13 @@ def _built():
     ensure_built()
 
 
-def w1_kernel_to_logical(a: np.ndarray, Is: int) -> np.ndarray:
-    """Kernel row-block order of W1 (gate block j, then up block j) back to gate rows then up rows; works on
-    code rows ([2Is, K]) and on scale rows ([2Is/128, K/128]) alike, with `Is` in the same row units."""
-    blk = a.shape[0] // (2 * Is // 128)      # rows per 128-feature block: 128 for codes, 1 for scales
-    nb = Is // 128
-    out = np.empty_like(a)
-    for j in range(nb):
-        out[j * blk:(j + 1) * blk] = a[(2 * j) * blk:(2 * j + 1) * blk]
-        out[(nb + j) * blk:(nb + j + 1) * blk] = a[(2 * j + 1) * blk:(2 * j + 2) * blk]
+def w1_kernel_to_logical(q: np.ndarray, Is: int) -> np.ndarray:
+    """W1 codes from kernel row order (gate and up interleaved per 64 features) back to gate rows then up rows."""
+    kr = np.arange(2 * Is)
+    f = (kr // 128) * 64 + kr % 64
+    logical = np.where(kr % 128 < 64, f, Is + f)
+    out = np.empty_like(q)
+    out[logical] = q
     return out
 
 
@@ -83,7 +81,7 @@ def gpu_o_shared(cfg, se, x_bits):
 def check_weights(cfg, se, w1, w2):
     Is, H = cfg.shared_inter, cfg.hidden
     q1 = w1_kernel_to_logical(se.w1.cpu().numpy().reshape(2 * Is, H), Is)
-    s1 = w1_kernel_to_logical(se.w1_scales.cpu().numpy().reshape(2 * Is // 128, H // 128), Is)
+    s1 = se.w1_scales.cpu().numpy().reshape(2 * Is // 128, H // 128)         # logical block order
     q1_ref, s1_ref = fp8block.quantize_blocks(w1)
     assert (s1.view(np.uint32) == s1_ref.view(np.uint32)).all(), f"{(s1 != s1_ref).sum()} W1 scales differ"
     assert (q1 == q1_ref).all(), f"{(q1 != q1_ref).sum()} W1 codes differ"
