@@ -142,12 +142,14 @@ def setup_layer(wl, max_tokens):
     from synthgen import gpu as sgpu
     if wl.w_format == _lib.W_MXFP4:
         return setup_mx_layer(wl, max_tokens)
-    cfg = api.config(wl.H, wl.I, wl.E, wl.k, max_tokens, wl.swiglu_limit, shared_inter=wl.shared_I)
+    cfg = api.config(wl.H, wl.I, wl.E, wl.k, max_tokens, wl.swiglu_limit, shared_inter=wl.shared_I,
+                     ep_first=wl.ep_first, ep_count=wl.ep_count)
     layer = api.MoELayer(cfg)
-    for e0 in range(0, wl.E, 16):
-        n = min(16, wl.E - e0)
-        layer.quantize_weights(1, e0, sgpu.expert_w1(wl, e0, n))
-        layer.quantize_weights(2, e0, sgpu.expert_w2(wl, e0, n))
+    n_local = wl.ep_count or wl.E   # expert parallelism: local expert l is global expert ep_first + l
+    for e0 in range(0, n_local, 16):
+        n = min(16, n_local - e0)
+        layer.quantize_weights(1, e0, sgpu.expert_w1(wl, wl.ep_first + e0, n))
+        layer.quantize_weights(2, e0, sgpu.expert_w2(wl, wl.ep_first + e0, n))
     if wl.shared_I:
         layer.quantize_shared_weights(1, sgpu.shared_w1(wl))
         layer.quantize_shared_weights(2, sgpu.shared_w2(wl))
@@ -200,6 +202,7 @@ def run_ours(args, wl, rank, world):
     torch.cuda.set_device(dev)
     cfg, layer = setup_layer(wl, wl.T)
     T, H, k, E = wl.T, wl.H, wl.k, wl.E
+    E_loc = wl.ep_count or E   # counts, offsets and padded offsets are per local expert
     mx = wl.w_format == 1
     x = sgpu.activations(wl, sg.EVAL_SEED + rank)
     y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
@@ -207,8 +210,8 @@ def run_ours(args, wl, rank, world):
     i32 = dict(dtype=torch.int32, device=dev)
     cap = api.capacity_rows(cfg, T)
     bufs = dict(logits=torch.empty(T, E, dtype=torch.float32, device=dev), ids=torch.empty(T * k, **i32),
-                w=torch.empty(T * k, dtype=torch.float32, device=dev), counts=torch.empty(E, **i32),
-                offsets=torch.empty(E, **i32), poff=torch.empty(E, **i32), slot=torch.empty(T * k, **i32),
+                w=torch.empty(T * k, dtype=torch.float32, device=dev), counts=torch.empty(E_loc, **i32),
+                offsets=torch.empty(E_loc, **i32), poff=torch.empty(E_loc, **i32), slot=torch.empty(T * k, **i32),
                 por=torch.empty(cap, **i32),
                 # slot activations: NVFP4 codes + scales, or bf16 rows for MXFP4 layers
                 a1=torch.empty(cap * H * 2 if mx else cap * H // 2, dtype=torch.uint8, device=dev),
@@ -216,8 +219,10 @@ def run_ours(args, wl, rank, world):
                 a2=torch.empty(cap * wl.I * 2 if mx else cap * wl.I // 2, dtype=torch.uint8, device=dev),
                 a2sf=torch.empty(16 if mx else cap * wl.I // 16, dtype=torch.uint8, device=dev))
     se = wl.shared_I > 0
-    if se:   # the shared expert's fp32 output rows and the routed W2 rows, combined in one pass
+    ep = wl.ep_count > 0
+    if se:   # the shared expert's fp32 output rows
         bufs["o_shared"] = torch.empty(T, H, dtype=torch.float32, device=dev)
+    if se or ep:   # the routed W2 rows, combined in a separate pass (with the slot mask under EP)
         bufs["o_pairs"] = torch.empty(T * k, H, dtype=torch.float32, device=dev)
     b = bufs
     stream = torch.cuda.current_stream()
@@ -251,11 +256,13 @@ def run_ours(args, wl, rank, world):
                                        layer.alpha1, layer.gs2, b["a2"], b["a2sf"], layer.ws)
         if e is not None:
             e[3].record(stream)
-        if se:
+        if se or ep:
             api.moe_grouped_gemm_w2(cfg, T, b["a2"], b["a2sf"], b["poff"], b["por"], W.w2_fp4, W.w2_sf,
                                     layer.alpha2, b["o_pairs"], layer.ws)
-            stream.wait_event(join_ev)
-            api.moe_combine_shared(cfg, T, b["o_pairs"], b["w"], None, b["o_shared"], y)
+            if se:
+                stream.wait_event(join_ev)
+            api.moe_combine_shared(cfg, T, b["o_pairs"], b["w"], b["slot"] if ep else None,
+                                   b["o_shared"] if se else None, y)
             if e is not None:
                 e[4].record(stream)
             return
@@ -337,6 +344,28 @@ def run_ours(args, wl, rank, world):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     assert layer.read_error() == 0
 
+    # ---------------- the per-batch activation scale (fp4moe_batch_gs1), timed alone: one launch per call
+    bgs = None
+    if not mx:
+        gs1_keep, a1_keep = layer.gs1.clone(), layer.alpha1.clone()
+        for _ in range(3):
+            layer.batch_gs1(x)
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        reps = 50
+        g0.record(stream)
+        for _ in range(reps):
+            layer.batch_gs1(x)
+        g1.record(stream)
+        torch.cuda.synchronize()
+        layer.gs1.copy_(gs1_keep)
+        layer.alpha1.copy_(a1_keep)
+        bgs_us = g0.elapsed_time(g1) * 1e3 / reps
+        bgs_bytes = T * H * 2 + E_loc * 8   # x read once; the weight scales read and alpha written
+        bgs = {"us": bgs_us, "algorithmic_bytes": bgs_bytes, "achieved_gbs": bgs_bytes / (bgs_us * 1e-6) / 1e9,
+               "launches": 1}
+    assert layer.read_error() == 0
+
     out = {
         "metric": METRIC, "value": job_tokens_per_s(T, world, args.steps, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
@@ -360,7 +389,11 @@ def run_ours(args, wl, rank, world):
         "e2e": {"value": job_tokens_per_s(T, world, args.steps, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2},
         "clocks": clk.summary(),
+        "batch_gs1": bgs,
     }
+    if ep:
+        out["config"]["expert_parallel"] = {"ep_first": wl.ep_first, "ep_count": wl.ep_count,
+                                            "note": "one rank's share: routing over all experts, GEMMs over the local ones"}
     if se:
         se_ms = stage_ms["shared_expert"]
         se_gbs = se_bytes / (se_ms * 1e-3) / 1e9
@@ -394,7 +427,8 @@ def oracle_sample_time(wl, n_tokens: int, repeats: int = 1):
         return cache[e]
 
     for e in np.unique(ids):   # weight prep is load time, outside the timed region
-        expert(int(e))
+        if not wl.ep_count or wl.ep_first <= e < wl.ep_first + wl.ep_count:
+            expert(int(e))
     shared = None
     if wl.shared_I:
         from oracle import fp8block
@@ -410,7 +444,12 @@ def oracle_sample_time(wl, n_tokens: int, repeats: int = 1):
             mxfp4.mx_moe_tokens(x, ids, w, expert, wl.swiglu_limit)
         else:
             o_se = None if shared is None else fp8block.shared_out(x, shared, wl.swiglu_limit)
-            moe.moe_tokens(x, ids, w, expert, gs1, gs2, wl.swiglu_limit, shared=o_se)
+            if wl.ep_count:   # one rank's share: local ids, pairs held elsewhere masked
+                from oracle import layout
+                moe.moe_tokens(x, layout.local_ids(ids, wl.ep_first, wl.ep_count), w,
+                               lambda l: expert(wl.ep_first + l), gs1, gs2, wl.swiglu_limit, shared=o_se)
+            else:
+                moe.moe_tokens(x, ids, w, expert, gs1, gs2, wl.swiglu_limit, shared=o_se)
     dt = time.perf_counter() - t0
     return n_tokens * repeats / dt, dt
 

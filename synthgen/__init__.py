@@ -118,6 +118,8 @@ class Workload:
     I_logical: int = 0   # logical intermediate (MXFP4 TP shard); 0 = same as I
     w_format: int = 0    # 0 = NVFP4, 1 = MXFP4
     shared_I: int = 0    # intermediate of the shared expert (block-FP8); 0 = none
+    ep_first: int = 0    # expert parallelism: the layer holds experts [ep_first, ep_first + ep_count)
+    ep_count: int = 0    # 0 = all experts
 
     @property
     def I_log(self) -> int:
@@ -139,9 +141,12 @@ TP3_MXFP4 = dataclasses.replace(DSV4_DECODE, name="dsv4_flash_tp3_rank0_mxfp4_T5
 # the layer with DeepSeek-V4-Flash's shared expert (intermediate 2048, "TP3 shape plan")
 TINY_SHARED = dataclasses.replace(TINY, name="tiny_shared", T=200, shared_I=256)
 DSV4_DECODE_SHARED = dataclasses.replace(DSV4_DECODE, name="dsv4_flash_decode_shared_T64", shared_I=2048)
+# one rank's share under expert parallelism: 48 of the 256 experts ("EP Configuration")
+DSV4_DECODE_EP48 = dataclasses.replace(DSV4_DECODE, name="dsv4_flash_decode_ep48_T64", ep_first=96, ep_count=48)
 GRAPH_SWEEP_T = tuple(2**i for i in range(13))  # 1 .. 4096
 
-WORKLOADS = {w.name: w for w in (TINY, DSV4_DECODE, DSV4_PREFILL_ZIPF, TP3_MXFP4, TINY_SHARED, DSV4_DECODE_SHARED)}
+WORKLOADS = {w.name: w for w in (TINY, DSV4_DECODE, DSV4_PREFILL_ZIPF, TP3_MXFP4, TINY_SHARED, DSV4_DECODE_SHARED,
+                                 DSV4_DECODE_EP48)}
 
 
 def activations_bf16(wl: Workload, seed: int, T: int | None = None, row0: int = 0) -> np.ndarray:
