@@ -32,14 +32,17 @@
 //               are also pulled into L2 a few stages ahead
 //               (cp.async.bulk.prefetch.L2). The shared-memory ring runs on
 //               across tile boundaries, so the weight stream never stops.
-//   warp 5      MMA issuer. tcgen05.cp costs about the same per instruction
-//               whatever its size, and it sits on this thread's critical path.
-//               So the resident scales are copied into TMEM only once, for
-//               the whole of K, and stay there while the operand is fixed.
-//               Each stage then copies only its 8 streamed scale tiles. Then
+//   warp 6      scale copier. tcgen05.cp costs about the same per instruction
+//               whatever its size, and holds its issuing thread. So the
+//               resident scales are copied into TMEM only once, for the whole
+//               of K, and stay there while the operand is fixed. Each stage
+//               then copies only its 8 streamed scale tiles, and commits them
+//               to a per-stage barrier.
+//   warp 5      MMA issuer. Once a stage's operands and scales are in place,
 //               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (K = 64
 //               each) accumulates in fp32 in TMEM, and tcgen05.commit frees the
-//               ring slot and then hands the accumulator to the epilogue.
+//               ring slot and then hands the accumulator to the epilogue. The
+//               copier works on the next stage meanwhile.
 //   warps 0-3   epilogue. tcgen05.ld gives one accumulator row per thread. It
 //               moves all 128 columns to registers, frees the accumulator for
 //               the next tile's MMAs, then computes. Padding rows are skipped
@@ -78,7 +81,7 @@ constexpr int STR_OFF = RES_OFF + ATOMS * SF_TILE;      // scale tiles of the st
 constexpr int STAGE_BYTES = STR_OFF + ATOMS * SF_TILE;  // 73728, a multiple of 1024
 constexpr int BAR_OFF = STAGES * STAGE_BYTES;
 constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;    // barriers + 1024-byte alignment slack
-constexpr int THREADS = 192;
+constexpr int THREADS = 224;  // 4 epilogue warps, producer, MMA issuer, scale copier
 constexpr int PREFETCH = 6;         // ring stages pulled into L2 ahead of the ring
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 128;  // one accumulator: 128 fp32 columns
@@ -165,7 +168,7 @@ __device__ __forceinline__ Chunk decode_chunk(int c, const int* s_cstart, const 
 // order (static schedule), or the chunks it takes from the global counter (dynamic schedule). In the dynamic
 // schedule the producer takes a chunk and hands its id to the MMA issuer and the epilogue warps through a
 // small shared-memory ring; every role then walks the same tiles in the same order.
-enum SourceRole { kRoleProducer = 0, kRoleMma = 1, kRoleEpilogue = 2 };
+enum SourceRole { kRoleProducer = 0, kRoleMma = 1, kRoleEpilogue = 2, kRoleCopier = 3 };
 
 template <int ROLE>
 struct TileSource {
@@ -214,7 +217,7 @@ struct TileSource {
         if (c >= n_chunks) c = -1;
         s_sched[q] = c;
         mbar_arrive(bar_sfull + 8 * q);
-      } else if constexpr (ROLE == kRoleMma) {
+      } else if constexpr (ROLE == kRoleMma || ROLE == kRoleCopier) {
         if (!mbar_wait(bar_sfull + 8 * q, qph, prm.err)) {
           done = true;
           return false;
@@ -296,6 +299,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t bar_drain = bar_tempty + 16;
   const uint32_t bar_sfull = bar_drain + 8;            // kSchedSlots x 8 bytes: a chunk id was written
   const uint32_t bar_sempty = bar_sfull + 8 * kSchedSlots;  // kSchedSlots x 8 bytes: it was read
+  const uint32_t bar_sready = bar_sempty + 8 * kSchedSlots;  // STAGES x 8 bytes: the stage's scales are in TMEM
+  const uint32_t bar_cdrain = bar_sready + 8 * STAGES;       // the copier's last copies completed
 
   for (int e = threadIdx.x; e < E; e += THREADS) s_poff[e] = __ldcg(prm.poff + e);
   if (prm.dyn) {
@@ -335,8 +340,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(bar_drain, 1);
     for (int q = 0; q < kSchedSlots; ++q) {
       mbar_init(bar_sfull + 8 * q, 1);
-      mbar_init(bar_sempty + 8 * q, 1 + 4);  // the MMA issuer and the four epilogue warps
+      mbar_init(bar_sempty + 8 * q, 1 + 1 + 4);  // the MMA issuer, the scale copier and the four epilogue warps
     }
+    for (int s = 0; s < STAGES; ++s) mbar_init(bar_sready + 8 * s, 1);  // the copier's commit
+    mbar_init(bar_cdrain, 1);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -431,13 +438,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int j = max(0, it - STAGES); j < it; ++j) drain_wait(bar_full + 8 * (j % STAGES), (uint32_t)(j / STAGES) & 1u);
   } else if (warp == 5 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    // This single thread is the throughput limit of the kernel: every instruction here runs at full
-    // latency. So the per-stage work is one wait, 8 (+8 for a new fixed operand) scale copies, 8 MMAs
-    // and one commit, fully unrolled, and stage and phase are counters. Every shared-memory descriptor is
-    // built from its full byte address: the 14-bit address field wraps with the shared window, so
-    // adding offsets to an already-masked descriptor could carry into the reserved bits.
+    // This thread and the scale copier (warp 6) share the per-stage tensor-core instruction stream: every
+    // tcgen05 instruction holds its issuing thread for about the same time, so the copier issues the stage's
+    // scale copies (and commits them to bar_sready) while this thread issues the MMAs of the stage before.
+    // Every shared-memory descriptor is built from its full byte address: the 14-bit address field wraps
+    // with the shared window, so adding offsets to an already-masked descriptor could carry into the
+    // reserved bits.
     constexpr uint32_t idesc = idesc_nvf4(BM, BN);
-    int tl = 0, prev_key = INT_MIN;
+    int tl = 0;
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -447,9 +455,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (; ok && src.next(t, prm, tau0, s_poff, s_cstart, s_sched, bar_sfull, bar_sempty, n_chunks, E, NT, r128);
          ++tl) {
       const bool res_a = (t.me == 1);
-      const int key = res_a ? t.mt : -1 - (t.e * NT + t.nt);
-      const bool new_res = (key != prev_key);
-      prev_key = key;
       const int b = tl % nacc;
       const uint32_t use = (uint32_t)(tl / nacc);
       // the epilogue has drained this accumulator buffer
@@ -457,22 +462,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         ok = false;
         break;
       }
-      // before new scales overwrite the resident ones, every earlier MMA must be complete: with one buffer
-      // the wait above implies it; with two, also wait until the other buffer's last tile was drained
-      if (new_res && nacc == 2 && tl > 0 &&
-          !mbar_wait(bar_tempty + 8 * (b ^ 1), ((uint32_t)((tl - 1) / 2) & 1u), prm.err)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
       const uint32_t acc = tmem + ACC_COLS * b;
       for (int kb = 0; kb < KB; ++kb) {
-        if (!mbar_wait(bar_full + 8 * s, ph, prm.err)) {
+        // the operands are in shared memory and the copier's scale copies for this stage have completed
+        if (!mbar_wait(bar_full + 8 * s, ph, prm.err) || !mbar_wait(bar_sready + 8 * s, ph, prm.err)) {
           ok = false;
           break;
         }
-        // order the tensor-core reads of this stage after the mbarrier wait that made the TMA
-        // writes visible (without it MMAs can read stale shared memory)
+        // order the tensor-core reads of this stage after the waits that made the TMA writes and the
+        // scale copies visible (without it MMAs can read stale shared memory)
         tc_fence_after();
         const uint32_t st = smem + (uint32_t)s * STAGE_BYTES;
         const uint32_t res_t = tmem + res_col + 4u * ATOMS * kb;
@@ -480,13 +478,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t sfa_t = res_a ? res_t : str_t;  // TMEM scales of A and of B for this stage
         const uint32_t sfb_t = res_a ? str_t : res_t;
         const uint32_t acc0 = kb > 0 ? 1u : 0u;
-        if (kb * ATOMS + ATOMS <= katoms_total) {  // a full stage: 8 scale atoms, 8 MMAs
-          if (new_res) {
-#pragma unroll
-            for (int a = 0; a < ATOMS; ++a) tc_cp_scales(res_t + 4 * a, desc_scales(st + RES_OFF + a * SF_TILE));
-          }
-#pragma unroll
-          for (int a = 0; a < ATOMS; ++a) tc_cp_scales(str_t + 4 * a, desc_scales(st + STR_OFF + a * SF_TILE));
+        if (kb * ATOMS + ATOMS <= katoms_total) {  // a full stage: 8 MMAs
 #pragma unroll
           for (int a = 0; a < ATOMS; ++a) {
             const uint32_t ko = (a >> 2) * HALF_BYTES + (a & 3) * 32;  // K offset inside the stage
@@ -495,10 +487,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         } else {  // the partial last stage of a K that is not a multiple of 512
           const int atoms = katoms_total - kb * ATOMS;
-          for (int a = 0; a < atoms; ++a) {
-            if (new_res) tc_cp_scales(res_t + 4 * a, desc_scales(st + RES_OFF + a * SF_TILE));
-            tc_cp_scales(str_t + 4 * a, desc_scales(st + STR_OFF + a * SF_TILE));
-          }
           for (int a = 0; a < atoms; ++a) {
             const uint32_t ko = (a >> 2) * HALF_BYTES + (a & 3) * 32;
             tc_mma_nvf4(acc, desc_sw128(st + ko), desc_sw128(st + A_BYTES + ko), idesc, sfa_t + 4 * a,
@@ -516,6 +504,66 @@ __global__ void __launch_bounds__(THREADS, 1)
     // no MMA may still write TMEM when it is freed
     tc_commit(bar_drain);
     drain_wait(bar_drain, 0);
+  } else if (warp == 6 && lane == 0) {
+    // ------------------------------------------------------------ scale copier
+    // Per stage: the 8 streamed scale tiles (and, for a new fixed operand, its 8 resident ones) from the
+    // stage's shared memory into TMEM, then one commit to bar_sready. TMEM slot s of the streamed scales
+    // is free again once stage s is full: the producer refilled it only after the MMAs of its previous use
+    // committed bar_empty. Resident scales are overwritten only after every MMA of the previous tile has
+    // completed (its bar_tfull commit).
+    int tl = 0, prev_key = INT_MIN;
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    TileSource<kRoleCopier> src;
+    src.init(prm, tau0, tau1, s_poff, E, NT, r128);
+    Tile t;
+    for (; ok && src.next(t, prm, tau0, s_poff, s_cstart, s_sched, bar_sfull, bar_sempty, n_chunks, E, NT, r128);
+         ++tl) {
+      const bool res_a = (t.me == 1);
+      const int key = res_a ? t.mt : -1 - (t.e * NT + t.nt);
+      const bool new_res = (key != prev_key);
+      prev_key = key;
+      if (new_res && tl > 0) {
+        const int pb = (tl - 1) % nacc;
+        if (!mbar_wait(bar_tfull + 8 * pb, (uint32_t)((tl - 1) / nacc) & 1u, prm.err)) {
+          ok = false;
+          break;
+        }
+      }
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(bar_full + 8 * s, ph, prm.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t st = smem + (uint32_t)s * STAGE_BYTES;
+        const uint32_t res_t = tmem + res_col + 4u * ATOMS * kb;
+        const uint32_t str_t = tmem + str_col + SFB_STAGE_COLS * s;
+        if (kb * ATOMS + ATOMS <= katoms_total) {  // a full stage: 8 scale atoms
+          if (new_res) {
+#pragma unroll
+            for (int a = 0; a < ATOMS; ++a) tc_cp_scales(res_t + 4 * a, desc_scales(st + RES_OFF + a * SF_TILE));
+          }
+#pragma unroll
+          for (int a = 0; a < ATOMS; ++a) tc_cp_scales(str_t + 4 * a, desc_scales(st + STR_OFF + a * SF_TILE));
+        } else {  // the partial last stage of a K that is not a multiple of 512
+          const int atoms = katoms_total - kb * ATOMS;
+          for (int a = 0; a < atoms; ++a) {
+            if (new_res) tc_cp_scales(res_t + 4 * a, desc_scales(st + RES_OFF + a * SF_TILE));
+            tc_cp_scales(str_t + 4 * a, desc_scales(st + STR_OFF + a * SF_TILE));
+          }
+        }
+        tc_commit(bar_sready + 8 * s);
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    // no copy may still write TMEM when it is freed
+    tc_commit(bar_cdrain);
+    drain_wait(bar_cdrain, 0);
   } else if (warp < 4) {
     // ------------------------------------------------------------ epilogue
     int tl = 0;
