@@ -207,6 +207,15 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+// 32 bytes to a 32-byte-aligned global address in one 256-bit store (sm_100 and later), so a thread writing a
+// row fills whole L2 sectors; the line is not allocated in L1.
+__device__ __forceinline__ void st_global_v8(float* p, float a, float b, float c, float d, float e, float f, float g,
+                                             float h) {
+  asm volatile("st.global.L1::no_allocate.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(a), "f"(b),
+               "f"(c), "f"(d), "f"(e), "f"(f), "f"(g), "f"(h)
+               : "memory");
+}
+
 // ----------------------------------------------------------- PTX: tcgen05 --
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)

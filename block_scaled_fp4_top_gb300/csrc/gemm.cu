@@ -109,6 +109,7 @@ struct Params {
   float* amax;
   float* o_pairs;
   uint32_t* err;
+  int o_pairs32;  // W2: o_pairs is 32-byte aligned (every row is then, H being a multiple of 256)
   int dyn;     // 1: dynamic chunk schedule (large T); 0: contiguous static ranges (decode sizes)
   int* sched;  // dynamic schedule: next-chunk counter, zero at launch
 };
@@ -572,13 +573,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     Tile t;
     for (; src.next(t, prm, tau0, s_poff, s_cstart, s_sched, bar_sfull, bar_sempty, n_chunks, E, NT, r128); ++tl) {
       const int r = t.mt * BM + warp * 32 + lane;
+      // the row's pair and the expert's alpha are loaded before the accumulator wait, which hides them
       const int p = __ldcg(prm.pair_of_row + r);
-      const bool any_real = __any_sync(0xFFFFFFFFu, p >= 0);
+      const float alpha = __ldg(prm.alpha + t.e);
       const int b = tl % nacc;
       const uint32_t use = (uint32_t)(tl / nacc);
       // the whole warp takes one decision: tcgen05.ld is warp-collective
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_tfull + 8 * b, use & 1u, prm.err) ? 1 : 0)) break;
       tc_fence_after();
+      const bool any_real = __any_sync(0xFFFFFFFFu, p >= 0);
       const uint32_t tacc = tmem + ACC_COLS * b + ((uint32_t)(warp * 32) << 16);
       float v[128];
       if (any_real) {
@@ -595,13 +598,23 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_tempty + 8 * b);  // the accumulator is free for the next tile
       if (p < 0) continue;                     // padding rows carry nothing ("Bug 14")
-      const float alpha = __ldg(prm.alpha + t.e);
       if constexpr (MODE == kW2Rows) {
-        float4* d4 = reinterpret_cast<float4*>(prm.o_pairs + (size_t)p * prm.H + t.nt * BN);
+        float* d = prm.o_pairs + (size_t)p * prm.H + t.nt * BN;
+        if (prm.o_pairs32) {
+          // the thread's row in 32-byte stores: whole L2 sectors, half the write transactions of 16-byte ones
 #pragma unroll
-        for (int q = 0; q < 32; ++q)
-          d4[q] = make_float4(__fmul_rn(v[4 * q], alpha), __fmul_rn(v[4 * q + 1], alpha),
-                              __fmul_rn(v[4 * q + 2], alpha), __fmul_rn(v[4 * q + 3], alpha));
+          for (int q = 0; q < 16; ++q)
+            st_global_v8(d + 8 * q, __fmul_rn(v[8 * q], alpha), __fmul_rn(v[8 * q + 1], alpha),
+                         __fmul_rn(v[8 * q + 2], alpha), __fmul_rn(v[8 * q + 3], alpha), __fmul_rn(v[8 * q + 4], alpha),
+                         __fmul_rn(v[8 * q + 5], alpha), __fmul_rn(v[8 * q + 6], alpha),
+                         __fmul_rn(v[8 * q + 7], alpha));
+        } else {  // a caller's buffer aligned to 16 bytes only
+          float4* d4 = reinterpret_cast<float4*>(d);
+#pragma unroll
+          for (int q = 0; q < 32; ++q)
+            d4[q] = make_float4(__fmul_rn(v[4 * q], alpha), __fmul_rn(v[4 * q + 1], alpha),
+                                __fmul_rn(v[4 * q + 2], alpha), __fmul_rn(v[4 * q + 3], alpha));
+        }
       } else {
         // columns [0, 64): gate of features 64 nt .. 64 nt + 63; columns [64, 128): up of the same features
         const float L = prm.limit;
@@ -740,6 +753,7 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
   prm.out_sf = out_sf;
   prm.amax = amax;
   prm.o_pairs = o_pairs;
+  prm.o_pairs32 = (reinterpret_cast<uintptr_t>(o_pairs) & 31u) == 0 ? 1 : 0;
   prm.err = err;
   // the dynamic chunk schedule pays off once experts average a whole m-tile (prefill sizes)
   prm.dyn = ((int64_t)T * cfg.top_k >= (int64_t)local_experts(cfg) * BM) ? 1 : 0;

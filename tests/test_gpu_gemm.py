@@ -112,6 +112,24 @@ def test_w2_rows_against_fp64(H, I, counts):
     assert ok.all(), f"max err/bound {(err / np.maximum(bound, 1e-30)).max():.3e}"
 
 
+def test_w2_rows_to_a_16_byte_aligned_buffer():
+    """A caller's o_pairs aligned to 16 bytes only gets the same rows, bit for bit, as a 32-byte-aligned one."""
+    import torch
+    from block_scaled_fp4_top_gb300 import api
+    H, I, counts = 256, 128, [3, 0, 140]
+    cfg, T, cap, ids, L, _, t = _setup(H, I, counts, 1, which=2)
+    o = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+    api.moe_grouped_gemm_w2(cfg, T, t["a"], t["asf"], t["poff"], t["por"], t["w"], t["wsf"], t["alpha"], o, t["ws"])
+    big = torch.full((T * H + 8,), float("nan"), dtype=torch.float32, device="cuda")
+    o16 = big[4:4 + T * H].view(T, H)
+    assert o16.data_ptr() % 32 == 16
+    api.moe_grouped_gemm_w2(cfg, T, t["a"], t["asf"], t["poff"], t["por"], t["w"], t["wsf"], t["alpha"], o16,
+                            t["ws"])
+    torch.cuda.synchronize()
+    assert api.fp4moe_read_error(t["ws"]) == 0
+    assert torch.equal(o.view(torch.int32), o16.view(torch.int32))
+
+
 @pytest.mark.parametrize("H,I,counts", [(256, 128, [3, 0, 140]), (512, 256, [1, 257, 2]),
                                         (256, 128, [600, 5, 130])])   # the last one takes the dynamic schedule
 def test_w1_swiglu_requant(H, I, counts):
