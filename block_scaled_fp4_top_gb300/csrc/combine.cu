@@ -21,6 +21,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return l | (h << 16);
 }
 
+// Eight fp32 values through L2: one 256-bit load (sm_100 and later) when the address is 32-byte aligned.
+template <bool V8>
+__device__ __forceinline__ void ld8_cg(const float* p, float (&v)[8]) {
+  if constexpr (V8) {
+    asm volatile("ld.global.cg.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
+                 : "l"(p)
+                 : "memory");
+  } else {
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(p)), b = __ldcg(reinterpret_cast<const float4*>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+}
+
+template <bool V8>
 __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float* __restrict__ o,
                                                       const float* __restrict__ w,
                                                       const int32_t* __restrict__ slot_of_pair,
@@ -35,28 +51,16 @@ __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float*
   for (int j = 0; j < k; ++j) {
     if (slot_of_pair != nullptr && __ldcg(slot_of_pair + (size_t)t * k + j) < 0) continue;  // not held here
     const float wj = __ldcg(w + (size_t)t * k + j);
-    const float4* src = reinterpret_cast<const float4*>(o + ((size_t)t * k + j) * H + col);
-    const float4 a = __ldcg(src), b = __ldcg(src + 1);
-    acc[0] = fmaf(wj, a.x, acc[0]);
-    acc[1] = fmaf(wj, a.y, acc[1]);
-    acc[2] = fmaf(wj, a.z, acc[2]);
-    acc[3] = fmaf(wj, a.w, acc[3]);
-    acc[4] = fmaf(wj, b.x, acc[4]);
-    acc[5] = fmaf(wj, b.y, acc[5]);
-    acc[6] = fmaf(wj, b.z, acc[6]);
-    acc[7] = fmaf(wj, b.w, acc[7]);
+    float v[8];
+    ld8_cg<V8>(o + ((size_t)t * k + j) * H + col, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
   }
   if (o_shared != nullptr) {  // the shared expert, weight 1, after the routed terms
-    const float4* src = reinterpret_cast<const float4*>(o_shared + (size_t)t * H + col);
-    const float4 a = __ldcg(src), b = __ldcg(src + 1);
-    acc[0] += a.x;
-    acc[1] += a.y;
-    acc[2] += a.z;
-    acc[3] += a.w;
-    acc[4] += b.x;
-    acc[5] += b.y;
-    acc[6] += b.z;
-    acc[7] += b.w;
+    float v[8];
+    ld8_cg<V8>(o_shared + (size_t)t * H + col, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += v[i];
   }
   *reinterpret_cast<uint4*>(y + (size_t)t * H + col) =
       make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
@@ -69,8 +73,12 @@ fp4moe_status combine_launch(const fp4moe_config& cfg, int32_t T, const float* o
                              const int32_t* slot_of_pair, const float* o_shared, uint16_t* y, cudaStream_t st) {
   if (T == 0) return FP4MOE_OK;
   const int H = cfg.hidden;
-  return launch_pdl(combine_kernel, dim3((H / 8 + 255) / 256, T), dim3(256), 0, st, H, cfg.top_k, o_pairs, w,
-                    slot_of_pair, o_shared, y) ==
+  // 256-bit loads when every row start is 32-byte aligned (H is a multiple of 256)
+  const bool v8 = ((reinterpret_cast<uintptr_t>(o_pairs) | reinterpret_cast<uintptr_t>(o_shared)) & 31u) == 0;
+  return (v8 ? launch_pdl(combine_kernel<true>, dim3((H / 8 + 255) / 256, T), dim3(256), 0, st, H, cfg.top_k, o_pairs,
+                          w, slot_of_pair, o_shared, y)
+             : launch_pdl(combine_kernel<false>, dim3((H / 8 + 255) / 256, T), dim3(256), 0, st, H, cfg.top_k,
+                          o_pairs, w, slot_of_pair, o_shared, y)) ==
                  cudaSuccess
              ? FP4MOE_OK
              : FP4MOE_CUDA_ERROR;

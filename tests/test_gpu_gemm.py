@@ -173,3 +173,28 @@ def test_w1_swiglu_requant(H, I, counts):
     rel = np.linalg.norm(got_deq[real] - ref_deq[real]) / np.linalg.norm(ref_deq[real])
     assert rel < 2e-2, rel
     assert (sf[real] == s_ref[real]).mean() >= 0.99
+
+
+def test_combine_reads_16_byte_aligned_rows_the_same():
+    """moe_combine gives the same y, bit for bit, for pair rows in a 32-byte- and a 16-byte-aligned buffer; and
+    matches the weighted sum y = bf16(sum_j w_j o_j) computed in fp64 within one bf16 rounding."""
+    import torch
+    from block_scaled_fp4_top_gb300 import api
+    T, H, k = 37, 512, 6
+    cfg = api.config(H, 128, 8, k, T, 10.0)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    o = torch.randn(T * k, H, device="cuda", generator=g)
+    w = torch.rand(T * k, device="cuda", generator=g)
+    y = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    api.moe_combine(cfg, T, o, w, y)
+    big = torch.empty(T * k * H + 8, device="cuda")
+    o16 = big[4:4 + T * k * H].view(T * k, H)
+    o16.copy_(o)
+    assert o16.data_ptr() % 32 == 16
+    y16 = torch.empty_like(y)
+    api.moe_combine(cfg, T, o16, w, y16)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y16.view(torch.int16))
+    ref = (w.double().view(T, k, 1) * o.double().view(T, k, H)).sum(1)
+    err = (y.double() - ref).abs()
+    assert (err <= ref.abs() * 2.0 ** -8 + 1e-6).all()
