@@ -488,48 +488,64 @@ __device__ __forceinline__ void warp_argmax(const float (&v)[MAXV], uint32_t eli
 }
 
 // The compensated dot product of warp_exact_dot, with the token row read from global memory (it stays in
-// L1 across the candidates of a token) in batches of 4 chunks per lane.
+// L1 across the candidates of a token). Lane l takes chunks l, l + 32, ... in batches of 2 per lane, the
+// next batch's loads in flight while the current one is summed, into four independent compensated pairs
+// (more independent dependency chains per lane), which two-sums merge at the end.
+__device__ __forceinline__ void acc_chunk(float (&s)[4], float (&c)[4], const uint4& xv, const uint4& wv) {
+  acc_prod(s[0], c[0], bf16_lo(xv.x), bf16_lo(wv.x));
+  acc_prod(s[1], c[1], bf16_hi(xv.x), bf16_hi(wv.x));
+  acc_prod(s[2], c[2], bf16_lo(xv.y), bf16_lo(wv.y));
+  acc_prod(s[3], c[3], bf16_hi(xv.y), bf16_hi(wv.y));
+  acc_prod(s[0], c[0], bf16_lo(xv.z), bf16_lo(wv.z));
+  acc_prod(s[1], c[1], bf16_hi(xv.z), bf16_hi(wv.z));
+  acc_prod(s[2], c[2], bf16_lo(xv.w), bf16_lo(wv.w));
+  acc_prod(s[3], c[3], bf16_hi(xv.w), bf16_hi(wv.w));
+}
+
 __device__ __noinline__ float warp_exact_dot_global(const uint4* __restrict__ xr, const uint4* __restrict__ wrow,
                                                    int nchunks) {
   const int lane = threadIdx.x & 31;
-  float s0 = 0.0f, c0 = 0.0f, s1 = 0.0f, c1 = 0.0f;
-  for (int base = 0; base < nchunks; base += 32 * 4) {
-    uint4 xv[4], wv[4];
+  constexpr int B = 2;  // chunks per lane per batch
+  float s[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  uint4 xv[B], wv[B];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int ch = base + lane + 32 * j;
-      if (ch < nchunks) {
-        xv[j] = __ldg(xr + ch);
-        wv[j] = __ldg(wrow + ch);
-      }
+  for (int j = 0; j < B; ++j) {
+    const int ch = lane + 32 * j;
+    xv[j] = ch < nchunks ? __ldg(xr + ch) : zero;
+    wv[j] = ch < nchunks ? __ldg(wrow + ch) : zero;
+  }
+  for (int base = 0; base < nchunks; base += 32 * B) {
+    uint4 xn[B], wn[B];
+#pragma unroll
+    for (int j = 0; j < B; ++j) {  // the next batch (zero past the row: zero products add nothing)
+      const int ch = base + 32 * B + lane + 32 * j;
+      xn[j] = ch < nchunks ? __ldg(xr + ch) : zero;
+      wn[j] = ch < nchunks ? __ldg(wrow + ch) : zero;
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (base + lane + 32 * j < nchunks) {
-        acc_prod(s0, c0, bf16_lo(xv[j].x), bf16_lo(wv[j].x));
-        acc_prod(s1, c1, bf16_hi(xv[j].x), bf16_hi(wv[j].x));
-        acc_prod(s0, c0, bf16_lo(xv[j].y), bf16_lo(wv[j].y));
-        acc_prod(s1, c1, bf16_hi(xv[j].y), bf16_hi(wv[j].y));
-        acc_prod(s0, c0, bf16_lo(xv[j].z), bf16_lo(wv[j].z));
-        acc_prod(s1, c1, bf16_hi(xv[j].z), bf16_hi(wv[j].z));
-        acc_prod(s0, c0, bf16_lo(xv[j].w), bf16_lo(wv[j].w));
-        acc_prod(s1, c1, bf16_hi(xv[j].w), bf16_hi(wv[j].w));
-      }
+    for (int j = 0; j < B; ++j) acc_chunk(s, c, xv[j], wv[j]);
+#pragma unroll
+    for (int j = 0; j < B; ++j) {
+      xv[j] = xn[j];
+      wv[j] = wn[j];
     }
   }
-  float s, e0;
-  two_sum(s0, s1, s, e0);
-  float c = __fadd_rn(__fadd_rn(c0, c1), e0);
+  float a, ea, b, eb, sum, e;
+  two_sum(s[0], s[1], a, ea);
+  two_sum(s[2], s[3], b, eb);
+  two_sum(a, b, sum, e);
+  float cc = __fadd_rn(__fadd_rn(__fadd_rn(c[0], c[1]), __fadd_rn(c[2], c[3])), __fadd_rn(__fadd_rn(ea, eb), e));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
-    const float so = __shfl_xor_sync(kFull, s, off);
-    const float co = __shfl_xor_sync(kFull, c, off);
+    const float so = __shfl_xor_sync(kFull, sum, off);
+    const float co = __shfl_xor_sync(kFull, cc, off);
     float ns, ne;
-    two_sum(s, so, ns, ne);
-    s = ns;
-    c = __fadd_rn(__fadd_rn(c, co), ne);
+    two_sum(sum, so, ns, ne);
+    sum = ns;
+    cc = __fadd_rn(__fadd_rn(cc, co), ne);
   }
-  return __fadd_rn(s, c);
+  return __fadd_rn(sum, cc);
 }
 
 // One warp per token, 8 tokens per CTA, no block barriers: for large T, where throughput matters more than
