@@ -71,7 +71,7 @@ constexpr int BN = 128;            // weight rows per tile (MMA N)
 constexpr int KBYTES = 128;        // bytes of K in one 128-byte swizzle atom: 256 FP4 = 4 MMAs of K = 64
 constexpr int HALVES = 2;          // K atoms per ring stage: 512 FP4 = 8 MMAs per stage
 constexpr int ATOMS = 4 * HALVES;  // 64-element scale atoms per stage
-constexpr int STAGES = 3;
+constexpr int STAGES = 3;  // six half-size stages were slower: per-stage overhead outweighs the extra slack
 constexpr int HALF_BYTES = BM * KBYTES;        // one 128-row x 128-byte swizzled block (16 KB)
 constexpr int A_BYTES = HALVES * HALF_BYTES;
 constexpr int B_BYTES = HALVES * HALF_BYTES;   // pre-tiled weight blocks of consecutive k-stages
@@ -121,6 +121,8 @@ struct Params {
 // activation and weight tiles in L2, and the load balances itself.
 constexpr int kChunk = 4;
 constexpr int kSchedSlots = 4;  // chunk ids handed from the producer to the MMA issuer and the epilogue
+// full, empty, tfull (2), tempty (2), drain, sfull, sempty, sready, cdrain: all in the 256 bytes at BAR_OFF
+static_assert(8 * (2 * STAGES + 2 + 2 + 1 + 2 * kSchedSlots + STAGES + 1) <= 256, "barriers fit their area");
 
 __device__ __forceinline__ int expert_chunks(int me, int NT) {
   return me == 0 ? 0 : (me == 1 ? (NT + kChunk - 1) / kChunk : ((me + kChunk - 1) / kChunk) * NT);
