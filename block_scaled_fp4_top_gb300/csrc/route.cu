@@ -31,6 +31,8 @@ namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr int kSmallPairs = 4096;    // single-CTA layout up to this many (token, k) pairs
+constexpr int kSmallHist = 8192;     // its per-chunk expert histogram: min(32, 8192 / E) chunks
+static_assert(kMaxExperts <= 8192 && kMaxExperts <= 32767, "a chunk row fits the histogram; ids fit int16");
 
 __device__ __forceinline__ int block_inclusive_scan(int v, int* s_warp) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -85,8 +87,9 @@ __device__ __forceinline__ void offsets_and_pads(int E, int cap, int c, int* s_w
 }
 
 // Decode-sized layout in one CTA of 1024 threads: histogram, offsets, pads,
-// and slots in ascending pair order (warp 0 walks the pairs 32 at a time;
-// lanes sharing an expert rank themselves by lane order).
+// and slots in ascending pair order. Each warp walks its own contiguous chunk
+// of pairs 32 at a time from its chunk's per-expert base; lanes sharing an
+// expert rank themselves by lane order.
 // Local expert of global id g: g - first for the experts [first, first + E) this layer holds, -1 for an
 // expert held elsewhere (its pair is masked out, "Bug 8"), -2 for an id outside [0, Eg) (an error).
 __device__ __forceinline__ int local_expert(int g, int Eg, int first, int E) {
@@ -104,41 +107,55 @@ __global__ void __launch_bounds__(1024) layout_small_kernel(int npairs, int Eg, 
                                                             int32_t* __restrict__ pair_of_row, uint32_t* err) {
   pdl_wait();
   pdl_trigger();
-  __shared__ int s_cnt[kMaxExperts];
-  __shared__ int s_base[kMaxExperts];
+  // The pairs are cut into nch contiguous chunks, one per warp; s_hist[ch * E + e] counts expert e in chunk
+  // ch, then holds the chunk's first slot for e. Slots stay in ascending pair order.
+  __shared__ int s_hist[kSmallHist];
   __shared__ int s_warp[32];
-  __shared__ int s_ids[kSmallPairs];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  __shared__ int16_t s_ids[kSmallPairs];  // local expert ids (E <= 1024), -1 for a masked pair
+  const int nch = min(32, kSmallHist / E);
+  const int len = (npairs + nch - 1) / nch;
+  for (int i = threadIdx.x; i < nch * E; i += blockDim.x) s_hist[i] = 0;
   __syncthreads();
   for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
-    int e = local_expert(__ldcg(ids + p), Eg, first, E);
-    if (e >= 0) atomicAdd(&s_cnt[e], 1);
+    const int e = local_expert(__ldcg(ids + p), Eg, first, E);
+    if (e >= 0) atomicAdd(&s_hist[(p / len) * E + e], 1);
     else if (e == -2) raise_error(err, FP4MOE_ERR_EXPERT_ID);
-    s_ids[p] = e < 0 ? -1 : e;
+    s_ids[p] = (int16_t)(e < 0 ? -1 : e);
   }
   __syncthreads();
-  const int c = (threadIdx.x < E) ? s_cnt[threadIdx.x] : 0;
+  int c = 0;
+  if (threadIdx.x < E)
+    for (int ch = 0; ch < nch; ++ch) c += s_hist[ch * E + threadIdx.x];
   int start;
   offsets_and_pads(E, cap, c, s_warp, counts, offsets, poff, pair_of_row, err, start);
-  if (threadIdx.x < E) s_base[threadIdx.x] = start;
+  if (threadIdx.x < E) {
+    int base = start;
+    for (int ch = 0; ch < nch; ++ch) {
+      const int n = s_hist[ch * E + threadIdx.x];
+      s_hist[ch * E + threadIdx.x] = base;
+      base += n;
+    }
+  }
   __syncthreads();
-  if (threadIdx.x >= 32) return;
-  const int lane = threadIdx.x;
-  for (int pb = 0; pb < npairs; pb += 32) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp >= nch) return;
+  int* base = s_hist + warp * E;
+  const int p1 = min(npairs, (warp + 1) * len);
+  for (int pb = warp * len; pb < p1; pb += 32) {
     const int p = pb + lane;
-    const int e = (p < npairs) ? s_ids[p] : -1;
+    const int e = (p < p1) ? s_ids[p] : -1;
     const unsigned peers = __match_any_sync(kFull, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
     if (e >= 0) {
-      const int slot = s_base[e] + rank;
+      const int slot = base[e] + rank;
       slot_of_pair[p] = slot;
       if (slot < cap) pair_of_row[slot] = p;
       else raise_error(err, FP4MOE_ERR_CAPACITY);
-    } else if (p < npairs) {
+    } else if (p < p1) {
       slot_of_pair[p] = -1;  // held by no local expert: no slot
     }
     __syncwarp();
-    if (e >= 0 && rank == 0) s_base[e] += __popc(peers);
+    if (e >= 0 && rank == 0) base[e] += __popc(peers);
     __syncwarp();
   }
 }
