@@ -32,12 +32,13 @@
 //               are also pulled into L2 a few stages ahead
 //               (cp.async.bulk.prefetch.L2). The shared-memory ring runs on
 //               across tile boundaries, so the weight stream never stops.
-//   warp 6      scale copier. tcgen05.cp costs about the same per instruction
-//               whatever its size, and holds its issuing thread. So the
+//   warps 6-7   scale copiers. tcgen05.cp costs about the same per instruction
+//               whatever its size, and holds its issuing thread (about 190
+//               cycles), so two threads share each stage's copies. The
 //               resident scales are copied into TMEM only once, for the whole
 //               of K, and stay there while the operand is fixed. Each stage
-//               then copies only its 8 streamed scale tiles, and commits them
-//               to a per-stage barrier.
+//               then copies only its 8 streamed scale tiles, and each copier
+//               commits its share to a per-stage barrier.
 //   warp 5      MMA issuer. Once a stage's operands and scales are in place,
 //               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (K = 64
 //               each) accumulates in fp32 in TMEM, and tcgen05.commit frees the
@@ -81,7 +82,8 @@ constexpr int STR_OFF = RES_OFF + ATOMS * SF_TILE;      // scale tiles of the st
 constexpr int STAGE_BYTES = STR_OFF + ATOMS * SF_TILE;  // 73728, a multiple of 1024
 constexpr int BAR_OFF = STAGES * STAGE_BYTES;
 constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;    // barriers + 1024-byte alignment slack
-constexpr int THREADS = 224;  // 4 epilogue warps, producer, MMA issuer, scale copier
+constexpr int NCOPY = 2;       // scale-copier warps: each tcgen05.cp holds its issuing thread, so they share a stage
+constexpr int THREADS = 192 + 32 * NCOPY;  // 4 epilogue warps, producer, MMA issuer, scale copiers
 constexpr int PREFETCH = 6;         // ring stages pulled into L2 ahead of the ring
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 128;  // one accumulator: 128 fp32 columns
@@ -343,10 +345,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(bar_drain, 1);
     for (int q = 0; q < kSchedSlots; ++q) {
       mbar_init(bar_sfull + 8 * q, 1);
-      mbar_init(bar_sempty + 8 * q, 1 + 1 + 4);  // the MMA issuer, the scale copier and the four epilogue warps
+      mbar_init(bar_sempty + 8 * q, 1 + NCOPY + 4);  // the MMA issuer, the scale copiers and the epilogue warps
     }
-    for (int s = 0; s < STAGES; ++s) mbar_init(bar_sready + 8 * s, 1);  // the copier's commit
-    mbar_init(bar_cdrain, 1);
+    for (int s = 0; s < STAGES; ++s) mbar_init(bar_sready + 8 * s, NCOPY);  // one commit per copier
+    mbar_init(bar_cdrain, NCOPY);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -507,8 +509,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     // no MMA may still write TMEM when it is freed
     tc_commit(bar_drain);
     drain_wait(bar_drain, 0);
-  } else if (warp == 6 && lane == 0) {
-    // ------------------------------------------------------------ scale copier
+  } else if (warp >= 6 && warp < 6 + NCOPY && lane == 0) {
+    // ------------------------------------------------------------ scale copiers
+    // Copier c takes the scale atoms a with a % NCOPY == c of every stage.
+    const int cpy = warp - 6;
     // Per stage: the 8 streamed scale tiles (and, for a new fixed operand, its 8 resident ones) from the
     // stage's shared memory into TMEM, then one commit to bar_sready. TMEM slot s of the streamed scales
     // is free again once stage s is full: the producer refilled it only after the MMAs of its previous use
@@ -543,16 +547,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t st = smem + (uint32_t)s * STAGE_BYTES;
         const uint32_t res_t = tmem + res_col + 4u * ATOMS * kb;
         const uint32_t str_t = tmem + str_col + SFB_STAGE_COLS * s;
-        if (kb * ATOMS + ATOMS <= katoms_total) {  // a full stage: 8 scale atoms
+        if (kb * ATOMS + ATOMS <= katoms_total) {  // a full stage: 8 scale atoms, shared by the copiers
           if (new_res) {
 #pragma unroll
-            for (int a = 0; a < ATOMS; ++a) tc_cp_scales(res_t + 4 * a, desc_scales(st + RES_OFF + a * SF_TILE));
+            for (int a = cpy; a < ATOMS; a += NCOPY)
+              tc_cp_scales(res_t + 4 * a, desc_scales(st + RES_OFF + a * SF_TILE));
           }
 #pragma unroll
-          for (int a = 0; a < ATOMS; ++a) tc_cp_scales(str_t + 4 * a, desc_scales(st + STR_OFF + a * SF_TILE));
+          for (int a = cpy; a < ATOMS; a += NCOPY) tc_cp_scales(str_t + 4 * a, desc_scales(st + STR_OFF + a * SF_TILE));
         } else {  // the partial last stage of a K that is not a multiple of 512
           const int atoms = katoms_total - kb * ATOMS;
-          for (int a = 0; a < atoms; ++a) {
+          for (int a = cpy; a < atoms; a += NCOPY) {
             if (new_res) tc_cp_scales(res_t + 4 * a, desc_scales(st + RES_OFF + a * SF_TILE));
             tc_cp_scales(str_t + 4 * a, desc_scales(st + STR_OFF + a * SF_TILE));
           }
