@@ -31,29 +31,43 @@ namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr int kSmallPairs = 4096;    // single-CTA layout up to this many (token, k) pairs
-constexpr int kSmallHist = 8192;     // its per-chunk expert histogram: min(32, 8192 / E) chunks
+constexpr int kSmallHist = 8192;     // its per-chunk expert histogram: at most min(32, 8192 / E) chunks
 static_assert(kMaxExperts <= 8192 && kMaxExperts <= 32767, "a chunk row fits the histogram; ids fit int16");
 
-__device__ __forceinline__ int block_inclusive_scan(int v, int* s_warp) {
+// Inclusive block scans of two values at once (one set of barriers for both); s_warp holds 64 ints.
+__device__ __forceinline__ int2 block_inclusive_scan2(int2 v, int* s_warp) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const int o = __shfl_up_sync(kFull, v, off);
-    if (lane >= off) v += o;
+    const int ox = __shfl_up_sync(kFull, v.x, off);
+    const int oy = __shfl_up_sync(kFull, v.y, off);
+    if (lane >= off) {
+      v.x += ox;
+      v.y += oy;
+    }
   }
-  if (lane == 31) s_warp[warp] = v;
+  if (lane == 31) {
+    s_warp[warp] = v.x;
+    s_warp[32 + warp] = v.y;
+  }
   __syncthreads();
   if (warp == 0) {
-    int w = (lane < (int)(blockDim.x >> 5)) ? s_warp[lane] : 0;
+    const bool in = lane < (int)(blockDim.x >> 5);
+    int wx = in ? s_warp[lane] : 0, wy = in ? s_warp[32 + lane] : 0;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(kFull, w, off);
-      if (lane >= off) w += o;
+      const int ox = __shfl_up_sync(kFull, wx, off);
+      const int oy = __shfl_up_sync(kFull, wy, off);
+      if (lane >= off) {
+        wx += ox;
+        wy += oy;
+      }
     }
-    s_warp[lane] = w;
+    s_warp[lane] = wx;
+    s_warp[32 + lane] = wy;
   }
   __syncthreads();
-  const int r = v + (warp > 0 ? s_warp[warp - 1] : 0);
+  const int2 r = make_int2(v.x + (warp > 0 ? s_warp[warp - 1] : 0), v.y + (warp > 0 ? s_warp[32 + warp - 1] : 0));
   __syncthreads();
   return r;
 }
@@ -68,8 +82,8 @@ __device__ __forceinline__ void offsets_and_pads(int E, int cap, int c, int* s_w
   __shared__ int s_R;
   const int e = threadIdx.x;
   const int P = (c + 127) & ~127;
-  const int oc = block_inclusive_scan(c, s_warp);
-  const int op = block_inclusive_scan(P, s_warp);
+  const int2 sc = block_inclusive_scan2(make_int2(c, P), s_warp);
+  const int oc = sc.x, op = sc.y;
   start = op - P;
   if (e < E) {
     counts[e] = c;
@@ -82,7 +96,13 @@ __device__ __forceinline__ void offsets_and_pads(int E, int cap, int c, int* s_w
   }
   __syncthreads();
   const int R = min(s_R, cap);
-  for (int r = threadIdx.x; r < R; r += blockDim.x) pair_of_row[r] = -1;
+  int r0 = 0;
+  if ((reinterpret_cast<uintptr_t>(pair_of_row) & 15u) == 0) {  // four rows per store where aligned
+    const int4 m1 = make_int4(-1, -1, -1, -1);
+    for (int q = threadIdx.x; q < R / 4; q += blockDim.x) reinterpret_cast<int4*>(pair_of_row)[q] = m1;
+    r0 = R & ~3;
+  }
+  for (int r = r0 + threadIdx.x; r < R; r += blockDim.x) pair_of_row[r] = -1;
   __syncthreads();
 }
 
@@ -110,9 +130,10 @@ __global__ void __launch_bounds__(1024) layout_small_kernel(int npairs, int Eg, 
   // The pairs are cut into nch contiguous chunks, one per warp; s_hist[ch * E + e] counts expert e in chunk
   // ch, then holds the chunk's first slot for e. Slots stay in ascending pair order.
   __shared__ int s_hist[kSmallHist];
-  __shared__ int s_warp[32];
+  __shared__ int s_warp[64];
   __shared__ int16_t s_ids[kSmallPairs];  // local expert ids (E <= 1024), -1 for a masked pair
-  const int nch = min(32, kSmallHist / E);
+  // at most one chunk of 32 pairs per warp keeps the per-expert chunk walks below short
+  const int nch = max(1, min(min(32, kSmallHist / E), (npairs + 31) / 32));
   const int len = (npairs + nch - 1) / nch;
   for (int i = threadIdx.x; i < nch * E; i += blockDim.x) s_hist[i] = 0;
   __syncthreads();
@@ -188,7 +209,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(int E, int nchunks, int cap,
                                                     uint32_t* err) {
   pdl_wait();
   pdl_trigger();
-  __shared__ int s_warp[32];
+  __shared__ int s_warp[64];
   const int e = threadIdx.x;
   int c = 0;
   if (e < E) {

@@ -46,10 +46,10 @@ constexpr int RT_BM = 128;                 // experts per tile (MMA M)
 constexpr int RT_MAX_BN = 256;             // tokens per tile (MMA N): min(256, T rounded up to 32)
 constexpr int RT_KBYTES = 128;             // one 64-element bf16 K atom per row (128-byte swizzle)
 constexpr int RT_A = RT_BM * RT_KBYTES;    // w tile of one K atom: 16 KB
-constexpr int RT_STAGE = RT_A + RT_MAX_BN * RT_KBYTES;  // + x tile: 48 KB at most
-constexpr int RT_STAGES = 4;
-constexpr int RT_BAR_OFF = RT_STAGES * RT_STAGE;
-constexpr int RT_SMEM = RT_BAR_OFF + 128 + 1024;
+constexpr int RT_MAX_STAGE = RT_A + RT_MAX_BN * RT_KBYTES;  // + x tile: 48 KB at most
+constexpr int RT_BAR_OFF = 4 * RT_MAX_STAGE;  // the ring: 4 stages of the largest tile, more of smaller ones
+constexpr int RT_MAX_STAGES = 8;
+constexpr int RT_SMEM = RT_BAR_OFF + 16 * RT_MAX_STAGES + 8 + 1024;
 constexpr int RT_THREADS = 192;
 constexpr int RT_RS = RT_MAX_BN + 4;       // row stride (floats) of the cluster-reduction tile
 constexpr int RT_MAX_SPLIT = 8;            // portable cluster size
@@ -61,6 +61,7 @@ constexpr float kBoundUlp = 4.76837158203125e-7f;
 
 struct RouterParams {
   int T, H, E, S, BN;
+  int NS, stage;  // ring stages and bytes per stage (RT_A + BN * RT_KBYTES, a multiple of 4 KB)
   float* lt;     // [T][E] approximate logits (no bias)
   float* nw2;    // [E] |w_e|^2
   uint32_t* err;
@@ -107,16 +108,17 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* smem_gen = smem_raw + (smem - smem_u32(smem_raw));
+  const int NS = p.NS, STAGE = p.stage;
   const uint32_t bar_full = smem + RT_BAR_OFF;
-  const uint32_t bar_empty = bar_full + 8 * RT_STAGES;
-  const uint32_t bar_done = bar_empty + 8 * RT_STAGES;
+  const uint32_t bar_empty = bar_full + 8 * RT_MAX_STAGES;
+  const uint32_t bar_done = bar_empty + 8 * RT_MAX_STAGES;
 
   if (warp == 0) {
     tmem_alloc(smem_u32(&s_tmem), RT_MAX_BN);
     tmem_relinquish();
   }
   if (threadIdx.x == 128) {
-    for (int s = 0; s < RT_STAGES; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1 + 4);  // the MMA commit and one arrive per norm warp
     }
@@ -138,32 +140,32 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     const uint64_t pol = policy_evict_last();  // x and w are each read by several CTAs
     int issued = a0;
     for (int j = a0; j < a1; ++j, ++issued) {
-      const int it = j - a0, s = it % RT_STAGES;
-      if (!mbar_wait(bar_empty + 8 * s, ((uint32_t)(it / RT_STAGES) & 1u) ^ 1u, p.err)) {
+      const int it = j - a0, s = it % NS;
+      if (!mbar_wait(bar_empty + 8 * s, ((uint32_t)(it / NS) & 1u) ^ 1u, p.err)) {
         ok = false;
         break;
       }
-      const uint32_t st = smem + s * RT_STAGE;
+      const uint32_t st = smem + s * STAGE;
       mbar_arrive_expect_tx(bar_full + 8 * s, RT_A + BN * RT_KBYTES);
       tma_load_2d(st, &tmW, bar_full + 8 * s, j * RT_KBYTES, et * RT_BM, pol);
       tma_load_2d(st + RT_A, &tmX, bar_full + 8 * s, j * RT_KBYTES, tt * BN, pol);
     }
     // on every path, let the copies already issued land before the ring is reused or the CTA exits
-    for (int j = max(a0, issued - RT_STAGES); j < issued; ++j) {
+    for (int j = max(a0, issued - NS); j < issued; ++j) {
       const int it = j - a0;
-      drain_wait(bar_full + 8 * (it % RT_STAGES), (uint32_t)(it / RT_STAGES) & 1u);
+      drain_wait(bar_full + 8 * (it % NS), (uint32_t)(it / NS) & 1u);
     }
   } else if (warp == 5 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idesc = idesc_bf16(RT_BM, BN);
     for (int j = a0; j < a1 && ok; ++j) {
-      const int it = j - a0, s = it % RT_STAGES;
-      if (!mbar_wait(bar_full + 8 * s, (uint32_t)(it / RT_STAGES) & 1u, p.err)) {
+      const int it = j - a0, s = it % NS;
+      if (!mbar_wait(bar_full + 8 * s, (uint32_t)(it / NS) & 1u, p.err)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t st = smem + s * RT_STAGE;
+      const uint32_t st = smem + s * STAGE;
 #pragma unroll
       for (int q = 0; q < 4; ++q)  // K = 16 bf16 = 32 bytes per MMA
         tc_mma_bf16(tmem, desc_sw128(st + 32 * q), desc_sw128(st + RT_A + 32 * q), idesc,
@@ -175,12 +177,12 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   } else if (warp < 4) {
     // ------------------------------------------------------------------ norms
     for (int j = a0; j < a1 && ok; ++j) {
-      const int it = j - a0, s = it % RT_STAGES;
-      if (!mbar_wait(bar_full + 8 * s, (uint32_t)(it / RT_STAGES) & 1u, p.err)) {
+      const int it = j - a0, s = it % NS;
+      if (!mbar_wait(bar_full + 8 * s, (uint32_t)(it / NS) & 1u, p.err)) {
         ok = false;
         break;
       }
-      if (do_w) sw = row_sumsq(smem_gen + s * RT_STAGE + i * RT_KBYTES, i, sw);
+      if (do_w) sw = row_sumsq(smem_gen + s * STAGE + i * RT_KBYTES, i, sw);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * s);
     }
@@ -233,13 +235,20 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       const int row = (int)rank * R + idx % R;
       const int c = (idx / R) * 4;
       const uint32_t off = (uint32_t)(row * RT_RS + c) * 4u;
-      float4 a = ld_cluster_f4(map_cluster(red_s + off, 0));
-      for (int q = 1; q < S; ++q) {
-        const float4 b = ld_cluster_f4(map_cluster(red_s + off, (uint32_t)q));
-        a.x += b.x;
-        a.y += b.y;
-        a.z += b.z;
-        a.w += b.w;
+      // all S loads are in flight before the first add; the sum still runs in rank order
+      float4 b[RT_MAX_SPLIT];
+#pragma unroll
+      for (int q = 0; q < RT_MAX_SPLIT; ++q)
+        if (q < S) b[q] = ld_cluster_f4(map_cluster(red_s + off, (uint32_t)q));
+      float4 a = b[0];
+#pragma unroll
+      for (int q = 1; q < RT_MAX_SPLIT; ++q) {
+        if (q < S) {
+          a.x += b[q].x;
+          a.y += b[q].y;
+          a.z += b[q].z;
+          a.w += b[q].w;
+        }
       }
       const int e = et * RT_BM + row, t = tt * BN + c;
       if (e < p.E) {
@@ -252,8 +261,14 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     }
     if (rank == 0 && warp < 4 && do_w) {
       const uint32_t onw = (uint32_t)(RT_BM * RT_RS + i) * 4u;
-      float nw = ld_cluster_f32(map_cluster(red_s + onw, 0));
-      for (int q = 1; q < S; ++q) nw += ld_cluster_f32(map_cluster(red_s + onw, (uint32_t)q));
+      float b[RT_MAX_SPLIT];
+#pragma unroll
+      for (int q = 0; q < RT_MAX_SPLIT; ++q)
+        if (q < S) b[q] = ld_cluster_f32(map_cluster(red_s + onw, (uint32_t)q));
+      float nw = b[0];
+#pragma unroll
+      for (int q = 1; q < RT_MAX_SPLIT; ++q)
+        if (q < S) nw += b[q];
       if (e_row < p.E) p.nw2[e_row] = nw;
     }
     cluster_sync();  // no CTA leaves while another still reads its shared memory
@@ -321,43 +336,30 @@ __device__ float warp_exact_dot(const uint4* xs, const uint4* __restrict__ wrow,
   return __fadd_rn(s, c);
 }
 
-// One warp picks the k largest of key[list[0..n)] (descending, ties to the lower expert id): writes the
-// picks to sel_e / sel_v (lane 0's registers are authoritative) and returns the k-th value, or NaN when
-// fewer than k finite-or-infinite keys exist.
-__device__ float warp_select(const float* key, const int* list, int n, int k, int* sel_e, float* sel_v) {
-  const int lane = threadIdx.x & 31;
-  uint32_t taken = 0;  // bit q: item lane + 32 q already picked
-  float kth = __int_as_float(0x7FC00000);
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int be = INT_MAX, bq = -1;
-    for (int q = 0; lane + 32 * q < n; ++q) {
-      if ((taken >> q) & 1u) continue;
-      const int e = list ? list[lane + 32 * q] : lane + 32 * q;
-      const float v = key[e];
-      if (v > bv || (v == bv && e < be)) {
-        bv = v;
-        be = e;
-        bq = q;
-      }
+// The rank of the item (v, e) among the n items key[f], f = list[j] (f = j without a list): how many of
+// them come before it in the order value descending, expert id ascending. A NaN item comes before
+// nothing, and a NaN v is never ranked. The items of a top-k pick are those of rank < k, and rank r goes
+// to place r, so every thread can rank its own items at once.
+__device__ __forceinline__ int rank_among(const float* key, const int* list, int n, float v, int e) {
+  int r = 0;
+  if (list == nullptr) {
+    int j = 0;
+    for (; j + 4 <= n; j += 4) {  // key is 16-byte aligned: one broadcast load per four items
+      const float4 u = *reinterpret_cast<const float4*>(key + j);
+      r += (u.x > v || (u.x == v && j < e)) ? 1 : 0;
+      r += (u.y > v || (u.y == v && j + 1 < e)) ? 1 : 0;
+      r += (u.z > v || (u.z == v && j + 2 < e)) ? 1 : 0;
+      r += (u.w > v || (u.w == v && j + 3 < e)) ? 1 : 0;
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(kFull, bv, off);
-      const int oe = __shfl_xor_sync(kFull, be, off);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
-        be = oe;
-      }
+    for (; j < n; ++j) r += (key[j] > v || (key[j] == v && j < e)) ? 1 : 0;
+  } else {
+    for (int j = 0; j < n; ++j) {
+      const int f = list[j];
+      const float u = key[f];
+      r += (u > v || (u == v && f < e)) ? 1 : 0;
     }
-    if (be == INT_MAX) return __int_as_float(0x7FC00000);  // only NaN keys remain
-    // the lane that holds the winner marks it taken
-    if (bq >= 0 && (list ? list[lane + 32 * bq] : lane + 32 * bq) == be) taken |= 1u << bq;
-    sel_e[j] = be;
-    sel_v[j] = bv;
-    kth = bv;
   }
-  return kth;
+  return r;
 }
 
 // One CTA of 256 threads per token.
@@ -371,12 +373,14 @@ __global__ void __launch_bounds__(256) router_refine_kernel(int H, int E, int k,
   pdl_trigger();
   __shared__ uint4 s_x[kMaxChunksPerLane * 32];
   __shared__ float s_l[kMaxExperts];
-  __shared__ float s_lo[kMaxExperts];
+  __shared__ __align__(16) float s_lo[kMaxExperts];
   __shared__ float s_hi[kMaxExperts];
   __shared__ int s_cand[kMaxExperts];
   __shared__ float s_part[8];
   __shared__ int s_m;
   __shared__ float s_tau;
+  __shared__ int s_sel_e[kMaxTopK];
+  __shared__ float s_sel_v[kMaxTopK];
   const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunks = H / 8;
@@ -392,7 +396,11 @@ __global__ void __launch_bounds__(256) router_refine_kernel(int H, int E, int k,
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(kFull, sq, off);
   if (lane == 0) s_part[warp] = sq;
-  if (threadIdx.x == 0) s_m = 0;
+  if (threadIdx.x == 0) {
+    s_m = 0;
+    s_tau = __int_as_float(0x7FC00000);  // stays NaN when fewer than k lower ends are numbers
+  }
+  if (threadIdx.x < kMaxTopK) s_sel_e[threadIdx.x] = -1;
   __syncthreads();
   float nx2 = 0.0f;
 #pragma unroll
@@ -408,11 +416,10 @@ __global__ void __launch_bounds__(256) router_refine_kernel(int H, int E, int k,
     s_hi[e] = __fadd_ru(l, d);
   }
   __syncthreads();
-  if (warp == 0) {
-    int se[kMaxTopK];
-    float sv[kMaxTopK];
-    const float tau = warp_select(s_lo, nullptr, E, k, se, sv);
-    if (lane == 0) s_tau = tau;
+  // tau = the k-th largest lower end: the one of rank k - 1
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const float v = s_lo[e];
+    if (v == v && rank_among(s_lo, nullptr, E, v, e) == k - 1) s_tau = v;
   }
   __syncthreads();
   const float tau = s_tau;
@@ -429,33 +436,43 @@ __global__ void __launch_bounds__(256) router_refine_kernel(int H, int E, int k,
     if (lane == 0) s_l[e] = l;
   }
   __syncthreads();
-  if (warp == 0) {
-    int se[kMaxTopK];
-    float sv[kMaxTopK];
-    const float kth = warp_select(s_l, s_cand, m, k, se, sv);
-    if (lane == 0) {
-      if (kth != kth) {  // fewer than k comparable logits: NaN input
-        raise_error(err, FP4MOE_ERR_EXPERT_ID);
-        for (int j = 0; j < k; ++j) {
-          ids_out[(size_t)t * k + j] = 0;
-          w_out[(size_t)t * k + j] = 0.0f;
-        }
-      } else {
-        const float lmax = sv[0];
-        float ex[kMaxTopK];
-        float sum = 0.0f;
-        for (int j = 0; j < k; ++j) {
-          ex[j] = expf(__fsub_rn(sv[j], lmax));
-          sum = __fadd_rn(sum, ex[j]);
-        }
-        for (int j = 0; j < k; ++j) {
-          ids_out[(size_t)t * k + j] = se[j];
-          w_out[(size_t)t * k + j] = __fdiv_rn(ex[j], sum);
-        }
+  // the top k of the candidates by exact logit: the candidate of rank r < k takes place r
+  for (int c = threadIdx.x; c < m; c += blockDim.x) {
+    const int e = s_cand[c];
+    const float v = s_l[e];
+    if (v == v) {
+      const int r = rank_among(s_l, s_cand, m, v, e);
+      if (r < k) {
+        s_sel_e[r] = e;
+        s_sel_v[r] = v;
       }
     }
   }
   for (int e = threadIdx.x; e < E; e += blockDim.x) lrow[e] = s_l[e];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bool bad = false;
+    for (int j = 0; j < k; ++j) bad |= s_sel_e[j] < 0;
+    if (bad) {  // fewer than k comparable logits: NaN input
+      raise_error(err, FP4MOE_ERR_EXPERT_ID);
+      for (int j = 0; j < k; ++j) {
+        ids_out[(size_t)t * k + j] = 0;
+        w_out[(size_t)t * k + j] = 0.0f;
+      }
+    } else {
+      const float lmax = s_sel_v[0];
+      float ex[kMaxTopK];
+      float sum = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        ex[j] = expf(__fsub_rn(s_sel_v[j], lmax));
+        sum = __fadd_rn(sum, ex[j]);
+      }
+      for (int j = 0; j < k; ++j) {
+        ids_out[(size_t)t * k + j] = s_sel_e[j];
+        w_out[(size_t)t * k + j] = __fdiv_rn(ex[j], sum);
+      }
+    }
+  }
 }
 
 // Argmax over this warp's register arrays (item lane + 32 q is expert lane + 32 q): the largest v among the
@@ -716,6 +733,8 @@ fp4moe_status router_topk_launch(const fp4moe_config& cfg, int32_t T, const uint
   prm.E = E;
   prm.S = S;
   prm.BN = BN;
+  prm.stage = RT_A + BN * RT_KBYTES;
+  prm.NS = RT_BAR_OFF / prm.stage < RT_MAX_STAGES ? RT_BAR_OFF / prm.stage : RT_MAX_STAGES;
   prm.lt = logits;
   prm.nw2 = nw2;
   prm.err = err;

@@ -28,7 +28,7 @@ def _built():
     ensure_built()
 
 
-def route_gpu(wl, T, x_bits, max_tokens=None, wr_bits=None):
+def route_gpu(wl, T, x_bits, max_tokens=None, wr_bits=None, expect_err=0):
     import torch
     from block_scaled_fp4_top_gb300 import api
     cfg = api.config(wl.H, wl.I, wl.E, wl.k, max_tokens or max(T, 1), wl.swiglu_limit)
@@ -47,7 +47,7 @@ def route_gpu(wl, T, x_bits, max_tokens=None, wr_bits=None):
     api.moe_route(cfg, T, x, wr, bias_t, out["logits"], out["ids"], out["w"], out["counts"], out["offsets"],
                   out["poff"], out["slot"], out["por"], ws)
     torch.cuda.synchronize()
-    assert api.fp4moe_read_error(ws) == 0
+    assert api.fp4moe_read_error(ws) == expect_err
     res = {k: v.cpu().numpy() for k, v in out.items()}
     return cfg, cap, res, x, ws
 
@@ -158,3 +158,46 @@ def test_route_ties_and_zero_rows():
     assert np.allclose(g["w"][: T * wl.k].reshape(T, wl.k), w_r, rtol=3e-6, atol=1e-7)
     L = layout.slots(ids_r, wl.E)
     assert (g["slot"][: T * wl.k] == L["slot_of_pair"]).all()
+
+
+BF16_NAN = 0x7FC0
+
+
+@pytest.mark.parametrize("T", [40, 4100])  # one CTA per token; one warp per token from 4096 tokens on
+def test_route_nan_router_row_is_never_picked(T):
+    """A NaN logit ranks below every number: expert 11's router row holds a NaN, token 3 is expert 11's own
+    row (so 11 would top its list), and no token picks 11. Everything else matches the oracle."""
+    wl = sg.DSV4_DECODE
+    wr_clean = sg.router_bf16(wl)
+    wr_bits = wr_clean.copy()
+    wr_bits[11, 5] = BF16_NAN
+    x_bits = sg.activations_bf16(wl, sg.EVAL_SEED, T=T).copy()
+    x_bits[3] = wr_clean[11]
+    _, _, g, _, _ = route_gpu(wl, T, x_bits, wr_bits=wr_bits)
+    ref_l = moe.router_logits(x_bits, wr_bits, sg.router_bias_f32(wl))
+    assert np.isnan(ref_l[:, 11]).all() and np.isnan(g["logits"][:T, 11]).all()
+    ids_r, w_r = moe.topk_softmax(ref_l, wl.k)
+    ids = g["ids"][: T * wl.k].reshape(T, wl.k)
+    assert (ids == ids_r).all() and not (ids == 11).any()
+    assert np.allclose(g["w"][: T * wl.k].reshape(T, wl.k), w_r, rtol=3e-6, atol=1e-7)
+    L = layout.slots(ids_r, wl.E)
+    assert (g["counts"] == L["counts"]).all() and (g["slot"][: T * wl.k] == L["slot_of_pair"]).all()
+
+
+@pytest.mark.parametrize("T", [40, 4100])
+def test_route_nan_token_reports_expert_id_error(T):
+    """A token with a NaN in its row has no comparable logit: the call reports FP4MOE_ERR_EXPERT_ID and
+    that token gets ids 0 and weights 0, while every other token still matches the oracle."""
+    from block_scaled_fp4_top_gb300 import _lib
+    wl = sg.DSV4_DECODE
+    x_bits = sg.activations_bf16(wl, sg.EVAL_SEED, T=T).copy()
+    x_bits[5, 17] = BF16_NAN
+    _, _, g, _, _ = route_gpu(wl, T, x_bits, expect_err=_lib.ERR_EXPERT_ID)
+    ids = g["ids"][: T * wl.k].reshape(T, wl.k)
+    w = g["w"][: T * wl.k].reshape(T, wl.k)
+    assert (ids[5] == 0).all() and (w[5] == 0).all()
+    keep = np.arange(T) != 5
+    ref_l = moe.router_logits(x_bits[keep], sg.router_bf16(wl), sg.router_bias_f32(wl))
+    ids_r, w_r = moe.topk_softmax(ref_l, wl.k)
+    assert (ids[keep] == ids_r).all()
+    assert np.allclose(w[keep], w_r, rtol=3e-6, atol=1e-7)
