@@ -11,7 +11,7 @@
 // Launches, each with a fixed grid chosen from the host-known T:
 //   1-2. router_mma + router_refine (router.cu): logits and softmax top-k.
 //   then, for T*k <= kSmallPairs (decode):
-//   3. layout_small  1 CTA: counts, offsets, padded offsets, slot ranks and
+//   3. layout_small  8 CTAs, one slice of rows each: counts, offsets, padded offsets, slot ranks and
 //                    pair_of_row
 //   otherwise (prefill):
 //   3. hist          grid (chunks of 64 tokens): per-chunk expert histograms
@@ -30,7 +30,8 @@ namespace fp4moe {
 namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr int kSmallPairs = 4096;    // single-CTA layout up to this many (token, k) pairs
+constexpr int kSmallPairs = 4096;    // one-launch layout up to this many (token, k) pairs
+constexpr int kSmallParts = 8;       // its CTAs, one slice of the padded rows each
 constexpr int kSmallHist = 8192;     // its per-chunk expert histogram: at most min(32, 8192 / E) chunks
 static_assert(kMaxExperts <= 8192 && kMaxExperts <= 32767, "a chunk row fits the histogram; ids fit int16");
 
@@ -73,41 +74,49 @@ __device__ __forceinline__ int2 block_inclusive_scan2(int2 v, int* s_warp) {
 }
 
 // Counts, inclusive offsets and padded offsets for expert e = threadIdx.x
-// (1024 threads), given its count c; pads its padding rows with -1.
-// Returns the first row of the expert's block in `start`.
-// All padded rows [0, min(R, cap)) get -1 with coalesced stores; real rows
-// are overwritten by the slot pass that follows.
+// (1024 threads), given its count c. Returns the first row of the expert's
+// block in `start`. The R padded rows are cut into nparts slices, a multiple
+// of 4 rows apart; this CTA (part) alone writes the rows [r_lo, r_hi): here
+// every one of them below cap gets -1 with coalesced stores, and the slot
+// pass that follows overwrites the real ones. Part 0 writes counts, offsets
+// and padded offsets.
 __device__ __forceinline__ void offsets_and_pads(int E, int cap, int c, int* s_warp, int32_t* counts, int32_t* offsets,
-                                                 int32_t* poff, int32_t* pair_of_row, uint32_t* err, int& start) {
+                                                 int32_t* poff, int32_t* pair_of_row, uint32_t* err, int part,
+                                                 int nparts, int& start, int& r_lo, int& r_hi) {
   __shared__ int s_R;
   const int e = threadIdx.x;
   const int P = (c + 127) & ~127;
   const int2 sc = block_inclusive_scan2(make_int2(c, P), s_warp);
   const int oc = sc.x, op = sc.y;
   start = op - P;
-  if (e < E) {
+  if (e < E && part == 0) {
     counts[e] = c;
     offsets[e] = oc;
     poff[e] = op;
   }
   if (e == E - 1) {
     s_R = op;
-    if (op > cap) raise_error(err, FP4MOE_ERR_CAPACITY);
+    if (op > cap && part == 0) raise_error(err, FP4MOE_ERR_CAPACITY);
   }
   __syncthreads();
-  const int R = min(s_R, cap);
-  int r0 = 0;
+  const int R = s_R;
+  r_lo = (int)((long long)(R / 4) * part / nparts) * 4;
+  r_hi = part + 1 == nparts ? R : (int)((long long)(R / 4) * (part + 1) / nparts) * 4;
+  const int R0 = min(r_lo, cap), R1 = min(r_hi, cap);
+  int r0 = R0;
   if ((reinterpret_cast<uintptr_t>(pair_of_row) & 15u) == 0) {  // four rows per store where aligned
     const int4 m1 = make_int4(-1, -1, -1, -1);
-    for (int q = threadIdx.x; q < R / 4; q += blockDim.x) reinterpret_cast<int4*>(pair_of_row)[q] = m1;
-    r0 = R & ~3;
+    for (int q = R0 / 4 + threadIdx.x; q < R1 / 4; q += blockDim.x) reinterpret_cast<int4*>(pair_of_row)[q] = m1;
+    r0 = max(R0, R1 & ~3);
   }
-  for (int r = r0 + threadIdx.x; r < R; r += blockDim.x) pair_of_row[r] = -1;
+  for (int r = r0 + threadIdx.x; r < R1; r += blockDim.x) pair_of_row[r] = -1;
   __syncthreads();
 }
 
-// Decode-sized layout in one CTA of 1024 threads: histogram, offsets, pads,
-// and slots in ascending pair order. Each warp walks its own contiguous chunk
+// Decode-sized layout in kSmallParts CTAs of 1024 threads: each builds the
+// whole histogram, offsets and slot ranks (a few thousand pairs at most) and
+// writes only the rows of its own slice, so no CTA waits for another and no
+// row has two writers. Slots run in ascending pair order. Each warp walks its own contiguous chunk
 // of pairs 32 at a time from its chunk's per-expert base; lanes sharing an
 // expert rank themselves by lane order.
 // Local expert of global id g: g - first for the experts [first, first + E) this layer holds, -1 for an
@@ -148,7 +157,9 @@ __global__ void __launch_bounds__(1024) layout_small_kernel(int npairs, int Eg, 
   if (threadIdx.x < E)
     for (int ch = 0; ch < nch; ++ch) c += s_hist[ch * E + threadIdx.x];
   int start;
-  offsets_and_pads(E, cap, c, s_warp, counts, offsets, poff, pair_of_row, err, start);
+  int r_lo, r_hi;
+  offsets_and_pads(E, cap, c, s_warp, counts, offsets, poff, pair_of_row, err, blockIdx.x, gridDim.x, start, r_lo,
+                   r_hi);
   if (threadIdx.x < E) {
     int base = start;
     for (int ch = 0; ch < nch; ++ch) {
@@ -169,10 +180,12 @@ __global__ void __launch_bounds__(1024) layout_small_kernel(int npairs, int Eg, 
     const int rank = __popc(peers & ((1u << lane) - 1u));
     if (e >= 0) {
       const int slot = base[e] + rank;
-      slot_of_pair[p] = slot;
-      if (slot < cap) pair_of_row[slot] = p;
-      else raise_error(err, FP4MOE_ERR_CAPACITY);
-    } else if (p < p1) {
+      if (slot >= r_lo && slot < r_hi) {  // the slice that holds the slot writes both maps
+        slot_of_pair[p] = slot;
+        if (slot < cap) pair_of_row[slot] = p;
+        else raise_error(err, FP4MOE_ERR_CAPACITY);
+      }
+    } else if (p < p1 && blockIdx.x == 0) {
       slot_of_pair[p] = -1;  // held by no local expert: no slot
     }
     __syncwarp();
@@ -226,7 +239,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(int E, int nchunks, int cap,
     }
   }
   int start;
-  offsets_and_pads(E, cap, c, s_warp, counts, offsets, poff, pair_of_row, err, start);
+  int r_lo, r_hi;  // one part: every row
+  offsets_and_pads(E, cap, c, s_warp, counts, offsets, poff, pair_of_row, err, 0, 1, start, r_lo, r_hi);
 }
 
 // Slot of every pair of one 64-token chunk, in ascending pair order.
@@ -281,7 +295,7 @@ fp4moe_status route_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* 
   if (rs != FP4MOE_OK) return rs;
   cudaError_t r = cudaSuccess;
   if (npairs <= kSmallPairs) {
-    r = launch_pdl(layout_small_kernel, dim3(1), dim3(1024), 0, st, npairs, Eg, first, E, cap, (const int32_t*)ids,
+    r = launch_pdl(layout_small_kernel, dim3(kSmallParts), dim3(1024), 0, st, npairs, Eg, first, E, cap, (const int32_t*)ids,
                    counts, offsets, poff, slot_of_pair, pair_of_row, err);
   } else {
     const int nchunks = (T + kRouteChunk - 1) / kRouteChunk;

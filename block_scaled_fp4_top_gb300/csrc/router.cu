@@ -336,28 +336,16 @@ __device__ float warp_exact_dot(const uint4* xs, const uint4* __restrict__ wrow,
   return __fadd_rn(s, c);
 }
 
-// The rank of the item (v, e) among the n items key[f], f = list[j] (f = j without a list): how many of
-// them come before it in the order value descending, expert id ascending. A NaN item comes before
-// nothing, and a NaN v is never ranked. The items of a top-k pick are those of rank < k, and rank r goes
-// to place r, so every thread can rank its own items at once.
+// The rank of the item (v, e) among the n items key[list[j]]: how many of them come before it in the order
+// value descending, expert id ascending. A NaN item comes before nothing, and a NaN v is never ranked. The
+// items of a top-k pick are those of rank < k, and rank r goes to place r, so every thread can rank its own
+// items at once; the ranks do not depend on the order of the list.
 __device__ __forceinline__ int rank_among(const float* key, const int* list, int n, float v, int e) {
   int r = 0;
-  if (list == nullptr) {
-    int j = 0;
-    for (; j + 4 <= n; j += 4) {  // key is 16-byte aligned: one broadcast load per four items
-      const float4 u = *reinterpret_cast<const float4*>(key + j);
-      r += (u.x > v || (u.x == v && j < e)) ? 1 : 0;
-      r += (u.y > v || (u.y == v && j + 1 < e)) ? 1 : 0;
-      r += (u.z > v || (u.z == v && j + 2 < e)) ? 1 : 0;
-      r += (u.w > v || (u.w == v && j + 3 < e)) ? 1 : 0;
-    }
-    for (; j < n; ++j) r += (key[j] > v || (key[j] == v && j < e)) ? 1 : 0;
-  } else {
-    for (int j = 0; j < n; ++j) {
-      const int f = list[j];
-      const float u = key[f];
-      r += (u > v || (u == v && f < e)) ? 1 : 0;
-    }
+  for (int j = 0; j < n; ++j) {
+    const int f = list[j];
+    const float u = key[f];
+    r += (u > v || (u == v && f < e)) ? 1 : 0;
   }
   return r;
 }
@@ -373,11 +361,12 @@ __global__ void __launch_bounds__(256) router_refine_kernel(int H, int E, int k,
   pdl_trigger();
   __shared__ uint4 s_x[kMaxChunksPerLane * 32];
   __shared__ float s_l[kMaxExperts];
-  __shared__ __align__(16) float s_lo[kMaxExperts];
+  __shared__ float s_lo[kMaxExperts];
   __shared__ float s_hi[kMaxExperts];
   __shared__ int s_cand[kMaxExperts];
   __shared__ float s_part[8];
-  __shared__ int s_m;
+  __shared__ float s_wmax[8];
+  __shared__ int s_m, s_n2;
   __shared__ float s_tau;
   __shared__ int s_sel_e[kMaxTopK];
   __shared__ float s_sel_v[kMaxTopK];
@@ -398,6 +387,7 @@ __global__ void __launch_bounds__(256) router_refine_kernel(int H, int E, int k,
   if (lane == 0) s_part[warp] = sq;
   if (threadIdx.x == 0) {
     s_m = 0;
+    s_n2 = 0;
     s_tau = __int_as_float(0x7FC00000);  // stays NaN when fewer than k lower ends are numbers
   }
   if (threadIdx.x < kMaxTopK) s_sel_e[threadIdx.x] = -1;
@@ -406,20 +396,45 @@ __global__ void __launch_bounds__(256) router_refine_kernel(int H, int E, int k,
 #pragma unroll
   for (int w8 = 0; w8 < 8; ++w8) nx2 += s_part[w8];
   const float nx = sqrtf(nx2);
+  float wmax = -INFINITY;  // this warp's largest lower end (a NaN never wins)
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     float l = __ldcg(lrow + e);
     if (bias != nullptr) l = __fadd_rn(l, bias[e]);
     // the fp32 norms are low by at most ~3e-4 relative: the (1 + 2^-10) factor keeps the bound above it
     const float d = fmaf(kBoundRel * 1.0009765625f, nx * sqrtf(__ldcg(nw2 + e)), kBoundUlp * fabsf(l));
+    const float lo = __fsub_rd(l, d);
     s_l[e] = l;
-    s_lo[e] = __fsub_rd(l, d);
+    s_lo[e] = lo;
     s_hi[e] = __fadd_ru(l, d);
+    wmax = fmaxf(wmax, lo);
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(kFull, wmax, off));
+  if (lane == 0) s_wmax[warp] = wmax;
   __syncthreads();
-  // tau = the k-th largest lower end: the one of rank k - 1
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const float v = s_lo[e];
-    if (v == v && rank_among(s_lo, nullptr, E, v, e) == k - 1) s_tau = v;
+  // theta <= tau: the k-th largest of the eight warp maxima. Each is the lower end of a different expert (or
+  // -inf for a warp without a number), so k experts reach theta and the k-th largest lower end does too.
+  float theta = -INFINITY;
+  if (k <= 8) {
+    const int q0 = lane & 7;
+    const float mq = s_wmax[q0];
+    int r = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float o = s_wmax[q];
+      r += (o > mq || (o == mq && q < q0)) ? 1 : 0;
+    }
+    const unsigned b = __ballot_sync(kFull, lane < 8 && r == k - 1);
+    theta = __shfl_sync(kFull, mq, __ffs(b) - 1);
+  }
+  // tau = the k-th largest lower end: the one of rank k - 1 among those that reach theta (a NaN never does)
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (s_lo[e] >= theta) s_cand[atomicAdd(&s_n2, 1)] = e;
+  __syncthreads();
+  const int n2 = s_n2;
+  for (int c = threadIdx.x; c < n2; c += blockDim.x) {
+    const int e = s_cand[c];
+    if (rank_among(s_lo, s_cand, n2, s_lo[e], e) == k - 1) s_tau = s_lo[e];
   }
   __syncthreads();
   const float tau = s_tau;
