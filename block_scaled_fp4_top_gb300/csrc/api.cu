@@ -98,6 +98,7 @@ WsLayout ws_layout(const fp4moe_config& c) {
   const size_t nchunks = std::max<size_t>(1, (Tm + kRouteChunk - 1) / kRouteChunk);
   L.hist = take(nchunks * E * 4);
   L.nw2 = take(E * 4);
+  L.rt_part = take(router_partial_bytes(c));
   L.logits = take(Tm * E * 4);
   L.ids = take(Tm * k * 4);
   L.w = take(Tm * k * 4);
@@ -128,14 +129,16 @@ WsLayout ws_layout(const fp4moe_config& c) {
 // Scratch of moe_route_noalloc, owned by the library image. Layout:
 // [0, 256) error word, then the squared norms of the router rows (the
 // router's error bound), then the per-chunk expert histograms of the large-T
-// layout.
+// layout, then the router's partial tiles for a single tile of tokens
+// (16 K splits of up to 256 tokens and their norm rows).
 namespace {
 constexpr size_t kScratchErr = 0;
 constexpr size_t kScratchNw2 = 256;
 constexpr size_t kScratchHist = kScratchNw2 + 4 * (size_t)FP4MOE_NOALLOC_MAX_EXPERTS;
-static_assert(kScratchHist + 4 * (size_t)FP4MOE_NOALLOC_MAX_EXPERTS *
-                                     ((FP4MOE_NOALLOC_MAX_TOKENS + kRouteChunk - 1) / kRouteChunk) ==
-                  FP4MOE_NOALLOC_SCRATCH_BYTES,
+constexpr size_t kScratchPart = kScratchHist + 4 * (size_t)FP4MOE_NOALLOC_MAX_EXPERTS *
+                                                   ((FP4MOE_NOALLOC_MAX_TOKENS + kRouteChunk - 1) / kRouteChunk);
+constexpr size_t kScratchPartBytes = 16 * (256 + 1) * 4 * (size_t)FP4MOE_NOALLOC_MAX_EXPERTS;
+static_assert(kScratchPart + kScratchPartBytes == FP4MOE_NOALLOC_SCRATCH_BYTES,
               "scratch layout and its advertised size disagree");
 
 __device__ __align__(256) uint8_t g_route_scratch[FP4MOE_NOALLOC_SCRATCH_BYTES];
@@ -238,7 +241,8 @@ fp4moe_status forward_impl(const fp4moe_config* cfg, int32_t T, const uint16_t* 
   auto routed = [&]() -> fp4moe_status {
     FP4_TRY(route_launch(*cfg, T, x, router_w, router_bias, at<float>(ws, L.logits), ids, w,
                          at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets), poff, at<int32_t>(ws, L.slot), por,
-                         at<int32_t>(ws, L.hist), at<float>(ws, L.nw2), err, st));
+                         at<int32_t>(ws, L.hist), at<float>(ws, L.nw2), at<float>(ws, L.rt_part),
+                         router_partial_bytes(*cfg), err, st));
     if (mx) {
       uint16_t* a1 = at<uint16_t>(ws, L.a1);
       uint16_t* a2 = at<uint16_t>(ws, L.a2);
@@ -332,8 +336,8 @@ fp4moe_status moe_route(const fp4moe_config* cfg, int32_t T, const uint16_t* x, 
   const WsLayout L = ws_layout(*cfg);
   float* logits = logits_out ? logits_out : at<float>(ws, L.logits);
   return route_launch(*cfg, T, x, router_w, router_bias, logits, topk_ids, topk_w, counts, offsets, padded_offsets,
-                      slot_of_pair, pair_of_row, at<int32_t>(ws, L.hist), at<float>(ws, L.nw2), err_word(ws),
-                      (cudaStream_t)stream);
+                      slot_of_pair, pair_of_row, at<int32_t>(ws, L.hist), at<float>(ws, L.nw2),
+                      at<float>(ws, L.rt_part), router_partial_bytes(*cfg), err_word(ws), (cudaStream_t)stream);
 }
 
 fp4moe_status moe_route_noalloc(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
@@ -354,7 +358,8 @@ fp4moe_status moe_route_noalloc(const fp4moe_config* cfg, int32_t T, const uint1
   if (cudaMemsetAsync(s + kScratchErr, 0, 4, st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
   return route_launch(*cfg, T, x, router_w, router_bias, logits_out, topk_ids, topk_w, counts, offsets,
                       padded_offsets, slot_of_pair, pair_of_row, reinterpret_cast<int32_t*>(s + kScratchHist),
-                      reinterpret_cast<float*>(s + kScratchNw2),
+                      reinterpret_cast<float*>(s + kScratchNw2), reinterpret_cast<float*>(s + kScratchPart),
+                      kScratchPartBytes,
                       err != nullptr ? err : reinterpret_cast<uint32_t*>(s + kScratchErr), st);
 }
 
@@ -552,7 +557,7 @@ fp4moe_status fp4moe_calibrate(const fp4moe_config* cfg, int32_t T, const uint16
   FP4_TRY(route_launch(*cfg, T, x_warm, router_w, router_bias, at<float>(ws, L.logits), at<int32_t>(ws, L.ids),
                        at<float>(ws, L.w), at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets), poff,
                        at<int32_t>(ws, L.slot), por, at<int32_t>(ws, L.hist), at<float>(ws, L.nw2),
-                       err, st));
+                       at<float>(ws, L.rt_part), router_partial_bytes(*cfg), err, st));
   FP4_TRY(quant_scatter_launch(*cfg, T, x_warm, gs1_out, at<int32_t>(ws, L.slot), at<uint8_t>(ws, L.a1),
                                at<uint8_t>(ws, L.a1sf), st));
   float* alpha = at<float>(ws, L.alpha_tmp);

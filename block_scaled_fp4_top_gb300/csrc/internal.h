@@ -32,24 +32,28 @@ inline int local_experts(const fp4moe_config& c) { return c.ep_count > 0 ? c.ep_
 
 // Byte offsets of the regions of a workspace sized for cfg.max_tokens.
 struct WsLayout {
-  size_t hist, nw2, logits, ids, w, counts, offsets, poff, slot, por, a1, a1sf, a2, a2sf, opairs, alpha_tmp;
+  size_t hist, nw2, rt_part, logits, ids, w, counts, offsets, poff, slot, por, a1, a1sf, a2, a2sf, opairs, alpha_tmp;
   size_t se_qx, se_sx, se_qh, se_sh, se_o;  // shared expert (cfg.shared_inter > 0)
   size_t total;
 };
 WsLayout ws_layout(const fp4moe_config& cfg);
 
 // Router logits and top-k (router.cu). logits [T][E] receives the approximate logits, then the final ones;
-// nw2 [E] receives the squared norms of the router rows.
+// nw2 [E] receives the squared norms of the router rows. part (part_bytes, may be null) holds the partial
+// tiles when K is split over independent CTAs (a single tile of tokens): router_partial_bytes(cfg) is
+// enough for any T <= cfg.max_tokens; with less room the split runs over a cluster instead.
 fp4moe_status router_topk_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const uint16_t* wr,
-                                 const float* bias, float* logits, float* nw2, int32_t* ids, float* w, uint32_t* err,
-                                 cudaStream_t st);
+                                 const float* bias, float* logits, float* nw2, float* part, size_t part_bytes,
+                                 int32_t* ids, float* w, uint32_t* err, cudaStream_t st);
+size_t router_partial_bytes(const fp4moe_config& cfg);
 
 // The whole routing step: router_topk_launch, then counts, offsets and slots. hist: per-chunk histograms
 // for large T (nchunks x E int32).
 fp4moe_status route_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
                            const float* bias, float* logits, int32_t* ids, float* w, int32_t* counts,
                            int32_t* offsets, int32_t* poff, int32_t* slot_of_pair, int32_t* pair_of_row,
-                           int32_t* hist, float* nw2, uint32_t* err, cudaStream_t st);
+                           int32_t* hist, float* nw2, float* part, size_t part_bytes, uint32_t* err,
+                           cudaStream_t st);
 
 fp4moe_status quant_scatter_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const float* gs1,
                                    const int32_t* slot_of_pair, uint8_t* a1, uint8_t* a1_sf, cudaStream_t st);

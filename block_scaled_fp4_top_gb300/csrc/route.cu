@@ -286,12 +286,14 @@ __global__ void __launch_bounds__(256) slots_kernel(int T, int Eg, int first, in
 fp4moe_status route_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
                            const float* bias, float* logits, int32_t* ids, float* w, int32_t* counts,
                            int32_t* offsets, int32_t* poff, int32_t* slot_of_pair, int32_t* pair_of_row,
-                           int32_t* hist, float* nw2, uint32_t* err, cudaStream_t st) {
+                           int32_t* hist, float* nw2, float* part, size_t part_bytes, uint32_t* err,
+                           cudaStream_t st) {
   const int Eg = cfg.num_experts, first = cfg.ep_count > 0 ? cfg.ep_first : 0, E = local_experts(cfg);
   const int k = cfg.top_k;
   const int cap = (int)capacity_rows(cfg, T);
   const int npairs = T * k;
-  const fp4moe_status rs = router_topk_launch(cfg, T, x, router_w, bias, logits, nw2, ids, w, err, st);
+  const fp4moe_status rs =
+      router_topk_launch(cfg, T, x, router_w, bias, logits, nw2, part, part_bytes, ids, w, err, st);
   if (rs != FP4MOE_OK) return rs;
   cudaError_t r = cudaSuccess;
   if (npairs <= kSmallPairs) {

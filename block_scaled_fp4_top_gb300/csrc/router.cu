@@ -8,10 +8,13 @@
 //
 // Pass 1, router_mma_kernel: approximate logits on the tensor cores.
 //   tcgen05.mma kind::f16 (bf16 x bf16, fp32 accumulate in TMEM). A tile is
-//   128 tokens x 128 experts, and K may be split over a thread-block cluster
-//   of S CTAs. The S partial tiles are summed through distributed shared
-//   memory, in rank order, so the result is run-to-run deterministic without
-//   atomics or a global partial buffer. While the MMAs run, the four
+//   128 experts x up to 256 tokens. With a single tile of tokens (decode), K
+//   is split over up to 16 independent CTAs that write fp32 partial tiles to
+//   the workspace, and pass 2 sums them in split order. With more tiles, K
+//   may be split over a thread-block cluster of S CTAs whose partial tiles
+//   are summed through distributed shared memory in rank order. Either way
+//   the sum has a fixed order, so the result is run-to-run deterministic
+//   without atomics. While the MMAs run, the four
 //   epilogue warps read the same shared-memory stages and accumulate the
 //   squared norms |x_t|^2 and |w_e|^2 needed by the error bound.
 // Pass 2, router_refine_kernel: one CTA per token.
@@ -53,6 +56,7 @@ constexpr int RT_SMEM = RT_BAR_OFF + 16 * RT_MAX_STAGES + 8 + 1024;
 constexpr int RT_THREADS = 192;
 constexpr int RT_RS = RT_MAX_BN + 4;       // row stride (floats) of the cluster-reduction tile
 constexpr int RT_MAX_SPLIT = 8;            // portable cluster size
+constexpr int RT_MAX_PART_SPLIT = 16;      // one tile of tokens: K split over independent CTAs
 constexpr int kWarpRefineMinT = 4096;  // from this many tokens on, one warp (not one CTA) per token (measured: T = 512 is faster with a CTA per token, T = 8192 with a warp)
 static_assert(RT_BM * RT_RS * 4 + RT_BM * 4 <= RT_BAR_OFF, "reduction tile must fit in the ring");
 // d = kBoundRel |x||w| + kBoundUlp |l~|: 2^-12 and 2^-21
@@ -61,6 +65,7 @@ constexpr float kBoundUlp = 4.76837158203125e-7f;
 
 struct RouterParams {
   int T, H, E, S, BN;
+  int partial;    // 1: the S CTAs of a K split write partial tiles lt[split][T][E], nw2[split][E]; no cluster
   int NS, stage;  // ring stages and bytes per stage (RT_A + BN * RT_KBYTES, a multiple of 4 KB)
   float* lt;     // [T][E] approximate logits (no bias)
   float* nw2;    // [E] |w_e|^2
@@ -90,7 +95,7 @@ __device__ __forceinline__ float row_sumsq(const uint8_t* row, int i, float a) {
   return a;
 }
 
-// grid (ceil(E/128), ceil(T/BN), S), cluster (1, 1, S), 192 threads. The tile
+// grid (ceil(E/128), ceil(T/BN), S), cluster (1, 1, S) (no cluster for partial tiles), 192 threads. The tile
 // is 128 experts (MMA M, TMEM lanes) x BN tokens (MMA N, TMEM columns).
 // warp 4: TMA producer; warp 5: MMA issuer; warps 0-3: norms, then epilogue.
 // Every CTA reaches both cluster barriers on every path: a bounded wait that
@@ -193,7 +198,9 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
 
   const int e_row = et * RT_BM + i;  // expert of TMEM lane / thread i (i < 128)
   const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-  if (S == 1) {
+  if (S == 1 || p.partial) {
+    float* lt = p.lt + (size_t)split * p.T * p.E;  // split is 0 without a K split
+    float* nw2 = p.nw2 + (size_t)split * p.E;
     if (warp < 4) {
       for (int c = 0; c < BN; c += 32) {
         float v[32];
@@ -203,11 +210,11 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
 #pragma unroll
           for (int q = 0; q < 32; ++q) {
             const int t = tt * BN + c + q;
-            if (t < p.T) p.lt[(size_t)t * p.E + e_row] = v[q];  // a warp stores 32 consecutive experts
+            if (t < p.T) lt[(size_t)t * p.E + e_row] = v[q];  // a warp stores 32 consecutive experts
           }
         }
       }
-      if (do_w && e_row < p.E) p.nw2[e_row] = sw;
+      if (do_w && e_row < p.E) nw2[e_row] = sw;
     }
   } else {
     // every CTA of the cluster parks its partial tile in its own (idle) ring memory
@@ -351,7 +358,11 @@ __device__ __forceinline__ int rank_among(const float* key, const int* list, int
 }
 
 // One CTA of 256 threads per token.
-__global__ void __launch_bounds__(256) router_refine_kernel(int H, int E, int k, const uint16_t* __restrict__ x,
+// part (null without a K split over independent CTAs): S partial logit tiles [S][T][E], then S partial norm
+// rows [S][E], summed here in split order.
+__global__ void __launch_bounds__(256) router_refine_kernel(int T, int H, int E, int k, int S,
+                                                            const float* __restrict__ part,
+                                                            const uint16_t* __restrict__ x,
                                                             const uint16_t* __restrict__ wr,
                                                             const float* __restrict__ bias,
                                                             const float* __restrict__ nw2, float* logits,
@@ -398,10 +409,34 @@ __global__ void __launch_bounds__(256) router_refine_kernel(int H, int E, int k,
   const float nx = sqrtf(nx2);
   float wmax = -INFINITY;  // this warp's largest lower end (a NaN never wins)
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    float l = __ldcg(lrow + e);
+    float l, nw;
+    if (part != nullptr) {  // every load in flight before the sums, which run in split order
+      const float* pl = part + (size_t)t * E + e;
+      const float* pn = part + (size_t)S * T * E + e;
+      float vl[RT_MAX_PART_SPLIT], vn[RT_MAX_PART_SPLIT];
+#pragma unroll
+      for (int s = 0; s < RT_MAX_PART_SPLIT; ++s) {
+        if (s < S) {
+          vl[s] = __ldcg(pl + (size_t)s * T * E);
+          vn[s] = __ldcg(pn + (size_t)s * E);
+        }
+      }
+      l = vl[0];
+      nw = vn[0];
+#pragma unroll
+      for (int s = 1; s < RT_MAX_PART_SPLIT; ++s) {
+        if (s < S) {
+          l += vl[s];
+          nw += vn[s];
+        }
+      }
+    } else {
+      l = __ldcg(lrow + e);
+      nw = __ldcg(nw2 + e);
+    }
     if (bias != nullptr) l = __fadd_rn(l, bias[e]);
     // the fp32 norms are low by at most ~3e-4 relative: the (1 + 2^-10) factor keeps the bound above it
-    const float d = fmaf(kBoundRel * 1.0009765625f, nx * sqrtf(__ldcg(nw2 + e)), kBoundUlp * fabsf(l));
+    const float d = fmaf(kBoundRel * 1.0009765625f, nx * sqrtf(nw), kBoundUlp * fabsf(l));
     const float lo = __fsub_rd(l, d);
     s_l[e] = l;
     s_lo[e] = lo;
@@ -726,9 +761,16 @@ bool configure_router() {
 
 }  // namespace
 
+// Enough for every T <= min(max_tokens, 256) (a single tile of tokens), so the split chosen below depends only
+// on T, E and H, never on the buffer.
+size_t router_partial_bytes(const fp4moe_config& cfg) {
+  const size_t Tt = (size_t)std::min(cfg.max_tokens, RT_MAX_BN);
+  return (size_t)RT_MAX_PART_SPLIT * (Tt + 1) * (size_t)cfg.num_experts * 4;
+}
+
 fp4moe_status router_topk_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const uint16_t* wr,
-                                 const float* bias, float* logits, float* nw2, int32_t* ids, float* w, uint32_t* err,
-                                 cudaStream_t st) {
+                                 const float* bias, float* logits, float* nw2, float* part, size_t part_bytes,
+                                 int32_t* ids, float* w, uint32_t* err, cudaStream_t st) {
   if (T == 0) return FP4MOE_OK;
   const int H = cfg.hidden, E = cfg.num_experts, k = cfg.top_k;
   if (!configure_router()) return FP4MOE_CUDA_ERROR;
@@ -739,9 +781,21 @@ fp4moe_status router_topk_launch(const fp4moe_config& cfg, int32_t T, const uint
   const int n_et = (E + RT_BM - 1) / RT_BM, n_tt = (T + BN - 1) / BN;
   const int nsm = sm_count();
   if (nsm <= 0) return FP4MOE_CUDA_ERROR;
-  // split K over a cluster while the tiles alone leave SMs idle, keeping at least 2 K atoms per split
+  // One tile of tokens: split K over up to 16 independent CTAs with at least 4 K atoms each, whose partial
+  // tiles the refine sums. Otherwise split K over a cluster while the tiles alone leave SMs idle, keeping at
+  // least 2 K atoms per split, and sum through distributed shared memory.
   int S = 1;
-  while (S * 2 <= RT_MAX_SPLIT && n_et * n_tt * S * 2 <= nsm && (H / 64) >= 4 * S) S *= 2;
+  bool partial = false;
+  if (n_tt == 1 && part != nullptr) {
+    while (S * 2 <= RT_MAX_PART_SPLIT && n_et * S * 2 <= nsm && (H / 64) >= 4 * S * 2 &&
+           (size_t)S * 2 * ((size_t)T + 1) * E * 4 <= part_bytes)
+      S *= 2;
+    partial = S > 1;
+  }
+  if (!partial) {
+    S = 1;
+    while (S * 2 <= RT_MAX_SPLIT && n_et * n_tt * S * 2 <= nsm && (H / 64) >= 4 * S) S *= 2;
+  }
   RouterParams prm;
   prm.T = T;
   prm.H = H;
@@ -750,8 +804,9 @@ fp4moe_status router_topk_launch(const fp4moe_config& cfg, int32_t T, const uint
   prm.BN = BN;
   prm.stage = RT_A + BN * RT_KBYTES;
   prm.NS = RT_BAR_OFF / prm.stage < RT_MAX_STAGES ? RT_BAR_OFF / prm.stage : RT_MAX_STAGES;
-  prm.lt = logits;
-  prm.nw2 = nw2;
+  prm.partial = partial ? 1 : 0;
+  prm.lt = partial ? part : logits;
+  prm.nw2 = partial ? part + (size_t)S * T * E : nw2;
   prm.err = err;
 
   cudaLaunchConfig_t lc = {};
@@ -765,14 +820,14 @@ fp4moe_status router_topk_launch(const fp4moe_config& cfg, int32_t T, const uint
   attr[1].id = cudaLaunchAttributeClusterDimension;
   attr[1].val.clusterDim.x = 1;
   attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = S;
+  attr[1].val.clusterDim.z = partial ? 1 : S;
   lc.attrs = attr;
   lc.numAttrs = 2;
   if (cudaLaunchKernelEx(&lc, router_mma_kernel, tmX, tmW, prm) != cudaSuccess) return FP4MOE_CUDA_ERROR;
   cudaError_t r;
   if (T < kWarpRefineMinT) {  // latency-bound: one CTA per token spreads its exact dot products over 8 warps
-    r = launch_pdl(router_refine_kernel, dim3(T), dim3(256), 0, st, H, E, k, x, wr, bias, (const float*)nw2, logits,
-                   ids, w, err);
+    r = launch_pdl(router_refine_kernel, dim3(T), dim3(256), 0, st, (int)T, H, E, k, partial ? S : 1,
+                   partial ? (const float*)part : nullptr, x, wr, bias, (const float*)nw2, logits, ids, w, err);
   } else {
     const int maxv = (E + 31) / 32;
     const float* cnw2 = nw2;

@@ -232,8 +232,9 @@ fp4moe_status moe_route(const fp4moe_config* cfg, int32_t T, const uint16_t* x, 
  * no cudaMalloc, no cudaFree, no allocating library routine.
  *
  * Its outputs and their meaning are those of moe_route, computed by the same
- * kernels. What moe_route keeps in `ws` (the per-chunk expert histograms and
- * the squared norms of the router rows) lives here in one
+ * kernels. What moe_route keeps in `ws` (the per-chunk expert histograms, the
+ * squared norms of the router rows and, for T <= 256, the router's partial
+ * logit tiles of a split K) lives here in one
  * library-owned scratch array in device memory, a file-scope __device__
  * array of FP4MOE_NOALLOC_SCRATCH_BYTES bytes in the library image. The array
  * bounds the sizes:
@@ -262,7 +263,7 @@ fp4moe_status moe_route(const fp4moe_config* cfg, int32_t T, const uint16_t* x, 
  */
 #define FP4MOE_NOALLOC_MAX_TOKENS 8192
 #define FP4MOE_NOALLOC_MAX_EXPERTS 256
-#define FP4MOE_NOALLOC_SCRATCH_BYTES (256 + 4 * 256 + 4 * 256 * (8192 / 64))
+#define FP4MOE_NOALLOC_SCRATCH_BYTES (256 + 4 * 256 + 4 * 256 * (8192 / 64) + 16 * 257 * 4 * 256)
 fp4moe_status moe_route_noalloc(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const uint16_t* router_w,
                                 const float* router_bias, float* logits_out, int32_t* topk_ids, float* topk_w,
                                 int32_t* counts, int32_t* offsets, int32_t* padded_offsets, int32_t* slot_of_pair,
