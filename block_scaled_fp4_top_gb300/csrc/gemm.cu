@@ -84,7 +84,7 @@ constexpr int BAR_OFF = STAGES * STAGE_BYTES;
 constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;    // barriers + 1024-byte alignment slack
 constexpr int NCOPY = 2;       // scale-copier warps: each tcgen05.cp holds its issuing thread, so they share a stage
 constexpr int THREADS = 192 + 32 * NCOPY;  // 4 epilogue warps, producer, MMA issuer, scale copiers
-constexpr int PREFETCH = 6;         // ring stages pulled into L2 ahead of the ring
+constexpr int PREFETCH = 2;         // ring stages pulled into L2 ahead of the ring (measured: 1-2 best, 6 costs 4 %)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 128;  // one accumulator: 128 fp32 columns
 constexpr uint32_t SFB_STAGE_COLS = 4 * ATOMS;  // B scales of one ring stage
