@@ -48,13 +48,29 @@ __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float*
   const int col = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
   if (col >= H) return;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int j = 0; j < k; ++j) {
-    if (slot_of_pair != nullptr && __ldcg(slot_of_pair + (size_t)t * k + j) < 0) continue;  // not held here
-    const float wj = __ldcg(w + (size_t)t * k + j);
-    float v[8];
-    ld8_cg<V8>(o + ((size_t)t * k + j) * H + col, v);
+  // the token's k weights and slots first, then the rows of up to 8 pairs at a time, all in flight before
+  // the sums, which run in pair order; a pair held by no local expert has no row and is skipped
+  float wj[kMaxTopK];
+  bool held[kMaxTopK];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
+  for (int j = 0; j < kMaxTopK; ++j) {
+    held[j] = j < k && (slot_of_pair == nullptr || __ldcg(slot_of_pair + (size_t)t * k + j) >= 0);
+    wj[j] = j < k ? __ldcg(w + (size_t)t * k + j) : 0.0f;
+  }
+#pragma unroll
+  for (int j0 = 0; j0 < kMaxTopK; j0 += 8) {
+    if (j0 >= k) break;
+    float v[8][8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj)
+      if (held[j0 + jj]) ld8_cg<V8>(o + ((size_t)t * k + j0 + jj) * H + col, v[jj]);
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      if (held[j0 + jj]) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[j0 + jj], v[jj][i], acc[i]);
+      }
+    }
   }
   if (o_shared != nullptr) {  // the shared expert, weight 1, after the routed terms
     float v[8];

@@ -419,11 +419,13 @@ __global__ void __launch_bounds__(256) scatter_rows_bf16_kernel(int H, int k, co
   const int t = blockIdx.y;
   const int c = blockIdx.x * blockDim.x + threadIdx.x;  // 16-byte chunk
   if (c >= H / 8) return;
+  int s[kMaxTopK];  // the k slots and the chunk are all loaded before the first store
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) s[j] = j < k ? __ldcg(slot_of_pair + (size_t)t * k + j) : -1;
   const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + c);
-  for (int j = 0; j < k; ++j) {
-    const int s = __ldcg(slot_of_pair + (size_t)t * k + j);
-    if (s >= 0) reinterpret_cast<uint4*>(a1 + (size_t)s * H)[c] = v;  // -1: held by no local expert
-  }
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j)
+    if (s[j] >= 0) reinterpret_cast<uint4*>(a1 + (size_t)s[j] * H)[c] = v;  // -1: held by no local expert
 }
 
 }  // namespace

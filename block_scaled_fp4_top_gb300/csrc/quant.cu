@@ -29,6 +29,10 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(int T, int H, int k,
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (int64_t)T * C) return;
   const int t = (int)(i / C), b = (int)(i - (int64_t)t * C);
+  // every load is issued before the first use: the token's k slots, the global scale and the block
+  int rows[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) rows[j] = j < k ? __ldcg(slot_of_pair + (size_t)t * k + j) : -1;
   const float g = __ldg(gs1);
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H) + 2 * b;
   const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
@@ -37,9 +41,10 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(int T, int H, int k,
                        bf16_lo(u1.z), bf16_hi(u1.z), bf16_lo(u1.w), bf16_hi(u1.w)};
   uint32_t lo, hi;
   const uint32_t sf = quant_block16(v, g, lo, hi);
-  for (int j = 0; j < k; ++j) {
-    const int row = __ldcg(slot_of_pair + (size_t)t * k + j);
-    if (row < 0) continue;  // held by no local expert
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    const int row = rows[j];
+    if (row < 0) continue;  // past k, or held by no local expert
     *reinterpret_cast<uint2*>(a1 + (size_t)row * (H >> 1) + b * 8) = make_uint2(lo, hi);
     a1_sf[sf_offset(row, b, C)] = (uint8_t)sf;
   }
