@@ -47,7 +47,7 @@ FALLBACK_HBM_GBS = 6800.0
 # with, so it is reported while their hash matches and as null otherwise.
 W1_TRAFFIC = {
     # workload name: (bytes per launch, sha256 of the GEMM sources)
-    "dsv4_flash_decode_T64": (1957580800 + 3746816, "35e06267dd4a688a3c5ba7b086940cda6366c4be81b0b7d8d794ed88d960f49b"),
+    "dsv4_flash_decode_T64": (1949501184 + 3749888, "82922fc62bf52307e5b8132cfa640783a76ade7c2f51e42f0d053666816d26bd"),
 }
 GEMM_SOURCES = ("block_scaled_fp4_top_gb300/csrc/gemm.cu", "block_scaled_fp4_top_gb300/csrc/common.cuh")
 
