@@ -13,6 +13,9 @@
 #include "internal.h"
 
 namespace fp4moe {
+
+int sm_count();
+
 namespace {
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -36,7 +39,11 @@ __device__ __forceinline__ void ld8_cg(const float* p, float (&v)[8]) {
   }
 }
 
-template <bool V8>
+// BATCH: a grid of one wave (decode). The token's k weights and slots are loaded first, then the rows of up
+// to 8 pairs at a time, all in flight before the sums. Otherwise many waves (prefill) keep the memory system
+// busy instead, and a lean loop keeps more CTAs resident. Either way the sum runs in pair order and a pair
+// held by no local expert (it has no row) is skipped.
+template <bool V8, bool BATCH>
 __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float* __restrict__ o,
                                                       const float* __restrict__ w,
                                                       const int32_t* __restrict__ slot_of_pair,
@@ -48,27 +55,36 @@ __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float*
   const int col = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
   if (col >= H) return;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  // the token's k weights and slots first, then the rows of up to 8 pairs at a time, all in flight before
-  // the sums, which run in pair order; a pair held by no local expert has no row and is skipped
-  float wj[kMaxTopK];
-  bool held[kMaxTopK];
+  if constexpr (!BATCH) {
+    for (int j = 0; j < k; ++j) {
+      if (slot_of_pair != nullptr && __ldcg(slot_of_pair + (size_t)t * k + j) < 0) continue;
+      const float wj = __ldcg(w + (size_t)t * k + j);
+      float v[8];
+      ld8_cg<V8>(o + ((size_t)t * k + j) * H + col, v);
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    held[j] = j < k && (slot_of_pair == nullptr || __ldcg(slot_of_pair + (size_t)t * k + j) >= 0);
-    wj[j] = j < k ? __ldcg(w + (size_t)t * k + j) : 0.0f;
-  }
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
+    }
+  } else {
+    float wj[kMaxTopK];
+    bool held[kMaxTopK];
 #pragma unroll
-  for (int j0 = 0; j0 < kMaxTopK; j0 += 8) {
-    if (j0 >= k) break;
-    float v[8][8];
+    for (int j = 0; j < kMaxTopK; ++j) {
+      held[j] = j < k && (slot_of_pair == nullptr || __ldcg(slot_of_pair + (size_t)t * k + j) >= 0);
+      wj[j] = j < k ? __ldcg(w + (size_t)t * k + j) : 0.0f;
+    }
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj)
-      if (held[j0 + jj]) ld8_cg<V8>(o + ((size_t)t * k + j0 + jj) * H + col, v[jj]);
+    for (int j0 = 0; j0 < kMaxTopK; j0 += 8) {
+      if (j0 >= k) break;
+      float v[8][8];
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      if (held[j0 + jj]) {
+      for (int jj = 0; jj < 8; ++jj)
+        if (held[j0 + jj]) ld8_cg<V8>(o + ((size_t)t * k + j0 + jj) * H + col, v[jj]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[j0 + jj], v[jj][i], acc[i]);
+      for (int jj = 0; jj < 8; ++jj) {
+        if (held[j0 + jj]) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[j0 + jj], v[jj][i], acc[i]);
+        }
       }
     }
   }
@@ -91,13 +107,21 @@ fp4moe_status combine_launch(const fp4moe_config& cfg, int32_t T, const float* o
   const int H = cfg.hidden;
   // 256-bit loads when every row start is 32-byte aligned (H is a multiple of 256)
   const bool v8 = ((reinterpret_cast<uintptr_t>(o_pairs) | reinterpret_cast<uintptr_t>(o_shared)) & 31u) == 0;
-  return (v8 ? launch_pdl(combine_kernel<true>, dim3((H / 8 + 255) / 256, T), dim3(256), 0, st, H, cfg.top_k, o_pairs,
-                          w, slot_of_pair, o_shared, y)
-             : launch_pdl(combine_kernel<false>, dim3((H / 8 + 255) / 256, T), dim3(256), 0, st, H, cfg.top_k,
-                          o_pairs, w, slot_of_pair, o_shared, y)) ==
-                 cudaSuccess
-             ? FP4MOE_OK
-             : FP4MOE_CUDA_ERROR;
+  const dim3 grid((H / 8 + 255) / 256, T);
+  const bool batch = (int64_t)grid.x * grid.y <= sm_count();  // one wave: latency rules
+  cudaError_t r;
+  if (v8) {
+    r = batch ? launch_pdl(combine_kernel<true, true>, grid, dim3(256), 0, st, H, cfg.top_k, o_pairs, w, slot_of_pair,
+                           o_shared, y)
+              : launch_pdl(combine_kernel<true, false>, grid, dim3(256), 0, st, H, cfg.top_k, o_pairs, w,
+                           slot_of_pair, o_shared, y);
+  } else {
+    r = batch ? launch_pdl(combine_kernel<false, true>, grid, dim3(256), 0, st, H, cfg.top_k, o_pairs, w,
+                           slot_of_pair, o_shared, y)
+              : launch_pdl(combine_kernel<false, false>, grid, dim3(256), 0, st, H, cfg.top_k, o_pairs, w,
+                           slot_of_pair, o_shared, y);
+  }
+  return r == cudaSuccess ? FP4MOE_OK : FP4MOE_CUDA_ERROR;
 }
 
 }  // namespace fp4moe
