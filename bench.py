@@ -405,52 +405,71 @@ def run_ours(args, wl, rank, world):
     return out
 
 
-def oracle_sample_time(wl, n_tokens: int, repeats: int = 1):
-    """The oracle, as it stands, on the first n_tokens of the evaluation batch. Returns (tokens/s, seconds)."""
-    import dataclasses
-    from oracle import moe, mxfp4
-    x = sg.activations_bf16(wl, sg.EVAL_SEED, T=n_tokens)
-    wr = sg.router_bf16(wl)
-    bias = sg.router_bias_f32(wl)
-    ids, w = moe.topk_softmax(moe.router_logits(x, wr, bias), wl.k)
-    cache = {}
-    mx = wl.w_format == 1
-    full = dataclasses.replace(wl, I=2048, I_logical=2048)
-    plan = mxfp4.tp_plan(2048, 3, 32, 128)
+class OracleSample:
+    """The oracle, as it stands, on the first n_tokens of the evaluation batch.
 
-    def expert(e):
-        if e not in cache:
-            if mx:   # rank 0 of the TP3 shard, as the GPU arm runs it
-                cache[e] = mxfp4.mx_expert_shard(sg.expert_w1_f32(full, e), sg.expert_w2_f32(full, e), plan, 0)
+    The expert weights those tokens route to are quantised once, here: that is load time, outside every
+    timed region. run(rows) then times the oracle's layer on those token rows (routing, experts, combine).
+    """
+
+    def __init__(self, wl, n_tokens: int):
+        import dataclasses
+        from oracle import moe, mxfp4
+        self.wl, self.n = wl, n_tokens
+        self.x = sg.activations_bf16(wl, sg.EVAL_SEED, T=n_tokens)
+        self.wr = sg.router_bf16(wl)
+        self.bias = sg.router_bias_f32(wl)
+        ids, _ = moe.topk_softmax(moe.router_logits(self.x, self.wr, self.bias), wl.k)
+        self.cache = {}
+        self.mx = wl.w_format == 1
+        self.full = dataclasses.replace(wl, I=2048, I_logical=2048)
+        self.plan = mxfp4.tp_plan(2048, 3, 32, 128)
+        for e in np.unique(ids):
+            if not wl.ep_count or wl.ep_first <= e < wl.ep_first + wl.ep_count:
+                self.expert(int(e))
+        self.shared = None
+        if wl.shared_I:
+            from oracle import fp8block
+            self.shared = fp8block.quantize_shared(sg.shared_w1_f32(wl), sg.shared_w2_f32(wl))
+        # the timing needs plausible global scales, not calibrated ones: take gs1 from the sample's amax
+        self.gs1 = np.float32(2688.0) / np.float32(np.abs(sg.bf16_bits_to_f32(self.x)).max())
+        self.gs2 = np.float32(2688.0 / 100.0)
+
+    def expert(self, e: int):
+        from oracle import moe, mxfp4
+        if e not in self.cache:
+            wl = self.wl
+            if self.mx:   # rank 0 of the TP3 shard, as the GPU arm runs it
+                self.cache[e] = mxfp4.mx_expert_shard(sg.expert_w1_f32(self.full, e), sg.expert_w2_f32(self.full, e),
+                                                      self.plan, 0)
             else:
-                cache[e] = moe.quantize_expert(sg.expert_w1_f32(wl, e), sg.expert_w2_f32(wl, e))
-        return cache[e]
+                self.cache[e] = moe.quantize_expert(sg.expert_w1_f32(wl, e), sg.expert_w2_f32(wl, e))
+        return self.cache[e]
 
-    for e in np.unique(ids):   # weight prep is load time, outside the timed region
-        if not wl.ep_count or wl.ep_first <= e < wl.ep_first + wl.ep_count:
-            expert(int(e))
-    shared = None
-    if wl.shared_I:
-        from oracle import fp8block
-        shared = fp8block.quantize_shared(sg.shared_w1_f32(wl), sg.shared_w2_f32(wl))
-    # the timing needs plausible global scales, not calibrated ones: take gs1 from this sample's amax
-    gs1 = np.float32(2688.0) / np.float32(np.abs(sg.bf16_bits_to_f32(x)).max())
-    gs2 = np.float32(2688.0 / 100.0)
-    t0 = time.perf_counter()
-    for _ in range(repeats):
-        l = moe.router_logits(x, wr, bias)
+    def run(self, rows) -> float:
+        from oracle import fp8block, moe, mxfp4
+        wl, x = self.wl, self.x[rows]
+        t0 = time.perf_counter()
+        l = moe.router_logits(x, self.wr, self.bias)
         ids, w = moe.topk_softmax(l, wl.k)
-        if mx:
-            mxfp4.mx_moe_tokens(x, ids, w, expert, wl.swiglu_limit)
+        if self.mx:
+            mxfp4.mx_moe_tokens(x, ids, w, self.expert, wl.swiglu_limit)
         else:
-            o_se = None if shared is None else fp8block.shared_out(x, shared, wl.swiglu_limit)
+            o_se = None if self.shared is None else fp8block.shared_out(x, self.shared, wl.swiglu_limit)
             if wl.ep_count:   # one rank's share: local ids, pairs held elsewhere masked
                 from oracle import layout
                 moe.moe_tokens(x, layout.local_ids(ids, wl.ep_first, wl.ep_count), w,
-                               lambda l: expert(wl.ep_first + l), gs1, gs2, wl.swiglu_limit, shared=o_se)
+                               lambda le: self.expert(wl.ep_first + le), self.gs1, self.gs2, wl.swiglu_limit,
+                               shared=o_se)
             else:
-                moe.moe_tokens(x, ids, w, expert, gs1, gs2, wl.swiglu_limit, shared=o_se)
-    dt = time.perf_counter() - t0
+                moe.moe_tokens(x, ids, w, self.expert, self.gs1, self.gs2, wl.swiglu_limit, shared=o_se)
+        return time.perf_counter() - t0
+
+
+def oracle_sample_time(wl, n_tokens: int, repeats: int = 1):
+    """The oracle on the first n_tokens of the evaluation batch, repeats times. Returns (tokens/s, seconds)."""
+    sample = OracleSample(wl, n_tokens)
+    dt = sum(sample.run(slice(0, n_tokens)) for _ in range(repeats))
     return n_tokens * repeats / dt, dt
 
 
@@ -475,6 +494,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=sg.DSV4_DECODE.name, choices=sorted(sg.WORKLOADS))
     ap.add_argument("--oracle-tokens", type=int, default=2)
+    ap.add_argument("--reference-budget", type=float, default=60.0,
+                    help="--impl reference: stop timing oracle steps once they took this many seconds")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--experts", type=int, default=0,
                     help="override E (smaller case for profiler captures; the default is the workload's E)")
@@ -492,20 +513,29 @@ def main():
         if rank != 0:
             return
         cores, model = cpu_info()
+        # Each step is the oracle on one token of a fixed pool (the batch's first --oracle-tokens tokens, their
+        # experts prepared once, untimed). The oracle takes seconds per token, so the run stops once the timed
+        # steps pass --reference-budget seconds, or after --steps, whichever comes first, and reports how many
+        # steps it timed; warm-up is at most one step (the oracle has nothing to warm up).
+        sample = OracleSample(wl, args.oracle_tokens)
+        n_warm = min(args.warmup, 1)
+        for i in range(n_warm):
+            sample.run([i % sample.n])
         per_step = []
-        for _ in range(args.steps):
-            v, dt = oracle_sample_time(wl, args.oracle_tokens)
-            per_step.append(dt)
-        tokens = args.oracle_tokens * args.steps
-        val = tokens / sum(per_step)
+        while len(per_step) < max(args.steps, 1) and sum(per_step) < args.reference_budget:
+            per_step.append(sample.run([len(per_step) % sample.n]))
+        steps = len(per_step)
+        val = steps / sum(per_step)
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(per_step) / args.steps,
+            "steps": steps, "steps_requested": args.steps, "warmup": n_warm, "warmup_requested": args.warmup,
+            "reference_budget_s": args.reference_budget, "ms_per_step": 1e3 * sum(per_step) / steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
             "data": "synthetic", "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
                                             "top_k": wl.k},
             "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": f"{args.oracle_tokens} tokens of the {wl.name} batch per step ({model})"},
+                             "sample": f"one token per step, cycling over the first {args.oracle_tokens} tokens of "
+                                       f"the {wl.name} batch; {steps} steps timed ({model})"},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }))
         return

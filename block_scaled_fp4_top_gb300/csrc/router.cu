@@ -368,8 +368,6 @@ __global__ void __launch_bounds__(256) router_refine_kernel(int T, int H, int E,
                                                             const float* __restrict__ nw2, float* logits,
                                                             int32_t* __restrict__ ids_out,
                                                             float* __restrict__ w_out, uint32_t* err) {
-  pdl_wait();
-  pdl_trigger();
   __shared__ uint4 s_x[kMaxChunksPerLane * 32];
   __shared__ float s_l[kMaxExperts];
   __shared__ float s_lo[kMaxExperts];
@@ -385,7 +383,9 @@ __global__ void __launch_bounds__(256) router_refine_kernel(int T, int H, int E,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunks = H / 8;
   float* lrow = logits + (size_t)t * E;
-  // the token row goes to shared memory once; its squared norm is a fixed-order block sum
+  // The token row goes to shared memory once; its squared norm is a fixed-order block sum. x is the
+  // layer's input: router_mma, the launch this one follows, began only after whatever wrote x had
+  // finished, so x is read before the wait on router_mma.
   const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
   float sq = 0.0f;
   for (int c = threadIdx.x; c < nchunks; c += blockDim.x) {
@@ -393,6 +393,8 @@ __global__ void __launch_bounds__(256) router_refine_kernel(int T, int H, int E,
     s_x[c] = v;
     sq = sumsq8(v, sq);
   }
+  pdl_wait();  // the partial tiles, logits and norms of router_mma from here on
+  pdl_trigger();
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(kFull, sq, off);
   if (lane == 0) s_part[warp] = sq;
