@@ -13,7 +13,7 @@ What the pages fix:
   ("DSV4 -> vLLM: CUDA-Graph Safety / GPU-Native Requirements", Graph B:
   "Router + MoE + SE").
 
-Readings where the pages stop (each is listed in the design doc):
+Readings where the pages stop:
 * Block-FP8 is E4M3 with one fp32 scale per block: 128 x 128 blocks for
   weights and 1 x 128 groups along K for activations. This is the recipe of
   the DeepSeek-V3 technical report (section 3.3, "FP8 training"). The 128

@@ -20,7 +20,7 @@ The oracle states this per token. It does not scatter, pad or tile:
       o_e    = W2~_e h~
   y_t   = bf16( sum_{j = 0..k-1} w_t,j * o_{e_j} )  (in j order)
 
-Readings where the pages are silent (each one is listed in the design doc):
+Readings where the pages are silent:
 * The clamp form. "Lucifer-CUTLASS TP3 virtual-padding audit", section
   "TP3 shape plan", gives only swiglu_limit = 10. Reading: the gate is clamped
   above at +L and the up projection is clamped to [-L, L].
