@@ -1,7 +1,8 @@
 """GPU: moe_route_noalloc, the workspace-free routing call, against moe_route.
 
-moe_route_noalloc keeps its histograms and arrival counters in one scratch
-array owned by the library instead of a caller workspace. Its outputs must
+moe_route_noalloc keeps its histograms, router-row norms and partial router
+tiles in one scratch array owned by the library instead of a caller
+workspace. Its outputs must
 match those of moe_route on the same inputs. Here that holds for two calls in
 a row, and again after a call of the other layout path (a small T and a large
 T), because the second call finds the scratch as the first call left it. The
