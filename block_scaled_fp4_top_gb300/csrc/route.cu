@@ -113,12 +113,6 @@ __device__ __forceinline__ void offsets_and_pads(int E, int cap, int c, int* s_w
   __syncthreads();
 }
 
-// Decode-sized layout in kSmallParts CTAs of 1024 threads: each builds the
-// whole histogram, offsets and slot ranks (a few thousand pairs at most) and
-// writes only the rows of its own slice, so no CTA waits for another and no
-// row has two writers. Slots run in ascending pair order. Each warp walks its own contiguous chunk
-// of pairs 32 at a time from its chunk's per-expert base; lanes sharing an
-// expert rank themselves by lane order.
 // Local expert of global id g: g - first for the experts [first, first + E) this layer holds, -1 for an
 // expert held elsewhere (its pair is masked out, "Bug 8"), -2 for an id outside [0, Eg) (an error).
 __device__ __forceinline__ int local_expert(int g, int Eg, int first, int E) {
@@ -127,6 +121,12 @@ __device__ __forceinline__ int local_expert(int g, int Eg, int first, int E) {
   return (l >= 0 && l < E) ? l : -1;
 }
 
+// Decode-sized layout in kSmallParts CTAs of 1024 threads: each builds the
+// whole histogram, offsets and slot ranks (a few thousand pairs at most) and
+// writes only the rows of its own slice, so no CTA waits for another and no
+// row has two writers. Slots run in ascending pair order. Each warp walks its own contiguous chunk
+// of pairs 32 at a time from its chunk's per-expert base; lanes sharing an
+// expert rank themselves by lane order.
 __global__ void __launch_bounds__(1024) layout_small_kernel(int npairs, int Eg, int first, int E, int cap,
                                                             const int32_t* __restrict__ ids,
                                                             int32_t* __restrict__ counts,
