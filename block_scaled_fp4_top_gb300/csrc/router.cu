@@ -449,8 +449,9 @@ __global__ void __launch_bounds__(256) router_refine_kernel(int T, int H, int E,
   for (int off = 16; off > 0; off >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(kFull, wmax, off));
   if (lane == 0) s_wmax[warp] = wmax;
   __syncthreads();
-  // theta <= tau: the k-th largest of the eight warp maxima. Each is the lower end of a different expert (or
-  // -inf for a warp without a number), so k experts reach theta and the k-th largest lower end does too.
+  // theta <= tau: the k-th largest of the eight warp maxima. Each is the lower end of a different expert, so
+  // when theta is a number at least k experts reach it, and so does the k-th largest lower end. A warp with
+  // no number has the maximum -inf; if theta is -inf, every expert whose lower end is a number is kept.
   float theta = -INFINITY;
   if (k <= 8) {
     const int q0 = lane & 7;
