@@ -48,6 +48,25 @@ def test_topk_ties_go_to_lower_expert():
     assert list(ids[0]) == [0, 1]  # -0 == +0
 
 
+def test_topk_ranks_nan_below_every_number():
+    """Brute force on small rows of numbers, +-0, +-inf and NaN: the k picks are the first k of the order
+    (NaN after every number, -inf included; then value descending; then the lower id), so a NaN logit is
+    picked only when fewer than k numbers exist."""
+    rng = np.random.default_rng(7)
+    pool = np.array([np.nan, np.inf, -np.inf, 0.0, -0.0, 1.0, -1.0, 2.5], dtype=np.float32)
+    for _ in range(400):
+        E = int(rng.integers(3, 9))
+        k = int(rng.integers(1, E + 1))
+        l = rng.choice(pool, size=(1, E)).astype(np.float32)
+        def key(e):
+            v = l[0, e]
+            return (bool(np.isnan(v)), 0.0 if np.isnan(v) else -float(v), e)
+        order = sorted(range(E), key=key)
+        with np.errstate(invalid="ignore", over="ignore"):  # the weights of such rows are not checked here
+            ids, _ = moe.topk_softmax(l, k)
+        assert list(ids[0]) == order[:k], (l, k)
+
+
 def test_swiglu_clamp_against_torch_silu():
     g = np.array([-50, -3, 0, 2.5, 9.99, 10, 11, 1e4])
     u = np.array([-1e3, -10, -9.5, 0, 3, 10, 10.5, 50])
