@@ -13,7 +13,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfp4moe.s
 c_i32, c_u32, c_f32, c_sz, c_vp = ctypes.c_int32, ctypes.c_uint32, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
 
 OK, INVALID_ARG, MISALIGNED, CAPACITY, UNSUPPORTED, CUDA_ERROR = range(6)
-ERR_TIMEOUT, ERR_EXPERT_ID, ERR_CAPACITY = 0x1, 0x2, 0x4
+ERR_TIMEOUT, ERR_EXPERT_ID, ERR_CAPACITY, ERR_NAN = 0x1, 0x2, 0x4, 0x8
+SAT_L1, SAT_L2 = 0x1, 0x2
 W_NVFP4, W_MXFP4 = 0, 1
 
 
@@ -54,6 +55,8 @@ SIGNATURES = {
     "fp4moe_selftest_wait_timeout": (c_i32, [c_vp, ctypes.c_int64, c_vp, c_vp]),
     "fp4moe_batch_gs1": (c_i32, [CP, c_i32] + [c_vp] * 6),
     "fp4moe_read_error": (c_i32, [c_vp, ctypes.POINTER(c_u32), c_i32, c_vp]),
+    "fp4moe_read_scale_status": (c_i32, [c_vp, ctypes.POINTER(c_u32), ctypes.POINTER(c_f32), c_i32, c_vp]),
+    "fp4moe_refresh_gs2": (c_i32, [CP] + [c_vp] * 5),
     "fp4moe_shared_weight_bytes": (c_i32, [CP, ctypes.POINTER(c_sz), ctypes.POINTER(c_sz), ctypes.POINTER(c_sz),
                                            ctypes.POINTER(c_sz)]),
     "fp4moe_shared_quantize_weights": (c_i32, [CP, c_i32] + [c_vp] * 4),

@@ -196,6 +196,19 @@ def fp4moe_read_error(ws, clear=True, stream=None) -> int:
     return v.value
 
 
+def fp4moe_read_scale_status(ws, clear=True, stream=None):
+    """(FP4MOE_SAT_* flags, running amax|h| since the last gs2 refresh)."""
+    v, a = ctypes.c_uint32(), ctypes.c_float()
+    _check(_lib.load().fp4moe_read_scale_status(_p(ws), ctypes.byref(v), ctypes.byref(a), 1 if clear else 0,
+                                                _s(stream)), "fp4moe_read_scale_status")
+    return v.value, a.value
+
+
+def fp4moe_refresh_gs2(cfg, ws, gw2, gs2_inout, alpha2_out, stream=None):
+    _check(_lib.load().fp4moe_refresh_gs2(ctypes.byref(cfg), _p(ws), _p(gw2), _p(gs2_inout), _p(alpha2_out),
+                                          _s(stream)), "fp4moe_refresh_gs2")
+
+
 # --------------------------------------------------------------------------
 @dataclass
 class Weights:
@@ -307,3 +320,11 @@ class MoELayer:
 
     def read_error(self, clear=True) -> int:
         return fp4moe_read_error(self.ws, clear)
+
+    def read_scale_status(self, clear=True):
+        """(FP4MOE_SAT_* flags, running amax|h|) of this layer's workspace."""
+        return fp4moe_read_scale_status(self.ws, clear)
+
+    def refresh_gs2(self, stream=None):
+        """gs2 and alpha2 from the amax|h| of the calls since the last refresh (lagged, on the device)."""
+        fp4moe_refresh_gs2(self.cfg, self.ws, self.weights.gw2, self.gs2, self.alpha2, stream)

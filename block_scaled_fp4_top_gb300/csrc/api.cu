@@ -8,6 +8,7 @@
 // hidden host syncs, allocations and device-value branches that a captured
 // step must not contain.
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -76,6 +77,8 @@ Tp* at(void* ws, size_t off) {
   return reinterpret_cast<Tp*>(static_cast<uint8_t*>(ws) + off);
 }
 inline uint32_t* err_word(void* ws) { return at<uint32_t>(ws, kWsErr); }
+inline uint32_t* scale_flags(void* ws) { return at<uint32_t>(ws, kWsScaleFlags); }
+inline float* amax_h_run(void* ws) { return at<float>(ws, kWsAmaxHRun); }
 
 }  // namespace
 
@@ -143,22 +146,13 @@ static_assert(kScratchPart + kScratchPartBytes == FP4MOE_NOALLOC_SCRATCH_BYTES,
 
 __device__ __align__(256) uint8_t g_route_scratch[FP4MOE_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-uint8_t* g_scratch_ptr[kMaxDevices];
-
-// Device address of the scratch on the current device. The first request on
-// a device looks it up with cudaGetSymbolAddress; later ones reuse it.
+// Device address of the scratch in the current device's context, looked up on every call: the lookup allocates
+// nothing, and a fresh lookup stays right after the context is torn down and created again (the module is then
+// loaded again, possibly at another address).
 fp4moe_status route_scratch(uint8_t** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP4MOE_CUDA_ERROR;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) return FP4MOE_CUDA_ERROR;
-    g_scratch_ptr[dev] = static_cast<uint8_t*>(p);
-  }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) return FP4MOE_CUDA_ERROR;
+  *out = static_cast<uint8_t*>(p);
   return FP4MOE_OK;
 }
 }  // namespace
@@ -167,6 +161,7 @@ namespace {
 // The shared expert runs beside the routing and the routed experts: moe_forward_shared forks it onto a
 // library-owned stream and joins it back before the combine, with events. Each host thread gets its own side
 // stream and event pair per device (two threads never share an event), created on first use.
+constexpr int kMaxDevices = 64;
 struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
@@ -251,12 +246,12 @@ fp4moe_status forward_impl(const fp4moe_config* cfg, int32_t T, const uint16_t* 
       return mx_gemm_launch(true, *cfg, T, a2, poff, por, w2_fp4, w2_sf, nullptr, at<float>(ws, L.opairs), err, st);
     }
     FP4_TRY(quant_scatter_launch(*cfg, T, x, gs1, at<int32_t>(ws, L.slot), at<uint8_t>(ws, L.a1),
-                                 at<uint8_t>(ws, L.a1sf), st));
+                                 at<uint8_t>(ws, L.a1sf), scale_flags(ws), err, st));
     FP4_TRY(gemm_launch(kW1SwiGLU, *cfg, T, at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf), poff, por, w1_fp4, w1_sf,
-                        alpha1, gs2, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), nullptr, nullptr, err,
-                        at<int>(ws, kWsSchedW1), st));
+                        alpha1, gs2, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), amax_h_run(ws), scale_flags(ws),
+                        nullptr, err, at<int>(ws, kWsSchedW1), st));
     return gemm_launch(kW2Rows, *cfg, T, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), poff, por, w2_fp4, w2_sf,
-                       alpha2, nullptr, nullptr, nullptr, nullptr, at<float>(ws, L.opairs), err,
+                       alpha2, nullptr, nullptr, nullptr, nullptr, nullptr, at<float>(ws, L.opairs), err,
                        at<int>(ws, kWsSchedW2), st);
   };
   const fp4moe_status rr = routed();
@@ -374,7 +369,8 @@ fp4moe_status moe_quantize_scatter(const fp4moe_config* cfg, int32_t T, const ui
                                     (cudaStream_t)stream);
   }
   FP4_TRY(check_ptrs(x, gs1, slot_of_pair, a1_fp4, a1_sf, ws));
-  return quant_scatter_launch(*cfg, T, x, gs1, slot_of_pair, a1_fp4, a1_sf, (cudaStream_t)stream);
+  return quant_scatter_launch(*cfg, T, x, gs1, slot_of_pair, a1_fp4, a1_sf, scale_flags(ws), err_word(ws),
+                              (cudaStream_t)stream);
 }
 
 fp4moe_status moe_grouped_gemm_w1_swiglu(const fp4moe_config* cfg, int32_t T, const uint8_t* a1_fp4,
@@ -392,7 +388,8 @@ fp4moe_status moe_grouped_gemm_w1_swiglu(const fp4moe_config* cfg, int32_t T, co
   }
   FP4_TRY(check_ptrs(a1_fp4, a1_sf, padded_offsets, pair_of_row, w1_fp4, w1_sf, alpha1, gs2, a2_fp4, a2_sf, ws));
   return gemm_launch(kW1SwiGLU, *cfg, T, a1_fp4, a1_sf, padded_offsets, pair_of_row, w1_fp4, w1_sf, alpha1, gs2,
-                     a2_fp4, a2_sf, nullptr, nullptr, err_word(ws), at<int>(ws, kWsSchedW1), (cudaStream_t)stream);
+                     a2_fp4, a2_sf, amax_h_run(ws), scale_flags(ws), nullptr, err_word(ws), at<int>(ws, kWsSchedW1),
+                     (cudaStream_t)stream);
 }
 
 fp4moe_status moe_grouped_gemm_w2(const fp4moe_config* cfg, int32_t T, const uint8_t* a2_fp4, const uint8_t* a2_sf,
@@ -408,7 +405,8 @@ fp4moe_status moe_grouped_gemm_w2(const fp4moe_config* cfg, int32_t T, const uin
   }
   FP4_TRY(check_ptrs(a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, o_pairs, ws));
   return gemm_launch(kW2Rows, *cfg, T, a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, nullptr,
-                     nullptr, nullptr, nullptr, o_pairs, err_word(ws), at<int>(ws, kWsSchedW2), (cudaStream_t)stream);
+                     nullptr, nullptr, nullptr, nullptr, o_pairs, err_word(ws), at<int>(ws, kWsSchedW2),
+                     (cudaStream_t)stream);
 }
 
 fp4moe_status moe_combine(const fp4moe_config* cfg, int32_t T, const float* o_pairs, const float* topk_w,
@@ -438,7 +436,8 @@ fp4moe_status moe_grouped_gemm_w2_combine(const fp4moe_config* cfg, int32_t T, c
   }
   FP4_TRY(check_ptrs(a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, topk_w, y, ws));
   FP4_TRY(gemm_launch(kW2Rows, *cfg, T, a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, nullptr,
-                      nullptr, nullptr, nullptr, o, err_word(ws), at<int>(ws, kWsSchedW2), (cudaStream_t)stream));
+                      nullptr, nullptr, nullptr, nullptr, o, err_word(ws), at<int>(ws, kWsSchedW2),
+                      (cudaStream_t)stream));
   return combine_launch(*cfg, T, o, topk_w, nullptr, nullptr, y, (cudaStream_t)stream);
 }
 
@@ -559,12 +558,12 @@ fp4moe_status fp4moe_calibrate(const fp4moe_config* cfg, int32_t T, const uint16
                        at<int32_t>(ws, L.slot), por, at<int32_t>(ws, L.hist), at<float>(ws, L.nw2),
                        at<float>(ws, L.rt_part), router_partial_bytes(*cfg), err, st));
   FP4_TRY(quant_scatter_launch(*cfg, T, x_warm, gs1_out, at<int32_t>(ws, L.slot), at<uint8_t>(ws, L.a1),
-                               at<uint8_t>(ws, L.a1sf), st));
+                               at<uint8_t>(ws, L.a1sf), scale_flags(ws), err, st));
   float* alpha = at<float>(ws, L.alpha_tmp);
   FP4_TRY(make_alpha_launch(local_experts(*cfg), gs1_out, gw1, alpha, st));
   if (cudaMemsetAsync(amax_h, 0, 4, st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
   FP4_TRY(gemm_launch(kW1Amax, *cfg, T, at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf), poff, por, w1_fp4, w1_sf,
-                      alpha, nullptr, nullptr, nullptr, amax_h, nullptr, err, at<int>(ws, kWsSchedW1), st));
+                      alpha, nullptr, nullptr, nullptr, amax_h, nullptr, nullptr, err, at<int>(ws, kWsSchedW1), st));
   if (cudaMemcpyAsync(gs2_out, amax_h, 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
   return gs_from_amax_launch(1, gs2_out, st);
 }
@@ -604,6 +603,32 @@ fp4moe_status fp4moe_read_error(void* ws, uint32_t* err_host, int32_t clear, fp4
     if (cudaStreamSynchronize(st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
   }
   return FP4MOE_OK;
+}
+
+fp4moe_status fp4moe_read_scale_status(void* ws, uint32_t* flags_host, float* amax_h_host, int32_t clear,
+                                       fp4moe_stream_t stream) {
+  if (ws == nullptr || flags_host == nullptr) return FP4MOE_INVALID_ARG;
+  const cudaStream_t st = (cudaStream_t)stream;
+  uint32_t words[2] = {0u, 0u};  // the flags word and the running amax|h|, adjacent in the header
+  static_assert(kWsAmaxHRun == kWsScaleFlags + 4, "scale words are adjacent");
+  if (cudaMemcpyAsync(words, at<uint8_t>(ws, kWsScaleFlags), 8, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return FP4MOE_CUDA_ERROR;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
+  *flags_host = words[0];
+  if (amax_h_host != nullptr) memcpy(amax_h_host, &words[1], 4);
+  if (clear) {
+    if (cudaMemsetAsync(at<uint8_t>(ws, kWsScaleFlags), 0, 4, st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
+  }
+  return FP4MOE_OK;
+}
+
+fp4moe_status fp4moe_refresh_gs2(const fp4moe_config* cfg, void* ws, const float* gw2, float* gs2_inout,
+                                 float* alpha2_out, fp4moe_stream_t stream) {
+  FP4_TRY(check_cfg(cfg));
+  if (is_mx(cfg)) return FP4MOE_UNSUPPORTED;  // MXFP4 layers keep bf16 activations: no global scales
+  FP4_TRY(check_ptrs(ws, gw2, gs2_inout, alpha2_out));
+  return refresh_gs2_launch(local_experts(*cfg), amax_h_run(ws), gw2, gs2_inout, alpha2_out, (cudaStream_t)stream);
 }
 
 }  // extern "C"

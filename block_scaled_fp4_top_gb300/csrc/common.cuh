@@ -33,6 +33,8 @@ constexpr size_t kWsSchedW1 = 32;   // int, dynamic-schedule chunk counter of th
 constexpr size_t kWsSchedW2 = 36;   // int, dynamic-schedule chunk counter of the W2 GEMM
 constexpr size_t kWsBatchAmax = 40; // uint, batch amax accumulator of fp4moe_batch_gs1 (zero between calls)
 constexpr size_t kWsBatchDone = 44; // uint, its CTA arrival counter (zero between calls)
+constexpr size_t kWsScaleFlags = 48;  // uint, sticky FP4MOE_SAT_* bits (fp4moe_read_scale_status)
+constexpr size_t kWsAmaxHRun = 52;    // float, amax|h| of the W1 epilogues since the last refresh or clear
 constexpr size_t kWsHeader = 256;
 
 __device__ __forceinline__ void raise_error(uint32_t* err, uint32_t bits) { atomicOr(err, bits); }
@@ -66,12 +68,16 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
 // NVFP4 quantisation of one 16-element block under global scale g.
 // Returns the E4M3 scale byte; codes_lo/codes_hi get the 8 packed code bytes
 // (element 2i in the low nibble of byte i; bytes 0-3 in codes_lo, 4-7 in codes_hi).
+// s_out receives the unrounded block scale s. s > kE4M3SatAbove means the
+// E4M3 scale saturated: s rounds above the largest finite E4M3 value, so the
+// global scale g no longer covers this block.
 __device__ __forceinline__ uint32_t quant_block16(const float (&v)[16], float g, uint32_t& codes_lo,
-                                                  uint32_t& codes_hi) {
+                                                  uint32_t& codes_hi, float& s_out) {
   float a = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(v[i]));
   const float s = __fmul_rn(__fdiv_rn(a, 6.0f), g);
+  s_out = s;
   const uint32_t sf = cvt_e4m3(s);
   const float inv = (sf == 0u) ? 0.0f : __fdiv_rn(g, e4m3_to_f32(sf));
   uint32_t lo = 0, hi = 0;
@@ -84,6 +90,36 @@ __device__ __forceinline__ uint32_t quant_block16(const float (&v)[16], float g,
   codes_hi = hi;
   return sf;
 }
+__device__ __forceinline__ uint32_t quant_block16(const float (&v)[16], float g, uint32_t& codes_lo,
+                                                  uint32_t& codes_hi) {
+  float s;
+  return quant_block16(v, g, codes_lo, codes_hi, s);
+}
+
+// max that propagates NaN (fmaxf returns the other operand instead).
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// The clamped SwiGLU of the routed and shared experts: silu(min(g, L)) * clamp(u, -L, L).
+// A NaN gate or up gives a NaN h: the comparisons are written so that NaN
+// passes through (fminf/fmaxf would replace it by a clamp bound). The gate's
+// floor at -80 only keeps the exponential finite (silu(-80) is about -1e-33).
+// The exponential and the division use the fast hardware approximations (a
+// few ulp): h only feeds a requantiser or a bf16 rounding and the
+// tolerance-checked output.
+__device__ __forceinline__ float swiglu_clamped(float g, float u, float L) {
+  float gc = g > L ? L : g;
+  gc = gc < -80.0f ? -80.0f : gc;
+  const float uc = u > L ? L : (u < -L ? -L : u);
+  return __fdividef(gc, 1.0f + __expf(-gc)) * uc;
+}
+
+// E4M3 round-to-nearest-even takes s above 448 (to the 480 that the format lacks) exactly when s > 464, the
+// midpoint; ties go to 448, the even code. A block scale beyond it saturates.
+constexpr float kE4M3SatAbove = 464.0f;
 
 // Byte offset of scale (r, c) in the 128x4 tile layout of a matrix with C scale columns.
 __device__ __forceinline__ uint32_t sf_offset(uint32_t r, uint32_t c, uint32_t C) {

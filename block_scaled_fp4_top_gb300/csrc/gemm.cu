@@ -51,7 +51,12 @@
 //               TMEM at all.
 //     W1: alpha, then the clamped SwiGLU (gate columns 0-63, up columns
 //         64-127, from the W1 kernel row order), then NVFP4 requantisation
-//         into the L2 slot buffers ("Bug 6", "Bug 7").
+//         into the L2 slot buffers ("Bug 6", "Bug 7"). Each thread also keeps
+//         the amax of its h (NaN-propagating). When the CTA is done, each warp
+//         folds it into the running amax|h| of the workspace, sets
+//         FP4MOE_SAT_L2 if that amax made an E4M3 block scale saturate
+//         under gs2 (a stale L2 scale, "Bug 5" and "Bug 6"), or
+//         FP4MOE_ERR_NAN if an h was NaN.
 //     W1 amax: the same SwiGLU, reduced to amax|h| for calibration.
 //     W2: alpha, then fp32 rows stored per (token, k) pair.
 // Every spin-wait is bounded (mbar_wait). A timeout sets FP4MOE_ERR_TIMEOUT
@@ -108,7 +113,8 @@ struct Params {
   const float* gs2;
   uint8_t* out_codes;
   uint8_t* out_sf;
-  float* amax;
+  float* amax;       // W1 amax: the calibration maximum; W1 + SwiGLU: the running amax|h| (both non-negative)
+  uint32_t* status;  // W1 + SwiGLU: sticky FP4MOE_SAT_* bits
   float* o_pairs;
   uint32_t* err;
   int o_pairs32;  // W2: o_pairs is 32-byte aligned (every row is then, H being a multiple of 256)
@@ -260,15 +266,6 @@ struct TileSource {
 struct AMaps {
   CUtensorMap box[4];
 };
-
-// silu(min(g, L)) * clamp(u, -L, L). The exponential and the division use the
-// fast hardware approximations (a few ulp): h only feeds the requantiser
-// and the tolerance-checked output. The quantiser itself stays IEEE-exact.
-__device__ __forceinline__ float swiglu(float g, float u, float L) {
-  const float gc = fmaxf(fminf(g, L), -80.0f);  // silu(-80) is ~1e-33: the floor only keeps exp finite
-  const float uc = fminf(fmaxf(u, -L), L);
-  return __fdividef(gc, 1.0f + __expf(-gc)) * uc;
-}
 
 // Contiguous share [tau0, tau1) of `total` tiles for CTA c of G.
 __device__ __forceinline__ void cta_range(int total, int& tau0, int& tau1) {
@@ -575,6 +572,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp < 4) {
     // ------------------------------------------------------------ epilogue
     int tl = 0;
+    float hrun = 0.0f;  // W1 modes: amax|h| of this thread's rows, NaN if any h was NaN
     TileSource<kRoleEpilogue> src;
     src.init(prm, tau0, tau1, s_poff, E, NT, r128);
     Tile t;
@@ -626,11 +624,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         // columns [0, 64): gate of features 64 nt .. 64 nt + 63; columns [64, 128): up of the same features
         const float L = prm.limit;
         if constexpr (MODE == kW1Amax) {
-          float hmax = 0.0f;
 #pragma unroll
           for (int j = 0; j < 64; ++j)
-            hmax = fmaxf(hmax, fabsf(swiglu(__fmul_rn(v[j], alpha), __fmul_rn(v[64 + j], alpha), L)));
-          atomicMax(reinterpret_cast<unsigned int*>(prm.amax), __float_as_uint(hmax));
+            hrun = fmax_nan(hrun, fabsf(swiglu_clamped(__fmul_rn(v[j], alpha), __fmul_rn(v[64 + j], alpha), L)));
         } else {
           const float g2 = __ldg(prm.gs2);
           uint32_t codes[8];
@@ -639,8 +635,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int blk = 0; blk < 4; ++blk) {
             float h[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              h[j] = swiglu(__fmul_rn(v[blk * 16 + j], alpha), __fmul_rn(v[64 + blk * 16 + j], alpha), L);
+            for (int j = 0; j < 16; ++j) {
+              h[j] = swiglu_clamped(__fmul_rn(v[blk * 16 + j], alpha), __fmul_rn(v[64 + blk * 16 + j], alpha), L);
+              hrun = fmax_nan(hrun, fabsf(h[j]));
+            }
             const uint32_t sf = quant_block16(h, g2, codes[2 * blk], codes[2 * blk + 1]);
             sfw |= sf << (8 * blk);
           }
@@ -648,6 +646,23 @@ __global__ void __launch_bounds__(THREADS, 1)
           dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
           dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
           *reinterpret_cast<uint32_t*>(prm.out_sf + sf_offset(r, t.nt * 4, prm.I >> 4)) = sfw;
+        }
+      }
+    }
+    if constexpr (MODE != kW2Rows) {
+      // one amax per warp: NaN -> error bit; else the running (or calibration) maximum, and for the hot path
+      // the saturation test of the largest block, RN(RN(amax/6) * gs2) > 464, the quantiser's own arithmetic
+      __syncwarp();
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) hrun = fmax_nan(hrun, __shfl_xor_sync(0xFFFFFFFFu, hrun, off));
+      if (lane == 0) {
+        if (hrun != hrun) {
+          raise_error(prm.err, FP4MOE_ERR_NAN);
+        } else if (hrun > 0.0f) {
+          atomicMax(reinterpret_cast<unsigned int*>(prm.amax), __float_as_uint(hrun));
+          if constexpr (MODE == kW1SwiGLU) {
+            if (__fmul_rn(__fdiv_rn(hrun, 6.0f), __ldg(prm.gs2)) > kE4M3SatAbove) atomicOr(prm.status, FP4MOE_SAT_L2);
+          }
         }
       }
     }
@@ -731,9 +746,11 @@ size_t tiled_weight_bytes(int32_t rows, int32_t K) { return (size_t)rows * (size
 fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, const uint8_t* a_codes,
                           const uint8_t* a_sf, const int32_t* poff, const int32_t* pair_of_row,
                           const uint8_t* b_codes, const uint8_t* b_sf, const float* alpha, const float* gs2,
-                          uint8_t* out_codes, uint8_t* out_sf, float* amax, float* o_pairs, uint32_t* err,
-                          int* sched, cudaStream_t st) {
+                          uint8_t* out_codes, uint8_t* out_sf, float* amax, uint32_t* status, float* o_pairs,
+                          uint32_t* err, int* sched, cudaStream_t st) {
   if (T == 0) return FP4MOE_OK;
+  if (mode != kW2Rows && amax == nullptr) return FP4MOE_INVALID_ARG;
+  if (mode == kW1SwiGLU && status == nullptr) return FP4MOE_INVALID_ARG;
   const bool w2 = (mode == kW2Rows);
   const int Kc = w2 ? cfg.inter : cfg.hidden;
   if (Kc > kMaxResidentK) return FP4MOE_UNSUPPORTED;
@@ -759,6 +776,7 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
   prm.out_codes = out_codes;
   prm.out_sf = out_sf;
   prm.amax = amax;
+  prm.status = status;
   prm.o_pairs = o_pairs;
   prm.o_pairs32 = (reinterpret_cast<uintptr_t>(o_pairs) & 31u) == 0 ? 1 : 0;
   prm.err = err;

@@ -55,8 +55,14 @@ fp4moe_status route_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* 
                            int32_t* hist, float* nw2, float* part, size_t part_bytes, uint32_t* err,
                            cudaStream_t st);
 
+// status: sticky FP4MOE_SAT_L1 when a block scale saturates; err: FP4MOE_ERR_NAN for a NaN in x
 fp4moe_status quant_scatter_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const float* gs1,
-                                   const int32_t* slot_of_pair, uint8_t* a1, uint8_t* a1_sf, cudaStream_t st);
+                                   const int32_t* slot_of_pair, uint8_t* a1, uint8_t* a1_sf, uint32_t* status,
+                                   uint32_t* err, cudaStream_t st);
+// gs2 and alpha2 from the running amax|h| of the W1 epilogues (left as they are when it is zero), which is
+// then cleared: fp4moe_refresh_gs2
+fp4moe_status refresh_gs2_launch(int32_t E, float* amax_run, const float* gw2, float* gs2, float* alpha2,
+                                 cudaStream_t st);
 
 // rows [n_rows_total][K] fp32 -> NVFP4; g indexed by row / g_div; optional W1 gate/up row permutation
 // (rows_per_group = rows of one expert, inter = I, or 0 for no permutation); tiled != 0 writes the codes in
@@ -80,8 +86,8 @@ enum GemmMode { kW1SwiGLU = 0, kW1Amax = 1, kW2Rows = 2 };
 fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, const uint8_t* a_codes,
                           const uint8_t* a_sf, const int32_t* poff, const int32_t* pair_of_row,
                           const uint8_t* b_codes, const uint8_t* b_sf, const float* alpha, const float* gs2,
-                          uint8_t* out_codes, uint8_t* out_sf, float* amax, float* o_pairs, uint32_t* err,
-                          int* sched, cudaStream_t st);
+                          uint8_t* out_codes, uint8_t* out_sf, float* amax, uint32_t* status, float* o_pairs,
+                          uint32_t* err, int* sched, cudaStream_t st);
 
 // selftest.cu: one bounded wait that runs out (see fp4moe_selftest_wait_timeout)
 fp4moe_status selftest_wait_launch(uint32_t* err, int64_t limit_ns, uint32_t* result, cudaStream_t st);

@@ -113,13 +113,6 @@ __device__ __forceinline__ uint32_t e8m0_bf16_bits(uint32_t s) {
   return s << 7;
 }
 
-// silu(min(g, L)) * clamp(u, -L, L), as in gemm.cu
-__device__ __forceinline__ float swiglu(float g, float u, float L) {
-  const float gc = fmaxf(fminf(g, L), -80.0f);
-  const float uc = fminf(fmaxf(u, -L), L);
-  return __fdividef(gc, 1.0f + __expf(-gc)) * uc;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
   const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
@@ -314,7 +307,8 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
               uint32_t hw[16];
 #pragma unroll
               for (int i = 0; i < 16; ++i)
-                hw[i] = pack_bf16x2(swiglu(gv[2 * i], uv[2 * i], L), swiglu(gv[2 * i + 1], uv[2 * i + 1], L));
+                hw[i] = pack_bf16x2(swiglu_clamped(gv[2 * i], uv[2 * i], L),
+                                    swiglu_clamped(gv[2 * i + 1], uv[2 * i + 1], L));
               uint4* dst = reinterpret_cast<uint4*>(prm.out_bf16 + (size_t)r * prm.I + t.nt * 64 + 32 * q);
 #pragma unroll
               for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hw[4 * i], hw[4 * i + 1], hw[4 * i + 2], hw[4 * i + 3]);

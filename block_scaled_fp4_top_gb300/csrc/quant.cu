@@ -15,14 +15,26 @@
 namespace fp4moe {
 namespace {
 
+// Set `bit` in `*word` if any active lane of the warp asks for it: one atomic per warp, and none once the bit
+// is already set (a stale scale can make every block of a large batch saturate).
+__device__ __forceinline__ void warp_flag(bool want, uint32_t* word, uint32_t bit) {
+  const unsigned m = __activemask();
+  const unsigned b = __ballot_sync(m, want);
+  if (b != 0u && (threadIdx.x & 31u) == (unsigned)(__ffs(b) - 1) && !(*(volatile uint32_t*)word & bit))
+    atomicOr(word, bit);
+}
+
 // One thread per 16-element block: thread i quantises block i % (H/16) of
 // token i / (H/16) once and writes it to the token's k slot rows. Consecutive
 // threads cover consecutive blocks of a row, so loads and code stores are
-// contiguous. Padding rows are never touched.
+// contiguous. Padding rows are never touched. A block whose scale saturates
+// (s = RN(RN(amax/6) * gs1) rounds above 448 in E4M3, s > 464) sets
+// FP4MOE_SAT_L1 in `status`; a NaN in x sets FP4MOE_ERR_NAN in `err`.
 __global__ void __launch_bounds__(256) quant_scatter_kernel(int T, int H, int k, const uint16_t* __restrict__ x,
                                                             const float* __restrict__ gs1,
                                                             const int32_t* __restrict__ slot_of_pair,
-                                                            uint8_t* __restrict__ a1, uint8_t* __restrict__ a1_sf) {
+                                                            uint8_t* __restrict__ a1, uint8_t* __restrict__ a1_sf,
+                                                            uint32_t* status, uint32_t* err) {
   pdl_wait();
   pdl_trigger();
   const int C = H >> 4;
@@ -40,7 +52,11 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(int T, int H, int k,
                        bf16_lo(u0.w), bf16_hi(u0.w), bf16_lo(u1.x), bf16_hi(u1.x), bf16_lo(u1.y), bf16_hi(u1.y),
                        bf16_lo(u1.z), bf16_hi(u1.z), bf16_lo(u1.w), bf16_hi(u1.w)};
   uint32_t lo, hi;
-  const uint32_t sf = quant_block16(v, g, lo, hi);
+  float s;
+  const uint32_t sf = quant_block16(v, g, lo, hi, s);
+  bool nan = false;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) nan |= (v[i] != v[i]);
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j) {
     const int row = rows[j];
@@ -48,6 +64,8 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(int T, int H, int k,
     *reinterpret_cast<uint2*>(a1 + (size_t)row * (H >> 1) + b * 8) = make_uint2(lo, hi);
     a1_sf[sf_offset(row, b, C)] = (uint8_t)sf;
   }
+  warp_flag(s > kE4M3SatAbove, status, FP4MOE_SAT_L1);
+  warp_flag(nan, err, FP4MOE_ERR_NAN);
 }
 
 // Byte offset of code byte `kbyte` of kernel row o in the pre-tiled weight
@@ -168,7 +186,34 @@ __global__ void __launch_bounds__(256) batch_gs1_kernel(int64_t n, const uint16_
   for (int e = threadIdx.x; e < E; e += blockDim.x) alpha1[e] = __fdiv_rn(1.0f, __fmul_rn(s_g, gw1[e]));
 }
 
+// gs2 = RN(2688 / amax) from the running amax|h| of the W1 epilogues, and alpha2[e] = RN(1 / RN(gs2 * gw2[e])),
+// in one CTA; then the running amax is cleared. With no h since the last refresh (amax 0) gs2 and alpha2 stay.
+__global__ void __launch_bounds__(256) refresh_gs2_kernel(int E, float* amax_run, const float* __restrict__ gw2,
+                                                          float* gs2, float* __restrict__ alpha2) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float s_g;
+  if (threadIdx.x == 0) {
+    const float a = *(volatile float*)amax_run;
+    s_g = a > 0.0f ? global_scale_from_amax(a) : 0.0f;
+    if (a > 0.0f) gs2[0] = s_g;
+  }
+  __syncthreads();
+  if (s_g > 0.0f)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) alpha2[e] = __fdiv_rn(1.0f, __fmul_rn(s_g, gw2[e]));
+  __syncthreads();
+  if (threadIdx.x == 0) *amax_run = 0.0f;
+}
+
 }  // namespace
+
+fp4moe_status refresh_gs2_launch(int32_t E, float* amax_run, const float* gw2, float* gs2, float* alpha2,
+                                 cudaStream_t st) {
+  return launch_pdl(refresh_gs2_kernel, dim3(1), dim3(256), 0, st, (int)E, amax_run, gw2, gs2, alpha2) ==
+                 cudaSuccess
+             ? FP4MOE_OK
+             : FP4MOE_CUDA_ERROR;
+}
 
 fp4moe_status batch_gs1_launch(int32_t T, int32_t H, const uint16_t* x, int32_t E, const float* gw1, float* gs1,
                                float* alpha1, unsigned int* acc, unsigned int* done, cudaStream_t st) {
@@ -183,11 +228,12 @@ fp4moe_status batch_gs1_launch(int32_t T, int32_t H, const uint16_t* x, int32_t 
 
 
 fp4moe_status quant_scatter_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const float* gs1,
-                                   const int32_t* slot_of_pair, uint8_t* a1, uint8_t* a1_sf, cudaStream_t st) {
+                                   const int32_t* slot_of_pair, uint8_t* a1, uint8_t* a1_sf, uint32_t* status,
+                                   uint32_t* err, cudaStream_t st) {
   if (T == 0) return FP4MOE_OK;
   const int64_t threads = (int64_t)T * (cfg.hidden / 16);
   return launch_pdl(quant_scatter_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, st, T, cfg.hidden,
-                    cfg.top_k, x, gs1, slot_of_pair, a1, a1_sf) == cudaSuccess
+                    cfg.top_k, x, gs1, slot_of_pair, a1, a1_sf, status, err) == cudaSuccess
              ? FP4MOE_OK
              : FP4MOE_CUDA_ERROR;
 }

@@ -98,13 +98,6 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// silu(min(g, L)) * clamp(u, -L, L), as in the routed experts
-__device__ __forceinline__ float swiglu(float g, float u, float L) {
-  const float gc = fmaxf(fminf(g, L), -80.0f);
-  const float uc = fminf(fmaxf(u, -L), L);
-  return __fdividef(gc, 1.0f + __expf(-gc)) * uc;
-}
-
 // Two E4M3 codes (RNE, satfinite) of lo / s and hi / s in the low 16 bits, lo in the low byte.
 __device__ __forceinline__ uint32_t e4m3x2_scaled(float lo, float hi, float s) {
   uint16_t r;
@@ -297,7 +290,7 @@ __global__ void __launch_bounds__(SE_THREADS, 1)
       if (warp < 8) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          acc[i] = swiglu(acc[i], acc[32 + i], prm.limit);
+          acc[i] = swiglu_clamped(acc[i], acc[32 + i], prm.limit);
           amax = fmaxf(amax, fabsf(acc[i]));
         }
         s_amax[hf][r] = amax;
@@ -395,7 +388,7 @@ __global__ void __launch_bounds__(SE_THREADS, 1)
           float h[8], amax = 0.0f;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            h[i] = swiglu(v[i], v[8 + i], prm.limit);
+            h[i] = swiglu_clamped(v[i], v[8 + i], prm.limit);
             amax = fmaxf(amax, fabsf(h[i]));
           }
 #pragma unroll

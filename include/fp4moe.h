@@ -31,6 +31,9 @@
  *    once before first use. Its first 4 bytes are a sticky device error word:
  *    a bitwise OR of FP4MOE_ERR_* values. Kernels set bits there instead of
  *    trapping. Read and clear it with fp4moe_read_error outside any graph.
+ *    A second sticky word reports saturated activation block scales
+ *    (FP4MOE_SAT_*, fp4moe_read_scale_status), beside the running amax of h
+ *    that fp4moe_refresh_gs2 turns into a new L2 scale.
  *    Calls that share a workspace must be ordered on one stream.
  *
  * Padded layout (from "Current Bug", sections "Bug 2", "Bug 4", "Bug 9" and
@@ -155,6 +158,16 @@ typedef enum fp4moe_status {
 #define FP4MOE_ERR_TIMEOUT   0x1u  /* a bounded wait inside a kernel expired; its tile was skipped */
 #define FP4MOE_ERR_EXPERT_ID 0x2u  /* a routed expert id was outside [0, E) */
 #define FP4MOE_ERR_CAPACITY  0x4u  /* padded rows R exceeded CAP */
+#define FP4MOE_ERR_NAN       0x8u  /* a NaN reached an NVFP4 activation quantiser (x in moe_quantize_scatter,
+                                      or h in the W1 epilogue or fp4moe_calibrate); the codes of that block
+                                      are unspecified, and so are the outputs of its token */
+
+/* Scale-status bits: a second sticky word of the workspace (fp4moe_read_scale_status). They are not
+ * errors: a fixed activation global scale that a batch outgrows saturates its E4M3 block scales, which is
+ * part of the definition ("Current Bug", "Bug 5"). They tell the caller that a scale has gone stale. */
+#define FP4MOE_SAT_L1 0x1u  /* some L1 block scale s = RN(RN(amax/6) * gs1) of x saturated: s > 464, so E4M3
+                               rounding takes it above 448, the largest finite value */
+#define FP4MOE_SAT_L2 0x2u  /* the same for h under gs2 in the W1 epilogue */
 
 #define FP4MOE_W_NVFP4 0
 #define FP4MOE_W_MXFP4 1
@@ -249,10 +262,13 @@ fp4moe_status moe_route(const fp4moe_config* cfg, int32_t T, const uint16_t* x, 
  *     scratch that each call clears, so they are lost.
  *
  * Set-up and sharing:
- *   - The first call made on each device (that device current) looks up the
- *     array's device address with cudaGetSymbolAddress. It returns
- *     FP4MOE_CUDA_ERROR if the lookup fails. Make that first call before any
- *     stream capture begins.
+ *   - Every call looks up the array's device address in the current
+ *     device's context with cudaGetSymbolAddress, which allocates nothing. The
+ *     address therefore stays right after a context is destroyed and created
+ *     again (cudaDeviceReset), when the library's device code is loaded anew.
+ *     The call returns FP4MOE_CUDA_ERROR if the lookup fails. Make the first
+ *     call on each device before any stream capture begins: that lookup may
+ *     load the library's device code.
  *   - Every call on a device shares the one array. Each call clears, on
  *     `stream`, the part that must start at zero (the scratch error word);
  *     every other byte it reads it has written first. Two calls whose work
@@ -478,6 +494,29 @@ fp4moe_status fp4moe_quantize_weights(const fp4moe_config* cfg, int32_t which, i
 fp4moe_status fp4moe_batch_gs1(const fp4moe_config* cfg, int32_t T, const uint16_t* x, const float* gw1,
                                float* gs1_out, float* alpha1_out, void* ws, fp4moe_stream_t stream);
 
+/*
+ * fp4moe_refresh_gs2: the L2 activation global scale taken from the h of
+ * recent calls instead of the warm-up pass, with no host synchronisation.
+ * Every W1 epilogue (moe_grouped_gemm_w1_swiglu, moe_forward) folds the
+ * amax of the h it quantised into a running maximum in the workspace header.
+ * This call, in one launch on `stream`:
+ *   if that running amax a > 0:
+ *     gs2_inout[0] = RN(2688 / a),
+ *     alpha2_out[e] = RN(1 / RN(gs2_inout[0] * gw2[e])) for every local expert e;
+ *   (with a == 0, no h since the last refresh, gs2 and alpha2 are left alone)
+ * and then clears the running amax.
+ * The scale is LAGGED: it covers the calls made before the refresh and
+ * applies to the calls made after it. A batch whose h exceeds the range of
+ * the gs2 it ran with still saturates in E4M3, and sets FP4MOE_SAT_L2; a
+ * refresh then adapts gs2 for the next calls. That is the calibration drift
+ * of "Current Bug", "Bug 5" and "Bug 6" (an L2 amax of about 286 against a
+ * scale taken from a much smaller range), detected and corrected on the device.
+ * gw2 [E] is the W2 weight global-scale table of fp4moe_quantize_weights.
+ * MXFP4 layers have no global scales: FP4MOE_UNSUPPORTED.
+ */
+fp4moe_status fp4moe_refresh_gs2(const fp4moe_config* cfg, void* ws, const float* gw2, float* gs2_inout,
+                                 float* alpha2_out, fp4moe_stream_t stream);
+
 /* alpha[e] = RN(1 / RN(gs_act[0] * gs_w[e])) for e < n. */
 fp4moe_status fp4moe_make_alpha(int32_t n, const float* gs_act, const float* gs_w, float* alpha,
                                 fp4moe_stream_t stream);
@@ -528,6 +567,16 @@ fp4moe_status fp4moe_selftest_wait_timeout(uint32_t* err, int64_t limit_ns, uint
  * outside graphs, between steps.
  */
 fp4moe_status fp4moe_read_error(void* ws, uint32_t* err_host, int32_t clear, fp4moe_stream_t stream);
+
+/*
+ * fp4moe_read_scale_status: copy the workspace's sticky FP4MOE_SAT_* word to
+ * *flags_host and, when amax_h_host is not NULL, the running amax|h| of the
+ * W1 epilogues since the last fp4moe_refresh_gs2 (0 if none). If clear != 0,
+ * zero the flags word afterwards (the running amax is cleared only by a
+ * refresh). SYNCHRONISES `stream`: use it outside graphs, between steps.
+ */
+fp4moe_status fp4moe_read_scale_status(void* ws, uint32_t* flags_host, float* amax_h_host, int32_t clear,
+                                       fp4moe_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -125,6 +125,54 @@ def expert_out(qe: QuantExpert, h: np.ndarray, gs2) -> np.ndarray:
     return ht @ W2.T
 
 
+def activation_scale(x_bits: np.ndarray) -> np.float32:
+    """gs1 = g(amax |x|) of a warm-up batch ("Current Bug" sections "Bug 5" and "Bug 6")."""
+    return nvfp4.global_scale(F32(np.abs(bf16_to_f64(x_bits)).max()))
+
+
+def dequantized_activations(x_bits: np.ndarray, gs) -> np.ndarray:
+    """x~ = dequant(quant(x, gs)) in fp64 [n, H]: the L1 activations every routed expert sees."""
+    q, sf = nvfp4.quantize_rows(bf16_to_f64(x_bits).astype(F32), gs)
+    return nvfp4.dequantize(q, sf, gs)
+
+
+def hidden_amax(qe: QuantExpert, xt: np.ndarray, limit: float) -> float:
+    """amax |RN_f32(h)| of one expert over dequantised activation rows xt [n, H] (0 for no rows)."""
+    if xt.shape[0] == 0:
+        return 0.0
+    return float(np.abs(expert_hidden(qe, xt, limit).astype(F32)).max())
+
+
+def pair_rows(qe: QuantExpert, xt: np.ndarray, gs2, limit: float, quantize_activations: bool = True) -> np.ndarray:
+    """One expert's W2 output rows o [n, H] (fp64) for dequantised activation rows xt [n, H].
+
+    quantize_activations=False skips the L2 codec (h goes to W2 as it is).
+    """
+    h = expert_hidden(qe, xt, limit)
+    if quantize_activations:
+        return expert_out(qe, h, gs2)
+    return h @ nvfp4.dequantize(qe.w2_q, qe.w2_sf, qe.w2_gs).T
+
+
+def routed_rows(ids: np.ndarray) -> dict:
+    """expert -> (token rows tt, slots jj) of every routed pair; pairs held by no local expert (-1, "Bug 8") are
+    left out."""
+    return {int(e): np.nonzero(ids == e) for e in np.unique(ids) if e >= 0}
+
+
+def combine(ids: np.ndarray, w: np.ndarray, outs: np.ndarray, shared: np.ndarray | None = None) -> np.ndarray:
+    """y = bf16( sum_{j = 0..k-1} w[:, j] * outs[:, j] (+ shared) ), summed in j order; pairs with id -1 (held
+    elsewhere) are skipped. outs [n, k, H] fp64. Returns bf16 bits [n, H]."""
+    n, k = ids.shape
+    acc = np.zeros((n, outs.shape[2]), dtype=np.float64)
+    for j in range(k):
+        held = (ids[:, j] >= 0)[:, None]
+        acc = np.where(held, acc + w[:, j:j + 1] * outs[:, j], acc)
+    if shared is not None:
+        acc = acc + shared
+    return f32_to_bf16_bits(acc.astype(F32))
+
+
 def moe_tokens(x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray,
                expert: Callable[[int], QuantExpert], gs1, gs2, limit: float,
                quantize_activations: bool = True, shared: np.ndarray | None = None) -> np.ndarray:
@@ -136,33 +184,12 @@ def moe_tokens(x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray,
     ``shared`` [n, H] is a shared expert's output, added with weight 1 after the
     routed terms (``fp8block.shared_out``).
     """
-    x = bf16_to_f64(x_bits)
-    n, H = x.shape
-    k = ids.shape[1]
-    if quantize_activations:
-        q, sf = nvfp4.quantize_rows(x.astype(F32), gs1)
-        xt = nvfp4.dequantize(q, sf, gs1)
-    else:
-        xt = x
-    outs = np.zeros((n, k, H), dtype=np.float64)
-    for e in np.unique(ids):
-        if e < 0:   # a pair held by no local expert ("Bug 8"): left out of this layer's sum
-            continue
-        tt, jj = np.nonzero(ids == e)
-        qe = expert(int(e))
-        h = expert_hidden(qe, xt[tt], limit)
-        if quantize_activations:
-            o = expert_out(qe, h, gs2)
-        else:
-            o = h @ nvfp4.dequantize(qe.w2_q, qe.w2_sf, qe.w2_gs).T
-        outs[tt, jj] = o
-    acc = np.zeros((n, H), dtype=np.float64)
-    for j in range(k):
-        held = (ids[:, j] >= 0)[:, None]
-        acc = np.where(held, acc + w[:, j:j + 1] * outs[:, j], acc)
-    if shared is not None:
-        acc = acc + shared
-    return f32_to_bf16_bits(acc.astype(F32))
+    xt = dequantized_activations(x_bits, gs1) if quantize_activations else bf16_to_f64(x_bits)
+    n, H = xt.shape
+    outs = np.zeros((n, ids.shape[1], H), dtype=np.float64)
+    for e, (tt, jj) in routed_rows(ids).items():
+        outs[tt, jj] = pair_rows(expert(e), xt[tt], gs2, limit, quantize_activations)
+    return combine(ids, w, outs, shared)
 
 
 def calibrate(x_bits: np.ndarray, ids: np.ndarray, expert: Callable[[int], QuantExpert], limit: float):
@@ -173,16 +200,9 @@ def calibrate(x_bits: np.ndarray, ids: np.ndarray, expert: Callable[[int], Quant
     With expert parallelism the ids are local and masked pairs (-1) are skipped:
     the fix of "Bug 13", where global ids matched no local expert and gs2 came out 0.
     """
-    x = bf16_to_f64(x_bits)
-    gs1 = nvfp4.global_scale(F32(np.abs(x).max()))
-    q, sf = nvfp4.quantize_rows(x.astype(F32), gs1)
-    xt = nvfp4.dequantize(q, sf, gs1)
+    gs1 = activation_scale(x_bits)
+    xt = dequantized_activations(x_bits, gs1)
     amax_h = 0.0
-    for e in np.unique(ids):
-        if e < 0:
-            continue
-        tt, _ = np.nonzero(ids == e)
-        h = expert_hidden(expert(int(e)), xt[tt], limit)
-        amax_h = max(amax_h, float(np.abs(h.astype(F32)).max()))
-    gs2 = nvfp4.global_scale(F32(amax_h))
-    return gs1, gs2
+    for e, (tt, _) in routed_rows(ids).items():
+        amax_h = max(amax_h, hidden_amax(expert(e), xt[tt], limit))
+    return gs1, nvfp4.global_scale(F32(amax_h))

@@ -94,8 +94,8 @@ def mx_quantize_rows(v: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
 def mx_dequantize(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     """codes [R, K] and E8M0 scales [R, K/32] -> fp64 [R, K]."""
     R, K = q.shape
-    el = codecs.e2m1_decode(q).reshape(R, K // MX_BLOCK, MX_BLOCK)
-    return (el * codecs.e8m0_decode(s)[:, :, None]).reshape(R, K)
+    el = codecs.E2M1_TABLE[np.asarray(q, dtype=np.uint8) & 0xF].reshape(R, K // MX_BLOCK, MX_BLOCK)
+    return (el * codecs.E8M0_TABLE[np.asarray(s, dtype=np.uint8)][:, :, None]).reshape(R, K)
 
 
 # ------------------------------------------------------- the MXFP4 layer ----
@@ -113,30 +113,51 @@ class MxExpert(NamedTuple):
     w2_s: np.ndarray    # [H, Ik / 32]
 
 
-def mx_expert_shard(w1_full: np.ndarray, w2_full: np.ndarray, plan: TPPlan, rank: int) -> MxExpert:
-    """Quantise one expert's full logical matrices to MXFP4, then cut rank `rank`'s shard.
+class MxCheckpoint(NamedTuple):
+    """One expert's full-width MXFP4 tensors as a checkpoint stores them ("Packed W2 weight is wrong"):
+    W13 codes unpacked one per row element, W2 codes packed two per byte, one E8M0 byte per 32 elements."""
+    w13_q: np.ndarray       # [2 I, H] codes, gate rows first
+    w13_s: np.ndarray       # [2 I, H / 32]
+    w2_packed: np.ndarray   # [H, I / 2] bytes, element 2i in the low nibble
+    w2_s: np.ndarray        # [H, I / 32]
 
-    The shard follows "Required loader changes": source offsets counted in
+
+def mx_checkpoint(w1_full: np.ndarray, w2_full: np.ndarray) -> MxCheckpoint:
+    """Quantise one expert's full logical matrices: w1_full [2 I, H] (gate rows first), w2_full [H, I] fp32."""
+    q1, s1 = mx_quantize_rows(w1_full)
+    q2, s2 = mx_quantize_rows(w2_full)
+    packed = (q2[:, 0::2] | (q2[:, 1::2] << 4)).astype(np.uint8)           # element 2i in the low nibble
+    return MxCheckpoint(q1, s1, packed, s2)
+
+
+def mx_shard_checkpoint(ck: MxCheckpoint, plan: TPPlan, rank: int) -> MxExpert:
+    """Cut rank `rank`'s kernel-width shard out of a quantised checkpoint.
+
+    The cut follows "Required loader changes": source offsets counted in
     logical elements and converted to each tensor's storage unit. W13 takes
     1 unpacked row per element. Packed W2 takes 2 elements per byte. W2
     scales take 32 elements per E8M0 group. The destination is zero-filled
     first.
-    w1_full [2 I, H] (gate rows first), w2_full [H, I] fp32; I is the full width.
     """
-    I = w2_full.shape[1]
-    q1, s1 = mx_quantize_rows(w1_full)
-    gate_q = shard_axis(q1[:I], 0, I, plan, rank, 1)
-    up_q = shard_axis(q1[I:], 0, I, plan, rank, 1)
-    gate_s = shard_axis(s1[:I], 0, I, plan, rank, 1)
-    up_s = shard_axis(s1[I:], 0, I, plan, rank, 1)
-    q2, s2 = mx_quantize_rows(w2_full)
-    packed = (q2[:, 0::2] | (q2[:, 1::2] << 4)).astype(np.uint8)           # element 2i in the low nibble
-    packed_shard = shard_axis(packed, 1, I, plan, rank, 2)
+    I = ck.w13_q.shape[0] // 2
+    gate_q = shard_axis(ck.w13_q[:I], 0, I, plan, rank, 1)
+    up_q = shard_axis(ck.w13_q[I:], 0, I, plan, rank, 1)
+    gate_s = shard_axis(ck.w13_s[:I], 0, I, plan, rank, 1)
+    up_s = shard_axis(ck.w13_s[I:], 0, I, plan, rank, 1)
+    packed_shard = shard_axis(ck.w2_packed, 1, I, plan, rank, 2)
     w2_q = np.empty((packed_shard.shape[0], packed_shard.shape[1] * 2), dtype=np.uint8)
     w2_q[:, 0::2] = packed_shard & 0xF
     w2_q[:, 1::2] = packed_shard >> 4
-    w2_s = shard_axis(s2, 1, I, plan, rank, 32)
+    w2_s = shard_axis(ck.w2_s, 1, I, plan, rank, 32)
     return MxExpert(np.concatenate([gate_q, up_q]), np.concatenate([gate_s, up_s]), w2_q, w2_s)
+
+
+def mx_expert_shard(w1_full: np.ndarray, w2_full: np.ndarray, plan: TPPlan, rank: int) -> MxExpert:
+    """Quantise one expert's full logical matrices to MXFP4, then cut rank `rank`'s shard.
+
+    w1_full [2 I, H] (gate rows first), w2_full [H, I] fp32; I is the full width.
+    """
+    return mx_shard_checkpoint(mx_checkpoint(w1_full, w2_full), plan, rank)
 
 
 def _bf16_round(v: np.ndarray) -> np.ndarray:
@@ -173,10 +194,6 @@ def mx_moe_partials(x_bits: np.ndarray, ids: np.ndarray, expert, limit: float) -
 
 
 def mx_moe_tokens(x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray, expert, limit: float) -> np.ndarray:
-    """The MXFP4 layer on one rank: y = bf16(sum_j w_j o_j) in j order. Returns bf16 bits [n, H]."""
-    from .moe import f32_to_bf16_bits
-    outs = mx_moe_partials(x_bits, ids, expert, limit)
-    acc = np.zeros(outs.shape[::2], dtype=np.float64)
-    for j in range(ids.shape[1]):
-        acc = acc + w[:, j:j + 1] * outs[:, j]
-    return f32_to_bf16_bits(acc.astype(np.float32))
+    """The MXFP4 layer on one rank: y = bf16(sum_j w_j o_j) in j order (``moe.combine``). Returns bf16 bits [n, H]."""
+    from .moe import combine
+    return combine(ids, w, mx_moe_partials(x_bits, ids, expert, limit))

@@ -52,6 +52,22 @@ def global_scale(amax) -> np.float32:
     return F32(GS_NUMERATOR / a)
 
 
+def block_scales(v: np.ndarray, g) -> np.ndarray:
+    """Step 2 of the quantiser before its E4M3 rounding: s = RN(RN(a / 6) * g) per 16-element block, fp32 [R, K/16].
+
+    E4M3 rounding takes s above 448, the largest finite value, exactly when s > 464 (the midpoint to the next
+    power-of-two step; the tie goes to 448, the even code): such a block's scale saturates.
+    """
+    v = np.asarray(v, dtype=F32)
+    R, K = v.shape
+    g = np.broadcast_to(np.asarray(g, dtype=F32).reshape(-1, 1) if np.ndim(g) else F32(g), (R, 1)).astype(F32)
+    a = np.abs(v.reshape(R, K // NVFP4_BLOCK, NVFP4_BLOCK)).max(axis=2)
+    return ((a / F32(6.0)).astype(F32) * g).astype(F32)
+
+
+E4M3_SATURATES_ABOVE = 464.0
+
+
 def quantize_rows(v: np.ndarray, g) -> tuple[np.ndarray, np.ndarray]:
     """NVFP4-quantise rows of fp32 values.
 
@@ -64,9 +80,7 @@ def quantize_rows(v: np.ndarray, g) -> tuple[np.ndarray, np.ndarray]:
     assert K % NVFP4_BLOCK == 0
     g = np.broadcast_to(np.asarray(g, dtype=F32).reshape(-1, 1) if np.ndim(g) else F32(g), (R, 1)).astype(F32)
     blocks = v.reshape(R, K // NVFP4_BLOCK, NVFP4_BLOCK)
-    a = np.abs(blocks).max(axis=2)                                   # exact
-    s = (a / F32(6.0)).astype(F32) * g                               # RN(RN(a/6) * g)
-    s = s.astype(F32)
+    s = block_scales(v, g)                                           # RN(RN(a/6) * g), a = max|v| exact
     sf = codecs.e4m3_encode(s)                                       # [R, K/16]
     sf_val = codecs.e4m3_decode(sf).astype(F32)                      # exact in fp32
     with np.errstate(divide="ignore"):
@@ -94,8 +108,8 @@ def dequantize(q: np.ndarray, sf: np.ndarray, g) -> np.ndarray:
     """decode(q) * decode(sf) / g in fp64; q [R, K] codes, sf [R, K/16]."""
     R, K = q.shape
     g = np.asarray(g, dtype=np.float64).reshape(-1, 1) if np.ndim(g) else np.float64(g)
-    el = codecs.e2m1_decode(q).reshape(R, K // NVFP4_BLOCK, NVFP4_BLOCK)
-    sc = codecs.e4m3_decode(sf)[:, :, None]
+    el = codecs.E2M1_TABLE[np.asarray(q, dtype=np.uint8) & 0xF].reshape(R, K // NVFP4_BLOCK, NVFP4_BLOCK)
+    sc = codecs.E4M3_TABLE[np.asarray(sf, dtype=np.uint8)][:, :, None]
     return (el * sc).reshape(R, K) / g
 
 

@@ -26,3 +26,12 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def oracle_svc():
+    """One pool of oracle worker processes for the whole session (tests/oracle_pool.py)."""
+    from oracle_pool import OracleService
+    svc = OracleService()
+    yield svc
+    svc.close()

@@ -10,6 +10,12 @@ m-tiles, and K is partial (a stage of 2 atoms) or runs over several stages.
 * W1: the clamped SwiGLU + requantisation epilogue is compared with the
   oracle's quantiser applied to the fp64 reference h. Codes must agree
   except at rounding ties that the fp32 accumulation moves.
+* Scale bytes: the 0.5 .. 2 band, and the whole finite E4M3 range (0x00,
+  the subnormals 0x01 .. 0x07, up to 0x7E = 448) on both operands.
+* The clamp: a W1 case whose gate and up values reach about +-50, with codes
+  equal to the oracle's wherever both gate and up are clamped, and a W1 case
+  with a NaN alpha, which must raise FP4MOE_ERR_NAN and leave every other
+  expert's rows as they are.
 """
 import numpy as np
 import pytest
@@ -32,9 +38,15 @@ def _layout(counts, seed):
     return ids.reshape(-1, 1), layout.slots(ids.reshape(-1, 1), len(counts))
 
 
-def _rand_operand(rng, rows, K, lo=0x30, hi=0x40):
+def _rand_operand(rng, rows, K, full_range=False):
+    """Random E2M1 codes and E4M3 scale bytes: 0x30 .. 0x40 (0.5 .. 2), or every finite byte 0x00 .. 0x7E with
+    0x00, the subnormals 0x01 .. 0x07 and 0x7E each forced into the first blocks."""
     q = rng.integers(0, 16, (rows, K)).astype(np.uint8)
-    s = rng.integers(lo, hi + 1, (rows, K // 16)).astype(np.uint8)
+    if not full_range:
+        return q, rng.integers(0x30, 0x41, (rows, K // 16)).astype(np.uint8)
+    s = rng.integers(0x00, 0x7F, (rows, K // 16)).astype(np.uint8)
+    special = np.array([0x00, 0x01, 0x02, 0x03, 0x04, 0x05, 0x06, 0x07, 0x7E], np.uint8)
+    s.reshape(-1)[: min(s.size, 4 * special.size)] = np.tile(special, 4)[: min(s.size, 4 * special.size)]
     return q, s
 
 
@@ -43,7 +55,7 @@ def _dec(q, s):
     return (codecs.e2m1_decode(q).reshape(R, K // 16, 16) * codecs.e4m3_decode(s)[:, :, None]).reshape(R, K)
 
 
-def _setup(H, I, counts, seed, which):
+def _setup(H, I, counts, seed, which, full_range=False, alpha_mult=1.0):
     import torch
     from block_scaled_fp4_top_gb300 import api
     rng = np.random.default_rng(seed)
@@ -55,14 +67,14 @@ def _setup(H, I, counts, seed, which):
     R = L["R"]
     K = I if which == 2 else H
     N = H if which == 2 else 2 * I
-    qa, sa = _rand_operand(rng, cap, K)
+    qa, sa = _rand_operand(rng, cap, K, full_range)
     real = np.zeros(cap, dtype=bool)
     real[:R] = L["pair_of_row"] >= 0
     qa[~real] = 0
     sa[~real] = 0
-    qw, sw = _rand_operand(rng, E * N, K)
-    # W1 output feeds a SwiGLU clamped at 10: keep the accumulators O(1) there
-    alpha = (rng.uniform(0.5, 2.0, E) * (1.0 if which == 2 else 0.25 / np.sqrt(K))).astype(np.float32)
+    qw, sw = _rand_operand(rng, E * N, K, full_range)
+    # W1 output feeds a SwiGLU clamped at 10: keep the accumulators O(1) there (alpha_mult drives them past it)
+    alpha = (rng.uniform(0.5, 2.0, E) * (1.0 if which == 2 else 0.25 / np.sqrt(K)) * alpha_mult).astype(np.float32)
     por = np.full(cap, -1, np.int64)
     por[:R] = L["pair_of_row"]
     dev = dict(device="cuda")
@@ -79,16 +91,18 @@ def _setup(H, I, counts, seed, which):
     return cfg, T, cap, ids, L, (qa, sa, qw, sw, alpha), t
 
 
-@pytest.mark.parametrize("H,I,counts", [
-    (256, 128, [1, 0, 130, 5]),          # K = 128: one partial stage (2 scale atoms)
-    (256, 768, [300, 1, 0]),             # K = 768: 3 full stages
-    (512, 2048, [129, 128, 0, 2]),       # K = 2048: 8 stages around a 3-deep ring
-    (256, 768, [600, 5, 130]),           # T >= E * 128: the dynamic chunk schedule (5-, 1- and 2-m-tile experts)
+@pytest.mark.parametrize("H,I,counts,full_range", [
+    (256, 128, [1, 0, 130, 5], False),          # K = 128: one partial stage (2 scale atoms)
+    (256, 768, [300, 1, 0], False),             # K = 768: 3 full stages
+    (512, 2048, [129, 128, 0, 2], False),       # K = 2048: 8 stages around a 3-deep ring
+    (256, 768, [600, 5, 130], False),           # T >= E * 128: the dynamic chunk schedule (5-, 1-, 2-m-tile experts)
+    (256, 768, [3, 0, 140], True),              # every finite E4M3 scale byte, static schedule
+    (256, 768, [600, 5, 130], True),            # every finite E4M3 scale byte, dynamic schedule
 ])
-def test_w2_rows_against_fp64(H, I, counts):
+def test_w2_rows_against_fp64(H, I, counts, full_range):
     import torch
     from block_scaled_fp4_top_gb300 import api
-    cfg, T, cap, ids, L, (qa, sa, qw, sw, alpha), t = _setup(H, I, counts, 1, which=2)
+    cfg, T, cap, ids, L, (qa, sa, qw, sw, alpha), t = _setup(H, I, counts, 1, which=2, full_range=full_range)
     o = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
     api.moe_grouped_gemm_w2(cfg, T, t["a"], t["asf"], t["poff"], t["por"], t["w"], t["wsf"], t["alpha"], o, t["ws"])
     torch.cuda.synchronize()
@@ -130,37 +144,52 @@ def test_w2_rows_to_a_16_byte_aligned_buffer():
     assert torch.equal(o.view(torch.int32), o16.view(torch.int32))
 
 
-@pytest.mark.parametrize("H,I,counts", [(256, 128, [3, 0, 140]), (512, 256, [1, 257, 2]),
-                                        (256, 128, [600, 5, 130])])   # the last one takes the dynamic schedule
-def test_w1_swiglu_requant(H, I, counts):
-    import torch
-    from block_scaled_fp4_top_gb300 import api
-    cfg, T, cap, ids, L, (qa, sa, qw, sw, alpha), t = _setup(H, I, counts, 2, which=1)
-    E = len(counts)
+def _w1_reference(I, ids, L, qa, sa, qw, sw, alpha, cap):
+    """fp64 gate, up and the oracle's SwiGLU h [cap, I] of every real row (kernel row order -> features)."""
+    E = len(alpha)
+    H = qa.shape[1]
     A = _dec(qa, sa)
-    Wk = _dec(qw, sw).reshape(E, 2 * I, H)  # kernel row order
-    # kernel row order -> gate/up features
+    Wk = _dec(qw, sw).reshape(E, 2 * I, H)
     f = np.arange(I)
     gate_rows = 128 * (f // 64) + f % 64
     up_rows = gate_rows + 64
-    R = L["R"]
-    h = np.zeros((cap, I))
-    for r in range(R):
+    g = np.zeros((cap, I))
+    u = np.zeros((cap, I))
+    for r in range(L["R"]):
         p = L["pair_of_row"][r]
         if p < 0:
             continue
-        e = int(ids[p, 0])
-        acc = Wk[e] @ A[r] * alpha[e]
-        h[r] = moe.swiglu(acc[gate_rows], acc[up_rows], 10.0)
-    gs2 = nvfp4.global_scale(np.float32(np.abs(h).max()))
+        acc = Wk[int(ids[p, 0])] @ A[r] * alpha[int(ids[p, 0])]
+        g[r], u[r] = acc[gate_rows], acc[up_rows]
+    return g, u, moe.swiglu(g, u, 10.0)
+
+
+def _run_w1(cfg, T, cap, I, t, gs2, alpha=None):
+    import torch
+    from block_scaled_fp4_top_gb300 import api
     a2 = torch.full((cap * I // 2,), 0xEE, dtype=torch.uint8, device="cuda")
     a2sf = torch.full((cap * I // 16,), 0xEE, dtype=torch.uint8, device="cuda")
-    api.moe_grouped_gemm_w1_swiglu(cfg, T, t["a"], t["asf"], t["poff"], t["por"], t["w"], t["wsf"], t["alpha"],
+    api.moe_grouped_gemm_w1_swiglu(cfg, T, t["a"], t["asf"], t["poff"], t["por"], t["w"], t["wsf"],
+                                   t["alpha"] if alpha is None else alpha,
                                    torch.tensor([gs2], dtype=torch.float32, device="cuda"), a2, a2sf, t["ws"])
     torch.cuda.synchronize()
+    return a2.cpu().numpy().reshape(cap, I // 2), a2sf.cpu().numpy()
+
+
+@pytest.mark.parametrize("H,I,counts,full_range", [(256, 128, [3, 0, 140], False), (512, 256, [1, 257, 2], False),
+                                                   (256, 128, [600, 5, 130], False),  # the dynamic schedule
+                                                   (256, 256, [3, 0, 140], True),     # every finite E4M3 scale byte
+                                                   (256, 256, [600, 5, 130], True)])
+def test_w1_swiglu_requant(H, I, counts, full_range):
+    from block_scaled_fp4_top_gb300 import api
+    cfg, T, cap, ids, L, (qa, sa, qw, sw, alpha), t = _setup(H, I, counts, 2, which=1, full_range=full_range)
+    R = L["R"]
+    _, _, h = _w1_reference(I, ids, L, qa, sa, qw, sw, alpha, cap)
+    gs2 = nvfp4.global_scale(np.float32(np.abs(h).max()))
+    codes, sf_all = _run_w1(cfg, T, cap, I, t, gs2)
     assert api.fp4moe_read_error(t["ws"]) == 0
-    codes = a2.cpu().numpy().reshape(cap, I // 2)[:R]
-    sf = nvfp4.unswizzle(a2sf.cpu().numpy()[: R * I // 16], R, I // 16)
+    codes = codes[:R]
+    sf = nvfp4.unswizzle(sf_all[: R * I // 16], R, I // 16)
     q_ref, s_ref = nvfp4.quantize_rows(h[:R].astype(np.float32), gs2)
     got_deq = nvfp4.dequantize(nvfp4.unpack_codes(codes), sf, gs2)
     ref_deq = nvfp4.dequantize(q_ref, s_ref, gs2)
@@ -173,6 +202,63 @@ def test_w1_swiglu_requant(H, I, counts):
     rel = np.linalg.norm(got_deq[real] - ref_deq[real]) / np.linalg.norm(ref_deq[real])
     assert rel < 2e-2, rel
     assert (sf[real] == s_ref[real]).mean() >= 0.99
+
+
+def test_w1_swiglu_clamp_past_the_limit():
+    """Gate and up driven to an RMS of about 46 (alpha x 8): a large share of both is clamped. Where gate and up are
+    both past the limit, h is +-silu(10) * 10 exactly and the codes must equal the oracle's; elsewhere they agree
+    up to rounding ties. A missing lower clamp on up, a gate clamped on both sides or a wrong limit fail it."""
+    from block_scaled_fp4_top_gb300 import api
+    H, I, counts = 256, 256, [3, 0, 140, 1]
+    cfg, T, cap, ids, L, (qa, sa, qw, sw, alpha), t = _setup(H, I, counts, 4, which=1, alpha_mult=8.0)
+    R = L["R"]
+    g, u, h = _w1_reference(I, ids, L, qa, sa, qw, sw, alpha, cap)
+    real = L["pair_of_row"] >= 0
+    gr, ur = g[:R][real], u[:R][real]
+    assert (gr > 10).mean() > 0.2 and (gr < -10).mean() > 0.2, "gate not driven past the limit"
+    assert (np.abs(ur) > 10).mean() > 0.4, "up not driven past the limit"
+    gs2 = nvfp4.global_scale(np.float32(np.abs(h).max()))
+    codes, sf_all = _run_w1(cfg, T, cap, I, t, gs2)
+    assert api.fp4moe_read_error(t["ws"]) == 0
+    got = nvfp4.unpack_codes(codes[:R])[real]
+    q_ref, s_ref = nvfp4.quantize_rows(h[:R].astype(np.float32), gs2)
+    q_ref = q_ref[real]
+    both = (gr > 10) & (np.abs(ur) > 10)
+    assert both.sum() > 1000
+    assert np.array_equal(got[both], q_ref[both]), "codes of doubly clamped elements differ from the oracle's"
+    assert (got == q_ref).mean() >= 0.995
+    sf = nvfp4.unswizzle(sf_all[: R * I // 16], R, I // 16)
+    assert (sf[real] == s_ref[real]).mean() >= 0.99
+
+
+def test_w1_nan_alpha_sets_the_nan_bit_and_spares_other_experts():
+    """A NaN alpha makes its expert's gate and up NaN. The oracle's SwiGLU gives NaN there (it has no codes for
+    such rows); the epilogue must raise FP4MOE_ERR_NAN, and every other expert's codes and scales must equal
+    those of a run with a finite alpha, bit for bit."""
+    import torch
+    from block_scaled_fp4_top_gb300 import _lib, api
+    H, I, counts = 256, 128, [3, 0, 140, 5]
+    cfg, T, cap, ids, L, (qa, sa, qw, sw, alpha), t = _setup(H, I, counts, 6, which=1)
+    R = L["R"]
+    _, _, h = _w1_reference(I, ids, L, qa, sa, qw, sw, alpha, cap)
+    gs2 = nvfp4.global_scale(np.float32(np.abs(h).max()))
+    clean_codes, clean_sf = _run_w1(cfg, T, cap, I, t, gs2)
+    assert api.fp4moe_read_error(t["ws"]) == 0
+    bad = alpha.copy()
+    bad[2] = np.nan
+    with np.errstate(invalid="ignore"):
+        _, _, h_bad = _w1_reference(I, ids, L, qa, sa, qw, sw, bad, cap)
+    nan_codes, nan_sf = _run_w1(cfg, T, cap, I, t, gs2, alpha=torch.from_numpy(bad).cuda())
+    assert api.fp4moe_read_error(t["ws"]) == _lib.ERR_NAN
+    por = L["pair_of_row"]
+    expert_of_row = np.where(por >= 0, ids[np.maximum(por, 0), 0], -1)
+    rows2 = np.nonzero(expert_of_row == 2)[0]
+    others = np.nonzero((expert_of_row >= 0) & (expert_of_row != 2))[0]
+    assert np.isnan(h_bad[rows2]).all() and not np.isnan(h_bad[others]).any()
+    assert np.array_equal(nan_codes[others], clean_codes[others])
+    C = I // 16
+    sfo = lambda flat: nvfp4.unswizzle(flat[: R * C], R, C)[others]
+    assert np.array_equal(sfo(nan_sf), sfo(clean_sf))
 
 
 def test_combine_reads_16_byte_aligned_rows_the_same():

@@ -8,9 +8,11 @@ buffer is refilled, outside the graph, with a freshly seeded batch (seed
 Every replay must:
 * equal the eager call on the same input, bit for bit;
 * leave the device error word at zero.
-Replays 0 and 99 of every bucket also compare their top-k ids for all tokens
-with the oracle's routing. A few sampled tokens of those replays also compare
-their output rows with the oracle's layer, within the float bar.
+Replays 0 and 99 of every bucket also compare their top-k ids and weights for
+all tokens with the oracle's routing, and output rows with the oracle's layer
+(with the oracle's own warm-up scales) within the float bar: every token of
+the buckets T <= 64; the first, the last and two seeded tokens of every
+larger bucket.
 
 The captured step must contain no host synchronisation, allocation or
 device-value branch ("CUDA-Graph Safety / GPU-Native Requirements",
@@ -21,14 +23,22 @@ import numpy as np
 import pytest
 
 import synthgen as sg
-from helpers import OracleExperts, bits_to_torch, ensure_built, float_parity, make_layer, torch_to_bits
+from helpers import bits_to_torch, ensure_built, float_parity, make_layer, torch_to_bits
 from oracle import moe
 
 pytestmark = pytest.mark.gpu
 
 REPLAYS = 100
 CHECKED = (0, REPLAYS - 1)
-ORACLE_TOKENS = {1: [0], 64: [37], 4096: [4095]}  # bucket -> token rows checked against the oracle layer
+
+
+def oracle_tokens(T: int, replay: int) -> np.ndarray:
+    """Token rows whose outputs are checked against the oracle: all of them up to T = 64, else the first, the
+    last and two seeded others."""
+    if T <= 64:
+        return np.arange(T)
+    rng = np.random.default_rng(1000 * T + replay)
+    return np.sort(np.concatenate([[0, T - 1], rng.choice(np.arange(1, T - 1), 2, replace=False)]))
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -36,16 +46,19 @@ def _built():
     ensure_built()
 
 
-def test_graph_sweep_replays():
+def test_graph_sweep_replays(oracle_svc):
     import torch
     from synthgen import gpu as sgpu
     wl = sg.DSV4_DECODE
     Tmax = max(sg.GRAPH_SWEEP_T)
     layer = make_layer(wl, Tmax)
-    layer.calibrate(bits_to_torch(sg.activations_bf16(wl, sg.WARMUP_SEED, T=wl.T)))
-    gs1, gs2 = np.float32(layer.gs1.item()), np.float32(layer.gs2.item())
+    xw = sg.activations_bf16(wl, sg.WARMUP_SEED, T=wl.T)
+    layer.calibrate(bits_to_torch(xw))
+    gs1, gs2 = oracle_svc.calibrate(wl, xw)
+    assert float(layer.gs1.item()) == float(gs1)
+    assert float(layer.gs2.item()) == pytest.approx(float(gs2), rel=1e-5)
     wr = sg.router_bf16(wl)
-    experts = OracleExperts(wl)
+    checked_x, checked_y, labels = [], [], []   # rows compared with the oracle's layer after the sweep
     dev = "cuda"
     for T in sg.GRAPH_SWEEP_T:
         x = torch.empty(T, wl.H, dtype=torch.bfloat16, device=dev)
@@ -77,12 +90,18 @@ def test_graph_sweep_replays():
                 got_ids = ids.cpu().numpy().reshape(T, wl.k)
                 assert (got_ids == ids_ref).all(), f"T={T} replay {i}: top-k ids differ from the oracle"
                 assert np.allclose(w.cpu().numpy().reshape(T, wl.k), w_ref, rtol=3e-6, atol=1e-7)
-                rows = ORACLE_TOKENS.get(T, [])
-                if rows:
-                    y_ref = moe.moe_tokens(x_bits[rows], ids_ref[rows], w_ref[rows], experts, gs1, gs2,
-                                           wl.swiglu_limit)
-                    y_got = torch_to_bits(y)[rows]
-                    float_parity(sg.bf16_bits_to_f32(y_got), sg.bf16_bits_to_f32(y_ref))
+                rows = oracle_tokens(T, i)
+                checked_x.append(x_bits[rows])
+                checked_y.append(torch_to_bits(y)[rows])
+                labels.append((T, i))
         torch.cuda.synchronize()
         assert layer.read_error() == 0
         del g
+    # every checked row of every bucket against the oracle, in one pass over the experts
+    ref = oracle_svc.layer(wl, checked_x, gs1, gs2)
+    assert sum(len(r) for r in checked_x) == 2 * (127 + 4 * 6)
+    for (T, i), got, (y_ref, _, _) in zip(labels, checked_y, ref):
+        try:
+            float_parity(sg.bf16_bits_to_f32(got), sg.bf16_bits_to_f32(y_ref))
+        except AssertionError as exc:
+            raise AssertionError(f"T={T} replay {i}: {exc}") from None

@@ -13,9 +13,17 @@ unit.
 
 The layer's outputs must meet the float bar against the oracle's layer, and
 the top-k ids must match exactly:
-* at a tiny TP3 shape, on all three ranks and all tokens;
-* at the DeepSeek-V4-Flash shard (hidden 4096, 704 of 768, 256 experts,
-  top-k 6, T = 512), on rank 0 and sampled tokens.
+* at a tiny TP3 shape, on all three ranks and all tokens, with ordinary
+  weights and with weights large enough that most gate and up values pass
+  the SwiGLU limit;
+* a NaN in one token's x gives a NaN output row, as in the oracle, and
+  leaves the other tokens within the bar;
+* at the DeepSeek-V4-Flash shape, all three TP3 ranks (hidden 4096, 704 of
+  768, 256 experts, top-k 6) at T = 1, 8, 16 and 64, eager and under CUDA
+  graph replay: each rank against the oracle's shard, and the three ranks'
+  sum against the oracle's full-width layer ("4. MoE hardware tests");
+* on rank 0 at T = 512, 64 sampled tokens.
+The DSV4-scale oracle work runs on the test-side worker pool.
 """
 import dataclasses
 
@@ -86,18 +94,22 @@ def _forward(layer, x_bits, k):
     return torch_to_bits(y), ids.cpu().numpy().reshape(T, k)
 
 
-def test_tiny_tp3_all_ranks():
+@pytest.mark.parametrize("w_sigma", [0.05, 1.5])   # 1.5: gate and up far past the SwiGLU limit
+def test_tiny_tp3_all_ranks(w_sigma):
     import torch
     rng = np.random.default_rng(21)
     H, I, E, k, T = 256, 192, 8, 2, 16
     plan = mxfp4.tp_plan(I, 3, 32, 128)
     Ik, Il = plan.kernel_local, plan.logical_per_rank
     assert (Il, Ik) == (64, 128)
-    w1f = (rng.standard_normal((E, 2 * I, H)) * 0.05).astype(np.float32)
+    w1f = (rng.standard_normal((E, 2 * I, H)) * w_sigma).astype(np.float32)
     w2f = (rng.standard_normal((E, H, I)) * 0.05).astype(np.float32)
     router = moe.f32_to_bf16_bits((rng.standard_normal((E, H)) / 16).astype(np.float32))
     x_bits = moe.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
     ids_ref, w_ref = moe.topk_softmax(moe.router_logits(x_bits, router), k)
+    if w_sigma > 1:  # most gate and up values are clamped: a wrong clamp would move y far outside the bar
+        gu = moe.bf16_to_f64(x_bits) @ w1f[0].astype(np.float64).T
+        assert (gu[:, :I] > 10).mean() > 0.3 and (np.abs(gu[:, I:]) > 10).mean() > 0.6
     y_sum = np.zeros((T, H))
     for rank in range(3):
         layer = _mx_layer(H, Ik, Il, E, k, T)
@@ -126,41 +138,109 @@ def test_tiny_tp3_all_ranks():
     float_parity(y_sum, sg.bf16_bits_to_f32(y_full))
 
 
-def test_dsv4_tp3_rank0_sampled_tokens():
+def test_nan_token_propagates_to_its_output_row():
+    """bf16 activations with MXFP4 weights have no activation quantiser: a NaN in x flows through both GEMMs
+    into the token's output row, as it does in the oracle. The other tokens stay within the bar."""
+    import torch
+    rng = np.random.default_rng(22)
+    H, I, E, k, T = 256, 128, 8, 2, 16
+    plan = mxfp4.tp_plan(I, 1, 32, 128)
+    w1f = (rng.standard_normal((E, 2 * I, H)) * 0.05).astype(np.float32)
+    w2f = (rng.standard_normal((E, H, I)) * 0.05).astype(np.float32)
+    router = moe.f32_to_bf16_bits((rng.standard_normal((E, H)) / 16).astype(np.float32))
+    x_bits = moe.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    x_bits[5, 40] = 0x7FC0
+    layer = _mx_layer(H, I, I, E, k, T)
+    layer.quantize_weights(1, 0, torch.from_numpy(w1f).cuda())
+    layer.quantize_weights(2, 0, torch.from_numpy(w2f).cuda())
+    layer.set_router(bits_to_torch(router))
+    y, ids = _forward(layer, x_bits, k)
+    ex = {e: mxfp4.mx_expert_shard(w1f[e], w2f[e], plan, 0) for e in range(E)}
+    with np.errstate(invalid="ignore"):
+        ids_ref, w_ref = moe.topk_softmax(moe.router_logits(x_bits, router), k)
+        y_ref = sg.bf16_bits_to_f32(mxfp4.mx_moe_tokens(x_bits, ids_ref, w_ref, lambda e: ex[e], 10.0))
+    yf = sg.bf16_bits_to_f32(y)
+    assert np.isnan(y_ref[5]).all() and np.isnan(yf[5]).all()
+    others = np.arange(T) != 5
+    assert (ids[others] == ids_ref[others]).all()
+    float_parity(yf[others], y_ref[others])
+
+
+def _dsv4_mx_rank_layer(wl, wl_full, plan, rank, max_tokens, chunk=8):
+    """The DSV4 TP3 rank's layer: the kernel-local fp32 shard of the generator's full-width experts, cut on the
+    GPU and quantised by the library."""
     import torch
     from synthgen import gpu as sgpu
-    wl = sg.TP3_MXFP4
-    wl_full = dataclasses.replace(wl, I=2048, I_logical=2048)  # the generator's view of the unsharded experts
-    plan = mxfp4.tp_plan(2048, 3, 32, 128)
-    Ik, Il = plan.kernel_local, plan.logical_per_rank
-    assert (Il, Ik, wl.I, wl.I_logical) == (704, 768, 768, 704)
-    rank, chunk = 0, 8
-    layer = _mx_layer(wl.H, Ik, Il, wl.E, wl.k, wl.T)
+    Ik, Il, If = plan.kernel_local, plan.logical_per_rank, wl_full.I
+    a, n = rank * Il, max(0, min(Il, If - rank * Il))
+    layer = _mx_layer(wl.H, Ik, Il, wl.E, wl.k, max_tokens)
     for e0 in range(0, wl.E, chunk):
         w1f = sgpu.expert_w1(wl_full, e0, chunk)
         w1l = torch.zeros(chunk, 2 * Ik, wl.H, dtype=torch.float32, device="cuda")
-        w1l[:, :Il] = w1f[:, rank * Il:rank * Il + Il]
-        w1l[:, Ik:Ik + Il] = w1f[:, 2048 + rank * Il:2048 + rank * Il + Il]
+        w1l[:, :n] = w1f[:, a:a + n]
+        w1l[:, Ik:Ik + n] = w1f[:, If + a:If + a + n]
         del w1f
         layer.quantize_weights(1, e0, w1l)
         w2f = sgpu.expert_w2(wl_full, e0, chunk)
         w2l = torch.zeros(chunk, wl.H, Ik, dtype=torch.float32, device="cuda")
-        w2l[:, :, :Il] = w2f[:, :, rank * Il:rank * Il + Il]
+        w2l[:, :, :n] = w2f[:, :, a:a + n]
         del w2f
         layer.quantize_weights(2, e0, w2l)
         torch.cuda.synchronize()
     layer.set_router(sgpu.router(wl))
+    return layer
+
+
+def test_dsv4_tp3_three_ranks_sum_to_the_full_width_layer(oracle_svc):
+    import torch
+    wl = sg.TP3_MXFP4
+    wl_full = dataclasses.replace(wl, I=2048, I_logical=2048)   # the generator's view of the unsharded experts
+    plan = mxfp4.tp_plan(2048, 3, 32, 128)
+    assert (plan.logical_per_rank, plan.kernel_local) == (704, 768)
+    full = mxfp4.tp_plan(2048, 1, 32, 128)
+    Ts = (1, 8, 16, 64)
+    x_bits = sg.activations_bf16(wl, sg.EVAL_SEED, T=max(Ts))  # the smaller batches are its leading rows
+    ids_ref, w_ref = moe.topk_softmax(moe.router_logits(x_bits, sg.router_bf16(wl)), wl.k)
+    parts = oracle_svc.mx_partials(wl_full, x_bits, ids_ref, [(plan, 0), (plan, 1), (plan, 2), (full, 0)])
+    y_rank_ref = [sg.bf16_bits_to_f32(moe.combine(ids_ref, w_ref, o)) for o in parts[:3]]
+    y_full_ref = sg.bf16_bits_to_f32(moe.combine(ids_ref, w_ref, parts[3]))
+    sums = {T: np.zeros((T, wl.H)) for T in Ts}
+    for rank in range(3):
+        layer = _dsv4_mx_rank_layer(wl, wl_full, plan, rank, max(Ts))
+        for T in Ts:
+            y, ids = _forward(layer, x_bits[:T], wl.k)
+            assert (ids == ids_ref[:T]).all(), (rank, T)
+            yf = sg.bf16_bits_to_f32(y)
+            float_parity(yf, y_rank_ref[rank][:T])
+            sums[T] += yf
+            # the same call captured in a CUDA graph and replayed gives the eager rows, bit for bit
+            xs = bits_to_torch(x_bits[:T])
+            ys = torch.empty(T, wl.H, dtype=torch.bfloat16, device="cuda")
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                layer.forward(xs, ys)
+            for _ in range(2):
+                ys.fill_(0)
+                g.replay()
+                torch.cuda.synchronize()
+                assert np.array_equal(torch_to_bits(ys), y), (rank, T)
+            assert layer.read_error() == 0
+            del g
+        del layer
+        torch.cuda.empty_cache()
+    for T in Ts:
+        float_parity(sums[T], y_full_ref[:T])
+
+
+def test_dsv4_tp3_rank0_T512_sampled_tokens(oracle_svc):
+    wl = sg.TP3_MXFP4
+    wl_full = dataclasses.replace(wl, I=2048, I_logical=2048)
+    plan = mxfp4.tp_plan(2048, 3, 32, 128)
+    layer = _dsv4_mx_rank_layer(wl, wl_full, plan, 0, wl.T)
     x_bits = sg.activations_bf16(wl, sg.EVAL_SEED)
     y, ids = _forward(layer, x_bits, wl.k)
     ids_ref, w_ref = moe.topk_softmax(moe.router_logits(x_bits, sg.router_bf16(wl)), wl.k)
     assert (ids == ids_ref).all()
-    rows = np.array([0, 511])
-    cache = {}
-
-    def expert(e):
-        if e not in cache:
-            cache[e] = mxfp4.mx_expert_shard(sg.expert_w1_f32(wl_full, e), sg.expert_w2_f32(wl_full, e), plan, rank)
-        return cache[e]
-
-    y_ref = mxfp4.mx_moe_tokens(x_bits[rows], ids_ref[rows], w_ref[rows], expert, wl.swiglu_limit)
-    float_parity(sg.bf16_bits_to_f32(y[rows]), sg.bf16_bits_to_f32(y_ref))
+    rows = np.sort(np.random.default_rng(512).choice(wl.T, 64, replace=False))
+    part, = oracle_svc.mx_partials(wl_full, x_bits[rows], ids_ref[rows], [(plan, 0)])
+    float_parity(sg.bf16_bits_to_f32(y[rows]), sg.bf16_bits_to_f32(moe.combine(ids_ref[rows], w_ref[rows], part)))

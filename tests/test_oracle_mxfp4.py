@@ -144,8 +144,58 @@ def test_layer_on_exactly_representable_weights_is_the_textbook_moe():
             h = h.float().bfloat16().double()
             y[t] += float(w[t, j]) * (W2 @ h)
     ref = y.float().bfloat16().view(torch.int16).numpy().view(np.uint16)
-    ok = (got == ref) | (np.abs(sg_bf16_to_f32(got) - sg_bf16_to_f32(ref)) <= 2 ** -7 * np.abs(sg_bf16_to_f32(ref)))
-    assert ok.all()
+    # the dense path rounds h and y exactly as the oracle does; only the fp64 summation order differs, which
+    # cannot move a bf16 rounding here, so the bits must agree (a truncating or skipped h rounding would not)
+    assert np.array_equal(got, ref)
+
+
+def _torch_bf16(v64):
+    import torch
+    return torch.from_numpy(np.asarray(v64, dtype=np.float64)).float().bfloat16().double().numpy()
+
+
+def test_bf16_round_is_round_to_nearest_even_through_fp32():
+    """_bf16_round against torch's fp64 -> fp32 -> bf16 conversion, on exact bf16 ties (low half 0x8000 with
+    even and odd high halves), the fp32 neighbours of every tie, exact bf16 values, and fp64 values a hair
+    above or below a tie that fp32 rounding moves onto it."""
+    pytest.importorskip("torch")
+    rng = np.random.default_rng(3)
+    hi = rng.integers(0, 0x7F00, 2048).astype(np.uint32)            # finite, both parities of the last bf16 bit
+    lows = np.array([0x8000, 0x7FFF, 0x8001, 0x0000, 0xFFFF, 0x4000, 0xC000], dtype=np.uint32)
+    bits = ((hi[:, None] << 16) | lows[None, :]).reshape(-1)
+    v32 = bits.view(np.float32).astype(np.float64)
+    v = np.concatenate([v32, -v32, v32 * (1 + 2.0 ** -40), v32 * (1 - 2.0 ** -40), -v32 * (1 + 2.0 ** -40)])
+    got = mxfp4._bf16_round(v)
+    ref = _torch_bf16(v)
+    assert np.array_equal(got.view(np.uint64), ref.view(np.uint64))
+    # the ties themselves go to the even neighbour, which truncation (or no rounding) would not give
+    tie = v32[(bits & 0xFFFF) == 0x8000]
+    up = ((tie.astype(np.float32).view(np.uint32) >> 16) & 1) == 1
+    r = mxfp4._bf16_round(tie).astype(np.float32).view(np.uint32) >> 16
+    assert ((r & 1) == 0).all() and (r[up] == (tie[up].astype(np.float32).view(np.uint32) >> 16) + 1).all()
+
+
+def test_expert_out_rounds_h_to_bf16_before_w2():
+    """With W2 the identity (exact in MXFP4: 1 = E2M1 4 x 2^-2), mx_expert_out returns h itself after its bf16
+    rounding. Checked bit for bit against torch's SwiGLU in fp64 rounded to bf16."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(8)
+    H = I = 64
+    vals = codecs.e2m1_decode(np.arange(16, dtype=np.uint8))
+    q = rng.integers(0, 16, (2 * I, H)).astype(np.uint8)
+    q[:, ::32] = 7                                                   # amax 6 per block: X = 0 after the shift
+    w1 = (vals[q] * 2.0 ** -3).astype(np.float32)                    # exact in MXFP4
+    w2 = np.eye(H, I, dtype=np.float32)
+    ex = mxfp4.mx_expert_shard(w1, w2, mxfp4.tp_plan(I, 1, 32, 64), 0)
+    assert np.array_equal(mxfp4.mx_dequantize(ex.w1_q, ex.w1_s), w1.astype(np.float64))
+    assert np.array_equal(mxfp4.mx_dequantize(ex.w2_q, ex.w2_s), w2.astype(np.float64))
+    x = sg_bf16_to_f32(moe.f32_to_bf16_bits((rng.standard_normal((16, H)) * 3).astype(np.float32))).astype(np.float64)
+    o = mxfp4.mx_expert_out(ex, x, 10.0)
+    gu = torch.from_numpy(x) @ torch.from_numpy(w1.astype(np.float64)).T      # exact: few-bit products, short sums
+    g, u = gu[:, :I].clamp(max=10.0), gu[:, I:].clamp(-10.0, 10.0)
+    h = (g * torch.sigmoid(g) * u).float().bfloat16().double().numpy()
+    assert np.array_equal(o, h)
+    assert not np.array_equal(o, (g * torch.sigmoid(g) * u).numpy())   # the rounding is really there
 
 
 def sg_bf16_to_f32(u):

@@ -3,6 +3,7 @@ import json
 import os
 
 import numpy as np
+import pytest
 
 from oracle import codecs, nvfp4
 
@@ -127,3 +128,20 @@ def test_per_expert_swizzle_equals_whole_buffer_when_starts_are_aligned():
     packed = np.concatenate([b[:c] for b, c in zip(blocks, counts)])
     packed = np.concatenate([packed, np.zeros((len(per_expert) // C - len(packed), C), dtype=np.uint8)])
     assert not (nvfp4.swizzle(packed) == per_expert).all()
+
+
+def test_e4m3_saturation_threshold_is_the_midpoint_464():
+    """block_scales' saturation threshold: above 464 E4M3 rounding would leave 448 (0x7E); at or below it the
+    scale byte is an ordinary rounding to 448 or less. Checked against torch's float8_e4m3fn conversion, which
+    rounds to nearest even (and overflows to NaN instead of saturating)."""
+    torch = pytest.importorskip("torch")
+    s = np.array([448.0, 450.0, 463.99997, 464.0, np.nextafter(np.float32(464.0), np.float32(1e9)), 470.0, 500.0],
+                 dtype=np.float32)
+    t = torch.from_numpy(s).to(torch.float8_e4m3fn).float().numpy()
+    rounds_above = ~(t <= 448.0)                       # NaN (overflow) or a value above 448
+    assert list(rounds_above) == list(s > nvfp4.E4M3_SATURATES_ABOVE)
+    # and the scale the quantiser takes for such a block is the saturated 448 byte
+    v = np.zeros((1, 16), np.float32)
+    v[0, 0] = 6.0 * 470.0                              # s = 470 with g = 1
+    assert nvfp4.block_scales(v, 1.0)[0, 0] == np.float32(470.0)
+    assert nvfp4.quantize_rows(v, 1.0)[1][0, 0] == 0x7E

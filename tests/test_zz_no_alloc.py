@@ -46,8 +46,9 @@ def _inputs(wl, T, seed):
     return x, wr, (None if bias is None else torch.from_numpy(bias).cuda())
 
 
-def _route_both(wl, T, seed, calls=2):
-    """moe_route once, then `calls` back-to-back moe_route_noalloc calls on the same inputs."""
+def _route_both(wl, T, seed, calls=2, null_err=False):
+    """moe_route once, then `calls` back-to-back moe_route_noalloc calls on the same inputs (with err NULL when
+    null_err: errors then go to the scratch's own word, which each call clears)."""
     import torch
     from block_scaled_fp4_top_gb300 import api
     cfg = api.config(wl.H, wl.I, wl.E, wl.k, max(T, 1), wl.swiglu_limit)
@@ -64,7 +65,7 @@ def _route_both(wl, T, seed, calls=2):
     for _ in range(calls):
         got = _outputs(wl, T, cap)
         api.moe_route_noalloc(cfg, T, x, wr, bias, got["logits"], got["ids"], got["w"], got["counts"],
-                              got["offsets"], got["poff"], got["slot"], got["por"], err)
+                              got["offsets"], got["poff"], got["slot"], got["por"], None if null_err else err)
         runs.append(got)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
@@ -90,6 +91,49 @@ def test_noalloc_matches_moe_route_two_calls_in_a_row(wl, T):
     ref, runs = _route_both(wl, T, sg.EVAL_SEED, calls=2)
     for got in runs:
         _compare(ref, got, T, wl.k)
+
+
+def test_noalloc_with_no_error_word():
+    ref, runs = _route_both(sg.DSV4_DECODE, 64, sg.EVAL_SEED, calls=2, null_err=True)
+    for got in runs:
+        _compare(ref, got, 64, sg.DSV4_DECODE.k)
+
+
+def test_noalloc_takes_no_device_memory_eager_or_captured():
+    """After a first eager call, further calls (eager, and captured in a CUDA graph and replayed) leave the
+    device's free memory as it was: the call allocates nothing. The replay gives the eager outputs."""
+    import torch
+    from block_scaled_fp4_top_gb300 import api
+    wl, T = sg.DSV4_DECODE, 64
+    cfg = api.config(wl.H, wl.I, wl.E, wl.k, T, wl.swiglu_limit)
+    cap = api.capacity_rows(cfg, T)
+    x, wr, bias = _inputs(wl, T, sg.EVAL_SEED)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    eager, cap_out = _outputs(wl, T, cap), _outputs(wl, T, cap)
+    call = lambda o, stream=None: api.moe_route_noalloc(cfg, T, x, wr, bias, o["logits"], o["ids"], o["w"],
+                                                        o["counts"], o["offsets"], o["poff"], o["slot"], o["por"],
+                                                        err, stream)
+    call(eager)                                             # the first call on the device, outside capture
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    call(eager)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            call(cap_out, s)
+    torch.cuda.current_stream().wait_stream(s)
+    free1 = torch.cuda.mem_get_info()[0]                    # the graph itself may hold memory; the call adds none
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free1
+    assert int(err.item()) == 0
+    for key in eager:
+        assert torch.equal(eager[key], cap_out[key]), key
 
 
 def test_noalloc_tiny_and_empty():
