@@ -49,6 +49,8 @@ SIGNATURES = {
     "moe_grouped_gemm_w2_combine": (c_i32, [CP, c_i32] + [c_vp] * 11),
     "moe_forward": (c_i32, [CP, c_i32] + [c_vp] * 16),
     "fp4moe_quantize_weights": (c_i32, [CP, c_i32, c_i32] + [c_vp] * 5),
+    "fp4moe_tp_shard_units": (c_i32, [c_i32] * 6 + [ctypes.POINTER(c_i32)] * 3),
+    "fp4moe_shard_mxfp4": (c_i32, [CP] + [c_i32] * 5 + [c_vp] * 5),
     "fp4moe_make_alpha": (c_i32, [c_i32] + [c_vp] * 4),
     "fp4moe_calibrate": (c_i32, [CP, c_i32] + [c_vp] * 10),
     "fp4moe_quantize_rows_f32": (c_i32, [c_i32, c_i32] + [c_vp] * 5),

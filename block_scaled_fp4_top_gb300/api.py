@@ -129,6 +129,20 @@ def fp4moe_quantize_weights(cfg, which, n_experts, w, codes_out, sf_out, gs_out,
                                                _p(sf_out), _p(gs_out), _s(stream)), "fp4moe_quantize_weights")
 
 
+def fp4moe_tp_shard_units(width, tp, align, kernel_align, rank, unit):
+    """(source offset, units copied, zero tail) of one rank's slice, in storage units (host arithmetic)."""
+    out = [ctypes.c_int32() for _ in range(3)]
+    _check(_lib.load().fp4moe_tp_shard_units(width, tp, align, kernel_align, rank, unit,
+                                             *[ctypes.byref(v) for v in out]), "fp4moe_tp_shard_units")
+    return tuple(v.value for v in out)
+
+
+def fp4moe_shard_mxfp4(cfg, which, n_experts, full_inter, tp, tp_rank, ck_codes, ck_sf, codes_out, sf_out,
+                       stream=None):
+    _check(_lib.load().fp4moe_shard_mxfp4(ctypes.byref(cfg), which, n_experts, full_inter, tp, tp_rank, _p(ck_codes),
+                                          _p(ck_sf), _p(codes_out), _p(sf_out), _s(stream)), "fp4moe_shard_mxfp4")
+
+
 def fp4moe_make_alpha(n, gs_act, gs_w, alpha, stream=None):
     _check(_lib.load().fp4moe_make_alpha(n, _p(gs_act), _p(gs_w), _p(alpha), _s(stream)), "fp4moe_make_alpha")
 
@@ -274,6 +288,22 @@ class MoELayer:
             codes, sf, gs = W.w2_fp4, W.w2_sf, W.gw2
         fp4moe_quantize_weights(cfg, which, n, w.contiguous(), codes[e0 * per_c:(e0 + n) * per_c],
                                 sf[e0 * per_s:(e0 + n) * per_s], gs[e0:e0 + n])
+
+    def shard_mxfp4_weights(self, which: int, e0: int, ck_codes: torch.Tensor, ck_sf: torch.Tensor,
+                            full_inter: int, tp: int, tp_rank: int):
+        """Cut rank tp_rank's shard of experts [e0, e0 + n) from a quantised full-width MXFP4 checkpoint.
+
+        which=1: ck_codes [n, 2 full_inter, H / 2] bytes (gate rows first), ck_sf [n, 2 full_inter, H / 32];
+        which=2: ck_codes [n, H, full_inter / 2], ck_sf [n, H, full_inter / 32] (see fp4moe_shard_mxfp4).
+        """
+        cfg, W = self.cfg, self.weights
+        n = ck_codes.shape[0]
+        E = cfg.ep_count or cfg.num_experts
+        b1, s1, b2, s2 = weight_bytes(cfg)
+        per_c, per_s = (b1 // E, s1 // E) if which == 1 else (b2 // E, s2 // E)
+        codes, sf = (W.w1_fp4, W.w1_sf) if which == 1 else (W.w2_fp4, W.w2_sf)
+        fp4moe_shard_mxfp4(cfg, which, n, full_inter, tp, tp_rank, ck_codes.contiguous(), ck_sf.contiguous(),
+                           codes[e0 * per_c:(e0 + n) * per_c], sf[e0 * per_s:(e0 + n) * per_s])
 
     def quantize_shared_weights(self, which: int, w: torch.Tensor):
         """Block-FP8 of the shared expert's W1 (which=1, [2 Is, H], gate rows then up) or W2 (which=2, [H, Is])."""

@@ -8,6 +8,7 @@
 // hidden host syncs, allocations and device-value branches that a captured
 // step must not contain.
 #include <algorithm>
+#include <climits>
 #include <cstring>
 #include <mutex>
 
@@ -20,6 +21,14 @@ namespace {
 
 inline bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// "Lucifer-CUTLASS TP3 virtual-padding audit", "TP3 shape plan": the logical width of each rank is
+// align_up(ceil(width / tp), align) and the kernel-local width rounds it up to kernel_align.
+inline void tp_widths(int64_t width, int64_t tp, int64_t align, int64_t kernel_align, int64_t& local,
+                      int64_t& kernel) {
+  local = ((width + tp - 1) / tp + align - 1) / align * align;
+  kernel = (local + kernel_align - 1) / kernel_align * kernel_align;
+}
 
 fp4moe_status check_cfg(const fp4moe_config* c) {
   if (c == nullptr) return FP4MOE_INVALID_ARG;
@@ -277,7 +286,7 @@ using namespace fp4moe;
 
 extern "C" {
 
-int32_t fp4moe_abi_version(void) { return 102; }
+int32_t fp4moe_abi_version(void) { return 103; }
 
 const char* fp4moe_status_string(fp4moe_status s) {
   switch (s) {
@@ -526,6 +535,44 @@ fp4moe_status fp4moe_quantize_weights(const fp4moe_config* cfg, int32_t which, i
     return FP4MOE_CUDA_ERROR;
   return quant_rows_launch((int64_t)n_experts * rows, K, rows, which == 1 ? cfg->inter : 0, 1, w, gs_out, rows,
                            codes_out, sf_out, st);
+}
+
+fp4moe_status fp4moe_tp_shard_units(int32_t width, int32_t tp, int32_t align, int32_t kernel_align, int32_t rank,
+                                    int32_t unit, int32_t* src_offset, int32_t* count, int32_t* zero_tail) {
+  if (width <= 0 || tp <= 0 || align <= 0 || kernel_align <= 0 || unit <= 0 || rank < 0 || rank >= tp)
+    return FP4MOE_INVALID_ARG;
+  int64_t local = 0, kernel = 0;
+  tp_widths(width, tp, align, kernel_align, local, kernel);
+  const int64_t start = (int64_t)rank * local;
+  const int64_t n = std::max<int64_t>(0, std::min<int64_t>(local, (int64_t)width - start));
+  // a slice that splits a storage unit cannot be cut in that unit
+  if (start % unit != 0 || n % unit != 0 || kernel % unit != 0 || kernel > INT32_MAX) return FP4MOE_UNSUPPORTED;
+  if (src_offset) *src_offset = (int32_t)(start / unit);
+  if (count) *count = (int32_t)(n / unit);
+  if (zero_tail) *zero_tail = (int32_t)((kernel - n) / unit);
+  return FP4MOE_OK;
+}
+
+fp4moe_status fp4moe_shard_mxfp4(const fp4moe_config* cfg, int32_t which, int32_t n_experts, int32_t full_inter,
+                                 int32_t tp, int32_t tp_rank, const uint8_t* ck_codes, const uint8_t* ck_sf,
+                                 uint8_t* codes_out, uint8_t* sf_out, fp4moe_stream_t stream) {
+  FP4_TRY(check_cfg(cfg));
+  if (!is_mx(cfg)) return FP4MOE_UNSUPPORTED;
+  if (which != 1 && which != 2) return FP4MOE_INVALID_ARG;
+  if (n_experts < 0 || n_experts > local_experts(*cfg)) return FP4MOE_INVALID_ARG;
+  if (full_inter <= 0 || full_inter % 32 != 0) return FP4MOE_UNSUPPORTED;  // whole E8M0 groups, whole bytes
+  int32_t first = 0, count = 0, tail = 0;
+  FP4_TRY(fp4moe_tp_shard_units(full_inter, tp, 32, 128, tp_rank, 1, &first, &count, &tail));
+  // the plan's widths must be the layer's: the logical width per rank, and the kernel width it rounds up to
+  int64_t local = 0, kernel = 0;
+  tp_widths(full_inter, tp, 32, 128, local, kernel);
+  if (kernel != cfg->inter || local != cfg->inter_logical) return FP4MOE_INVALID_ARG;
+  FP4_TRY(check_ptrs(ck_codes, ck_sf, codes_out, sf_out));
+  const bool w1 = which == 1;
+  const int32_t rows = w1 ? 2 * cfg->inter : cfg->hidden;
+  const int32_t Kd = w1 ? cfg->hidden : cfg->inter;
+  return mx_shard_launch(n_experts, w1, rows, Kd, cfg->inter, full_inter, w1 ? cfg->hidden : full_inter, first, count,
+                         ck_codes, ck_sf, codes_out, sf_out, (cudaStream_t)stream);
 }
 
 fp4moe_status fp4moe_make_alpha(int32_t n, const float* gs_act, const float* gs_w, float* alpha,

@@ -100,6 +100,12 @@ fp4moe_status mx_gemm_launch(bool w2, const fp4moe_config& cfg, int32_t T, const
                              cudaStream_t st);
 fp4moe_status mx_quant_rows_launch(int64_t n_rows, int32_t K, int32_t rows_per_group, int32_t inter, const float* in,
                                    uint8_t* codes, uint8_t* sf, cudaStream_t st);
+// one TP rank's shard of a quantised full-width MXFP4 checkpoint into the atom-tiled layout (fp4moe_shard_mxfp4).
+// w1: rows = 2 Ik logical W13 rows, Kd = H; else rows = H, Kd = Ik. src_row_elems: elements of one source row
+// (H for W13, I_full for W2). first / count: the rank's logical slice of I.
+fp4moe_status mx_shard_launch(int32_t n_experts, bool w1, int32_t rows, int32_t Kd, int32_t Ik, int32_t full_inter,
+                              int32_t src_row_elems, int32_t first, int32_t count, const uint8_t* src_codes,
+                              const uint8_t* src_sf, uint8_t* codes, uint8_t* sf, cudaStream_t st);
 fp4moe_status scatter_rows_bf16_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x,
                                        const int32_t* slot_of_pair, uint16_t* a1, cudaStream_t st);
 

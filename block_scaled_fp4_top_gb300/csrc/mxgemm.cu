@@ -404,6 +404,55 @@ __global__ void __launch_bounds__(256) mx_quant_rows_kernel(int64_t n_rows, int 
   sf[blk_idx * MX_BS_BYTES + 2 * rr + (blk & 1)] = (uint8_t)(X + 127);
 }
 
+// One rank's kernel-local shard cut from an already quantised full-width MXFP4 checkpoint ("Lucifer-CUTLASS
+// TP3 virtual-padding audit", "Packed W2 weight is wrong", "W2 E8M0 scales are wrong", "Required loader
+// changes"). The slice is counted in logical elements and read in each tensor's own storage unit: W13 in
+// unpacked rows, packed W2 codes in bytes of 2 elements, E8M0 scales in groups of 32. Destinations past the
+// rank's logical count get zero codes and zero scale bytes. One thread moves one 32-element group (16 code
+// bytes and one scale byte) into the atom-tiled layout that the MX GEMMs read.
+//   W13 (w1 = true): src codes [n][2 I_full][K / 2], scales [n][2 I_full][K / 32]; dest logical row lr of
+//     [0, 2 Ik): gate rows [0, Ik), up rows [Ik, 2 Ik); the source row of kernel feature f < count is
+//     (up ? I_full : 0) + first + f.
+//   W2 (w1 = false): src codes [n][rows][I_full / 2], scales [n][rows][I_full / 32]; dest group b < Ik / 32
+//     holds source elements first + 32 b .. first + 32 b + 31 when 32 b < count.
+__global__ void __launch_bounds__(256) mx_shard_kernel(int64_t n_items, bool w1, int rows, int Kd, int Ik,
+                                                       int full_inter, int src_row_elems, int first, int count,
+                                                       const uint8_t* __restrict__ src_codes,
+                                                       const uint8_t* __restrict__ src_sf,
+                                                       uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+  const int nb = Kd / 32;  // destination groups per row
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n_items) return;
+  const int64_t row = idx / nb;  // destination row over all experts
+  const int blk = (int)(idx - row * nb);
+  const int64_t g = row / rows;
+  const int lr = (int)(row - g * rows);
+  int kr = lr;  // row in kernel order
+  int64_t src_row = -1, src_elem = 0;  // source row (over all experts) and element offset inside it
+  if (w1) {
+    const bool up = lr >= Ik;
+    const int f = up ? lr - Ik : lr;
+    kr = 128 * (f / 64) + (up ? 64 : 0) + f % 64;
+    if (f < count) {
+      src_row = g * 2 * (int64_t)full_inter + (up ? full_inter : 0) + first + f;
+      src_elem = 32 * (int64_t)blk;
+    }
+  } else if (32 * blk < count) {
+    src_row = row;
+    src_elem = first + 32 * (int64_t)blk;
+  }
+  uint4 c = make_uint4(0u, 0u, 0u, 0u);
+  uint8_t s = 0;
+  if (src_row >= 0) {
+    c = *reinterpret_cast<const uint4*>(src_codes + src_row * (src_row_elems / 2) + src_elem / 2);
+    s = src_sf[src_row * (src_row_elems / 32) + src_elem / 32];
+  }
+  const int ka = Kd / 64, rt = kr / 128, rr = kr % 128, atom = blk / 2;
+  const size_t blk_idx = ((size_t)g * (rows / 128) + rt) * ka + atom;
+  *reinterpret_cast<uint4*>(codes + blk_idx * MX_BC_BYTES + 32 * rr + 16 * (blk & 1)) = c;
+  sf[blk_idx * MX_BS_BYTES + 2 * rr + (blk & 1)] = s;
+}
+
 // bf16 activation rows into slot order: each token's row goes to its k slots.
 __global__ void __launch_bounds__(256) scatter_rows_bf16_kernel(int H, int k, const uint16_t* __restrict__ x,
                                                                 const int32_t* __restrict__ slot_of_pair,
@@ -469,6 +518,16 @@ fp4moe_status mx_quant_rows_launch(int64_t n_rows, int32_t K, int32_t rows_per_g
   if (n_rows == 0) return FP4MOE_OK;
   const int64_t n = n_rows * (K / 32);
   mx_quant_rows_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(n_rows, K, rows_per_group, inter, in, codes, sf);
+  return cudaGetLastError() == cudaSuccess ? FP4MOE_OK : FP4MOE_CUDA_ERROR;
+}
+
+fp4moe_status mx_shard_launch(int32_t n_experts, bool w1, int32_t rows, int32_t Kd, int32_t Ik, int32_t full_inter,
+                              int32_t src_row_elems, int32_t first, int32_t count, const uint8_t* src_codes,
+                              const uint8_t* src_sf, uint8_t* codes, uint8_t* sf, cudaStream_t st) {
+  const int64_t n = (int64_t)n_experts * rows * (Kd / 32);
+  if (n == 0) return FP4MOE_OK;
+  mx_shard_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(n, w1, rows, Kd, Ik, full_inter, src_row_elems, first,
+                                                              count, src_codes, src_sf, codes, sf);
   return cudaGetLastError() == cudaSuccess ? FP4MOE_OK : FP4MOE_CUDA_ERROR;
 }
 

@@ -478,6 +478,62 @@ fp4moe_status fp4moe_quantize_weights(const fp4moe_config* cfg, int32_t which, i
                                       uint8_t* codes_out, uint8_t* sf_out, float* gs_out, fp4moe_stream_t stream);
 
 /*
+ * fp4moe_tp_shard_units: where one tensor-parallel rank's slice of an axis
+ * lies, counted in that tensor's storage unit. Host arithmetic only; no GPU.
+ * Source: "Lucifer-CUTLASS TP3 virtual-padding audit", "TP3 shape plan" (the
+ * per-rank width align_up(ceil(width / tp), align) and the kernel width that
+ * rounds it up to kernel_align) and "Required loader changes" (offsets taken
+ * in logical elements, then divided by the elements per storage unit: 1 for
+ * unpacked W13 rows, 2 for packed W2 bytes, 32 for E8M0 groups).
+ *   width: logical elements of the full axis (e.g. 2048); tp: ranks; rank in
+ *   [0, tp); unit: elements per storage unit.
+ *   src_offset: first source unit of the rank's slice; count: units copied
+ *   (the last rank may get fewer, or none); zero_tail: destination units
+ *   past the slice, up to the kernel width, which must be zero. Any output
+ *   pointer may be NULL.
+ * For width 2048, tp 3, align 32, kernel_align 128: unit 1 gives offsets
+ * 0/704/1408 with tails 64/64/128; unit 2 gives 0/352/704 with tails
+ * 32/32/64; unit 32 gives 0/22/44 with tails 2/2/4.
+ * Errors: FP4MOE_INVALID_ARG for a non-positive size or a rank outside
+ * [0, tp); FP4MOE_UNSUPPORTED when a slice boundary or the kernel width
+ * splits a storage unit.
+ */
+fp4moe_status fp4moe_tp_shard_units(int32_t width, int32_t tp, int32_t align, int32_t kernel_align, int32_t rank,
+                                    int32_t unit, int32_t* src_offset, int32_t* count, int32_t* zero_tail);
+
+/*
+ * fp4moe_shard_mxfp4: cut tensor-parallel rank tp_rank's kernel-local shard
+ * of n_experts experts out of an already quantised, full-width MXFP4
+ * checkpoint, straight into the atom-tiled MXFP4 weight layout above. Load
+ * time, not the hot path; it never synchronises.
+ * Source: "Lucifer-CUTLASS TP3 virtual-padding audit", sections "Packed W2
+ * weight is wrong", "W2 E8M0 scales are wrong" and "Required loader
+ * changes": the slice of the intermediate axis is counted in logical
+ * elements and read in each tensor's storage unit, and every destination
+ * element past the rank's logical count is zero (zero codes, zero E8M0
+ * bytes).
+ *   cfg: an MXFP4 layer whose inter / inter_logical are the kernel and
+ *     logical widths of the plan of full_inter over tp ranks (align 32,
+ *     kernel align 128), e.g. 768 / 704 for 2048 over 3; otherwise
+ *     FP4MOE_INVALID_ARG.
+ *   which = 1: ck_codes [n][2 full_inter][H / 2] bytes (gate rows first,
+ *     then up; element 2c in the low nibble of byte c), ck_sf
+ *     [n][2 full_inter][H / 32] E8M0 bytes. Writes the W1 layout (kernel row
+ *     order).
+ *   which = 2: ck_codes [n][H][full_inter / 2] bytes (packed along the
+ *     intermediate axis), ck_sf [n][H][full_inter / 32]. Writes the W2 layout.
+ *   codes_out / sf_out: the layer's W1 or W2 weight buffers (or an offset
+ *     into them, for a chunk of experts).
+ * Because 32-element groups never straddle a rank boundary, the result equals
+ * fp4moe_quantize_weights applied to the rank's fp32 shard, byte for byte.
+ * All pointers 16-byte aligned. full_inter must be a multiple of 32
+ * (FP4MOE_UNSUPPORTED otherwise); NVFP4 layers: FP4MOE_UNSUPPORTED.
+ */
+fp4moe_status fp4moe_shard_mxfp4(const fp4moe_config* cfg, int32_t which, int32_t n_experts, int32_t full_inter,
+                                 int32_t tp, int32_t tp_rank, const uint8_t* ck_codes, const uint8_t* ck_sf,
+                                 uint8_t* codes_out, uint8_t* sf_out, fp4moe_stream_t stream);
+
+/*
  * fp4moe_batch_gs1: the L1 activation global scale taken from the batch in
  * hand rather than from a warm-up pass, with no host synchronisation:
  *   gs1_out[0] = RN(2688 / amax|x[0..T)|) (1 for an all-zero batch),

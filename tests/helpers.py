@@ -63,15 +63,41 @@ class OracleExperts:
         return self.cache[e]
 
 
-def float_parity(got: np.ndarray, ref: np.ndarray, rel_l2: float = 1e-2, max_abs_rms: float = 2e-2):
-    """The layer's float bar: relative L2 <= 1e-2 and max |err| <= 2e-2 * RMS(ref)."""
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """One unit in the last place of bf16 at |v| (8 significant bits; subnormals: 2^-133)."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a >= 2.0 ** -126, a, 1.0)))
+    return np.where(a >= 2.0 ** -126, 2.0 ** (e - 7), 2.0 ** -133)
+
+
+def float_parity(got: np.ndarray, ref: np.ndarray, rel_l2: float = 1e-2, max_abs_rms: float = 2e-2,
+                 bf16: bool = False, bf16_terms=None):
+    """The layer's float bar: relative L2 <= 1e-2 and max |err| <= 2e-2 * RMS(ref).
+
+    bf16=True: got and ref are both bf16 outputs, each rounded once from its own fp32 (GPU) or fp64 (oracle)
+    sum. Where 2e-2 * RMS is finer than one bf16 ulp of an element, a sum that lands on the other side of a
+    rounding boundary moves that element by one ulp whichever side is right, so an element's bar is
+    max(2e-2 * RMS, ulp(ref)).
+    bf16_terms=[t0, t1, ...]: got is a sum of bf16-rounded parts (tensor- or expert-parallel ranks) and ref
+    the bf16 whole. Each rounding adds up to half an ulp of its own value, so an element's bar is
+    2e-2 * RMS + (sum of ulp(t_i) + ulp(ref)) / 2.
+    """
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert np.isfinite(got).all(), "non-finite output"
     rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300)
     rms = np.sqrt(np.mean(ref ** 2))
-    mx = np.abs(got - ref).max() if got.size else 0.0
-    assert rel <= rel_l2 and mx <= max_abs_rms * rms, f"rel L2 {rel:.3e} (<= {rel_l2}), max abs {mx:.3e} (<= {max_abs_rms} * rms {rms:.3e})"
+    bar = np.full(ref.shape, max_abs_rms * rms)
+    if bf16:
+        bar = np.maximum(bar, bf16_ulp(ref))
+    if bf16_terms is not None:
+        bar = bar + 0.5 * (sum(bf16_ulp(t) for t in bf16_terms) + bf16_ulp(ref))
+    err = np.abs(got - ref)
+    mx = err.max() if got.size else 0.0
+    over = int((err > bar).sum())
+    assert rel <= rel_l2 and over == 0, (f"rel L2 {rel:.3e} (<= {rel_l2}), max abs {mx:.3e} (bar {max_abs_rms} * rms "
+                                         f"{rms:.3e}{' or the rounding slack' if bf16 or bf16_terms else ''}), "
+                                         f"{over} elements over their bar")
     return rel, mx / rms if rms > 0 else 0.0
 
 

@@ -98,7 +98,7 @@ def test_argument_checks(lib):
     assert lib.fp4moe_selftest_wait_timeout(p, 60_000_000, p, None) == _lib.INVALID_ARG  # above 50 ms
     assert lib.fp4moe_selftest_wait_timeout(ctypes.c_void_p(0x10002), 5_000_000, p, None) == _lib.MISALIGNED
     assert lib.fp4moe_status_string(_lib.CAPACITY) == b"FP4MOE_CAPACITY"
-    assert lib.fp4moe_abi_version() == 102
+    assert lib.fp4moe_abi_version() == 103
 
 
 def test_shared_expert_checks_and_sizes(lib):
@@ -127,3 +127,46 @@ def test_shared_expert_checks_and_sizes(lib):
     # an expert-parallel combine must be told which pairs are held here
     ep = _cfg(ep_first=0, ep_count=64)
     assert lib.moe_combine_shared(ctypes.byref(ep), 8, p, p, None, p, p, None) == _lib.INVALID_ARG
+
+
+def test_tp_shard_units_reproduce_the_tp3_plan(lib):
+    """The library's shard plan against the offsets and zero tails that "Lucifer-CUTLASS TP3 virtual-padding
+    audit" prints for 2048 over three ranks ("TP3 shape plan", "Packed W2 weight is wrong", "W2 E8M0 scales are
+    wrong"), in each tensor's storage unit, and against the oracle's plan on other widths."""
+    import json
+    from block_scaled_fp4_top_gb300 import api
+    from oracle import mxfp4
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "tp3_shard_plan.json")))
+    m = g["routed_moe"]
+    for key in ("w13_unpacked_rows", "w2_packed_bytes", "w2_e8m0_groups"):
+        ax = g[key]
+        got = [api.fp4moe_tp_shard_units(m["original"], g["tp"], m["align"], m["kernel_align"], r, ax["unit"])
+               for r in range(g["tp"])]
+        assert [o for o, _, _ in got] == ax["source_offsets"], key
+        assert [o + n for o, n, _ in got] == ax["source_ends"], key
+        assert [z for _, _, z in got] == ax["zero_tail"], key
+        assert {n + z for _, n, z in got} == {m["kernel_local"] // ax["unit"]}, key
+    for width, tp, unit in [(2048, 1, 32), (2048, 2, 2), (2048, 4, 32), (1536, 3, 32), (4096, 8, 2), (96, 3, 32)]:
+        plan = mxfp4.tp_plan(width, tp, 32, 128)
+        for r in range(tp):
+            assert api.fp4moe_tp_shard_units(width, tp, 32, 128, r, unit) == mxfp4.shard_units(width, plan, r, unit)
+
+
+def test_tp_shard_checks(lib):
+    from block_scaled_fp4_top_gb300 import _lib
+    out = [ctypes.c_int32() for _ in range(3)]
+    refs = [ctypes.byref(v) for v in out]
+    assert lib.fp4moe_tp_shard_units(2048, 3, 32, 128, 3, 1, *refs) == _lib.INVALID_ARG       # rank >= tp
+    assert lib.fp4moe_tp_shard_units(2048, 0, 32, 128, 0, 1, *refs) == _lib.INVALID_ARG       # no ranks
+    assert lib.fp4moe_tp_shard_units(2048, 3, 32, 128, 1, 3, *refs) == _lib.UNSUPPORTED       # 704 splits a unit
+    assert lib.fp4moe_tp_shard_units(2048, 3, 32, 128, 2, 32, None, None, None) == _lib.OK   # outputs optional
+    p = ctypes.c_void_p(0x10000)
+    mx = _cfg(w_format=_lib.W_MXFP4, inter=768, inter_logical=704)
+    assert lib.fp4moe_shard_mxfp4(ctypes.byref(_cfg()), 1, 4, 2048, 3, 0, p, p, p, p, None) == _lib.UNSUPPORTED
+    assert lib.fp4moe_shard_mxfp4(ctypes.byref(mx), 3, 4, 2048, 3, 0, p, p, p, p, None) == _lib.INVALID_ARG
+    assert lib.fp4moe_shard_mxfp4(ctypes.byref(mx), 1, 4, 2048, 2, 0, p, p, p, p, None) == _lib.INVALID_ARG  # widths
+    assert lib.fp4moe_shard_mxfp4(ctypes.byref(mx), 1, 4, 2040, 3, 0, p, p, p, p, None) == _lib.UNSUPPORTED
+    assert lib.fp4moe_shard_mxfp4(ctypes.byref(mx), 1, 4, 2048, 3, 3, p, p, p, p, None) == _lib.INVALID_ARG  # rank
+    assert lib.fp4moe_shard_mxfp4(ctypes.byref(mx), 2, 4, 2048, 3, 1, p, None, p, p, None) == _lib.INVALID_ARG
+    assert lib.fp4moe_shard_mxfp4(ctypes.byref(mx), 2, 4, 2048, 3, 1, p, p, ctypes.c_void_p(0x10008), p,
+                                  None) == _lib.MISALIGNED

@@ -95,7 +95,7 @@ def test_dsv4_decode_48_local_experts():
     assert (ids == ids_ref).all()
     rows = np.array([0, 21, 42, 63])
     y_ref = moe.moe_tokens(x[rows], loc[rows], w_ref[rows], lambda l: experts(first + l), gs1, gs2, wl.swiglu_limit)
-    float_parity(y[rows], sg.bf16_bits_to_f32(y_ref))
+    float_parity(y[rows], sg.bf16_bits_to_f32(y_ref), bf16=True)
 
 
 def test_tiny_two_rank_split_sums_to_the_layer():
@@ -108,6 +108,7 @@ def test_tiny_two_rank_split_sums_to_the_layer():
     ids_w, _ = moe.topk_softmax(moe.router_logits(xw, sg.router_bf16(wl), None), wl.k)
     gs1, gs2 = moe.calibrate(xw, ids_w, experts, wl.swiglu_limit)
     total = np.zeros((wl.T, wl.H))
+    parts = []
     for first in (0, 4):
         _, layer = ep_layer(wl, first, 4, wl.T)
         layer.set_global_scales(float(gs1), float(gs2))
@@ -115,7 +116,8 @@ def test_tiny_two_rank_split_sums_to_the_layer():
         assert (ids == ids_ref).all()
         loc = layout.local_ids(ids_ref, first, 4)
         y_ref = moe.moe_tokens(x, loc, w_ref, lambda l: experts(first + l), gs1, gs2, wl.swiglu_limit)
-        float_parity(y, sg.bf16_bits_to_f32(y_ref))
+        float_parity(y, sg.bf16_bits_to_f32(y_ref), bf16=True)
         total += y
+        parts.append(y)
     y_full = moe.moe_tokens(x, ids_ref, w_ref, experts, gs1, gs2, wl.swiglu_limit)
-    float_parity(total, sg.bf16_bits_to_f32(y_full))
+    float_parity(total, sg.bf16_bits_to_f32(y_full), bf16_terms=parts)

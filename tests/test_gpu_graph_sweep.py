@@ -102,6 +102,6 @@ def test_graph_sweep_replays(oracle_svc):
     assert sum(len(r) for r in checked_x) == 2 * (127 + 4 * 6)
     for (T, i), got, (y_ref, _, _) in zip(labels, checked_y, ref):
         try:
-            float_parity(sg.bf16_bits_to_f32(got), sg.bf16_bits_to_f32(y_ref))
+            float_parity(sg.bf16_bits_to_f32(got), sg.bf16_bits_to_f32(y_ref), bf16=True)
         except AssertionError as exc:
             raise AssertionError(f"T={T} replay {i}: {exc}") from None

@@ -83,14 +83,14 @@ def _mx_layer(H, Ik, Il, E, k, T):
     return api.MoELayer(cfg)
 
 
-def _forward(layer, x_bits, k):
+def _forward(layer, x_bits, k, expect_err=0):
     import torch
     T = x_bits.shape[0]
     y = torch.empty(T, layer.cfg.hidden, dtype=torch.bfloat16, device="cuda")
     ids = torch.empty(T * k, dtype=torch.int32, device="cuda")
     layer.forward(bits_to_torch(x_bits), y, ids)
     torch.cuda.synchronize()
-    assert layer.read_error() == 0
+    assert layer.read_error() == expect_err
     return torch_to_bits(y), ids.cpu().numpy().reshape(T, k)
 
 
@@ -111,6 +111,7 @@ def test_tiny_tp3_all_ranks(w_sigma):
         gu = moe.bf16_to_f64(x_bits) @ w1f[0].astype(np.float64).T
         assert (gu[:, :I] > 10).mean() > 0.3 and (np.abs(gu[:, I:]) > 10).mean() > 0.6
     y_sum = np.zeros((T, H))
+    parts = []
     for rank in range(3):
         layer = _mx_layer(H, Ik, Il, E, k, T)
         w1l, w2l = shard_fp32(w1f, w2f, plan, rank)
@@ -129,19 +130,22 @@ def test_tiny_tp3_all_ranks(w_sigma):
         y, ids = _forward(layer, x_bits, k)
         assert (ids == ids_ref).all()
         y_ref = mxfp4.mx_moe_tokens(x_bits, ids_ref, w_ref, lambda e: ex[e], 10.0)
-        float_parity(sg.bf16_bits_to_f32(y), sg.bf16_bits_to_f32(y_ref))
+        float_parity(sg.bf16_bits_to_f32(y), sg.bf16_bits_to_f32(y_ref), bf16=True)
         y_sum += sg.bf16_bits_to_f32(y)
+        parts.append(sg.bf16_bits_to_f32(y))
     # the three ranks' outputs sum to the full-width layer
     plan1 = mxfp4.tp_plan(I, 1, 32, 64)
     ex1 = {e: mxfp4.mx_expert_shard(w1f[e], w2f[e], plan1, 0) for e in range(E)}
     y_full = mxfp4.mx_moe_tokens(x_bits, ids_ref, w_ref, lambda e: ex1[e], 10.0)
-    float_parity(y_sum, sg.bf16_bits_to_f32(y_full))
+    float_parity(y_sum, sg.bf16_bits_to_f32(y_full), bf16_terms=parts)
 
 
 def test_nan_token_propagates_to_its_output_row():
     """bf16 activations with MXFP4 weights have no activation quantiser: a NaN in x flows through both GEMMs
-    into the token's output row, as it does in the oracle. The other tokens stay within the bar."""
+    into the token's output row, as it does in the oracle. The router reports FP4MOE_ERR_EXPERT_ID for the
+    token (a NaN logit ranks nowhere; it gets ids 0 with weights 0). The other tokens stay within the bar."""
     import torch
+    from block_scaled_fp4_top_gb300 import _lib
     rng = np.random.default_rng(22)
     H, I, E, k, T = 256, 128, 8, 2, 16
     plan = mxfp4.tp_plan(I, 1, 32, 128)
@@ -154,7 +158,7 @@ def test_nan_token_propagates_to_its_output_row():
     layer.quantize_weights(1, 0, torch.from_numpy(w1f).cuda())
     layer.quantize_weights(2, 0, torch.from_numpy(w2f).cuda())
     layer.set_router(bits_to_torch(router))
-    y, ids = _forward(layer, x_bits, k)
+    y, ids = _forward(layer, x_bits, k, expect_err=_lib.ERR_EXPERT_ID)
     ex = {e: mxfp4.mx_expert_shard(w1f[e], w2f[e], plan, 0) for e in range(E)}
     with np.errstate(invalid="ignore"):
         ids_ref, w_ref = moe.topk_softmax(moe.router_logits(x_bits, router), k)
@@ -163,7 +167,7 @@ def test_nan_token_propagates_to_its_output_row():
     assert np.isnan(y_ref[5]).all() and np.isnan(yf[5]).all()
     others = np.arange(T) != 5
     assert (ids[others] == ids_ref[others]).all()
-    float_parity(yf[others], y_ref[others])
+    float_parity(yf[others], y_ref[others], bf16=True)
 
 
 def _dsv4_mx_rank_layer(wl, wl_full, plan, rank, max_tokens, chunk=8):
@@ -205,14 +209,16 @@ def test_dsv4_tp3_three_ranks_sum_to_the_full_width_layer(oracle_svc):
     y_rank_ref = [sg.bf16_bits_to_f32(moe.combine(ids_ref, w_ref, o)) for o in parts[:3]]
     y_full_ref = sg.bf16_bits_to_f32(moe.combine(ids_ref, w_ref, parts[3]))
     sums = {T: np.zeros((T, wl.H)) for T in Ts}
+    parts = {T: [] for T in Ts}
     for rank in range(3):
         layer = _dsv4_mx_rank_layer(wl, wl_full, plan, rank, max(Ts))
         for T in Ts:
             y, ids = _forward(layer, x_bits[:T], wl.k)
             assert (ids == ids_ref[:T]).all(), (rank, T)
             yf = sg.bf16_bits_to_f32(y)
-            float_parity(yf, y_rank_ref[rank][:T])
+            float_parity(yf, y_rank_ref[rank][:T], bf16=True)
             sums[T] += yf
+            parts[T].append(yf)
             # the same call captured in a CUDA graph and replayed gives the eager rows, bit for bit
             xs = bits_to_torch(x_bits[:T])
             ys = torch.empty(T, wl.H, dtype=torch.bfloat16, device="cuda")
@@ -229,7 +235,7 @@ def test_dsv4_tp3_three_ranks_sum_to_the_full_width_layer(oracle_svc):
         del layer
         torch.cuda.empty_cache()
     for T in Ts:
-        float_parity(sums[T], y_full_ref[:T])
+        float_parity(sums[T], y_full_ref[:T], bf16_terms=parts[T])
 
 
 def test_dsv4_tp3_rank0_T512_sampled_tokens(oracle_svc):
@@ -243,4 +249,54 @@ def test_dsv4_tp3_rank0_T512_sampled_tokens(oracle_svc):
     assert (ids == ids_ref).all()
     rows = np.sort(np.random.default_rng(512).choice(wl.T, 64, replace=False))
     part, = oracle_svc.mx_partials(wl_full, x_bits[rows], ids_ref[rows], [(plan, 0)])
-    float_parity(sg.bf16_bits_to_f32(y[rows]), sg.bf16_bits_to_f32(moe.combine(ids_ref[rows], w_ref[rows], part)))
+    float_parity(sg.bf16_bits_to_f32(y[rows]), sg.bf16_bits_to_f32(moe.combine(ids_ref[rows], w_ref[rows], part)),
+                 bf16=True)
+
+
+def _pack_nibbles(q: np.ndarray) -> np.ndarray:
+    """Codes [..., K] -> bytes [..., K / 2], element 2c in the low nibble of byte c (the checkpoint packing)."""
+    return (q[..., 0::2] | (q[..., 1::2] << 4)).astype(np.uint8)
+
+
+@pytest.mark.parametrize("H,I,E", [(256, 192, 8), (4096, 2048, 3)])
+def test_shard_mxfp4_checkpoint(H, I, E):
+    """fp4moe_shard_mxfp4 cuts every TP3 rank's shard out of a full-width, already quantised MXFP4 checkpoint
+    (W13 rows unpacked, W2 codes packed two per byte along I, one E8M0 byte per 32 elements). Its bytes equal
+    (a) the oracle's cut of the same checkpoint, in logical units converted to each storage unit ("Packed W2
+    weight is wrong", "W2 E8M0 scales are wrong"), and (b) the library's own quantisation of the rank's
+    zero-padded fp32 shard. Every destination byte is written: the buffers start filled with 0xAB."""
+    import torch
+    rng = np.random.default_rng(31)
+    w1f = (rng.standard_normal((E, 2 * I, H)) * 0.05).astype(np.float32)
+    w2f = (rng.standard_normal((E, H, I)) * 0.05).astype(np.float32)
+    w2f[:, 5, 32:64] = 0                                      # an all-zero group: scale byte 0 (X = -127)
+    w1f[:, 7, :32] *= 1e-30                                   # a group far below the others
+    cks = [mxfp4.mx_checkpoint(w1f[e], w2f[e]) for e in range(E)]
+    ck13 = torch.from_numpy(np.stack([_pack_nibbles(c.w13_q) for c in cks])).cuda()
+    ck13s = torch.from_numpy(np.stack([c.w13_s for c in cks])).cuda()
+    ck2 = torch.from_numpy(np.stack([c.w2_packed for c in cks])).cuda()
+    ck2s = torch.from_numpy(np.stack([c.w2_s for c in cks])).cuda()
+    plan = mxfp4.tp_plan(I, 3, 32, 128)
+    Ik, Il = plan.kernel_local, plan.logical_per_rank
+    for rank in range(3):
+        cut = _mx_layer(H, Ik, Il, E, 2, 16)
+        for t in (cut.weights.w1_fp4, cut.weights.w1_sf, cut.weights.w2_fp4, cut.weights.w2_sf):
+            t.fill_(0xAB)
+        cut.shard_mxfp4_weights(1, 0, ck13, ck13s, I, 3, rank)
+        cut.shard_mxfp4_weights(2, 0, ck2, ck2s, I, 3, rank)
+        ref = _mx_layer(H, Ik, Il, E, 2, 16)
+        w1l, w2l = shard_fp32(w1f, w2f, plan, rank)
+        ref.quantize_weights(1, 0, torch.from_numpy(w1l).cuda())
+        ref.quantize_weights(2, 0, torch.from_numpy(w2l).cuda())
+        torch.cuda.synchronize()
+        for a, b in [(cut.weights.w1_fp4, ref.weights.w1_fp4), (cut.weights.w1_sf, ref.weights.w1_sf),
+                     (cut.weights.w2_fp4, ref.weights.w2_fp4), (cut.weights.w2_sf, ref.weights.w2_sf)]:
+            assert torch.equal(a, b), rank
+        q1, s1 = untile_mx(cut.weights.w1_fp4.cpu().numpy(), cut.weights.w1_sf.cpu().numpy(), E, 2 * Ik, H)
+        q2, s2 = untile_mx(cut.weights.w2_fp4.cpu().numpy(), cut.weights.w2_sf.cpu().numpy(), E, H, Ik)
+        for e in range(E):
+            ex = mxfp4.mx_shard_checkpoint(cks[e], plan, rank)
+            assert np.array_equal(kernel_to_logical_w1(q1[e:e + 1], Ik)[0], ex.w1_q), (rank, e)
+            assert np.array_equal(kernel_to_logical_w1(s1[e:e + 1], Ik)[0], ex.w1_s), (rank, e)
+            assert np.array_equal(q2[e], ex.w2_q) and np.array_equal(s2[e], ex.w2_s), (rank, e)
+        del cut, ref

@@ -86,7 +86,7 @@ def test_stale_gs2_is_flagged_and_refreshed():
     y_new = _forward(layer, x16)
     assert layer.read_scale_status()[0] == 0
     ref = moe.moe_tokens(x16, ids, w, experts, gs1_16, nvfp4.global_scale(np.float32(amax16)), wl.swiglu_limit)
-    float_parity(sg.bf16_bits_to_f32(y_new), sg.bf16_bits_to_f32(ref))
+    float_parity(sg.bf16_bits_to_f32(y_new), sg.bf16_bits_to_f32(ref), bf16=True)
     # the stale run really lost range: it is further from that reference than the refreshed one
     err = lambda y: np.linalg.norm(sg.bf16_bits_to_f32(y) - sg.bf16_bits_to_f32(ref))
     assert err(y_stale) > err(y_new)

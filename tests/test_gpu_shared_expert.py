@@ -190,7 +190,7 @@ def test_layer_with_shared_expert_tiny_all_tokens():
     o_ref = fp8block.shared_out(x, fp8block.quantize_shared(sg.shared_w1_f32(wl), sg.shared_w2_f32(wl)),
                                 wl.swiglu_limit)
     y_ref = moe.moe_tokens(x, ids_ref, w_ref, OracleExperts(wl), gs1, gs2, wl.swiglu_limit, shared=o_ref)
-    float_parity(sg.bf16_bits_to_f32(torch_to_bits(y)), sg.bf16_bits_to_f32(y_ref))
+    float_parity(sg.bf16_bits_to_f32(torch_to_bits(y)), sg.bf16_bits_to_f32(y_ref), bf16=True)
 
 
 def test_layer_with_shared_expert_dsv4_decode_and_graph_replay():
@@ -230,7 +230,7 @@ def test_layer_with_shared_expert_dsv4_decode_and_graph_replay():
                                 wl.swiglu_limit)
     y_ref = moe.moe_tokens(x_bits[rows], ids_ref[rows], w_ref[rows], OracleExperts(wl), gs1, gs2, wl.swiglu_limit,
                            shared=o_ref)
-    float_parity(sg.bf16_bits_to_f32(torch_to_bits(y)[rows]), sg.bf16_bits_to_f32(y_ref))
+    float_parity(sg.bf16_bits_to_f32(torch_to_bits(y)[rows]), sg.bf16_bits_to_f32(y_ref), bf16=True)
 
 
 def test_tp3_shards_against_oracle_and_their_sum():
