@@ -194,19 +194,16 @@ def setup_mx_layer(wl, max_tokens, rank=0, tp=3):
     return cfg, layer
 
 
-def run_ours(args, wl, rank, world):
+def build_step(wl, cfg, layer, x, y, dev, n_stage_steps):
+    """The layer's hot path as the four C-ABI calls (route, quantise-scatter, W1, W2 + combine) on
+    preallocated buffers. step(e, es) records CUDA events e[0..4] between the calls (and es[0..1] around the
+    shared expert on its side stream) when given them."""
     import torch
     from block_scaled_fp4_top_gb300 import api
-    from synthgen import gpu as sgpu
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    cfg, layer = setup_layer(wl, wl.T)
+    W = layer.weights
     T, H, k, E = wl.T, wl.H, wl.k, wl.E
     E_loc = wl.ep_count or E   # counts, offsets and padded offsets are per local expert
     mx = wl.w_format == 1
-    x = sgpu.activations(wl, sg.EVAL_SEED + rank)
-    y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-    W = layer.weights
     i32 = dict(dtype=torch.int32, device=dev)
     cap = api.capacity_rows(cfg, T)
     bufs = dict(logits=torch.empty(T, E, dtype=torch.float32, device=dev), ids=torch.empty(T * k, **i32),
@@ -227,11 +224,12 @@ def run_ours(args, wl, rank, world):
     b = bufs
     stream = torch.cuda.current_stream()
     n_stage = 5
+    se_ev = None
     if se:   # the shared expert runs beside the routed path, as moe_forward_shared runs it
         side = torch.cuda.Stream()
         fork_ev, join_ev = torch.cuda.Event(), torch.cuda.Event()
-        se_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_stage + 1)] for _ in range(args.steps)]
+        se_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_stage_steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_stage + 1)] for _ in range(n_stage_steps)]
 
     def step(e=None, es=None):
         if se:
@@ -271,19 +269,42 @@ def run_ours(args, wl, rank, world):
         if e is not None:
             e[4].record(stream)
 
+    return step, bufs, ev, se_ev
+
+
+def run_ours(args, wl, rank, world):
+    import torch
+    from block_scaled_fp4_top_gb300 import api
+    from synthgen import gpu as sgpu
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    cfg, layer = setup_layer(wl, wl.T)
+    T, H, k, E = wl.T, wl.H, wl.k, wl.E
+    E_loc = wl.ep_count or E   # counts, offsets and padded offsets are per local expert
+    mx = wl.w_format == 1
+    se = wl.shared_I > 0
+    ep = wl.ep_count > 0
+    x = sgpu.activations(wl, sg.EVAL_SEED + rank)
+    y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    n_stage_steps = min(args.steps, 200)
+    step, b, ev, se_ev = build_step(wl, cfg, layer, x, y, dev, n_stage_steps)
+
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    # the timed region: the steps back to back, events only at its two ends, so each kernel's prologue
+    # still overlaps its predecessor's tail (programmatic dependent launch)
     with ClockSampler(dev.index) as clk:
         time.sleep(0.3)  # let the sampler start before the timed region
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         for i in range(args.steps):
-            step(ev[i], se_ev[i] if se else None)
+            step()
         t1.record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -292,6 +313,11 @@ def run_ours(args, wl, rank, world):
     err = layer.read_error()
     if err != 0:
         raise RuntimeError(f"device error word {err:#x}")
+    # the stage split, from a second pass with events between the calls: an event between two launches ends
+    # the overlap, so these durations are serialised ones and their sum exceeds the step time above
+    for i in range(n_stage_steps):
+        step(ev[i], se_ev[i] if se else None)
+    torch.cuda.synchronize()
     stage_names = ["route", "quantize_scatter", "w1_swiglu_requant", "w2_combine"]
     stage_ms = {n: float(np.mean([e[j].elapsed_time(e[j + 1]) for e in ev])) for j, n in enumerate(stage_names)}
     if se:   # on the side stream, beside the routed stages
@@ -379,6 +405,9 @@ def run_ours(args, wl, rank, world):
         "layer_hbm_gbs": layer_bytes / (step_ms * 1e-3) / 1e9,
         "layer_algorithmic_bytes": layer_bytes, "n_active_experts": n_active, "padded_rows": R,
         "stages_us": {n: v * 1e3 for n, v in stage_ms.items()},
+        "stages_note": f"serialised: a second pass of {n_stage_steps} steps with CUDA events between the calls, "
+                       "which stop each kernel's prologue from overlapping its predecessor; the step time above has "
+                       "no events inside",
         "roofline": {"kernel": "mx_gemm_kernel<W1 SwiGLU bf16>" if mx else "grouped_gemm_kernel<W1 SwiGLU requant>",
                      "bound": "hbm", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
@@ -403,6 +432,104 @@ def run_ours(args, wl, rank, world):
                                 "achieved_gbs": se_gbs, "frac_hbm": se_gbs / peak,
                                 "tflops": 2 * T * 3 * Is * H / (se_ms * 1e-3) / 1e12}
     return out
+
+
+def fp4_dense_peak(dev):
+    """The dense NVFP4 tensor-core rate of this GPU, measured: fp4moe_tensor_peak_probe at N = 128 and 256
+    (one CTA per SM issuing back-to-back M = 128, K = 64 block-scaled MMAs on shared-memory operands), timed with
+    CUDA events on its stream after two warm-up launches."""
+    import torch
+    from block_scaled_fp4_top_gb300 import api
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    err = torch.zeros(4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    by_n, us = {}, {}
+    with ClockSampler(dev.index) as clk:
+        time.sleep(0.3)
+        for n, iters in ((128, 40000), (256, 20000)):
+            for _ in range(2):
+                api.fp4moe_tensor_peak_probe(n, iters, err)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 5
+            e0.record(stream)
+            for _ in range(reps):
+                api.fp4moe_tensor_peak_probe(n, iters, err)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            sec = e0.elapsed_time(e1) * 1e-3 / reps
+            by_n[str(n)] = nsm * iters * 4 * 2 * 128 * n * 64 / sec / 1e12
+            us[str(n)] = sec * 1e6
+    if int(err[0].item()) != 0:
+        raise RuntimeError("tensor peak probe: a bounded wait ran out")
+    return {"tflops": max(by_n.values()), "tflops_by_n": by_n, "us_per_launch_by_n": us, "sms": nsm,
+            "kernel": "tensor_peak_kernel: tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X, "
+                      "M=128, K=64, operands in shared memory", "clocks": clk.summary()}
+
+
+def run_prefill(args, dev, fp4_peak_tflops):
+    """The Zipf-routed prefill workload (T = 8192, DSV4 shapes): the same four calls as the decode step, timed
+    the same way, with the layer's HBM fraction and the GEMMs' tensor-pipe share of the measured FP4 peak."""
+    import torch
+    from synthgen import gpu as sgpu
+    wl = sg.DSV4_PREFILL_ZIPF
+    cfg, layer = setup_layer(wl, wl.T)
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+    x = sgpu.activations(wl, sg.EVAL_SEED)
+    y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    steps, n_stage_steps = args.prefill_steps, min(args.prefill_steps, 50)
+    step, b, ev, _ = build_step(wl, cfg, layer, x, y, dev, n_stage_steps)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        time.sleep(0.3)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    for i in range(n_stage_steps):
+        step(ev[i])
+    torch.cuda.synchronize()
+    err = layer.read_error()
+    if err != 0:
+        raise RuntimeError(f"prefill: device error word {err:#x}")
+    names = ["route", "quantize_scatter", "w1_swiglu_requant", "w2_combine"]
+    st = {n: float(np.mean([e[j].elapsed_time(e[j + 1]) for e in ev])) for j, n in enumerate(names)}
+    counts = b["counts"].cpu().numpy()
+    n_active = int((counts > 0).sum())
+    w1_bytes = n_active * (2 * I * H // 2 + 2 * I * H // 16)
+    w2_bytes = n_active * (H * I // 2 + H * I // 16)
+    a1 = T * k * (H // 2 + H // 16)    # A1 rows: written by the scatter, read by W1
+    a2 = T * k * (I // 2 + I // 16)    # A2 rows: written by W1, read by W2
+    layer_bytes = w1_bytes + w2_bytes + E * H * 2 + 2 * T * H * 2 + 2 * (a1 + a2)
+    flops_w1, flops_w2 = 2 * T * k * 2 * I * H, 2 * T * k * I * H
+    hbm, hbm_kind = peaks()
+    us = ms * 1e3
+    w1_s, w2_s = st["w1_swiglu_requant"] * 1e-3, st["w2_combine"] * 1e-3
+    return {
+        "workload": wl.name, "T": T, "us_per_layer": us, "tokens_per_s": T / (ms * 1e-3), "steps": steps,
+        "n_active_experts": n_active, "padded_rows": int(b["poff"][-1].item()), "max_tokens_per_expert":
+            int(counts.max()), "zero_token_experts": int((counts == 0).sum()),
+        "layer_algorithmic_bytes": layer_bytes,
+        "layer_hbm_gbs": layer_bytes / (ms * 1e-3) / 1e9, "layer_hbm_frac": layer_bytes / (ms * 1e-3) / 1e9 / hbm,
+        "hbm_peak_gbs": hbm, "hbm_peak_kind": hbm_kind,
+        "flops": flops_w1 + flops_w2,
+        "tensor_pipe_frac_layer": (flops_w1 + flops_w2) / (ms * 1e-3) / 1e12 / fp4_peak_tflops,
+        "fp4_peak_tflops": fp4_peak_tflops,
+        "stages_us": {n: v * 1e3 for n, v in st.items()},
+        "stages_note": f"serialised: {n_stage_steps} steps with CUDA events between the calls",
+        "w1": {"us": w1_s * 1e6, "algorithmic_bytes": w1_bytes + a1 + a2, "hbm_frac": (w1_bytes + a1 + a2) / w1_s / 1e9 / hbm,
+               "tflops": flops_w1 / w1_s / 1e12, "tensor_pipe_frac": flops_w1 / w1_s / 1e12 / fp4_peak_tflops},
+        "w2_combine": {"us": w2_s * 1e6, "algorithmic_bytes": w2_bytes + a2 + T * H * 2,
+                       "hbm_frac": (w2_bytes + a2 + T * H * 2) / w2_s / 1e9 / hbm,
+                       "tflops": flops_w2 / w2_s / 1e12, "tensor_pipe_frac": flops_w2 / w2_s / 1e12 / fp4_peak_tflops},
+        "clocks": clk.summary(),
+        "l2": "inputs larger than L2: ~3.4 GB of expert weights streamed per step (L2 129 MB)",
+    }
 
 
 class OracleSample:
@@ -467,10 +594,37 @@ class OracleSample:
 
 
 def oracle_sample_time(wl, n_tokens: int, repeats: int = 1):
-    """The oracle on the first n_tokens of the evaluation batch, repeats times. Returns (tokens/s, seconds)."""
+    """The oracle on the first n_tokens of the evaluation batch, repeats times.
+
+    Returns a dict: tokens/s and seconds of the layer (routing, experts, combine); weight_decode_s, the time
+    to dequantise the weights of the experts those tokens route to into fp64 tables (the oracle does this
+    inside its layer, once per expert per call, so it is part of the seconds, reported apart); prep_s, the
+    load-time quantisation of those experts (untimed)."""
+    from oracle import mxfp4, nvfp4
+    t0 = time.perf_counter()
     sample = OracleSample(wl, n_tokens)
+    prep = time.perf_counter() - t0
     dt = sum(sample.run(slice(0, n_tokens)) for _ in range(repeats))
-    return n_tokens * repeats / dt, dt
+    t0 = time.perf_counter()
+    for qe in sample.cache.values():
+        if sample.mx:
+            mxfp4.mx_dequantize(qe.w1_q, qe.w1_s), mxfp4.mx_dequantize(qe.w2_q, qe.w2_s)
+        else:
+            nvfp4.dequantize(qe.w1_q, qe.w1_sf, qe.w1_gs), nvfp4.dequantize(qe.w2_q, qe.w2_sf, qe.w2_gs)
+    decode = (time.perf_counter() - t0) * repeats
+    return {"value": n_tokens * repeats / dt, "seconds": dt, "weight_decode_s": decode, "prep_s": prep,
+            "experts": len(sample.cache)}
+
+
+def oracle_single_thread(wl_name: str, n_tokens: int):
+    """oracle_sample_time in a child process whose BLAS and OpenMP pools hold one thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", VECLIB_MAXIMUM_THREADS="1", NUMEXPR_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-only", "--workload", wl_name,
+                        "--oracle-tokens", str(n_tokens)], capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        return {"error": (r.stderr or r.stdout).strip().splitlines()[-1:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
 
 
 def cpu_info():
@@ -497,6 +651,10 @@ def main():
     ap.add_argument("--reference-budget", type=float, default=60.0,
                     help="--impl reference: stop timing oracle steps once they took this many seconds")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the FP4 peak probe and the Zipf prefill measurement that follow the decode run")
+    ap.add_argument("--prefill-steps", type=int, default=50)
+    ap.add_argument("--oracle-only", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--experts", type=int, default=0,
                     help="override E (smaller case for profiler captures; the default is the workload's E)")
     args = ap.parse_args()
@@ -508,6 +666,9 @@ def main():
         wl = dataclasses.replace(wl, E=args.experts, name=f"{wl.name}_E{args.experts}")
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.oracle_only:   # the single-thread leg of the CPU baseline, run as a child process
+        print(json.dumps(oracle_sample_time(wl, args.oracle_tokens)))
+        return
 
     if args.impl == "reference":
         if rank != 0:
@@ -547,12 +708,28 @@ def main():
     from block_scaled_fp4_top_gb300 import _lib
     _lib.load()
     out = run_ours(args, wl, rank, world)
+    if rank == 0 and not args.no_prefill and wl.name == sg.DSV4_DECODE.name and world == 1:
+        dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+        peak = fp4_dense_peak(dev)
+        out["fp4_dense_peak"] = peak
+        torch.cuda.empty_cache()
+        out["prefill"] = run_prefill(args, dev, peak["tflops"])
+        torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu_baseline:
         cores, model = cpu_info()
-        v, dt = oracle_sample_time(wl, args.oracle_tokens)
-        out["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                               "sample": f"first {args.oracle_tokens} tokens of the {wl.name} batch, {dt:.1f} s "
-                                         f"({model}; numpy BLAS default threads)"}
+        allc = oracle_sample_time(wl, args.oracle_tokens)
+        one = oracle_single_thread(wl.name, args.oracle_tokens)
+        out["cpu_baseline"] = {
+            "value": allc["value"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {args.oracle_tokens} tokens of the {wl.name} batch ({allc['experts']} experts), "
+                      f"{allc['seconds']:.1f} s on all {cores} cores (numpy BLAS default threads)",
+            "cpu_model": model,
+            "all_cores": {"value": allc["value"], "seconds": allc["seconds"], "threads": cores,
+                          "weight_decode_s": allc["weight_decode_s"]},
+            "single_thread": {k: one.get(k) for k in ("value", "seconds", "weight_decode_s", "error") if k in one},
+            "weight_prep_s": allc["prep_s"],
+            "note": "weight_decode_s: dequantising the sample's experts to fp64 tables, a part of the seconds that "
+                    "the oracle repeats on every call; weight_prep_s: their quantisation at load time, untimed"}
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:

@@ -54,6 +54,7 @@ SIGNATURES = {
     "fp4moe_make_alpha": (c_i32, [c_i32] + [c_vp] * 4),
     "fp4moe_calibrate": (c_i32, [CP, c_i32] + [c_vp] * 10),
     "fp4moe_quantize_rows_f32": (c_i32, [c_i32, c_i32] + [c_vp] * 5),
+    "fp4moe_tensor_peak_probe": (c_i32, [c_i32, c_i32, c_vp, c_vp]),
     "fp4moe_selftest_wait_timeout": (c_i32, [c_vp, ctypes.c_int64, c_vp, c_vp]),
     "fp4moe_batch_gs1": (c_i32, [CP, c_i32] + [c_vp] * 6),
     "fp4moe_read_error": (c_i32, [c_vp, ctypes.POINTER(c_u32), c_i32, c_vp]),

@@ -163,6 +163,11 @@ def fp4moe_quantize_rows_f32(rows, K, inp, g, codes, sf, stream=None):
            "fp4moe_quantize_rows_f32")
 
 
+def fp4moe_tensor_peak_probe(n, iters, err, stream=None):
+    """Launch the dense FP4 tensor-core rate probe (see include/fp4moe.h); the caller times it."""
+    _check(_lib.load().fp4moe_tensor_peak_probe(n, iters, _p(err), _s(stream)), "fp4moe_tensor_peak_probe")
+
+
 def fp4moe_selftest_wait_timeout(err, limit_ns, result, stream=None):
     """One bounded wait that runs out on purpose (a test of the failure path; see include/fp4moe.h)."""
     _check(_lib.load().fp4moe_selftest_wait_timeout(_p(err), int(limit_ns), _p(result), _s(stream)),

@@ -633,6 +633,12 @@ fp4moe_status fp4moe_quantize_rows_f32(int32_t rows, int32_t K, const float* in,
   return quant_rows_launch(rows, K, rows > 0 ? rows : 1, 0, 0, in, g, 1, codes, sf, (cudaStream_t)stream);
 }
 
+fp4moe_status fp4moe_tensor_peak_probe(int32_t n, int32_t iters, uint32_t* err, fp4moe_stream_t stream) {
+  if ((n != 128 && n != 256) || iters < 1 || iters > (1 << 22)) return FP4MOE_INVALID_ARG;
+  FP4_TRY(check_ptrs(err));
+  return tensor_peak_launch(n, iters, err, (cudaStream_t)stream);
+}
+
 fp4moe_status fp4moe_selftest_wait_timeout(uint32_t* err, int64_t limit_ns, uint32_t* result, fp4moe_stream_t stream) {
   if (err == nullptr || result == nullptr) return FP4MOE_INVALID_ARG;
   if (((reinterpret_cast<uintptr_t>(err) | reinterpret_cast<uintptr_t>(result)) & 3u) != 0) return FP4MOE_MISALIGNED;

@@ -89,6 +89,11 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
                           uint8_t* out_codes, uint8_t* out_sf, float* amax, uint32_t* status, float* o_pairs,
                           uint32_t* err, int* sched, cudaStream_t st);
 
+// SMs of the current device (cached per device), 0 on error
+int sm_count();
+// probe.cu: dense FP4 tensor-core throughput (fp4moe_tensor_peak_probe)
+fp4moe_status tensor_peak_launch(int32_t n, int32_t iters, uint32_t* err, cudaStream_t st);
+
 // selftest.cu: one bounded wait that runs out (see fp4moe_selftest_wait_timeout)
 fp4moe_status selftest_wait_launch(uint32_t* err, int64_t limit_ns, uint32_t* result, cudaStream_t st);
 

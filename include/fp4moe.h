@@ -602,6 +602,24 @@ fp4moe_status fp4moe_quantize_rows_f32(int32_t rows, int32_t K, const float* in,
                                        uint8_t* sf, fp4moe_stream_t stream);
 
 /*
+ * fp4moe_tensor_peak_probe: a measurement of the dense NVFP4 tensor-core
+ * rate, the denominator of the grouped GEMMs' tensor-pipe utilisation. The
+ * pages give no peak for the hardware; this replaces a vendor figure by a
+ * measured one.
+ * One CTA per SM issues iters x 4 back-to-back
+ * tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X of shape
+ * M = 128, N = n, K = 64 on operands held in shared memory (no global
+ * traffic), then waits for them. The caller times the launch on `stream`;
+ * it performs (SMs) x iters x 4 x 2 x 128 x n x 64 flops, where SMs is the
+ * device's multiprocessor count.
+ *   n: 128 or 256; iters in [1, 2^22]; err: device uint32 receiving
+ *   FP4MOE_ERR_TIMEOUT if the final bounded wait runs out.
+ * Errors: FP4MOE_INVALID_ARG for other sizes or a NULL err, FP4MOE_MISALIGNED
+ * for an err not 16-byte aligned.
+ */
+fp4moe_status fp4moe_tensor_peak_probe(int32_t n, int32_t iters, uint32_t* err, fp4moe_stream_t stream);
+
+/*
  * fp4moe_selftest_wait_timeout: a test of the failure path, with no
  * counterpart in the source pages. Every spin-wait in the library's kernels
  * is bounded: when it runs out it sets FP4MOE_ERR_TIMEOUT in the error word,
