@@ -1,0 +1,271 @@
+// Tile schedules shared by the persistent grouped GEMMs (gemm.cu: 128 x 128 tiles, gemm_wide.cu: 128 x 256
+// tiles): the dynamic chunk schedule, the per-role tile source and the static contiguous ranges. A kernel's
+// parameter block P provides dyn, sched and err.
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+#include "tiles.cuh"
+
+namespace fp4moe {
+
+// Parameters of one grouped GEMM launch (both tile shapes). NT counts the kernel's own n-tiles.
+struct GemmParams {
+  int E, K, KB, b_rows, NT, k, cap, I, H, nacc;  // KB: ring stages per tile; nacc: accumulators (128 x 128 kernel)
+  float limit;
+  const int32_t* poff;
+  const int32_t* pair_of_row;
+  const uint8_t* b_codes;
+  const uint8_t* a_sf;
+  const uint8_t* b_sf;
+  const float* alpha;
+  const float* gs2;
+  uint8_t* out_codes;
+  uint8_t* out_sf;
+  float* amax;       // W1 amax: the calibration maximum; W1 + SwiGLU: the running amax|h| (both non-negative)
+  uint32_t* status;  // W1 + SwiGLU: sticky FP4MOE_SAT_* bits
+  float* o_pairs;
+  uint32_t* err;
+  int o_pairs32;  // W2: o_pairs is 32-byte aligned (every row is then, H being a multiple of 256)
+  int dyn;     // 1: dynamic chunk schedule (large T); 0: contiguous static ranges (decode sizes)
+  int* sched;  // dynamic schedule: next-chunk counter, zero at launch
+};
+
+// Tensor maps of the activation codes whose boxes are 16, 32, 64 and 128 rows
+// high (128 bytes wide, 128-byte swizzle).
+struct AMaps {
+  CUtensorMap box[4];
+};
+
+// gemm_wide.cu: the 128 x 256 tile kernel. gemm_wide_fits: K and the weight rows suit it (K % 256, rows %
+// 256). gemm_wide_launch takes the 128 x 128 kernel's parameters (NT, KB of 128-row tiles and 512-deep
+// stages) and derives its own.
+bool gemm_wide_fits(int K, int b_rows);
+fp4moe_status gemm_wide_launch(GemmMode mode, const GemmParams& prm, const AMaps& tmA, cudaStream_t st);
+
+namespace {
+
+// Dynamic schedule. A chunk is at most kChunk tiles of one expert: for a one-m-tile expert, up to kChunk
+// n-tiles (the activation tile fixed); otherwise one n-tile over up to kChunk m-tiles (the weight tile
+// fixed). Chunks are numbered expert by expert (for several m-tiles: m-block, then n-tile), and CTAs take
+// them in that order from a global counter. So the CTAs running at any moment share one expert's
+// activation and weight tiles in L2, and the load balances itself.
+constexpr int kChunk = 4;
+constexpr int kSchedSlots = 4;  // chunk ids handed from the producer to the MMA issuer and the epilogue
+
+__device__ __forceinline__ int expert_chunks(int me, int NT) {
+  return me == 0 ? 0 : (me == 1 ? (NT + kChunk - 1) / kChunk : ((me + kChunk - 1) / kChunk) * NT);
+}
+
+struct Chunk {
+  int e, pm0, me;  // expert, its first m-tile, its m-tiles
+  int n0, m0;      // first n-tile and m-tile of the chunk
+  int count;       // tiles in the chunk
+  bool along_n;    // one m-tile: walk n-tiles n0.. with m fixed; else m-tiles m0.. with n fixed
+
+  __device__ __forceinline__ Tile tile(int i) const {
+    const int mt = along_n ? m0 : m0 + i;
+    return Tile{e, along_n ? n0 + i : n0, mt, me, mt == pm0 + me - 1};
+  }
+};
+
+// Chunk c; s_cstart[e] is the first chunk of expert e (empty experts share the next one's start).
+__device__ __forceinline__ Chunk decode_chunk(int c, const int* s_cstart, const int* poff, int E, int NT, int r128) {
+  int lo = 0, hi = E - 1;  // the last expert whose first chunk is <= c
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_cstart[mid] <= c) lo = mid;
+    else hi = mid - 1;
+  }
+  Chunk k;
+  k.e = lo;
+  k.pm0 = lo > 0 ? min(poff[lo - 1] >> 7, r128) : 0;
+  k.me = min(poff[lo] >> 7, r128) - k.pm0;
+  const int l = c - s_cstart[lo];
+  k.along_n = (k.me == 1);
+  if (k.along_n) {
+    k.n0 = l * kChunk;
+    k.m0 = k.pm0;
+    k.count = min(kChunk, NT - k.n0);
+  } else {
+    k.n0 = l % NT;
+    const int mb = l / NT;
+    k.m0 = k.pm0 + mb * kChunk;
+    k.count = min(kChunk, k.me - mb * kChunk);
+  }
+  return k;
+}
+
+// The tiles of one CTA, in order, as each role sees them: its contiguous share [tau0, tau1) of the tile
+// order (static schedule), or the chunks it takes from the global counter (dynamic schedule). In the dynamic
+// schedule the producer takes a chunk and hands its id to the MMA issuer and the epilogue warps through a
+// small shared-memory ring; every role then walks the same tiles in the same order.
+enum SourceRole { kRoleProducer = 0, kRoleMma = 1, kRoleEpilogue = 2, kRoleCopier = 3 };
+
+template <int ROLE>
+struct TileSource {
+  // static schedule
+  TileCursor cur;
+  int tau, tau1;
+  // dynamic schedule
+  Chunk ck;
+  int ci, q;
+  uint32_t qph;
+  bool dyn, done;
+
+  template <class P>
+  __device__ __forceinline__ void init(const P& prm, int tau0_, int tau1_, const int* poff, int E, int NT,
+                                       int r128) {
+    dyn = prm.dyn != 0;
+    tau = tau0_;
+    tau1 = tau1_;
+    if (!dyn && tau < tau1) cur.seek(tau, poff, E, NT, r128);
+    ck.count = 0;
+    ci = 0;
+    q = 0;
+    qph = 0;
+    done = false;
+  }
+
+  // The next tile, or false at the end (or when a bounded wait gave up).
+  template <class P>
+  __device__ __forceinline__ bool next(Tile& t, const P& prm, int tau0, const int* poff, const int* cstart,
+                                       int* s_sched, uint32_t bar_sfull, uint32_t bar_sempty, int n_chunks, int E,
+                                       int NT, int r128) {
+    if (!dyn) {
+      if (tau >= tau1) return false;
+      if (tau > tau0) cur.step(poff, E, NT, r128);
+      ++tau;
+      t = cur.tile();
+      return true;
+    }
+    while (ci >= ck.count) {
+      if (done) return false;
+      int c;
+      if constexpr (ROLE == kRoleProducer) {
+        if (!mbar_wait(bar_sempty + 8 * q, qph ^ 1u, prm.err)) {  // the slot's previous id was read by all
+          done = true;
+          return false;
+        }
+        c = atomicAdd(prm.sched, 1);
+        if (c >= n_chunks) c = -1;
+        s_sched[q] = c;
+        mbar_arrive(bar_sfull + 8 * q);
+      } else if constexpr (ROLE == kRoleMma || ROLE == kRoleCopier) {
+        if (!mbar_wait(bar_sfull + 8 * q, qph, prm.err)) {
+          done = true;
+          return false;
+        }
+        c = s_sched[q];
+        mbar_arrive(bar_sempty + 8 * q);
+      } else {
+        // the whole warp takes one decision
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_sfull + 8 * q, qph, prm.err) ? 1 : 0)) {
+          done = true;
+          return false;
+        }
+        c = s_sched[q];
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(bar_sempty + 8 * q);
+      }
+      if (++q == kSchedSlots) {
+        q = 0;
+        qph ^= 1u;
+      }
+      if (c < 0) {
+        done = true;
+        return false;
+      }
+      ck = decode_chunk(c, cstart, poff, E, NT, r128);
+      ci = 0;
+    }
+    t = ck.tile(ci++);
+    return true;
+  }
+};
+
+
+// Contiguous share [tau0, tau1) of `total` tiles for CTA c of G.
+__device__ __forceinline__ void cta_range(int total, int& tau0, int& tau1) {
+  tau0 = (int)(((long long)total * blockIdx.x) / gridDim.x);
+  tau1 = (int)(((long long)total * (blockIdx.x + 1)) / gridDim.x);
+}
+
+
+// The epilogue of one accumulator row: 128 columns of weight tile nt for activation row r, which holds pair
+// p (p >= 0). W2: the alpha-scaled fp32 row of the pair. W1: alpha, then the clamped SwiGLU (gate columns
+// 0-63, up columns 64-127, from the W1 kernel row order) and its NVFP4 requantisation into the L2 slot
+// buffers ("Bug 6", "Bug 7"). W1 amax: the same SwiGLU, reduced only. hrun keeps the NaN-propagating
+// amax|h| of the thread's rows.
+template <int MODE, class P>
+__device__ __forceinline__ void epilogue_row(const P& prm, const float (&v)[128], int r, int p, int nt, float alpha,
+                                             float& hrun) {
+  if constexpr (MODE == kW2Rows) {
+    float* d = prm.o_pairs + (size_t)p * prm.H + nt * 128;
+    if (prm.o_pairs32) {
+      // the thread's row in 32-byte stores: whole L2 sectors, half the write transactions of 16-byte ones
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        st_global_v8(d + 8 * q, __fmul_rn(v[8 * q], alpha), __fmul_rn(v[8 * q + 1], alpha),
+                     __fmul_rn(v[8 * q + 2], alpha), __fmul_rn(v[8 * q + 3], alpha), __fmul_rn(v[8 * q + 4], alpha),
+                     __fmul_rn(v[8 * q + 5], alpha), __fmul_rn(v[8 * q + 6], alpha), __fmul_rn(v[8 * q + 7], alpha));
+    } else {  // a caller's buffer aligned to 16 bytes only
+      float4* d4 = reinterpret_cast<float4*>(d);
+#pragma unroll
+      for (int q = 0; q < 32; ++q)
+        d4[q] = make_float4(__fmul_rn(v[4 * q], alpha), __fmul_rn(v[4 * q + 1], alpha), __fmul_rn(v[4 * q + 2], alpha),
+                            __fmul_rn(v[4 * q + 3], alpha));
+    }
+  } else {
+    // columns [0, 64): gate of features 64 nt .. 64 nt + 63; columns [64, 128): up of the same features
+    const float L = prm.limit;
+    if constexpr (MODE == kW1Amax) {
+#pragma unroll
+      for (int j = 0; j < 64; ++j)
+        hrun = fmax_nan(hrun, fabsf(swiglu_clamped(__fmul_rn(v[j], alpha), __fmul_rn(v[64 + j], alpha), L)));
+    } else {
+      const float g2 = __ldg(prm.gs2);
+      uint32_t codes[8];
+      uint32_t sfw = 0;
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk) {
+        float h[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          h[j] = swiglu_clamped(__fmul_rn(v[blk * 16 + j], alpha), __fmul_rn(v[64 + blk * 16 + j], alpha), L);
+          hrun = fmax_nan(hrun, fabsf(h[j]));
+        }
+        const uint32_t sf = quant_block16(h, g2, codes[2 * blk], codes[2 * blk + 1]);
+        sfw |= sf << (8 * blk);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(prm.out_codes + (size_t)r * (prm.I >> 1) + nt * 32);
+      dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+      dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+      *reinterpret_cast<uint32_t*>(prm.out_sf + sf_offset(r, nt * 4, prm.I >> 4)) = sfw;
+    }
+  }
+}
+
+// One amax per warp once a CTA is done: NaN -> error bit; else the running (or calibration) maximum, and for
+// the hot path the saturation test of the largest block, RN(RN(amax/6) * gs2) > 464, the quantiser's own
+// arithmetic ("Bug 5", "Bug 6").
+template <int MODE, class P>
+__device__ __forceinline__ void epilogue_amax_flush(const P& prm, float hrun) {
+  if constexpr (MODE != kW2Rows) {
+    __syncwarp();
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) hrun = fmax_nan(hrun, __shfl_xor_sync(0xFFFFFFFFu, hrun, off));
+    if ((threadIdx.x & 31) == 0) {
+      if (hrun != hrun) {
+        raise_error(prm.err, FP4MOE_ERR_NAN);
+      } else if (hrun > 0.0f) {
+        atomicMax(reinterpret_cast<unsigned int*>(prm.amax), __float_as_uint(hrun));
+        if constexpr (MODE == kW1SwiGLU) {
+          if (__fmul_rn(__fdiv_rn(hrun, 6.0f), __ldg(prm.gs2)) > kE4M3SatAbove) atomicOr(prm.status, FP4MOE_SAT_L2);
+        }
+      }
+    }
+  }
+}
+}  // namespace
+}  // namespace fp4moe

@@ -6,7 +6,8 @@ m-tiles, and K is partial (a stage of 2 atoms) or runs over several stages.
 * W2: every real pair's fp32 row is compared with an fp64 matmul of the
   decoded operands. Padding rows must not be written.
 * Cases with T >= E * 128 run the dynamic chunk schedule (prefill sizes),
-  the others the static contiguous one (decode sizes).
+  the others the static contiguous one (decode sizes). With K a multiple of
+  256 the dynamic cases run the 128 x 256 tile kernel (gemm_wide.cu).
 * W1: the clamped SwiGLU + requantisation epilogue is compared with the
   oracle's quantiser applied to the fp64 reference h. Codes must agree
   except at rounding ties that the fp32 accumulation moves.
@@ -98,6 +99,7 @@ def _setup(H, I, counts, seed, which, full_range=False, alpha_mult=1.0):
     (256, 768, [600, 5, 130], False),           # T >= E * 128: the dynamic chunk schedule (5-, 1-, 2-m-tile experts)
     (256, 768, [3, 0, 140], True),              # every finite E4M3 scale byte, static schedule
     (256, 768, [600, 5, 130], True),            # every finite E4M3 scale byte, dynamic schedule
+    (512, 256, [600, 5, 130], False),           # dynamic schedule, two 256-row weight tiles of the wide kernel
 ])
 def test_w2_rows_against_fp64(H, I, counts, full_range):
     import torch
@@ -204,12 +206,13 @@ def test_w1_swiglu_requant(H, I, counts, full_range):
     assert (sf[real] == s_ref[real]).mean() >= 0.99
 
 
-def test_w1_swiglu_clamp_past_the_limit():
+@pytest.mark.parametrize("counts", [[3, 0, 140, 1], [600, 5, 130, 1]])  # static; dynamic (128 x 256 tiles)
+def test_w1_swiglu_clamp_past_the_limit(counts):
     """Gate and up driven to an RMS of about 46 (alpha x 8): a large share of both is clamped. Where gate and up are
     both past the limit, h is +-silu(10) * 10 exactly and the codes must equal the oracle's; elsewhere they agree
     up to rounding ties. A missing lower clamp on up, a gate clamped on both sides or a wrong limit fail it."""
     from block_scaled_fp4_top_gb300 import api
-    H, I, counts = 256, 256, [3, 0, 140, 1]
+    H, I = 256, 256
     cfg, T, cap, ids, L, (qa, sa, qw, sw, alpha), t = _setup(H, I, counts, 4, which=1, alpha_mult=8.0)
     R = L["R"]
     g, u, h = _w1_reference(I, ids, L, qa, sa, qw, sw, alpha, cap)
