@@ -160,6 +160,51 @@ def mx_expert_shard(w1_full: np.ndarray, w2_full: np.ndarray, plan: TPPlan, rank
     return mx_shard_checkpoint(mx_checkpoint(w1_full, w2_full), plan, rank)
 
 
+# ------------------------------------- MXFP4 weights on the NVFP4 tensor-core form ----
+#
+# The block-scaled FP4 MMA that the NVFP4 layer runs multiplies an E2M1 code by an E4M3 scale per 16
+# elements. An MX scale 2^X (E8M0, per 32) is a power of two, and E4M3 holds every power of two from 2^-9
+# (the subnormal 0x01) to 2^8 (0x78). So with one power-of-two factor per matrix, G = X_max - 8, the MX
+# value e2m1(q) * 2^X equals e2m1(q) * e4m3(sf) / gw exactly, for sf = E4M3(2^(X - G)) on both 16-element
+# halves of the block and the quant-direction global scale gw = 2^-G. This holds for every block whose X
+# lies in the 18-binade window [X_max - 17, X_max]; an all-zero block (E8M0 byte 0, zero codes) takes
+# sf = 0. A nonzero block below the window has no exact form and is rejected.
+
+E4M3_POW2_MIN = -9   # 0x01, the smallest subnormal
+E4M3_POW2_MAX = 8    # 0x78 = 256; 512 is past the largest finite value, 448
+
+
+def e4m3_pow2_byte(d: int) -> int:
+    """The E4M3 byte of 2^d for -9 <= d <= 8 (bias 7: normals (d + 7) << 3 from d = -6; subnormals m / 8 * 2^-6)."""
+    if not E4M3_POW2_MIN <= d <= E4M3_POW2_MAX:
+        raise ValueError(f"2^{d} has no E4M3 form")
+    return (d + 7) << 3 if d >= -6 else 1 << (d + 9)
+
+
+def mx_as_nvfp4(q: np.ndarray, s: np.ndarray):
+    """One matrix's MXFP4 weights (codes [R, K], E8M0 bytes [R, K/32]) as NVFP4 operands.
+
+    Returns (codes [R, K] unchanged, E4M3 scale bytes [R, K/16], gw fp32) with
+    nvfp4.dequantize(codes, sf, gw) == mx_dequantize(q, s) exactly.
+    """
+    s = np.asarray(s, dtype=np.uint8)
+    if (s == 0xFF).any():
+        raise ValueError("an E8M0 scale is NaN")
+    live = s > 0
+    if live.any() and (np.asarray(q, dtype=np.uint8).reshape(s.shape[0], s.shape[1], MX_BLOCK)[~live] & 0x7).any():
+        raise ValueError("a block with E8M0 byte 0 has nonzero codes")
+    X = s.astype(np.int64) - 127
+    G = int(X[live].max()) - E4M3_POW2_MAX if live.any() else 0
+    table = {d: e4m3_pow2_byte(d) for d in range(E4M3_POW2_MIN, E4M3_POW2_MAX + 1)}
+    d = X - G
+    if (live & (d < E4M3_POW2_MIN)).any():
+        raise ValueError("a block lies more than 17 binades below the matrix's largest")
+    sf32 = np.zeros(s.shape, dtype=np.uint8)
+    sf32[live] = np.vectorize(table.__getitem__, otypes=[np.uint8])(d[live])
+    sf = np.repeat(sf32, 2, axis=1)                                        # both 16-element halves
+    return np.asarray(q, dtype=np.uint8), sf, np.float32(np.ldexp(1.0, -G))
+
+
 def _bf16_round(v: np.ndarray) -> np.ndarray:
     """fp64 -> fp32 (round to nearest) -> bf16 (round to nearest even), returned as fp64."""
     b = np.ascontiguousarray(v.astype(np.float32)).view(np.uint32).astype(np.uint64)

@@ -200,3 +200,51 @@ def test_expert_out_rounds_h_to_bf16_before_w2():
 
 def sg_bf16_to_f32(u):
     return (np.ascontiguousarray(u, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+# ---------------------------------------------- MXFP4 weights in the NVFP4 operand form ----
+
+def test_e4m3_powers_of_two():
+    """Every power of two from 2^-9 to 2^8 has exactly one E4M3 byte, the one the codec decodes to it; the
+    neighbours of the range have none (2^-10 underflows, 2^9 = 512 is past 448)."""
+    from oracle import codecs
+    for d in range(-9, 9):
+        b = mxfp4.e4m3_pow2_byte(d)
+        assert codecs.e4m3_decode(np.array([b], np.uint8))[0] == 2.0 ** d
+        hits = [c for c in range(0x7F) if codecs.e4m3_decode(np.array([c], np.uint8))[0] == 2.0 ** d]
+        assert hits == [b]
+    for d in (-10, 9):
+        with pytest.raises(ValueError):
+            mxfp4.e4m3_pow2_byte(d)
+
+
+def test_mx_as_nvfp4_is_exact_across_the_window():
+    """Blocks spread over the whole 18-binade window, an all-zero block and a window-edge block: the NVFP4 form
+    dequantises to the MX values bit for bit, and gw = 2^-(X_max - 8)."""
+    from oracle import nvfp4
+    rng = np.random.default_rng(5)
+    v = rng.uniform(-1.0, 1.0, (128, 32, 32))
+    v[:, :, 0] = 1.5                                   # every block's amax: 1.5 before its scaling
+    exps = np.arange(32) % 18                          # block j scaled by 2^-(j % 18): X from -2 down to -19
+    v = (v * np.ldexp(1.0, -exps)[None, :, None]).reshape(128, 1024).astype(np.float32)
+    v[3, 64:96] = 0.0                                  # an all-zero block
+    q, s = mxfp4.mx_quantize_rows(v)
+    X = s.astype(int) - 127
+    q2, sf, gw = mxfp4.mx_as_nvfp4(q, s)
+    assert gw == np.float32(2.0 ** -(X[s > 0].max() - 8))
+    assert np.array_equal(q2, q) and (sf[3, 4:6] == 0).all()
+    assert np.array_equal(nvfp4.dequantize(q2, sf, gw), mxfp4.mx_dequantize(q, s))
+    assert X[s > 0].max() - X[s > 0].min() == 17    # the window is full
+    assert np.array_equal(sf[:, 0::2], sf[:, 1::2])     # both halves of a 32-element block share the scale
+
+
+def test_mx_as_nvfp4_rejects_a_block_below_the_window():
+    v = np.ones((128, 64), np.float32)
+    v[0, 32:] = 2.0 ** -20                             # 20 binades below the rest
+    q, s = mxfp4.mx_quantize_rows(v)
+    with pytest.raises(ValueError):
+        mxfp4.mx_as_nvfp4(q, s)
+    s_nan = s.copy()
+    s_nan[1, 0] = 0xFF
+    with pytest.raises(ValueError):
+        mxfp4.mx_as_nvfp4(q, s_nan)
