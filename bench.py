@@ -142,6 +142,8 @@ def setup_layer(wl, max_tokens):
     from synthgen import gpu as sgpu
     if wl.w_format == _lib.W_MXFP4:
         return setup_mx_layer(wl, max_tokens)
+    if wl.w_format == 2:   # the TP3 shard's MXFP4 weights on the NVFP4 path
+        return setup_mx_nvfp4_layer(wl, max_tokens)
     cfg = api.config(wl.H, wl.I, wl.E, wl.k, max_tokens, wl.swiglu_limit, shared_inter=wl.shared_I,
                      ep_first=wl.ep_first, ep_count=wl.ep_count)
     layer = api.MoELayer(cfg)
@@ -158,6 +160,30 @@ def setup_layer(wl, max_tokens):
     layer.calibrate(sgpu.activations(wl, sg.WARMUP_SEED))
     torch.cuda.synchronize()
     torch.cuda.empty_cache()  # drop the fp32 weight staging buffers
+    return cfg, layer
+
+
+def setup_mx_nvfp4_layer(wl, max_tokens):
+    """Rank 0 of the TP3 MXFP4 shard (as setup_mx_layer builds it), its weights converted to the NVFP4 operand
+    form on the GPU (fp4moe_mxfp4_as_nvfp4), then calibrated like the NVFP4 layer."""
+    import dataclasses
+    import torch
+    from block_scaled_fp4_top_gb300 import api
+    from synthgen import gpu as sgpu
+    _, mx = setup_mx_layer(dataclasses.replace(wl, w_format=1), max_tokens)
+    cfg = api.config(wl.H, wl.I, wl.E, wl.k, max_tokens, wl.swiglu_limit, inter_logical=wl.I_logical)
+    layer = api.MoELayer(cfg)
+    err = torch.zeros(4, dtype=torch.int32, device="cuda")
+    layer.load_mxfp4_weights(1, 0, mx.weights.w1_fp4, mx.weights.w1_sf, err)
+    layer.load_mxfp4_weights(2, 0, mx.weights.w2_fp4, mx.weights.w2_sf, err)
+    torch.cuda.synchronize()
+    if int(err[0].item()) != 0:
+        raise RuntimeError(f"fp4moe_mxfp4_as_nvfp4: error word {int(err[0].item()):#x}")
+    del mx
+    layer.set_router(sgpu.router(wl), None)
+    layer.calibrate(sgpu.activations(wl, sg.WARMUP_SEED))
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     return cfg, layer
 
 
@@ -396,6 +422,8 @@ def run_ours(args, wl, rank, world):
         "metric": METRIC, "value": job_tokens_per_s(T, world, args.steps, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": ("mxfp4 weights x bf16 activations (exact bf16 expansion, fp32 accumulate)" if mx
+                                                         else "mxfp4 weights (e8m0 scales as exact e4m3 powers of two) x nvfp4 activations, fp32 accumulate"
+                                                         if wl.w_format == 2
                                                          else "nvfp4 (e2m1 x e2m1, e4m3 block scales, fp32 accumulate)"),
         "data": "synthetic (seeded SplitMix64 / Irwin-Hall normal; NVFP4 weights quantised from N(0,0.02))",
         "config": {"workload": wl.name, "T": T, "H": H, "I": I, "E": E, "top_k": k, "swiglu_limit": wl.swiglu_limit,
@@ -569,6 +597,11 @@ class OracleSample:
             if self.mx:   # rank 0 of the TP3 shard, as the GPU arm runs it
                 self.cache[e] = mxfp4.mx_expert_shard(sg.expert_w1_f32(self.full, e), sg.expert_w2_f32(self.full, e),
                                                       self.plan, 0)
+            elif wl.w_format == 2:   # the same shard in the NVFP4 operand form
+                sh = mxfp4.mx_expert_shard(sg.expert_w1_f32(self.full, e), sg.expert_w2_f32(self.full, e), self.plan, 0)
+                q1, s1, g1 = mxfp4.mx_as_nvfp4(sh.w1_q, sh.w1_s)
+                q2, s2, g2 = mxfp4.mx_as_nvfp4(sh.w2_q, sh.w2_s)
+                self.cache[e] = moe.QuantExpert(q1, s1, g1, q2, s2, g2)
             else:
                 self.cache[e] = moe.quantize_expert(sg.expert_w1_f32(wl, e), sg.expert_w2_f32(wl, e))
         return self.cache[e]

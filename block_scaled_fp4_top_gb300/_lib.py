@@ -13,7 +13,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfp4moe.s
 c_i32, c_u32, c_f32, c_sz, c_vp = ctypes.c_int32, ctypes.c_uint32, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
 
 OK, INVALID_ARG, MISALIGNED, CAPACITY, UNSUPPORTED, CUDA_ERROR = range(6)
-ERR_TIMEOUT, ERR_EXPERT_ID, ERR_CAPACITY, ERR_NAN = 0x1, 0x2, 0x4, 0x8
+ERR_TIMEOUT, ERR_EXPERT_ID, ERR_CAPACITY, ERR_NAN, ERR_SCALE_RANGE = 0x1, 0x2, 0x4, 0x8, 0x10
 SAT_L1, SAT_L2 = 0x1, 0x2
 W_NVFP4, W_MXFP4 = 0, 1
 
@@ -49,6 +49,7 @@ SIGNATURES = {
     "moe_grouped_gemm_w2_combine": (c_i32, [CP, c_i32] + [c_vp] * 11),
     "moe_forward": (c_i32, [CP, c_i32] + [c_vp] * 16),
     "fp4moe_quantize_weights": (c_i32, [CP, c_i32, c_i32] + [c_vp] * 5),
+    "fp4moe_mxfp4_as_nvfp4": (c_i32, [CP, c_i32, c_i32] + [c_vp] * 7),
     "fp4moe_tp_shard_units": (c_i32, [c_i32] * 6 + [ctypes.POINTER(c_i32)] * 3),
     "fp4moe_shard_mxfp4": (c_i32, [CP] + [c_i32] * 5 + [c_vp] * 5),
     "fp4moe_make_alpha": (c_i32, [c_i32] + [c_vp] * 4),

@@ -129,6 +129,12 @@ def fp4moe_quantize_weights(cfg, which, n_experts, w, codes_out, sf_out, gs_out,
                                                _p(sf_out), _p(gs_out), _s(stream)), "fp4moe_quantize_weights")
 
 
+def fp4moe_mxfp4_as_nvfp4(cfg, which, n_experts, mx_codes, mx_sf, codes_out, sf_out, gw_out, err, stream=None):
+    _check(_lib.load().fp4moe_mxfp4_as_nvfp4(ctypes.byref(cfg), which, n_experts, _p(mx_codes), _p(mx_sf),
+                                             _p(codes_out), _p(sf_out), _p(gw_out), _p(err), _s(stream)),
+           "fp4moe_mxfp4_as_nvfp4")
+
+
 def fp4moe_tp_shard_units(width, tp, align, kernel_align, rank, unit):
     """(source offset, units copied, zero tail) of one rank's slice, in storage units (host arithmetic)."""
     out = [ctypes.c_int32() for _ in range(3)]
@@ -309,6 +315,21 @@ class MoELayer:
         codes, sf = (W.w1_fp4, W.w1_sf) if which == 1 else (W.w2_fp4, W.w2_sf)
         fp4moe_shard_mxfp4(cfg, which, n, full_inter, tp, tp_rank, ck_codes.contiguous(), ck_sf.contiguous(),
                            codes[e0 * per_c:(e0 + n) * per_c], sf[e0 * per_s:(e0 + n) * per_s])
+
+    def load_mxfp4_weights(self, which: int, e0: int, mx_codes: torch.Tensor, mx_sf: torch.Tensor,
+                           err: torch.Tensor):
+        """NVFP4 layers: take experts [e0, e0 + n) of W1 (which=1) or W2 (which=2) from MXFP4 weights in the
+        atom-tiled MX layout (fp4moe_mxfp4_as_nvfp4); n follows from the buffer sizes of an MXFP4 layer of the
+        same hidden and inter. err receives FP4MOE_ERR_SCALE_RANGE for a scale without an exact form."""
+        cfg, W = self.cfg, self.weights
+        E = cfg.ep_count or cfg.num_experts
+        b1, s1, b2, s2 = weight_bytes(cfg)
+        rows, K = (2 * cfg.inter, cfg.hidden) if which == 1 else (cfg.hidden, cfg.inter)
+        n = mx_codes.numel() // (rows * K // 2)
+        per_c, per_s = (b1 // E, s1 // E) if which == 1 else (b2 // E, s2 // E)
+        codes, sf, gw = (W.w1_fp4, W.w1_sf, W.gw1) if which == 1 else (W.w2_fp4, W.w2_sf, W.gw2)
+        fp4moe_mxfp4_as_nvfp4(cfg, which, n, mx_codes.contiguous(), mx_sf.contiguous(),
+                              codes[e0 * per_c:(e0 + n) * per_c], sf[e0 * per_s:(e0 + n) * per_s], gw[e0:e0 + n], err)
 
     def quantize_shared_weights(self, which: int, w: torch.Tensor):
         """Block-FP8 of the shared expert's W1 (which=1, [2 Is, H], gate rows then up) or W2 (which=2, [H, Is])."""

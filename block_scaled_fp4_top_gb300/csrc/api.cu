@@ -46,8 +46,8 @@ fp4moe_status check_cfg(const fp4moe_config* c) {
   if (c->shared_inter % 128 != 0) return FP4MOE_UNSUPPORTED;  // whole 128 x 128 FP8 blocks
   if (c->shared_inter > 0 && (c->hidden > 4096 || c->shared_inter > 4096))
     return FP4MOE_UNSUPPORTED;  // the shared GEMM keeps up to 32 K blocks of scales in shared memory
-  if (c->w_format == FP4MOE_W_NVFP4) {
-    if (c->inter_logical != 0 && c->inter_logical != c->inter) return FP4MOE_UNSUPPORTED;
+  if (c->w_format == FP4MOE_W_NVFP4) {  // a TP shard: whole 16-element scale blocks inside the kernel width
+    if (c->inter_logical < 0 || c->inter_logical > c->inter || c->inter_logical % 16 != 0) return FP4MOE_UNSUPPORTED;
   } else {  // MXFP4: the logical width is whole 32-element scale groups inside the kernel width
     if (c->inter_logical < 0 || c->inter_logical > c->inter || c->inter_logical % 32 != 0) return FP4MOE_UNSUPPORTED;
   }
@@ -286,7 +286,7 @@ using namespace fp4moe;
 
 extern "C" {
 
-int32_t fp4moe_abi_version(void) { return 103; }
+int32_t fp4moe_abi_version(void) { return 104; }
 
 const char* fp4moe_status_string(fp4moe_status s) {
   switch (s) {
@@ -573,6 +573,20 @@ fp4moe_status fp4moe_shard_mxfp4(const fp4moe_config* cfg, int32_t which, int32_
   const int32_t Kd = w1 ? cfg->hidden : cfg->inter;
   return mx_shard_launch(n_experts, w1, rows, Kd, cfg->inter, full_inter, w1 ? cfg->hidden : full_inter, first, count,
                          ck_codes, ck_sf, codes_out, sf_out, (cudaStream_t)stream);
+}
+
+fp4moe_status fp4moe_mxfp4_as_nvfp4(const fp4moe_config* cfg, int32_t which, int32_t n_experts, const uint8_t* mx_codes,
+                                   const uint8_t* mx_sf, uint8_t* codes_out, uint8_t* sf_out, float* gw_out,
+                                   uint32_t* err, fp4moe_stream_t stream) {
+  FP4_TRY(check_cfg(cfg));
+  if (is_mx(cfg)) return FP4MOE_UNSUPPORTED;  // the target is an NVFP4 layer
+  if (which != 1 && which != 2) return FP4MOE_INVALID_ARG;
+  if (n_experts < 0 || n_experts > local_experts(*cfg)) return FP4MOE_INVALID_ARG;
+  FP4_TRY(check_ptrs(mx_codes, mx_sf, codes_out, sf_out, gw_out, err));
+  const int32_t rows = which == 1 ? 2 * cfg->inter : cfg->hidden;
+  const int32_t K = which == 1 ? cfg->hidden : cfg->inter;
+  return mx_as_nvfp4_launch(n_experts, rows, K, mx_codes, mx_sf, codes_out, sf_out, gw_out, err,
+                            (cudaStream_t)stream);
 }
 
 fp4moe_status fp4moe_make_alpha(int32_t n, const float* gs_act, const float* gs_w, float* alpha,

@@ -111,6 +111,11 @@ fp4moe_status mx_quant_rows_launch(int64_t n_rows, int32_t K, int32_t rows_per_g
 fp4moe_status mx_shard_launch(int32_t n_experts, bool w1, int32_t rows, int32_t Kd, int32_t Ik, int32_t full_inter,
                               int32_t src_row_elems, int32_t first, int32_t count, const uint8_t* src_codes,
                               const uint8_t* src_sf, uint8_t* codes, uint8_t* sf, cudaStream_t st);
+// MXFP4 weights (atom-tiled MX layout) -> the NVFP4 weight layout with E4M3 scales 2^(X - G) and gw = 2^-G
+// (fp4moe_mxfp4_as_nvfp4). rows = 2 I (W1) or H (W2); K = H (W1) or I (W2).
+fp4moe_status mx_as_nvfp4_launch(int32_t n_experts, int32_t rows, int32_t K, const uint8_t* mx_codes,
+                                 const uint8_t* mx_sf, uint8_t* codes, uint8_t* sf, float* gw, uint32_t* err,
+                                 cudaStream_t st);
 fp4moe_status scatter_rows_bf16_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x,
                                        const int32_t* slot_of_pair, uint16_t* a1, cudaStream_t st);
 

@@ -453,6 +453,86 @@ __global__ void __launch_bounds__(256) mx_shard_kernel(int64_t n_items, bool w1,
   sf[blk_idx * MX_BS_BYTES + 2 * rr + (blk & 1)] = s;
 }
 
+// MXFP4 weights in the NVFP4 operand form, for the block-scaled FP4 MMA of the NVFP4 layer. An MX scale
+// 2^X is a power of two, and E4M3 holds every power of two from 2^-9 (0x01) to 2^8 (0x78), so with one
+// factor per matrix, G = X_max - 8, the value e2m1(q) * 2^X is exactly e2m1(q) * e4m3(2^(X - G)) / gw with
+// gw = 2^-G, for every block within 17 binades of the matrix's largest.
+// Kernel 1: the largest E8M0 byte of each expert's matrix -> gw[e] (1 for a matrix of all-zero blocks).
+__global__ void __launch_bounds__(256) mx_gw_kernel(int64_t per_expert, const uint8_t* __restrict__ sf, float* gw,
+                                                    uint32_t* err) {
+  const uint8_t* p = sf + (size_t)blockIdx.x * per_expert;
+  uint32_t m = 0;
+  bool nan = false;
+  for (int64_t i = threadIdx.x; i < per_expert; i += blockDim.x) {
+    const uint32_t b = p[i];
+    nan |= (b == 0xFFu);
+    m = max(m, b);
+  }
+  __shared__ uint32_t s_m[8];
+  __shared__ int s_nan;
+  if (threadIdx.x == 0) s_nan = 0;
+  __syncthreads();
+  if (nan) s_nan = 1;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  if ((threadIdx.x & 31) == 0) s_m[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = max(m, s_m[w]);
+    m = max(m, s_m[0]);
+    if (s_nan) raise_error(err, FP4MOE_ERR_SCALE_RANGE);
+    // X_max = m - 127 (m = 0: no live block); G = X_max - 8; gw = 2^-G
+    // (clamped so that gw stays a normal fp32; a matrix that needs more raises the error in kernel 2)
+    const int G = (m == 0u || m == 0xFFu) ? 0 : max(-126, min(126, (int)m - 127 - 8));
+    gw[blockIdx.x] = ldexpf(1.0f, -G);
+  }
+}
+
+// Kernel 2: one thread per (row, 32-element block): its 16 code bytes move from the atom-tiled MXFP4 layout
+// to the pre-tiled NVFP4 layout, and its scale becomes E4M3(2^(X - G)) in both 16-element scale columns of
+// the NVFP4 scale layout. E8M0 byte 0 (an all-zero block) gives scale 0. A NaN byte, nonzero codes under byte
+// 0, or a block outside the 18-binade window sets FP4MOE_ERR_SCALE_RANGE (and takes scale 0, or the nearest
+// power of two in the window).
+__global__ void __launch_bounds__(256) mx_as_nvfp4_kernel(int64_t n_items, int rows, int K,
+                                                          const uint8_t* __restrict__ mx_codes,
+                                                          const uint8_t* __restrict__ mx_sf, const float* gw,
+                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                          uint32_t* err) {
+  const int nb = K / 32;
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n_items) return;
+  const int64_t row = idx / nb;
+  const int blk = (int)(idx - row * nb);
+  const int64_t e = row / rows;
+  const int lr = (int)(row - e * rows);
+  const int ka = K / 64, rt = lr / 128, rr = lr % 128;
+  const size_t src_blk = ((size_t)e * (rows / 128) + rt) * ka + blk / 2;
+  const uint4 c = *reinterpret_cast<const uint4*>(mx_codes + src_blk * MX_BC_BYTES + 32 * rr + 16 * (blk & 1));
+  const uint32_t b = mx_sf[src_blk * MX_BS_BYTES + 2 * rr + (blk & 1)];
+  uint32_t out = 0u;
+  if (b == 0xFFu || (b == 0u && ((c.x | c.y | c.z | c.w) & 0x77777777u) != 0u)) {
+    raise_error(err, FP4MOE_ERR_SCALE_RANGE);  // NaN scale, or nonzero codes under the all-zero block's byte 0
+  } else if (b != 0u) {
+    const int G = -ilogbf(__ldg(gw + e));
+    int d = (int)b - 127 - G;
+    if (d < -9 || d > 8) {
+      raise_error(err, FP4MOE_ERR_SCALE_RANGE);
+      d = max(-9, min(8, d));
+    }
+    out = d >= -6 ? (uint32_t)(d + 7) << 3 : 1u << (d + 9);  // E4M3 of 2^d: normal, else subnormal m / 8 * 2^-6
+  }
+  // pre-tiled NVFP4 codes: 16 KB blocks [expert][row tile][k stage of 256], row i 128 bytes, 16-byte chunk j
+  // at i * 128 + (j ^ (i % 8)) * 16
+  const int kst = (K + 255) / 256, stage = blk / 8, j = blk % 8;
+  const size_t dst_blk = ((size_t)e * (rows / 128) + rt) * kst + stage;
+  *reinterpret_cast<uint4*>(codes + dst_blk * 16384 + rr * 128 + ((j ^ (rr & 7)) * 16)) = c;
+  // NVFP4 scales: 128 x 4 tiles per expert, C = K / 16 columns; columns 2 blk and 2 blk + 1 are adjacent
+  const int C = K / 16, col = 2 * blk;
+  const size_t so = (size_t)e * rows * C + ((size_t)(lr >> 7) * (C >> 2) + (col >> 2)) * 512 + (lr & 31) * 16 +
+                    ((lr & 127) >> 5) * 4 + (col & 3);
+  *reinterpret_cast<uint16_t*>(sf + so) = (uint16_t)(out | (out << 8));
+}
+
 // bf16 activation rows into slot order: each token's row goes to its k slots.
 __global__ void __launch_bounds__(256) scatter_rows_bf16_kernel(int H, int k, const uint16_t* __restrict__ x,
                                                                 const int32_t* __restrict__ slot_of_pair,
@@ -528,6 +608,20 @@ fp4moe_status mx_shard_launch(int32_t n_experts, bool w1, int32_t rows, int32_t 
   if (n == 0) return FP4MOE_OK;
   mx_shard_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(n, w1, rows, Kd, Ik, full_inter, src_row_elems, first,
                                                               count, src_codes, src_sf, codes, sf);
+  return cudaGetLastError() == cudaSuccess ? FP4MOE_OK : FP4MOE_CUDA_ERROR;
+}
+
+fp4moe_status mx_as_nvfp4_launch(int32_t n_experts, int32_t rows, int32_t K, const uint8_t* mx_codes,
+                                 const uint8_t* mx_sf, uint8_t* codes, uint8_t* sf, float* gw, uint32_t* err,
+                                 cudaStream_t st) {
+  if (n_experts == 0) return FP4MOE_OK;
+  mx_gw_kernel<<<n_experts, 256, 0, st>>>((int64_t)rows * (K / 32), mx_sf, gw, err);
+  if (cudaGetLastError() != cudaSuccess) return FP4MOE_CUDA_ERROR;
+  if (K % 256 != 0 &&  // the last k-stage of every block is padded with zero codes
+      cudaMemsetAsync(codes, 0, (size_t)n_experts * rows * ((K + 255) / 256) * 128, st) != cudaSuccess)
+    return FP4MOE_CUDA_ERROR;
+  const int64_t n = (int64_t)n_experts * rows * (K / 32);
+  mx_as_nvfp4_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(n, rows, K, mx_codes, mx_sf, gw, codes, sf, err);
   return cudaGetLastError() == cudaSuccess ? FP4MOE_OK : FP4MOE_CUDA_ERROR;
 }
 

@@ -161,6 +161,8 @@ typedef enum fp4moe_status {
 #define FP4MOE_ERR_NAN       0x8u  /* a NaN reached an NVFP4 activation quantiser (x in moe_quantize_scatter,
                                       or h in the W1 epilogue or fp4moe_calibrate); the codes of that block
                                       are unspecified, and so are the outputs of its token */
+#define FP4MOE_ERR_SCALE_RANGE 0x10u /* fp4moe_mxfp4_as_nvfp4: an MX scale is NaN, or lies more than 17 binades
+                                         below its matrix's largest, and has no exact E4M3 form */
 
 /* Scale-status bits: a second sticky word of the workspace (fp4moe_read_scale_status). They are not
  * errors: a fixed activation global scale that a batch outgrows saturates its E4M3 block scales, which is
@@ -476,6 +478,35 @@ fp4moe_status moe_forward_shared(const fp4moe_config* cfg, int32_t T, const uint
  */
 fp4moe_status fp4moe_quantize_weights(const fp4moe_config* cfg, int32_t which, int32_t n_experts, const float* w,
                                       uint8_t* codes_out, uint8_t* sf_out, float* gs_out, fp4moe_stream_t stream);
+
+/*
+ * fp4moe_mxfp4_as_nvfp4: MXFP4 weights for the NVFP4 layer's block-scaled
+ * FP4 MMA. Load time, not the hot path; it never synchronises.
+ * Source: "Lucifer-CUTLASS TP3 virtual-padding audit" ("Remaining kernel
+ * assumptions": MXFP4 expert weights, E2M1 codes with one E8M0 scale per 32
+ * elements) and "Current Bug" ("Data Flow": the NVFP4 grouped GEMM). An MX
+ * scale 2^X is a power of two, and E4M3 holds every power of two from 2^-9
+ * to 2^8, so with one factor per expert matrix, G = X_max - 8, the MX value
+ * e2m1(q) * 2^X is exactly e2m1(q) * e4m3(sf) / gw for sf = E4M3(2^(X - G))
+ * on both 16-element halves of the block and gw = 2^-G. The layer then runs
+ * the NVFP4 hot path unchanged (NVFP4 activations with gs1 / gs2 and alpha =
+ * 1 / (gs * gw)).
+ *   cfg: the target NVFP4 layer (w_format FP4MOE_W_NVFP4; for a TP shard,
+ *     inter is the kernel width and inter_logical the logical one).
+ *   which = 1: mx_codes / mx_sf are n_experts experts of W1 in the
+ *     atom-tiled MXFP4 layout (as fp4moe_quantize_weights or
+ *     fp4moe_shard_mxfp4 write it for an MXFP4 layer of the same hidden and
+ *     inter); codes_out / sf_out / gw_out receive the W1 layout and gw1.
+ *     which = 2: the same for W2 and gw2.
+ *   err: device uint32 receiving FP4MOE_ERR_SCALE_RANGE if an E8M0 byte is
+ *     NaN, a block with byte 0 has nonzero codes, or a block lies outside
+ *     the 18-binade window [X_max - 17, X_max] (its scale is then clamped
+ *     into the window and the result is no longer exact).
+ * All pointers 16-byte aligned. MXFP4 target layers: FP4MOE_UNSUPPORTED.
+ */
+fp4moe_status fp4moe_mxfp4_as_nvfp4(const fp4moe_config* cfg, int32_t which, int32_t n_experts, const uint8_t* mx_codes,
+                                   const uint8_t* mx_sf, uint8_t* codes_out, uint8_t* sf_out, float* gw_out,
+                                   uint32_t* err, fp4moe_stream_t stream);
 
 /*
  * fp4moe_tp_shard_units: where one tensor-parallel rank's slice of an axis

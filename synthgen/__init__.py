@@ -116,7 +116,7 @@ class Workload:
     zipf_beta: float = 0.0
     zipf_dead: int = 0   # experts at the tail of the Zipf ranking that get bias -1e4
     I_logical: int = 0   # logical intermediate (MXFP4 TP shard); 0 = same as I
-    w_format: int = 0    # 0 = NVFP4, 1 = MXFP4
+    w_format: int = 0    # 0 = NVFP4, 1 = MXFP4, 2 = MXFP4 weights in the NVFP4 operand form (NVFP4 activations)
     shared_I: int = 0    # intermediate of the shared expert (block-FP8); 0 = none
     ep_first: int = 0    # expert parallelism: the layer holds experts [ep_first, ep_first + ep_count)
     ep_count: int = 0    # 0 = all experts
@@ -138,6 +138,9 @@ DSV4_PREFILL_ZIPF = dataclasses.replace(DSV4_DECODE, name="dsv4_flash_prefill_zi
                                         zipf_s=1.1, zipf_beta=1.0, zipf_dead=16)
 TP3_MXFP4 = dataclasses.replace(DSV4_DECODE, name="dsv4_flash_tp3_rank0_mxfp4_T512", T=512, I=768,
                                 I_logical=704, w_format=1, outlier_p=0.0, outlier_mult=1.0)
+# the same shard's MXFP4 weights carried on the NVFP4 block-scaled path (fp4moe_mxfp4_as_nvfp4), with NVFP4
+# activations
+TP3_MXFP4_NVACT = dataclasses.replace(TP3_MXFP4, name="dsv4_flash_tp3_rank0_mxfp4w_nvfp4a_T512", w_format=2)
 # the layer with DeepSeek-V4-Flash's shared expert (intermediate 2048, "TP3 shape plan")
 TINY_SHARED = dataclasses.replace(TINY, name="tiny_shared", T=200, shared_I=256)
 DSV4_DECODE_SHARED = dataclasses.replace(DSV4_DECODE, name="dsv4_flash_decode_shared_T64", shared_I=2048)
@@ -145,7 +148,8 @@ DSV4_DECODE_SHARED = dataclasses.replace(DSV4_DECODE, name="dsv4_flash_decode_sh
 DSV4_DECODE_EP48 = dataclasses.replace(DSV4_DECODE, name="dsv4_flash_decode_ep48_T64", ep_first=96, ep_count=48)
 GRAPH_SWEEP_T = tuple(2**i for i in range(13))  # 1 .. 4096
 
-WORKLOADS = {w.name: w for w in (TINY, DSV4_DECODE, DSV4_PREFILL_ZIPF, TP3_MXFP4, TINY_SHARED, DSV4_DECODE_SHARED,
+WORKLOADS = {w.name: w for w in (TINY, DSV4_DECODE, DSV4_PREFILL_ZIPF, TP3_MXFP4, TP3_MXFP4_NVACT, TINY_SHARED,
+                                 DSV4_DECODE_SHARED,
                                  DSV4_DECODE_EP48)}
 
 

@@ -56,12 +56,22 @@ def _mx_checkpoint(wl_full: sg.Workload, e: int) -> mxfp4.MxCheckpoint:
     return ck
 
 
+def _mxnv_expert(wl_full: sg.Workload, e: int, plan, rank) -> moe.QuantExpert:
+    """Rank `rank`'s MXFP4 shard of expert e in the NVFP4 operand form (mxfp4.mx_as_nvfp4 per matrix)."""
+    sh = mxfp4.mx_shard_checkpoint(_mx_checkpoint(wl_full, e), plan, rank)
+    q1, s1, g1 = mxfp4.mx_as_nvfp4(sh.w1_q, sh.w1_s)
+    q2, s2, g2 = mxfp4.mx_as_nvfp4(sh.w2_q, sh.w2_s)
+    return moe.QuantExpert(q1, s1, g1, q2, s2, g2)
+
+
 def _expert_jobs(wl: sg.Workload, e: int, requests: list) -> list:
     """Run one expert's requests. Each request is a tuple whose first item names it:
 
     ("amax", x_bits, gs1)            -> moe.hidden_amax of the rows, quantised under gs1
     ("rows", x_bits, gs1, gs2)       -> moe.pair_rows of the rows (fp64 [n, H])
     ("mx_rows", x_bits, plan, rank)  -> mxfp4.mx_expert_out of rank's shard (wl is the full-width workload)
+    ("mxnv_amax", x_bits, gs1, plan, rank)        -> moe.hidden_amax of rank's shard in the NVFP4 operand form
+    ("mxnv_rows", x_bits, gs1, gs2, plan, rank)   -> moe.pair_rows of the same
     """
     out = []
     for req in requests:
@@ -72,6 +82,14 @@ def _expert_jobs(wl: sg.Workload, e: int, requests: list) -> list:
         elif kind == "rows":
             _, x_bits, gs1, gs2 = req
             out.append(moe.pair_rows(_nv_expert(wl, e), moe.dequantized_activations(x_bits, gs1), gs2,
+                                     wl.swiglu_limit))
+        elif kind == "mxnv_amax":
+            _, x_bits, gs1, plan, rank = req
+            out.append(moe.hidden_amax(_mxnv_expert(wl, e, plan, rank), moe.dequantized_activations(x_bits, gs1),
+                                       wl.swiglu_limit))
+        elif kind == "mxnv_rows":
+            _, x_bits, gs1, gs2, plan, rank = req
+            out.append(moe.pair_rows(_mxnv_expert(wl, e, plan, rank), moe.dequantized_activations(x_bits, gs1), gs2,
                                      wl.swiglu_limit))
         elif kind == "mx_rows":
             _, x_bits, plan, rank = req
@@ -178,6 +196,31 @@ class OracleService:
         """
         rr = moe.routed_rows(ids)
         per_expert = {e: [("mx_rows", x_bits[tt], plan, rank) for plan, rank in plans] for e, (tt, _) in rr.items()}
+        res = self.run(wl_full, per_expert)
+        outs = []
+        for i in range(len(plans)):
+            o = np.zeros((x_bits.shape[0], ids.shape[1], wl_full.H))
+            for e, (tt, jj) in rr.items():
+                o[tt, jj] = res[e][i]
+            outs.append(o)
+        return outs
+
+    # ---------------------------------- MXFP4 weights on the NVFP4 path (mxfp4.mx_as_nvfp4) --
+
+    def mxnv_calibrate(self, wl_full: sg.Workload, xw_bits: np.ndarray, plan, rank):
+        """moe.calibrate of rank's NVFP4-form shard on a warm-up batch."""
+        gs1 = moe.activation_scale(xw_bits)
+        ids, _ = moe.topk_softmax(moe.router_logits(xw_bits, sg.router_bf16(wl_full), sg.router_bias_f32(wl_full)),
+                                  wl_full.k)
+        reqs = {e: [("mxnv_amax", xw_bits[tt], gs1, plan, rank)] for e, (tt, _) in moe.routed_rows(ids).items()}
+        amax = max([r[0] for r in self.run(wl_full, reqs).values()], default=0.0)
+        return gs1, nvfp4.global_scale(np.float32(amax))
+
+    def mxnv_partials(self, wl_full: sg.Workload, x_bits: np.ndarray, ids: np.ndarray, gs1, gs2, plans: list) -> list:
+        """Per-(token, j) partial rows [n, k, H] of the NVFP4-form shards (plan, rank), under gs1 and gs2."""
+        rr = moe.routed_rows(ids)
+        per_expert = {e: [("mxnv_rows", x_bits[tt], gs1, gs2, plan, rank) for plan, rank in plans]
+                      for e, (tt, _) in rr.items()}
         res = self.run(wl_full, per_expert)
         outs = []
         for i in range(len(plans)):

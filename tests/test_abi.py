@@ -98,7 +98,7 @@ def test_argument_checks(lib):
     assert lib.fp4moe_selftest_wait_timeout(p, 60_000_000, p, None) == _lib.INVALID_ARG  # above 50 ms
     assert lib.fp4moe_selftest_wait_timeout(ctypes.c_void_p(0x10002), 5_000_000, p, None) == _lib.MISALIGNED
     assert lib.fp4moe_status_string(_lib.CAPACITY) == b"FP4MOE_CAPACITY"
-    assert lib.fp4moe_abi_version() == 103
+    assert lib.fp4moe_abi_version() == 104
 
 
 def test_shared_expert_checks_and_sizes(lib):

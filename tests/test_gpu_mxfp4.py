@@ -32,7 +32,7 @@ import pytest
 
 import synthgen as sg
 from helpers import bits_to_torch, ensure_built, float_parity, torch_to_bits
-from oracle import moe, mxfp4
+from oracle import moe, mxfp4, nvfp4
 
 pytestmark = pytest.mark.gpu
 
@@ -300,3 +300,175 @@ def test_shard_mxfp4_checkpoint(H, I, E):
             assert np.array_equal(kernel_to_logical_w1(s1[e:e + 1], Ik)[0], ex.w1_s), (rank, e)
             assert np.array_equal(q2[e], ex.w2_q) and np.array_equal(s2[e], ex.w2_s), (rank, e)
         del cut, ref
+
+
+# ------------------------------------------ MXFP4 weights on the NVFP4 block-scaled MMA ----
+#
+# fp4moe_mxfp4_as_nvfp4 writes MXFP4 weights in the NVFP4 operand form: codes unchanged, each E8M0 scale
+# 2^X as E4M3(2^(X - G)) on both 16-element halves, gw = 2^-G per expert matrix (G = X_max - 8). The layer
+# then runs the NVFP4 hot path (NVFP4 activations). The oracle's side is mxfp4.mx_as_nvfp4 on its own MX
+# shard, fed to moe's NVFP4 layer.
+
+def _nv_layer(H, Ik, Il, E, k, T):
+    from block_scaled_fp4_top_gb300 import api
+    return api.MoELayer(api.config(H, Ik, E, k, T, 10.0, inter_logical=Il))
+
+
+def _nv_from_mx(mx_layer, H, Ik, Il, E, k, T, e0=0):
+    """An NVFP4 layer whose weights are the MXFP4 layer's, converted on the GPU; returns (layer, err word)."""
+    import torch
+    nv = _nv_layer(H, Ik, Il, E, k, T)
+    err = torch.zeros(4, dtype=torch.int32, device="cuda")
+    W = mx_layer.weights
+    nv.load_mxfp4_weights(1, e0, W.w1_fp4, W.w1_sf, err)
+    nv.load_mxfp4_weights(2, e0, W.w2_fp4, W.w2_sf, err)
+    torch.cuda.synchronize()
+    return nv, err
+
+
+def test_mx_as_nvfp4_bytes_match_the_oracle():
+    """Codes, E4M3 scale bytes and gw of the converted weights equal mxfp4.mx_as_nvfp4 of the oracle's shard,
+    on all three ranks of a tiny TP3 shape (whose zero tails are all-zero blocks)."""
+    import torch
+    from helpers import untile_weights
+    rng = np.random.default_rng(41)
+    H, I, E = 256, 192, 4
+    plan = mxfp4.tp_plan(I, 3, 32, 128)
+    Ik, Il = plan.kernel_local, plan.logical_per_rank
+    w1f = (rng.standard_normal((E, 2 * I, H)) * 0.05).astype(np.float32)
+    w2f = (rng.standard_normal((E, H, I)) * 0.05).astype(np.float32)
+    w1f[:, :, :32] *= 2.0 ** -12                        # a column of blocks 12 binades down (inside the window)
+    for rank in range(3):
+        mx = _mx_layer(H, Ik, Il, E, 2, 16)
+        w1l, w2l = shard_fp32(w1f, w2f, plan, rank)
+        mx.quantize_weights(1, 0, torch.from_numpy(w1l).cuda())
+        mx.quantize_weights(2, 0, torch.from_numpy(w2l).cuda())
+        nv, err = _nv_from_mx(mx, H, Ik, Il, E, 2, 16)
+        assert int(err[0].item()) == 0
+        W = nv.weights
+        for which, (codes, sf, gw) in ((1, (W.w1_fp4, W.w1_sf, W.gw1)), (2, (W.w2_fp4, W.w2_sf, W.gw2))):
+            R, K = (2 * Ik, H) if which == 1 else (H, Ik)
+            c = untile_weights(codes.cpu().numpy(), E * R, K // 2, R)
+            s = sf.cpu().numpy().reshape(E, -1)
+            for e in range(E):
+                ex = mxfp4.mx_expert_shard(w1f[e], w2f[e], plan, rank)
+                q, sm = (ex.w1_q, ex.w1_s) if which == 1 else (ex.w2_q, ex.w2_s)
+                q_ref, sf_ref, gw_ref = mxfp4.mx_as_nvfp4(q, sm)
+                got_q = nvfp4.unpack_codes(c[e * R:(e + 1) * R])
+                got_s = nvfp4.unswizzle(s[e], R, K // 16)
+                if which == 1:   # the NVFP4 layout keeps W1 rows in kernel order
+                    got_q = kernel_to_logical_w1(got_q[None], Ik)[0]
+                    got_s = kernel_to_logical_w1(got_s[None], Ik)[0]
+                assert np.array_equal(got_q, q_ref), (rank, which, e)
+                assert np.array_equal(got_s, sf_ref), (rank, which, e)
+                assert float(gw[e].item()) == float(gw_ref), (rank, which, e)
+
+
+def test_mx_as_nvfp4_flags_a_block_outside_the_window():
+    """A block 20 binades below its matrix's largest has no exact E4M3 form: FP4MOE_ERR_SCALE_RANGE."""
+    import torch
+    from block_scaled_fp4_top_gb300 import _lib
+    H, I, E = 256, 128, 2
+    w1 = np.ones((E, 2 * I, H), np.float32) * 0.05
+    w1[1, 3, 64:96] = 0.05 * 2.0 ** -20
+    w2 = np.ones((E, H, I), np.float32) * 0.05
+    mx = _mx_layer(H, I, I, E, 2, 16)
+    mx.quantize_weights(1, 0, torch.from_numpy(w1).cuda())
+    mx.quantize_weights(2, 0, torch.from_numpy(w2).cuda())
+    _, err = _nv_from_mx(mx, H, I, I, E, 2, 16)
+    assert int(err[0].item()) == _lib.ERR_SCALE_RANGE
+
+
+def test_mx_weights_nvfp4_activations_tiny_tp3_ranks_sum():
+    """The layer on each tiny TP3 rank against the oracle's NVFP4 layer on the NVFP4-form shard, all ranks under
+    the full-width layer's activation scales; the three ranks sum to the full-width layer."""
+    import torch
+    rng = np.random.default_rng(43)
+    H, I, E, k, T = 256, 192, 8, 2, 48
+    plan = mxfp4.tp_plan(I, 3, 32, 128)
+    full = mxfp4.tp_plan(I, 1, 32, 64)
+    Ik, Il = plan.kernel_local, plan.logical_per_rank
+    w1f = (rng.standard_normal((E, 2 * I, H)) * 0.05).astype(np.float32)
+    w2f = (rng.standard_normal((E, H, I)) * 0.05).astype(np.float32)
+    router = moe.f32_to_bf16_bits((rng.standard_normal((E, H)) / 16).astype(np.float32))
+    x_bits = moe.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    xw_bits = moe.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+
+    def nv_expert(e, pl, rank):
+        ex = mxfp4.mx_expert_shard(w1f[e], w2f[e], pl, rank)
+        q1, s1, g1 = mxfp4.mx_as_nvfp4(ex.w1_q, ex.w1_s)
+        q2, s2, g2 = mxfp4.mx_as_nvfp4(ex.w2_q, ex.w2_s)
+        return moe.QuantExpert(q1, s1, g1, q2, s2, g2)
+
+    full_ex = {e: nv_expert(e, full, 0) for e in range(E)}
+    ids_w, _ = moe.topk_softmax(moe.router_logits(xw_bits, router), k)
+    gs1, gs2 = moe.calibrate(xw_bits, ids_w, lambda e: full_ex[e], 10.0)
+    ids_ref, w_ref = moe.topk_softmax(moe.router_logits(x_bits, router), k)
+    y_full = sg.bf16_bits_to_f32(moe.moe_tokens(x_bits, ids_ref, w_ref, lambda e: full_ex[e], gs1, gs2, 10.0))
+    parts = []
+    for rank in range(3):
+        mx = _mx_layer(H, Ik, Il, E, k, T)
+        w1l, w2l = shard_fp32(w1f, w2f, plan, rank)
+        mx.quantize_weights(1, 0, torch.from_numpy(w1l).cuda())
+        mx.quantize_weights(2, 0, torch.from_numpy(w2l).cuda())
+        nv, err = _nv_from_mx(mx, H, Ik, Il, E, k, T)
+        assert int(err[0].item()) == 0
+        nv.set_router(bits_to_torch(router))
+        nv.set_global_scales(float(gs1), float(gs2))
+        y, ids = _forward(nv, x_bits, k)
+        assert (ids == ids_ref).all()
+        ex = {e: nv_expert(e, plan, rank) for e in range(E)}
+        y_ref = moe.moe_tokens(x_bits, ids_ref, w_ref, lambda e: ex[e], gs1, gs2, 10.0)
+        yf = sg.bf16_bits_to_f32(y)
+        float_parity(yf, sg.bf16_bits_to_f32(y_ref), bf16=True)
+        parts.append(yf)
+    float_parity(sum(parts), y_full, bf16_terms=parts)
+
+
+def test_mx_weights_nvfp4_activations_dsv4_tp3(oracle_svc):
+    """DeepSeek-V4-Flash TP3 (hidden 4096, 704 of 768, 256 experts, top-k 6) at T = 64: each rank's layer, with
+    its MXFP4 shard converted on the GPU and the full-width layer's activation scales, against the oracle; the
+    ranks' sum against the full-width layer; and the rank-0 layer captured in a CUDA graph replays the eager
+    rows bit for bit."""
+    import torch
+    wl = sg.TP3_MXFP4
+    wl_full = dataclasses.replace(wl, I=2048, I_logical=2048)
+    plan = mxfp4.tp_plan(2048, 3, 32, 128)
+    full = mxfp4.tp_plan(2048, 1, 32, 128)
+    T = 64
+    xw_bits = sg.activations_bf16(wl, sg.WARMUP_SEED, T=256)
+    gs1, gs2 = oracle_svc.mxnv_calibrate(wl_full, xw_bits, full, 0)
+    x_bits = sg.activations_bf16(wl, sg.EVAL_SEED, T=T)
+    ids_ref, w_ref = moe.topk_softmax(moe.router_logits(x_bits, sg.router_bf16(wl)), wl.k)
+    parts_ref = oracle_svc.mxnv_partials(wl_full, x_bits, ids_ref, gs1, gs2,
+                                         [(plan, 0), (plan, 1), (plan, 2), (full, 0)])
+    y_full = sg.bf16_bits_to_f32(moe.combine(ids_ref, w_ref, parts_ref[3]))
+    parts = []
+    for rank in range(3):
+        mx = _dsv4_mx_rank_layer(wl, wl_full, plan, rank, T)
+        nv, err = _nv_from_mx(mx, wl.H, wl.I, wl.I_log, wl.E, wl.k, T)
+        del mx
+        assert int(err[0].item()) == 0
+        nv.set_router(bits_to_torch(sg.router_bf16(wl)))
+        nv.set_global_scales(float(gs1), float(gs2))
+        y, ids = _forward(nv, x_bits, wl.k)
+        assert (ids == ids_ref).all(), rank
+        yf = sg.bf16_bits_to_f32(y)
+        float_parity(yf, sg.bf16_bits_to_f32(moe.combine(ids_ref, w_ref, parts_ref[rank])), bf16=True)
+        parts.append(yf)
+        if rank == 0:
+            xs = bits_to_torch(x_bits)
+            ys = torch.empty(T, wl.H, dtype=torch.bfloat16, device="cuda")
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                nv.forward(xs, ys)
+            for _ in range(2):
+                ys.fill_(0)
+                g.replay()
+                torch.cuda.synchronize()
+                assert np.array_equal(torch_to_bits(ys), y)
+            del g
+        assert nv.read_error() == 0
+        del nv
+        torch.cuda.empty_cache()
+    float_parity(sum(parts), y_full, bf16_terms=parts)
