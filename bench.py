@@ -246,7 +246,7 @@ def build_step(wl, cfg, layer, x, y, dev, n_stage_steps):
     if se:   # the shared expert's fp32 output rows
         bufs["o_shared"] = torch.empty(T, H, dtype=torch.float32, device=dev)
     if se or ep:   # the routed W2 rows, combined in a separate pass (with the slot mask under EP)
-        bufs["o_pairs"] = torch.empty(T * k, H, dtype=torch.float32, device=dev)
+        bufs["o_pairs"] = torch.empty(T * k, H, dtype=torch.bfloat16, device=dev)   # bf16 pair rows
     b = bufs
     stream = torch.cuda.current_stream()
     n_stage = 5

@@ -124,7 +124,7 @@ WsLayout ws_layout(const fp4moe_config& c) {
   L.a1sf = take(mx ? 0 : cap * (size_t)c.hidden / 16);
   L.a2 = take(mx ? cap * (size_t)c.inter * 2 : cap * (size_t)c.inter / 2);
   L.a2sf = take(mx ? 0 : cap * (size_t)c.inter / 16);
-  L.opairs = take(Tm * k * (size_t)c.hidden * 4);
+  L.opairs = take(Tm * k * (size_t)c.hidden * 2);  // bf16 pair rows
   L.alpha_tmp = take(E * 4);
   if (c.shared_inter > 0) {  // the shared expert: FP8 activations, their scales, and its fp32 output
     const size_t tcap = se_tcap(c), Is = (size_t)c.shared_inter, H = (size_t)c.hidden;
@@ -252,7 +252,7 @@ fp4moe_status forward_impl(const fp4moe_config* cfg, int32_t T, const uint16_t* 
       uint16_t* a2 = at<uint16_t>(ws, L.a2);
       FP4_TRY(scatter_rows_bf16_launch(*cfg, T, x, at<int32_t>(ws, L.slot), a1, st));
       FP4_TRY(mx_gemm_launch(false, *cfg, T, a1, poff, por, w1_fp4, w1_sf, a2, nullptr, err, st));
-      return mx_gemm_launch(true, *cfg, T, a2, poff, por, w2_fp4, w2_sf, nullptr, at<float>(ws, L.opairs), err, st);
+      return mx_gemm_launch(true, *cfg, T, a2, poff, por, w2_fp4, w2_sf, nullptr, at<uint16_t>(ws, L.opairs), err, st);
     }
     FP4_TRY(quant_scatter_launch(*cfg, T, x, gs1, at<int32_t>(ws, L.slot), at<uint8_t>(ws, L.a1),
                                  at<uint8_t>(ws, L.a1sf), scale_flags(ws), err, st));
@@ -260,7 +260,7 @@ fp4moe_status forward_impl(const fp4moe_config* cfg, int32_t T, const uint16_t* 
                         alpha1, gs2, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), amax_h_run(ws), scale_flags(ws),
                         nullptr, err, at<int>(ws, kWsSchedW1), st));
     return gemm_launch(kW2Rows, *cfg, T, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), poff, por, w2_fp4, w2_sf,
-                       alpha2, nullptr, nullptr, nullptr, nullptr, nullptr, at<float>(ws, L.opairs), err,
+                       alpha2, nullptr, nullptr, nullptr, nullptr, nullptr, at<uint16_t>(ws, L.opairs), err,
                        at<int>(ws, kWsSchedW2), st);
   };
   const fp4moe_status rr = routed();
@@ -269,7 +269,7 @@ fp4moe_status forward_impl(const fp4moe_config* cfg, int32_t T, const uint16_t* 
     rs = FP4MOE_CUDA_ERROR;
   FP4_TRY(rr);
   FP4_TRY(rs);
-  FP4_TRY(combine_launch(*cfg, T, at<float>(ws, L.opairs), w, cfg->ep_count > 0 ? at<int32_t>(ws, L.slot) : nullptr,
+  FP4_TRY(combine_launch(*cfg, T, at<uint16_t>(ws, L.opairs), w, cfg->ep_count > 0 ? at<int32_t>(ws, L.slot) : nullptr,
                          o_shared, y, st));
   const size_t pk = (size_t)T * cfg->top_k;
   if (topk_ids_out && pk && cudaMemcpyAsync(topk_ids_out, ids, pk * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
@@ -286,7 +286,7 @@ using namespace fp4moe;
 
 extern "C" {
 
-int32_t fp4moe_abi_version(void) { return 104; }
+int32_t fp4moe_abi_version(void) { return 105; }
 
 const char* fp4moe_status_string(fp4moe_status s) {
   switch (s) {
@@ -403,7 +403,7 @@ fp4moe_status moe_grouped_gemm_w1_swiglu(const fp4moe_config* cfg, int32_t T, co
 
 fp4moe_status moe_grouped_gemm_w2(const fp4moe_config* cfg, int32_t T, const uint8_t* a2_fp4, const uint8_t* a2_sf,
                                   const int32_t* padded_offsets, const int32_t* pair_of_row, const uint8_t* w2_fp4,
-                                  const uint8_t* w2_sf, const float* alpha2, float* o_pairs, void* ws,
+                                  const uint8_t* w2_sf, const float* alpha2, uint16_t* o_pairs, void* ws,
                                   fp4moe_stream_t stream) {
   FP4_TRY(check_cfg(cfg));
   FP4_TRY(check_T(cfg, T));
@@ -418,7 +418,7 @@ fp4moe_status moe_grouped_gemm_w2(const fp4moe_config* cfg, int32_t T, const uin
                      (cudaStream_t)stream);
 }
 
-fp4moe_status moe_combine(const fp4moe_config* cfg, int32_t T, const float* o_pairs, const float* topk_w,
+fp4moe_status moe_combine(const fp4moe_config* cfg, int32_t T, const uint16_t* o_pairs, const float* topk_w,
                           uint16_t* y, fp4moe_stream_t stream) {
   FP4_TRY(check_cfg(cfg));
   FP4_TRY(check_T(cfg, T));
@@ -436,7 +436,7 @@ fp4moe_status moe_grouped_gemm_w2_combine(const fp4moe_config* cfg, int32_t T, c
   FP4_TRY(check_T(cfg, T));
   if (cfg->ep_count > 0) return FP4MOE_UNSUPPORTED;  // the pairs held elsewhere are known only to moe_forward
   const WsLayout L = ws_layout(*cfg);
-  float* o = at<float>(ws, L.opairs);
+  uint16_t* o = at<uint16_t>(ws, L.opairs);
   if (is_mx(cfg)) {
     FP4_TRY(check_ptrs(a2_fp4, padded_offsets, pair_of_row, w2_fp4, w2_sf, topk_w, y, ws));
     FP4_TRY(mx_gemm_launch(true, *cfg, T, reinterpret_cast<const uint16_t*>(a2_fp4), padded_offsets, pair_of_row,
@@ -481,7 +481,7 @@ fp4moe_status moe_shared_expert(const fp4moe_config* cfg, int32_t T, const uint1
   return shared_launch(*cfg, T, x, *se, o_shared, ws, (cudaStream_t)stream);
 }
 
-fp4moe_status moe_combine_shared(const fp4moe_config* cfg, int32_t T, const float* o_pairs, const float* topk_w,
+fp4moe_status moe_combine_shared(const fp4moe_config* cfg, int32_t T, const uint16_t* o_pairs, const float* topk_w,
                                  const int32_t* slot_of_pair, const float* o_shared, uint16_t* y,
                                  fp4moe_stream_t stream) {
   FP4_TRY(check_cfg(cfg));

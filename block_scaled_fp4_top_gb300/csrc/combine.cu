@@ -2,11 +2,11 @@
 // expert's row o_shared[t] (weight 1, added last) when the layer has one.
 //
 // This is the scatter_add of "Current Bug: CuTeDSLMoERunner" ("Data Flow"),
-// restated as a gather. The second GEMM stores one fp32 row per (token, k)
-// pair and drops padding rows ("Bug 14"). Every token then sums its k rows in
-// a fixed j order, so the result has no atomics and is run-to-run
-// deterministic. One thread owns 8 consecutive columns, loaded and stored as
-// 128-bit vectors. Inputs written by the kernels just before are read through
+// restated as a gather. The second GEMM stores one bf16 row per (token, k)
+// pair (l2_out is BF16 there) and drops padding rows ("Bug 14"). Every token
+// then sums its k rows in fp32 in a fixed j order, so the result has no
+// atomics and is run-to-run deterministic. One thread owns 8 consecutive
+// columns: one 128-bit load per pair row, one 128-bit store of y. Inputs written by the kernels just before are read through
 // L2 (ld.global.cg): with programmatic dependent launch this kernel may start
 // before they finish.
 #include "common.cuh"
@@ -24,6 +24,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return l | (h << 16);
 }
 
+// Eight bf16 values through L2 as fp32.
+__device__ __forceinline__ void ld8_bf16_cg(const uint16_t* p, float (&v)[8]) {
+  const uint4 q = __ldcg(reinterpret_cast<const uint4*>(p));
+  v[0] = bf16_lo(q.x); v[1] = bf16_hi(q.x); v[2] = bf16_lo(q.y); v[3] = bf16_hi(q.y);
+  v[4] = bf16_lo(q.z); v[5] = bf16_hi(q.z); v[6] = bf16_lo(q.w); v[7] = bf16_hi(q.w);
+}
+
 // Eight fp32 values through L2: one 256-bit load (sm_100 and later) when the address is 32-byte aligned.
 template <bool V8>
 __device__ __forceinline__ void ld8_cg(const float* p, float (&v)[8]) {
@@ -39,12 +46,13 @@ __device__ __forceinline__ void ld8_cg(const float* p, float (&v)[8]) {
   }
 }
 
-// BATCH: a grid of one wave (decode). The token's k weights and slots are loaded first, then the rows of up
+// V8: the shared expert's fp32 rows are 32-byte aligned. BATCH: a grid of one wave (decode). The token's k
+// weights and slots are loaded first, then the rows of up
 // to 8 pairs at a time, all in flight before the sums. Otherwise many waves (prefill) keep the memory system
 // busy instead, and a lean loop keeps more CTAs resident. Either way the sum runs in pair order and a pair
 // held by no local expert (it has no row) is skipped.
 template <bool V8, bool BATCH>
-__global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float* __restrict__ o,
+__global__ void __launch_bounds__(256) combine_kernel(int H, int k, const uint16_t* __restrict__ o,
                                                       const float* __restrict__ w,
                                                       const int32_t* __restrict__ slot_of_pair,
                                                       const float* __restrict__ o_shared,
@@ -60,7 +68,7 @@ __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float*
       if (slot_of_pair != nullptr && __ldcg(slot_of_pair + (size_t)t * k + j) < 0) continue;
       const float wj = __ldcg(w + (size_t)t * k + j);
       float v[8];
-      ld8_cg<V8>(o + ((size_t)t * k + j) * H + col, v);
+      ld8_bf16_cg(o + ((size_t)t * k + j) * H + col, v);
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
     }
@@ -78,7 +86,7 @@ __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float*
       float v[8][8];
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj)
-        if (held[j0 + jj]) ld8_cg<V8>(o + ((size_t)t * k + j0 + jj) * H + col, v[jj]);
+        if (held[j0 + jj]) ld8_bf16_cg(o + ((size_t)t * k + j0 + jj) * H + col, v[jj]);
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
         if (held[j0 + jj]) {
@@ -101,12 +109,12 @@ __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float*
 
 }  // namespace
 
-fp4moe_status combine_launch(const fp4moe_config& cfg, int32_t T, const float* o_pairs, const float* w,
+fp4moe_status combine_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* o_pairs, const float* w,
                              const int32_t* slot_of_pair, const float* o_shared, uint16_t* y, cudaStream_t st) {
   if (T == 0) return FP4MOE_OK;
   const int H = cfg.hidden;
-  // 256-bit loads when every row start is 32-byte aligned (H is a multiple of 256)
-  const bool v8 = ((reinterpret_cast<uintptr_t>(o_pairs) | reinterpret_cast<uintptr_t>(o_shared)) & 31u) == 0;
+  // 256-bit loads of the shared expert's fp32 rows when every row start is 32-byte aligned (H % 256 == 0)
+  const bool v8 = (reinterpret_cast<uintptr_t>(o_shared) & 31u) == 0;
   const dim3 grid((H / 8 + 255) / 256, T);
   const bool batch = (int64_t)grid.x * grid.y <= sm_count();  // one wave: latency rules
   cudaError_t r;

@@ -43,6 +43,12 @@ __device__ __forceinline__ void raise_error(uint32_t* err, uint32_t bits) { atom
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Two fp32 values as bf16 (round to nearest even), `lo` in the low half.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+         ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+}
+
 // ----------------------------------------------------------- FP8/FP4 cvt --
 // E4M3 (satfinite, RNE) of a non-negative fp32; returns the byte.
 __device__ __forceinline__ uint32_t cvt_e4m3(float s) {

@@ -520,7 +520,7 @@ size_t tiled_weight_bytes(int32_t rows, int32_t K) { return (size_t)rows * (size
 fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, const uint8_t* a_codes,
                           const uint8_t* a_sf, const int32_t* poff, const int32_t* pair_of_row,
                           const uint8_t* b_codes, const uint8_t* b_sf, const float* alpha, const float* gs2,
-                          uint8_t* out_codes, uint8_t* out_sf, float* amax, uint32_t* status, float* o_pairs,
+                          uint8_t* out_codes, uint8_t* out_sf, float* amax, uint32_t* status, uint16_t* o_pairs,
                           uint32_t* err, int* sched, cudaStream_t st) {
   if (T == 0) return FP4MOE_OK;
   if (mode != kW2Rows && amax == nullptr) return FP4MOE_INVALID_ARG;

@@ -24,9 +24,9 @@ struct GemmParams {
   uint8_t* out_sf;
   float* amax;       // W1 amax: the calibration maximum; W1 + SwiGLU: the running amax|h| (both non-negative)
   uint32_t* status;  // W1 + SwiGLU: sticky FP4MOE_SAT_* bits
-  float* o_pairs;
+  uint16_t* o_pairs;  // W2: bf16 rows [T*k][H] ("Data Flow": l2_out is BF16)
   uint32_t* err;
-  int o_pairs32;  // W2: o_pairs is 32-byte aligned (every row is then, H being a multiple of 256)
+  int o_pairs32;  // W2: o_pairs is 32-byte aligned (every 128-column piece of a row is then)
   int dyn;     // 1: dynamic chunk schedule (large T); 0: contiguous static ranges (decode sizes)
   int* sched;  // dynamic schedule: next-chunk counter, zero at launch
 };
@@ -193,7 +193,7 @@ __device__ __forceinline__ void cta_range(int total, int& tau0, int& tau1) {
 
 
 // The epilogue of one accumulator row: 128 columns of weight tile nt for activation row r, which holds pair
-// p (p >= 0). W2: the alpha-scaled fp32 row of the pair. W1: alpha, then the clamped SwiGLU (gate columns
+// p (p >= 0). W2: the alpha-scaled row of the pair, rounded once to bf16. W1: alpha, then the clamped SwiGLU (gate columns
 // 0-63, up columns 64-127, from the W1 kernel row order) and its NVFP4 requantisation into the L2 slot
 // buffers ("Bug 6", "Bug 7"). W1 amax: the same SwiGLU, reduced only. hrun keeps the NaN-propagating
 // amax|h| of the thread's rows.
@@ -201,20 +201,23 @@ template <int MODE, class P>
 __device__ __forceinline__ void epilogue_row(const P& prm, const float (&v)[128], int r, int p, int nt, float alpha,
                                              float& hrun) {
   if constexpr (MODE == kW2Rows) {
-    float* d = prm.o_pairs + (size_t)p * prm.H + nt * 128;
-    if (prm.o_pairs32) {
-      // the thread's row in 32-byte stores: whole L2 sectors, half the write transactions of 16-byte ones
+    uint16_t* d = prm.o_pairs + (size_t)p * prm.H + nt * 128;
+    // the alpha-scaled row as bf16 pairs, 16 values (32 bytes) at a time
 #pragma unroll
-      for (int q = 0; q < 16; ++q)
-        st_global_v8(d + 8 * q, __fmul_rn(v[8 * q], alpha), __fmul_rn(v[8 * q + 1], alpha),
-                     __fmul_rn(v[8 * q + 2], alpha), __fmul_rn(v[8 * q + 3], alpha), __fmul_rn(v[8 * q + 4], alpha),
-                     __fmul_rn(v[8 * q + 5], alpha), __fmul_rn(v[8 * q + 6], alpha), __fmul_rn(v[8 * q + 7], alpha));
-    } else {  // a caller's buffer aligned to 16 bytes only
-      float4* d4 = reinterpret_cast<float4*>(d);
+    for (int q = 0; q < 8; ++q) {
+      uint32_t w[8];
 #pragma unroll
-      for (int q = 0; q < 32; ++q)
-        d4[q] = make_float4(__fmul_rn(v[4 * q], alpha), __fmul_rn(v[4 * q + 1], alpha), __fmul_rn(v[4 * q + 2], alpha),
-                            __fmul_rn(v[4 * q + 3], alpha));
+      for (int i = 0; i < 8; ++i)
+        w[i] = bf16x2_rn(__fmul_rn(v[16 * q + 2 * i], alpha), __fmul_rn(v[16 * q + 2 * i + 1], alpha));
+      if (prm.o_pairs32) {  // whole 32-byte L2 sectors: half the write transactions of 16-byte stores
+        st_global_v8(reinterpret_cast<float*>(d) + 8 * q, __uint_as_float(w[0]), __uint_as_float(w[1]),
+                     __uint_as_float(w[2]), __uint_as_float(w[3]), __uint_as_float(w[4]), __uint_as_float(w[5]),
+                     __uint_as_float(w[6]), __uint_as_float(w[7]));
+      } else {  // a caller's buffer aligned to 16 bytes only
+        uint4* d4 = reinterpret_cast<uint4*>(d) + 2 * q;
+        d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
     }
   } else {
     // columns [0, 64): gate of features 64 nt .. 64 nt + 63; columns [64, 128): up of the same features

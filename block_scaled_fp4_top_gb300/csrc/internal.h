@@ -86,7 +86,7 @@ enum GemmMode { kW1SwiGLU = 0, kW1Amax = 1, kW2Rows = 2 };
 fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, const uint8_t* a_codes,
                           const uint8_t* a_sf, const int32_t* poff, const int32_t* pair_of_row,
                           const uint8_t* b_codes, const uint8_t* b_sf, const float* alpha, const float* gs2,
-                          uint8_t* out_codes, uint8_t* out_sf, float* amax, uint32_t* status, float* o_pairs,
+                          uint8_t* out_codes, uint8_t* out_sf, float* amax, uint32_t* status, uint16_t* o_pairs,
                           uint32_t* err, int* sched, cudaStream_t st);
 
 // SMs of the current device (cached per device), 0 on error
@@ -101,7 +101,7 @@ fp4moe_status selftest_wait_launch(uint32_t* err, int64_t limit_ns, uint32_t* re
 // w2 = true: W2 into fp32 rows o_pairs [T*k][H]. Weights in the atom-tiled MXFP4 layout (see fp4moe.h).
 fp4moe_status mx_gemm_launch(bool w2, const fp4moe_config& cfg, int32_t T, const uint16_t* a_bf16,
                              const int32_t* poff, const int32_t* pair_of_row, const uint8_t* b_codes,
-                             const uint8_t* b_sf, uint16_t* out_bf16, float* o_pairs, uint32_t* err,
+                             const uint8_t* b_sf, uint16_t* out_bf16, uint16_t* o_pairs, uint32_t* err,
                              cudaStream_t st);
 fp4moe_status mx_quant_rows_launch(int64_t n_rows, int32_t K, int32_t rows_per_group, int32_t inter, const float* in,
                                    uint8_t* codes, uint8_t* sf, cudaStream_t st);
@@ -121,7 +121,7 @@ fp4moe_status scatter_rows_bf16_launch(const fp4moe_config& cfg, int32_t T, cons
 
 // y[t] = bf16(sum_j w[t,j] o[t*k+j] + o_shared[t]); with slot_of_pair, pairs without a slot (held by no local
 // expert) are left out of the sum; o_shared may be null
-fp4moe_status combine_launch(const fp4moe_config& cfg, int32_t T, const float* o_pairs, const float* w,
+fp4moe_status combine_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* o_pairs, const float* w,
                              const int32_t* slot_of_pair, const float* o_shared, uint16_t* y, cudaStream_t st);
 
 // segemm.cu: the block-FP8 shared expert. se_tcap: rows of its activation buffers (max_tokens rounded up to

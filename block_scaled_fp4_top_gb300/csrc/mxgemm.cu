@@ -72,7 +72,7 @@ struct MxParams {
   const uint8_t* b_codes;
   const uint8_t* b_sf;
   uint16_t* out_bf16;  // W1: h rows [cap][I] bf16
-  float* o_pairs;      // W2: fp32 rows [T*k][H]
+  uint16_t* o_pairs;   // W2: bf16 rows [T*k][H]
   uint32_t* err;
 };
 
@@ -321,9 +321,11 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
             tmem_ld32(tacc + 32 * q, v);
             tmem_ld_wait();
             if (p >= 0) {
-              float4* d4 = reinterpret_cast<float4*>(prm.o_pairs + (size_t)p * prm.H + t.nt * MX_BN + 32 * q);
+              uint4* d4 = reinterpret_cast<uint4*>(prm.o_pairs + (size_t)p * prm.H + t.nt * MX_BN + 32 * q);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+              for (int i = 0; i < 4; ++i)
+                d4[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                   pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
             }
           }
         }
@@ -555,7 +557,7 @@ __global__ void __launch_bounds__(256) scatter_rows_bf16_kernel(int H, int k, co
 
 fp4moe_status mx_gemm_launch(bool w2, const fp4moe_config& cfg, int32_t T, const uint16_t* a_bf16,
                              const int32_t* poff, const int32_t* pair_of_row, const uint8_t* b_codes,
-                             const uint8_t* b_sf, uint16_t* out_bf16, float* o_pairs, uint32_t* err,
+                             const uint8_t* b_sf, uint16_t* out_bf16, uint16_t* o_pairs, uint32_t* err,
                              cudaStream_t st) {
   if (T == 0) return FP4MOE_OK;
   MxParams prm;

@@ -322,20 +322,23 @@ fp4moe_status moe_grouped_gemm_w1_swiglu(const fp4moe_config* cfg, int32_t T, co
 /*
  * moe_grouped_gemm_w2: the second grouped GEMM on its own. For every real
  * row r (pair p = pair_of_row[r]),
- *   o_pairs[p][:] = alpha2[e] * (A2[r] . W2_e)  (fp32 [T*k][H]).
- * Source: "Current Bug", "Data Flow" (L2 grouped GEMM -> l2_out).
+ *   o_pairs[p][:] = bf16( alpha2[e] * (A2[r] . W2_e) )  (bf16 [T*k][H]),
+ * the fp32 accumulator rounded once to bf16 (round to nearest even).
+ * Source: "Current Bug", "Data Flow" (L2 grouped GEMM -> l2_out (BF16)).
+ * Rows of pairs that no local expert holds are not written.
  */
 fp4moe_status moe_grouped_gemm_w2(const fp4moe_config* cfg, int32_t T, const uint8_t* a2_fp4, const uint8_t* a2_sf,
                                   const int32_t* padded_offsets, const int32_t* pair_of_row, const uint8_t* w2_fp4,
-                                  const uint8_t* w2_sf, const float* alpha2, float* o_pairs, void* ws,
+                                  const uint8_t* w2_sf, const float* alpha2, uint16_t* o_pairs, void* ws,
                                   fp4moe_stream_t stream);
 
 /*
  * moe_combine: y[t][:] = bf16( sum_{j=0..k-1} topk_w[t][j] * o_pairs[t*k+j][:] ),
- * accumulated in fp32 in j order. Source: "Current Bug", "Data Flow"
- * (scatter_add -> y) and "Bug 14" (padding rows are dropped).
+ * o_pairs bf16 [T*k][H] (as moe_grouped_gemm_w2 writes it), accumulated in
+ * fp32 in j order. Source: "Current Bug", "Data Flow" (l2_out (BF16) ->
+ * scatter_add -> y) and "Bug 14" (padding rows are dropped).
  */
-fp4moe_status moe_combine(const fp4moe_config* cfg, int32_t T, const float* o_pairs, const float* topk_w,
+fp4moe_status moe_combine(const fp4moe_config* cfg, int32_t T, const uint16_t* o_pairs, const float* topk_w,
                           uint16_t* y, fp4moe_stream_t stream);
 
 /* moe_grouped_gemm_w2 followed by moe_combine, with o_pairs inside `ws`. */
@@ -427,7 +430,7 @@ fp4moe_status moe_shared_expert(const fp4moe_config* cfg, int32_t T, const uint1
  * slot -1 (held by another rank) are left out, which makes it valid for
  * expert-parallel layers. o_shared may be NULL (no shared term).
  */
-fp4moe_status moe_combine_shared(const fp4moe_config* cfg, int32_t T, const float* o_pairs, const float* topk_w,
+fp4moe_status moe_combine_shared(const fp4moe_config* cfg, int32_t T, const uint16_t* o_pairs, const float* topk_w,
                                  const int32_t* slot_of_pair, const float* o_shared, uint16_t* y,
                                  fp4moe_stream_t stream);
 

@@ -17,8 +17,8 @@ The oracle states this per token. It does not scatter, pad or tile:
       [g; u] = alpha-scaled W1~_e x~_t
       h      = silu(min(g, L)) * clamp(u, -L, L)
       h~     = dequant(quant(RN_f32(h), gs2))
-      o_e    = W2~_e h~
-  y_t   = bf16( sum_{j = 0..k-1} w_t,j * o_{e_j} )  (in j order)
+      o_e    = W2~_e h~, returned in bf16 (l2_out is BF16 in "Data Flow")
+  y_t   = bf16( sum_{j = 0..k-1} w_t,j * bf16(o_{e_j}) )  (in j order)
 
 Readings where the pages are silent:
 * The clamp form. "Lucifer-CUTLASS TP3 virtual-padding audit", section
@@ -160,10 +160,19 @@ def routed_rows(ids: np.ndarray) -> dict:
     return {int(e): np.nonzero(ids == e) for e in np.unique(ids) if e >= 0}
 
 
+def l2_out_bf16(outs: np.ndarray) -> np.ndarray:
+    """The second GEMM's output as "Data Flow" returns it (l2_out, BF16): fp64 -> fp32 -> bf16, round to nearest
+    even at each step, back as fp64."""
+    return bf16_to_f64(f32_to_bf16_bits(np.asarray(outs, dtype=np.float64).astype(F32)))
+
+
 def combine(ids: np.ndarray, w: np.ndarray, outs: np.ndarray, shared: np.ndarray | None = None) -> np.ndarray:
-    """y = bf16( sum_{j = 0..k-1} w[:, j] * outs[:, j] (+ shared) ), summed in j order; pairs with id -1 (held
-    elsewhere) are skipped. outs [n, k, H] fp64. Returns bf16 bits [n, H]."""
+    """y = bf16( sum_{j = 0..k-1} w[:, j] * bf16(outs[:, j]) (+ shared) ), summed in j order; pairs with id -1
+    (held elsewhere) are skipped. outs [n, k, H] fp64 are the pair rows of the second GEMM, which "Data Flow"
+    returns in BF16 (l2_out) before the scatter_add; shared (fp32 values) is added as it is. Returns bf16
+    bits [n, H]."""
     n, k = ids.shape
+    outs = l2_out_bf16(outs)
     acc = np.zeros((n, outs.shape[2]), dtype=np.float64)
     for j in range(k):
         held = (ids[:, j] >= 0)[:, None]

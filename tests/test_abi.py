@@ -63,7 +63,7 @@ def test_sizes(lib):
                                 256 * 4096 * 2048 // 16)
     ws = api.workspace_bytes(cfg)
     cap = layout.capacity_rows(64, 6, 256)
-    assert ws >= cap * (4096 // 2 + 4096 // 16 + 2048 // 2 + 2048 // 16) + 64 * 6 * 4096 * 4
+    assert ws >= cap * (4096 // 2 + 4096 // 16 + 2048 // 2 + 2048 // 16) + 64 * 6 * 4096 * 2   # bf16 pair rows
     assert api.workspace_bytes(_cfg(hidden=100)) == 0  # unsupported shape -> 0
 
 
@@ -98,7 +98,7 @@ def test_argument_checks(lib):
     assert lib.fp4moe_selftest_wait_timeout(p, 60_000_000, p, None) == _lib.INVALID_ARG  # above 50 ms
     assert lib.fp4moe_selftest_wait_timeout(ctypes.c_void_p(0x10002), 5_000_000, p, None) == _lib.MISALIGNED
     assert lib.fp4moe_status_string(_lib.CAPACITY) == b"FP4MOE_CAPACITY"
-    assert lib.fp4moe_abi_version() == 104
+    assert lib.fp4moe_abi_version() == 105
 
 
 def test_shared_expert_checks_and_sizes(lib):

@@ -97,7 +97,7 @@ def test_identity_codec_layer_is_the_textbook_dense_moe():
     gu = torch.einsum("th,eoh->teo", xt, W1)
     I = wl.I
     h = F.silu(gu[..., :I].clamp(max=wl.swiglu_limit)) * gu[..., I:].clamp(-wl.swiglu_limit, wl.swiglu_limit)
-    o = torch.einsum("tei,ehi->teh", h, W2)
+    o = torch.einsum("tei,ehi->teh", h, W2).float().bfloat16().double()   # l2_out is BF16 ("Data Flow")
     lt = torch.from_numpy(l.astype(np.float64))
     tv, ti = torch.topk(lt, wl.k, dim=1)
     wt = torch.softmax(tv, dim=1)
@@ -129,8 +129,9 @@ def _naive_layer(x_bits, ids, w, experts, gs1, gs2, L):
             h = moe.swiglu(np.array(gate), np.array(up), L).astype(np.float32).reshape(1, I)
             q2, s2 = nvfp4.quantize_rows(h, gs2)
             ht = [float(codecs.e2m1_decode(q2[0, c])) * float(codecs.e4m3_decode(s2[0, c // 16])) / float(gs2) for c in range(I)]
-            for r in range(H):
-                acc[r] += w[t, j] * sum(w2(r, c) * ht[c] for c in range(I))
+            for r in range(H):   # each pair row leaves the second GEMM in BF16 ("Data Flow": l2_out)
+                o_r = sum(w2(r, c) * ht[c] for c in range(I))
+                acc[r] += w[t, j] * float(torch.tensor(o_r, dtype=torch.float64).float().bfloat16().double())
         out.append(acc)
     return np.array(out)
 
@@ -165,7 +166,8 @@ def test_calibration_scales_come_from_the_warmup_batch():
 
 
 def test_expert_parallel_parts_sum_to_the_layer():
-    """The rank parts of an EP split (masked pairs left out) sum to the whole layer, before the bf16 rounding."""
+    """The rank parts of an EP split (masked pairs left out) sum to the whole layer, before the final bf16
+    rounding (each pair row already in BF16, as the second GEMM returns it)."""
     wl = sg.TINY
     x = sg.activations_bf16(wl, sg.EVAL_SEED, T=6)
     ids, w = moe.topk_softmax(moe.router_logits(x, sg.router_bf16(wl), None), wl.k)
@@ -189,7 +191,7 @@ def test_expert_parallel_parts_sum_to_the_layer():
                     continue
                 qe = expert(first + int(ids_local[t, j]))
                 h = moe.expert_hidden(qe, xt[t:t + 1], wl.swiglu_limit)
-                acc[t] += w[t, j] * moe.expert_out(qe, h, gs2)[0]
+                acc[t] += w[t, j] * moe.l2_out_bf16(moe.expert_out(qe, h, gs2))[0]
         return acc
 
     full = layer_sum(ids, 0)

@@ -142,7 +142,7 @@ def test_layer_on_exactly_representable_weights_is_the_textbook_moe():
             g, u = gu[:I], gu[I:]
             h = torch.minimum(g, torch.tensor(L)) * torch.sigmoid(torch.minimum(g, torch.tensor(L))) * u.clamp(-L, L)
             h = h.float().bfloat16().double()
-            y[t] += float(w[t, j]) * (W2 @ h)
+            y[t] += float(w[t, j]) * (W2 @ h).float().bfloat16().double()   # l2_out is BF16 ("Data Flow")
     ref = y.float().bfloat16().view(torch.int16).numpy().view(np.uint16)
     # the dense path rounds h and y exactly as the oracle does; only the fp64 summation order differs, which
     # cannot move a bf16 rounding here, so the bits must agree (a truncating or skipped h rounding would not)
