@@ -1,8 +1,9 @@
 // Dense FP4 tensor-core throughput probe: the peak that the prefill GEMMs'
 // tensor-pipe utilisation is reported against.
 //
-// One CTA per SM. Each stages one zeroed K atom of A (128 rows) and B (n rows)
-// in shared memory with the 128-byte swizzle, zeroes its block scales in TMEM,
+// One CTA per SM. Each stages one K atom of A (128 rows) and B (n rows) of
+// pseudo-random codes in shared memory with the 128-byte swizzle, sets its
+// block scales in TMEM to 1.0,
 // and then one thread issues `iters` x 4 back-to-back
 // tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X (M = 128,
 // N = n, K = 64) into one TMEM accumulator: the grouped GEMMs' instruction at
@@ -26,9 +27,11 @@ __global__ void __launch_bounds__(128, 1) tensor_peak_kernel(int n, int iters, u
   const uint32_t smem = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t a_s = smem, b_s = smem + 16384u, sf_s = smem + 16384u + 32768u;
   const int warp = threadIdx.x >> 5;
-  // zero operands and the scale tile: the values do not matter for the rate, but stay finite
-  uint4* base = reinterpret_cast<uint4*>(smem_raw + (smem - smem_u32(smem_raw)));
-  for (int i = threadIdx.x; i < (16384 + 32768 + 512) / 16; i += blockDim.x) base[i] = make_uint4(0u, 0u, 0u, 0u);
+  // operands: pseudo-random codes (every E2M1 value, as real data has them; zeros could take a cheaper path
+  // through the tensor core); scales: all 0x38 (1.0), so every product stays finite
+  uint32_t* base = reinterpret_cast<uint32_t*>(smem_raw + (smem - smem_u32(smem_raw)));
+  for (int i = threadIdx.x; i < (16384 + 32768) / 4; i += blockDim.x) base[i] = (uint32_t)i * 2654435761u ^ 0x5bd1e995u;
+  for (int i = threadIdx.x; i < 512 / 4; i += blockDim.x) base[(16384 + 32768) / 4 + i] = 0x38383838u;
   fence_proxy_async_smem();
   if (warp == 0) {
     tmem_alloc(smem_u32(&s_tmem), 512);
@@ -44,7 +47,7 @@ __global__ void __launch_bounds__(128, 1) tensor_peak_kernel(int n, int iters, u
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   if (threadIdx.x == 0) {
-    // zero scales: A's at columns 256..271, B's at 384..447 (room for any N up to 256)
+    // scales 1.0: A's at columns 256..271, B's at 384..447 (room for any N up to 256)
     for (int c = 0; c < 4; ++c) tc_cp_scales(tmem + 256 + 4 * c, desc_scales(sf_s));
     for (int c = 0; c < 16; ++c) tc_cp_scales(tmem + 384 + 4 * c, desc_scales(sf_s));
     const uint32_t idesc = n == 256 ? idesc_nvf4(128, 256) : idesc_nvf4(128, 128);
