@@ -214,8 +214,11 @@ __global__ void __launch_bounds__(256) hist_kernel(int T, int Eg, int first, int
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(size_t)blockIdx.x * E + e] = sh[e];
 }
 
-// One CTA of 1024 threads, thread e = expert e: exclusive prefix of the chunk
-// histograms (in place), then counts, offsets, padded offsets and pads.
+// One CTA of 1024 threads: exclusive prefix of the chunk histograms over the chunks (in place), then
+// counts, offsets, padded offsets and pads. Each expert's column is split among tpe = 1024 / E threads
+// (a power of two, at most 32, so one warp holds them all): every part loads its run of chunk counts at
+// once, the parts' sums are scanned across their lanes, and each part rewrites its run from its own base.
+// For E = 256 that is four parts of 32 chunks at T = 8192: one round trip to L2 instead of eight.
 __global__ void __launch_bounds__(1024) scan_kernel(int E, int nchunks, int cap, int32_t* __restrict__ hist,
                                                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                     int32_t* __restrict__ poff, int32_t* __restrict__ pair_of_row,
@@ -223,47 +226,92 @@ __global__ void __launch_bounds__(1024) scan_kernel(int E, int nchunks, int cap,
   pdl_wait();
   pdl_trigger();
   __shared__ int s_warp[64];
-  const int e = threadIdx.x;
-  int c = 0;
+  __shared__ int s_c[kMaxExperts];
+  int tpe = 1;
+  while (tpe < 32 && tpe * 2 * E <= 1024) tpe *= 2;
+  const int e = threadIdx.x / tpe, q = threadIdx.x % tpe;
+  const int per = (nchunks + tpe - 1) / tpe, b0 = q * per, b1 = min(nchunks, b0 + per);
+  int sum = 0;
   if (e < E) {
-    // 16 chunk counts are loaded before any is overwritten, so the loads overlap
-    for (int b0 = 0; b0 < nchunks; b0 += 16) {
+    // this part's chunk counts, 16 loads in flight at a time
+    for (int bb = b0; bb < b1; bb += 16) {
       int h[16];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) h[q] = (b0 + q < nchunks) ? __ldcg(hist + (size_t)(b0 + q) * E + e) : 0;
+      for (int i = 0; i < 16; ++i) h[i] = (bb + i < b1) ? __ldcg(hist + (size_t)(bb + i) * E + e) : 0;
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        if (b0 + q < nchunks) hist[(size_t)(b0 + q) * E + e] = c;
-        c += h[q];
-      }
+      for (int i = 0; i < 16; ++i) sum += h[i];
     }
   }
+  // exclusive prefix of the parts' sums across the tpe lanes of expert e (one warp holds them all)
+  int incl = sum;
+  for (int off = 1; off < tpe; off <<= 1) {
+    const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off, tpe);
+    if (q >= off) incl += o;
+  }
+  int run = incl - sum;
+  if (e < E) {
+    for (int bb = b0; bb < b1; bb += 16) {
+      int h[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) h[i] = (bb + i < b1) ? __ldcg(hist + (size_t)(bb + i) * E + e) : 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (bb + i < b1) hist[(size_t)(bb + i) * E + e] = run;
+        run += h[i];
+      }
+    }
+    if (q == tpe - 1) s_c[e] = incl;  // the expert's total count
+  }
+  __syncthreads();
+  const int c = threadIdx.x < E ? s_c[threadIdx.x] : 0;
   int start;
   int r_lo, r_hi;  // one part: every row
   offsets_and_pads(E, cap, c, s_warp, counts, offsets, poff, pair_of_row, err, 0, 1, start, r_lo, r_hi);
 }
 
-// Slot of every pair of one 64-token chunk, in ascending pair order.
-__global__ void __launch_bounds__(256) slots_kernel(int T, int Eg, int first, int E, int k, int cap,
-                                                    const int32_t* __restrict__ ids,
-                                                    const int32_t* __restrict__ counts,
-                                                    const int32_t* __restrict__ poff,
-                                                    const int32_t* __restrict__ chunk_base,
-                                                    int32_t* __restrict__ slot_of_pair,
-                                                    int32_t* __restrict__ pair_of_row, uint32_t* err) {
+// Slot of every pair of one 64-token chunk, in ascending pair order. The chunk's pairs are cut into one
+// contiguous run per warp. Each warp counts its run's pairs per expert into its own shared-memory row; a
+// prefix over the warp rows then gives every warp, for every expert, the first slot after the pairs of the
+// chunk's earlier runs; within a run, lanes that share an expert rank themselves by lane order, 32 pairs at
+// a time. No slot depends on the order of atomics.
+constexpr int kSlotWarps = 8;
+__global__ void __launch_bounds__(32 * kSlotWarps) slots_kernel(int T, int Eg, int first, int E, int k, int cap,
+                                                                const int32_t* __restrict__ ids,
+                                                                const int32_t* __restrict__ counts,
+                                                                const int32_t* __restrict__ poff,
+                                                                const int32_t* __restrict__ chunk_base,
+                                                                int32_t* __restrict__ slot_of_pair,
+                                                                int32_t* __restrict__ pair_of_row, uint32_t* err) {
   pdl_wait();
   pdl_trigger();
-  __shared__ int base[kMaxExperts];
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    base[e] = __ldcg(chunk_base + (size_t)blockIdx.x * E + e) + (__ldcg(poff + e) - ((__ldcg(counts + e) + 127) & ~127));
+  extern __shared__ int s_cnt[];  // [kSlotWarps][E]: pairs of each warp's run per expert, then its first slot
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kSlotWarps * E; i += blockDim.x) s_cnt[i] = 0;
   __syncthreads();
-  if (threadIdx.x >= 32) return;
-  const int lane = threadIdx.x;
   const int p0 = blockIdx.x * kRouteChunk * k;
   const int p1 = min(T, (blockIdx.x + 1) * kRouteChunk) * k;
-  for (int pb = p0; pb < p1; pb += 32) {
+  const int per = ((p1 - p0) + kSlotWarps - 1) / kSlotWarps;
+  const int w0 = min(p1, p0 + warp * per), w1 = min(p1, w0 + per);
+  for (int p = w0 + lane; p < w1; p += 32) {
+    const int e = local_expert(__ldcg(ids + p), Eg, first, E);
+    if (e >= 0) atomicAdd(&s_cnt[warp * E + e], 1);
+  }
+  __syncthreads();
+  // per expert: the chunk's base slot, then each warp row's first slot (exclusive prefix over the warps)
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = __ldcg(chunk_base + (size_t)blockIdx.x * E + e) + (__ldcg(poff + e) - ((__ldcg(counts + e) + 127) & ~127));
+#pragma unroll
+    for (int w = 0; w < kSlotWarps; ++w) {
+      const int c = s_cnt[w * E + e];
+      s_cnt[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  int* base = s_cnt + warp * E;
+  for (int pb = w0; pb < w1; pb += 32) {
     const int p = pb + lane;
-    int e = (p < p1) ? local_expert(__ldcg(ids + p), Eg, first, E) : -1;
+    int e = (p < w1) ? local_expert(__ldcg(ids + p), Eg, first, E) : -1;
     if (e < 0) e = -1;
     const unsigned peers = __match_any_sync(kFull, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
@@ -272,7 +320,7 @@ __global__ void __launch_bounds__(256) slots_kernel(int T, int Eg, int first, in
       slot_of_pair[p] = slot;
       if (slot < cap) pair_of_row[slot] = p;
       else raise_error(err, FP4MOE_ERR_CAPACITY);
-    } else if (p < p1) {
+    } else if (p < w1) {
       slot_of_pair[p] = -1;  // held by no local expert: no slot
     }
     __syncwarp();
@@ -306,7 +354,8 @@ fp4moe_status route_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* 
       r = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, st, E, nchunks, cap, hist, counts, offsets, poff,
                      pair_of_row, err);
     if (r == cudaSuccess)
-      r = launch_pdl(slots_kernel, dim3(nchunks), dim3(256), 0, st, T, Eg, first, E, k, cap, (const int32_t*)ids,
+      r = launch_pdl(slots_kernel, dim3(nchunks), dim3(32 * kSlotWarps), (size_t)kSlotWarps * E * sizeof(int), st, T, Eg,
+                     first, E, k, cap, (const int32_t*)ids,
                      (const int32_t*)counts, (const int32_t*)poff, (const int32_t*)hist, slot_of_pair, pair_of_row,
                      err);
   }
