@@ -108,7 +108,9 @@ def test_route_zipf_prefill():
     assert L["counts"].max() > 1000 and (L["counts"] == 0).sum() >= 16
 
 
-@pytest.mark.parametrize("wl,T", [(sg.TINY, 16), (sg.TINY, 3), (sg.DSV4_DECODE, 64)])
+# DSV4 at T = 300 and the Zipf prefill at T = 8192 take the four-blocks-per-thread path (T * H / 16 >= 65536)
+@pytest.mark.parametrize("wl,T", [(sg.TINY, 16), (sg.TINY, 3), (sg.DSV4_DECODE, 64), (sg.DSV4_DECODE, 300),
+                                  (sg.DSV4_PREFILL_ZIPF, 8192)])
 def test_quantize_scatter_bit_exact(wl, T):
     import torch
     from block_scaled_fp4_top_gb300 import api
