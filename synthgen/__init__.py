@@ -10,14 +10,10 @@ Generator (counter-based, so any slice of any tensor can be drawn on its own):
   generators", OOPSLA 2014). The stream key of a tensor is
   ``mix64(seed * GOLDEN + tensor_id)``. Element ``i`` of the tensor is
   ``mix64(key + (i + 1) * GOLDEN)``. Everything is modulo 2**64.
-* Approximate normal variate of element ``i``: the Irwin-Hall sum of the twelve
-  16-bit fields of words ``3i, 3i + 1, 3i + 2``, ``S`` in ``[0, 786420]``,
-  centred and scaled to unit variance: ``z = f32(S - 393210) * 2**-16`` (both
-  steps exact). Then ``value = f32(z * sigma)``, one IEEE fp32 multiplication
-  with round-to-nearest-even. Twelve uniforms put the support out to 6 sigma
-  (a normal passes 6 sigma with probability 2e-9) and leave about half the
-  normal's mass beyond 3.5 sigma (2.5e-4 against 4.65e-4), where a sum of four
-  uniforms, bounded at 3.46 sigma, has none.
+* Approximate normal variate: Irwin-Hall sum of the four 16-bit fields of that
+  64-bit word, ``S`` in ``[0, 262140]``, centred and scaled to unit variance:
+  ``z = f32(S - 131070) * f32(sqrt(3) / 65536)``. Then ``value = f32(z * sigma)``.
+  Each step is one IEEE fp32 operation with round-to-nearest-even.
   A second implementation (``synthgen/csrc/synth.cu``) therefore gives the same
   bits on the GPU.
 * Bernoulli(p) mask: the high 32 bits of a second stream's word, compared with
@@ -39,10 +35,9 @@ import numpy as np
 GOLDEN = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
-#: Irwin-Hall(12 x 16 bit): centre 12 * 65535 / 2 and scale 2^-16 (variance 1 - 2^-32)
-IH_WORDS = 3
-IH_SCALE = np.float32(2.0 ** -16)
-IH_CENTRE = 393210
+#: fp32 sqrt(3)/65536, bit pattern 0x37ddb3d7 (the GPU twin uses the same bits)
+IH_SCALE = np.uint32(0x37DDB3D7).view(np.float32)
+IH_CENTRE = 131070
 
 # tensor ids (one independent stream per id)
 TID_X = 1
@@ -76,17 +71,11 @@ def raw64(seed: int, tensor_id: int, start: int, count: int) -> np.ndarray:
 
 
 def normal_f32(seed: int, tensor_id: int, start: int, count: int, sigma: float) -> np.ndarray:
-    out = np.empty(count, dtype=np.float32)
+    r = raw64(seed, tensor_id, start, count)
     m = np.uint64(0xFFFF)
-    step = 1 << 22  # elements per chunk: bounds the uint64 temporaries
-    for c0 in range(0, count, step):
-        n = min(step, count - c0)
-        r = raw64(seed, tensor_id, IH_WORDS * (start + c0), IH_WORDS * n)
-        s = ((r & m) + ((r >> np.uint64(16)) & m) + ((r >> np.uint64(32)) & m) + (r >> np.uint64(48)))
-        s = s.reshape(n, IH_WORDS).sum(axis=1).astype(np.int64)
-        z = (s - IH_CENTRE).astype(np.float32) * IH_SCALE
-        out[c0:c0 + n] = (z * np.float32(sigma)).astype(np.float32)
-    return out
+    s = ((r & m) + ((r >> np.uint64(16)) & m) + ((r >> np.uint64(32)) & m) + (r >> np.uint64(48))).astype(np.int64)
+    z = (s - IH_CENTRE).astype(np.float32) * IH_SCALE
+    return (z * np.float32(sigma)).astype(np.float32)
 
 
 def bernoulli_mask(seed: int, tensor_id: int, start: int, count: int, p: float) -> np.ndarray:
@@ -231,7 +220,7 @@ def shared_w2_f32(wl: Workload) -> np.ndarray:
 
 def describe(wl: Workload) -> dict:
     d = dataclasses.asdict(wl)
-    d["generator"] = "SplitMix64 counter streams, Irwin-Hall(12x16-bit) unit normal"
+    d["generator"] = "SplitMix64 counter streams, Irwin-Hall(4x16-bit) unit normal"
     return d
 
 

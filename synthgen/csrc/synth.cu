@@ -6,8 +6,7 @@
 //   SplitMix64 (Steele, Lea and Flood, OOPSLA 2014) counter streams:
 //     key = mix64(seed * GOLDEN + tensor_id),
 //     word(i) = mix64(key + (i + 1) * GOLDEN)
-//   Irwin-Hall(12 x 16 bit) unit normal of element i from words 3i .. 3i + 2:
-//     z = f32(S - 393210) * 2^-16 (both steps exact)
+//   Irwin-Hall(4 x 16 bit) unit normal: z = f32(S - 131070) * f32(sqrt(3)/65536)
 //   value = f32(z * sigma). Optional Bernoulli(p) outlier mask from a second
 //   stream (high 32 bits < thr) multiplies by `mult`. bf16 output uses RNE.
 // This module holds no arithmetic of the MoE layer.
@@ -18,8 +17,8 @@
 namespace {
 
 constexpr uint64_t kGolden = 0x9E3779B97F4A7C15ull;
-constexpr float kIhScale = 1.52587890625e-05f;  // 2^-16
-constexpr int64_t kIhCentre = 393210;
+constexpr uint32_t kIhScaleBits = 0x37DDB3D7u;  // fp32 sqrt(3)/65536
+constexpr int64_t kIhCentre = 131070;
 
 __host__ __device__ __forceinline__ uint64_t mix64(uint64_t z) {
   z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
@@ -28,13 +27,10 @@ __host__ __device__ __forceinline__ uint64_t mix64(uint64_t z) {
 }
 
 __device__ __forceinline__ float unit_normal(uint64_t key, uint64_t i) {
-  int64_t s = 0;
-#pragma unroll
-  for (int w = 0; w < 3; ++w) {
-    const uint64_t r = mix64(key + (3 * i + w + 1) * kGolden);
-    s += (int64_t)(r & 0xFFFF) + (int64_t)((r >> 16) & 0xFFFF) + (int64_t)((r >> 32) & 0xFFFF) + (int64_t)(r >> 48);
-  }
-  return __fmul_rn(__int2float_rn((int)(s - kIhCentre)), kIhScale);
+  const uint64_t r = mix64(key + (i + 1) * kGolden);
+  const int64_t s = (int64_t)(r & 0xFFFF) + (int64_t)((r >> 16) & 0xFFFF) + (int64_t)((r >> 32) & 0xFFFF) +
+                    (int64_t)(r >> 48);
+  return __fmul_rn(__int2float_rn((int)(s - kIhCentre)), __uint_as_float(kIhScaleBits));
 }
 
 __global__ void normal_f32_kernel(uint64_t key, uint64_t start, uint64_t count, float sigma, float* out) {
