@@ -47,9 +47,10 @@ FALLBACK_HBM_GBS = 6800.0
 # with, so it is reported while their hash matches and as null otherwise.
 W1_TRAFFIC = {
     # workload name: (bytes per launch, sha256 of the GEMM sources)
-    "dsv4_flash_decode_T64": (1949501184 + 3749888, "82922fc62bf52307e5b8132cfa640783a76ade7c2f51e42f0d053666816d26bd"),
+    "dsv4_flash_decode_T64": (1949534720 + 3865856, "fbe49a716509c578b14c9b8e162adfbe2b91e75f29af2bfa2e6990fcbd3461f7"),
 }
-GEMM_SOURCES = ("block_scaled_fp4_top_gb300/csrc/gemm.cu", "block_scaled_fp4_top_gb300/csrc/common.cuh")
+GEMM_SOURCES = ("block_scaled_fp4_top_gb300/csrc/gemm.cu", "block_scaled_fp4_top_gb300/csrc/gemm_sched.cuh",
+                "block_scaled_fp4_top_gb300/csrc/common.cuh")
 
 
 def gemm_sources_sha() -> str:
