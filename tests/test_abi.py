@@ -170,3 +170,24 @@ def test_tp_shard_checks(lib):
     assert lib.fp4moe_shard_mxfp4(ctypes.byref(mx), 2, 4, 2048, 3, 1, p, None, p, p, None) == _lib.INVALID_ARG
     assert lib.fp4moe_shard_mxfp4(ctypes.byref(mx), 2, 4, 2048, 3, 1, p, p, ctypes.c_void_p(0x10008), p,
                                   None) == _lib.MISALIGNED
+
+
+def test_mxfp4_as_nvfp4_and_probe_checks(lib):
+    """Argument checks of the MXFP4-to-NVFP4 weight conversion and of the tensor-core probe; each fails before
+    any CUDA call."""
+    from block_scaled_fp4_top_gb300 import _lib
+    p = ctypes.c_void_p(0x10000)
+    nv = _cfg(inter=768, inter_logical=704)
+    mx = _cfg(w_format=_lib.W_MXFP4, inter=768, inter_logical=704)
+    assert lib.fp4moe_mxfp4_as_nvfp4(ctypes.byref(mx), 1, 4, p, p, p, p, p, p, None) == _lib.UNSUPPORTED
+    assert lib.fp4moe_mxfp4_as_nvfp4(ctypes.byref(nv), 3, 4, p, p, p, p, p, p, None) == _lib.INVALID_ARG
+    assert lib.fp4moe_mxfp4_as_nvfp4(ctypes.byref(nv), 1, 257, p, p, p, p, p, p, None) == _lib.INVALID_ARG
+    assert lib.fp4moe_mxfp4_as_nvfp4(ctypes.byref(nv), 1, 4, p, p, p, p, p, None, None) == _lib.INVALID_ARG
+    assert lib.fp4moe_mxfp4_as_nvfp4(ctypes.byref(nv), 2, 4, p, p, p, ctypes.c_void_p(0x10004), p, p,
+                                     None) == _lib.MISALIGNED
+    # NVFP4 TP shards: the logical width is whole 16-element scale blocks inside the kernel width
+    assert lib.moe_route(ctypes.byref(_cfg(inter=768, inter_logical=700)), 8, *([p] * 13)) == _lib.UNSUPPORTED
+    assert lib.moe_route(ctypes.byref(_cfg(inter=768, inter_logical=800)), 8, *([p] * 13)) == _lib.UNSUPPORTED
+    assert lib.fp4moe_tensor_peak_probe(64, 10, p, None) == _lib.INVALID_ARG
+    assert lib.fp4moe_tensor_peak_probe(128, 0, p, None) == _lib.INVALID_ARG
+    assert lib.fp4moe_tensor_peak_probe(256, 10, None, None) == _lib.INVALID_ARG
