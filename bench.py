@@ -561,6 +561,67 @@ def run_prefill(args, dev, fp4_peak_tflops):
     }
 
 
+def run_side_workload(args, wl, dev):
+    """A second workload measured in the same run, the way the decode line is (run_ours), cut to its figures."""
+    import copy
+    sub = copy.copy(args)
+    sub.steps, sub.warmup = args.side_steps, max(3, min(args.warmup, 10))
+    r = run_ours(sub, wl, 0, 1)
+    keep = ("us_per_layer", "value", "layer_hbm_gbs", "layer_algorithmic_bytes", "n_active_experts", "stages_us",
+            "dtype", "clocks")
+    out = {"workload": wl.name, "T": wl.T, "steps": sub.steps, **{k: r[k] for k in keep}}
+    out["tokens_per_s"] = out.pop("value")
+    out["w1"] = {k: r["roofline"][k] for k in ("kernel", "achieved", "peak", "frac", "algorithmic_bytes_per_launch")}
+    out["e2e_tokens_per_s"] = r["e2e"]["value"]
+    return out
+
+
+def run_graph_sweep(args, dev):
+    """Config-5 style batch sweep: the decode-shape layer captured in one CUDA graph per T over fixed-capacity
+    buffers; each replay is timed alone (CUDA events around the replay) after a write of 256 MB that flushes
+    L2, so even the smallest batches stream their experts' weights from HBM."""
+    import torch
+    from synthgen import gpu as sgpu
+    wl = sg.DSV4_DECODE
+    Ts = (1, 8, 64, 512, 4096)
+    cfg, layer = setup_layer(wl, max(Ts))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    hbm, _ = peaks()
+    res = []
+    for T in Ts:
+        x = sgpu.activations(wl, sg.EVAL_SEED, T=T)
+        y = torch.empty(T, wl.H, dtype=torch.bfloat16, device=dev)
+        ids = torch.empty(T * wl.k, dtype=torch.int32, device=dev)
+        layer.forward(x, y, ids)   # eager first: load-time set-up of the launch path happens outside the capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            layer.forward(x, y, ids)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        n_active = int(np.unique(ids.cpu().numpy()).size)
+        tot = 0.0
+        for _ in range(args.side_steps):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            tot += e0.elapsed_time(e1)
+        us = tot * 1e3 / args.side_steps
+        nbytes = n_active * (2 * wl.I * wl.H * 9 // 16 + wl.H * wl.I * 9 // 16) + wl.E * wl.H * 2 + 2 * T * wl.H * 2
+        res.append({"T": T, "us_per_replay": us, "tokens_per_s": T / (us * 1e-6), "n_active_experts": n_active,
+                    "algorithmic_bytes": nbytes, "hbm_frac": nbytes / (us * 1e-6) / 1e9 / hbm})
+        del g
+    if layer.read_error() != 0:
+        raise RuntimeError("graph sweep: device error word set")
+    return {"workload": "dsv4_flash_decode graph replay per T", "replays_per_T": args.side_steps,
+            "l2": "256 MB written before every replay (L2 flushed); events around the replay only", "by_T": res}
+
+
 class OracleSample:
     """The oracle, as it stands, on the first n_tokens of the evaluation batch.
 
@@ -688,6 +749,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the FP4 peak probe and the Zipf prefill measurement that follow the decode run")
     ap.add_argument("--prefill-steps", type=int, default=50)
+    ap.add_argument("--side-steps", type=int, default=30,
+                    help="steps of the TP3 MXFP4 workloads and replays per T of the graph sweep in the default run")
     ap.add_argument("--oracle-only", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--experts", type=int, default=0,
                     help="override E (smaller case for profiler captures; the default is the workload's E)")
@@ -748,6 +811,11 @@ def main():
         out["fp4_dense_peak"] = peak
         torch.cuda.empty_cache()
         out["prefill"] = run_prefill(args, dev, peak["tflops"])
+        torch.cuda.empty_cache()
+        # config 4 (the TP3 MXFP4 shard): the bf16-activation path and the NVFP4-operand variant
+        out["tp3_mxfp4"] = [run_side_workload(args, w, dev) for w in (sg.TP3_MXFP4, sg.TP3_MXFP4_NVACT)]
+        torch.cuda.empty_cache()
+        out["graph_sweep"] = run_graph_sweep(args, dev)
         torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu_baseline:
         cores, model = cpu_info()
