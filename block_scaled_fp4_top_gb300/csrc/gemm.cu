@@ -100,6 +100,7 @@ constexpr uint32_t SFB_STAGE_COLS = 4 * ATOMS;  // B scales of one ring stage
 // else 1.
 static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
 static_assert(SMEM_BYTES + 8 * kMaxExperts + 128 <= 232448, "shared memory budget (dynamic + static)");
+constexpr int kWidePairsPerExpert = 8;  // static schedule: the 128 x 256 kernel from this average on
 constexpr int kMaxResidentK = (TMEM_COLS - ACC_COLS - SFB_STAGE_COLS * STAGES) * 16;  // 4608 with one accumulator
 
 using Params = GemmParams;
@@ -116,9 +117,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   __shared__ int s_cstart[kMaxExperts + 1];  // dynamic schedule: first chunk of every expert
   __shared__ int s_sched[kSchedSlots];
 
-  pdl_wait();  // the routing / quantisation results of the previous launch are needed from here on
-  pdl_trigger();
-  if (*(volatile uint32_t*)prm.err & kAbortMask) return;  // an earlier timeout poisons the call
+  // Static schedule: the routing layout is final before this grid starts (each kernel of the chain waits on
+  // its predecessor before it lets its successor start), so the set-up below (tile range, TMEM, barriers)
+  // overlaps the previous kernel, and the wait comes after it. The dynamic schedule's counter is zeroed just
+  // before the launch, so that launch cannot overlap anything and waits first.
+  const bool early = !prm.dyn;
+  if (!early) {
+    pdl_wait();  // the routing / quantisation results of the previous launch are needed from here on
+    pdl_trigger();
+    if (*(volatile uint32_t*)prm.err & kAbortMask) return;  // an earlier timeout poisons the call
+  }
   const int E = prm.E, NT = prm.NT;
   const int R = min(__ldcg(prm.poff + E - 1), prm.cap);
   const int r128 = R / BM;
@@ -193,6 +201,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int nacc = prm.nacc;
   const uint32_t res_col = ACC_COLS * nacc;
   const uint32_t str_col = res_col + 4u * katoms_total;
+  if (early) {
+    pdl_wait();  // the activations and every other result of the previous launch are needed from here on
+    pdl_trigger();
+    if (*(volatile uint32_t*)prm.err & kAbortMask) tau1 = tau0;  // an earlier timeout: no role takes a tile
+  }
 
   if (warp == 4 && lane == 0) {
     // ------------------------------------------------------------ producer
@@ -563,9 +576,11 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
   for (int b = 0; b < 4; ++b)
     if (!encode_u8_sw128(&tmA.box[b], a_codes, (uint64_t)prm.K / 2, (uint64_t)prm.cap, 16u << b))
       return FP4MOE_CUDA_ERROR;
-  // prefill sizes: 128 x 256 tiles (gemm_wide.cu), which move fewer shared-memory bytes and issue fewer MMAs
-  // per MAC
-  if (prm.dyn && gemm_wide_fits(prm.K, prm.b_rows)) return gemm_wide_launch(mode, prm, tmA, st);
+  // 128 x 256 tiles (gemm_wide.cu) move fewer shared-memory bytes and issue fewer MMAs per MAC. They pay from
+  // about eight pairs per expert on average: on the DeepSeek-V4-Flash shape (256 experts, top-6), equal at 256
+  // tokens and 3-5 % faster per layer from 512 tokens up; below that the 128 x 128 tiles balance better.
+  const bool wide = prm.dyn || (int64_t)T * cfg.top_k >= kWidePairsPerExpert * (int64_t)prm.E;
+  if (wide && gemm_wide_fits(prm.K, prm.b_rows)) return gemm_wide_launch(mode, prm, tmA, st);
   const int nsm = sm_count();
   if (nsm <= 0) return FP4MOE_CUDA_ERROR;
   const int max_tiles = (prm.cap / BM) * prm.NT;

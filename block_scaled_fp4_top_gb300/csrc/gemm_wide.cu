@@ -75,9 +75,13 @@ __global__ void __launch_bounds__(WTHREADS, 1)
   __shared__ int s_cstart[kMaxExperts + 1];  // dynamic schedule: first chunk of every expert
   __shared__ int s_sched[kSchedSlots];
 
-  pdl_wait();  // the routing / quantisation results of the previous launch are needed from here on
-  pdl_trigger();
-  if (*(volatile uint32_t*)prm.err & kAbortMask) return;  // an earlier timeout poisons the call
+  // As in the 128 x 128 kernel: with the static schedule the set-up overlaps the previous kernel.
+  const bool early = !prm.dyn;
+  if (!early) {
+    pdl_wait();  // the routing / quantisation results of the previous launch are needed from here on
+    pdl_trigger();
+    if (*(volatile uint32_t*)prm.err & kAbortMask) return;  // an earlier timeout poisons the call
+  }
   const int E = prm.E, NT = prm.NT;  // NT: 256-row weight tiles
   const int R = min(__ldcg(prm.poff + E - 1), prm.cap);
   const int r128 = R / WBM;
@@ -147,6 +151,11 @@ __global__ void __launch_bounds__(WTHREADS, 1)
   const int KB = prm.KB;  // ring stages per tile: K / 256
   const int katoms_total = prm.K / 64;
   const int NT128 = 2 * NT;  // 128-row weight tiles of one expert
+  if (early) {
+    pdl_wait();  // the activations and every other result of the previous launch are needed from here on
+    pdl_trigger();
+    if (*(volatile uint32_t*)prm.err & kAbortMask) tau1 = tau0;  // an earlier timeout: no role takes a tile
+  }
 
   if (warp == WPRODUCER && lane == 0) {
     // ------------------------------------------------------------ producer

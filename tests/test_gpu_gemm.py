@@ -6,8 +6,10 @@ m-tiles, and K is partial (a stage of 2 atoms) or runs over several stages.
 * W2: every real pair's bf16 row is compared with an fp64 matmul of the
   decoded operands (fp32 accumulation bound plus half a bf16 ulp).
 * Cases with T >= E * 128 run the dynamic chunk schedule (prefill sizes),
-  the others the static contiguous one (decode sizes). With K a multiple of
-  256 the dynamic cases run the 128 x 256 tile kernel (gemm_wide.cu).
+  the others the static contiguous one (decode sizes). With K and the
+  weight rows multiples of 256, the dynamic cases and the static ones with
+  at least 8 pairs per expert run the 128 x 256 tile kernel (gemm_wide.cu);
+  the sparse 16-expert cases keep the 128 x 128 one at every K.
 * W1: the clamped SwiGLU + requantisation epilogue is compared with the
   oracle's quantiser applied to the fp64 reference h. Codes must agree
   except at rounding ties that the fp32 accumulation moves.
@@ -25,6 +27,10 @@ from helpers import bf16_ulp, dump, ensure_built, tile_weights
 from oracle import codecs, layout, moe, nvfp4
 
 pytestmark = pytest.mark.gpu
+
+
+# 16 experts, 26 pairs: fewer than 8 per expert, so the static schedule keeps its 128 x 128 kernel
+SPARSE16 = [1, 0, 3, 0, 2, 5, 0, 1, 2, 0, 0, 4, 1, 0, 5, 2]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -100,6 +106,8 @@ def _setup(H, I, counts, seed, which, full_range=False, alpha_mult=1.0):
     (256, 768, [3, 0, 140], True),              # every finite E4M3 scale byte, static schedule
     (256, 768, [600, 5, 130], True),            # every finite E4M3 scale byte, dynamic schedule
     (512, 256, [600, 5, 130], False),           # dynamic schedule, two 256-row weight tiles of the wide kernel
+    (256, 768, SPARSE16, False),                # under 8 pairs per expert: static, 128 x 128 tiles, K = 768
+    (512, 256, SPARSE16, True),                 # the same, every finite E4M3 scale byte
 ])
 def test_w2_rows_against_fp64(H, I, counts, full_range):
     import torch
@@ -181,7 +189,9 @@ def _run_w1(cfg, T, cap, I, t, gs2, alpha=None):
 @pytest.mark.parametrize("H,I,counts,full_range", [(256, 128, [3, 0, 140], False), (512, 256, [1, 257, 2], False),
                                                    (256, 128, [600, 5, 130], False),  # the dynamic schedule
                                                    (256, 256, [3, 0, 140], True),     # every finite E4M3 scale byte
-                                                   (256, 256, [600, 5, 130], True)])
+                                                   (256, 256, [600, 5, 130], True),
+                                                   (256, 256, SPARSE16, False),       # static, 128 x 128 tiles
+                                                   (512, 256, SPARSE16, True)])
 def test_w1_swiglu_requant(H, I, counts, full_range):
     from block_scaled_fp4_top_gb300 import api
     cfg, T, cap, ids, L, (qa, sa, qw, sw, alpha), t = _setup(H, I, counts, 2, which=1, full_range=full_range)
@@ -206,7 +216,13 @@ def test_w1_swiglu_requant(H, I, counts, full_range):
     assert (sf[real] == s_ref[real]).mean() >= 0.99
 
 
-@pytest.mark.parametrize("counts", [[3, 0, 140, 1], [600, 5, 130, 1]])  # static; dynamic (128 x 256 tiles)
+# 32 experts, 178 pairs (fewer than 8 per expert): the static schedule on its 128 x 128 kernel, with enough rows for
+# a thousand doubly clamped elements
+SPARSE32 = [9, 0, 7, 12, 0, 8, 5, 0, 11, 6, 0, 9, 7, 0, 10, 4, 8, 0, 6, 13, 0, 7, 9, 0, 5, 8, 0, 12, 6, 0, 9, 7]
+
+
+# static and dynamic schedules on 128 x 256 tiles, and the static one on 128 x 128 tiles
+@pytest.mark.parametrize("counts", [[3, 0, 140, 1], [600, 5, 130, 1], SPARSE32])
 def test_w1_swiglu_clamp_past_the_limit(counts):
     """Gate and up driven to an RMS of about 46 (alpha x 8): a large share of both is clamped. Where gate and up are
     both past the limit, h is +-silu(10) * 10 exactly and the codes must equal the oracle's; elsewhere they agree
