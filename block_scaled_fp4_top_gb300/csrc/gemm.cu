@@ -117,22 +117,20 @@ __global__ void __launch_bounds__(THREADS, 1)
   __shared__ int s_cstart[kMaxExperts + 1];  // dynamic schedule: first chunk of every expert
   __shared__ int s_sched[kSchedSlots];
 
-  // Static schedule: the routing layout is final before this grid starts (each kernel of the chain waits on
-  // its predecessor before it lets its successor start), so the set-up below (tile range, TMEM, barriers)
-  // overlaps the previous kernel, and the wait comes after it. The dynamic schedule's counter is zeroed just
-  // before the launch, so that launch cannot overlap anything and waits first.
-  const bool early = !prm.dyn;
-  if (!early) {
-    pdl_wait();  // the routing / quantisation results of the previous launch are needed from here on
-    pdl_trigger();
-    if (*(volatile uint32_t*)prm.err & kAbortMask) return;  // an earlier timeout poisons the call
-  }
+  __shared__ int s_abort;
+
+  // The routing layout is final before this grid starts (each kernel of the chain waits on its predecessor
+  // before it lets its successor start), so the set-up below (tile ranges, TMEM, barriers, the chunk table)
+  // overlaps the previous kernel, and the wait for it comes after. The counter (dynamic schedule, or the
+  // static schedule's pool) is zero by then: cleared by the quantise-scatter two kernels back, or by a
+  // memset right before the launch, which this launch cannot overlap.
   const int E = prm.E, NT = prm.NT;
   const int R = min(__ldcg(prm.poff + E - 1), prm.cap);
   const int r128 = R / BM;
+  const int pool = (!prm.dyn && prm.steal) ? tail_pool(r128 * NT, (int)gridDim.x) : 0;
   int tau0, tau1;
-  cta_range(r128 * NT, tau0, tau1);
-  if (tau0 >= tau1) return;
+  cta_range(r128 * NT - pool, tau0, tau1);
+  if (tau0 >= tau1 && pool == 0) return;  // (with a pool every CTA has at least three tiles of its own)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -194,17 +192,20 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const int n_chunks = prm.dyn ? s_cstart[E] : 0;
+  int n_chunks = prm.dyn ? s_cstart[E] : pool;
 
   const int KB = prm.KB;
   const int katoms_total = prm.K / 64;
   const int nacc = prm.nacc;
   const uint32_t res_col = ACC_COLS * nacc;
   const uint32_t str_col = res_col + 4u * katoms_total;
-  if (early) {
-    pdl_wait();  // the activations and every other result of the previous launch are needed from here on
-    pdl_trigger();
-    if (*(volatile uint32_t*)prm.err & kAbortMask) tau1 = tau0;  // an earlier timeout: no role takes a tile
+  pdl_wait();  // the activations and every other result of the previous launch are needed from here on
+  pdl_trigger();
+  if (threadIdx.x == 0) s_abort = (*(volatile uint32_t*)prm.err & kAbortMask) != 0;
+  __syncthreads();
+  if (s_abort) {  // an earlier timeout poisons the call: no role takes a tile
+    tau1 = tau0;
+    n_chunks = 0;
   }
 
   if (warp == 4 && lane == 0) {
@@ -534,7 +535,7 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
                           const uint8_t* a_sf, const int32_t* poff, const int32_t* pair_of_row,
                           const uint8_t* b_codes, const uint8_t* b_sf, const float* alpha, const float* gs2,
                           uint8_t* out_codes, uint8_t* out_sf, float* amax, uint32_t* status, uint16_t* o_pairs,
-                          uint32_t* err, int* sched, cudaStream_t st) {
+                          uint32_t* err, int* sched, bool sched_zeroed, cudaStream_t st) {
   if (T == 0) return FP4MOE_OK;
   if (mode != kW2Rows && amax == nullptr) return FP4MOE_INVALID_ARG;
   if (mode == kW1SwiGLU && status == nullptr) return FP4MOE_INVALID_ARG;
@@ -569,8 +570,10 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
   prm.err = err;
   // the dynamic chunk schedule pays off once experts average a whole m-tile (prefill sizes)
   prm.dyn = ((int64_t)T * cfg.top_k >= (int64_t)local_experts(cfg) * BM) ? 1 : 0;
+  if (prm.dyn && sched == nullptr) return FP4MOE_INVALID_ARG;
+  prm.steal = (!prm.dyn && sched != nullptr) ? 1 : 0;
   prm.sched = sched;
-  if (prm.dyn && (sched == nullptr || cudaMemsetAsync(sched, 0, sizeof(int), st) != cudaSuccess))
+  if (sched != nullptr && !sched_zeroed && cudaMemsetAsync(sched, 0, sizeof(int), st) != cudaSuccess)
     return FP4MOE_CUDA_ERROR;
   AMaps tmA;
   for (int b = 0; b < 4; ++b)

@@ -28,7 +28,8 @@ struct GemmParams {
   uint32_t* err;
   int o_pairs32;  // W2: o_pairs is 32-byte aligned (every 128-column piece of a row is then)
   int dyn;     // 1: dynamic chunk schedule (large T); 0: contiguous static ranges (decode sizes)
-  int* sched;  // dynamic schedule: next-chunk counter, zero at launch
+  int steal;   // static schedule: the last tiles form a pool that CTAs take from `sched` once their range is done
+  int* sched;  // dynamic schedule, or the static schedule's pool: next-chunk counter, zero at launch
 };
 
 // Tensor maps of the activation codes whose boxes are 16, 32, 64 and 128 rows
@@ -52,6 +53,15 @@ namespace {
 // activation and weight tiles in L2, and the load balances itself.
 constexpr int kChunk = 4;
 constexpr int kSchedSlots = 4;  // chunk ids handed from the producer to the MMA issuer and the epilogue
+constexpr int kPoolPerCta = 3;  // static schedule: pool tiles per CTA
+
+// Static schedule with a pool: of the N tiles, the last ones (about three per CTA, at most a quarter) are not
+// assigned. A CTA that has finished its contiguous range takes them one at a time from the counter, in tile
+// order, so CTAs that stream slower than others (their place on the chip, the expert boundaries in their
+// range) no longer hold up the whole launch. Fewer than four tiles per CTA: no pool.
+__device__ __forceinline__ int tail_pool(int N, int G) {
+  return N >= 4 * G ? min(kPoolPerCta * G, N / 4) : 0;
+}
 
 __device__ __forceinline__ int expert_chunks(int me, int NT) {
   return me == 0 ? 0 : (me == 1 ? (NT + kChunk - 1) / kChunk : ((me + kChunk - 1) / kChunk) * NT);
@@ -96,10 +106,27 @@ __device__ __forceinline__ Chunk decode_chunk(int c, const int* s_cstart, const 
   return k;
 }
 
+// Pool tile i of the static schedule (tile tau of the order) as a one-tile chunk.
+__device__ __forceinline__ Chunk pool_tile(int tau, const int* poff, int E, int NT, int r128) {
+  TileCursor c;
+  c.seek(tau, poff, E, NT, r128);
+  Chunk k;
+  k.e = c.e;
+  k.pm0 = c.pm0;
+  k.me = c.me;
+  k.n0 = c.nt;
+  k.m0 = c.pm0 + c.ml;
+  k.count = 1;
+  k.along_n = true;
+  return k;
+}
+
 // The tiles of one CTA, in order, as each role sees them: its contiguous share [tau0, tau1) of the tile
-// order (static schedule), or the chunks it takes from the global counter (dynamic schedule). In the dynamic
-// schedule the producer takes a chunk and hands its id to the MMA issuer and the epilogue warps through a
-// small shared-memory ring; every role then walks the same tiles in the same order.
+// order (static schedule), then, with a pool, the pool tiles it takes from the counter; or the chunks it
+// takes from the global counter (dynamic schedule). Whatever comes from the counter, the producer takes and
+// hands its id to the MMA issuer, the scale copiers and the epilogue warps through a small shared-memory
+// ring; every role then walks the same tiles in the same order. n_chunks counts the chunks (dynamic) or the
+// pool tiles (static), which are the last n_chunks of the r128 * NT tiles.
 enum SourceRole { kRoleProducer = 0, kRoleMma = 1, kRoleEpilogue = 2, kRoleCopier = 3 };
 
 template <int ROLE>
@@ -133,11 +160,13 @@ struct TileSource {
                                        int* s_sched, uint32_t bar_sfull, uint32_t bar_sempty, int n_chunks, int E,
                                        int NT, int r128) {
     if (!dyn) {
-      if (tau >= tau1) return false;
-      if (tau > tau0) cur.step(poff, E, NT, r128);
-      ++tau;
-      t = cur.tile();
-      return true;
+      if (tau < tau1) {
+        if (tau > tau0) cur.step(poff, E, NT, r128);
+        ++tau;
+        t = cur.tile();
+        return true;
+      }
+      if (n_chunks <= 0) return false;  // no pool
     }
     while (ci >= ck.count) {
       if (done) return false;
@@ -176,7 +205,7 @@ struct TileSource {
         done = true;
         return false;
       }
-      ck = decode_chunk(c, cstart, poff, E, NT, r128);
+      ck = dyn ? decode_chunk(c, cstart, poff, E, NT, r128) : pool_tile(r128 * NT - n_chunks + c, poff, E, NT, r128);
       ci = 0;
     }
     t = ck.tile(ci++);

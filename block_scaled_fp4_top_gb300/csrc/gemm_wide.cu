@@ -75,19 +75,16 @@ __global__ void __launch_bounds__(WTHREADS, 1)
   __shared__ int s_cstart[kMaxExperts + 1];  // dynamic schedule: first chunk of every expert
   __shared__ int s_sched[kSchedSlots];
 
-  // As in the 128 x 128 kernel: with the static schedule the set-up overlaps the previous kernel.
-  const bool early = !prm.dyn;
-  if (!early) {
-    pdl_wait();  // the routing / quantisation results of the previous launch are needed from here on
-    pdl_trigger();
-    if (*(volatile uint32_t*)prm.err & kAbortMask) return;  // an earlier timeout poisons the call
-  }
+  __shared__ int s_abort;
+
+  // As in the 128 x 128 kernel: the set-up overlaps the previous kernel, and the counter is zero by the wait.
   const int E = prm.E, NT = prm.NT;  // NT: 256-row weight tiles
   const int R = min(__ldcg(prm.poff + E - 1), prm.cap);
   const int r128 = R / WBM;
+  const int pool = (!prm.dyn && prm.steal) ? tail_pool(r128 * NT, (int)gridDim.x) : 0;
   int tau0, tau1;
-  cta_range(r128 * NT, tau0, tau1);
-  if (tau0 >= tau1) return;
+  cta_range(r128 * NT - pool, tau0, tau1);
+  if (tau0 >= tau1 && pool == 0) return;  // (with a pool every CTA has at least three tiles of its own)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -147,14 +144,17 @@ __global__ void __launch_bounds__(WTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const int n_chunks = prm.dyn ? s_cstart[E] : 0;
+  int n_chunks = prm.dyn ? s_cstart[E] : pool;
   const int KB = prm.KB;  // ring stages per tile: K / 256
   const int katoms_total = prm.K / 64;
   const int NT128 = 2 * NT;  // 128-row weight tiles of one expert
-  if (early) {
-    pdl_wait();  // the activations and every other result of the previous launch are needed from here on
-    pdl_trigger();
-    if (*(volatile uint32_t*)prm.err & kAbortMask) tau1 = tau0;  // an earlier timeout: no role takes a tile
+  pdl_wait();  // the activations and every other result of the previous launch are needed from here on
+  pdl_trigger();
+  if (threadIdx.x == 0) s_abort = (*(volatile uint32_t*)prm.err & kAbortMask) != 0;
+  __syncthreads();
+  if (s_abort) {  // an earlier timeout poisons the call: no role takes a tile
+    tau1 = tau0;
+    n_chunks = 0;
   }
 
   if (warp == WPRODUCER && lane == 0) {
