@@ -5,7 +5,9 @@ Default workload: DeepSeek-V4-Flash decode, T=64 tokens, H=4096, I=2048,
 E=256, top-k 6, swiglu_limit 10. Weights are NVFP4, quantised from seeded
 synthetic N(0, 0.02) values. Activations are seeded, with 1% outliers x20.
 A step is one pass of the whole layer: route, quantise+scatter,
-W1+SwiGLU+requant, W2, combine. Workloads with a shared expert
+W1+SwiGLU+requant, W2, combine, issued by one moe_forward call. The
+per-stage split comes from a second pass that makes the four stage calls
+separately, with CUDA events between them. Workloads with a shared expert
 (dsv4_flash_decode_shared_T64) also run its three block-FP8 kernels on a side
 stream beside the routed path (as moe_forward_shared does), and the combine
 adds its output.
@@ -319,19 +321,21 @@ def run_ours(args, wl, rank, world):
 
     for _ in range(args.warmup):
         step()
+        layer.forward(x, y)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    # the timed region: the steps back to back, events only at its two ends, so each kernel's prologue
-    # still overlaps its predecessor's tail (programmatic dependent launch)
+    # the timed region: moe_forward (one C-ABI call per step, the layer as a caller runs it) back to back,
+    # events only at its two ends, so each kernel's prologue still overlaps its predecessor's tail
+    # (programmatic dependent launch)
     with ClockSampler(dev.index) as clk:
         time.sleep(0.3)  # let the sampler start before the timed region
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         for i in range(args.steps):
-            step()
+            layer.forward(x, y)
         t1.record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -496,8 +500,9 @@ def fp4_dense_peak(dev):
 
 
 def run_prefill(args, dev, fp4_peak_tflops):
-    """The Zipf-routed prefill workload (T = 8192, DSV4 shapes): the same four calls as the decode step, timed
-    the same way, with the layer's HBM fraction and the GEMMs' tensor-pipe share of the measured FP4 peak."""
+    """The Zipf-routed prefill workload (T = 8192, DSV4 shapes), timed like the decode step (moe_forward back to
+    back, then the four stage calls with events between them for the split), with the layer's HBM fraction and
+    the GEMMs' tensor-pipe share of the measured FP4 peak."""
     import torch
     from synthgen import gpu as sgpu
     wl = sg.DSV4_PREFILL_ZIPF
@@ -510,13 +515,14 @@ def run_prefill(args, dev, fp4_peak_tflops):
     stream = torch.cuda.current_stream()
     for _ in range(max(args.warmup, 3)):
         step()
+        layer.forward(x, y)
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
         time.sleep(0.3)
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         for _ in range(steps):
-            step()
+            layer.forward(x, y)
         t1.record(stream)
         torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / steps

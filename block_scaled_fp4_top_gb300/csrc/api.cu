@@ -254,16 +254,14 @@ fp4moe_status forward_impl(const fp4moe_config* cfg, int32_t T, const uint16_t* 
       FP4_TRY(mx_gemm_launch(false, *cfg, T, a1, poff, por, w1_fp4, w1_sf, a2, nullptr, err, st));
       return mx_gemm_launch(true, *cfg, T, a2, poff, por, w2_fp4, w2_sf, nullptr, at<uint16_t>(ws, L.opairs), err, st);
     }
-    // the quantise-scatter also zeroes both GEMMs' schedule counters, so no memset splits the launch chain
-    static_assert(kWsSchedW2 == kWsSchedW1 + 4, "the two schedule counters are adjacent");
     FP4_TRY(quant_scatter_launch(*cfg, T, x, gs1, at<int32_t>(ws, L.slot), at<uint8_t>(ws, L.a1),
-                                 at<uint8_t>(ws, L.a1sf), scale_flags(ws), err, at<int32_t>(ws, kWsSchedW1), st));
+                                 at<uint8_t>(ws, L.a1sf), scale_flags(ws), err, st));
     FP4_TRY(gemm_launch(kW1SwiGLU, *cfg, T, at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf), poff, por, w1_fp4, w1_sf,
                         alpha1, gs2, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), amax_h_run(ws), scale_flags(ws),
-                        nullptr, err, at<int>(ws, kWsSchedW1), true, st));
+                        nullptr, err, at<int>(ws, kWsSchedW1), st));
     return gemm_launch(kW2Rows, *cfg, T, at<uint8_t>(ws, L.a2), at<uint8_t>(ws, L.a2sf), poff, por, w2_fp4, w2_sf,
                        alpha2, nullptr, nullptr, nullptr, nullptr, nullptr, at<uint16_t>(ws, L.opairs), err,
-                       at<int>(ws, kWsSchedW2), true, st);
+                       at<int>(ws, kWsSchedW2), st);
   };
   const fp4moe_status rr = routed();
   // the join is waited on every path, so a stream capture never ends with the side branch open
@@ -381,7 +379,7 @@ fp4moe_status moe_quantize_scatter(const fp4moe_config* cfg, int32_t T, const ui
   }
   FP4_TRY(check_ptrs(x, gs1, slot_of_pair, a1_fp4, a1_sf, ws));
   return quant_scatter_launch(*cfg, T, x, gs1, slot_of_pair, a1_fp4, a1_sf, scale_flags(ws), err_word(ws),
-                              nullptr, (cudaStream_t)stream);
+                              (cudaStream_t)stream);
 }
 
 fp4moe_status moe_grouped_gemm_w1_swiglu(const fp4moe_config* cfg, int32_t T, const uint8_t* a1_fp4,
@@ -400,7 +398,7 @@ fp4moe_status moe_grouped_gemm_w1_swiglu(const fp4moe_config* cfg, int32_t T, co
   FP4_TRY(check_ptrs(a1_fp4, a1_sf, padded_offsets, pair_of_row, w1_fp4, w1_sf, alpha1, gs2, a2_fp4, a2_sf, ws));
   return gemm_launch(kW1SwiGLU, *cfg, T, a1_fp4, a1_sf, padded_offsets, pair_of_row, w1_fp4, w1_sf, alpha1, gs2,
                      a2_fp4, a2_sf, amax_h_run(ws), scale_flags(ws), nullptr, err_word(ws), at<int>(ws, kWsSchedW1),
-                     false, (cudaStream_t)stream);
+                     (cudaStream_t)stream);
 }
 
 fp4moe_status moe_grouped_gemm_w2(const fp4moe_config* cfg, int32_t T, const uint8_t* a2_fp4, const uint8_t* a2_sf,
@@ -417,7 +415,7 @@ fp4moe_status moe_grouped_gemm_w2(const fp4moe_config* cfg, int32_t T, const uin
   FP4_TRY(check_ptrs(a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, o_pairs, ws));
   return gemm_launch(kW2Rows, *cfg, T, a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, nullptr,
                      nullptr, nullptr, nullptr, nullptr, o_pairs, err_word(ws), at<int>(ws, kWsSchedW2),
-                     false, (cudaStream_t)stream);
+                     (cudaStream_t)stream);
 }
 
 fp4moe_status moe_combine(const fp4moe_config* cfg, int32_t T, const uint16_t* o_pairs, const float* topk_w,
@@ -448,7 +446,7 @@ fp4moe_status moe_grouped_gemm_w2_combine(const fp4moe_config* cfg, int32_t T, c
   FP4_TRY(check_ptrs(a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, topk_w, y, ws));
   FP4_TRY(gemm_launch(kW2Rows, *cfg, T, a2_fp4, a2_sf, padded_offsets, pair_of_row, w2_fp4, w2_sf, alpha2, nullptr,
                       nullptr, nullptr, nullptr, nullptr, o, err_word(ws), at<int>(ws, kWsSchedW2),
-                      false, (cudaStream_t)stream));
+                      (cudaStream_t)stream));
   return combine_launch(*cfg, T, o, topk_w, nullptr, nullptr, y, (cudaStream_t)stream);
 }
 
@@ -621,13 +619,12 @@ fp4moe_status fp4moe_calibrate(const fp4moe_config* cfg, int32_t T, const uint16
                        at<int32_t>(ws, L.slot), por, at<int32_t>(ws, L.hist), at<float>(ws, L.nw2),
                        at<float>(ws, L.rt_part), router_partial_bytes(*cfg), err, st));
   FP4_TRY(quant_scatter_launch(*cfg, T, x_warm, gs1_out, at<int32_t>(ws, L.slot), at<uint8_t>(ws, L.a1),
-                               at<uint8_t>(ws, L.a1sf), scale_flags(ws), err, nullptr, st));
+                               at<uint8_t>(ws, L.a1sf), scale_flags(ws), err, st));
   float* alpha = at<float>(ws, L.alpha_tmp);
   FP4_TRY(make_alpha_launch(local_experts(*cfg), gs1_out, gw1, alpha, st));
   if (cudaMemsetAsync(amax_h, 0, 4, st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
   FP4_TRY(gemm_launch(kW1Amax, *cfg, T, at<uint8_t>(ws, L.a1), at<uint8_t>(ws, L.a1sf), poff, por, w1_fp4, w1_sf,
-                      alpha, nullptr, nullptr, nullptr, amax_h, nullptr, nullptr, err, at<int>(ws, kWsSchedW1), false,
-                      st));
+                      alpha, nullptr, nullptr, nullptr, amax_h, nullptr, nullptr, err, at<int>(ws, kWsSchedW1), st));
   if (cudaMemcpyAsync(gs2_out, amax_h, 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess) return FP4MOE_CUDA_ERROR;
   return gs_from_amax_launch(1, gs2_out, st);
 }

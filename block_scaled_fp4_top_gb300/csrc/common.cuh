@@ -29,8 +29,10 @@ constexpr uint32_t kAbortMask = FP4MOE_ERR_TIMEOUT;
 constexpr size_t kWsErr = 0;        // uint32 error word
 constexpr size_t kWsAmaxH = 16;     // float, calibration scratch (amax of h)
 constexpr size_t kWsAmaxX = 20;     // float, calibration scratch (amax of x)
-constexpr size_t kWsSchedW1 = 32;   // int, schedule counter of the W1 GEMM (dynamic chunks or static pool)
-constexpr size_t kWsSchedW2 = 36;   // int, schedule counter of the W2 GEMM (dynamic chunks or static pool)
+// int pairs {chunks taken, CTAs finished} of the W1 and W2 GEMMs' schedules (dynamic chunks or the static
+// pool): zero between launches, the last CTA of each launch zeroes its pair
+constexpr size_t kWsSchedW1 = 64;
+constexpr size_t kWsSchedW2 = 72;
 constexpr size_t kWsBatchAmax = 40; // uint, batch amax accumulator of fp4moe_batch_gs1 (zero between calls)
 constexpr size_t kWsBatchDone = 44; // uint, its CTA arrival counter (zero between calls)
 constexpr size_t kWsScaleFlags = 48;  // uint, sticky FP4MOE_SAT_* bits (fp4moe_read_scale_status)

@@ -121,16 +121,18 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   // The routing layout is final before this grid starts (each kernel of the chain waits on its predecessor
   // before it lets its successor start), so the set-up below (tile ranges, TMEM, barriers, the chunk table)
-  // overlaps the previous kernel, and the wait for it comes after. The counter (dynamic schedule, or the
-  // static schedule's pool) is zero by then: cleared by the quantise-scatter two kernels back, or by a
-  // memset right before the launch, which this launch cannot overlap.
+  // overlaps the previous kernel, and the wait for it comes after. The schedule counter (dynamic chunks, or
+  // the static schedule's pool) is zero at launch; the last CTA to finish zeroes it again.
   const int E = prm.E, NT = prm.NT;
   const int R = min(__ldcg(prm.poff + E - 1), prm.cap);
   const int r128 = R / BM;
   const int pool = (!prm.dyn && prm.steal) ? tail_pool(r128 * NT, (int)gridDim.x) : 0;
   int tau0, tau1;
   cta_range(r128 * NT - pool, tau0, tau1);
-  if (tau0 >= tau1 && pool == 0) return;  // (with a pool every CTA has at least three tiles of its own)
+  if (tau0 >= tau1 && pool == 0 && !prm.dyn) {  // (with a pool every CTA has at least three tiles of its own)
+    if (threadIdx.x == 0) sched_release(prm.sched);
+    return;
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -284,6 +286,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         bulk_load(st + STR_OFF, sf_str + (size_t)kb * ATOMS * SF_TILE, atoms * SF_TILE, bar_full + 8 * s, pol_str);
       }
     }
+    sched_release(prm.sched);  // this CTA takes no more chunks
     // on every path, let the copies already issued land before the CTA exits
     for (int j = max(0, it - STAGES); j < it; ++j) drain_wait(bar_full + 8 * (j % STAGES), (uint32_t)(j / STAGES) & 1u);
   } else if (warp == 5 && lane == 0) {
@@ -535,7 +538,7 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
                           const uint8_t* a_sf, const int32_t* poff, const int32_t* pair_of_row,
                           const uint8_t* b_codes, const uint8_t* b_sf, const float* alpha, const float* gs2,
                           uint8_t* out_codes, uint8_t* out_sf, float* amax, uint32_t* status, uint16_t* o_pairs,
-                          uint32_t* err, int* sched, bool sched_zeroed, cudaStream_t st) {
+                          uint32_t* err, int* sched, cudaStream_t st) {
   if (T == 0) return FP4MOE_OK;
   if (mode != kW2Rows && amax == nullptr) return FP4MOE_INVALID_ARG;
   if (mode == kW1SwiGLU && status == nullptr) return FP4MOE_INVALID_ARG;
@@ -572,9 +575,7 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
   prm.dyn = ((int64_t)T * cfg.top_k >= (int64_t)local_experts(cfg) * BM) ? 1 : 0;
   if (prm.dyn && sched == nullptr) return FP4MOE_INVALID_ARG;
   prm.steal = (!prm.dyn && sched != nullptr) ? 1 : 0;
-  prm.sched = sched;
-  if (sched != nullptr && !sched_zeroed && cudaMemsetAsync(sched, 0, sizeof(int), st) != cudaSuccess)
-    return FP4MOE_CUDA_ERROR;
+  prm.sched = sched;  // zero between launches: no memset splits the launch chain
   AMaps tmA;
   for (int b = 0; b < 4; ++b)
     if (!encode_u8_sw128(&tmA.box[b], a_codes, (uint64_t)prm.K / 2, (uint64_t)prm.cap, 16u << b))

@@ -29,7 +29,7 @@ struct GemmParams {
   int o_pairs32;  // W2: o_pairs is 32-byte aligned (every 128-column piece of a row is then)
   int dyn;     // 1: dynamic chunk schedule (large T); 0: contiguous static ranges (decode sizes)
   int steal;   // static schedule: the last tiles form a pool that CTAs take from `sched` once their range is done
-  int* sched;  // dynamic schedule, or the static schedule's pool: next-chunk counter, zero at launch
+  int* sched;  // {next chunk or pool tile, CTAs finished}: zero at launch, zeroed again by the launch's last CTA
 };
 
 // Tensor maps of the activation codes whose boxes are 16, 32, 64 and 128 rows
@@ -104,6 +104,18 @@ __device__ __forceinline__ Chunk decode_chunk(int c, const int* s_cstart, const 
     k.count = min(kChunk, k.me - mb * kChunk);
   }
   return k;
+}
+
+// The schedule's counter pair is zero between launches: the last CTA of a launch to stop taking chunks zeroes
+// both words. One thread per CTA calls this: the producer, once it takes no more chunks (off the critical
+// path: the CTA's last tiles are still in flight), or thread 0 of a CTA with nothing to do.
+__device__ __forceinline__ void sched_release(int* sched) {
+  if (sched == nullptr) return;
+  __threadfence();
+  if (atomicAdd(sched + 1, 1) == (int)gridDim.x - 1) {
+    atomicExch(sched, 0);
+    atomicExch(sched + 1, 0);
+  }
 }
 
 // Pool tile i of the static schedule (tile tau of the order) as a one-tile chunk.

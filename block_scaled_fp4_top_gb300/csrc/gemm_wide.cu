@@ -77,14 +77,18 @@ __global__ void __launch_bounds__(WTHREADS, 1)
 
   __shared__ int s_abort;
 
-  // As in the 128 x 128 kernel: the set-up overlaps the previous kernel, and the counter is zero by the wait.
+  // As in the 128 x 128 kernel: the set-up overlaps the previous kernel, and the schedule counter is zero at
+  // launch and zeroed again by the last CTA to finish.
   const int E = prm.E, NT = prm.NT;  // NT: 256-row weight tiles
   const int R = min(__ldcg(prm.poff + E - 1), prm.cap);
   const int r128 = R / WBM;
   const int pool = (!prm.dyn && prm.steal) ? tail_pool(r128 * NT, (int)gridDim.x) : 0;
   int tau0, tau1;
   cta_range(r128 * NT - pool, tau0, tau1);
-  if (tau0 >= tau1 && pool == 0) return;  // (with a pool every CTA has at least three tiles of its own)
+  if (tau0 >= tau1 && pool == 0 && !prm.dyn) {  // (with a pool every CTA has at least three tiles of its own)
+    if (threadIdx.x == 0) sched_release(prm.sched);
+    return;
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -209,6 +213,7 @@ __global__ void __launch_bounds__(WTHREADS, 1)
                   pol_w);
       }
     }
+    sched_release(prm.sched);  // this CTA takes no more chunks
     // on every path, let the copies already issued land before the CTA exits
     for (int j = max(0, it - WSTAGES); j < it; ++j)
       drain_wait(bar_full + 8 * (j % WSTAGES), (uint32_t)(j / WSTAGES) & 1u);

@@ -58,7 +58,7 @@ fp4moe_status route_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* 
 // status: sticky FP4MOE_SAT_L1 when a block scale saturates; err: FP4MOE_ERR_NAN for a NaN in x
 fp4moe_status quant_scatter_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const float* gs1,
                                    const int32_t* slot_of_pair, uint8_t* a1, uint8_t* a1_sf, uint32_t* status,
-                                   uint32_t* err, int32_t* sched_zero, cudaStream_t st);
+                                   uint32_t* err, cudaStream_t st);
 // gs2 and alpha2 from the running amax|h| of the W1 epilogues (left as they are when it is zero), which is
 // then cleared: fp4moe_refresh_gs2
 fp4moe_status refresh_gs2_launch(int32_t E, float* amax_run, const float* gw2, float* gs2, float* alpha2,
@@ -87,7 +87,7 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
                           const uint8_t* a_sf, const int32_t* poff, const int32_t* pair_of_row,
                           const uint8_t* b_codes, const uint8_t* b_sf, const float* alpha, const float* gs2,
                           uint8_t* out_codes, uint8_t* out_sf, float* amax, uint32_t* status, uint16_t* o_pairs,
-                          uint32_t* err, int* sched, bool sched_zeroed, cudaStream_t st);
+                          uint32_t* err, int* sched, cudaStream_t st);
 
 // SMs of the current device (cached per device), 0 on error
 int sm_count();

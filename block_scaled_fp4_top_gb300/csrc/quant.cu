@@ -34,12 +34,9 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(int T, int H, int k,
                                                             const float* __restrict__ gs1,
                                                             const int32_t* __restrict__ slot_of_pair,
                                                             uint8_t* __restrict__ a1, uint8_t* __restrict__ a1_sf,
-                                                            uint32_t* status, uint32_t* err,
-                                                            int32_t* sched_zero) {
+                                                            uint32_t* status, uint32_t* err) {
   pdl_wait();
   pdl_trigger();
-  // the schedule counters of the two grouped GEMMs that follow (they take from them only after their waits)
-  if (sched_zero != nullptr && blockIdx.x == 0 && threadIdx.x < 2) sched_zero[threadIdx.x] = 0;
   const int C = H >> 4;
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (int64_t)T * C) return;
@@ -232,11 +229,11 @@ fp4moe_status batch_gs1_launch(int32_t T, int32_t H, const uint16_t* x, int32_t 
 
 fp4moe_status quant_scatter_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* x, const float* gs1,
                                    const int32_t* slot_of_pair, uint8_t* a1, uint8_t* a1_sf, uint32_t* status,
-                                   uint32_t* err, int32_t* sched_zero, cudaStream_t st) {
+                                   uint32_t* err, cudaStream_t st) {
   if (T == 0) return FP4MOE_OK;
   const int64_t threads = (int64_t)T * (cfg.hidden / 16);
   return launch_pdl(quant_scatter_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, st, T, cfg.hidden,
-                    cfg.top_k, x, gs1, slot_of_pair, a1, a1_sf, status, err, sched_zero) == cudaSuccess
+                    cfg.top_k, x, gs1, slot_of_pair, a1, a1_sf, status, err) == cudaSuccess
              ? FP4MOE_OK
              : FP4MOE_CUDA_ERROR;
 }

@@ -28,7 +28,9 @@
  *  - T (tokens) is a host integer, 0 <= T <= cfg->max_tokens. It selects the
  *    launch sizes, so one CUDA graph is captured per T.
  *  - `ws` is a device workspace of fp4moe_workspace_bytes(cfg) bytes. Zero it
- *    once before first use. Its first 4 bytes are a sticky device error word:
+ *    once before first use: its header holds counters (the grouped GEMMs'
+ *    tile schedules, fp4moe_batch_gs1) that every call leaves at zero again,
+ *    so no call needs a memset. Its first 4 bytes are a sticky device error word:
  *    a bitwise OR of FP4MOE_ERR_* values. Kernels set bits there instead of
  *    trapping. Read and clear it with fp4moe_read_error outside any graph.
  *    A second sticky word reports saturated activation block scales
