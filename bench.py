@@ -49,7 +49,7 @@ FALLBACK_HBM_GBS = 6800.0
 # with, so it is reported while their hash matches and as null otherwise.
 W1_TRAFFIC = {
     # workload name: (bytes per launch, sha256 of the GEMM sources)
-    "dsv4_flash_decode_T64": (1949534720 + 3865856, "fbe49a716509c578b14c9b8e162adfbe2b91e75f29af2bfa2e6990fcbd3461f7"),
+    "dsv4_flash_decode_T64": (1949527808 + 3527936, "a5c9eaa615e931912a419630c193ce1f6ef8c308a2a81e3819d1fb5d386076e2"),
 }
 GEMM_SOURCES = ("block_scaled_fp4_top_gb300/csrc/gemm.cu", "block_scaled_fp4_top_gb300/csrc/gemm_sched.cuh",
                 "block_scaled_fp4_top_gb300/csrc/common.cuh")
