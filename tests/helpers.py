@@ -28,6 +28,17 @@ def torch_to_bits(t) -> np.ndarray:
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
+# Bytes [64, 80) of the workspace header: the two grouped GEMMs' schedule counter pairs (chunks or pool tiles
+# taken, CTAs done). The library keeps them at zero between calls, so that no call needs a memset.
+SCHED_COUNTERS = slice(64, 80)
+
+
+def assert_sched_counters_zero(ws):
+    """The grouped GEMMs' schedule counters are back at zero (after a synchronize)."""
+    words = ws[SCHED_COUNTERS].cpu().numpy().view(np.int32)
+    assert (words == 0).all(), f"schedule counters left at {words.tolist()}"
+
+
 def make_layer(wl: sg.Workload, max_tokens: int, chunk: int = 16):
     """GPU layer whose weights come from the GPU twin of the generator, quantised by the library."""
     import torch

@@ -15,7 +15,8 @@ import numpy as np
 import pytest
 
 import synthgen as sg
-from helpers import OracleExperts, bits_to_torch, ensure_built, float_parity, make_layer, torch_to_bits
+from helpers import (OracleExperts, assert_sched_counters_zero, bits_to_torch, ensure_built, float_parity,
+                     make_layer, torch_to_bits)
 from oracle import moe
 
 pytestmark = pytest.mark.gpu
@@ -54,6 +55,7 @@ def _forward(layer, wl, x_bits):
     layer.forward(x[:T] if T else x, y, ids, None)
     torch.cuda.synchronize()
     assert layer.read_error() == 0
+    assert_sched_counters_zero(layer.ws)
     return sg.bf16_bits_to_f32(torch_to_bits(y))[:T], ids.cpu().numpy()[: T * wl.k].reshape(T, wl.k)
 
 

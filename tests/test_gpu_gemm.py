@@ -23,7 +23,7 @@ m-tiles, and K is partial (a stage of 2 atoms) or runs over several stages.
 import numpy as np
 import pytest
 
-from helpers import bf16_ulp, dump, ensure_built, tile_weights
+from helpers import assert_sched_counters_zero, bf16_ulp, dump, ensure_built, tile_weights
 from oracle import codecs, layout, moe, nvfp4
 
 pytestmark = pytest.mark.gpu
@@ -117,6 +117,7 @@ def test_w2_rows_against_fp64(H, I, counts, full_range):
     api.moe_grouped_gemm_w2(cfg, T, t["a"], t["asf"], t["poff"], t["por"], t["w"], t["wsf"], t["alpha"], o, t["ws"])
     torch.cuda.synchronize()
     assert api.fp4moe_read_error(t["ws"]) == 0
+    assert_sched_counters_zero(t["ws"])
     got = o.float().cpu().numpy().astype(np.float64)
     A = _dec(qa, sa)
     Wd = _dec(qw, sw).reshape(len(counts), H, I)
@@ -183,6 +184,7 @@ def _run_w1(cfg, T, cap, I, t, gs2, alpha=None):
                                    t["alpha"] if alpha is None else alpha,
                                    torch.tensor([gs2], dtype=torch.float32, device="cuda"), a2, a2sf, t["ws"])
     torch.cuda.synchronize()
+    assert_sched_counters_zero(t["ws"])
     return a2.cpu().numpy().reshape(cap, I // 2), a2sf.cpu().numpy()
 
 

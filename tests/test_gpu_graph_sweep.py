@@ -23,7 +23,7 @@ import numpy as np
 import pytest
 
 import synthgen as sg
-from helpers import bits_to_torch, ensure_built, float_parity, make_layer, torch_to_bits
+from helpers import assert_sched_counters_zero, bits_to_torch, ensure_built, float_parity, make_layer, torch_to_bits
 from oracle import moe
 
 pytestmark = pytest.mark.gpu
@@ -96,6 +96,7 @@ def test_graph_sweep_replays(oracle_svc):
                 labels.append((T, i))
         torch.cuda.synchronize()
         assert layer.read_error() == 0
+        assert_sched_counters_zero(layer.ws)   # the replays leave the GEMMs' counters as they found them
         del g
     # every checked row of every bucket against the oracle, in one pass over the experts
     ref = oracle_svc.layer(wl, checked_x, gs1, gs2)
