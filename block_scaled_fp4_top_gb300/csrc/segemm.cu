@@ -29,8 +29,8 @@
 // h spans two tiles, so W1 runs as clusters of 2 n-tiles that swap the per-row amax (or, when K
 // is split, reduce both tiles together) through distributed shared memory.
 //
-// K split: with fewer tiles than SMs (decode), K is cut into S slices over the z dimension of the
-// cluster. Each CTA leaves its fp32 partial tile in shared memory; after a cluster barrier each
+// K split: with fewer tiles than half of the SMs (decode; the other half stays free for the routing that
+// runs beside the shared expert), K is cut into S slices over the z dimension of the cluster. Each CTA leaves its fp32 partial tile in shared memory; after a cluster barrier each
 // CTA sums a share of the rows over all slices, in slice order (deterministic), and runs the
 // epilogue on them.
 // Every wait is bounded, as in the routed GEMMs; a timeout sets FP4MOE_ERR_TIMEOUT and skips work.
@@ -560,6 +560,11 @@ fp4moe_status se_forward_launch(const fp4moe_config& cfg, int32_t T, const uint1
   if (!configure_se<0>() || !configure_se<1>()) return FP4MOE_CUDA_ERROR;
   const int nsm = sm_count();
   if (nsm <= 0) return FP4MOE_CUDA_ERROR;
+  // The shared expert runs beside the routing on a side stream. Its K slices are capped at half of the SMs,
+  // so the routing kernels and the routed W1 find free SMs while it runs. Uncapped (96 and 128 CTAs), it held
+  // the routed chain back by about 15 us. Capped, the DSV4 decode layer took 460.8 us with it against 468.0
+  // (453.7 us without the shared expert).
+  const int se_sms = nsm / 2;
   const unsigned mt = (unsigned)((T + SE_BM - 1) / SE_BM);
   SeMaps m1, m2;
   if (!encode_u8_sw128(&m1.a, qx, (uint64_t)H, (uint64_t)T, SE_BM) ||
@@ -581,14 +586,14 @@ fp4moe_status se_forward_launch(const fp4moe_config& cfg, int32_t T, const uint1
   p.h_codes = qh;
   p.h_scale = sh;
   const dim3 g1((unsigned)(2 * Is / SE_BN), mt);
-  if (launch_se_gemm<0>(g1, k_slices<0>((int)g1.x, (int)mt, p.KB, nsm), st, m1, p) != cudaSuccess)
+  if (launch_se_gemm<0>(g1, k_slices<0>((int)g1.x, (int)mt, p.KB, se_sms), st, m1, p) != cudaSuccess)
     return FP4MOE_CUDA_ERROR;
   p.KB = Is / 128;
   p.a_scale = sh;
   p.w_scale = s2;
   p.out = out;
   const dim3 g2((unsigned)(H / SE_BN), mt);
-  return launch_se_gemm<1>(g2, k_slices<1>((int)g2.x, (int)mt, p.KB, nsm), st, m2, p) == cudaSuccess
+  return launch_se_gemm<1>(g2, k_slices<1>((int)g2.x, (int)mt, p.KB, se_sms), st, m2, p) == cudaSuccess
              ? FP4MOE_OK
              : FP4MOE_CUDA_ERROR;
 }

@@ -16,7 +16,7 @@ import numpy as np
 import pytest
 
 import synthgen as sg
-from helpers import bits_to_torch, ensure_built, make_layer, torch_to_bits
+from helpers import assert_sched_counters_zero, bits_to_torch, ensure_built, make_layer, torch_to_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -76,6 +76,7 @@ def test_abort_bit_poisons_then_recovers():
     torch.cuda.synchronize()
     assert time.perf_counter() - t0 < 2.0, "a poisoned call must not wait out its limits"
     assert layer.read_error(clear=True) & _lib.ERR_TIMEOUT
+    assert_sched_counters_zero(layer.ws)   # the skipped GEMMs still leave their schedule counters at zero
 
     layer.forward(x, y)
     torch.cuda.synchronize()
