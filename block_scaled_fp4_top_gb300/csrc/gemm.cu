@@ -105,8 +105,9 @@ constexpr int kMaxResidentK = (TMEM_COLS - ACC_COLS - SFB_STAGE_COLS * STAGES) *
 
 using Params = GemmParams;
 
-// full, empty, tfull (2), tempty (2), drain, sfull, sempty, sready, cdrain: all in the 256 bytes at BAR_OFF
-static_assert(8 * (2 * STAGES + 2 + 2 + 1 + 2 * kSchedSlots + STAGES + 1) <= 256, "barriers fit their area");
+// full, empty, tfull (2), tempty (2), drain, sfull, sempty, sready, cdrain, resfree: all in the 256 bytes at
+// BAR_OFF
+static_assert(8 * (2 * STAGES + 2 + 2 + 1 + 2 * kSchedSlots + STAGES + 1 + 1) <= 256, "barriers fit their area");
 
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -145,6 +146,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t bar_sempty = bar_sfull + 8 * kSchedSlots;  // kSchedSlots x 8 bytes: it was read
   const uint32_t bar_sready = bar_sempty + 8 * kSchedSlots;  // STAGES x 8 bytes: the stage's scales are in TMEM
   const uint32_t bar_cdrain = bar_sready + 8 * STAGES;       // the copier's last copies completed
+  // one phase per change of the fixed operand: every MMA that read the resident scales before it completed
+  const uint32_t bar_resfree = bar_cdrain + 8;
 
   for (int e = threadIdx.x; e < E; e += THREADS) s_poff[e] = __ldcg(prm.poff + e);
   if (prm.dyn) {
@@ -188,6 +191,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int s = 0; s < STAGES; ++s) mbar_init(bar_sready + 8 * s, NCOPY);  // one commit per copier
     mbar_init(bar_cdrain, NCOPY);
+    mbar_init(bar_resfree, 1);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -298,7 +302,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // with the shared window, so adding offsets to an already-masked descriptor could carry into the
     // reserved bits.
     constexpr uint32_t idesc = idesc_nvf4(BM, BN);
-    int tl = 0;
+    int tl = 0, prev_key = INT_MIN;
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -308,6 +312,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (; ok && src.next(t, prm, tau0, s_poff, s_cstart, s_sched, bar_sfull, bar_sempty, n_chunks, E, NT, r128);
          ++tl) {
       const bool res_a = (t.me == 1);
+      const int key = res_a ? t.mt : -1 - (t.e * NT + t.nt);
+      // a new fixed operand: bar_resfree completes once every MMA issued so far (all of them read the old
+      // resident scales) has completed, and the copiers wait for that before they overwrite them
+      if (tl > 0 && key != prev_key) tc_commit(bar_resfree);
+      prev_key = key;
       const int b = tl % nacc;
       const uint32_t use = (uint32_t)(tl / nacc);
       // the epilogue has drained this accumulator buffer
@@ -364,9 +373,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     // Per stage: the 8 streamed scale tiles (and, for a new fixed operand, its 8 resident ones) from the
     // stage's shared memory into TMEM, then one commit to bar_sready. TMEM slot s of the streamed scales
     // is free again once stage s is full: the producer refilled it only after the MMAs of its previous use
-    // committed bar_empty. Resident scales are overwritten only after every MMA of the previous tile has
-    // completed (its bar_tfull commit).
-    int tl = 0, prev_key = INT_MIN;
+    // committed bar_empty. Resident scales are overwritten only after every MMA that read them has
+    // completed: the MMA issuer commits bar_resfree once per change of the fixed operand, before the new
+    // operand's first MMA. A copier can be several tiles ahead of the MMAs (a tile of one or two ring
+    // stages), but never a whole change ahead: it cannot pass a change until the MMAs of the change before
+    // have completed, so the parity of its wait always names the right phase. (A wait on the previous
+    // tile's accumulator barrier could name a phase two uses back when the copier ran two tiles ahead.)
+    int tl = 0, prev_key = INT_MIN, nchg = 0;
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -380,11 +393,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool new_res = (key != prev_key);
       prev_key = key;
       if (new_res && tl > 0) {
-        const int pb = (tl - 1) % nacc;
-        if (!mbar_wait(bar_tfull + 8 * pb, (uint32_t)((tl - 1) / nacc) & 1u, prm.err)) {
+        if (!mbar_wait(bar_resfree, (uint32_t)nchg & 1u, prm.err)) {
           ok = false;
           break;
         }
+        ++nchg;
       }
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait(bar_full + 8 * s, ph, prm.err)) {

@@ -9,7 +9,10 @@ m-tiles, and K is partial (a stage of 2 atoms) or runs over several stages.
   the others the static contiguous one (decode sizes). With K and the
   weight rows multiples of 256, the dynamic cases and the static ones with
   at least 8 pairs per expert run the 128 x 256 tile kernel (gemm_wide.cu);
-  the sparse 16-expert cases keep the 128 x 128 one at every K.
+  the sparse 16-expert cases keep the 128 x 128 one at every K. The sparse
+  48-expert cases have 1152 tiles of 128 x 128, enough for the static
+  schedule's tail pool: their last 288 tiles go to whichever CTAs finish
+  their own range first.
 * W1: the clamped SwiGLU + requantisation epilogue is compared with the
   oracle's quantiser applied to the fp64 reference h. Codes must agree
   except at rounding ties that the fp32 accumulation moves.
@@ -31,6 +34,9 @@ pytestmark = pytest.mark.gpu
 
 # 16 experts, 26 pairs: fewer than 8 per expert, so the static schedule keeps its 128 x 128 kernel
 SPARSE16 = [1, 0, 3, 0, 2, 5, 0, 1, 2, 0, 0, 4, 1, 0, 5, 2]
+# 48 experts, 36 of them live with 1-3 pairs: with 4096 weight rows that is 1152 tiles of 128 x 128, so the
+# static schedule keeps its last 288 tiles in the pool that CTAs take from once their own range is done
+SPARSE48 = [(7 * e) % 4 for e in range(48)]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -108,6 +114,7 @@ def _setup(H, I, counts, seed, which, full_range=False, alpha_mult=1.0):
     (512, 256, [600, 5, 130], False),           # dynamic schedule, two 256-row weight tiles of the wide kernel
     (256, 768, SPARSE16, False),                # under 8 pairs per expert: static, 128 x 128 tiles, K = 768
     (512, 256, SPARSE16, True),                 # the same, every finite E4M3 scale byte
+    (4096, 256, SPARSE48, False),               # static schedule with its tail pool
 ])
 def test_w2_rows_against_fp64(H, I, counts, full_range):
     import torch
@@ -193,7 +200,8 @@ def _run_w1(cfg, T, cap, I, t, gs2, alpha=None):
                                                    (256, 256, [3, 0, 140], True),     # every finite E4M3 scale byte
                                                    (256, 256, [600, 5, 130], True),
                                                    (256, 256, SPARSE16, False),       # static, 128 x 128 tiles
-                                                   (512, 256, SPARSE16, True)])
+                                                   (512, 256, SPARSE16, True),
+                                                   (256, 2048, SPARSE48, False)])     # the tail pool
 def test_w1_swiglu_requant(H, I, counts, full_range):
     from block_scaled_fp4_top_gb300 import api
     cfg, T, cap, ids, L, (qa, sa, qw, sw, alpha), t = _setup(H, I, counts, 2, which=1, full_range=full_range)
