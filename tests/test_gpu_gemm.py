@@ -12,7 +12,9 @@ m-tiles, and K is partial (a stage of 2 atoms) or runs over several stages.
   the sparse 16-expert cases keep the 128 x 128 one at every K. The sparse
   48-expert cases have 1152 tiles of 128 x 128, enough for the static
   schedule's tail pool: their last 288 tiles go to whichever CTAs finish
-  their own range first.
+  their own range first. With one or two ring stages per tile (K <= 1024)
+  the scale copiers run tiles ahead of the MMAs there, which tests the
+  barrier that guards the resident scales at each change of expert.
 * W1: the clamped SwiGLU + requantisation epilogue is compared with the
   oracle's quantiser applied to the fp64 reference h. Codes must agree
   except at rounding ties that the fp32 accumulation moves.
@@ -201,7 +203,8 @@ def _run_w1(cfg, T, cap, I, t, gs2, alpha=None):
                                                    (256, 256, [600, 5, 130], True),
                                                    (256, 256, SPARSE16, False),       # static, 128 x 128 tiles
                                                    (512, 256, SPARSE16, True),
-                                                   (256, 2048, SPARSE48, False)])     # the tail pool
+                                                   (256, 2048, SPARSE48, False),      # the tail pool
+                                                   (512, 2048, SPARSE48, True)])      # the same, one full stage
 def test_w1_swiglu_requant(H, I, counts, full_range):
     from block_scaled_fp4_top_gb300 import api
     cfg, T, cap, ids, L, (qa, sa, qw, sw, alpha), t = _setup(H, I, counts, 2, which=1, full_range=full_range)
