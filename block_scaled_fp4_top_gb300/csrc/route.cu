@@ -102,7 +102,7 @@ __device__ __forceinline__ void offsets_and_pads(int E, int cap, int c, int* s_w
   const int R = s_R;
   r_lo = (int)((long long)(R / 4) * part / nparts) * 4;
   r_hi = part + 1 == nparts ? R : (int)((long long)(R / 4) * (part + 1) / nparts) * 4;
-  const int R0 = min(r_lo, cap), R1 = min(r_hi, cap);
+  const int R0 = min(r_lo, cap), R1 = pair_of_row != nullptr ? min(r_hi, cap) : R0;  // no map: no row fill
   int r0 = R0;
   if ((reinterpret_cast<uintptr_t>(pair_of_row) & 15u) == 0) {  // four rows per store where aligned
     const int4 m1 = make_int4(-1, -1, -1, -1);
@@ -215,14 +215,13 @@ __global__ void __launch_bounds__(256) hist_kernel(int T, int Eg, int first, int
 }
 
 // One CTA of 1024 threads: exclusive prefix of the chunk histograms over the chunks (in place), then
-// counts, offsets, padded offsets and pads. Each expert's column is split among tpe = 1024 / E threads
+// counts, offsets and padded offsets (slots_kernel marks the padding rows). Each expert's column is split among tpe = 1024 / E threads
 // (a power of two, at most 32, so one warp holds them all): every part loads its run of chunk counts at
 // once, the parts' sums are scanned across their lanes, and each part rewrites its run from its own base.
 // For E = 256 that is four parts of 32 chunks at T = 8192: one round trip to L2 instead of eight.
 __global__ void __launch_bounds__(1024) scan_kernel(int E, int nchunks, int cap, int32_t* __restrict__ hist,
                                                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                                                    int32_t* __restrict__ poff, int32_t* __restrict__ pair_of_row,
-                                                    uint32_t* err) {
+                                                    int32_t* __restrict__ poff, uint32_t* err) {
   pdl_wait();
   pdl_trigger();
   __shared__ int s_warp[64];
@@ -265,15 +264,17 @@ __global__ void __launch_bounds__(1024) scan_kernel(int E, int nchunks, int cap,
   __syncthreads();
   const int c = threadIdx.x < E ? s_c[threadIdx.x] : 0;
   int start;
-  int r_lo, r_hi;  // one part: every row
-  offsets_and_pads(E, cap, c, s_warp, counts, offsets, poff, pair_of_row, err, 0, 1, start, r_lo, r_hi);
+  int r_lo, r_hi;
+  // the padding rows' -1 is left to slots_kernel, spread over its CTAs: one CTA writing all R rows here took
+  // longer than the rest of this kernel
+  offsets_and_pads(E, cap, c, s_warp, counts, offsets, poff, nullptr, err, 0, 1, start, r_lo, r_hi);
 }
 
 // Slot of every pair of one 64-token chunk, in ascending pair order. The chunk's pairs are cut into one
 // contiguous run per warp. Each warp counts its run's pairs per expert into its own shared-memory row; a
 // prefix over the warp rows then gives every warp, for every expert, the first slot after the pairs of the
 // chunk's earlier runs; within a run, lanes that share an expert rank themselves by lane order, 32 pairs at
-// a time. No slot depends on the order of atomics.
+// a time. No slot depends on the order of atomics. The CTAs also mark the padding rows -1, expert by expert.
 constexpr int kSlotWarps = 8;
 __global__ void __launch_bounds__(32 * kSlotWarps) slots_kernel(int T, int Eg, int first, int E, int k, int cap,
                                                                 const int32_t* __restrict__ ids,
@@ -327,6 +328,12 @@ __global__ void __launch_bounds__(32 * kSlotWarps) slots_kernel(int T, int Eg, i
     if (e >= 0 && rank == 0) base[e] += __popc(peers);
     __syncwarp();
   }
+  // the padding rows of experts blockIdx.x, blockIdx.x + gridDim.x, ...: -1 (rows from cap on are not written)
+  for (int e = blockIdx.x; e < E; e += gridDim.x) {
+    const int n = __ldcg(counts + e), pe = __ldcg(poff + e);
+    const int end = min(pe, cap);
+    for (int r = pe - (((n + 127) & ~127) - n) + threadIdx.x; r < end; r += blockDim.x) pair_of_row[r] = -1;
+  }
 }
 
 }  // namespace
@@ -351,8 +358,7 @@ fp4moe_status route_launch(const fp4moe_config& cfg, int32_t T, const uint16_t* 
     const int nchunks = (T + kRouteChunk - 1) / kRouteChunk;
     r = launch_pdl(hist_kernel, dim3(nchunks), dim3(256), 0, st, T, Eg, first, E, k, (const int32_t*)ids, hist, err);
     if (r == cudaSuccess)
-      r = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, st, E, nchunks, cap, hist, counts, offsets, poff,
-                     pair_of_row, err);
+      r = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, st, E, nchunks, cap, hist, counts, offsets, poff, err);
     if (r == cudaSuccess)
       r = launch_pdl(slots_kernel, dim3(nchunks), dim3(32 * kSlotWarps), (size_t)kSlotWarps * E * sizeof(int), st, T, Eg,
                      first, E, k, cap, (const int32_t*)ids,
