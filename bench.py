@@ -301,6 +301,50 @@ def build_step(wl, cfg, layer, x, y, dev, n_stage_steps):
     return step, bufs, ev, se_ev
 
 
+def e2e_pipeline(layer, x, y, stream):
+    """The end-to-end loop as a caller would pipeline it: every step copies its input from pinned host memory,
+    runs moe_forward and copies its output back to pinned host memory. The copies run on a second stream
+    with two device buffers each way, so step i's output copy and step i + 1's input copy overlap the
+    compute of the steps around them; events keep every buffer's reuse ordered. run(n) runs n steps and
+    returns CUDA events recorded before the first input copy and after the last output copy; last(n) is the
+    host copy of the output of the last of those n steps."""
+    import torch
+    copy = torch.cuda.Stream()
+    x_host = torch.empty_like(x, device="cpu").pin_memory()
+    x_host.copy_(x.cpu())
+    y_host = [torch.empty_like(y, device="cpu").pin_memory() for _ in range(2)]
+    x_dev = [torch.empty_like(x) for _ in range(2)]
+    y_dev = [torch.empty_like(y) for _ in range(2)]
+    ev = lambda: torch.cuda.Event()
+    x_ready, done, y_free = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+
+    def run(n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        copy.wait_stream(stream)
+        e0.record(copy)
+        with torch.cuda.stream(copy):
+            x_dev[0].copy_(x_host, non_blocking=True)
+        x_ready[0].record(copy)
+        for i in range(n):
+            b = i & 1
+            stream.wait_event(x_ready[b])            # this step's input is on the device
+            stream.wait_event(y_free[b])             # its output buffer was copied out two steps ago
+            layer.forward(x_dev[b], y_dev[b])
+            done[b].record(stream)
+            with torch.cuda.stream(copy):
+                if i + 1 < n:                        # the next input, once step i - 1 no longer reads its buffer
+                    copy.wait_event(done[1 - b])
+                    x_dev[1 - b].copy_(x_host, non_blocking=True)
+                    x_ready[1 - b].record(copy)
+                copy.wait_event(done[b])             # this step's output, once it is written
+                y_host[b].copy_(y_dev[b], non_blocking=True)
+                y_free[b].record(copy)
+        e1.record(copy)
+        return e0, e1
+    run.last = lambda n: y_host[(n - 1) & 1]
+    return run
+
+
 def run_ours(args, wl, rank, world):
     import torch
     from block_scaled_fp4_top_gb300 import api
@@ -378,26 +422,15 @@ def run_ours(args, wl, rank, world):
     step_ms = ms / args.steps
 
     # ---------------- e2e: moe_forward with pinned host buffers, copies inside the timed region
-    x_host = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
-    x_host.copy_(x.cpu())
-    y_host = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
-    x_dev = torch.empty_like(x)
-    for _ in range(args.warmup):
-        x_dev.copy_(x_host, non_blocking=True)
-        layer.forward(x_dev, y)
-        y_host.copy_(y, non_blocking=True)
+    e2e_run = e2e_pipeline(layer, x, y, stream)
+    e2e_run(args.warmup)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        x_dev.copy_(x_host, non_blocking=True)
-        layer.forward(x_dev, y)
-        y_host.copy_(y, non_blocking=True)
-    e1.record(stream)
+    e0, e1 = e2e_run(args.steps)
     torch.cuda.synchronize()
+    # the pipelined steps give the output of the eager steps above, bit for bit
+    assert torch.equal(e2e_run.last(args.steps), y.cpu()), "e2e output differs from the timed steps' output"
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     assert layer.read_error() == 0
 
