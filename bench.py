@@ -49,10 +49,10 @@ FALLBACK_HBM_GBS = 6800.0
 # with, so it is reported while their hash matches and as null otherwise.
 W1_TRAFFIC = {
     # workload name: (bytes per launch, sha256 of the GEMM sources)
-    "dsv4_flash_decode_T64": (1949527808 + 3527936, "a5c9eaa615e931912a419630c193ce1f6ef8c308a2a81e3819d1fb5d386076e2"),
+    "dsv4_flash_decode_T64": (1948484864 + 8056320, "2fbffc0559935b722dde6eb582efbe14a491aa1701e7463ec351f103e6271e88"),
 }
-GEMM_SOURCES = ("block_scaled_fp4_top_gb300/csrc/gemm.cu", "block_scaled_fp4_top_gb300/csrc/gemm_sched.cuh",
-                "block_scaled_fp4_top_gb300/csrc/common.cuh")
+GEMM_SOURCES = ("block_scaled_fp4_top_gb300/csrc/gemm.cu", "block_scaled_fp4_top_gb300/csrc/gemm_wide.cu",
+                "block_scaled_fp4_top_gb300/csrc/gemm_sched.cuh", "block_scaled_fp4_top_gb300/csrc/common.cuh")
 
 
 def gemm_sources_sha() -> str:
@@ -474,7 +474,7 @@ def run_ours(args, wl, rank, world):
         "stages_note": f"serialised: a second pass of {n_stage_steps} steps with CUDA events between the calls, "
                        "which stop each kernel's prologue from overlapping its predecessor; the step time above has "
                        "no events inside",
-        "roofline": {"kernel": "mx_gemm_kernel<W1 SwiGLU bf16>" if mx else "grouped_gemm_kernel<W1 SwiGLU requant>",
+        "roofline": {"kernel": "mx_gemm_kernel<W1 SwiGLU bf16>" if mx else "grouped_gemm_wide_kernel<W1 SwiGLU requant>",
                      "bound": "hbm", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": w1_bytes + act1, "traffic": w1_traffic(wl.name)},

@@ -8,6 +8,11 @@
 // searchsorted(padded_offsets, row, right=True) on offsets with no leading 0
 // ("Bug 2", "Bug 4").
 //
+// This 128 x 128 kernel now serves only the W2 GEMM whose K (the intermediate
+// width) is an odd multiple of 128. Every other grouped GEMM runs on the
+// 128 x 256 kernel of gemm_wide.cu, which shares the tile schedules and the
+// row epilogues (gemm_sched.cuh); this one still carries the W1 modes.
+//
 // Persistent kernel, one CTA per SM. Output tiles are 128 activation rows x
 // 128 weight rows. They are numbered expert by expert; inside expert e, with
 // M_e m-tiles, the n-tiles run slowest and the m-tiles fastest. CTA c takes
@@ -100,7 +105,6 @@ constexpr uint32_t SFB_STAGE_COLS = 4 * ATOMS;  // B scales of one ring stage
 // else 1.
 static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
 static_assert(SMEM_BYTES + 8 * kMaxExperts + 128 <= 232448, "shared memory budget (dynamic + static)");
-constexpr int kWidePairsPerExpert = 8;  // static schedule: the 128 x 256 kernel from this average on
 constexpr int kMaxResidentK = (TMEM_COLS - ACC_COLS - SFB_STAGE_COLS * STAGES) * 16;  // 4608 with one accumulator
 
 using Params = GemmParams;
@@ -593,31 +597,21 @@ fp4moe_status gemm_launch(GemmMode mode, const fp4moe_config& cfg, int32_t T, co
   for (int b = 0; b < 4; ++b)
     if (!encode_u8_sw128(&tmA.box[b], a_codes, (uint64_t)prm.K / 2, (uint64_t)prm.cap, 16u << b))
       return FP4MOE_CUDA_ERROR;
-  // 128 x 256 tiles (gemm_wide.cu) move fewer shared-memory bytes and issue fewer MMAs per MAC. They pay from
-  // about eight pairs per expert on average: on the DeepSeek-V4-Flash shape (256 experts, top-6), equal at 256
-  // tokens and 3-5 % faster per layer from 512 tokens up; below that the 128 x 128 tiles balance better.
-  const bool wide = prm.dyn || (int64_t)T * cfg.top_k >= kWidePairsPerExpert * (int64_t)prm.E;
-  if (wide && gemm_wide_fits(prm.K, prm.b_rows)) return gemm_wide_launch(mode, prm, tmA, st);
+  // 128 x 256 tiles (gemm_wide.cu) wherever K and the weight rows allow them: they halve the tiles, and with
+  // them the per-tile activation reloads, scale copies and epilogues, and they issue fewer MMAs per MAC. On the
+  // DeepSeek-V4-Flash shape they are faster at every batch size (decode, T = 64: 430 against 452 us per layer
+  // back to back). W1's K (hidden) and rows (2 x intermediate) always allow them; this kernel remains for a
+  // W2 whose K (intermediate) is an odd multiple of 128.
+  if (gemm_wide_fits(prm.K, prm.b_rows)) return gemm_wide_launch(mode, prm, tmA, st);
+  if (mode != kW2Rows) return FP4MOE_UNSUPPORTED;  // (not reached: the configuration check guarantees it)
   const int nsm = sm_count();
   if (nsm <= 0) return FP4MOE_CUDA_ERROR;
   const int max_tiles = (prm.cap / BM) * prm.NT;
   const unsigned grid = (unsigned)(max_tiles < nsm ? max_tiles : nsm);
-  cudaError_t r = cudaErrorInvalidValue;
-  switch (mode) {
-    case kW1SwiGLU:
-      if (!configure_once<kW1SwiGLU>()) return FP4MOE_CUDA_ERROR;
-      r = launch_pdl(grouped_gemm_kernel<kW1SwiGLU>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, tmA, prm);
-      break;
-    case kW1Amax:
-      if (!configure_once<kW1Amax>()) return FP4MOE_CUDA_ERROR;
-      r = launch_pdl(grouped_gemm_kernel<kW1Amax>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, tmA, prm);
-      break;
-    case kW2Rows:
-      if (!configure_once<kW2Rows>()) return FP4MOE_CUDA_ERROR;
-      r = launch_pdl(grouped_gemm_kernel<kW2Rows>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, tmA, prm);
-      break;
-  }
-  return r == cudaSuccess ? FP4MOE_OK : FP4MOE_CUDA_ERROR;
+  if (!configure_once<kW2Rows>()) return FP4MOE_CUDA_ERROR;
+  return launch_pdl(grouped_gemm_kernel<kW2Rows>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, tmA, prm) == cudaSuccess
+             ? FP4MOE_OK
+             : FP4MOE_CUDA_ERROR;
 }
 
 }  // namespace fp4moe

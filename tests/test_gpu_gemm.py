@@ -6,15 +6,15 @@ m-tiles, and K is partial (a stage of 2 atoms) or runs over several stages.
 * W2: every real pair's bf16 row is compared with an fp64 matmul of the
   decoded operands (fp32 accumulation bound plus half a bf16 ulp).
 * Cases with T >= E * 128 run the dynamic chunk schedule (prefill sizes),
-  the others the static contiguous one (decode sizes). With K and the
-  weight rows multiples of 256, the dynamic cases and the static ones with
-  at least 8 pairs per expert run the 128 x 256 tile kernel (gemm_wide.cu);
-  the sparse 16-expert cases keep the 128 x 128 one at every K. The sparse
-  48-expert cases have 1152 tiles of 128 x 128, enough for the static
-  schedule's tail pool: their last 288 tiles go to whichever CTAs finish
-  their own range first. With one or two ring stages per tile (K <= 1024)
-  the scale copiers run tiles ahead of the MMAs there, which tests the
-  barrier that guards the resident scales at each change of expert.
+  the others the static contiguous one (decode sizes). Where K and the
+  weight rows are multiples of 256 (every W1) the 128 x 256 tile kernel
+  runs (gemm_wide.cu); a W2 with K an odd multiple of 128 (128, 384) runs
+  the 128 x 128 kernel (gemm.cu). The sparse 64-expert cases have enough
+  tiles for the static schedule's tail pool: the last three tiles per CTA
+  go to whichever CTAs finish their own range first. In the 128 x 128 case
+  (K = 384, one ring stage per tile) the scale copiers can run tiles ahead
+  of the MMAs, which tests the barrier that guards the resident scales at
+  each change of expert.
 * W1: the clamped SwiGLU + requantisation epilogue is compared with the
   oracle's quantiser applied to the fp64 reference h. Codes must agree
   except at rounding ties that the fp32 accumulation moves.
@@ -34,11 +34,12 @@ from oracle import codecs, layout, moe, nvfp4
 pytestmark = pytest.mark.gpu
 
 
-# 16 experts, 26 pairs: fewer than 8 per expert, so the static schedule keeps its 128 x 128 kernel
+# 16 experts, 26 pairs: the static schedule with a tile or two per CTA
 SPARSE16 = [1, 0, 3, 0, 2, 5, 0, 1, 2, 0, 0, 4, 1, 0, 5, 2]
-# 48 experts, 36 of them live with 1-3 pairs: with 4096 weight rows that is 1152 tiles of 128 x 128, so the
-# static schedule keeps its last 288 tiles in the pool that CTAs take from once their own range is done
-SPARSE48 = [(7 * e) % 4 for e in range(48)]
+# 64 experts, 48 of them live with 1-3 pairs: with 4096 weight rows that is 768 tiles of 128 x 256 (1536 of
+# 128 x 128), so the static schedule keeps its last tiles in the pool that CTAs take from once their own
+# range is done
+SPARSE64 = [(7 * e) % 4 for e in range(64)]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -114,9 +115,10 @@ def _setup(H, I, counts, seed, which, full_range=False, alpha_mult=1.0):
     (256, 768, [3, 0, 140], True),              # every finite E4M3 scale byte, static schedule
     (256, 768, [600, 5, 130], True),            # every finite E4M3 scale byte, dynamic schedule
     (512, 256, [600, 5, 130], False),           # dynamic schedule, two 256-row weight tiles of the wide kernel
-    (256, 768, SPARSE16, False),                # under 8 pairs per expert: static, 128 x 128 tiles, K = 768
+    (256, 768, SPARSE16, False),                # static schedule, K = 768
     (512, 256, SPARSE16, True),                 # the same, every finite E4M3 scale byte
-    (4096, 256, SPARSE48, False),               # static schedule with its tail pool
+    (4096, 256, SPARSE64, False),               # static schedule with its tail pool, 128 x 256 tiles
+    (4096, 384, SPARSE64, False),               # the same on the 128 x 128 kernel (K = 384)
 ])
 def test_w2_rows_against_fp64(H, I, counts, full_range):
     import torch
@@ -201,10 +203,10 @@ def _run_w1(cfg, T, cap, I, t, gs2, alpha=None):
                                                    (256, 128, [600, 5, 130], False),  # the dynamic schedule
                                                    (256, 256, [3, 0, 140], True),     # every finite E4M3 scale byte
                                                    (256, 256, [600, 5, 130], True),
-                                                   (256, 256, SPARSE16, False),       # static, 128 x 128 tiles
+                                                   (256, 256, SPARSE16, False),       # static schedule
                                                    (512, 256, SPARSE16, True),
-                                                   (256, 2048, SPARSE48, False),      # the tail pool
-                                                   (512, 2048, SPARSE48, True)])      # the same, one full stage
+                                                   (256, 2048, SPARSE64, False),      # the tail pool
+                                                   (512, 2048, SPARSE64, True)])      # the same, K = 512
 def test_w1_swiglu_requant(H, I, counts, full_range):
     from block_scaled_fp4_top_gb300 import api
     cfg, T, cap, ids, L, (qa, sa, qw, sw, alpha), t = _setup(H, I, counts, 2, which=1, full_range=full_range)
@@ -229,12 +231,12 @@ def test_w1_swiglu_requant(H, I, counts, full_range):
     assert (sf[real] == s_ref[real]).mean() >= 0.99
 
 
-# 32 experts, 178 pairs (fewer than 8 per expert): the static schedule on its 128 x 128 kernel, with enough rows for
-# a thousand doubly clamped elements
+# 32 experts, 178 pairs: the static schedule over many experts, with enough rows for a thousand doubly clamped
+# elements
 SPARSE32 = [9, 0, 7, 12, 0, 8, 5, 0, 11, 6, 0, 9, 7, 0, 10, 4, 8, 0, 6, 13, 0, 7, 9, 0, 5, 8, 0, 12, 6, 0, 9, 7]
 
 
-# static and dynamic schedules on 128 x 256 tiles, and the static one on 128 x 128 tiles
+# static and dynamic schedules
 @pytest.mark.parametrize("counts", [[3, 0, 140, 1], [600, 5, 130, 1], SPARSE32])
 def test_w1_swiglu_clamp_past_the_limit(counts):
     """Gate and up driven to an RMS of about 46 (alpha x 8): a large share of both is clamped. Where gate and up are
