@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_poff[kMaxExperts];
-  __shared__ int s_cstart[kMaxExperts + 1];  // dynamic schedule: first chunk of every expert
+  __shared__ int s_cstart[kMaxExperts + 2];  // dynamic schedule: the chunk table (build_chunk_table)
   __shared__ int s_sched[kSchedSlots];
 
   __shared__ int s_abort;
@@ -156,24 +156,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   for (int e = threadIdx.x; e < E; e += THREADS) s_poff[e] = __ldcg(prm.poff + e);
   if (prm.dyn) {
     __syncthreads();
-    if (warp == 0) {  // first chunk of every expert: per-lane sums over a block of experts, then a warp scan
-      const int per = (E + 31) / 32, e0 = lane * per, e1 = min(E, e0 + per);
-      int sum = 0;
-      for (int e = e0; e < e1; ++e)
-        sum += expert_chunks(min(s_poff[e] >> 7, r128) - (e > 0 ? min(s_poff[e - 1] >> 7, r128) : 0), NT);
-      int incl = sum;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-        if (lane >= off) incl += o;
-      }
-      int run = incl - sum;
-      for (int e = e0; e < e1; ++e) {
-        s_cstart[e] = run;
-        run += expert_chunks(min(s_poff[e] >> 7, r128) - (e > 0 ? min(s_poff[e - 1] >> 7, r128) : 0), NT);
-      }
-      if (lane == 31) s_cstart[E] = incl;
-    }
+    if (warp == 0) build_chunk_table(s_poff, s_cstart, E, NT, r128, (int)gridDim.x, lane);
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(&s_tmem), TMEM_COLS);

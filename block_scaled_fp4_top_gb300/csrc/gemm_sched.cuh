@@ -63,8 +63,52 @@ __device__ __forceinline__ int tail_pool(int N, int G) {
   return N >= 4 * G ? min(kPoolPerCta * G, N / 4) : 0;
 }
 
-__device__ __forceinline__ int expert_chunks(int me, int NT) {
-  return me == 0 ? 0 : (me == 1 ? (NT + kChunk - 1) / kChunk : ((me + kChunk - 1) / kChunk) * NT);
+// Tiles per chunk of expert e: kChunk, except for the experts at the end of the order that hold the last
+// two tiles per CTA or so, whose tiles go out one at a time. A chunk of four tiles taken last held the end of
+// a launch up to its own length after the median CTA: a 35 us spread of CTA end times on the Zipf prefill W1.
+__device__ __forceinline__ int chunk_tiles(int e, int e_tail) { return e >= e_tail ? 1 : kChunk; }
+
+__device__ __forceinline__ int expert_chunks(int me, int NT, int sz) {
+  return me == 0 ? 0 : (me == 1 ? (NT + sz - 1) / sz : ((me + sz - 1) / sz) * NT);
+}
+
+// m-tiles of expert e (its padded rows, up to r128 m-tiles in all)
+__device__ __forceinline__ int expert_mtiles(const int* poff, int e, int r128) {
+  return min(poff[e] >> 7, r128) - (e > 0 ? min(poff[e - 1] >> 7, r128) : 0);
+}
+
+// The dynamic schedule's chunk table, built by one warp: s_cstart[e] is the first chunk of expert e (empty
+// experts share the next one's start), s_cstart[E] the number of chunks and s_cstart[E + 1] the first expert
+// of the single-tile tail (the experts from the end of the order that hold at least 2 G tiles).
+__device__ __forceinline__ void build_chunk_table(const int* s_poff, int* s_cstart, int E, int NT, int r128, int G,
+                                                  int lane) {
+  int e_tail = 0;
+  if (lane == 0) {
+    int tiles = 0, e = E;
+    while (e > 0 && tiles < 2 * G) {
+      --e;
+      tiles += expert_mtiles(s_poff, e, r128) * NT;
+    }
+    e_tail = e;
+  }
+  e_tail = __shfl_sync(0xFFFFFFFFu, e_tail, 0);
+  // per-lane sums over a block of experts, then a warp scan
+  const int per = (E + 31) / 32, e0 = lane * per, e1 = min(E, e0 + per);
+  int sum = 0;
+  for (int e = e0; e < e1; ++e) sum += expert_chunks(expert_mtiles(s_poff, e, r128), NT, chunk_tiles(e, e_tail));
+  int incl = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  int run = incl - sum;
+  for (int e = e0; e < e1; ++e) {
+    s_cstart[e] = run;
+    run += expert_chunks(expert_mtiles(s_poff, e, r128), NT, chunk_tiles(e, e_tail));
+  }
+  if (lane == 31) s_cstart[E] = incl;
+  if (lane == 0) s_cstart[E + 1] = e_tail;
 }
 
 struct Chunk {
@@ -79,7 +123,7 @@ struct Chunk {
   }
 };
 
-// Chunk c; s_cstart[e] is the first chunk of expert e (empty experts share the next one's start).
+// Chunk c of the table of build_chunk_table.
 __device__ __forceinline__ Chunk decode_chunk(int c, const int* s_cstart, const int* poff, int E, int NT, int r128) {
   int lo = 0, hi = E - 1;  // the last expert whose first chunk is <= c
   while (lo < hi) {
@@ -92,16 +136,17 @@ __device__ __forceinline__ Chunk decode_chunk(int c, const int* s_cstart, const 
   k.pm0 = lo > 0 ? min(poff[lo - 1] >> 7, r128) : 0;
   k.me = min(poff[lo] >> 7, r128) - k.pm0;
   const int l = c - s_cstart[lo];
+  const int sz = chunk_tiles(lo, s_cstart[E + 1]);
   k.along_n = (k.me == 1);
   if (k.along_n) {
-    k.n0 = l * kChunk;
+    k.n0 = l * sz;
     k.m0 = k.pm0;
-    k.count = min(kChunk, NT - k.n0);
+    k.count = min(sz, NT - k.n0);
   } else {
     k.n0 = l % NT;
     const int mb = l / NT;
-    k.m0 = k.pm0 + mb * kChunk;
-    k.count = min(kChunk, k.me - mb * kChunk);
+    k.m0 = k.pm0 + mb * sz;
+    k.count = min(sz, k.me - mb * sz);
   }
   return k;
 }
