@@ -49,7 +49,7 @@ FALLBACK_HBM_GBS = 6800.0
 # with, so it is reported while their hash matches and as null otherwise.
 W1_TRAFFIC = {
     # workload name: (bytes per launch, sha256 of the GEMM sources)
-    "dsv4_flash_decode_T64": (1948672512 + 7872768, "df1cd4e8f1ec4e4a9a5279584e872a3ba7e6a66555c1a6ce25f23b77f9310f07"),
+    "dsv4_flash_decode_T64": (1948672512 + 7872768, "75391954e7b25c7165249bf2d4b6525bdb0df307ccb299a98605588f4e41fb4c"),
 }
 GEMM_SOURCES = ("block_scaled_fp4_top_gb300/csrc/gemm.cu", "block_scaled_fp4_top_gb300/csrc/gemm_wide.cu",
                 "block_scaled_fp4_top_gb300/csrc/gemm_sched.cuh", "block_scaled_fp4_top_gb300/csrc/common.cuh")

@@ -1,4 +1,6 @@
-// Block-scaled NVFP4 grouped GEMMs with 128 x 256 output tiles, for the dynamic (prefill-size) schedule.
+// Block-scaled NVFP4 grouped GEMMs with 128 x 256 output tiles: every W1, and every W2 whose K is a multiple
+// of 256, under both tile schedules (static with its tail pool at decode sizes, dynamic chunks at prefill
+// sizes; gemm_sched.cuh).
 //
 // The same GEMMs as gemm.cu ("Current Bug: CuTeDSLMoERunner", "Data Flow": run_nvfp4_grouped_gemm for L1
 // and L2; searchsorted(right=True) tile ownership on offsets without a leading 0, "Bug 2" and "Bug 4"; per
@@ -7,7 +9,8 @@
 // feeds twice the MACs, and each tcgen05.mma (M = 128, N = 256, K = 64) does twice the work of the
 // 128 x 128 one, so both the ring's bytes and the MMA instructions per MAC fall. At prefill sizes the
 // 128 x 128 kernel is bound by neither alone but by the per-stage ring latency, the MMA issue and a
-// four-warp epilogue together; this kernel attacks all three.
+// four-warp epilogue together; this kernel attacks all three. At decode sizes, where both stream weights at
+// the HBM rate, its half as many tiles start, hand over and finish with less idle time between kernels.
 //
 // The accumulator takes 256 of TMEM's 512 columns, so there is one of it, not two. The epilogue has eight
 // warps (two per TMEM lane quarter, one per 128-column half) that move the whole accumulator to registers,
