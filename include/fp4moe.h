@@ -213,11 +213,11 @@ fp4moe_status fp4moe_weight_bytes(const fp4moe_config* cfg, size_t* w1_codes, si
  * dependent launch, so consecutive kernels overlap their launch latency.
  * Each of them waits for its predecessor before it lets its own successor
  * start. So when a grouped GEMM starts, the kernel two places before it has
- * finished, and a GEMM with the static (decode-size) schedule reads
- * padded_offsets and pair_of_row during a set-up that overlaps its
- * predecessor. A caller's own kernel placed right before a grouped GEMM
- * must therefore not trigger its dependents before it has written those
- * two arrays (kernels that never trigger early, and copies, are fine).
+ * finished, and the GEMM reads padded_offsets and pair_of_row during a
+ * set-up that overlaps its predecessor. A caller's own kernel placed right
+ * before a grouped GEMM must therefore not trigger its dependents before it
+ * has written those two arrays (kernels that never trigger early, and
+ * copies, are fine).
  *   l[t,e] = RN_f32(sum_h x[t,h]*router_w[e,h]) (+ router_bias[e] in fp32):
  *     the exact sum rounded once, to within an ulp (an fp32 compensated
  *     two-sum reduction in a fixed order).
