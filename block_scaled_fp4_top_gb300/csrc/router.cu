@@ -295,42 +295,70 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
-// Add the exact bf16 x bf16 product to the compensated pair (s, c).
-__device__ __forceinline__ void acc_prod(float& s, float& c, float xv, float wv) {
-  float e;
-  two_sum(s, __fmul_rn(xv, wv), s, e);  // the product is exact in fp32 (8-bit significands)
-  c = __fadd_rn(c, e);
+// Two fp32 lanes in one 64-bit register, lane 0 in the low word, for the packed f32x2 add, sub and mul of
+// sm_100 and later. Each lane rounds to nearest even exactly as the scalar instruction would, so a packed chain
+// gives the same bits as two scalar chains, one per lane, in half the instructions.
+typedef unsigned long long f32x2_t;
+
+__device__ __forceinline__ f32x2_t add_x2(f32x2_t a, f32x2_t b) {
+  f32x2_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2_t sub_x2(f32x2_t a, f32x2_t b) {
+  f32x2_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2_t mul_x2(f32x2_t a, f32x2_t b) {
+  f32x2_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// The two bf16 of a 32-bit word as fp32 lanes: the low half in lane 0, the high half in lane 1.
+__device__ __forceinline__ f32x2_t bf16x2_widen(uint32_t w) {
+  return (static_cast<f32x2_t>(w & 0xFFFF0000u) << 32) | static_cast<f32x2_t>(w << 16);
+}
+__device__ __forceinline__ float lane0(f32x2_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float lane1(f32x2_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+
+// Add the exact bf16 x bf16 products of the word pair (xw, ww) to the compensated pairs (s, c), lane by lane:
+// Knuth's two-sum on each lane. Each product is exact in fp32 (8-bit significands).
+__device__ __forceinline__ void acc_prod_x2(f32x2_t& s, f32x2_t& c, uint32_t xw, uint32_t ww) {
+  const f32x2_t p = mul_x2(bf16x2_widen(xw), bf16x2_widen(ww));
+  const f32x2_t sn = add_x2(s, p);
+  const f32x2_t bb = sub_x2(sn, s);
+  const f32x2_t e = add_x2(sub_x2(s, sub_x2(sn, bb)), sub_x2(p, bb));
+  s = sn;
+  c = add_x2(c, e);
 }
 
 constexpr int kMaxChunksPerLane = 18;  // H <= 4608: 576 16-byte chunks over 32 lanes
 
 // Exact-sum-rounded-once logit (within an ulp) of the token row xs (in shared memory) and expert row w, by
 // one warp. Lane l takes the 16-byte chunks l, l + 32, ..., all of whose loads are issued before the
-// arithmetic, with two compensated accumulators; a fixed butterfly merges the lanes.
+// arithmetic, with two compensated accumulators (the low and the high bf16 of each word, the lanes of one
+// packed pair); a fixed butterfly merges the lanes.
 __device__ float warp_exact_dot(const uint4* xs, const uint4* __restrict__ wrow, int nchunks) {
   const int lane = threadIdx.x & 31;
   uint4 wv[kMaxChunksPerLane];
 #pragma unroll
   for (int j = 0; j < kMaxChunksPerLane; ++j)
     if (lane + 32 * j < nchunks) wv[j] = __ldg(wrow + lane + 32 * j);
-  float s0 = 0.0f, c0 = 0.0f, s1 = 0.0f, c1 = 0.0f;
+  f32x2_t S = 0ull, C = 0ull;
 #pragma unroll
   for (int j = 0; j < kMaxChunksPerLane; ++j) {
     if (lane + 32 * j < nchunks) {
       const uint4 xv = xs[lane + 32 * j];
-      acc_prod(s0, c0, bf16_lo(xv.x), bf16_lo(wv[j].x));
-      acc_prod(s1, c1, bf16_hi(xv.x), bf16_hi(wv[j].x));
-      acc_prod(s0, c0, bf16_lo(xv.y), bf16_lo(wv[j].y));
-      acc_prod(s1, c1, bf16_hi(xv.y), bf16_hi(wv[j].y));
-      acc_prod(s0, c0, bf16_lo(xv.z), bf16_lo(wv[j].z));
-      acc_prod(s1, c1, bf16_hi(xv.z), bf16_hi(wv[j].z));
-      acc_prod(s0, c0, bf16_lo(xv.w), bf16_lo(wv[j].w));
-      acc_prod(s1, c1, bf16_hi(xv.w), bf16_hi(wv[j].w));
+      acc_prod_x2(S, C, xv.x, wv[j].x);
+      acc_prod_x2(S, C, xv.y, wv[j].y);
+      acc_prod_x2(S, C, xv.z, wv[j].z);
+      acc_prod_x2(S, C, xv.w, wv[j].w);
     }
   }
   float s, e0;
-  two_sum(s0, s1, s, e0);
-  float c = __fadd_rn(__fadd_rn(c0, c1), e0);
+  two_sum(lane0(S), lane1(S), s, e0);
+  float c = __fadd_rn(__fadd_rn(lane0(C), lane1(C)), e0);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     const float so = __shfl_xor_sync(kFull, s, off);
@@ -560,23 +588,20 @@ __device__ __forceinline__ void warp_argmax(const float (&v)[MAXV], uint32_t eli
 // The compensated dot product of warp_exact_dot, with the token row read from global memory (it stays in
 // L1 across the candidates of a token). Lane l takes chunks l, l + 32, ... in batches of 2 per lane, the
 // next batch's loads in flight while the current one is summed, into four independent compensated pairs
-// (more independent dependency chains per lane), which two-sums merge at the end.
-__device__ __forceinline__ void acc_chunk(float (&s)[4], float (&c)[4], const uint4& xv, const uint4& wv) {
-  acc_prod(s[0], c[0], bf16_lo(xv.x), bf16_lo(wv.x));
-  acc_prod(s[1], c[1], bf16_hi(xv.x), bf16_hi(wv.x));
-  acc_prod(s[2], c[2], bf16_lo(xv.y), bf16_lo(wv.y));
-  acc_prod(s[3], c[3], bf16_hi(xv.y), bf16_hi(wv.y));
-  acc_prod(s[0], c[0], bf16_lo(xv.z), bf16_lo(wv.z));
-  acc_prod(s[1], c[1], bf16_hi(xv.z), bf16_hi(wv.z));
-  acc_prod(s[2], c[2], bf16_lo(xv.w), bf16_lo(wv.w));
-  acc_prod(s[3], c[3], bf16_hi(xv.w), bf16_hi(wv.w));
+// (more independent dependency chains per lane) held as two packed pairs: the words x and z of a chunk go
+// to the first, y and w to the second. Two-sums merge the four at the end.
+__device__ __forceinline__ void acc_chunk(f32x2_t (&s)[2], f32x2_t (&c)[2], const uint4& xv, const uint4& wv) {
+  acc_prod_x2(s[0], c[0], xv.x, wv.x);
+  acc_prod_x2(s[1], c[1], xv.y, wv.y);
+  acc_prod_x2(s[0], c[0], xv.z, wv.z);
+  acc_prod_x2(s[1], c[1], xv.w, wv.w);
 }
 
 __device__ __noinline__ float warp_exact_dot_global(const uint4* __restrict__ xr, const uint4* __restrict__ wrow,
                                                    int nchunks) {
   const int lane = threadIdx.x & 31;
   constexpr int B = 2;  // chunks per lane per batch
-  float s[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  f32x2_t s[2] = {0ull, 0ull}, c[2] = {0ull, 0ull};
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   uint4 xv[B], wv[B];
 #pragma unroll
@@ -602,10 +627,11 @@ __device__ __noinline__ float warp_exact_dot_global(const uint4* __restrict__ xr
     }
   }
   float a, ea, b, eb, sum, e;
-  two_sum(s[0], s[1], a, ea);
-  two_sum(s[2], s[3], b, eb);
+  two_sum(lane0(s[0]), lane1(s[0]), a, ea);
+  two_sum(lane0(s[1]), lane1(s[1]), b, eb);
   two_sum(a, b, sum, e);
-  float cc = __fadd_rn(__fadd_rn(__fadd_rn(c[0], c[1]), __fadd_rn(c[2], c[3])), __fadd_rn(__fadd_rn(ea, eb), e));
+  float cc = __fadd_rn(__fadd_rn(__fadd_rn(lane0(c[0]), lane1(c[0])), __fadd_rn(lane0(c[1]), lane1(c[1]))),
+                       __fadd_rn(__fadd_rn(ea, eb), e));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     const float so = __shfl_xor_sync(kFull, sum, off);
