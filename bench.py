@@ -600,6 +600,41 @@ def run_prefill(args, dev, fp4_peak_tflops):
     }
 
 
+def run_route_only(args, wl, dev):
+    """moe_route alone on the workload's batch (x, router and bias from the seeded generator; no expert weights
+    are made): --warmup untimed calls, then --steps calls back to back between two CUDA events. A small case for
+    profiler captures of the routing kernels, not the bench line."""
+    import torch
+    from synthgen import gpu as sgpu
+    from block_scaled_fp4_top_gb300 import api
+    T = wl.T
+    cfg = api.config(wl.H, wl.I, wl.E, wl.k, T, wl.swiglu_limit)
+    i32 = dict(dtype=torch.int32, device=dev)
+    bufs = [torch.empty(T, wl.E, dtype=torch.float32, device=dev), torch.empty(T * wl.k, **i32),
+            torch.empty(T * wl.k, dtype=torch.float32, device=dev), torch.empty(wl.E, **i32),
+            torch.empty(wl.E, **i32), torch.empty(wl.E, **i32), torch.empty(T * wl.k, **i32),
+            torch.empty(api.capacity_rows(cfg, T), **i32)]
+    ws = torch.zeros(api.workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+    x = sgpu.activations(wl, sg.EVAL_SEED)
+    wr = sgpu.router(wl)
+    bias = sg.router_bias_f32(wl)
+    bias_t = None if bias is None else torch.from_numpy(bias).to(dev)
+    for _ in range(args.warmup):
+        api.moe_route(cfg, T, x, wr, bias_t, *bufs, ws)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        api.moe_route(cfg, T, x, wr, bias_t, *bufs, ws)
+    t1.record()
+    torch.cuda.synchronize()
+    err = api.fp4moe_read_error(ws)
+    if err != 0:
+        raise RuntimeError(f"route: device error word {err:#x}")
+    return {"route_only": wl.name, "T": T, "E": wl.E, "steps": args.steps, "warmup": args.warmup,
+            "us_per_call": t0.elapsed_time(t1) * 1e3 / args.steps}
+
+
 def run_side_workload(args, wl, dev):
     """A second workload measured in the same run, the way the decode line is (run_ours), cut to its figures."""
     import copy
@@ -791,6 +826,8 @@ def main():
     ap.add_argument("--side-steps", type=int, default=30,
                     help="steps of the TP3 MXFP4 workloads and replays per T of the graph sweep in the default run")
     ap.add_argument("--oracle-only", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--route-only", action="store_true",
+                    help="time moe_route alone on the workload (a small case for profiler captures)")
     ap.add_argument("--experts", type=int, default=0,
                     help="override E (smaller case for profiler captures; the default is the workload's E)")
     args = ap.parse_args()
@@ -843,6 +880,10 @@ def main():
     from block_scaled_fp4_top_gb300 import build as libbuild  # noqa: F401  (the library must exist)
     from block_scaled_fp4_top_gb300 import _lib
     _lib.load()
+    if args.route_only:
+        if rank == 0:
+            print(json.dumps(run_route_only(args, wl, torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))))))
+        return
     out = run_ours(args, wl, rank, world)
     if rank == 0 and not args.no_prefill and wl.name == sg.DSV4_DECODE.name and world == 1:
         dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
