@@ -600,23 +600,29 @@ __device__ __forceinline__ void acc_chunk(f32x2_t (&s)[2], f32x2_t (&c)[2], cons
 __device__ __noinline__ float warp_exact_dot_global(const uint4* __restrict__ xr, const uint4* __restrict__ wrow,
                                                    int nchunks) {
   const int lane = threadIdx.x & 31;
-  constexpr int B = 2;  // chunks per lane per batch
+  constexpr int B = 2;          // chunks per lane per batch
+  const int n = nchunks >> 5;   // chunks per lane: H is a multiple of 256, so nchunks = H / 8 is a multiple of 32
+  const int nb = n - n % B;     // those in whole batches; an odd last chunk is summed after them
+  xr += lane;
+  wrow += lane;
   f32x2_t s[2] = {0ull, 0ull}, c[2] = {0ull, 0ull};
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  uint4 xv[B], wv[B];
+  uint4 xv[B], wv[B], xn[B], wn[B];
 #pragma unroll
   for (int j = 0; j < B; ++j) {
-    const int ch = lane + 32 * j;
-    xv[j] = ch < nchunks ? __ldg(xr + ch) : zero;
-    wv[j] = ch < nchunks ? __ldg(wrow + ch) : zero;
+    xv[j] = wv[j] = xn[j] = wn[j] = zero;
+    if (j < nb) {
+      xv[j] = __ldg(xr + 32 * j);
+      wv[j] = __ldg(wrow + 32 * j);
+    }
   }
-  for (int base = 0; base < nchunks; base += 32 * B) {
-    uint4 xn[B], wn[B];
+  for (int it = 0; it < nb; it += B) {
+    if (it + B < nb) {  // the next batch, in flight while this one is summed (the same branch in every lane)
 #pragma unroll
-    for (int j = 0; j < B; ++j) {  // the next batch (zero past the row: zero products add nothing)
-      const int ch = base + 32 * B + lane + 32 * j;
-      xn[j] = ch < nchunks ? __ldg(xr + ch) : zero;
-      wn[j] = ch < nchunks ? __ldg(wrow + ch) : zero;
+      for (int j = 0; j < B; ++j) {
+        xn[j] = __ldg(xr + 32 * (it + B + j));
+        wn[j] = __ldg(wrow + 32 * (it + B + j));
+      }
     }
 #pragma unroll
     for (int j = 0; j < B; ++j) acc_chunk(s, c, xv[j], wv[j]);
@@ -626,6 +632,7 @@ __device__ __noinline__ float warp_exact_dot_global(const uint4* __restrict__ xr
       wv[j] = wn[j];
     }
   }
+  if (nb < n) acc_chunk(s, c, __ldg(xr + 32 * nb), __ldg(wrow + 32 * nb));
   float a, ea, b, eb, sum, e;
   two_sum(lane0(s[0]), lane1(s[0]), a, ea);
   two_sum(lane0(s[1]), lane1(s[1]), b, eb);
@@ -656,6 +663,10 @@ __global__ void __launch_bounds__(256, 3) router_refine_warp_kernel(int T, int H
                                                                  const float* __restrict__ nw2, float* logits,
                                                                  int32_t* __restrict__ ids_out,
                                                                  float* __restrict__ w_out, uint32_t* err) {
+  __shared__ int s_ce[8][32];          // each warp's candidates (at most 32 on the ranking path): experts
+  __shared__ float s_cv[8][32];        // and their exact logits
+  __shared__ int s_pe[8][kMaxTopK];    // each warp's k picks in order: experts
+  __shared__ float s_pv[8][kMaxTopK];  // and their exact logits
   pdl_wait();
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -725,11 +736,44 @@ __global__ void __launch_bounds__(256, 3) router_refine_warp_kernel(int T, int H
       }
     }
   }
-  // the top k of the candidates by exact logit
-  int se[kMaxTopK];
-  float sv[kMaxTopK];
+  // the top k of the candidates by exact logit: value descending, ties to the lower id, a NaN never taken. Pick
+  // j goes to place j of this warp's list s_pe/s_pv.
   bool bad = false;
-  {
+  int nc = 0;
+#pragma unroll
+  for (int q = 0; q < MAXV; ++q) nc += __popc(__ballot_sync(kFull, (cand >> q) & 1u));
+  if (nc <= 32) {
+    // the usual case (about k candidates): candidate p to lane p, each ranked against all of them at once (the
+    // count of candidates ahead of it in that order); rank r is pick r
+    int pos = 0;
+#pragma unroll
+    for (int q = 0; q < MAXV; ++q) {
+      const bool mine = (cand >> q) & 1u;
+      const uint32_t ball = __ballot_sync(kFull, mine);
+      if (mine) {
+        const int p = pos + __popc(ball & ((1u << lane) - 1u));
+        s_ce[warp][p] = lane + 32 * q;
+        s_cv[warp][p] = l[q];
+      }
+      pos += __popc(ball);
+    }
+    __syncwarp();
+    const bool have = lane < nc;
+    const int ce = have ? s_ce[warp][lane] : INT_MAX;
+    const float cv = have ? s_cv[warp][lane] : __int_as_float(0x7FC00000);
+    int rank = 0;
+    for (int i = 0; i < nc; ++i) {
+      const float vi = __shfl_sync(kFull, cv, i);
+      const int ei = __shfl_sync(kFull, ce, i);
+      rank += (vi > cv || (vi == cv && ei < ce)) ? 1 : 0;  // a NaN is ahead of nothing
+    }
+    const bool num = have && cv == cv;  // the numbers' ranks are 0, 1, ..., one each
+    bad = __popc(__ballot_sync(kFull, num)) < k;
+    if (num && rank < k) {
+      s_pe[warp][rank] = ce;
+      s_pv[warp][rank] = cv;
+    }
+  } else {  // more (a NaN bound, or many ties): k passes of a warp argmax
     uint32_t left = cand;
     for (int j = 0; j < k; ++j) {
       int be;
@@ -740,29 +784,30 @@ __global__ void __launch_bounds__(256, 3) router_refine_warp_kernel(int T, int H
         break;
       }
       if ((be & 31) == lane) left &= ~(1u << (be >> 5));
-      se[j] = be;
-      sv[j] = bv;
+      if (lane == 0) {
+        s_pe[warp][j] = be;
+        s_pv[warp][j] = bv;
+      }
     }
   }
-  if (lane == 0) {
-    if (bad) {  // fewer than k comparable logits: NaN input
-      raise_error(err, FP4MOE_ERR_EXPERT_ID);
-      for (int j = 0; j < k; ++j) {
-        ids_out[(size_t)t * k + j] = 0;
-        w_out[(size_t)t * k + j] = 0.0f;
-      }
-    } else {
-      const float lmax = sv[0];
-      float ex[kMaxTopK];
-      float sum = 0.0f;
-      for (int j = 0; j < k; ++j) {
-        ex[j] = expf(__fsub_rn(sv[j], lmax));
-        sum = __fadd_rn(sum, ex[j]);
-      }
-      for (int j = 0; j < k; ++j) {
-        ids_out[(size_t)t * k + j] = se[j];
-        w_out[(size_t)t * k + j] = __fdiv_rn(ex[j], sum);
-      }
+  __syncwarp();
+  // the softmax over the k picks, lane j taking pick j; the sum runs in pick order
+  if (bad) {  // fewer than k comparable logits: NaN input
+    if (lane == 0) raise_error(err, FP4MOE_ERR_EXPERT_ID);
+    if (lane < k) {
+      ids_out[(size_t)t * k + lane] = 0;
+      w_out[(size_t)t * k + lane] = 0.0f;
+    }
+  } else {
+    const int pe = lane < k ? s_pe[warp][lane] : 0;
+    const float pv = lane < k ? s_pv[warp][lane] : 0.0f;
+    const float lmax = __shfl_sync(kFull, pv, 0);
+    const float ex = lane < k ? expf(__fsub_rn(pv, lmax)) : 0.0f;
+    float sum = 0.0f;
+    for (int j = 0; j < k; ++j) sum = __fadd_rn(sum, __shfl_sync(kFull, ex, j));
+    if (lane < k) {
+      ids_out[(size_t)t * k + lane] = pe;
+      w_out[(size_t)t * k + lane] = __fdiv_rn(ex, sum);
     }
   }
 #pragma unroll

@@ -138,11 +138,13 @@ def test_quantize_scatter_bit_exact(wl, T):
     assert (codes[real] == want_c).all()
 
 
-def test_route_ties_and_zero_rows():
+@pytest.mark.parametrize("T", [40, 4100])  # one CTA per token; one warp per token from 4096 tokens on
+def test_route_ties_and_zero_rows(T):
     """Exact ties: experts 3 and 5 share a router row, and token 2 is all zeros (every logit 0).
-    Ties go to the lower expert id, and a zero row picks experts 0..k-1 with equal weights."""
+    Ties go to the lower expert id, and a zero row picks experts 0..k-1 with equal weights. With one warp per
+    token, the tied tokens take the ranking of a few candidates and the zero row (every expert a candidate)
+    the argmax passes."""
     wl = sg.DSV4_DECODE
-    T = 40
     x_bits = sg.activations_bf16(wl, sg.EVAL_SEED, T=T).copy()
     x_bits[2] = 0
     wr_bits = sg.router_bf16(wl).copy()
